@@ -1,0 +1,187 @@
+"""NVFP4 oracle: a plain, single-threaded CPU reference (C++, fp32 quantizer
+steps and an fp64 matmul).
+
+TEST INFRASTRUCTURE.  Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import it.  It shares no code with the CUDA
+library and never imports it.
+
+Functions and what pins them (tests/test_oracle.py):
+
+* ``e2m1_value`` / ``e4m3_value`` -- element decode from the type definitions
+  (OCP MX v1.0 E2M1; OCP FP8 E4M3 "fn").  Pinned by the exhaustive 16-entry
+  table and by all 256 bytes against torch.float8_e4m3fn.
+* ``e4m3_encode`` / ``e2m1_encode`` -- round to nearest, ties to even,
+  saturating.  Pinned by torch's fp8 cast and by brute-force argmin.
+* ``quantize`` / ``quantize_rows`` / ``tensor_scale`` -- the NVFP4 recipe
+  (tensor scale g/(6*448); block scale E4M3(block amax/6/s); codes
+  E2M1(x/d)).  Pinned by hand-worked blocks (tests/golden/) and by the
+  round-trip error bound.
+* ``dequant`` and ``matmul_abt`` -- the plain definitions; pinned by exact
+  rational brute force on tiny shapes and closed forms.
+* ``reference_gemm`` -- Y = Xhat W^T with Xhat = X for M <= 16 and
+  dequant(quantize(X)) for M > 16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libnvfp4_oracle.so")
+_lib = None
+
+DECODE_M_MAX = 16
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (single-threaded, no FP contraction)."""
+    src = os.path.join(_HERE, "nvfp4_oracle.cpp")
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-shared",
+                               "-ffp-contract=off", "-fno-fast-math", src, "-o", tmp])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I64, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+    lib.orc_e2m1_value.restype = ctypes.c_double
+    lib.orc_e2m1_value.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_value.restype = ctypes.c_double
+    lib.orc_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_encode.restype = ctypes.c_uint8
+    lib.orc_e4m3_encode.argtypes = [F]
+    lib.orc_e2m1_encode.restype = ctypes.c_uint8
+    lib.orc_e2m1_encode.argtypes = [F]
+    lib.orc_tensor_scale.restype = ctypes.c_int
+    lib.orc_tensor_scale.argtypes = [P, I64, I64, I64, P, P]
+    lib.orc_quantize_rows.restype = None
+    lib.orc_quantize_rows.argtypes = [P, I64, I64, I64, F, P, P]
+    lib.orc_quantize.restype = ctypes.c_int
+    lib.orc_quantize.argtypes = [P, I64, I64, I64, P, P, P]
+    lib.orc_dequant.restype = None
+    lib.orc_dequant.argtypes = [P, P, F, I64, I64, P]
+    lib.orc_bf16_to_f64.restype = None
+    lib.orc_bf16_to_f64.argtypes = [P, I64, P]
+    lib.orc_matmul_abt.restype = None
+    lib.orc_matmul_abt.argtypes = [P, I64, P, I64, I64, P, P]
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags.c_contiguous
+    return a.ctypes.data
+
+
+def e2m1_value(code: int) -> float:
+    return _load().orc_e2m1_value(code)
+
+
+def e4m3_value(byte: int) -> float:
+    return _load().orc_e4m3_value(byte)
+
+
+def e4m3_encode(u: float) -> int:
+    return _load().orc_e4m3_encode(u)
+
+
+def e2m1_encode(q: float) -> int:
+    return _load().orc_e2m1_encode(q)
+
+
+def tensor_scale(x_bf16: np.ndarray) -> tuple[float, float, bool]:
+    """(global amax, tensor scale g/2688, nonfinite flag) of a [rows, K] uint16 array."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, K = x.shape
+    g = np.zeros(1, np.float32)
+    s = np.zeros(1, np.float32)
+    bad = _load().orc_tensor_scale(_ptr(x), rows, K, K, _ptr(g), _ptr(s))
+    return float(g[0]), float(s[0]), bool(bad)
+
+
+def quantize_rows(x_bf16: np.ndarray, s: float) -> tuple[np.ndarray, np.ndarray]:
+    """Quantize rows with a given tensor scale -> (codes [rows,K/2], scales [rows,K/16])."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, K = x.shape
+    codes = np.empty((rows, K // 2), np.uint8)
+    scales = np.empty((rows, K // 16), np.uint8)
+    _load().orc_quantize_rows(_ptr(x), rows, K, K, np.float32(s), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def quantize(x_bf16: np.ndarray) -> tuple[np.ndarray, np.ndarray, float, bool]:
+    """Whole tensor -> (codes, scales, tensor scale, nonfinite flag)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, K = x.shape
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    codes = np.empty((rows, K // 2), np.uint8)
+    scales = np.empty((rows, K // 16), np.uint8)
+    s = np.zeros(1, np.float32)
+    bad = _load().orc_quantize(_ptr(x), rows, K, K, _ptr(codes), _ptr(scales), _ptr(s))
+    return codes, scales, float(s[0]), bool(bad)
+
+
+def dequant(codes: np.ndarray, scales: np.ndarray, s: float) -> np.ndarray:
+    """fp64 [rows, K] values e2m1 * e4m3 * s."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, K = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((rows, K), np.float64)
+    _load().orc_dequant(_ptr(codes), _ptr(scales), np.float32(s), rows, K, _ptr(out))
+    return out
+
+
+def bf16_to_f64(x_bf16: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    out = np.empty(x.shape, np.float64)
+    _load().orc_bf16_to_f64(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def matmul_abt(a: np.ndarray, b: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """(A B^T, |A| |B|^T) accumulated in fp64; a [M,K], b [N,K]."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    M, K = a.shape
+    N = b.shape[0]
+    y = np.empty((M, N), np.float64)
+    bound = np.empty((M, N), np.float64)
+    _load().orc_matmul_abt(_ptr(a), M, _ptr(b), N, K, _ptr(y), _ptr(bound))
+    return y, bound
+
+
+def activation_hat(x_bf16: np.ndarray, M_total: int, s_x: float | None = None) -> np.ndarray:
+    """The X operand the method multiplies: bf16 X itself for decode-sized M
+    (<= 16), dequant(quantize(X)) for larger M.  For a row sample of a large
+    X, pass the tensor scale of the whole X as s_x."""
+    if M_total <= DECODE_M_MAX:
+        return bf16_to_f64(x_bf16)
+    if s_x is None:
+        _, s_x, _ = tensor_scale(x_bf16)
+    c, sc = quantize_rows(x_bf16, s_x)
+    return dequant(c, sc, s_x)
+
+
+def reference_gemm(x_bf16: np.ndarray, M_total: int, w_codes: np.ndarray,
+                   w_scales: np.ndarray, s_w: float, s_x: float | None = None):
+    """(y_ref, bound) for rows of X against rows of W, in fp64."""
+    xh = activation_hat(x_bf16, M_total, s_x)
+    wh = dequant(w_codes, w_scales, s_w)
+    return matmul_abt(xh, wh)
+
+
+def tolerance(bound: np.ndarray) -> np.ndarray:
+    """Per-element acceptance band |y - y_ref| <= 2e-3 * sum|x w| + 1e-5."""
+    return 2e-3 * bound + 1e-5
