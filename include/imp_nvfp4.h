@@ -1,0 +1,131 @@
+/*
+ * imp_nvfp4.h -- NVFP4 weight-quantized linear layer for GB300 (sm_103a).
+ *
+ * The operation: the 4-bit weight-quantized linear layer that dominates the
+ * memory-bound decode step of a single-GPU LLM inference engine.  The imp
+ * engine README ("How it works": decode is bandwidth-bound, so the weights
+ * are stored in 4 bits (NVFP4) and multiplied without being unpacked to 16
+ * bits; prefill is compute-bound) and the engineering-log entry "NVFP4 at the
+ * bit level" (four bits and two scales) define the format:
+ *
+ *   W is N rows of K elements.  Each element is an E2M1 code (1 sign, 2
+ *   exponent, 1 mantissa bit: magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6), packed two
+ *   per byte -- element 2i in the low nibble of byte i of its row.  Every 16
+ *   consecutive elements of a row (a block) share one E4M3 scale byte
+ *   (OCP FP8 E4M3 "fn": bias 7, max 448, sign bit always 0 here).  The whole
+ *   tensor shares one fp32 scale s.  Element value = e2m1 * e4m3 * s.
+ *
+ * Quantizer recipe (bit-exact, IEEE fp32, every step correctly rounded):
+ *   g  = max |x| over the tensor;  s = g / 2688  (2688 = 6 * 448)
+ *   per block: a = max |x_j|; u = (a / 6) / s (u = 0 when s = 0);
+ *              sb = E4M3(u), round to nearest even, saturating at 448
+ *              d  = e4m3(sb) * s
+ *              code_j = 0 if d == 0, else sign(x_j) | E2M1(|x_j| / d), round
+ *              to nearest even, saturating at 6.
+ *
+ * Linear layer: Y[M][N] = X[M][K] * W^T, bf16 in and out, fp32 accumulation.
+ *   M <= 16 (decode, "1. The big picture", section "Two phases with very
+ *   different costs": one token per step, every weight read once): X stays
+ *   bf16; y[m][n] = s * sum_b e4m3(sb[n][b]) * sum_{j<16} x[m][16b+j] *
+ *   e2m1(c[n][16b+j]).
+ *   M > 16 (prefill): X is first quantized with the same recipe (its own
+ *   tensor scale s_x) and Y = s_x * s * sum over blocks of the products of
+ *   the two block-scaled E2M1 operands, on the block-scaled FP4 tensor cores.
+ *   The result is rounded to bf16 with round-to-nearest-even.
+ *
+ * Conventions for every entry point:
+ *   - All buffers are DEVICE memory allocated and owned by the caller.  The
+ *     library never allocates, frees or synchronizes, and keeps no state
+ *     between calls (it is thread-compatible).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream); all work
+ *     is enqueued on it asynchronously.
+ *   - The return value reports argument and launch errors only.  A call that
+ *     returns anything but IMP_OK has enqueued nothing.
+ *   - `dev_status` (device int32, may be NULL) receives data-dependent
+ *     conditions found while the kernels run: the kernels OR IMP_DEV_* flags
+ *     into it, so the caller zeroes it beforehand and reads it after the
+ *     stream synchronizes.  Kernels never trap; every wait inside a kernel is
+ *     bounded and sets IMP_DEV_TIMEOUT when it gives up.
+ *   - Row-major layouts; all base pointers 16-byte aligned; leading
+ *     dimensions (in elements) multiples of 8.
+ */
+#ifndef IMP_NVFP4_H
+#define IMP_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  IMP_OK = 0,
+  IMP_ERR_INVALID_ARG = 1,         /* NULL pointer, negative size, rows/K mismatch */
+  IMP_ERR_UNSUPPORTED_SHAPE = 2,   /* K not a positive multiple of 64 (16 for quantize) */
+  IMP_ERR_MISALIGNED = 3,          /* pointer not 16-byte aligned or ld not a multiple of 8 */
+  IMP_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the *_workspace_size() figure */
+  IMP_ERR_CUDA = 5                 /* a kernel launch failed (cudaGetLastError) */
+} imp_status;
+
+/* Flags OR-ed into *dev_status by the kernels. */
+enum {
+  IMP_DEV_OK = 0,
+  IMP_DEV_NONFINITE_INPUT = 1, /* a NaN or Inf in a tensor being quantized; outputs unspecified */
+  IMP_DEV_TIMEOUT = 2          /* a bounded in-kernel wait gave up; outputs unspecified */
+};
+
+/* An NVFP4 tensor of `rows` x `K` elements (device pointers, caller-owned):
+ *   codes        uint8[rows][K/2]   packed E2M1 codes, low nibble = even element
+ *   scales       uint8[rows][K/16]  E4M3 block scales, row-major
+ *   tensor_scale float[1]           s = global amax / 2688                        */
+typedef struct {
+  uint8_t *codes;
+  uint8_t *scales;
+  float *tensor_scale;
+  int64_t rows;
+  int64_t K;
+} imp_nvfp4_tensor;
+
+/* Bytes of workspace imp_nvfp4_quantize needs for a rows x K tensor
+ * (per-CTA partial maxima; no initialization required). */
+size_t imp_nvfp4_quantize_workspace_size(int64_t rows, int64_t K);
+
+/* Quantize a bf16 matrix to NVFP4 with the recipe above.
+ *   x_bf16    device bf16[rows][ldx]; only the first K columns are read.
+ *   rows, K   rows >= 0 (0 writes s = 0 and nothing else), K > 0, K % 16 == 0.
+ *   ldx       row stride of x in elements, ldx >= K, ldx % 8 == 0.
+ *   out       out->rows == rows, out->K == K; codes/scales/tensor_scale written.
+ *   Bit-exact: codes, scale bytes and s equal the recipe's for every input
+ *   without NaN/Inf.  A NaN or Inf sets IMP_DEV_NONFINITE_INPUT.            */
+imp_status imp_nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                              const imp_nvfp4_tensor *out, int32_t *dev_status,
+                              void *workspace, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace imp_nvfp4_gemm needs for Y[M][N] = X[M][K] W^T (0 for
+ * M <= 16; the quantized X and its scales for M > 16). */
+size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* Y = X * W^T.
+ *   x_bf16   device bf16[M][ldx], ldx >= K, ldx % 8 == 0.
+ *   M        M >= 0 (0 = nothing to do).  M <= 16 takes the decode path,
+ *            M > 16 the prefill path (X quantized on device, block-scaled FP4
+ *            tensor-core MMA).
+ *   K        K > 0, K % 64 == 0, and w->K == K.
+ *   w        NVFP4 weight with w->rows = N >= 0 rows (0 = nothing to do).
+ *   y_bf16   device bf16[M][ldy], ldy >= N, ldy % 8 == 0; fully overwritten.
+ *   Accuracy: |y - y_exact| <= 2e-3 * sum_k |x_k w_k| + 1e-5 per element, with
+ *   y_exact the exact product of the operands defined above.  Results are
+ *   bitwise reproducible from run to run (fixed reduction order).           */
+imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                          const imp_nvfp4_tensor *w, void *y_bf16, int64_t ldy,
+                          int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *imp_status_string(imp_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IMP_NVFP4_H */

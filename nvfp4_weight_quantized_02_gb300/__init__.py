@@ -1,0 +1,194 @@
+"""Python binding of libimp_nvfp4 (include/imp_nvfp4.h).
+
+Argument marshalling only: every step of the quantizer and the linear layer
+runs in the library's CUDA kernels.  The C entry points are exposed under
+their own names (``imp_nvfp4_quantize``, ``imp_nvfp4_gemm``, ...) and take raw
+integers (device addresses, sizes, a cudaStream_t handle).  ``quantize`` and
+``gemm`` wrap them for torch CUDA tensors: they allocate outputs and the
+workspace with torch and pass the current stream.
+
+The shared library is loaded on first use (or by ``load()``); if it has not
+been built (``python -m nvfp4_weight_quantized_02_gb300.build``) that raises
+ImportError: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+
+from .build import INCLUDE, LIB
+
+__all__ = [
+    "IMP_OK", "IMP_DEV_OK", "IMP_DEV_NONFINITE_INPUT", "IMP_DEV_TIMEOUT", "ImpNvfp4Tensor",
+    "imp_nvfp4_quantize", "imp_nvfp4_gemm", "imp_nvfp4_quantize_workspace_size",
+    "imp_nvfp4_gemm_workspace_size", "imp_status_string", "NVFP4Tensor", "quantize", "gemm",
+    "library_path", "header_functions", "ImpError", "load",
+]
+
+IMP_OK = 0
+IMP_ERR_INVALID_ARG = 1
+IMP_ERR_UNSUPPORTED_SHAPE = 2
+IMP_ERR_MISALIGNED = 3
+IMP_ERR_WORKSPACE_TOO_SMALL = 4
+IMP_ERR_CUDA = 5
+IMP_DEV_OK = 0
+IMP_DEV_NONFINITE_INPUT = 1
+IMP_DEV_TIMEOUT = 2
+DECODE_M_MAX = 16
+
+class ImpNvfp4Tensor(ctypes.Structure):
+    """ctypes mirror of imp_nvfp4_tensor."""
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("tensor_scale", ctypes.c_void_p), ("rows", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def _L():
+    """The loaded library.  Raises ImportError if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise ImportError(f"libimp_nvfp4.so is not built ({LIB}); run "
+                          "python -m nvfp4_weight_quantized_02_gb300.build")
+    lib = ctypes.CDLL(LIB)
+    P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.imp_nvfp4_quantize_workspace_size.restype = SZ
+    lib.imp_nvfp4_quantize_workspace_size.argtypes = [I64, I64]
+    lib.imp_nvfp4_quantize.restype = ctypes.c_int
+    lib.imp_nvfp4_quantize.argtypes = [P, I64, I64, I64, ctypes.POINTER(ImpNvfp4Tensor), P, P, SZ, P]
+    lib.imp_nvfp4_gemm_workspace_size.restype = SZ
+    lib.imp_nvfp4_gemm_workspace_size.argtypes = [I64, I64, I64]
+    lib.imp_nvfp4_gemm.restype = ctypes.c_int
+    lib.imp_nvfp4_gemm.argtypes = [P, I64, I64, I64, ctypes.POINTER(ImpNvfp4Tensor), P, I64, P, P,
+                                   SZ, P]
+    lib.imp_status_string.restype = ctypes.c_char_p
+    lib.imp_status_string.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def load() -> ctypes.CDLL:
+    """Load the library now (ImportError if it is missing)."""
+    return _L()
+
+
+def library_path() -> str:
+    return LIB
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/imp_nvfp4.h."""
+    text = open(os.path.join(INCLUDE, "imp_nvfp4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(imp_\w+)\s*\(", text)))
+
+
+def imp_status_string(status: int) -> str:
+    return _L().imp_status_string(status).decode()
+
+
+def imp_nvfp4_quantize_workspace_size(rows: int, K: int) -> int:
+    return _L().imp_nvfp4_quantize_workspace_size(rows, K)
+
+
+def imp_nvfp4_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return _L().imp_nvfp4_gemm_workspace_size(M, N, K)
+
+
+def imp_nvfp4_quantize(x_bf16: int, rows: int, K: int, ldx: int, out: ImpNvfp4Tensor,
+                       dev_status: int | None, workspace: int | None, ws_bytes: int,
+                       stream: int | None) -> int:
+    return _L().imp_nvfp4_quantize(x_bf16, rows, K, ldx, ctypes.byref(out), dev_status, workspace,
+                                   ws_bytes, stream)
+
+
+def imp_nvfp4_gemm(x_bf16: int, M: int, K: int, ldx: int, w: ImpNvfp4Tensor, y_bf16: int,
+                   ldy: int, dev_status: int | None, workspace: int | None, ws_bytes: int,
+                   stream: int | None) -> int:
+    return _L().imp_nvfp4_gemm(x_bf16, M, K, ldx, ctypes.byref(w), y_bf16, ldy, dev_status,
+                               workspace, ws_bytes, stream)
+
+
+class ImpError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {imp_status_string(status)}")
+        self.status = status
+
+
+# ---- torch convenience layer (allocation + marshalling) ----------------------
+
+@dataclass
+class NVFP4Tensor:
+    """Device NVFP4 tensor: codes uint8[rows][K/2], scales uint8[rows][K/16],
+    tensor_scale float32[1]."""
+    codes: "object"
+    scales: "object"
+    tensor_scale: "object"
+
+    @property
+    def rows(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.codes.shape[1] * 2
+
+    def c_struct(self) -> ImpNvfp4Tensor:
+        return ImpNvfp4Tensor(self.codes.data_ptr(), self.scales.data_ptr(),
+                              self.tensor_scale.data_ptr(), self.rows, self.K)
+
+    @staticmethod
+    def empty(rows: int, K: int, device="cuda"):
+        import torch
+        return NVFP4Tensor(torch.empty((rows, K // 2), dtype=torch.uint8, device=device),
+                           torch.empty((rows, K // 16), dtype=torch.uint8, device=device),
+                           torch.empty(1, dtype=torch.float32, device=device))
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def quantize(x, out: NVFP4Tensor | None = None, dev_status=None, stream=None) -> NVFP4Tensor:
+    """Quantize a 2-D bf16 CUDA tensor (row stride may exceed K) to NVFP4."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, K = x.shape
+    if out is None:
+        out = NVFP4Tensor.empty(rows, K, device=x.device)
+    ws_bytes = imp_nvfp4_quantize_workspace_size(rows, K)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    st = imp_nvfp4_quantize(x.data_ptr(), rows, K, x.stride(0), out.c_struct(),
+                            None if dev_status is None else dev_status.data_ptr(), ws.data_ptr(),
+                            ws_bytes, _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_quantize")
+    return out
+
+
+def gemm(x, w: NVFP4Tensor, y=None, dev_status=None, stream=None, workspace=None):
+    """Y = X W^T for a 2-D bf16 CUDA tensor X and an NVFP4 weight."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    N = w.rows
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ws_bytes = imp_nvfp4_gemm_workspace_size(M, N, K)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    st = imp_nvfp4_gemm(x.data_ptr(), M, K, x.stride(0), w.c_struct(), y.data_ptr(), y.stride(0),
+                        None if dev_status is None else dev_status.data_ptr(),
+                        None if workspace is None else workspace.data_ptr(), ws_bytes,
+                        _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_gemm")
+    return y

@@ -1,0 +1,187 @@
+// NVFP4 quantizer (bf16 -> E2M1 codes + E4M3 block scales + fp32 tensor
+// scale), bit-exact to the recipe in imp_nvfp4.h.
+//
+// Two HBM-bound passes over X:
+//   1. amax_partial_kernel: one max|x| per CTA (as bf16 magnitude bits, which
+//      order like the values; NaN/Inf bit patterns sort above every finite
+//      value, so the same max detects them).
+//   2. encode_kernel: every CTA folds the partial maxima into g and
+//      s = g / 2688, then each thread encodes one 16-element block: block amax
+//      a, u = (a/6)/s, E4M3 scale byte via cvt.rn.satfinite.e4m3x2, d = e4m3*s,
+//      and 16 E2M1 codes via cvt.rn.satfinite.e2m1x2 on |x|/d with the sign
+//      bit copied from x.  Every fp32 step is an explicitly rounded IEEE op
+//      (__fdiv_rn, __fmul_rn), so no contraction or approximation can change
+//      a byte.
+#include "quantize.cuh"
+
+namespace impfp4 {
+
+namespace {
+
+constexpr int kAmaxThreads = 256;
+constexpr int kEncThreads = 256;
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Per-half max of the magnitude bits of 8 bf16 values (sign bits cleared
+// before comparing).
+__device__ __forceinline__ uint32_t absmax8(uint4 a) {
+  return __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                  __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu));
+}
+
+// Block-wide max of a per-thread value; result valid in every thread.
+template <int kThreads>
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
+  v = warp_max_u32(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  uint32_t r = (lane < kThreads / 32) ? red[lane] : 0u;
+  r = warp_max_u32(r);
+  __syncthreads();
+  return r;
+}
+
+// Pass 1: per-CTA max of |x| as bf16 magnitude bits.  Warps stride over rows;
+// lanes read 16-byte vectors (8 elements) of a row.
+__global__ void __launch_bounds__(kAmaxThreads) amax_partial_kernel(const uint16_t *__restrict__ x,
+                                                                    int64_t rows, int64_t K,
+                                                                    int64_t ldx,
+                                                                    uint32_t *__restrict__ partial,
+                                                                    int32_t *status) {
+  __shared__ uint32_t red[kAmaxThreads / 32];
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (kAmaxThreads / 32);
+  const int64_t vec_per_row = K / 8;
+  uint32_t m2 = 0;  // two 16-bit maxima side by side
+  for (int64_t r = (int64_t)blockIdx.x * (kAmaxThreads / 32) + (threadIdx.x >> 5); r < rows;
+       r += warps_total) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + r * ldx);
+    int64_t v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 a = __ldg(row + v), b = __ldg(row + v + 32), c = __ldg(row + v + 64),
+                  d = __ldg(row + v + 96);
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(absmax8(a), absmax8(b)), __vmaxu2(absmax8(c), absmax8(d))));
+    }
+    for (; v < vec_per_row; v += 32) m2 = __vmaxu2(m2, absmax8(__ldg(row + v)));
+  }
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+  m = block_max_u32<kAmaxThreads>(m, red);
+  if (threadIdx.x == 0) {
+    partial[blockIdx.x] = m;
+    if (m >= 0x7F80u) report(status, IMP_DEV_NONFINITE_INPUT);
+  }
+}
+
+// Pass 2: fold the partial maxima, then encode one 16-element block per thread.
+__global__ void __launch_bounds__(kEncThreads) encode_kernel(
+    const uint16_t *__restrict__ x, int64_t rows, int64_t K, int64_t ldx,
+    const uint32_t *__restrict__ partial, int num_partial, uint8_t *__restrict__ codes,
+    uint8_t *__restrict__ scales, float *__restrict__ tensor_scale) {
+  __shared__ uint32_t red[kEncThreads / 32];
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < num_partial; i += kEncThreads) m = max(m, partial[i]);
+  m = block_max_u32<kEncThreads>(m, red);
+  const float g = bf16_bits_to_f32(m < 0x7F80u ? m : 0u);
+  const float s = __fdiv_rn(g, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s;
+
+  // Warps stride over segments of 32 consecutive blocks of a row; each lane
+  // encodes one block of its warp's segment.
+  const int64_t blocks_per_row = K / 16;
+  const int64_t segs_per_row = ceil_div(blocks_per_row, 32);
+  const int64_t total_segs = rows * segs_per_row;
+  const int lane = threadIdx.x & 31;
+  for (int64_t seg = (int64_t)blockIdx.x * (kEncThreads / 32) + (threadIdx.x >> 5); seg < total_segs;
+       seg += (int64_t)gridDim.x * (kEncThreads / 32)) {
+    const int64_t r = seg / segs_per_row;
+    const int64_t b = (seg - r * segs_per_row) * 32 + lane;
+    if (b >= blocks_per_row) continue;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + b * 16);
+    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t a2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a2 = __vmaxu2(a2, w[i] & 0x7FFF7FFFu);
+    const float a = bf16_bits_to_f32(max(a2 & 0xFFFFu, a2 >> 16));
+    float u = 0.0f;
+    if (s != 0.0f) u = __fdiv_rn(__fdiv_rn(a, 6.0f), s);
+    const uint32_t sb = f32_to_e4m3_satfinite(u);
+    const float d = __fmul_rn(f16lo_to_f32(e4m3x2_to_f16x2(sb)), s);
+    uint32_t packed[2] = {0u, 0u};
+    if (d != 0.0f) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float q[8];
+        uint32_t sign = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t wi = w[4 * h + i];
+          q[2 * i] = __fdiv_rn(bf16_bits_to_f32(wi & 0x7FFFu), d);
+          q[2 * i + 1] = __fdiv_rn(bf16_bits_to_f32((wi >> 16) & 0x7FFFu), d);
+          // sign of element 2i -> bit 3 of nibble 2i; element 2i+1 -> bit 3 of nibble 2i+1
+          sign |= ((wi >> 15) & 1u) << (8 * i + 3);
+          sign |= (wi >> 31) << (8 * i + 7);
+        }
+        packed[h] = f32x8_to_e2m1_packed(q) | sign;
+      }
+    }
+    *reinterpret_cast<uint2 *>(codes + r * (K / 2) + b * 8) = make_uint2(packed[0], packed[1]);
+    scales[r * blocks_per_row + b] = static_cast<uint8_t>(sb);
+  }
+}
+
+int num_sms_cached() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// One warp per row at a time; at most kMaxPartials CTAs, so the workspace
+// size does not depend on the device.
+constexpr int kMaxPartials = 1024;
+
+int amax_grid(int64_t rows) {
+  int64_t g = ceil_div(rows, kAmaxThreads / 32);
+  if (g > kMaxPartials) g = kMaxPartials;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+int num_sms() { return num_sms_cached(); }
+
+size_t quantize_workspace_bytes(int64_t rows, int64_t /*K*/) {
+  return static_cast<size_t>(amax_grid(rows)) * sizeof(uint32_t);
+}
+
+cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                            uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                            int32_t *status, void *workspace, cudaStream_t stream) {
+  const int ga = amax_grid(rows);
+  uint32_t *partial = static_cast<uint32_t *>(workspace);
+  amax_partial_kernel<<<ga, kAmaxThreads, 0, stream>>>(x, rows, K, ldx, partial, status);
+  const int64_t segs = rows * ceil_div(K / 16, 32);
+  int64_t ge = ceil_div(segs, kEncThreads / 32);
+  const int64_t cap = (int64_t)num_sms_cached() * 8;
+  if (ge > cap) ge = cap;
+  if (ge < 1) ge = 1;
+  encode_kernel<<<static_cast<int>(ge), kEncThreads, 0, stream>>>(x, rows, K, ldx, partial, ga,
+                                                                   codes, scales, tensor_scale);
+  return cudaGetLastError();
+}
+
+}  // namespace impfp4

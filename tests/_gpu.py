@@ -1,0 +1,48 @@
+"""Helpers shared by the GPU parity tests."""
+import numpy as np
+import torch
+
+import oracle
+
+
+def dev_bf16(bits: np.ndarray, ld: int | None = None) -> torch.Tensor:
+    """uint16 bf16 bit patterns -> CUDA bf16 tensor (optionally with row stride ld)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    if ld is not None and ld != bits.shape[1]:
+        big = torch.zeros((bits.shape[0], ld), dtype=torch.bfloat16)
+        big[:, : bits.shape[1]] = t
+        return big.cuda()[:, : bits.shape[1]]
+    return t.cuda()
+
+
+def dev_nvfp4(codes: np.ndarray, scales: np.ndarray, s: float):
+    import nvfp4_weight_quantized_02_gb300 as pkg
+    return pkg.NVFP4Tensor(torch.from_numpy(np.ascontiguousarray(codes)).cuda(),
+                           torch.from_numpy(np.ascontiguousarray(scales)).cuda(),
+                           torch.tensor([s], dtype=torch.float32).cuda())
+
+
+def num_sms() -> int:
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def sample_rows(N: int, seed: int, n_random: int = 128) -> np.ndarray:
+    """Rows to check at full size: both ends, rows at the CTA boundaries of a
+    one-CTA-per-SM grid, and a seeded random sample."""
+    G = min(num_sms(), N)
+    rows = set(range(min(N, 48))) | set(range(max(0, N - 48), N))
+    for c in range(0, G + 1, max(1, G // 16)):
+        b = N * c // G
+        rows |= {max(0, b - 1), min(N - 1, b)}
+    rng = np.random.default_rng(seed)
+    rows |= set(rng.integers(0, N, n_random).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarray, what: str):
+    err = np.abs(y_gpu.astype(np.float64) - y_ref)
+    tol = oracle.tolerance(bound)
+    bad = np.argwhere(~(err <= tol))
+    assert bad.size == 0, (f"{what}: {len(bad)} elements outside tolerance, first {bad[:4].tolist()}, "
+                           f"err {err[tuple(bad[0])]:.3e} tol {tol[tuple(bad[0])]:.3e}")
+    return float((err / tol).max()) if err.size else 0.0

@@ -1,0 +1,75 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/imp_nvfp4.h declares, and rejects bad arguments before touching the
+device."""
+import ctypes
+
+import pytest
+
+import nvfp4_weight_quantized_02_gb300 as pkg
+from nvfp4_weight_quantized_02_gb300 import ImpNvfp4Tensor
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return pkg.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = pkg.header_functions()
+    assert {"imp_nvfp4_quantize", "imp_nvfp4_gemm", "imp_nvfp4_quantize_workspace_size",
+            "imp_nvfp4_gemm_workspace_size", "imp_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert hasattr(pkg, n), n  # the binding uses the same names
+
+
+def test_status_strings():
+    assert pkg.imp_status_string(0) == "IMP_OK"
+    assert pkg.imp_status_string(pkg.IMP_ERR_MISALIGNED) == "IMP_ERR_MISALIGNED"
+    assert pkg.imp_status_string(99) == "IMP_ERR_UNKNOWN"
+
+
+def test_workspace_sizes():
+    assert pkg.imp_nvfp4_quantize_workspace_size(0, 64) == 0
+    assert 0 < pkg.imp_nvfp4_quantize_workspace_size(151936, 5120) <= 4096
+    assert pkg.imp_nvfp4_gemm_workspace_size(1, 17408, 5120) == 0
+
+
+A16 = 0x7F0000000000  # fake, 16-byte aligned "device" addresses: never dereferenced
+
+
+def _t(rows, K, codes=A16, scales=A16 + 0x100000, ts=A16 + 0x200000):
+    return ImpNvfp4Tensor(codes, scales, ts, rows, K)
+
+
+def test_gemm_rejects_bad_arguments():
+    g = pkg.imp_nvfp4_gemm
+    assert g(A16, -1, 64, 64, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16, 1, 96, 96, _t(8, 96), A16, 8, None, None, 0, None) == pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    assert g(A16, 1, 0, 64, _t(8, 0), A16, 8, None, None, 0, None) == pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    assert g(A16, 1, 64, 64, _t(8, 128), A16, 8, None, None, 0, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16, 1, 64, 64, _t(8, 64, codes=0), A16, 8, None, None, 0, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16, 1, 64, 64, _t(8, 64, codes=A16 + 8), A16, 8, None, None, 0, None) == pkg.IMP_ERR_MISALIGNED
+    assert g(A16, 1, 64, 64, _t(8, 64, ts=A16 + 2), A16, 8, None, None, 0, None) == pkg.IMP_ERR_MISALIGNED
+    assert g(None, 1, 64, 64, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16, 1, 64, 64, _t(8, 64), None, 8, None, None, 0, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16, 1, 64, 32, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16, 1, 64, 64, _t(8, 64), A16, 4, None, None, 0, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16 + 2, 1, 64, 64, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_ERR_MISALIGNED
+    assert g(A16, 2, 64, 68, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_ERR_MISALIGNED
+    assert g(A16, 2, 64, 64, _t(8, 64), A16, 12, None, None, 0, None) == pkg.IMP_ERR_MISALIGNED
+    # empty problems are valid and enqueue nothing
+    assert g(A16, 0, 64, 64, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_OK
+    assert g(A16, 4, 64, 64, _t(0, 64), A16, 8, None, None, 0, None) == pkg.IMP_OK
+
+
+def test_quantize_rejects_bad_arguments():
+    q = pkg.imp_nvfp4_quantize
+    assert q(A16, -1, 64, 64, _t(-1, 64), None, A16, 4096, None) == pkg.IMP_ERR_INVALID_ARG
+    assert q(A16, 4, 40, 40, _t(4, 40), None, A16, 4096, None) == pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    assert q(A16, 4, 64, 32, _t(4, 64), None, A16, 4096, None) == pkg.IMP_ERR_INVALID_ARG
+    assert q(A16, 4, 64, 64, _t(5, 64), None, A16, 4096, None) == pkg.IMP_ERR_INVALID_ARG
+    assert q(A16 + 4, 4, 64, 64, _t(4, 64), None, A16, 4096, None) == pkg.IMP_ERR_MISALIGNED
+    assert q(A16, 4, 64, 68, _t(4, 64), None, A16, 4096, None) == pkg.IMP_ERR_MISALIGNED
+    assert q(A16, 4, 64, 64, _t(4, 64), None, None, 0, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    assert q(A16, 4, 64, 64, _t(4, 64), None, A16, 2, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL

@@ -1,0 +1,104 @@
+"""Decode path (M <= 16) vs the oracle: every element of Y within
+|y - y_ref| <= 2e-3 * sum|x w| + 1e-5, on the workload shapes (full size;
+the largest checked on sampled output columns) and edge shapes; results
+bitwise repeatable."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import check_within_tolerance, dev_bf16, dev_nvfp4, sample_rows
+
+pkg = pytest.importorskip("nvfp4_weight_quantized_02_gb300")
+pytestmark = pytest.mark.gpu
+
+
+def run_gemm(x_bits, w_dev, ldx=None, ldy=None):
+    x = dev_bf16(x_bits, ldx)
+    M, N = x_bits.shape[0], w_dev.rows
+    ldy = ldy or N
+    ybig = torch.full((M, ldy), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y = ybig[:, :N]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkg.gemm(x, w_dev, y=y, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return y.float().cpu().numpy()
+
+
+def oracle_w(lin):
+    bits = lin.weight_bf16()
+    c, s, ts, _ = oracle.quantize(bits)
+    return c, s, ts
+
+
+SMALL = synth.workload("single_1k") + synth.workload("decode_0p6b")
+
+
+@pytest.mark.parametrize("lin", SMALL, ids=lambda l: f"{l.name}_{l.K}x{l.N}")
+def test_small_workloads_every_element(lin):
+    c, s, ts = oracle_w(lin)
+    x = lin.act_bf16()
+    y = run_gemm(x, dev_nvfp4(c, s, ts))
+    y_ref, bound = oracle.reference_gemm(x, lin.M, c, s, ts)
+    check_within_tolerance(y, y_ref, bound, lin.name)
+
+
+FULL = synth.workload("decode_27b") + synth.workload("skinny_27b")
+
+
+@pytest.mark.parametrize("lin", FULL, ids=lambda l: f"{l.name}_M{l.M}_{l.K}x{l.N}")
+def test_full_size_sampled(lin):
+    w_bits = lin.weight_bf16()
+    w = pkg.quantize(dev_bf16(w_bits))
+    x = lin.act_bf16()
+    y = run_gemm(x, w)
+    _, ts, _ = oracle.tensor_scale(w_bits)
+    rows = sample_rows(lin.N, seed=lin.N + lin.M)
+    c, s = oracle.quantize_rows(w_bits[rows], ts)
+    # the device weight equals the oracle's on the sampled rows
+    assert np.array_equal(w.codes.cpu().numpy()[rows], c)
+    assert np.array_equal(w.scales.cpu().numpy()[rows], s)
+    y_ref, bound = oracle.reference_gemm(x, lin.M, c, s, ts)
+    check_within_tolerance(y[:, rows], y_ref, bound, lin.name)
+    assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("M,K,N,ldx,ldy", [
+    (1, 64, 1, 64, 8), (1, 64, 7, 72, 16), (1, 320, 333, 320, 336), (2, 192, 50, 200, 56),
+    (3, 1024, 1000, 1024, 1000), (5, 2048, 77, 2056, 80), (7, 448, 9, 448, 16),
+    (16, 64, 300, 64, 304), (9, 5120, 129, 5120, 136), (1, 17408, 5, 17408, 8),
+    (16, 1024, 2, 1024, 8), (1, 4096, 152, 4096, 152), (1, 4096, 153, 4096, 160)])
+def test_edge_shapes(M, K, N, ldx, ldy):
+    lin = synth.Linear("edge", M, K, N, 123, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
+                       zero_block_p=0.02, x_outlier_frac=0.02)
+    c, s, ts = oracle_w(lin)
+    x = lin.act_bf16()
+    y = run_gemm(x, dev_nvfp4(c, s, ts), ldx, ldy)
+    y_ref, bound = oracle.reference_gemm(x, M, c, s, ts)
+    check_within_tolerance(y, y_ref, bound, f"M{M} K{K} N{N}")
+
+
+def test_extreme_activation_magnitudes():
+    # X spanning bf16's range (huge, tiny, subnormal): the f16 staging of X
+    # must not overflow or flush.
+    lin = synth.Linear("mag", 1, 1024, 64, 5)
+    c, s, ts = oracle_w(lin)
+    rng = np.random.default_rng(0)
+    for exp in (-130, -60, -20, 0, 20, 60, 120):
+        xf = (rng.standard_normal((1, 1024)) * 2.0 ** exp).astype(np.float32)
+        xb = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        y = run_gemm(xb, dev_nvfp4(c, s, ts))
+        y_ref, bound = oracle.reference_gemm(xb, 1, c, s, ts)
+        if exp <= 120 - 10:
+            check_within_tolerance(y, y_ref, bound, f"x ~ 2^{exp}")
+
+
+def test_bitwise_repeatable():
+    lin = synth.workload("decode_27b")[2]
+    w = pkg.quantize(dev_bf16(lin.weight_bf16()))
+    x = lin.act_bf16()
+    a = run_gemm(x, w)
+    b = run_gemm(x, w)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
