@@ -1,0 +1,411 @@
+"""Benchmark of the NVFP4 linear layer on GB300.
+
+One step is one decode pass of the 27B-class workload at M = 1: the up and
+gate projections (5120 -> 17408), the down projection (17408 -> 5120) and the
+LM head (5120 -> 151936), each Y = X W^T with an NVFP4 weight resident in
+HBM.  The metric is the rate at which the step streams its algorithmic bytes
+(NVFP4 weight bytes + bf16 X and Y), in GB/s, next to the HBM roofline.  The
+weights of one step (588 MB) exceed the 129 MB L2, so every step reads them
+from HBM.
+
+Also reported (same JSON line): the prefill GEMM on the block-scaled FP4
+tensor-core path when the library provides it, the per-M skinny decode
+rates, and the quantizer.
+
+The CPU baseline is the oracle (plain single-threaded C++, fp64 matmul) timed
+on a bounded row sample of the same workload.  ``--impl reference`` times only
+that oracle, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "decode_27b"
+METRIC = "NVFP4 GEMV HBM GB/s (% of GB300 peak) at M=1; prefill FP4 TFLOPS (% peak)"
+
+
+def step_bytes(lins) -> int:
+    """Algorithmic bytes of one decode step: NVFP4 weights + bf16 X + bf16 Y."""
+    return sum(l.weight_bytes + 2 * l.M * l.K + 2 * l.M * l.N for l in lins)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(lins, budget_s: float, max_rows: int | None = None):
+    """Time the oracle's decode GEMV (dequant + fp64 matmul) on leading rows of
+    each weight of the workload.  Returns (GB/s of NVFP4 weight, seconds,
+    description).  Quantization of the sampled rows happens before the clock."""
+    import oracle
+
+    prepared = []
+    for l in lins:
+        rows = max_rows or max(8, min(l.N, 512))
+        wb = l.weight_bf16(0, rows)
+        _, ts, _ = oracle.tensor_scale(wb)
+        c, s = oracle.quantize_rows(wb, ts)
+        prepared.append((l, c, s, ts, l.act_bf16(), rows))
+    done_bytes, t0, calls = 0, time.perf_counter(), 0
+    while True:
+        for l, c, s, ts, x, rows in prepared:
+            oracle.reference_gemm(x, l.M, c, s, ts)
+            done_bytes += rows * (l.K // 2 + l.K // 16)
+            calls += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    desc = (f"oracle decode GEMV (dequant + fp64 matmul, 1 thread) on the first "
+            f"{prepared[0][5]} rows of each of {len(lins)} weights, {calls} calls")
+    return done_bytes / dt / 1e9, dt, desc
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    lins = synth.workload(args.workload)
+    per_step = []
+    for _ in range(args.warmup):
+        cpu_oracle_sample(lins, 0.0, max_rows=64)
+    gbs_all = []
+    for _ in range(args.steps):
+        gbs, dt, desc = cpu_oracle_sample(lins, 0.0, max_rows=256)
+        per_step.append(dt)
+        gbs_all.append(gbs)
+    gbs = statistics.median(gbs_all)
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(per_step), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "M": 1, "shapes_KxN": [[l.K, l.N] for l in lins],
+                       "l2": "inputs larger than L2"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_weight_quantized_02_gb300 as pkg
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.load()
+
+    # ---- inputs resident in HBM (weights quantized on device; not timed)
+    lins = synth.workload(args.workload)
+    weights, xs, ys = [], [], []
+    for l in lins:
+        wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+        weights.append(pkg.quantize(wb))
+        del wb
+        xs.append(torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev))
+        ys.append(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize()
+
+    def step():
+        for x, w, y in zip(xs, weights, ys):
+            pkg.gemm(x, w, y=y, dev_status=status, stream=stream)
+
+    # per-kernel timing events (on the launching stream)
+    def timed_steps(k, per_kernel):
+        evs = []
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(k):
+            if per_kernel:
+                row = []
+                for x, w, y in zip(xs, weights, ys):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    pkg.gemm(x, w, y=y, dev_status=status, stream=stream)
+                    e1.record(stream)
+                    row.append((e0, e1))
+                evs.append(row)
+            else:
+                step()
+        end.record(stream)
+        return start, end, evs
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        start, end, _ = timed_steps(args.steps, per_kernel=False)
+        torch.cuda.synchronize()
+        elapsed_ms = start.elapsed_time(end)
+        # second pass with per-kernel events (for the roofline of the top kernel)
+        _, _, evs = timed_steps(args.steps, per_kernel=True)
+        torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        dist.barrier()
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the benchmark")
+
+    per_kernel_ms = [statistics.mean(row[i][0].elapsed_time(row[i][1]) for row in evs)
+                     for i in range(len(lins))]
+    bytes_step = step_bytes(lins)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
+
+    # ---- e2e through the public API with host buffers
+    pin_x = [torch.empty(x.shape, dtype=torch.bfloat16, pin_memory=True).copy_(x) for x in xs]
+    pin_y = [torch.empty(y.shape, dtype=torch.bfloat16, pin_memory=True) for y in ys]
+    h2d = sum(p.numel() * 2 for p in pin_x)
+    d2h = sum(p.numel() * 2 for p in pin_y)
+
+    def e2e_step():
+        for px, x, w, y, py in zip(pin_x, xs, weights, ys, pin_y):
+            x.copy_(px, non_blocking=True)
+            pkg.gemm(x, w, y=y, dev_status=status, stream=stream)
+            py.copy_(y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
+
+    hbm_peak, _, peak_kind = load_peaks()
+    top = int(np.argmax(per_kernel_ms))
+    top_bytes = lins[top].weight_bytes + 2 * lins[top].K + 2 * lins[top].N
+    achieved = top_bytes / (per_kernel_ms[top] * 1e-3) / 1e9
+    traffic = load_traffic("gemv_kernel", lins[top])
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra = bench_extras(args, pkg, dev, stream, hbm_peak)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 weights, bf16 x/y, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "M": 1, "shapes_KxN": [[l.K, l.N] for l in lins],
+                   "bytes_per_step": bytes_step, "l2": "inputs larger than L2 (588 MB per step)",
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_hbm_peak": value / world / hbm_peak,
+        "per_kernel_us": {l.name: 1e3 * t for l, t in zip(lins, per_kernel_ms)},
+        "per_kernel_gbs": {l.name: (l.weight_bytes + 2 * l.K + 2 * l.N) / (t * 1e-3) / 1e9
+                           for l, t in zip(lins, per_kernel_ms)},
+        "roofline": {"bound": "hbm", "kernel": f"gemv_kernel ({lins[top].name} "
+                     f"{lins[top].K}x{lins[top].N})", "achieved": achieved, "peak": hbm_peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": traffic},
+        "gpu_launches": args.steps * len(lins),
+        "clocks": clocks.summary(),
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+    }
+    line.update(extra)
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, dt, desc = cpu_oracle_sample(lins, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def load_traffic(kernel: str, lin):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    summary records one for this shape (profiles/traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(f"{kernel}:{lin.K}x{lin.N}")
+    except (OSError, ValueError):
+        return None
+
+
+def bench_extras(args, pkg, dev, stream, hbm_peak):
+    """Skinny-M decode rates (M = 2..16) and the quantizer rate."""
+    import torch
+
+    out = {}
+    lins = synth.workload("skinny_27b")
+    skinny = {}
+    cache = {}
+    for l in lins:
+        key = (l.K, l.N)
+        if key not in cache:
+            wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+            cache[key] = pkg.quantize(wb)
+            del wb
+        w = cache[key]
+        x = torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+        y = torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev)
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        times = []
+        for i in range(args.warmup + 10):
+            flush.zero_()  # evict W from L2 between launches
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pkg.gemm(x, w, y=y, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+        t = statistics.median(times)
+        b = l.weight_bytes + 2 * l.M * l.K + 2 * l.M * l.N
+        skinny[f"M{l.M}_{l.K}x{l.N}"] = {"us": 1e3 * t, "GB/s": b / (t * 1e-3) / 1e9,
+                                         "TFLOP/s": 2 * l.M * l.N * l.K / (t * 1e-3) / 1e12}
+    out["skinny_decode"] = skinny
+    del cache
+    # quantizer: the LM-head-sized weight
+    l = synth.workload("decode_27b")[3]
+    wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+    q = pkg.quantize(wb)
+    times = []
+    for i in range(args.warmup + 5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pkg.quantize(wb, out=q, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    t = statistics.median(times)
+    qb = 2 * 2 * l.N * l.K + l.N * l.K // 2 + l.N * l.K // 16  # two reads of X + writes
+    out["quantizer"] = {"shape": [l.N, l.K], "us": 1e3 * t, "GB/s": qb / (t * 1e-3) / 1e9,
+                        "frac_of_hbm_peak": qb / (t * 1e-3) / 1e9 / hbm_peak}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="decode workload (default decode_27b; <workload>:<name> for one problem)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

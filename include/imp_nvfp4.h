@@ -93,7 +93,8 @@ size_t imp_nvfp4_quantize_workspace_size(int64_t rows, int64_t K);
 
 /* Quantize a bf16 matrix to NVFP4 with the recipe above.
  *   x_bf16    device bf16[rows][ldx]; only the first K columns are read.
- *   rows, K   rows >= 0 (0 writes s = 0 and nothing else), K > 0, K % 16 == 0.
+ *   rows, K   rows >= 0 (0 writes s = 0 and nothing else; codes and scales
+ *             may then be NULL), K > 0, K % 16 == 0.
  *   ldx       row stride of x in elements, ldx >= K, ldx % 8 == 0.
  *   out       out->rows == rows, out->K == K; codes/scales/tensor_scale written.
  *   Bit-exact: codes, scale bytes and s equal the recipe's for every input
@@ -114,8 +115,9 @@ size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  *   K        K > 0, K % 64 == 0, and w->K == K.
  *   w        NVFP4 weight with w->rows = N >= 0 rows (0 = nothing to do).
  *   y_bf16   device bf16[M][ldy], ldy >= N, ldy % 8 == 0; fully overwritten.
- *   Accuracy: |y - y_exact| <= 2e-3 * sum_k |x_k w_k| + 1e-5 per element, with
- *   y_exact the exact product of the operands defined above.  Results are
+ *   Accuracy: |y - y_exact| <= 2e-3 * sum_k |x_k w_k| + 1e-5 + 2^-8 |y_exact|
+ *   per element, with y_exact the exact product of the operands defined
+ *   above; the last term is the rounding of the result to bf16.  Results are
  *   bitwise reproducible from run to run (fixed reduction order).           */
 imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                           const imp_nvfp4_tensor *w, void *y_bf16, int64_t ldy,

@@ -47,10 +47,16 @@ imp_status imp_nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64
   if (rows < 0 || K <= 0) return rows < 0 ? IMP_ERR_INVALID_ARG : IMP_ERR_UNSUPPORTED_SHAPE;
   if (K % 16) return IMP_ERR_UNSUPPORTED_SHAPE;
   if (ldx < K) return IMP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {
+    // Empty tensor: only the tensor scale (0) is written; codes and scales
+    // may be NULL.
+    if (!out || out->rows != 0 || out->K != K || !out->tensor_scale) return IMP_ERR_INVALID_ARG;
+    if (!aligned4(out->tensor_scale)) return IMP_ERR_MISALIGNED;
+    return from_cuda(cudaMemsetAsync(out->tensor_scale, 0, sizeof(float), s));
+  }
   imp_status st = check_tensor(out, rows, K);
   if (st != IMP_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (rows == 0) return from_cuda(cudaMemsetAsync(out->tensor_scale, 0, sizeof(float), s));
   if (!x_bf16) return IMP_ERR_INVALID_ARG;
   if (!aligned16(x_bf16) || ldx % 8) return IMP_ERR_MISALIGNED;
   const size_t need = impfp4::quantize_workspace_bytes(rows, K);
@@ -73,9 +79,10 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
   if (M < 0 || !w) return IMP_ERR_INVALID_ARG;
   if (K <= 0 || K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
   const int64_t N = w->rows;
+  if (N < 0 || w->K != K) return IMP_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return IMP_OK;  // nothing to read or write
   imp_status st = check_tensor(w, N, K);
   if (st != IMP_OK) return st;
-  if (M == 0 || N == 0) return IMP_OK;
   if (!x_bf16 || !y_bf16) return IMP_ERR_INVALID_ARG;
   if (ldx < K || ldy < N) return IMP_ERR_INVALID_ARG;
   if (!aligned16(x_bf16) || !aligned16(y_bf16) || ldx % 8 || ldy % 8) return IMP_ERR_MISALIGNED;

@@ -182,6 +182,32 @@ def reference_gemm(x_bf16: np.ndarray, M_total: int, w_codes: np.ndarray,
     return matmul_abt(xh, wh)
 
 
-def tolerance(bound: np.ndarray) -> np.ndarray:
-    """Per-element acceptance band |y - y_ref| <= 2e-3 * sum|x w| + 1e-5."""
-    return 2e-3 * bound + 1e-5
+BF16_UNIT_ROUNDOFF = 2.0 ** -8
+
+
+def tolerance(bound: np.ndarray, y_ref: np.ndarray | None = None) -> np.ndarray:
+    """Per-element acceptance band for a bf16 result:
+    |y - y_ref| <= 2e-3 * sum|x w| + 1e-5 + 2^-8 * |y_ref|.
+
+    The first two terms are the stated bound on the arithmetic.  The last is
+    the rounding of the result to bf16 (8 significant bits, unit roundoff
+    2^-8): the exactly rounded bf16 value of y_ref can itself differ from
+    y_ref by up to 2^-8 |y_ref|, which exceeds 2e-3 * sum|x w| whenever
+    |y_ref| > 0.512 * sum|x w| (short or one-signed sums)."""
+    tol = 2e-3 * bound + 1e-5
+    if y_ref is not None:
+        tol = tol + BF16_UNIT_ROUNDOFF * np.abs(y_ref)
+    return tol
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (normal range)."""
+    _, e = np.frexp(np.abs(np.asarray(v, dtype=np.float64)))
+    return np.ldexp(1.0, e - 8)
+
+
+def tight_tolerance(bound: np.ndarray, y_ref: np.ndarray) -> np.ndarray:
+    """A stricter band for kernels whose products are exact and whose sums are
+    fp32: one bf16 ulp of y_ref plus 2^-14 * sum|x w| (room for ~1000 fp32
+    roundings).  A dropped or doubled block moves y by far more than this."""
+    return bf16_ulp(y_ref) + 2.0 ** -14 * bound + 1e-30

@@ -164,7 +164,14 @@ def _w27(name, M, K, N, seed, outlier_frac):
 
 
 def workload(name: str) -> list[Linear]:
-    """The list of linear problems of a named workload."""
+    """The list of linear problems of a named workload.  ``<workload>:<name>``
+    selects one problem of a workload (e.g. ``decode_27b:down``)."""
+    if ":" in name:
+        base, part = name.split(":", 1)
+        sel = [l for l in workload(base) if l.name == part]
+        if not sel:
+            raise KeyError(name)
+        return sel
     if name == "single_1k":
         return [Linear("single", 1, 1024, 1024, 0)]
     if name == "decode_0p6b":

@@ -39,9 +39,18 @@ def sample_rows(N: int, seed: int, n_random: int = 128) -> np.ndarray:
     return np.array(sorted(rows), dtype=np.int64)
 
 
-def check_within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarray, what: str):
+def check_within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarray, what: str,
+                           tight: bool = True):
+    """The acceptance band (oracle.tolerance) on every element and, with
+    tight=True, the stricter band of exact products + fp32 sums."""
     err = np.abs(y_gpu.astype(np.float64) - y_ref)
-    tol = oracle.tolerance(bound)
+    if tight:
+        ttol = oracle.tight_tolerance(bound, y_ref)
+        tbad = np.argwhere(~(err <= ttol))
+        assert tbad.size == 0, (f"{what}: {len(tbad)} elements outside the tight band, first "
+                                f"{tbad[:4].tolist()}, err {err[tuple(tbad[0])]:.3e} tight tol "
+                                f"{ttol[tuple(tbad[0])]:.3e}")
+    tol = oracle.tolerance(bound, y_ref)
     bad = np.argwhere(~(err <= tol))
     assert bad.size == 0, (f"{what}: {len(bad)} elements outside tolerance, first {bad[:4].tolist()}, "
                            f"err {err[tuple(bad[0])]:.3e} tol {tol[tuple(bad[0])]:.3e}")

@@ -225,3 +225,26 @@ def test_roundtrip_error_bound(dist, scale):
     assert np.all(err[sub] <= lim2[sub])
     # Zero-scale blocks dequantize to zero.
     assert np.all(xq[d == 0] == 0)
+
+
+def test_tolerance_admits_correctly_rounded_bf16_and_tight_band_catches_a_dropped_block():
+    # One-signed short sums: |y| close to sum|x w|, where bf16 rounding alone
+    # exceeds 2e-3 * sum|x w|; the acceptance band must still admit the
+    # correctly rounded bf16 of the exact value.
+    rng = np.random.default_rng(3)
+    y = rng.uniform(0.5, 100.0, 10000) * rng.choice([-1, 1], 10000)
+    yb = torch.from_numpy(y).to(torch.bfloat16).to(torch.float64).numpy()
+    bound = np.abs(y)
+    assert np.all(np.abs(yb - y) <= oracle.tolerance(bound, y))
+    assert np.all(np.abs(yb - y) <= oracle.tight_tolerance(bound, y))
+    # Plant a mistake in an oracle result (drop one 16-element block of a
+    # K = 5120 row) and check the tight band rejects it.
+    lin = synth.Linear("drop", 1, 5120, 64, 21, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02)
+    codes, scales, s, _ = oracle.quantize(lin.weight_bf16())
+    x = lin.act_bf16()
+    y_ref, bound = oracle.reference_gemm(x, 1, codes, scales, s)
+    scales2 = scales.copy()
+    scales2[:, 100] = 0
+    y_bad, _ = oracle.reference_gemm(x, 1, codes, scales2, s)
+    err = np.abs(y_bad - y_ref)
+    assert np.mean(err > oracle.tight_tolerance(bound, y_ref)) > 0.5
