@@ -190,7 +190,9 @@ __global__ void __launch_bounds__(max_threads_for(CPT, MT), 1) gemv_kernel(const
     const int s = (int)(i % NS);
     // A warp whose wait gives up still meets the others at the named barrier
     // below, so no consumer can be left waiting there; all leave together.
-    const bool ready = mbar_wait_bounded(&full[s], (uint32_t)((i / NS) & 1), a.status);
+    // warp-uniform: the shuffles below need all 32 lanes
+    const bool ready =
+        __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[s], (uint32_t)((i / NS) & 1), a.status));
     if (!ready) *abort_flag = 1;
     const int64_t r0 = row_begin + i * RS;
     const int rows_i = (int)min((int64_t)RS, row_end - r0);
@@ -352,6 +354,7 @@ int pass_tile(int64_t M_left, int64_t N, int64_t K, Plan &p) {
 
 bool gemv_supported(int64_t M, int64_t N, int64_t K) {
   if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return false;
+  if (M == 1 && gemv_m1_supported(N, K)) return true;
   for (int64_t m0 = 0; m0 < M;) {
     Plan p;
     const int MT = pass_tile(M - m0, N, K, p);
@@ -364,6 +367,8 @@ bool gemv_supported(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_gemv(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const uint8_t *codes,
                         const uint8_t *scales, const float *tensor_scale, int64_t N, uint16_t *y,
                         int64_t ldy, int32_t *status, cudaStream_t stream) {
+  if (M == 1 && gemv_m1_supported(N, K))
+    return launch_gemv_m1(x, K, codes, scales, tensor_scale, N, y, status, stream);
   for (int64_t m0 = 0; m0 < M;) {
     Plan p;
     const int MT = pass_tile(M - m0, N, K, p);

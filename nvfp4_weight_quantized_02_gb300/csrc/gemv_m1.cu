@@ -1,0 +1,394 @@
+// Decode GEMV at M = 1: y[n] = s * sum_k x[k] * e2m1(c[n][k]) * e4m3(sb[n][k/16]).
+//
+// Decode is bandwidth-bound (imp README, "How it works"; "1. The big
+// picture", section "The most important number in this book"), so the kernel
+// is shaped to stream W at HBM speed with as few instructions per weight as
+// possible:
+//
+//  * Persistent grid, one CTA per SM; CTA c owns rows [N*c/G, N*(c+1)/G).
+//  * A producer thread streams stages of RS whole rows (codes, and scales when
+//    K % 256 == 0) into a shared-memory ring with 1-D bulk copies
+//    (cp.async.bulk + mbarrier transaction counts); rows of the [N][K/2] code
+//    array are contiguous, so a stage is one copy per array.
+//  * The multiply-accumulate runs on the tensor cores (mma.sync m16n8k16,
+//    f16 x f16 -> f32).  For one "unit" of two rows x 1024 k:
+//      lane L (= 4g + t) owns the two 16-element blocks 2L and 2L+1 of the
+//      unit in both rows: one 16-byte shared-memory read per row, all 32
+//      lanes reading 512 contiguous bytes (no bank conflicts).
+//      A row g    = row n,   the block group of lanes 4g..4g+3,
+//      A row g+8  = row n+1, the same block group,
+//      B column g = X at that block group's k,
+//    so D[g][g] and D[g+8][g] are the two rows' partial dot products over
+//    block group g; the other D entries are never read.  Eight mma steps
+//    cover the unit (step s takes elements 4(s%4)..4(s%4)+3 of block
+//    2L + s/4 in every lane).
+//  * A fragments: cvt.rn.f16x2.e2m1x2 per code byte, multiplied (HMUL2) by
+//    the block's E4M3 scale (cvt.rn.f16x2.e4m3x2).  e2m1 * e4m3 has at most
+//    6 significant bits and lies in [2^-10, 2688], so it is exact in f16.
+//  * B fragments: each warp owns a fixed K-slice and keeps X for it in
+//    registers as f16, scaled by one power of two 2^sh per call so that
+//    max|x| lies in [2^14, 2^15): exact for every element within 2^24 of the
+//    largest (smaller ones round to f16 subnormals: an absolute error below
+//    max|x| * 2^-39 per element).  The factor is undone in fp32 at the end.
+//  * Products are exact; sums are fp32 (tensor-core accumulation across the
+//    warp's units, then a shuffle butterfly, then a fixed-order sum of the
+//    per-warp partials), times the tensor scale, rounded to bf16.  No step
+//    depends on timing, so results are bitwise reproducible.
+#include "gemv.cuh"
+
+namespace impfp4 {
+
+namespace {
+
+constexpr int kProducer = 32;
+constexpr int kMaxStages = 8;
+constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kHeadBytes = 2 * kMaxStages * sizeof(uint64_t) + 16;
+constexpr int kUnitK = 1024;  // k per unit (per warp step over two rows)
+
+struct M1Args {
+  const uint16_t *x;
+  const uint8_t *codes;
+  const uint8_t *scales;
+  const float *tensor_scale;
+  uint16_t *y;
+  int64_t N, K;
+  int32_t *status;
+  int rows_per_stage;  // RS (even)
+  int nstages;         // NS
+  int warps_per_row;   // NWK: warps splitting K
+  int row_groups;      // RG: groups of warps taking different row pairs
+  int scales_bulk;
+  uint32_t stage_bytes, codes_stage_bytes;
+};
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %1, %2;" : "=r"(d) : "r"(a), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f16x2_pack(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// One unit: rows (r0, r1) of the stage, 1024 k starting at unit*1024.
+// cw0/cw1: the lane's 16 code bytes of each row; sc0/sc1: its two scale
+// bytes of each row; xr: the lane's 32 X values as 16 f16x2.
+__device__ __forceinline__ void unit_mma(float (&d)[4], float (&e)[4], const uint4 cw0, const uint4 cw1,
+                                         uint32_t sc0, uint32_t sc1, const uint32_t (&xr)[16]) {
+  const uint32_t s0 = e4m3x2_to_f16x2(sc0);  // (block 2L, block 2L+1) of row n
+  const uint32_t s1 = e4m3x2_to_f16x2(sc1);  // same blocks of row n+1
+  const uint32_t w0[4] = {cw0.x, cw0.y, cw0.z, cw0.w};
+  const uint32_t w1[4] = {cw1.x, cw1.y, cw1.z, cw1.w};
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    const uint32_t sa = prmt(s0, blk ? 0x3232u : 0x1010u);  // this block's scale in both halves
+    const uint32_t sb = prmt(s1, blk ? 0x3232u : 0x1010u);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      // 4 bytes = 8 elements = two mma steps
+      uint32_t h0[4], h1[4];
+      e2m1x8_to_f16x2x4(w0[2 * blk + half], h0);
+      e2m1x8_to_f16x2x4(w1[2 * blk + half], h1);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int ei = 8 * blk + 4 * half + 2 * q;  // f16x2 index of elements 4s'..4s'+1
+        // two independent accumulator chains (steps alternate)
+        mma16816(q ? e : d, hmul2(h0[2 * q], sa), hmul2(h1[2 * q], sb), hmul2(h0[2 * q + 1], sa),
+                 hmul2(h1[2 * q + 1], sb), xr[ei], xr[ei + 1]);
+      }
+    }
+  }
+}
+
+// Consumer warps per CTA an instantiation is compiled for: X takes 16
+// registers per unit, so wider K-slices get fewer, fatter warps.
+__host__ __device__ constexpr int max_consumer_warps(int ku) { return ku <= 2 ? 16 : 8; }
+
+template <int KU>
+__global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
+    gemv_m1_kernel(const M1Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int NS = a.nstages, RS = a.rows_per_stage, NWK = a.warps_per_row, RG = a.row_groups;
+  const int n_cw = NWK * RG;  // consumer warps
+  const int64_t KH = a.K / 2, KB = a.K / 16;
+  const int n_units = (int)ceil_div(a.K, kUnitK);
+
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + kMaxStages;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kMaxStages);
+  float *red = reinterpret_cast<float *>(smem + kHeadBytes);  // [NS][RS][NWK]
+  const size_t red_bytes = (size_t)NS * RS * NWK * sizeof(float) + 32 * sizeof(float);
+  float *wmax = red + (size_t)NS * RS * NWK;  // [32] per-warp max|x|
+  uint8_t *stages = smem + kHeadBytes + ceil_div(red_bytes, 128) * 128;
+
+  const int64_t G = gridDim.x;
+  const int64_t row_begin = a.N * (int64_t)blockIdx.x / G;
+  const int64_t row_end = a.N * ((int64_t)blockIdx.x + 1) / G;
+  const int64_t n_st = ceil_div(row_end - row_begin, RS);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], n_cw);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (threadIdx.x < kProducer) {
+    if (threadIdx.x != 0) return;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t i = 0; i < n_st; ++i) {
+      const int s = (int)(i % NS);
+      if (i >= NS && !mbar_wait_bounded(&empty[s], (uint32_t)(((i / NS) - 1) & 1), a.status)) {
+        ok = false;
+        break;
+      }
+      const int64_t r0 = row_begin + i * RS;
+      const int64_t rows_i = min((int64_t)RS, row_end - r0);
+      const uint32_t cbytes = (uint32_t)(rows_i * KH);
+      const uint32_t sbytes = a.scales_bulk ? (uint32_t)(rows_i * KB) : 0u;
+      uint8_t *st = stages + (size_t)s * a.stage_bytes;
+      mbar_arrive_expect_tx(&full[s], cbytes + sbytes);
+      bulk_g2s(st, a.codes + r0 * KH, cbytes, &full[s]);
+      if (sbytes) bulk_g2s(st + a.codes_stage_bytes, a.scales + r0 * KB, sbytes, &full[s]);
+      ++issued;
+    }
+    if (!ok) {
+      for (int64_t i = (issued > NS ? issued - NS : 0); i < issued; ++i)
+        mbar_wait_bounded(&full[i % NS], (uint32_t)((i / NS) & 1), a.status);
+    }
+    return;
+  }
+
+  const int cw = (threadIdx.x - kProducer) >> 5;  // consumer warp
+  const int lane = threadIdx.x & 31;
+  const int rg = cw / NWK, wk = cw - rg * NWK;
+  const int g = lane >> 2, t = lane & 3;
+  const int u0 = wk * KU;  // first unit of this warp's K-slice
+
+  // ---- X for this warp's K-slice: lane's 32 elements per unit
+  uint32_t xb[KU][16];  // raw bf16 pairs, then f16 pairs
+  uint32_t mx = 0;
+#pragma unroll
+  for (int j = 0; j < KU; ++j) {
+    const int64_t k0 = (int64_t)(u0 + j) * kUnitK + 32 * lane;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xb[j][i] = 0u;
+    if (u0 + j < n_units && k0 < a.K) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.x + k0);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 q = __ldg(src + v);
+        xb[j][4 * v] = q.x; xb[j][4 * v + 1] = q.y; xb[j][4 * v + 2] = q.z; xb[j][4 * v + 3] = q.w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mx = __vmaxu2(mx, xb[j][i] & 0x7FFF7FFFu);
+  }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if (lane == 0) wmax[cw] = __uint_as_float(mx << 16);
+  named_bar(1, n_cw * 32);
+  float xmax = 0.0f;
+  for (int w = 0; w < NWK; ++w) xmax = fmaxf(xmax, wmax[w]);
+  int sh = 0;
+  if (xmax > 0.0f && xmax < __int_as_float(0x7F800000)) {
+    int e;
+    frexpf(xmax, &e);
+    sh = 15 - e;
+  }
+#pragma unroll
+  for (int j = 0; j < KU; ++j)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      xb[j][i] = f16x2_pack(ldexpf(bf16_bits_to_f32(xb[j][i] & 0xFFFFu), sh),
+                            ldexpf(bf16_bits_to_f32(xb[j][i] >> 16), sh));
+  const float out_scale = *a.tensor_scale;
+  const float x_unscale = ldexpf(1.0f, -sh);
+  const bool diag = (t == (g >> 1));
+  const int dsel = g & 1;
+
+  for (int64_t i = 0; i < n_st; ++i) {
+    const int s = (int)(i % NS);
+    // warp-uniform: mma.sync and the shuffles below need all 32 lanes
+    const bool ready =
+        __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[s], (uint32_t)((i / NS) & 1), a.status));
+    if (!ready) *abort_flag = 1;
+    const int64_t r0 = row_begin + i * RS;
+    const int rows_i = (int)min((int64_t)RS, row_end - r0);
+    const uint8_t *st_codes = stages + (size_t)s * a.stage_bytes;
+    const uint8_t *st_scales = st_codes + a.codes_stage_bytes;
+    float *red_s = red + (size_t)s * RS * NWK;
+
+    for (int p = ready ? rg : RS; 2 * p < rows_i; p += RG) {
+      const int ra = 2 * p, rb = 2 * p + 1;
+      const bool has_b = rb < rows_i;
+      float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < KU; ++j) {
+        const int u = u0 + j;
+        if (u < n_units) {  // warp-uniform; lanes past K feed zeros to the mma
+          const int64_t kb = (int64_t)u * (kUnitK / 16) + 2 * lane;  // lane's first block
+          uint4 cw0 = make_uint4(0, 0, 0, 0), cw1 = make_uint4(0, 0, 0, 0);
+          uint32_t sc0 = 0, sc1 = 0;
+          if (kb < KB) {
+            cw0 = *reinterpret_cast<const uint4 *>(st_codes + ra * KH + kb * 8);
+            if (has_b) cw1 = *reinterpret_cast<const uint4 *>(st_codes + rb * KH + kb * 8);
+            if (a.scales_bulk) {
+              sc0 = *reinterpret_cast<const uint16_t *>(st_scales + ra * KB + kb);
+              if (has_b) sc1 = *reinterpret_cast<const uint16_t *>(st_scales + rb * KB + kb);
+            } else {
+              sc0 = __ldg(reinterpret_cast<const uint16_t *>(a.scales + (r0 + ra) * KB + kb));
+              if (has_b)
+                sc1 = __ldg(reinterpret_cast<const uint16_t *>(a.scales + (r0 + rb) * KB + kb));
+            }
+          }
+          unit_mma(d, d2, cw0, cw1, sc0, sc1, xb[j]);
+        }
+      }
+      // D[g][g] (row ra) and D[g+8][g] (row rb) live in lane (g, g/2).
+      float v0 = diag ? d[dsel] + d2[dsel] : 0.0f;
+      float v1 = diag ? d[2 + dsel] + d2[2 + dsel] : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, o);
+        v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, o);
+      }
+      if (lane == 0) {
+        red_s[ra * NWK + wk] = v0;
+        if (has_b) red_s[rb * NWK + wk] = v1;
+      }
+    }
+    named_bar(1, n_cw * 32);
+    if (*abort_flag) return;
+    for (int r = (threadIdx.x - kProducer); r < rows_i; r += n_cw * 32) {
+      float v = 0.0f;
+      for (int w = 0; w < NWK; ++w) v += red_s[r * NWK + w];
+      v = (v * x_unscale) * out_scale;
+      a.y[r0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+struct M1Plan {
+  int KU, NWK, RG, RS, NS, threads, scales_bulk;
+  uint32_t stage_bytes, codes_stage_bytes;
+  size_t smem;
+};
+
+bool make_m1_plan(int64_t N, int64_t K, M1Plan &p) {
+  const int n_units = (int)ceil_div(K, kUnitK);
+  // Fewest units per warp that keeps warps per row within the instantiation's
+  // limit (X registers: 16 per unit).
+  int KU = (int)ceil_div(n_units, 12);
+  while (KU <= 4 && ceil_div(n_units, KU) > max_consumer_warps(KU)) ++KU;
+  if (KU < 1) KU = 1;
+  if (KU > 4) return false;
+  p.KU = KU;
+  p.NWK = (int)ceil_div(n_units, KU);
+  int RG = max_consumer_warps(KU) / p.NWK;
+  if (RG < 1) RG = 1;
+  p.RG = RG;
+  p.threads = kProducer + 32 * p.NWK * p.RG;
+  if (p.NWK * p.RG > max_consumer_warps(KU)) return false;
+  p.scales_bulk = (K % 256 == 0) ? 1 : 0;
+  const int64_t row_bytes = K / 2 + (p.scales_bulk ? K / 16 : 0);
+  // Each row group takes one row pair per stage at least.
+  int64_t RS = 2 * p.RG;
+  while (RS * 2 * row_bytes <= 40 * 1024 && RS < 64) RS *= 2;
+  const int64_t rows_per_cta = ceil_div(N, num_sms());
+  const int64_t cap = 2 * ceil_div(rows_per_cta, 2);
+  if (RS > cap) RS = cap < 2 ? 2 : cap;
+  p.RS = (int)RS;
+  p.codes_stage_bytes = (uint32_t)(ceil_div(RS * (K / 2), 128) * 128);
+  const uint32_t sbytes = p.scales_bulk ? (uint32_t)(ceil_div(RS * (K / 16), 128) * 128) : 0u;
+  p.stage_bytes = p.codes_stage_bytes + sbytes;
+  int NS = kMaxStages;
+  auto total = [&](int ns) {
+    const size_t red = (size_t)ns * p.RS * p.NWK * sizeof(float) + 32 * sizeof(float);
+    return kHeadBytes + ceil_div(red, 128) * 128 + (size_t)ns * p.stage_bytes;
+  };
+  while (NS > 2 && total(NS) > kSmemBudget) --NS;
+  p.NS = NS;
+  p.smem = total(NS);
+  return p.smem <= 227 * 1024;
+}
+
+template <int KU>
+cudaError_t launch_m1(const M1Args &a, const M1Plan &p, int grid, cudaStream_t stream) {
+  auto kern = gemv_m1_kernel<KU>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, p.threads, p.smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemv_m1_supported(int64_t N, int64_t K) {
+  M1Plan p;
+  return N >= 1 && K >= 64 && K % 64 == 0 && make_m1_plan(N, K, p);
+}
+
+cudaError_t launch_gemv_m1(const uint16_t *x, int64_t K, const uint8_t *codes,
+                           const uint8_t *scales, const float *tensor_scale, int64_t N,
+                           uint16_t *y, int32_t *status, cudaStream_t stream) {
+  M1Plan p;
+  if (!make_m1_plan(N, K, p)) return cudaErrorInvalidConfiguration;
+  M1Args a;
+  a.x = x;
+  a.codes = codes;
+  a.scales = scales;
+  a.tensor_scale = tensor_scale;
+  a.y = y;
+  a.N = N;
+  a.K = K;
+  a.status = status;
+  a.rows_per_stage = p.RS;
+  a.nstages = p.NS;
+  a.warps_per_row = p.NWK;
+  a.row_groups = p.RG;
+  a.scales_bulk = p.scales_bulk;
+  a.stage_bytes = p.stage_bytes;
+  a.codes_stage_bytes = p.codes_stage_bytes;
+  int64_t grid = num_sms();
+  if (grid > N) grid = N;
+  switch (p.KU) {
+    case 1: return launch_m1<1>(a, p, (int)grid, stream);
+    case 2: return launch_m1<2>(a, p, (int)grid, stream);
+    case 3: return launch_m1<3>(a, p, (int)grid, stream);
+    case 4: return launch_m1<4>(a, p, (int)grid, stream);
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace impfp4
