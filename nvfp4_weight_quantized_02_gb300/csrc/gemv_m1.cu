@@ -58,6 +58,7 @@ struct M1Args {
   int nstages;         // NS
   int warps_per_row;   // NWK: warps splitting K
   int row_groups;      // RG: groups of warps taking different row pairs
+  int rows_per_block;  // RB: rows whose partial sums are reduced together
   int scales_bulk;
   uint32_t stage_bytes, codes_stage_bytes;
 };
@@ -123,14 +124,38 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], float (&e)[4], const uin
 }
 
 // Consumer warps per CTA an instantiation is compiled for: X takes 16
-// registers per unit, so wider K-slices get fewer, fatter warps.
-__host__ __device__ constexpr int max_consumer_warps(int ku) { return ku <= 2 ? 16 : 8; }
+// registers per unit, so wider K-slices get fewer warps.
+__host__ __device__ constexpr int max_consumer_warps(int ku) { return ku <= 1 ? 16 : ku == 2 ? 12 : 8; }
+
+// Partial dot products of one unit for NP row pairs (NP independent
+// accumulator pairs, so the tensor-core chains overlap).
+template <int NP>
+__device__ __forceinline__ void pairs_unit(float (&d)[NP][2][4], const uint8_t *st_codes,
+                                           const uint8_t *st_scales, const uint8_t *g_scales,
+                                           const int (&ra)[NP], const bool (&has_b)[NP],
+                                           int64_t KH, int64_t KB, int64_t kb, bool lane_in,
+                                           bool scales_bulk, const uint32_t (&xr)[16]) {
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    uint4 cw0 = make_uint4(0, 0, 0, 0), cw1 = make_uint4(0, 0, 0, 0);
+    uint32_t sc0 = 0, sc1 = 0;
+    if (lane_in) {
+      cw0 = *reinterpret_cast<const uint4 *>(st_codes + ra[p] * KH + kb * 8);
+      if (has_b[p]) cw1 = *reinterpret_cast<const uint4 *>(st_codes + (ra[p] + 1) * KH + kb * 8);
+      const uint8_t *sbase = scales_bulk ? st_scales : g_scales;
+      sc0 = *reinterpret_cast<const uint16_t *>(sbase + ra[p] * KB + kb);
+      if (has_b[p]) sc1 = *reinterpret_cast<const uint16_t *>(sbase + (ra[p] + 1) * KB + kb);
+    }
+    unit_mma(d[p][0], d[p][1], cw0, cw1, sc0, sc1, xr);
+  }
+}
 
 template <int KU>
 __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
     gemv_m1_kernel(const M1Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int NS = a.nstages, RS = a.rows_per_stage, NWK = a.warps_per_row, RG = a.row_groups;
+  const int RB = a.rows_per_block;
   const int n_cw = NWK * RG;  // consumer warps
   const int64_t KH = a.K / 2, KB = a.K / 16;
   const int n_units = (int)ceil_div(a.K, kUnitK);
@@ -138,9 +163,9 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + kMaxStages;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kMaxStages);
-  float *red = reinterpret_cast<float *>(smem + kHeadBytes);  // [NS][RS][NWK]
-  const size_t red_bytes = (size_t)NS * RS * NWK * sizeof(float) + 32 * sizeof(float);
-  float *wmax = red + (size_t)NS * RS * NWK;  // [32] per-warp max|x|
+  float *red = reinterpret_cast<float *>(smem + kHeadBytes);  // [RB][NWK]
+  float *wmax = red + (size_t)RB * NWK;                       // [32]
+  const size_t red_bytes = ((size_t)RB * NWK + 32) * sizeof(float);
   uint8_t *stages = smem + kHeadBytes + ceil_div(red_bytes, 128) * 128;
 
   const int64_t G = gridDim.x;
@@ -186,13 +211,14 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
   }
 
   const int cw = (threadIdx.x - kProducer) >> 5;  // consumer warp
+  const int ct = threadIdx.x - kProducer;
   const int lane = threadIdx.x & 31;
   const int rg = cw / NWK, wk = cw - rg * NWK;
   const int g = lane >> 2, t = lane & 3;
   const int u0 = wk * KU;  // first unit of this warp's K-slice
 
   // ---- X for this warp's K-slice: lane's 32 elements per unit
-  uint32_t xb[KU][16];  // raw bf16 pairs, then f16 pairs
+  uint32_t xb[KU][16];
   uint32_t mx = 0;
 #pragma unroll
   for (int j = 0; j < KU; ++j) {
@@ -234,6 +260,7 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
   const bool diag = (t == (g >> 1));
   const int dsel = g & 1;
 
+  int64_t blk_row0 = row_begin;  // first row of the current row block
   for (int64_t i = 0; i < n_st; ++i) {
     const int s = (int)(i % NS);
     // warp-uniform: mma.sync and the shuffles below need all 32 lanes
@@ -242,75 +269,100 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
     if (!ready) *abort_flag = 1;
     const int64_t r0 = row_begin + i * RS;
     const int rows_i = (int)min((int64_t)RS, row_end - r0);
+    const int rloc = (int)(r0 - blk_row0);  // stage offset within the row block
     const uint8_t *st_codes = stages + (size_t)s * a.stage_bytes;
     const uint8_t *st_scales = st_codes + a.codes_stage_bytes;
-    float *red_s = red + (size_t)s * RS * NWK;
+    const uint8_t *g_scales = a.scales + r0 * KB;
+    const int n_pairs = ready ? (rows_i + 1) / 2 : 0;
 
-    for (int p = ready ? rg : RS; 2 * p < rows_i; p += RG) {
-      const int ra = 2 * p, rb = 2 * p + 1;
-      const bool has_b = rb < rows_i;
-      float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int p = rg; p < n_pairs; p += 2 * RG) {
+      const bool two = p + RG < n_pairs;
+      float v[4];
+      if (two) {
+        const int ra[2] = {2 * p, 2 * (p + RG)};
+        const bool hb[2] = {2 * p + 1 < rows_i, 2 * (p + RG) + 1 < rows_i};
+        float d[2][2][4] = {};
 #pragma unroll
-      for (int j = 0; j < KU; ++j) {
-        const int u = u0 + j;
-        if (u < n_units) {  // warp-uniform; lanes past K feed zeros to the mma
-          const int64_t kb = (int64_t)u * (kUnitK / 16) + 2 * lane;  // lane's first block
-          uint4 cw0 = make_uint4(0, 0, 0, 0), cw1 = make_uint4(0, 0, 0, 0);
-          uint32_t sc0 = 0, sc1 = 0;
-          if (kb < KB) {
-            cw0 = *reinterpret_cast<const uint4 *>(st_codes + ra * KH + kb * 8);
-            if (has_b) cw1 = *reinterpret_cast<const uint4 *>(st_codes + rb * KH + kb * 8);
-            if (a.scales_bulk) {
-              sc0 = *reinterpret_cast<const uint16_t *>(st_scales + ra * KB + kb);
-              if (has_b) sc1 = *reinterpret_cast<const uint16_t *>(st_scales + rb * KB + kb);
-            } else {
-              sc0 = __ldg(reinterpret_cast<const uint16_t *>(a.scales + (r0 + ra) * KB + kb));
-              if (has_b)
-                sc1 = __ldg(reinterpret_cast<const uint16_t *>(a.scales + (r0 + rb) * KB + kb));
-            }
+        for (int j = 0; j < KU; ++j) {
+          const int u = u0 + j;
+          if (u < n_units) {
+            const int64_t kb = (int64_t)u * (kUnitK / 16) + 2 * lane;
+            pairs_unit<2>(d, st_codes, st_scales, g_scales, ra, hb, KH, KB, kb, kb < KB,
+                          a.scales_bulk, xb[j]);
           }
-          unit_mma(d, d2, cw0, cw1, sc0, sc1, xb[j]);
         }
-      }
-      // D[g][g] (row ra) and D[g+8][g] (row rb) live in lane (g, g/2).
-      float v0 = diag ? d[dsel] + d2[dsel] : 0.0f;
-      float v1 = diag ? d[2 + dsel] + d2[2 + dsel] : 0.0f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, o);
-        v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, o);
+        for (int q = 0; q < 2; ++q) {
+          // register selects, not a runtime array index (which would put d on the stack)
+          const float lo = dsel ? d[q][0][1] + d[q][1][1] : d[q][0][0] + d[q][1][0];
+          const float hi = dsel ? d[q][0][3] + d[q][1][3] : d[q][0][2] + d[q][1][2];
+          v[2 * q] = diag ? lo : 0.0f;
+          v[2 * q + 1] = diag ? hi : 0.0f;
+        }
+      } else {
+        const int ra[1] = {2 * p};
+        const bool hb[1] = {2 * p + 1 < rows_i};
+        float d[1][2][4] = {};
+#pragma unroll
+        for (int j = 0; j < KU; ++j) {
+          const int u = u0 + j;
+          if (u < n_units) {
+            const int64_t kb = (int64_t)u * (kUnitK / 16) + 2 * lane;
+            pairs_unit<1>(d, st_codes, st_scales, g_scales, ra, hb, KH, KB, kb, kb < KB,
+                          a.scales_bulk, xb[j]);
+          }
+        }
+        const float lo = dsel ? d[0][0][1] + d[0][1][1] : d[0][0][0] + d[0][1][0];
+        const float hi = dsel ? d[0][0][3] + d[0][1][3] : d[0][0][2] + d[0][1][2];
+        v[0] = diag ? lo : 0.0f;
+        v[1] = diag ? hi : 0.0f;
+        v[2] = v[3] = 0.0f;
       }
+      // D[g][g] (row 2p) and D[g+8][g] (row 2p+1) live in lane (g, g/2).
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] += __shfl_xor_sync(0xFFFFFFFFu, v[q], o);
       if (lane == 0) {
-        red_s[ra * NWK + wk] = v0;
-        if (has_b) red_s[rb * NWK + wk] = v1;
+        const int rr[4] = {2 * p, 2 * p + 1, 2 * (p + RG), 2 * (p + RG) + 1};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (rr[q] < rows_i && (q < 2 || two)) red[(rloc + rr[q]) * NWK + wk] = v[q];
       }
-    }
-    named_bar(1, n_cw * 32);
-    if (*abort_flag) return;
-    for (int r = (threadIdx.x - kProducer); r < rows_i; r += n_cw * 32) {
-      float v = 0.0f;
-      for (int w = 0; w < NWK; ++w) v += red_s[r * NWK + w];
-      v = (v * x_unscale) * out_scale;
-      a.y[r0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+
+    // End of a row block (or of the CTA's rows): fixed-order sums -> Y.
+    const int64_t blk_end = min(blk_row0 + RB, row_end);
+    if (r0 + rows_i >= blk_end || i + 1 == n_st) {
+      named_bar(1, n_cw * 32);
+      if (*abort_flag) return;
+      const int nr = (int)(r0 + rows_i - blk_row0);
+      for (int r = ct; r < nr; r += n_cw * 32) {
+        float acc = 0.0f;
+        for (int w = 0; w < NWK; ++w) acc += red[r * NWK + w];
+        acc = (acc * x_unscale) * out_scale;
+        a.y[blk_row0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+      }
+      named_bar(1, n_cw * 32);
+      blk_row0 = r0 + rows_i;
+    }
   }
 }
 
 struct M1Plan {
-  int KU, NWK, RG, RS, NS, threads, scales_bulk;
+  int KU, NWK, RG, RS, RB, NS, threads, scales_bulk;
   uint32_t stage_bytes, codes_stage_bytes;
   size_t smem;
 };
 
 bool make_m1_plan(int64_t N, int64_t K, M1Plan &p) {
   const int n_units = (int)ceil_div(K, kUnitK);
-  // Fewest units per warp that keeps warps per row within the instantiation's
-  // limit (X registers: 16 per unit).
-  int KU = (int)ceil_div(n_units, 12);
+  // Fewest units per warp whose warps-per-row fit the instantiation (X
+  // registers: 16 per unit).
+  int KU = 1;
   while (KU <= 4 && ceil_div(n_units, KU) > max_consumer_warps(KU)) ++KU;
-  if (KU < 1) KU = 1;
   if (KU > 4) return false;
   p.KU = KU;
   p.NWK = (int)ceil_div(n_units, KU);
@@ -318,24 +370,29 @@ bool make_m1_plan(int64_t N, int64_t K, M1Plan &p) {
   if (RG < 1) RG = 1;
   p.RG = RG;
   p.threads = kProducer + 32 * p.NWK * p.RG;
-  if (p.NWK * p.RG > max_consumer_warps(KU)) return false;
   p.scales_bulk = (K % 256 == 0) ? 1 : 0;
   const int64_t row_bytes = K / 2 + (p.scales_bulk ? K / 16 : 0);
-  // Each row group takes one row pair per stage at least.
+  // Each row group takes two row pairs per stage when they fit in ~40 KB.
   int64_t RS = 2 * p.RG;
-  while (RS * 2 * row_bytes <= 40 * 1024 && RS < 64) RS *= 2;
+  while (RS * 2 * row_bytes <= 40 * 1024 && RS < 128) RS *= 2;
   const int64_t rows_per_cta = ceil_div(N, num_sms());
   const int64_t cap = 2 * ceil_div(rows_per_cta, 2);
   if (RS > cap) RS = cap < 2 ? 2 : cap;
   p.RS = (int)RS;
+  // Row block: the rows whose partial sums wait in shared memory (<= 24 KB).
+  int64_t RB = (24 * 1024 / 4) / p.NWK;
+  RB = (RB / RS) * RS;
+  if (RB < RS) RB = RS;
+  if (RB > ceil_div(rows_per_cta, RS) * RS) RB = ceil_div(rows_per_cta, RS) * RS;
+  p.RB = (int)RB;
   p.codes_stage_bytes = (uint32_t)(ceil_div(RS * (K / 2), 128) * 128);
   const uint32_t sbytes = p.scales_bulk ? (uint32_t)(ceil_div(RS * (K / 16), 128) * 128) : 0u;
   p.stage_bytes = p.codes_stage_bytes + sbytes;
-  int NS = kMaxStages;
   auto total = [&](int ns) {
-    const size_t red = (size_t)ns * p.RS * p.NWK * sizeof(float) + 32 * sizeof(float);
+    const size_t red = ((size_t)p.RB * p.NWK + 32) * sizeof(float);
     return kHeadBytes + ceil_div(red, 128) * 128 + (size_t)ns * p.stage_bytes;
   };
+  int NS = kMaxStages;
   while (NS > 2 && total(NS) > kSmemBudget) --NS;
   p.NS = NS;
   p.smem = total(NS);
@@ -377,6 +434,7 @@ cudaError_t launch_gemv_m1(const uint16_t *x, int64_t K, const uint8_t *codes,
   a.nstages = p.NS;
   a.warps_per_row = p.NWK;
   a.row_groups = p.RG;
+  a.rows_per_block = p.RB;
   a.scales_bulk = p.scales_bulk;
   a.stage_bytes = p.stage_bytes;
   a.codes_stage_bytes = p.codes_stage_bytes;
