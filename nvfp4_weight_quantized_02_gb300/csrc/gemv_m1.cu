@@ -67,17 +67,8 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %1, %2;" : "=r"(d) : "r"(a), "r"(sel));
-  return d;
-}
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2 *>(&v); }
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -93,31 +84,32 @@ __device__ __forceinline__ uint32_t f16x2_pack(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// One unit: rows (r0, r1) of the stage, 1024 k starting at unit*1024.
-// cw0/cw1: the lane's 16 code bytes of each row; sc0/sc1: its two scale
-// bytes of each row; xr: the lane's 32 X values as 16 f16x2.
-__device__ __forceinline__ void unit_mma(float (&d)[4], float (&e)[4], const uint4 cw0, const uint4 cw1,
-                                         uint32_t sc0, uint32_t sc1, const uint32_t (&xr)[16]) {
-  const uint32_t s0 = e4m3x2_to_f16x2(sc0);  // (block 2L, block 2L+1) of row n
-  const uint32_t s1 = e4m3x2_to_f16x2(sc1);  // same blocks of row n+1
+// One unit: rows (n, n+1), 1024 k.  cw0/cw1: the lane's 16 code bytes of
+// each row; sc0/sc1: its two scale bytes of each row; xr: the lane's 32 X
+// values as 16 f16x2.  d and e are two independent accumulator chains.
+__device__ __forceinline__ void unit_mma(float (&d)[4], float (&e)[4], const uint4 cw0,
+                                         const uint4 cw1, uint32_t sc0, uint32_t sc1,
+                                         const uint32_t (&xr)[16]) {
+  const __half2 s0 = u32_as_h2(e4m3x2_to_f16x2(sc0));  // (block 2L, block 2L+1) of row n
+  const __half2 s1 = u32_as_h2(e4m3x2_to_f16x2(sc1));  // same blocks of row n+1
   const uint32_t w0[4] = {cw0.x, cw0.y, cw0.z, cw0.w};
   const uint32_t w1[4] = {cw1.x, cw1.y, cw1.z, cw1.w};
 #pragma unroll
   for (int blk = 0; blk < 2; ++blk) {
-    const uint32_t sa = prmt(s0, blk ? 0x3232u : 0x1010u);  // this block's scale in both halves
-    const uint32_t sb = prmt(s1, blk ? 0x3232u : 0x1010u);
+    const __half2 sa = blk ? __high2half2(s0) : __low2half2(s0);  // block scale, both halves
+    const __half2 sb = blk ? __high2half2(s1) : __low2half2(s1);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      // 4 bytes = 8 elements = two mma steps
-      uint32_t h0[4], h1[4];
+      uint32_t h0[4], h1[4];  // 4 bytes = 8 elements = two mma steps
       e2m1x8_to_f16x2x4(w0[2 * blk + half], h0);
       e2m1x8_to_f16x2x4(w1[2 * blk + half], h1);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const int ei = 8 * blk + 4 * half + 2 * q;  // f16x2 index of elements 4s'..4s'+1
-        // two independent accumulator chains (steps alternate)
-        mma16816(q ? e : d, hmul2(h0[2 * q], sa), hmul2(h1[2 * q], sb), hmul2(h0[2 * q + 1], sa),
-                 hmul2(h1[2 * q + 1], sb), xr[ei], xr[ei + 1]);
+        mma16816(q ? e : d, h2_as_u32(__hmul2(u32_as_h2(h0[2 * q]), sa)),
+                 h2_as_u32(__hmul2(u32_as_h2(h1[2 * q]), sb)),
+                 h2_as_u32(__hmul2(u32_as_h2(h0[2 * q + 1]), sa)),
+                 h2_as_u32(__hmul2(u32_as_h2(h1[2 * q + 1]), sb)), xr[ei], xr[ei + 1]);
       }
     }
   }
@@ -128,29 +120,41 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], float (&e)[4], const uin
 __host__ __device__ constexpr int max_consumer_warps(int ku) { return ku <= 1 ? 16 : ku == 2 ? 12 : 8; }
 
 // Partial dot products of one unit for NP row pairs (NP independent
-// accumulator pairs, so the tensor-core chains overlap).
-template <int NP>
+// accumulator pairs, so the tensor-core chains overlap).  Both rows of a pair
+// are always read: the stage buffer holds RS (even) rows, so the second row
+// of a short last pair is stale data whose result is discarded.
+// FULL: every lane's blocks lie inside K (K % 1024 == 0).  SB: scales are in
+// the stage (bulk-copied) rather than read from global memory.
+template <int NP, bool FULL, bool SB>
 __device__ __forceinline__ void pairs_unit(float (&d)[NP][2][4], const uint8_t *st_codes,
                                            const uint8_t *st_scales, const uint8_t *g_scales,
-                                           const int (&ra)[NP], const bool (&has_b)[NP],
-                                           int64_t KH, int64_t KB, int64_t kb, bool lane_in,
-                                           bool scales_bulk, const uint32_t (&xr)[16]) {
+                                           const int (&ra)[NP], int rows_i, int64_t KH,
+                                           int64_t KB, int64_t kb, const uint32_t (&xr)[16]) {
+  const bool lane_in = FULL || kb < KB;
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     uint4 cw0 = make_uint4(0, 0, 0, 0), cw1 = make_uint4(0, 0, 0, 0);
     uint32_t sc0 = 0, sc1 = 0;
     if (lane_in) {
-      cw0 = *reinterpret_cast<const uint4 *>(st_codes + ra[p] * KH + kb * 8);
-      if (has_b[p]) cw1 = *reinterpret_cast<const uint4 *>(st_codes + (ra[p] + 1) * KH + kb * 8);
-      const uint8_t *sbase = scales_bulk ? st_scales : g_scales;
-      sc0 = *reinterpret_cast<const uint16_t *>(sbase + ra[p] * KB + kb);
-      if (has_b[p]) sc1 = *reinterpret_cast<const uint16_t *>(sbase + (ra[p] + 1) * KB + kb);
+      const uint8_t *c = st_codes + ra[p] * KH + kb * 8;
+      cw0 = *reinterpret_cast<const uint4 *>(c);
+      cw1 = *reinterpret_cast<const uint4 *>(c + KH);
+      if (SB) {
+        const uint8_t *sp = st_scales + ra[p] * KB + kb;
+        sc0 = *reinterpret_cast<const uint16_t *>(sp);
+        sc1 = *reinterpret_cast<const uint16_t *>(sp + KB);
+      } else {
+        // global memory: never read past the stage's last row (the array may end there)
+        const int rb = ra[p] + 1 < rows_i ? ra[p] + 1 : ra[p];
+        sc0 = __ldg(reinterpret_cast<const uint16_t *>(g_scales + ra[p] * KB + kb));
+        sc1 = __ldg(reinterpret_cast<const uint16_t *>(g_scales + rb * KB + kb));
+      }
     }
     unit_mma(d[p][0], d[p][1], cw0, cw1, sc0, sc1, xr);
   }
 }
 
-template <int KU>
+template <int KU, bool FULL, bool SB>
 __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
     gemv_m1_kernel(const M1Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -280,15 +284,14 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
       float v[4];
       if (two) {
         const int ra[2] = {2 * p, 2 * (p + RG)};
-        const bool hb[2] = {2 * p + 1 < rows_i, 2 * (p + RG) + 1 < rows_i};
         float d[2][2][4] = {};
 #pragma unroll
         for (int j = 0; j < KU; ++j) {
           const int u = u0 + j;
           if (u < n_units) {
             const int64_t kb = (int64_t)u * (kUnitK / 16) + 2 * lane;
-            pairs_unit<2>(d, st_codes, st_scales, g_scales, ra, hb, KH, KB, kb, kb < KB,
-                          a.scales_bulk, xb[j]);
+            pairs_unit<2, FULL, SB>(d, st_codes, st_scales, g_scales, ra, rows_i, KH, KB, kb,
+                                    xb[j]);
           }
         }
 #pragma unroll
@@ -301,15 +304,14 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
         }
       } else {
         const int ra[1] = {2 * p};
-        const bool hb[1] = {2 * p + 1 < rows_i};
         float d[1][2][4] = {};
 #pragma unroll
         for (int j = 0; j < KU; ++j) {
           const int u = u0 + j;
           if (u < n_units) {
             const int64_t kb = (int64_t)u * (kUnitK / 16) + 2 * lane;
-            pairs_unit<1>(d, st_codes, st_scales, g_scales, ra, hb, KH, KB, kb, kb < KB,
-                          a.scales_bulk, xb[j]);
+            pairs_unit<1, FULL, SB>(d, st_codes, st_scales, g_scales, ra, rows_i, KH, KB, kb,
+                                    xb[j]);
           }
         }
         const float lo = dsel ? d[0][0][1] + d[0][1][1] : d[0][0][0] + d[0][1][0];
@@ -399,9 +401,9 @@ bool make_m1_plan(int64_t N, int64_t K, M1Plan &p) {
   return p.smem <= 227 * 1024;
 }
 
-template <int KU>
+template <int KU, bool FULL, bool SB>
 cudaError_t launch_m1(const M1Args &a, const M1Plan &p, int grid, cudaStream_t stream) {
-  auto kern = gemv_m1_kernel<KU>;
+  auto kern = gemv_m1_kernel<KU, FULL, SB>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
@@ -440,12 +442,19 @@ cudaError_t launch_gemv_m1(const uint16_t *x, int64_t K, const uint8_t *codes,
   a.codes_stage_bytes = p.codes_stage_bytes;
   int64_t grid = num_sms();
   if (grid > N) grid = N;
+  const bool full = (K % kUnitK) == 0;
+#define IMPFP4_KU(ku)                                                               \
+  case ku:                                                                          \
+    if (full && p.scales_bulk) return launch_m1<ku, true, true>(a, p, (int)grid, stream); \
+    if (p.scales_bulk) return launch_m1<ku, false, true>(a, p, (int)grid, stream);  \
+    return launch_m1<ku, false, false>(a, p, (int)grid, stream);
   switch (p.KU) {
-    case 1: return launch_m1<1>(a, p, (int)grid, stream);
-    case 2: return launch_m1<2>(a, p, (int)grid, stream);
-    case 3: return launch_m1<3>(a, p, (int)grid, stream);
-    case 4: return launch_m1<4>(a, p, (int)grid, stream);
+    IMPFP4_KU(1)
+    IMPFP4_KU(2)
+    IMPFP4_KU(3)
+    IMPFP4_KU(4)
   }
+#undef IMPFP4_KU
   return cudaErrorInvalidConfiguration;
 }
 
