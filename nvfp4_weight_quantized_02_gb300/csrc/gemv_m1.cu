@@ -117,7 +117,7 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], float (&e)[4], const uin
 
 // Consumer warps per CTA an instantiation is compiled for: X takes 16
 // registers per unit, so wider K-slices get fewer warps.
-__host__ __device__ constexpr int max_consumer_warps(int ku) { return ku <= 1 ? 16 : ku == 2 ? 12 : 8; }
+__host__ __device__ constexpr int max_consumer_warps(int ku) { return ku <= 1 ? 20 : ku == 2 ? 12 : 8; }
 
 // Partial dot products of one unit for NP row pairs (NP independent
 // accumulator pairs, so the tensor-core chains overlap).  Both rows of a pair
@@ -261,7 +261,6 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
                             ldexpf(bf16_bits_to_f32(xb[j][i] >> 16), sh));
   const float out_scale = *a.tensor_scale;
   const float x_unscale = ldexpf(1.0f, -sh);
-  const bool diag = (t == (g >> 1));
   const int dsel = g & 1;
 
   int64_t blk_row0 = row_begin;  // first row of the current row block
@@ -297,10 +296,8 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           // register selects, not a runtime array index (which would put d on the stack)
-          const float lo = dsel ? d[q][0][1] + d[q][1][1] : d[q][0][0] + d[q][1][0];
-          const float hi = dsel ? d[q][0][3] + d[q][1][3] : d[q][0][2] + d[q][1][2];
-          v[2 * q] = diag ? lo : 0.0f;
-          v[2 * q + 1] = diag ? hi : 0.0f;
+          v[2 * q] = dsel ? d[q][0][1] + d[q][1][1] : d[q][0][0] + d[q][1][0];
+          v[2 * q + 1] = dsel ? d[q][0][3] + d[q][1][3] : d[q][0][2] + d[q][1][2];
         }
       } else {
         const int ra[1] = {2 * p};
@@ -314,17 +311,20 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
                                     xb[j]);
           }
         }
-        const float lo = dsel ? d[0][0][1] + d[0][1][1] : d[0][0][0] + d[0][1][0];
-        const float hi = dsel ? d[0][0][3] + d[0][1][3] : d[0][0][2] + d[0][1][2];
-        v[0] = diag ? lo : 0.0f;
-        v[1] = diag ? hi : 0.0f;
+        v[0] = dsel ? d[0][0][1] + d[0][1][1] : d[0][0][0] + d[0][1][0];
+        v[1] = dsel ? d[0][0][3] + d[0][1][3] : d[0][0][2] + d[0][1][2];
         v[2] = v[3] = 0.0f;
       }
-      // D[g][g] (row 2p) and D[g+8][g] (row 2p+1) live in lane (g, g/2).
+      // D[g][g] (row 2p) and D[g+8][g] (row 2p+1) live in lane 4g + g/2, i.e.
+      // lanes 9j (g = 2j) and 9j + 4 (g = 2j + 1).  XOR 4, then 9, then 18
+      // gathers exactly those eight lanes into lane 0 (other lanes' sums are
+      // never read).
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] += __shfl_xor_sync(0xFFFFFFFFu, v[q], o);
+      for (int q = 0; q < 4; ++q) {
+        v[q] += __shfl_xor_sync(0xFFFFFFFFu, v[q], 4);
+        v[q] += __shfl_xor_sync(0xFFFFFFFFu, v[q], 9);
+        v[q] += __shfl_xor_sync(0xFFFFFFFFu, v[q], 18);
+      }
       if (lane == 0) {
         const int rr[4] = {2 * p, 2 * p + 1, 2 * (p + RG), 2 * (p + RG) + 1};
 #pragma unroll
