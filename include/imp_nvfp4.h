@@ -104,7 +104,7 @@ imp_status imp_nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64
                               void *workspace, size_t ws_bytes, void *stream);
 
 /* Bytes of workspace imp_nvfp4_gemm needs for Y[M][N] = X[M][K] W^T (0 for
- * M <= 16; the quantized X and its scales for M > 16). */
+ * M <= 16; for M > 16 the quantized X, X's and W's atom-layout scales). */
 size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /* Y = X * W^T.
@@ -122,6 +122,41 @@ size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                           const imp_nvfp4_tensor *w, void *y_bf16, int64_t ldy,
                           int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream);
+
+/* ---- tensor-core operand layout (prefill path) -----------------------------
+ * The block-scaled FP4 MMA reads block scales as 512-byte atoms: one atom
+ * holds the scales of 128 rows x 4 blocks (64 elements of K); row r of the
+ * atom sits at byte 16*(r % 32) + 4*((r / 32) % 4), block j of it at + j.
+ * Atoms of a 128-row block follow each other along K; row blocks follow each
+ * other; rows are padded to a multiple of 256.  Codes keep the row-major
+ * [rows][K/2] layout.  This is a one-time transform for weights (like an
+ * engine's cache of transformed weights).                                   */
+
+/* Bytes of atom-layout scales for a rows x K tensor (K % 64 == 0). */
+size_t imp_nvfp4_mma_scales_size(int64_t rows, int64_t K);
+
+/* Copy the row-major block scales of `t` into the atom layout.
+ *   t           NVFP4 tensor (row-major scales), rows >= 1, K % 64 == 0.
+ *   mma_scales  device buffer of >= imp_nvfp4_mma_scales_size(rows, K) bytes,
+ *               16-byte aligned; padding rows are written as 0.           */
+imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_scales, size_t bytes,
+                                 void *stream);
+
+/* Quantize like imp_nvfp4_quantize (bit-identical codes, scale bytes and
+ * tensor scale) but write the scales in the atom layout: out->scales must
+ * hold imp_nvfp4_mma_scales_size(rows, K) bytes.  K % 64 == 0.            */
+imp_status imp_nvfp4_quantize_mma(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                                  const imp_nvfp4_tensor *out, int32_t *dev_status,
+                                  void *workspace, size_t ws_bytes, void *stream);
+
+/* Y = Xq * Wq^T with both operands NVFP4 and their scales in the atom
+ * layout: the block-scaled FP4 tensor-core GEMM alone (tcgen05.mma
+ * kind::mxf4nvf4, fp32 accumulation in tensor memory), times
+ * s_x * s_w, rounded to bf16.
+ *   xq  M rows (M >= 1), K % 64 == 0;  wq  N rows, wq->K == K.
+ *   y   bf16[M][ldy], ldy >= N, ldy % 8 == 0.                             */
+imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor *wq,
+                              void *y_bf16, int64_t ldy, int32_t *dev_status, void *stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *imp_status_string(imp_status status);

@@ -24,7 +24,9 @@ __all__ = [
     "IMP_OK", "IMP_DEV_OK", "IMP_DEV_NONFINITE_INPUT", "IMP_DEV_TIMEOUT", "ImpNvfp4Tensor",
     "imp_nvfp4_quantize", "imp_nvfp4_gemm", "imp_nvfp4_quantize_workspace_size",
     "imp_nvfp4_gemm_workspace_size", "imp_status_string", "NVFP4Tensor", "quantize", "gemm",
-    "library_path", "header_functions", "ImpError", "load",
+    "library_path", "header_functions", "ImpError", "load", "imp_nvfp4_mma_scales_size",
+    "imp_nvfp4_prepare_mma", "imp_nvfp4_quantize_mma", "imp_nvfp4_gemm_fp4", "prepare_mma",
+    "quantize_mma", "gemm_fp4",
 ]
 
 IMP_OK = 0
@@ -68,6 +70,15 @@ def _L():
                                    SZ, P]
     lib.imp_status_string.restype = ctypes.c_char_p
     lib.imp_status_string.argtypes = [ctypes.c_int]
+    T = ctypes.POINTER(ImpNvfp4Tensor)
+    lib.imp_nvfp4_mma_scales_size.restype = SZ
+    lib.imp_nvfp4_mma_scales_size.argtypes = [I64, I64]
+    lib.imp_nvfp4_prepare_mma.restype = ctypes.c_int
+    lib.imp_nvfp4_prepare_mma.argtypes = [T, P, SZ, P]
+    lib.imp_nvfp4_quantize_mma.restype = ctypes.c_int
+    lib.imp_nvfp4_quantize_mma.argtypes = [P, I64, I64, I64, T, P, P, SZ, P]
+    lib.imp_nvfp4_gemm_fp4.restype = ctypes.c_int
+    lib.imp_nvfp4_gemm_fp4.argtypes = [T, T, P, I64, P, P]
     _lib = lib
     return lib
 
@@ -112,6 +123,28 @@ def imp_nvfp4_gemm(x_bf16: int, M: int, K: int, ldx: int, w: ImpNvfp4Tensor, y_b
                    stream: int | None) -> int:
     return _L().imp_nvfp4_gemm(x_bf16, M, K, ldx, ctypes.byref(w), y_bf16, ldy, dev_status,
                                workspace, ws_bytes, stream)
+
+
+def imp_nvfp4_mma_scales_size(rows: int, K: int) -> int:
+    return _L().imp_nvfp4_mma_scales_size(rows, K)
+
+
+def imp_nvfp4_prepare_mma(t: ImpNvfp4Tensor, mma_scales: int, nbytes: int,
+                          stream: int | None) -> int:
+    return _L().imp_nvfp4_prepare_mma(ctypes.byref(t), mma_scales, nbytes, stream)
+
+
+def imp_nvfp4_quantize_mma(x_bf16: int, rows: int, K: int, ldx: int, out: ImpNvfp4Tensor,
+                           dev_status: int | None, workspace: int | None, ws_bytes: int,
+                           stream: int | None) -> int:
+    return _L().imp_nvfp4_quantize_mma(x_bf16, rows, K, ldx, ctypes.byref(out), dev_status,
+                                       workspace, ws_bytes, stream)
+
+
+def imp_nvfp4_gemm_fp4(xq: ImpNvfp4Tensor, wq: ImpNvfp4Tensor, y_bf16: int, ldy: int,
+                       dev_status: int | None, stream: int | None) -> int:
+    return _L().imp_nvfp4_gemm_fp4(ctypes.byref(xq), ctypes.byref(wq), y_bf16, ldy, dev_status,
+                                   stream)
 
 
 class ImpError(RuntimeError):
@@ -191,4 +224,53 @@ def gemm(x, w: NVFP4Tensor, y=None, dev_status=None, stream=None, workspace=None
                         _stream_handle(stream))
     if st != IMP_OK:
         raise ImpError(st, "imp_nvfp4_gemm")
+    return y
+
+
+def prepare_mma(w: NVFP4Tensor, stream=None) -> NVFP4Tensor:
+    """The same tensor with its block scales laid out as tensor-core atoms."""
+    import torch
+    nbytes = imp_nvfp4_mma_scales_size(w.rows, w.K)
+    sc = torch.empty(nbytes, dtype=torch.uint8, device=w.codes.device)
+    st = imp_nvfp4_prepare_mma(w.c_struct(), sc.data_ptr(), nbytes, _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_prepare_mma")
+    return NVFP4Tensor(w.codes, sc, w.tensor_scale)
+
+
+def _struct(t: NVFP4Tensor) -> ImpNvfp4Tensor:
+    return ImpNvfp4Tensor(t.codes.data_ptr(), t.scales.data_ptr(), t.tensor_scale.data_ptr(),
+                          t.codes.shape[0], t.codes.shape[1] * 2)
+
+
+def quantize_mma(x, dev_status=None, stream=None) -> NVFP4Tensor:
+    """Quantize a bf16 CUDA matrix with its scales in the tensor-core atom layout."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, K = x.shape
+    out = NVFP4Tensor(torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device),
+                      torch.empty(imp_nvfp4_mma_scales_size(rows, K), dtype=torch.uint8,
+                                  device=x.device),
+                      torch.empty(1, dtype=torch.float32, device=x.device))
+    ws_bytes = imp_nvfp4_quantize_workspace_size(rows, K)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    st = imp_nvfp4_quantize_mma(x.data_ptr(), rows, K, x.stride(0), _struct(out),
+                                None if dev_status is None else dev_status.data_ptr(),
+                                ws.data_ptr(), ws_bytes, _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_quantize_mma")
+    return out
+
+
+def gemm_fp4(xq: NVFP4Tensor, wq: NVFP4Tensor, y=None, dev_status=None, stream=None):
+    """Y = Xq Wq^T on the block-scaled FP4 tensor cores (atom-layout scales)."""
+    import torch
+    M, N = xq.codes.shape[0], wq.codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.codes.device)
+    st = imp_nvfp4_gemm_fp4(_struct(xq), _struct(wq), y.data_ptr(), y.stride(0),
+                            None if dev_status is None else dev_status.data_ptr(),
+                            _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_gemm_fp4")
     return y

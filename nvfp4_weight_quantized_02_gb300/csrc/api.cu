@@ -1,5 +1,6 @@
 // The C ABI of imp_nvfp4.h: argument validation, workspace sizing and
 // dispatch to the quantizer, the decode path (M <= 16) and the prefill path.
+#include "gemm_tcgen05.cuh"
 #include "gemv.cuh"
 #include "quantize.cuh"
 
@@ -19,6 +20,24 @@ imp_status check_tensor(const imp_nvfp4_tensor *t, int64_t rows, int64_t K) {
 }
 
 imp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? IMP_OK : IMP_ERR_CUDA; }
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace of the prefill path: amax partials | X codes | X atom scales |
+// W atom scales | s_x.
+struct PrefillWs {
+  size_t partial, xcodes, xsc, wsc, sx, total;
+};
+PrefillWs prefill_ws(int64_t M, int64_t N, int64_t K) {
+  PrefillWs w;
+  w.partial = 0;
+  w.xcodes = align256(impfp4::quantize_workspace_bytes(M, K));
+  w.xsc = align256(w.xcodes + (size_t)M * (size_t)(K / 2));
+  w.wsc = align256(w.xsc + impfp4::mma_scale_bytes(M, K));
+  w.sx = align256(w.wsc + impfp4::mma_scale_bytes(N, K));
+  w.total = w.sx + 256;
+  return w;
+}
 
 }  // namespace
 
@@ -68,9 +87,64 @@ imp_status imp_nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64
 }
 
 size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 64) return 0;
   if (M <= kDecodeMaxM) return 0;
-  return 0;
+  return prefill_ws(M, N, K).total;
+}
+
+size_t imp_nvfp4_mma_scales_size(int64_t rows, int64_t K) {
+  if (rows <= 0 || K <= 0 || K % 64) return 0;
+  return impfp4::mma_scale_bytes(rows, K);
+}
+
+imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_scales, size_t bytes,
+                                 void *stream) {
+  if (!t || !mma_scales || t->rows < 1) return IMP_ERR_INVALID_ARG;
+  if (t->K <= 0 || t->K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  imp_status st = check_tensor(t, t->rows, t->K);
+  if (st != IMP_OK) return st;
+  if (!aligned16(mma_scales)) return IMP_ERR_MISALIGNED;
+  if (bytes < impfp4::mma_scale_bytes(t->rows, t->K)) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(impfp4::launch_scale_relayout(t->scales, t->rows, t->K,
+                                                 static_cast<uint8_t *>(mma_scales),
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+imp_status imp_nvfp4_quantize_mma(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                                  const imp_nvfp4_tensor *out, int32_t *dev_status,
+                                  void *workspace, size_t ws_bytes, void *stream) {
+  if (rows < 1 || !x_bf16) return IMP_ERR_INVALID_ARG;
+  if (K <= 0 || K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K) return IMP_ERR_INVALID_ARG;
+  imp_status st = check_tensor(out, rows, K);
+  if (st != IMP_OK) return st;
+  if (!aligned16(x_bf16) || ldx % 8) return IMP_ERR_MISALIGNED;
+  const size_t need = impfp4::quantize_workspace_bytes(rows, K);
+  if (!workspace || ws_bytes < need) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  return from_cuda(impfp4::launch_quantize_mma(static_cast<const uint16_t *>(x_bf16), rows, K,
+                                               ldx, out->codes, out->scales, out->tensor_scale,
+                                               dev_status, workspace,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor *wq,
+                              void *y_bf16, int64_t ldy, int32_t *dev_status, void *stream) {
+  if (!xq || !wq || !y_bf16) return IMP_ERR_INVALID_ARG;
+  const int64_t M = xq->rows, N = wq->rows, K = xq->K;
+  if (M < 1 || N < 1 || wq->K != K) return IMP_ERR_INVALID_ARG;
+  if (K <= 0 || K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return IMP_ERR_UNSUPPORTED_SHAPE;
+  imp_status st = check_tensor(xq, M, K);
+  if (st != IMP_OK) return st;
+  st = check_tensor(wq, N, K);
+  if (st != IMP_OK) return st;
+  if (ldy < N) return IMP_ERR_INVALID_ARG;
+  if (!aligned16(y_bf16) || ldy % 8) return IMP_ERR_MISALIGNED;
+  return from_cuda(impfp4::launch_gemm_mxf4(xq->codes, xq->scales, xq->tensor_scale, wq->codes,
+                                            wq->scales, wq->tensor_scale, M, N, K,
+                                            static_cast<uint16_t *>(y_bf16), ldy, dev_status,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
@@ -95,7 +169,23 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                                          w->codes, w->scales, w->tensor_scale, N,
                                          static_cast<uint16_t *>(y_bf16), ldy, dev_status, s));
   }
-  return IMP_ERR_UNSUPPORTED_SHAPE;
+  // Prefill: quantize X (scales straight into the atom layout), lay W's
+  // scales out as atoms, then the block-scaled FP4 tensor-core GEMM.
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  const PrefillWs L = prefill_ws(M, N, K);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  imp_nvfp4_tensor xq = {ws + L.xcodes, ws + L.xsc, reinterpret_cast<float *>(ws + L.sx), M, K};
+  imp_nvfp4_tensor wq = {w->codes, ws + L.wsc, w->tensor_scale, N, K};
+  cudaError_t e = impfp4::launch_quantize_mma(static_cast<const uint16_t *>(x_bf16), M, K, ldx,
+                                              xq.codes, xq.scales, xq.tensor_scale, dev_status,
+                                              ws + L.partial, s);
+  if (e == cudaSuccess) e = impfp4::launch_scale_relayout(w->scales, N, K, wq.scales, s);
+  if (e == cudaSuccess)
+    e = impfp4::launch_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, wq.codes, wq.scales,
+                                 wq.tensor_scale, M, N, K, static_cast<uint16_t *>(y_bf16), ldy,
+                                 dev_status, s);
+  return from_cuda(e);
 }
 
 }  // extern "C"

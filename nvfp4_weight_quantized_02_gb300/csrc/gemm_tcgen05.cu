@@ -1,0 +1,372 @@
+// Prefill NVFP4 GEMM on the block-scaled FP4 tensor cores of sm_103a:
+//   Y[M][N] = s_x * s_w * sum_k (e2m1_x * e4m3_x)[m][k] * (e2m1_w * e4m3_w)[n][k]
+// with X already quantized to NVFP4 by the same recipe as W.  Prefill is the
+// compute-bound phase (imp README, "How it works"; "1. The big picture",
+// section "Two phases with very different costs"), so it runs on
+// tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X: FP4 x FP4 products
+// with one E4M3 scale per 16 elements of each operand, fp32 accumulation in
+// tensor memory.
+//
+// Structure (one CTA per SM, persistent over 128 x 256 output tiles):
+//  * warp 0, one thread: TMA producer.  Per K-stage of 256 elements it loads
+//    the X tile (128 rows x 128 bytes) and the W tile (256 rows x 128 bytes)
+//    with 2-D tensor copies in the 128-byte swizzle, and the matching block
+//    scales (already in the 512-byte atom layout, see quantize.cuh) with
+//    bulk copies, into a 4-deep shared-memory ring.
+//  * warp 1: allocates 512 tensor-memory columns; one thread issues, per
+//    64-element K step, three tcgen05.cp (scales of the X rows and of the two
+//    128-row halves of the W tile into tensor memory) and one tcgen05.mma
+//    (M = 128, N = 256, K = 64) accumulating into columns 0..255;
+//    tcgen05.commit releases each ring stage and, at the end of a tile,
+//    signals the epilogue.
+//  * warps 2..5: epilogue.  Each thread owns one accumulator row (its warp's
+//    32-lane quarter of tensor memory), reads it 32 columns at a time with
+//    tcgen05.ld, multiplies by s_x * s_w, rounds to bf16 and stores to Y.
+// Every wait is bounded; on a timeout the kernel reports IMP_DEV_TIMEOUT,
+// drains its own copies and MMAs, frees tensor memory and returns.
+#include "gemm_tcgen05.cuh"
+#include "quantize.cuh"
+#include "tma.cuh"
+
+namespace impfp4 {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 256;  // BK in elements (128 bytes of codes)
+constexpr int MMA_K = 64;
+constexpr int KSTEPS = BK / MMA_K;  // 4 MMAs per stage
+constexpr int NSTAGE = 4;
+constexpr uint32_t A_BYTES = BM * BK / 2;                    // 16 KB
+constexpr uint32_t B_BYTES = BN * BK / 2;                    // 32 KB
+constexpr uint32_t SFA_BYTES = (BM / 128) * KSTEPS * 512;    // 2 KB
+constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;    // 4 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr uint32_t OFF_B = A_BYTES, OFF_SFA = A_BYTES + B_BYTES, OFF_SFB = OFF_SFA + SFA_BYTES;
+constexpr int kThreads = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_D = 0;     // accumulator: columns 0..255
+constexpr uint32_t TMEM_SF = 256;  // scales: 12 columns per K step (X 4, W 8)
+constexpr size_t kBarBytes = 256;
+constexpr size_t kSmemBytes = 1024 + NSTAGE * (size_t)STAGE_BYTES + kBarBytes;
+
+struct GemmArgs {
+  const uint8_t *sfa;  // X block scales, atom layout
+  const uint8_t *sfb;  // W block scales, atom layout
+  const float *s_x, *s_w;
+  uint16_t *y;
+  int64_t ldy;
+  int M, N, K;
+  int32_t *status;
+};
+
+// ---- tcgen05 helpers (inline PTX) --------------------------------------------
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, layout type.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // version
+  d |= (uint64_t)(layout & 7u) << 61;
+  return d;
+}
+constexpr uint32_t kLayoutNone = 0, kLayoutSw128 = 2;
+
+// Instruction descriptor, kind::mxf4nvf4 with E4M3 block scales: A and B are
+// E2M1 (format 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%5], [%6], p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTAGE * STAGE_BYTES);
+  uint64_t *empty = full + NSTAGE;
+  uint64_t *accf = empty + NSTAGE;  // accumulator ready for the epilogue
+  uint64_t *acce = accf + 1;        // accumulator drained by the epilogue
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(acce + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int MB = (a.M + BM - 1) / BM, NB = (a.N + BN - 1) / BN;
+  const int n_tiles = MB * NB;
+  const int n_ks = (a.K + BK - 1) / BK;
+  const int KA = a.K / 64;  // scale atoms per 128-row block
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(const_cast<uint32_t *>(tmem_slot))),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer
+    if (lane == 0) {
+      int64_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        const int mb = t % MB, nb = t / MB;
+        for (int ks = 0; ks < n_ks; ++ks, ++it) {
+          const int s = (int)(it % NSTAGE);
+          if (it >= NSTAGE &&
+              !mbar_wait_bounded(&empty[s], (uint32_t)(((it / NSTAGE) - 1) & 1), a.status)) {
+            ok = false;
+            break;
+          }
+          if (*abort_flag) { ok = false; break; }
+          const int natoms = min(KSTEPS, KA - ks * KSTEPS);
+          uint8_t *st = smem + (size_t)s * STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES + 3u * natoms * 512u);
+          tma_load_2d(st, &tmA, ks * (BK / 2), mb * BM, &full[s]);
+          tma_load_2d(st + OFF_B, &tmB, ks * (BK / 2), nb * BN, &full[s]);
+          const int64_t atom0 = (int64_t)ks * KSTEPS;
+          bulk_g2s(st + OFF_SFA, a.sfa + ((int64_t)mb * KA + atom0) * 512, natoms * 512u,
+                   &full[s]);
+          bulk_g2s(st + OFF_SFB, a.sfb + ((int64_t)(2 * nb) * KA + atom0) * 512, natoms * 512u,
+                   &full[s]);
+          bulk_g2s(st + OFF_SFB + 2048, a.sfb + ((int64_t)(2 * nb + 1) * KA + atom0) * 512,
+                   natoms * 512u, &full[s]);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        // drain: the last NSTAGE issued stages must land before shared memory is released
+        for (int64_t i = (it > NSTAGE ? it - NSTAGE : 0); i < it; ++i)
+          mbar_wait_bounded(&full[i % NSTAGE], (uint32_t)((i / NSTAGE) & 1), a.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer
+    if (lane == 0) {
+      int64_t it = 0;
+      int tile_iter = 0;
+      bool ok = true;
+      bool committed_any = false;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tile_iter) {
+        if (tile_iter > 0 &&
+            !mbar_wait_bounded(acce, (uint32_t)((tile_iter - 1) & 1), a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ks = 0; ks < n_ks; ++ks, ++it) {
+          const int s = (int)(it % NSTAGE);
+          if (!mbar_wait_bounded(&full[s], (uint32_t)((it / NSTAGE) & 1), a.status) ||
+              *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t *st = smem + (size_t)s * STAGE_BYTES;
+          const uint32_t sA = smem_u32(st), sB = smem_u32(st + OFF_B);
+          const uint32_t sSFA = smem_u32(st + OFF_SFA), sSFB = smem_u32(st + OFF_SFB);
+          const int nk = min(KSTEPS, (a.K - ks * BK) / MMA_K);
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint32_t sf = tmem + TMEM_SF + 12u * kk;
+            tc_cp_sf(sf, smem_desc(sSFA + kk * 512, 0, 128, kLayoutNone));
+            tc_cp_sf(sf + 4, smem_desc(sSFB + kk * 512, 0, 128, kLayoutNone));
+            tc_cp_sf(sf + 8, smem_desc(sSFB + 2048 + kk * 512, 0, 128, kLayoutNone));
+            tc_mma(tmem + TMEM_D, smem_desc(sA + kk * 32, 16, 1024, kLayoutSw128),
+                   smem_desc(sB + kk * 32, 16, 1024, kLayoutSw128), kIdesc, sf, sf + 4,
+                   (ks | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);  // stage free once these MMAs complete
+          committed_any = true;
+        }
+        if (!ok) break;
+        tc_commit(accf);  // tile accumulated
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        // let every issued MMA finish before tensor memory is freed
+        if (committed_any) {
+          const int64_t last = it - 1;
+          mbar_wait_bounded(&empty[last % NSTAGE], (uint32_t)((last / NSTAGE) & 1), a.status);
+        }
+      }
+    }
+  } else {
+    // ------------------------------ epilogue: warps 2..5
+    const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
+    const int row_in_tile = quarter * 32 + lane;
+    const float scale = (*a.s_x) * (*a.s_w);
+    int tile_iter = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_iter) {
+      const bool ready =
+          __all_sync(0xFFFFFFFFu, mbar_wait_bounded(accf, (uint32_t)(tile_iter & 1), a.status));
+      if (!ready || *abort_flag) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int mb = t % MB, nb = t / MB;
+      const int64_t m = (int64_t)mb * BM + row_in_tile;
+      const int n0 = nb * BN;
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D + c, r);
+        if (c + 32 == BN) {
+          tc_fence_before();
+          mbar_arrive(acce);  // accumulator may be overwritten now
+        }
+        if (m < a.M) {
+          uint16_t *dst = a.y + m * a.ldy + n0 + c;
+          if (n0 + c + 32 <= a.N) {
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              p[i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
+                               __uint_as_float(r[2 * i + 1]) * scale);
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+          } else {
+            for (int i = 0; i < 32 && n0 + c + i < a.N; ++i)
+              dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * scale));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+bool make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t row_bytes,
+                     uint64_t pitch, uint32_t box_rows, uint32_t box_bytes, bool swizzle128) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {box_bytes, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+size_t gemm_mxf4_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales,
+                             const float *s_x, const uint8_t *w_codes,
+                             const uint8_t *w_mma_scales, const float *s_w, int64_t M,
+                             int64_t N, int64_t K, uint16_t *y, int64_t ldy, int32_t *status,
+                             cudaStream_t stream) {
+  CUtensorMap tmA, tmB;
+  if (!make_tmap_u8_2d(&tmA, x_codes, (uint64_t)M, (uint64_t)(K / 2), (uint64_t)(K / 2), BM, 128,
+                       true) ||
+      !make_tmap_u8_2d(&tmB, w_codes, (uint64_t)N, (uint64_t)(K / 2), (uint64_t)(K / 2), BN, 128,
+                       true))
+    return cudaErrorInvalidValue;
+  GemmArgs a;
+  a.sfa = x_mma_scales;
+  a.sfb = w_mma_scales;
+  a.s_x = s_x;
+  a.s_w = s_w;
+  a.y = y;
+  a.ldy = ldy;
+  a.M = (int)M;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.status = status;
+  const int64_t tiles = ceil_div(M, BM) * ceil_div(N, BN);
+  int64_t grid = num_sms();
+  if (grid > tiles) grid = tiles;
+  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  gemm_mxf4_kernel<<<(int)grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace impfp4

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
   const int ct = threadIdx.x - kProducer;
   const int lane = threadIdx.x & 31;
   const int rg = cw / NWK, wk = cw - rg * NWK;
-  const int g = lane >> 2, t = lane & 3;
+  const int g = lane >> 2;
   const int u0 = wk * KU;  // first unit of this warp's K-slice
 
   // ---- X for this warp's K-slice: lane's 32 elements per unit
@@ -374,8 +374,9 @@ bool make_m1_plan(int64_t N, int64_t K, M1Plan &p) {
   p.threads = kProducer + 32 * p.NWK * p.RG;
   p.scales_bulk = (K % 256 == 0) ? 1 : 0;
   const int64_t row_bytes = K / 2 + (p.scales_bulk ? K / 16 : 0);
-  // Each row group takes two row pairs per stage when they fit in ~40 KB.
-  int64_t RS = 2 * p.RG;
+  // Each row group takes two row pairs per stage (two independent
+  // accumulator sets per warp), more while a stage stays under ~40 KB.
+  int64_t RS = 4 * p.RG;
   while (RS * 2 * row_bytes <= 40 * 1024 && RS < 128) RS *= 2;
   const int64_t rows_per_cta = ceil_div(N, num_sms());
   const int64_t cap = 2 * ceil_div(rows_per_cta, 2);

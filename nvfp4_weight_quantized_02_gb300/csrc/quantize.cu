@@ -79,6 +79,9 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partial_kernel(const uint16
 }
 
 // Pass 2: fold the partial maxima, then encode one 16-element block per thread.
+// MMA_LAYOUT: write the scale bytes in the tensor-core atom layout
+// (mma_scale_offset) instead of row-major.
+template <bool MMA_LAYOUT>
 __global__ void __launch_bounds__(kEncThreads) encode_kernel(
     const uint16_t *__restrict__ x, int64_t rows, int64_t K, int64_t ldx,
     const uint32_t *__restrict__ partial, int num_partial, uint8_t *__restrict__ codes,
@@ -132,7 +135,10 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(
       }
     }
     *reinterpret_cast<uint2 *>(codes + r * (K / 2) + b * 8) = make_uint2(packed[0], packed[1]);
-    scales[r * blocks_per_row + b] = static_cast<uint8_t>(sb);
+    if (MMA_LAYOUT)
+      scales[mma_scale_offset(r, b, K)] = static_cast<uint8_t>(sb);
+    else
+      scales[r * blocks_per_row + b] = static_cast<uint8_t>(sb);
   }
 }
 
@@ -179,8 +185,55 @@ cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t 
   const int64_t cap = (int64_t)num_sms_cached() * 8;
   if (ge > cap) ge = cap;
   if (ge < 1) ge = 1;
-  encode_kernel<<<static_cast<int>(ge), kEncThreads, 0, stream>>>(x, rows, K, ldx, partial, ga,
-                                                                   codes, scales, tensor_scale);
+  encode_kernel<false><<<static_cast<int>(ge), kEncThreads, 0, stream>>>(
+      x, rows, K, ldx, partial, ga, codes, scales, tensor_scale);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// One thread per 4-byte word of the atom layout: word w of atom (rb, kc)
+// holds row rb*128 + 32*(w % 4) + w / 4, blocks 4*kc .. 4*kc+3.
+__global__ void scale_relayout_kernel(const uint8_t *__restrict__ scales, int64_t rows, int64_t K,
+                                      uint8_t *__restrict__ mma_scales, int64_t total_words) {
+  const int64_t KB = K / 16, KA = K / 64;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_words;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t atom = i / 128, w = i % 128;
+    const int64_t rb = atom / KA, kc = atom % KA;
+    const int64_t r = rb * 128 + 32 * (w % 4) + w / 4;
+    uint32_t v = 0;
+    if (r < rows) v = *reinterpret_cast<const uint32_t *>(scales + r * KB + 4 * kc);
+    reinterpret_cast<uint32_t *>(mma_scales)[i] = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_scale_relayout(const uint8_t *scales, int64_t rows, int64_t K,
+                                  uint8_t *mma_scales, cudaStream_t stream) {
+  const int64_t words = (int64_t)mma_scale_bytes(rows, K) / 4;
+  int64_t grid = ceil_div(words, 256);
+  const int64_t cap = (int64_t)num_sms_cached() * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  scale_relayout_kernel<<<(int)grid, 256, 0, stream>>>(scales, rows, K, mma_scales, words);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                                uint8_t *codes, uint8_t *mma_scales, float *tensor_scale,
+                                int32_t *status, void *workspace, cudaStream_t stream) {
+  const int ga = amax_grid(rows);
+  uint32_t *partial = static_cast<uint32_t *>(workspace);
+  amax_partial_kernel<<<ga, kAmaxThreads, 0, stream>>>(x, rows, K, ldx, partial, status);
+  const int64_t segs = rows * ceil_div(K / 16, 32);
+  int64_t ge = ceil_div(segs, kEncThreads / 32);
+  const int64_t cap = (int64_t)num_sms_cached() * 8;
+  if (ge > cap) ge = cap;
+  if (ge < 1) ge = 1;
+  encode_kernel<true><<<static_cast<int>(ge), kEncThreads, 0, stream>>>(
+      x, rows, K, ldx, partial, ga, codes, mma_scales, tensor_scale);
   return cudaGetLastError();
 }
 

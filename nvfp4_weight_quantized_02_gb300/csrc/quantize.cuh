@@ -17,3 +17,35 @@ cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t 
                             int32_t *status, void *workspace, cudaStream_t stream);
 
 }  // namespace impfp4
+
+namespace impfp4 {
+
+// ---- block-scale layout used by the tensor-core (prefill) path -------------
+//
+// tcgen05.cp (shape 32x128b, warpx4) moves 512-byte scale "atoms" into tensor
+// memory; one atom holds the scales of 128 rows x 4 blocks (64 k), row r of
+// the atom at byte 16*(r % 32) + 4*((r / 32) % 4), block kb at + kb.  In
+// global memory the atoms of a 128-row block are stored consecutively along
+// K, and row blocks follow each other.  Rows are padded to a multiple of 256
+// so a 256-row operand tile never reads past the array.
+__host__ __device__ inline int64_t mma_scale_rows(int64_t rows) { return ((rows + 255) / 256) * 256; }
+__host__ __device__ inline size_t mma_scale_bytes(int64_t rows, int64_t K) {
+  return (size_t)mma_scale_rows(rows) * (size_t)(K / 16);
+}
+__host__ __device__ inline int64_t mma_scale_offset(int64_t r, int64_t kb, int64_t K) {
+  const int64_t atoms_per_rowblock = K / 64;
+  return ((r / 128) * atoms_per_rowblock + kb / 4) * 512 + 16 * (r % 32) + 4 * ((r / 32) % 4) +
+         (kb % 4);
+}
+
+// Row-major scales [rows][K/16] -> the atom layout above (padding rows = 0).
+cudaError_t launch_scale_relayout(const uint8_t *scales, int64_t rows, int64_t K,
+                                  uint8_t *mma_scales, cudaStream_t stream);
+
+// The quantizer writing its block scales in the atom layout (codes stay
+// row-major [rows][K/2]).  K % 64 == 0.
+cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                                uint8_t *codes, uint8_t *mma_scales, float *tensor_scale,
+                                int32_t *status, void *workspace, cudaStream_t stream);
+
+}  // namespace impfp4

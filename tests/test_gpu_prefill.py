@@ -1,0 +1,98 @@
+"""Prefill path (M > 16) vs the oracle: X quantized on device (bit-exact to
+the oracle's quantizer), block-scaled FP4 tensor-core GEMM within the
+acceptance band on every checked element; the scale-atom layout checked
+against its definition."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu import check_within_tolerance, dev_bf16, dev_nvfp4, sample_rows
+
+pkg = pytest.importorskip("nvfp4_weight_quantized_02_gb300")
+pytestmark = pytest.mark.gpu
+
+
+def atom_layout(scales: np.ndarray, K: int) -> np.ndarray:
+    """Row-major [rows][K/16] scale bytes -> the documented 512-byte atom layout
+    (128 rows x 4 blocks per atom; rows padded to a multiple of 256)."""
+    rows, KB = scales.shape
+    rpad = (rows + 255) // 256 * 256
+    out = np.zeros(rpad * KB, np.uint8)
+    r = np.arange(rows)[:, None]
+    kb = np.arange(KB)[None, :]
+    off = ((r // 128) * (K // 64) + kb // 4) * 512 + 16 * (r % 32) + 4 * ((r // 32) % 4) + kb % 4
+    out[off] = scales
+    return out
+
+
+def test_prepare_mma_matches_layout_definition():
+    rng = np.random.default_rng(0)
+    for rows, K in [(1, 64), (130, 320), (300, 1024)]:
+        sc = rng.integers(0, 0x7F, size=(rows, K // 16), dtype=np.uint8)
+        t = dev_nvfp4(np.zeros((rows, K // 2), np.uint8), sc, 1.0)
+        got = pkg.prepare_mma(t).scales.cpu().numpy()
+        np.testing.assert_array_equal(got, atom_layout(sc, K))
+
+
+def test_quantize_mma_equals_quantize_plus_layout():
+    lin = synth.Linear("qm", 300, 1024, 1, 31, x_outlier_frac=0.01)
+    xb = lin.act_bf16()
+    q = pkg.quantize_mma(dev_bf16(xb))
+    torch.cuda.synchronize()
+    c, s, ts, _ = oracle.quantize(xb)
+    np.testing.assert_array_equal(q.codes.cpu().numpy(), c)
+    np.testing.assert_array_equal(q.scales.cpu().numpy()[: atom_layout(s, 1024).size],
+                                  atom_layout(s, 1024)[: q.scales.numel()])
+    assert np.float32(q.tensor_scale.item()) == np.float32(ts)
+
+
+def run_prefill(lin, rows_check=None, cols_check=None, via="gemm"):
+    xb = lin.act_bf16()
+    wb = lin.weight_bf16()
+    w = pkg.quantize(dev_bf16(wb))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if via == "gemm":
+        y = pkg.gemm(dev_bf16(xb), w, dev_status=status)
+    else:
+        xq = pkg.quantize_mma(dev_bf16(xb), dev_status=status)
+        y = pkg.gemm_fp4(xq, pkg.prepare_mma(w), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, int(status.item())
+    y = y.float().cpu().numpy()
+    rows = np.arange(lin.M) if rows_check is None else rows_check
+    cols = np.arange(lin.N) if cols_check is None else cols_check
+    _, s_w, _ = oracle.tensor_scale(wb)
+    wc, wsc = oracle.quantize_rows(wb[cols], s_w)
+    _, s_x, _ = oracle.tensor_scale(xb)
+    y_ref, bound = oracle.reference_gemm(xb[rows], lin.M, wc, wsc, s_w, s_x=s_x)
+    ratio = check_within_tolerance(y[np.ix_(rows, cols)], y_ref, bound, lin.name, tight=False)
+    assert np.isfinite(y).all()
+    return ratio
+
+
+@pytest.mark.parametrize("M,K,N", [(128, 64, 256), (128, 256, 256), (256, 1024, 512),
+                                   (128, 320, 256), (200, 320, 300), (17, 128, 40),
+                                   (640, 5120, 768), (333, 2048, 1000)])
+def test_small_shapes_every_element(M, K, N):
+    lin = synth.Linear("pf", M, K, N, 77, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
+                       zero_block_p=0.01, x_outlier_frac=0.01)
+    run_prefill(lin, via="gemm_fp4")
+    run_prefill(lin, via="gemm")
+
+
+@pytest.mark.parametrize("lin", synth.workload("prefill_27b"), ids=lambda l: f"{l.K}x{l.N}")
+def test_full_size_sampled(lin):
+    rows = np.arange(0, lin.M, 32)  # the 64-row sample m = 32 i
+    cols = sample_rows(lin.N, seed=lin.K)
+    run_prefill(lin, rows_check=rows, cols_check=cols)
+
+
+def test_repeatable():
+    lin = synth.Linear("rep", 256, 1024, 512, 5, w_dist=synth.DIST_STUDENT_T4)
+    xb, wb = lin.act_bf16(), lin.weight_bf16()
+    w = pkg.quantize(dev_bf16(wb))
+    a = pkg.gemm(dev_bf16(xb), w).cpu()
+    b = pkg.gemm(dev_bf16(xb), w).cpu()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
