@@ -43,8 +43,11 @@ def test_quantize_mma_equals_quantize_plus_layout():
     torch.cuda.synchronize()
     c, s, ts, _ = oracle.quantize(xb)
     np.testing.assert_array_equal(q.codes.cpu().numpy(), c)
-    np.testing.assert_array_equal(q.scales.cpu().numpy()[: atom_layout(s, 1024).size],
-                                  atom_layout(s, 1024)[: q.scales.numel()])
+    # compare the bytes of real rows (padding rows are not written)
+    r = np.arange(300)[:, None]
+    kb = np.arange(64)[None, :]
+    off = ((r // 128) * 16 + kb // 4) * 512 + 16 * (r % 32) + 4 * ((r // 32) % 4) + kb % 4
+    np.testing.assert_array_equal(q.scales.cpu().numpy()[off], s)
     assert np.float32(q.tensor_scale.item()) == np.float32(ts)
 
 
