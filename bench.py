@@ -334,11 +334,62 @@ def load_traffic(kernel: str, lin):
         return None
 
 
-def bench_extras(args, pkg, dev, stream, hbm_peak):
-    """Skinny-M decode rates (M = 2..16) and the quantizer rate."""
+def fp4_peak_tflops():
+    """Dense FP4 tensor peak: the measured bf16 peak times the nominal
+    FP4 : bf16 ratio (13.5 : 2.25 PFLOP/s dense)."""
+    _, bf16, kind = load_peaks()
+    return bf16 * (13.5 / 2.25), kind
+
+
+def bench_prefill(args, pkg, dev, stream):
+    """Prefill GEMMs (M = 2048): the block-scaled FP4 tensor-core GEMM alone
+    (X already quantized, W scales in the atom layout) and the whole
+    imp_nvfp4_gemm call (X quantization + W scale layout + GEMM)."""
     import torch
 
-    out = {}
+    peak, kind = fp4_peak_tflops()
+    res = {}
+    for l in synth.workload("prefill_27b"):
+        wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+        w = pkg.quantize(wb)
+        del wb
+        wm = pkg.prepare_mma(w)
+        x = torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+        xq = pkg.quantize_mma(x)
+        y = torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), dtype=torch.uint8,
+                         device=dev)
+        flops = 2.0 * l.M * l.N * l.K
+        out = {}
+        for name, fn in (("gemm_fp4", lambda: pkg.gemm_fp4(xq, wm, y=y, stream=stream)),
+                         ("imp_nvfp4_gemm", lambda: pkg.gemm(x, w, y=y, stream=stream,
+                                                             workspace=ws))):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            reps = 20
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / reps
+            tf = flops / (t * 1e-3) / 1e12
+            out[name] = {"us": 1e3 * t, "TFLOP/s": tf, "frac_of_fp4_peak": tf / peak}
+        res[f"M{l.M}_{l.K}x{l.N}"] = out
+        del w, wm, x, xq, y, ws
+    res["fp4_peak_tflops"] = peak
+    res["fp4_peak_kind"] = f"{kind} bf16 x 6 (nominal fp4:bf16 ratio)"
+    return res
+
+
+def bench_extras(args, pkg, dev, stream, hbm_peak):
+    """Prefill GEMMs, skinny-M decode rates (M = 2..16) and the quantizer rate."""
+    import torch
+
+    out = {"prefill": bench_prefill(args, pkg, dev, stream)}
     lins = synth.workload("skinny_27b")
     skinny = {}
     cache = {}
