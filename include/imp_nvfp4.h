@@ -103,6 +103,28 @@ imp_status imp_nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64
                               const imp_nvfp4_tensor *out, int32_t *dev_status,
                               void *workspace, size_t ws_bytes, void *stream);
 
+/* Allocation-free quantizer (no counterpart in the source pages; an addition
+ * of this library).  For callers that may not allocate device memory at the
+ * point of the call -- a serving loop that forbids allocation after start-up,
+ * code running inside a stream capture, a process whose device memory is one
+ * fixed pool -- and so cannot provide imp_nvfp4_quantize's workspace.
+ * Same arguments, results and errors as imp_nvfp4_quantize, minus the
+ * workspace: the scratch (per-CTA partial maxima, 4 KB) lives in a fixed
+ * device array inside the library, which every GPU that loads the library
+ * keeps until the process exits.  Sizes whose scratch would exceed that
+ * array return IMP_ERR_WORKSPACE_TOO_SMALL (with 4 KB no valid size does).
+ *   - Allocates nothing and calls no allocating routine.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture that is to contain later calls.
+ *   - All calls share the one array: calls that can run at the same time on
+ *     the GPU (different streams, concurrent graphs) race and corrupt each
+ *     other's results.  The array needs no clearing: each call overwrites
+ *     what it reads.                                                        */
+imp_status imp_nvfp4_quantize_noalloc(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                                      const imp_nvfp4_tensor *out, int32_t *dev_status,
+                                      void *stream);
+
 /* Bytes of workspace imp_nvfp4_gemm needs for Y[M][N] = X[M][K] W^T (0 for
  * M <= 16; for M > 16 the quantized X, X's and W's atom-layout scales). */
 size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);

@@ -26,6 +26,7 @@ __all__ = [
     "imp_nvfp4_gemm_workspace_size", "imp_status_string", "NVFP4Tensor", "quantize", "gemm",
     "library_path", "header_functions", "ImpError", "load", "imp_nvfp4_mma_scales_size",
     "imp_nvfp4_prepare_mma", "imp_nvfp4_quantize_mma", "imp_nvfp4_gemm_fp4", "prepare_mma",
+    "imp_nvfp4_quantize_noalloc",
     "quantize_mma", "gemm_fp4",
 ]
 
@@ -77,6 +78,8 @@ def _L():
     lib.imp_nvfp4_prepare_mma.argtypes = [T, P, SZ, P]
     lib.imp_nvfp4_quantize_mma.restype = ctypes.c_int
     lib.imp_nvfp4_quantize_mma.argtypes = [P, I64, I64, I64, T, P, P, SZ, P]
+    lib.imp_nvfp4_quantize_noalloc.restype = ctypes.c_int
+    lib.imp_nvfp4_quantize_noalloc.argtypes = [P, I64, I64, I64, T, P, P]
     lib.imp_nvfp4_gemm_fp4.restype = ctypes.c_int
     lib.imp_nvfp4_gemm_fp4.argtypes = [T, T, P, I64, P, P]
     _lib = lib
@@ -139,6 +142,14 @@ def imp_nvfp4_quantize_mma(x_bf16: int, rows: int, K: int, ldx: int, out: ImpNvf
                            stream: int | None) -> int:
     return _L().imp_nvfp4_quantize_mma(x_bf16, rows, K, ldx, ctypes.byref(out), dev_status,
                                        workspace, ws_bytes, stream)
+
+
+def imp_nvfp4_quantize_noalloc(x_bf16: int, rows: int, K: int, ldx: int, out: ImpNvfp4Tensor,
+                               dev_status: int | None, stream: int | None) -> int:
+    """The quantizer without caller workspace (its scratch is a fixed array
+    inside the library); for callers that cannot allocate at call time."""
+    return _L().imp_nvfp4_quantize_noalloc(x_bf16, rows, K, ldx, ctypes.byref(out), dev_status,
+                                           stream)
 
 
 def imp_nvfp4_gemm_fp4(xq: ImpNvfp4Tensor, wq: ImpNvfp4Tensor, y_bf16: int, ldy: int,

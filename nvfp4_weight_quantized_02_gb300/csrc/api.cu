@@ -86,6 +86,30 @@ imp_status imp_nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64
                                            workspace, s));
 }
 
+imp_status imp_nvfp4_quantize_noalloc(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                                      const imp_nvfp4_tensor *out, int32_t *dev_status,
+                                      void *stream) {
+  if (rows < 0 || K <= 0) return rows < 0 ? IMP_ERR_INVALID_ARG : IMP_ERR_UNSUPPORTED_SHAPE;
+  if (K % 16) return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K) return IMP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {
+    if (!out || out->rows != 0 || out->K != K || !out->tensor_scale) return IMP_ERR_INVALID_ARG;
+    if (!aligned4(out->tensor_scale)) return IMP_ERR_MISALIGNED;
+    return from_cuda(cudaMemsetAsync(out->tensor_scale, 0, sizeof(float), s));
+  }
+  imp_status st = check_tensor(out, rows, K);
+  if (st != IMP_OK) return st;
+  if (!x_bf16) return IMP_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || ldx % 8) return IMP_ERR_MISALIGNED;
+  // the built-in scratch must hold this call's partial maxima
+  if (impfp4::quantize_workspace_bytes(rows, K) > impfp4::quantize_noalloc_capacity())
+    return IMP_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(impfp4::launch_quantize_noalloc(static_cast<const uint16_t *>(x_bf16), rows,
+                                                   K, ldx, out->codes, out->scales,
+                                                   out->tensor_scale, dev_status, s));
+}
+
 size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0 || K % 64) return 0;
   if (M <= kDecodeMaxM) return 0;

@@ -221,6 +221,41 @@ cudaError_t launch_scale_relayout(const uint8_t *scales, int64_t rows, int64_t K
   return cudaGetLastError();
 }
 
+// ---- allocation-free variant -------------------------------------------------
+//
+// Scratch of imp_nvfp4_quantize_noalloc: the per-CTA partial maxima of pass
+// 1, in a fixed device array instead of caller-provided workspace.  Every
+// GPU that loads the library holds these 4 KB until the process exits.
+namespace {
+__device__ __align__(256) uint32_t g_noalloc_partials[kMaxPartials];
+}
+
+size_t quantize_noalloc_capacity() { return sizeof(g_noalloc_partials); }
+
+cudaError_t launch_quantize_noalloc(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                                    uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                                    int32_t *status, cudaStream_t stream) {
+  if (quantize_workspace_bytes(rows, K) > sizeof(g_noalloc_partials))
+    return cudaErrorInvalidValue;  // caller checks sizes first; kept as a guard
+  // In host code g_noalloc_partials names a host-side shadow, not device
+  // memory: the device address is looked up once per device (with that
+  // device current) and cached.
+  static void *addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_partials);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  // Pass 1 writes every partial that pass 2 reads, so the array needs no
+  // clearing between calls.
+  return launch_quantize(x, rows, K, ldx, codes, scales, tensor_scale, status, addr[dev], stream);
+}
+
 cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
                                 uint8_t *codes, uint8_t *mma_scales, float *tensor_scale,
                                 int32_t *status, void *workspace, cudaStream_t stream) {

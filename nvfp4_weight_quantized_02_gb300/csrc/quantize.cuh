@@ -10,6 +10,16 @@ int num_sms();
 // Workspace (bytes) of launch_quantize for a rows x K tensor.
 size_t quantize_workspace_bytes(int64_t rows, int64_t K);
 
+// Bytes of the fixed scratch array of the allocation-free quantizer.
+size_t quantize_noalloc_capacity();
+
+// The two quantizer passes with their scratch in a fixed device array (no
+// caller workspace, no allocation).  Calls that overlap on the GPU share the
+// array and race.
+cudaError_t launch_quantize_noalloc(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                                    uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                                    int32_t *status, cudaStream_t stream);
+
 // Enqueue the two quantizer passes on `stream`.  Arguments are validated by
 // the caller (api.cu).  rows > 0.
 cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
