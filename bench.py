@@ -441,6 +441,87 @@ def bench_extras(args, pkg, dev, stream, hbm_peak):
     return out
 
 
+def run_prefill_workload(args):
+    """--workload prefill_27b: one step = the two prefill GEMMs (M = 2048) on
+    the block-scaled FP4 tensor cores, X already quantized and W's scales in
+    the atom layout; metric TFLOP/s.  e2e = imp_nvfp4_gemm from bf16 X copied
+    from pinned host memory (quantization + W scale layout + GEMM) with Y
+    copied back."""
+    import torch
+
+    import nvfp4_weight_quantized_02_gb300 as pkg
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pkg.load()
+    stream = torch.cuda.current_stream(dev)
+    lins = synth.workload(args.workload)
+    items = []
+    for l in lins:
+        wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+        w = pkg.quantize(wb)
+        del wb
+        x = torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+        items.append(dict(l=l, w=w, wm=pkg.prepare_mma(w), x=x, xq=pkg.quantize_mma(x),
+                          y=torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev),
+                          ws=torch.empty(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K),
+                                         dtype=torch.uint8, device=dev)))
+    flops = sum(2.0 * it["l"].M * it["l"].N * it["l"].K for it in items)
+
+    def step():
+        for it in items:
+            pkg.gemm_fp4(it["xq"], it["wm"], y=it["y"], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clocks:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, kind = fp4_peak_tflops()
+    value = flops / (ms * 1e-3) / 1e12
+    pin_x = [torch.empty(it["x"].shape, dtype=torch.bfloat16, pin_memory=True).copy_(it["x"])
+             for it in items]
+    pin_y = [torch.empty(it["y"].shape, dtype=torch.bfloat16, pin_memory=True) for it in items]
+
+    def e2e_step():
+        for px, py, it in zip(pin_x, pin_y, items):
+            it["x"].copy_(px, non_blocking=True)
+            pkg.gemm(it["x"], it["w"], y=it["y"], stream=stream, workspace=it["ws"])
+            py.copy_(it["y"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    line = {"metric": "prefill FP4 TFLOPS (block-scaled tcgen05 GEMM, M=2048)", "value": value,
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 x nvfp4, f32 accumulate, bf16 out", "data": "synthetic",
+            "config": {"workload": args.workload,
+                       "shapes_MxKxN": [[it["l"].M, it["l"].K, it["l"].N] for it in items]},
+            "roofline": {"bound": "tensor", "kernel": "gemm_mxf4_kernel", "achieved": value,
+                         "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
+                         "frac": value / peak, "traffic": None},
+            "gpu_launches": args.steps * len(items), "clocks": clocks.summary(),
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": sum(p.numel() * 2 for p in pin_x),
+                    "d2h_bytes_per_step": sum(p.numel() * 2 for p in pin_y)}}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,6 +538,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload.startswith("prefill"):
+        return run_prefill_workload(args)
     return run_native(args)
 
 
