@@ -14,14 +14,16 @@
 //    scales (already in the 512-byte atom layout, see quantize.cuh) with
 //    bulk copies, into a 4-deep shared-memory ring.
 //  * warp 1: allocates 512 tensor-memory columns; one thread issues, per
-//    64-element K step, three tcgen05.cp (scales of the X rows and of the two
-//    128-row halves of the W tile into tensor memory) and one tcgen05.mma
-//    (M = 128, N = 256, K = 64) accumulating into columns 0..255;
+//    stage, twelve tcgen05.cp (per 64-element K step: the scales of the X rows
+//    and of the two 128-row halves of the W tile, into one of two column
+//    banks) and then four tcgen05.mma (M = 128, N = 256, K = 64) accumulating
+//    into columns 0..255;
 //    tcgen05.commit releases each ring stage and, at the end of a tile,
 //    signals the epilogue.
-//  * warps 2..5: epilogue.  Each thread owns one accumulator row (its warp's
-//    32-lane quarter of tensor memory), reads it 32 columns at a time with
-//    tcgen05.ld, multiplies by s_x * s_w, rounds to bf16 and stores to Y.
+//  * warps 2..9: epilogue.  Each thread owns half of one accumulator row
+//    (its warp's 32-lane quarter of tensor memory, 128 of the 256 columns),
+//    reads it with tcgen05.ld, multiplies by s_x * s_w, rounds to bf16, hands
+//    the accumulator back, then stores to Y while the next tile's MMAs run.
 // Every wait is bounded; on a timeout the kernel reports IMP_DEV_TIMEOUT,
 // drains its own copies and MMAs, frees tensor memory and returns.
 #include "gemm_tcgen05.cuh"
@@ -42,10 +44,12 @@ constexpr uint32_t SFA_BYTES = (BM / 128) * KSTEPS * 512;    // 2 KB
 constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;    // 4 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t OFF_B = A_BYTES, OFF_SFA = A_BYTES + B_BYTES, OFF_SFB = OFF_SFA + SFA_BYTES;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kEpiThreads = 256;
+constexpr int kEpiCols = 128;  // accumulator columns per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_D = 0;     // accumulator: columns 0..255
-constexpr uint32_t TMEM_SF = 256;  // scales: 12 columns per K step (X 4, W 8)
+constexpr uint32_t TMEM_SF = 256;  // scales: 12 columns per K step (X 4, W 8), 2 banks of 48
 constexpr size_t kBarBytes = 256;
 constexpr size_t kSmemBytes = 1024 + NSTAGE * (size_t)STAGE_BYTES + kBarBytes;
 
@@ -149,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(accf, 1);
-    mbar_init(acce, 128);
+    mbar_init(acce, kEpiThreads);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -229,14 +233,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sA = smem_u32(st), sB = smem_u32(st + OFF_B);
           const uint32_t sSFA = smem_u32(st + OFF_SFA), sSFB = smem_u32(st + OFF_SFB);
           const int nk = min(KSTEPS, (a.K - ks * BK) / MMA_K);
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint32_t sf = tmem + TMEM_SF + 12u * kk;
-            tc_cp_sf(sf, smem_desc(sSFA + kk * 512, 0, 128, kLayoutNone));
-            tc_cp_sf(sf + 4, smem_desc(sSFB + kk * 512, 0, 128, kLayoutNone));
-            tc_cp_sf(sf + 8, smem_desc(sSFB + 2048 + kk * 512, 0, 128, kLayoutNone));
-            tc_mma(tmem + TMEM_D, smem_desc(sA + kk * 32, 16, 1024, kLayoutSw128),
-                   smem_desc(sB + kk * 32, 16, 1024, kLayoutSw128), kIdesc, sf, sf + 4,
-                   (ks | kk) != 0 ? 1u : 0u);
+          // Scale columns alternate between two banks of 48 by stage parity,
+          // so a stage's copies never overwrite scales an earlier, still
+          // running MMA reads.  All copies of the stage go first, then its
+          // MMAs (fewer copy/MMA switches in the tensor pipe).
+          const uint32_t sf0 = tmem + TMEM_SF + 48u * (uint32_t)(it & 1);
+          const uint64_t dA = smem_desc(sA, 16, 1024, kLayoutSw128);
+          const uint64_t dB = smem_desc(sB, 16, 1024, kLayoutSw128);
+          const uint64_t dSA = smem_desc(sSFA, 0, 128, kLayoutNone);
+          const uint64_t dSB = smem_desc(sSFB, 0, 128, kLayoutNone);
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            if (kk < nk) {
+              // descriptor start address is in 16-byte units: +512 B = +32
+              tc_cp_sf(sf0 + 12u * kk, dSA + 32u * kk);
+              tc_cp_sf(sf0 + 12u * kk + 4, dSB + 32u * kk);
+              tc_cp_sf(sf0 + 12u * kk + 8, dSB + 128u + 32u * kk);
+            }
+          }
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            if (kk < nk) {
+              // K step kk: +32 bytes inside the 128-byte swizzle atom (+2 units)
+              tc_mma(tmem + TMEM_D, dA + 2u * kk, dB + 2u * kk, kIdesc, sf0 + 12u * kk,
+                     sf0 + 12u * kk + 4, (ks | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&empty[s]);  // stage free once these MMAs complete
           committed_any = true;
@@ -254,9 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------ epilogue: warps 2..5
+    // ------------------------------ epilogue: warps 2..9
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
     const int row_in_tile = quarter * 32 + lane;
+    const int col0 = (warp - 2) / 4 * kEpiCols;  // warps 2..5: columns 0..127, 6..9: 128..255
     const float scale = (*a.s_x) * (*a.s_w);
     int tile_iter = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_iter) {
@@ -269,29 +291,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int mb = t % MB, nb = t / MB;
       const int64_t m = (int64_t)mb * BM + row_in_tile;
-      const int n0 = nb * BN;
-      for (int c = 0; c < BN; c += 32) {
+      const int n0 = nb * BN + col0;
+      // Drain this warp's 128 accumulator columns into registers (as bf16
+      // pairs), hand the accumulator back to the MMA warp, then store: the
+      // stores overlap the next tile's MMAs.
+      uint32_t p[kEpiCols / 2];
+#pragma unroll
+      for (int c = 0; c < kEpiCols; c += 32) {
         uint32_t r[32];
-        tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D + c, r);
-        if (c + 32 == BN) {
-          tc_fence_before();
-          mbar_arrive(acce);  // accumulator may be overwritten now
-        }
-        if (m < a.M) {
-          uint16_t *dst = a.y + m * a.ldy + n0 + c;
-          if (n0 + c + 32 <= a.N) {
-            uint32_t p[16];
+        tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D + col0 + c, r);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              p[i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
-                               __uint_as_float(r[2 * i + 1]) * scale);
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+        for (int i = 0; i < 16; ++i)
+          p[c / 2 + i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
+                                   __uint_as_float(r[2 * i + 1]) * scale);
+      }
+      tc_fence_before();
+      mbar_arrive(acce);  // accumulator may be overwritten now
+      if (m < a.M) {
+        uint16_t *dst = a.y + m * a.ldy + n0;
+        if (n0 + kEpiCols <= a.N) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
-          } else {
-            for (int i = 0; i < 32 && n0 + c + i < a.N; ++i)
-              dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * scale));
+          for (int i = 0; i < kEpiCols / 8; ++i)
+            d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kEpiCols / 2; ++i) {
+            if (n0 + 2 * i < a.N) dst[2 * i] = (uint16_t)(p[i] & 0xFFFFu);
+            if (n0 + 2 * i + 1 < a.N) dst[2 * i + 1] = (uint16_t)(p[i] >> 16);
           }
         }
       }
