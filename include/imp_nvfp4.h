@@ -145,27 +145,19 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                           const imp_nvfp4_tensor *w, void *y_bf16, int64_t ldy,
                           int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream);
 
-/* ---- tensor-core operand layouts (prefill path) ----------------------------
- * Codes keep the row-major [rows][K/2] layout; only the block scales move.
- * Weight (B operand) scales: 512-byte atoms, one per 128 rows x 4 blocks
- * (64 elements of K); row r of the atom at byte 16*(r % 32) + 4*((r/32) % 4),
- * block j of it at + j; atoms of a 128-row block consecutive along K; row
- * blocks consecutive; rows padded to a multiple of 256.  A one-time transform
- * (like an engine's cache of transformed weights).
- * Activation (A operand) scales: 4 KB chunks, one per 128 rows x 16 blocks
- * (256 elements of K), 128-row block major; in a chunk, byte x (< 32) of row
- * L (< 128) holds block 16*stage + 4*(x/4 - L/32) + x % 4 of the row when
- * 0 <= x/4 - L/32 <= 3, stored in 128-byte core matrices of 8 rows x 16
- * bytes at ((L/8)*2 + x/16)*128 + (L%8)*16 + x%16; rows padded to a multiple
- * of 256.  Written directly by imp_nvfp4_quantize_mma.                      */
+/* ---- tensor-core operand layout (prefill path) -----------------------------
+ * The block-scaled FP4 MMA reads block scales as 512-byte atoms: one atom
+ * holds the scales of 128 rows x 4 blocks (64 elements of K); row r of the
+ * atom sits at byte 16*(r % 32) + 4*((r / 32) % 4), block j of it at + j.
+ * Atoms of a 128-row block follow each other along K; row blocks follow each
+ * other; rows are padded to a multiple of 256.  Codes keep the row-major
+ * [rows][K/2] layout.  This is a one-time transform for weights (like an
+ * engine's cache of transformed weights).                                   */
 
-/* Bytes of weight-layout scales for a rows x K tensor (K % 64 == 0). */
+/* Bytes of atom-layout scales for a rows x K tensor (K % 64 == 0). */
 size_t imp_nvfp4_mma_scales_size(int64_t rows, int64_t K);
 
-/* Bytes of activation-layout scales for a rows x K tensor (K % 64 == 0). */
-size_t imp_nvfp4_act_scales_size(int64_t rows, int64_t K);
-
-/* Copy the row-major block scales of `t` into the weight (B operand) layout.
+/* Copy the row-major block scales of `t` into the atom layout.
  *   t           NVFP4 tensor (row-major scales), rows >= 1, K % 64 == 0.
  *   mma_scales  device buffer of >= imp_nvfp4_mma_scales_size(rows, K) bytes,
  *               16-byte aligned; padding rows are written as 0.           */
@@ -173,16 +165,14 @@ imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_scales, si
                                  void *stream);
 
 /* Quantize like imp_nvfp4_quantize (bit-identical codes, scale bytes and
- * tensor scale) but write the scales in the activation (A operand) layout:
- * out->scales must hold imp_nvfp4_act_scales_size(rows, K) bytes.
- * K % 64 == 0.                                                             */
+ * tensor scale) but write the scales in the atom layout: out->scales must
+ * hold imp_nvfp4_mma_scales_size(rows, K) bytes.  K % 64 == 0.            */
 imp_status imp_nvfp4_quantize_mma(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
                                   const imp_nvfp4_tensor *out, int32_t *dev_status,
                                   void *workspace, size_t ws_bytes, void *stream);
 
-/* Y = Xq * Wq^T with both operands NVFP4, xq's scales in the activation
- * layout and wq's in the weight layout: the block-scaled FP4 tensor-core
- * GEMM alone (tcgen05.mma
+/* Y = Xq * Wq^T with both operands NVFP4 and their scales in the atom
+ * layout: the block-scaled FP4 tensor-core GEMM alone (tcgen05.mma
  * kind::mxf4nvf4, fp32 accumulation in tensor memory), times
  * s_x * s_w, rounded to bf16.
  *   xq  M rows (M >= 1), K % 64 == 0;  wq  N rows, wq->K == K.

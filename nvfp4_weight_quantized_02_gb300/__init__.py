@@ -26,7 +26,6 @@ __all__ = [
     "imp_nvfp4_gemm_workspace_size", "imp_status_string", "NVFP4Tensor", "quantize", "gemm",
     "library_path", "header_functions", "ImpError", "load", "imp_nvfp4_mma_scales_size",
     "imp_nvfp4_prepare_mma", "imp_nvfp4_quantize_mma", "imp_nvfp4_gemm_fp4", "prepare_mma",
-    "imp_nvfp4_act_scales_size",
     "imp_nvfp4_quantize_noalloc",
     "quantize_mma", "gemm_fp4",
 ]
@@ -75,8 +74,6 @@ def _L():
     T = ctypes.POINTER(ImpNvfp4Tensor)
     lib.imp_nvfp4_mma_scales_size.restype = SZ
     lib.imp_nvfp4_mma_scales_size.argtypes = [I64, I64]
-    lib.imp_nvfp4_act_scales_size.restype = SZ
-    lib.imp_nvfp4_act_scales_size.argtypes = [I64, I64]
     lib.imp_nvfp4_prepare_mma.restype = ctypes.c_int
     lib.imp_nvfp4_prepare_mma.argtypes = [T, P, SZ, P]
     lib.imp_nvfp4_quantize_mma.restype = ctypes.c_int
@@ -133,10 +130,6 @@ def imp_nvfp4_gemm(x_bf16: int, M: int, K: int, ldx: int, w: ImpNvfp4Tensor, y_b
 
 def imp_nvfp4_mma_scales_size(rows: int, K: int) -> int:
     return _L().imp_nvfp4_mma_scales_size(rows, K)
-
-
-def imp_nvfp4_act_scales_size(rows: int, K: int) -> int:
-    return _L().imp_nvfp4_act_scales_size(rows, K)
 
 
 def imp_nvfp4_prepare_mma(t: ImpNvfp4Tensor, mma_scales: int, nbytes: int,
@@ -262,12 +255,12 @@ def _struct(t: NVFP4Tensor) -> ImpNvfp4Tensor:
 
 
 def quantize_mma(x, dev_status=None, stream=None) -> NVFP4Tensor:
-    """Quantize a bf16 CUDA matrix with its scales in the activation operand layout."""
+    """Quantize a bf16 CUDA matrix with its scales in the tensor-core atom layout."""
     import torch
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     rows, K = x.shape
     out = NVFP4Tensor(torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device),
-                      torch.empty(imp_nvfp4_act_scales_size(rows, K), dtype=torch.uint8,
+                      torch.empty(imp_nvfp4_mma_scales_size(rows, K), dtype=torch.uint8,
                                   device=x.device),
                       torch.empty(1, dtype=torch.float32, device=x.device))
     ws_bytes = imp_nvfp4_quantize_workspace_size(rows, K)

@@ -33,7 +33,7 @@ PrefillWs prefill_ws(int64_t M, int64_t N, int64_t K) {
   w.partial = 0;
   w.xcodes = align256(impfp4::quantize_workspace_bytes(M, K));
   w.xsc = align256(w.xcodes + (size_t)M * (size_t)(K / 2));
-  w.wsc = align256(w.xsc + impfp4::act_scale_bytes(M, K));
+  w.wsc = align256(w.xsc + impfp4::mma_scale_bytes(M, K));
   w.sx = align256(w.wsc + impfp4::mma_scale_bytes(N, K));
   w.total = w.sx + 256;
   return w;
@@ -119,11 +119,6 @@ size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
 size_t imp_nvfp4_mma_scales_size(int64_t rows, int64_t K) {
   if (rows <= 0 || K <= 0 || K % 64) return 0;
   return impfp4::mma_scale_bytes(rows, K);
-}
-
-size_t imp_nvfp4_act_scales_size(int64_t rows, int64_t K) {
-  if (rows <= 0 || K <= 0 || K % 64) return 0;
-  return impfp4::act_scale_bytes(rows, K);
 }
 
 imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_scales, size_t bytes,

@@ -14,12 +14,10 @@
 //    scales (already in the 512-byte atom layout, see quantize.cuh) with
 //    bulk copies, into a 4-deep shared-memory ring.
 //  * warp 1: allocates 512 tensor-memory columns; one thread issues, per
-//    stage, one 128x256b tcgen05.cp with the X scales of all four K steps,
-//    two 32x128b.warpx4 copies per K step with the scales of the two
-//    128-row halves of the W tile (into one of two column banks), then four
-//    tcgen05.mma (M = 128, N = 256, K = 64) accumulating into columns 0..255.
-//    tcgen05.cp costs about the same per instruction whatever its size, so
-//    the X scales travel in one copy per stage instead of four;
+//    stage, twelve tcgen05.cp (per 64-element K step: the scales of the X rows
+//    and of the two 128-row halves of the W tile, into one of two column
+//    banks) and then four tcgen05.mma (M = 128, N = 256, K = 64) accumulating
+//    into columns 0..255;
 //    tcgen05.commit releases each ring stage and, at the end of a tile,
 //    signals the epilogue.
 //  * warps 2..9: epilogue.  Each thread owns half of one accumulator row
@@ -42,7 +40,7 @@ constexpr int KSTEPS = BK / MMA_K;  // 4 MMAs per stage
 constexpr int NSTAGE = 4;
 constexpr uint32_t A_BYTES = BM * BK / 2;                    // 16 KB
 constexpr uint32_t B_BYTES = BN * BK / 2;                    // 32 KB
-constexpr uint32_t SFA_BYTES = 4096;                          // 4 KB: one packed chunk
+constexpr uint32_t SFA_BYTES = (BM / 128) * KSTEPS * 512;    // 2 KB
 constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;    // 4 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t OFF_B = A_BYTES, OFF_SFA = A_BYTES + B_BYTES, OFF_SFB = OFF_SFA + SFA_BYTES;
@@ -51,10 +49,7 @@ constexpr int kEpiThreads = 256;
 constexpr int kEpiCols = 128;  // accumulator columns per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_D = 0;     // accumulator: columns 0..255
-// scales, two banks of 40 columns by stage parity: X 8 columns (all 4 K
-// steps, one 128x256b copy), then W 8 columns per K step (two 32x128b copies)
-constexpr uint32_t TMEM_SF = 256;
-constexpr uint32_t SF_BANK = 40;
+constexpr uint32_t TMEM_SF = 256;  // scales: 12 columns per K step (X 4, W 8), 2 banks of 48
 constexpr size_t kBarBytes = 256;
 constexpr size_t kSmemBytes = 1024 + NSTAGE * (size_t)STAGE_BYTES + kBarBytes;
 
@@ -98,9 +93,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
-}
-__device__ __forceinline__ void tc_cp_sf_128x256(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
@@ -195,11 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int natoms = min(KSTEPS, KA - ks * KSTEPS);
           uint8_t *st = smem + (size_t)s * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES + 4096u + 2u * natoms * 512u);
+          mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES + 3u * natoms * 512u);
           tma_load_2d(st, &tmA, ks * (BK / 2), mb * BM, &full[s]);
           tma_load_2d(st + OFF_B, &tmB, ks * (BK / 2), nb * BN, &full[s]);
           const int64_t atom0 = (int64_t)ks * KSTEPS;
-          bulk_g2s(st + OFF_SFA, a.sfa + ((int64_t)mb * n_ks + ks) * 4096, 4096u, &full[s]);
+          bulk_g2s(st + OFF_SFA, a.sfa + ((int64_t)mb * KA + atom0) * 512, natoms * 512u,
+                   &full[s]);
           bulk_g2s(st + OFF_SFB, a.sfb + ((int64_t)(2 * nb) * KA + atom0) * 512, natoms * 512u,
                    &full[s]);
           bulk_g2s(st + OFF_SFB + 2048, a.sfb + ((int64_t)(2 * nb + 1) * KA + atom0) * 512,
@@ -246,27 +239,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           // so a stage's copies never overwrite scales an earlier, still
           // running MMA reads.  All copies of the stage go first, then its
           // MMAs (fewer copy/MMA switches in the tensor pipe).
-          const uint32_t sf0 = tmem + TMEM_SF + SF_BANK * (uint32_t)(it & 1);
+          const uint32_t sf0 = tmem + TMEM_SF + 48u * (uint32_t)(it & 1);
           const uint64_t dA = smem_desc(sA, 16, 1024, kLayoutSw128);
           const uint64_t dB = smem_desc(sB, 16, 1024, kLayoutSw128);
+          const uint64_t dSA = smem_desc(sSFA, 0, 128, kLayoutNone);
           const uint64_t dSB = smem_desc(sSFB, 0, 128, kLayoutNone);
-          // X scales of all 4 K steps: one copy (core matrices: 16-byte
-          // halves 128 B apart, 8-row groups 256 B apart)
-          tc_cp_sf_128x256(sf0, smem_desc(sSFA, 128, 256, kLayoutNone));
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
             if (kk < nk) {
-              // W scales of K step kk: rows 0..127 and 128..255 of the tile
-              tc_cp_sf(sf0 + 8u + 8u * kk, dSB + 32u * kk);
-              tc_cp_sf(sf0 + 8u + 8u * kk + 4, dSB + 128u + 32u * kk);
+              // descriptor start address is in 16-byte units: +512 B = +32
+              tc_cp_sf(sf0 + 12u * kk, dSA + 32u * kk);
+              tc_cp_sf(sf0 + 12u * kk + 4, dSB + 32u * kk);
+              tc_cp_sf(sf0 + 12u * kk + 8, dSB + 128u + 32u * kk);
             }
           }
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
             if (kk < nk) {
               // K step kk: +32 bytes inside the 128-byte swizzle atom (+2 units)
-              tc_mma(tmem + TMEM_D, dA + 2u * kk, dB + 2u * kk, kIdesc, sf0 + kk,
-                     sf0 + 8u + 8u * kk, (ks | kk) != 0 ? 1u : 0u);
+              tc_mma(tmem + TMEM_D, dA + 2u * kk, dB + 2u * kk, kIdesc, sf0 + 12u * kk,
+                     sf0 + 12u * kk + 4, (ks | kk) != 0 ? 1u : 0u);
             }
           }
           tc_commit(&empty[s]);  // stage free once these MMAs complete

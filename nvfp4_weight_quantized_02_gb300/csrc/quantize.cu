@@ -79,8 +79,8 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partial_kernel(const uint16
 }
 
 // Pass 2: fold the partial maxima, then encode one 16-element block per thread.
-// MMA_LAYOUT: write the scale bytes in the activation operand layout of the
-// tensor-core GEMM (act_scale_offset) instead of row-major.
+// MMA_LAYOUT: write the scale bytes in the tensor-core atom layout
+// (mma_scale_offset) instead of row-major.
 template <bool MMA_LAYOUT>
 __global__ void __launch_bounds__(kEncThreads) encode_kernel(
     const uint16_t *__restrict__ x, int64_t rows, int64_t K, int64_t ldx,
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(
     }
     *reinterpret_cast<uint2 *>(codes + r * (K / 2) + b * 8) = make_uint2(packed[0], packed[1]);
     if (MMA_LAYOUT)
-      scales[act_scale_offset(r, b, K)] = static_cast<uint8_t>(sb);
+      scales[mma_scale_offset(r, b, K)] = static_cast<uint8_t>(sb);
     else
       scales[r * blocks_per_row + b] = static_cast<uint8_t>(sb);
   }

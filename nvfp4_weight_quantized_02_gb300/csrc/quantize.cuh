@@ -48,36 +48,12 @@ __host__ __device__ inline int64_t mma_scale_offset(int64_t r, int64_t kb, int64
          (kb % 4);
 }
 
-// ---- activation (A-operand) block-scale layout ----------------------------
-//
-// The X operand's scales for one 256-element K stage (4 MMA K steps) of a
-// 128-row block move into tensor memory with a single tcgen05.cp of shape
-// 128x256b: row L of the 4 KB chunk (32 bytes) lands in tensor-memory lane L,
-// columns c..c+7.  The MMA of K step kk reads, in lane quarter q = L / 32,
-// column c + kk + q; so byte 4j + b of row L holds block 4(kk) + b of row L
-// for kk = j - q (0 <= kk <= 3; other bytes unused).  The chunk is stored in
-// core-matrix order (8 rows x 16 bytes per 128-byte core matrix, the two
-// 16-byte halves of a row 128 bytes apart, 8-row groups 256 bytes apart).
-// Chunks: 128-row block major, K stage minor; rows padded to a multiple of
-// 256.
-__host__ __device__ inline int64_t act_scale_stages(int64_t K) { return (K / 16 + 15) / 16; }
-__host__ __device__ inline size_t act_scale_bytes(int64_t rows, int64_t K) {
-  return (size_t)(mma_scale_rows(rows) / 128) * (size_t)act_scale_stages(K) * 4096;
-}
-__host__ __device__ inline int64_t act_scale_offset(int64_t r, int64_t kb, int64_t K) {
-  const int64_t L = r % 128, q = L / 32;
-  const int64_t st = kb / 16, kk = (kb % 16) / 4;
-  const int64_t x = 4 * (kk + q) + (kb % 4);  // byte within the 32-byte row
-  return ((r / 128) * act_scale_stages(K) + st) * 4096 + ((L / 8) * 2 + x / 16) * 128 +
-         (L % 8) * 16 + (x % 16);
-}
-
 // Row-major scales [rows][K/16] -> the atom layout above (padding rows = 0).
 cudaError_t launch_scale_relayout(const uint8_t *scales, int64_t rows, int64_t K,
                                   uint8_t *mma_scales, cudaStream_t stream);
 
-// The quantizer writing its block scales in the activation (A-operand)
-// layout (codes stay row-major [rows][K/2]).  K % 64 == 0.
+// The quantizer writing its block scales in the atom layout (codes stay
+// row-major [rows][K/2]).  K % 64 == 0.
 cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
                                 uint8_t *codes, uint8_t *mma_scales, float *tensor_scale,
                                 int32_t *status, void *workspace, cudaStream_t stream);
