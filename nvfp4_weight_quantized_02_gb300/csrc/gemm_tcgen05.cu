@@ -208,11 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer
+    // One thread, so every scalar instruction of this loop sits between two
+    // MMAs: stage index and phase rotate instead of being divided out, and
+    // each stage's descriptors are the stage-0 ones plus one offset (the
+    // 14-bit start-address field cannot carry: shared addresses < 256 KB).
     if (lane == 0) {
-      int64_t it = 0;
+      const uint64_t dA0 = smem_desc(smem_u32(smem), 16, 1024, kLayoutSw128);
+      const uint64_t dB0 = smem_desc(smem_u32(smem + OFF_B), 16, 1024, kLayoutSw128);
+      const uint64_t dSA0 = smem_desc(smem_u32(smem + OFF_SFA), 0, 128, kLayoutNone);
+      const uint64_t dSB0 = smem_desc(smem_u32(smem + OFF_SFB), 0, 128, kLayoutNone);
+      uint32_t s = 0, phase = 0;  // ring position of the next stage
+      int64_t issued = 0;         // stages consumed (for the drain on abort)
       int tile_iter = 0;
       bool ok = true;
-      bool committed_any = false;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tile_iter) {
         if (tile_iter > 0 &&
             !mbar_wait_bounded(acce, (uint32_t)((tile_iter - 1) & 1), a.status)) {
@@ -220,59 +228,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < n_ks; ++ks, ++it) {
-          const int s = (int)(it % NSTAGE);
+        for (int ks = 0; ks < n_ks; ++ks) {
           // No shared-memory flag is read in this loop: a generic shared load
           // issued behind in-flight tcgen05.mma stalls the issuing thread
           // (measured: ~2.5x slower MMA issue).  A stalled peer shows up as
           // a timed-out barrier wait instead.
-          if (!mbar_wait_bounded(&full[s], (uint32_t)((it / NSTAGE) & 1), a.status)) {
+          if (!mbar_wait_bounded(&full[s], phase, a.status)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint8_t *st = smem + (size_t)s * STAGE_BYTES;
-          const uint32_t sA = smem_u32(st), sB = smem_u32(st + OFF_B);
-          const uint32_t sSFA = smem_u32(st + OFF_SFA), sSFB = smem_u32(st + OFF_SFB);
-          const int nk = min(KSTEPS, (a.K - ks * BK) / MMA_K);
-          // Scale columns alternate between two banks of 48 by stage parity,
-          // so a stage's copies never overwrite scales an earlier, still
-          // running MMA reads.  All copies of the stage go first, then its
-          // MMAs (fewer copy/MMA switches in the tensor pipe).
-          const uint32_t sf0 = tmem + TMEM_SF + 48u * (uint32_t)(it & 1);
-          const uint64_t dA = smem_desc(sA, 16, 1024, kLayoutSw128);
-          const uint64_t dB = smem_desc(sB, 16, 1024, kLayoutSw128);
-          const uint64_t dSA = smem_desc(sSFA, 0, 128, kLayoutNone);
-          const uint64_t dSB = smem_desc(sSFB, 0, 128, kLayoutNone);
+          const uint64_t off = (uint64_t)(s * (STAGE_BYTES >> 4));
+          const uint64_t dA = dA0 + off, dB = dB0 + off, dSA = dSA0 + off, dSB = dSB0 + off;
+          // scale columns alternate between two banks of 48 by stage parity
+          const uint32_t sf0 = tmem + TMEM_SF + 48u * (s & 1u);
+          const uint32_t acc0 = ks != 0 ? 1u : 0u;
+          if (ks + 1 < n_ks || a.K % BK == 0) {
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS; ++kk) {
-            if (kk < nk) {
+            for (int kk = 0; kk < KSTEPS; ++kk) {
               // descriptor start address is in 16-byte units: +512 B = +32
               tc_cp_sf(sf0 + 12u * kk, dSA + 32u * kk);
               tc_cp_sf(sf0 + 12u * kk + 4, dSB + 32u * kk);
               tc_cp_sf(sf0 + 12u * kk + 8, dSB + 128u + 32u * kk);
             }
-          }
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS; ++kk) {
-            if (kk < nk) {
+            for (int kk = 0; kk < KSTEPS; ++kk)
               // K step kk: +32 bytes inside the 128-byte swizzle atom (+2 units)
               tc_mma(tmem + TMEM_D, dA + 2u * kk, dB + 2u * kk, kIdesc, sf0 + 12u * kk,
-                     sf0 + 12u * kk + 4, (ks | kk) != 0 ? 1u : 0u);
+                     sf0 + 12u * kk + 4, kk ? 1u : acc0);
+          } else {
+            const int nk = (a.K - ks * BK) / MMA_K;  // last, partial stage
+            for (int kk = 0; kk < nk; ++kk) {
+              tc_cp_sf(sf0 + 12u * kk, dSA + 32u * kk);
+              tc_cp_sf(sf0 + 12u * kk + 4, dSB + 32u * kk);
+              tc_cp_sf(sf0 + 12u * kk + 8, dSB + 128u + 32u * kk);
             }
+            for (int kk = 0; kk < nk; ++kk)
+              tc_mma(tmem + TMEM_D, dA + 2u * kk, dB + 2u * kk, kIdesc, sf0 + 12u * kk,
+                     sf0 + 12u * kk + 4, kk ? 1u : acc0);
           }
           tc_commit(&empty[s]);  // stage free once these MMAs complete
-          committed_any = true;
+          ++issued;
+          if (++s == NSTAGE) {
+            s = 0;
+            phase ^= 1u;
+          }
         }
         if (!ok) break;
         tc_commit(accf);  // tile accumulated
       }
       if (!ok) {
         *abort_flag = 1;
-        // let every issued MMA finish before tensor memory is freed
-        if (committed_any) {
-          const int64_t last = it - 1;
-          mbar_wait_bounded(&empty[last % NSTAGE], (uint32_t)((last / NSTAGE) & 1), a.status);
+        // let every issued MMA finish before tensor memory is freed: the last
+        // commit went to the stage before the current ring position
+        if (issued > 0) {
+          const uint32_t ls = s == 0 ? NSTAGE - 1 : s - 1;
+          const uint32_t lp = s == 0 ? (phase ^ 1u) : phase;
+          mbar_wait_bounded(&empty[ls], lp, a.status);
         }
       }
     }
