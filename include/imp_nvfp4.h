@@ -137,6 +137,11 @@ size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  *   K        K > 0, K % 64 == 0, and w->K == K.
  *   w        NVFP4 weight with w->rows = N >= 0 rows (0 = nothing to do).
  *   y_bf16   device bf16[M][ldy], ldy >= N, ldy % 8 == 0; fully overwritten.
+ *   Decode (M <= 16) kernels are launched with programmatic dependent launch:
+ *   when the previous kernel on the stream allows it (this library's decode
+ *   kernels do), the call may start streaming W before that kernel finishes;
+ *   X is read only after it completes.  So W must not be written by a kernel
+ *   that itself allows early launch (the quantizers here do not).
  *   Accuracy: |y - y_exact| <= 2e-3 * sum_k |x_k w_k| + 1e-5 + 2^-8 |y_exact|
  *   per element, with y_exact the exact product of the operands defined
  *   above; the last term is the rounding of the result to bf16.  Results are

@@ -177,6 +177,11 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
   const int64_t row_end = a.N * ((int64_t)blockIdx.x + 1) / G;
   const int64_t n_st = ceil_div(row_end - row_begin, RS);
 
+  // Programmatic dependent launch: the next kernel on the stream may start
+  // as soon as SMs free up; its weight stream then overlaps this kernel's
+  // tail.  Everything it reads before its own griddepcontrol.wait is weight
+  // data, which no kernel in a decode step writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
@@ -220,6 +225,11 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
   const int rg = cw / NWK, wk = cw - rg * NWK;
   const int g = lane >> 2;
   const int u0 = wk * KU;  // first unit of this warp's K-slice
+
+  // X (and Y) may belong to the previous kernel on the stream: wait for it
+  // to complete (a no-op without programmatic dependent launch).  The
+  // producer above does not wait -- it only reads the weight.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- X for this warp's K-slice: lane's 32 elements per unit
   uint32_t xb[KU][16];
@@ -408,7 +418,18 @@ cudaError_t launch_m1(const M1Args &a, const M1Plan &p, int grid, cudaStream_t s
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, p.threads, p.smem, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
