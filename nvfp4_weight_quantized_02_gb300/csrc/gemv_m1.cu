@@ -363,197 +363,6 @@ __global__ void __launch_bounds__(kProducer + 32 * max_consumer_warps(KU), 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// Row-owner variant for K <= 5120 (up to 5 units): every consumer warp keeps
-// X for the whole of K in registers and computes whole row pairs, so there
-// is no cross-warp reduction and no barrier among consumers.  Pairs of the
-// CTA's row range are dealt round-robin to warps (warp w: pairs w, w+NW,
-// ...), two at a time; a stage of RS rows holds RS/2 pairs and is released
-// when each of its pairs has arrived once on its empty barrier.
-// ---------------------------------------------------------------------------
-constexpr int kRowsWarps = 12;  // consumer warps of the row-owner kernel
-
-struct RowsArgs {
-  const uint16_t *x;
-  const uint8_t *codes;
-  const uint8_t *scales;
-  const float *tensor_scale;
-  uint16_t *y;
-  int64_t N, K;
-  int32_t *status;
-  int rows_per_stage;  // RS (even)
-  int nstages;         // NS
-  uint32_t stage_bytes, codes_stage_bytes;
-};
-
-template <int KU>
-__global__ void __launch_bounds__(kProducer + 32 * kRowsWarps, 1)
-    gemv_m1_rows_kernel(const RowsArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int NS = a.nstages, RS = a.rows_per_stage, PPS = RS / 2;
-  const int64_t KH = a.K / 2, KB = a.K / 16;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-  uint64_t *empty = full + kMaxStages;
-  uint8_t *stages = smem + kHeadBytes;
-
-  const int64_t G = gridDim.x;
-  const int64_t row_begin = a.N * (int64_t)blockIdx.x / G;
-  const int64_t row_end = a.N * ((int64_t)blockIdx.x + 1) / G;
-  const int64_t n_rows = row_end - row_begin;
-  const int64_t n_st = ceil_div(n_rows, RS);
-  const int64_t n_pairs = ceil_div(n_rows, 2);
-
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PPS);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (threadIdx.x < kProducer) {
-    if (threadIdx.x != 0) return;
-    int64_t issued = 0;
-    bool ok = true;
-    for (int64_t i = 0; i < n_st; ++i) {
-      const int s = (int)(i % NS);
-      if (i >= NS && !mbar_wait_bounded(&empty[s], (uint32_t)(((i / NS) - 1) & 1), a.status)) {
-        ok = false;
-        break;
-      }
-      const int64_t r0 = row_begin + i * RS;
-      const int64_t rows_i = min((int64_t)RS, row_end - r0);
-      const uint32_t cbytes = (uint32_t)(rows_i * KH);
-      const uint32_t sbytes = (uint32_t)(rows_i * KB);
-      uint8_t *st = stages + (size_t)s * a.stage_bytes;
-      mbar_arrive_expect_tx(&full[s], cbytes + sbytes);
-      bulk_g2s(st, a.codes + r0 * KH, cbytes, &full[s]);
-      bulk_g2s(st + a.codes_stage_bytes, a.scales + r0 * KB, sbytes, &full[s]);
-      ++issued;
-    }
-    if (!ok) {
-      for (int64_t i = (issued > NS ? issued - NS : 0); i < issued; ++i)
-        mbar_wait_bounded(&full[i % NS], (uint32_t)((i / NS) & 1), a.status);
-    }
-    return;
-  }
-
-  const int w = (threadIdx.x - kProducer) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;
-  const int dsel = g & 1;
-
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // X for all of K, this lane's 32 elements of every unit, as f16 scaled by
-  // one power of two (max|x| in [2^14, 2^15)); every warp holds all of X.
-  uint32_t xb[KU][16];
-  uint32_t mx = 0;
-#pragma unroll
-  for (int j = 0; j < KU; ++j) {
-    const int64_t k0 = (int64_t)j * kUnitK + 32 * lane;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) xb[j][i] = 0u;
-    if (k0 < a.K) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(a.x + k0);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const uint4 q = __ldg(src + v);
-        xb[j][4 * v] = q.x; xb[j][4 * v + 1] = q.y; xb[j][4 * v + 2] = q.z; xb[j][4 * v + 3] = q.w;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mx = __vmaxu2(mx, xb[j][i] & 0x7FFF7FFFu);
-  }
-  mx = max(mx & 0xFFFFu, mx >> 16);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  const float xmax = __uint_as_float(mx << 16);
-  int sh = 0;
-  if (xmax > 0.0f && xmax < __int_as_float(0x7F800000)) {
-    int e;
-    frexpf(xmax, &e);
-    sh = 15 - e;
-  }
-#pragma unroll
-  for (int j = 0; j < KU; ++j)
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      xb[j][i] = f16x2_pack(ldexpf(bf16_bits_to_f32(xb[j][i] & 0xFFFFu), sh),
-                            ldexpf(bf16_bits_to_f32(xb[j][i] >> 16), sh));
-  const float out_scale = ldexpf(1.0f, -sh) * *a.tensor_scale;
-  // blocks of this lane in unit j: 64 j + 2 lane (+1)
-  const int64_t lane_codes = 16 * lane, lane_scales = 2 * lane;
-
-  for (int64_t p0 = w; p0 < n_pairs; p0 += 2 * kRowsWarps) {
-    const int64_t p1 = p0 + kRowsWarps;
-    const bool two = p1 < n_pairs;
-    const int64_t pr[2] = {p0, two ? p1 : p0};
-    int slot[2];
-    bool ready = true;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int64_t stg = pr[q] / PPS;
-      slot[q] = (int)(stg % NS);
-      if (q == 0 || two)
-        ready = ready && mbar_wait_bounded(&full[slot[q]], (uint32_t)((stg / NS) & 1), a.status);
-    }
-    if (!__all_sync(0xFFFFFFFFu, ready)) return;  // a timed-out wait: status is set
-    float d[2][2][4] = {};
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int rr = (int)(pr[q] % PPS) * 2;  // row of the pair inside its stage
-      const uint8_t *st = stages + (size_t)slot[q] * a.stage_bytes;
-      const uint8_t *c = st + rr * KH + lane_codes;
-      const uint8_t *sp = st + a.codes_stage_bytes + rr * KB + lane_scales;
-#pragma unroll
-      for (int j = 0; j < KU; ++j) {
-        if ((int64_t)j * kUnitK + 32 * lane < a.K) {
-          const uint4 cw0 = *reinterpret_cast<const uint4 *>(c + j * (kUnitK / 2));
-          const uint4 cw1 = *reinterpret_cast<const uint4 *>(c + KH + j * (kUnitK / 2));
-          const uint32_t sc0 = *reinterpret_cast<const uint16_t *>(sp + j * (kUnitK / 16));
-          const uint32_t sc1 = *reinterpret_cast<const uint16_t *>(sp + KB + j * (kUnitK / 16));
-          unit_mma(d[q][0], d[q][1], cw0, cw1, sc0, sc1, xb[j]);
-        } else {
-          unit_mma(d[q][0], d[q][1], make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), 0u, 0u,
-                   xb[j]);
-        }
-      }
-    }
-    // D[g][g] (row 2p) and D[g+8][g] (row 2p+1) live in lanes 9j and 9j + 4;
-    // XOR 4, 9, 18 gathers those eight lanes into lane 0.
-    float v[4];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      v[2 * q] = dsel ? d[q][0][1] + d[q][1][1] : d[q][0][0] + d[q][1][0];
-      v[2 * q + 1] = dsel ? d[q][0][3] + d[q][1][3] : d[q][0][2] + d[q][1][2];
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v[q] += __shfl_xor_sync(0xFFFFFFFFu, v[q], 4);
-      v[q] += __shfl_xor_sync(0xFFFFFFFFu, v[q], 9);
-      v[q] += __shfl_xor_sync(0xFFFFFFFFu, v[q], 18);
-    }
-    __syncwarp();
-    if (lane == 0) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        if (q == 1 && !two) break;
-        const int64_t r = row_begin + 2 * pr[q];
-        a.y[r] = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * q] * out_scale));
-        if (r + 1 < row_end)
-          a.y[r + 1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * q + 1] * out_scale));
-        // release this pair's share of its stage; the last pair of a short
-        // last stage also releases the pairs that stage does not have
-        int arrivals = 1;
-        if (pr[q] == n_pairs - 1) arrivals += (int)(PPS - (n_pairs - (n_pairs - 1) / PPS * PPS));
-        for (int i = 0; i < arrivals; ++i) mbar_arrive(&empty[slot[q]]);
-      }
-    }
-  }
-}
-
 struct M1Plan {
   int KU, NWK, RG, RS, RB, NS, threads, scales_bulk;
   uint32_t stage_bytes, codes_stage_bytes;
@@ -624,57 +433,6 @@ cudaError_t launch_m1(const M1Args &a, const M1Plan &p, int grid, cudaStream_t s
   return cudaGetLastError();
 }
 
-struct RowsPlan {
-  int KU, RS, NS, threads;
-  uint32_t stage_bytes, codes_stage_bytes;
-  size_t smem;
-};
-
-bool make_rows_plan(int64_t N, int64_t K, RowsPlan &p) {
-  const int n_units = (int)ceil_div(K, kUnitK);
-  if (n_units > 5 || K % 256) return false;  // 6 units spill registers
-  p.KU = n_units;
-  p.threads = kProducer + 32 * kRowsWarps;
-  const int64_t row_bytes = K / 2 + K / 16;
-  int64_t RS = 2;
-  while ((RS * 2) * row_bytes <= 48 * 1024 && RS < 128) RS *= 2;
-  const int64_t rows_per_cta = ceil_div(N, num_sms());
-  const int64_t cap = 2 * ceil_div(rows_per_cta, 2);
-  if (RS > cap) RS = cap < 2 ? 2 : cap;
-  p.RS = (int)RS;
-  p.codes_stage_bytes = (uint32_t)(ceil_div(RS * (K / 2), 128) * 128);
-  p.stage_bytes = p.codes_stage_bytes + (uint32_t)(ceil_div(RS * (K / 16), 128) * 128);
-  int NS = kMaxStages;
-  while (NS > 2 && kHeadBytes + (size_t)NS * p.stage_bytes > kSmemBudget) --NS;
-  // pairs a warp holds at once (two, kRowsWarps apart) must fit in the ring
-  const int64_t pps = RS / 2;
-  if ((kRowsWarps + pps - 1) / pps + 1 >= NS) return false;
-  p.NS = NS;
-  p.smem = kHeadBytes + (size_t)NS * p.stage_bytes;
-  return p.smem <= 227 * 1024;
-}
-
-template <int KU>
-cudaError_t launch_rows(const RowsArgs &a, const RowsPlan &p, int grid, cudaStream_t stream) {
-  auto kern = gemv_m1_rows_kernel<KU>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(p.threads);
-  cfg.dynamicSmemBytes = p.smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, a);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 bool gemv_m1_supported(int64_t N, int64_t K) {
@@ -685,31 +443,6 @@ bool gemv_m1_supported(int64_t N, int64_t K) {
 cudaError_t launch_gemv_m1(const uint16_t *x, int64_t K, const uint8_t *codes,
                            const uint8_t *scales, const float *tensor_scale, int64_t N,
                            uint16_t *y, int32_t *status, cudaStream_t stream) {
-  int64_t grid0 = num_sms();
-  if (grid0 > N) grid0 = N;
-  RowsPlan rp;
-  if (make_rows_plan(N, K, rp)) {
-    RowsArgs ra;
-    ra.x = x;
-    ra.codes = codes;
-    ra.scales = scales;
-    ra.tensor_scale = tensor_scale;
-    ra.y = y;
-    ra.N = N;
-    ra.K = K;
-    ra.status = status;
-    ra.rows_per_stage = rp.RS;
-    ra.nstages = rp.NS;
-    ra.stage_bytes = rp.stage_bytes;
-    ra.codes_stage_bytes = rp.codes_stage_bytes;
-    switch (rp.KU) {
-      case 1: return launch_rows<1>(ra, rp, (int)grid0, stream);
-      case 2: return launch_rows<2>(ra, rp, (int)grid0, stream);
-      case 3: return launch_rows<3>(ra, rp, (int)grid0, stream);
-      case 4: return launch_rows<4>(ra, rp, (int)grid0, stream);
-      case 5: return launch_rows<5>(ra, rp, (int)grid0, stream);
-    }
-  }
   M1Plan p;
   if (!make_m1_plan(N, K, p)) return cudaErrorInvalidConfiguration;
   M1Args a;
