@@ -283,7 +283,7 @@ def run_native(args):
     top = int(np.argmax(per_kernel_ms))
     top_bytes = lins[top].weight_bytes + 2 * lins[top].K + 2 * lins[top].N
     achieved = top_bytes / (per_kernel_ms[top] * 1e-3) / 1e9
-    traffic = load_traffic("gemv_m1_kernel", lins[top])
+    traffic = load_traffic("gemv_tc_kernel", lins[top])
 
     extra = {}
     if rank == 0 and not args.no_extra:
@@ -301,7 +301,7 @@ def run_native(args):
         "per_kernel_us": {l.name: 1e3 * t for l, t in zip(lins, per_kernel_ms)},
         "per_kernel_gbs": {l.name: (l.weight_bytes + 2 * l.K + 2 * l.N) / (t * 1e-3) / 1e9
                            for l, t in zip(lins, per_kernel_ms)},
-        "roofline": {"bound": "hbm", "kernel": f"gemv_m1_kernel ({lins[top].name} "
+        "roofline": {"bound": "hbm", "kernel": f"gemv_tc_kernel ({lins[top].name} "
                      f"{lins[top].K}x{lins[top].N})", "achieved": achieved, "peak": hbm_peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic},

@@ -354,7 +354,7 @@ int pass_tile(int64_t M_left, int64_t N, int64_t K, Plan &p) {
 
 bool gemv_supported(int64_t M, int64_t N, int64_t K) {
   if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return false;
-  if (M == 1 && gemv_m1_supported(N, K)) return true;
+  if (gemv_tc_supported(M, N, K)) return true;
   for (int64_t m0 = 0; m0 < M;) {
     Plan p;
     const int MT = pass_tile(M - m0, N, K, p);
@@ -367,8 +367,8 @@ bool gemv_supported(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_gemv(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const uint8_t *codes,
                         const uint8_t *scales, const float *tensor_scale, int64_t N, uint16_t *y,
                         int64_t ldy, int32_t *status, cudaStream_t stream) {
-  if (M == 1 && gemv_m1_supported(N, K))
-    return launch_gemv_m1(x, K, codes, scales, tensor_scale, N, y, status, stream);
+  if (gemv_tc_supported(M, N, K))
+    return launch_gemv_tc(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status, stream);
   for (int64_t m0 = 0; m0 < M;) {
     Plan p;
     const int MT = pass_tile(M - m0, N, K, p);

@@ -17,10 +17,12 @@ cudaError_t launch_gemv(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, co
                         const uint8_t *scales, const float *tensor_scale, int64_t N, uint16_t *y,
                         int64_t ldy, int32_t *status, cudaStream_t stream);
 
-// The M = 1 tensor-core GEMV (gemv_m1.cu).
-bool gemv_m1_supported(int64_t N, int64_t K);
-cudaError_t launch_gemv_m1(const uint16_t *x, int64_t K, const uint8_t *codes,
-                           const uint8_t *scales, const float *tensor_scale, int64_t N,
-                           uint16_t *y, int32_t *status, cudaStream_t stream);
+// The tensor-core GEMV (gemv_tc.cu): passes of 1, 2, 4 or 8 rows of X,
+// each one stream of W.
+bool gemv_tc_supported(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemv_tc(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                           const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
+                           int64_t N, uint16_t *y, int64_t ldy, int32_t *status,
+                           cudaStream_t stream);
 
 }  // namespace impfp4

@@ -69,7 +69,13 @@ def test_full_size_sampled(lin):
     (1, 64, 1, 64, 8), (1, 64, 7, 72, 16), (1, 320, 333, 320, 336), (2, 192, 50, 200, 56),
     (3, 1024, 1000, 1024, 1000), (5, 2048, 77, 2056, 80), (7, 448, 9, 448, 16),
     (16, 64, 300, 64, 304), (9, 5120, 129, 5120, 136), (1, 17408, 5, 17408, 8),
-    (16, 1024, 2, 1024, 8), (1, 4096, 152, 4096, 152), (1, 4096, 153, 4096, 160)])
+    (16, 1024, 2, 1024, 8), (1, 4096, 152, 4096, 152), (1, 4096, 153, 4096, 160),
+    # tensor-core tiles of 2, 4 and 8 rows of X: several units per warp,
+    # partial last units (K % (128 * 8 / MT) != 0), scales read from global
+    # memory (K % 256 != 0), several passes with inactive rows
+    (8, 5120, 333, 5120, 336), (6, 3072, 200, 3080, 200), (8, 192, 70, 192, 72),
+    (4, 17408, 100, 17408, 104), (11, 2304, 97, 2304, 104), (13, 1088, 40, 1088, 40),
+    (2, 320, 19, 320, 24), (4, 576, 1500, 576, 1504)])
 def test_edge_shapes(M, K, N, ldx, ldy):
     lin = synth.Linear("edge", M, K, N, 123, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
                        zero_block_p=0.02, x_outlier_frac=0.02)
@@ -93,6 +99,21 @@ def test_extreme_activation_magnitudes():
         y_ref, bound = oracle.reference_gemm(xb, 1, c, s, ts)
         if exp <= 120 - 10:
             check_within_tolerance(y, y_ref, bound, f"x ~ 2^{exp}")
+
+
+@pytest.mark.parametrize("M", [2, 4, 8, 12])
+def test_extreme_activation_magnitudes_per_row(M):
+    # Rows of X of very different magnitude in one call: each row keeps its
+    # own power-of-two staging factor.
+    lin = synth.Linear("mag", M, 2048, 96, 6)
+    c, s, ts = oracle_w(lin)
+    rng = np.random.default_rng(M)
+    exps = [(-130, -60, -20, 0, 20, 60, 100)[i % 7] for i in range(M)]
+    xf = np.stack([rng.standard_normal(2048) * 2.0 ** e for e in exps]).astype(np.float32)
+    xb = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    y = run_gemm(xb, dev_nvfp4(c, s, ts))
+    y_ref, bound = oracle.reference_gemm(xb, M, c, s, ts)
+    check_within_tolerance(y, y_ref, bound, f"M{M} rows ~ 2^{exps}")
 
 
 def test_bitwise_repeatable():
