@@ -112,7 +112,8 @@ imp_status imp_nvfp4_quantize_noalloc(const void *x_bf16, int64_t rows, int64_t 
 
 size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0 || K % 64) return 0;
-  if (M <= kDecodeMaxM) return 0;
+  if (M <= kDecodeMaxM)
+    return impfp4::gemv_f4_shape_ok(M, N, K) ? impfp4::gemv_f4_workspace_bytes(M, N, K) : 0;
   return prefill_ws(M, N, K).total;
 }
 
@@ -189,9 +190,11 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= kDecodeMaxM) {
     if (!impfp4::gemv_supported(M, N, K)) return IMP_ERR_UNSUPPORTED_SHAPE;
+    if (need && !aligned16(workspace)) return IMP_ERR_MISALIGNED;
     return from_cuda(impfp4::launch_gemv(static_cast<const uint16_t *>(x_bf16), M, K, ldx,
                                          w->codes, w->scales, w->tensor_scale, N,
-                                         static_cast<uint16_t *>(y_bf16), ldy, dev_status, s));
+                                         static_cast<uint16_t *>(y_bf16), ldy, dev_status,
+                                         need ? workspace : nullptr, s));
   }
   // Prefill: quantize X (scales straight into the atom layout), lay W's
   // scales out as atoms, then the block-scaled FP4 tensor-core GEMM.

@@ -366,7 +366,10 @@ bool gemv_supported(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_gemv(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const uint8_t *codes,
                         const uint8_t *scales, const float *tensor_scale, int64_t N, uint16_t *y,
-                        int64_t ldy, int32_t *status, cudaStream_t stream) {
+                        int64_t ldy, int32_t *status, void *workspace, cudaStream_t stream) {
+  if (workspace && gemv_f4_supported(M, N, K, codes, scales))
+    return launch_gemv_f4(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status, workspace,
+                          stream);
   if (gemv_tc_supported(M, N, K))
     return launch_gemv_tc(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status, stream);
   for (int64_t m0 = 0; m0 < M;) {

@@ -13,9 +13,12 @@ bool gemv_supported(int64_t M, int64_t N, int64_t K);
 
 // Enqueue Y[M][N] = X[M][K] * W^T (bf16 X and Y, NVFP4 W) on `stream`.
 // Arguments are validated by the caller.  1 <= M <= 16, N >= 1, K % 64 == 0.
+// `workspace` (gemv_f4_workspace_bytes, 16-byte aligned) enables the FP4
+// tensor-core path for the shapes gemv_f4_shape_ok accepts; nullptr selects
+// the f16 tensor-core / CUDA-core paths.
 cudaError_t launch_gemv(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const uint8_t *codes,
                         const uint8_t *scales, const float *tensor_scale, int64_t N, uint16_t *y,
-                        int64_t ldy, int32_t *status, cudaStream_t stream);
+                        int64_t ldy, int32_t *status, void *workspace, cudaStream_t stream);
 
 // The tensor-core GEMV (gemv_tc.cu): passes of 1, 2, 4 or 8 rows of X,
 // each one stream of W.
@@ -23,6 +26,17 @@ bool gemv_tc_supported(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemv_tc(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status,
+                           cudaStream_t stream);
+
+// The block-scaled FP4 tensor-core GEMV (gemv_f4.cu): X split into NVFP4
+// components per call (needs a workspace), W streamed straight into
+// tcgen05.mma.kind::mxf4nvf4.  Passes of up to 4 rows of X.
+bool gemv_f4_shape_ok(int64_t M, int64_t N, int64_t K);
+size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K);
+bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const void *scales);
+cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                           const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
+                           int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
                            cudaStream_t stream);
 
 }  // namespace impfp4

@@ -1,0 +1,1109 @@
+// Decode GEMV (M <= 16) with the NVFP4 weight fed straight to the
+// block-scaled FP4 tensor cores:
+//   y[m][n] = s_w * sum_k x[m][k] * e2m1(c[n][k]) * e4m3(sb[n][k/16]).
+//
+// Decode is bandwidth-bound (imp README, "How it works"; "1. The big
+// picture", section "The most important number in this book"), so the aim
+// is to move W from HBM into the tensor cores with no per-weight work on the
+// CUDA cores at all.  tcgen05.mma.kind::mxf4nvf4 multiplies E2M1 codes with
+// E4M3 scales per 16 elements on both operands, exactly the weight format.
+// X, in bf16, is not: it is rewritten per call as a short sum of NVFP4
+// "components" (one extra operand row per component), the MMA's B operand:
+//
+//   x * 2^sh = sum_{c < 8} 2^(4 - 2c) * e4m3(sb_c[b]) * e2m1(q_c[k]),
+//
+// with the power-of-two prescale 2^sh putting the row's max|x| in
+// [2^14, 2^15) and component c quantizing the residual left by components
+// 0..c-1 (block amax / 6 -> E4M3 scale; value / scale -> E2M1, nearest).
+// Each component shrinks a block's residual by a factor of at least ~5.6,
+// so eight of them leave less than ~1e-9 of the block's largest |x| (fp32
+// rounding of the residual updates dominates).  Every MMA product
+// (E2M1 x E4M3 x E2M1 x E4M3) is exact; accumulation is fp32 in tensor
+// memory.  y sums the component columns with their power-of-two weights, in
+// a fixed order.
+//
+// Work split ("stream-K"): the (128-row tile, 256-element K chunk) sequence,
+// tile-major, is cut into gridDim.x equal contiguous ranges, one per CTA (one
+// CTA per SM).  A CTA's range covers whole tiles and at most two partial ones
+// ("segments"); a partial tile's CTAs leave fp32 partial sums in the
+// workspace and the last of them to finish adds them in K order.
+//
+// Two kernels share that scheme:
+//  * gemv_f4r_kernel (M <= 2, the usual decode case): everything in one
+//    launch.  Warp 3 streams W (codes: 128 rows x 128 B tiles, 128-byte
+//    swizzle; scales: 128 rows x 16 B) through a 6-deep ring with TMA and
+//    never waits for the previous kernel (W is never written on the
+//    stream).  Meanwhile warps 4..11 wait for it and split the K chunks of
+//    X this CTA needs into components directly in shared memory (B operand,
+//    swizzled, and its scale atoms), publishing each chunk as soon as it is
+//    split; warps 0..2 issue the MMAs (stage i -> issuer i % 3) as chunks
+//    become ready, and warps 8..11 go on to the epilogue.
+//  * gemv_f4_kernel (M = 3..16, passes of up to four rows of X): a separate
+//    split kernel (xsplit_kernel) writes the components and scale atoms to
+//    the workspace, and they travel with W in each stage of an 8-deep ring;
+//    four MMA issuers (warps 0..3), producer warp 4, epilogue warps 8..11.
+// Issuer: its warp relays the stage's W scales into 512-byte atoms; one
+// thread copies both operands' atoms to tensor memory (tcgen05.cp) and issues
+// four M=128 x N=N_MMA x K=64 MMAs into its own accumulator.  One issuing
+// thread sustains one MMA per ~130 cycles; three or four keep the tensor core
+// ahead of HBM.  Epilogue: thread = tile row (its tensor-memory lane).
+// Every wait is bounded; on a timeout the kernel reports IMP_DEV_TIMEOUT,
+// drains its own copies and MMAs, frees tensor memory and returns.
+#include <atomic>
+#include <chrono>
+#include <mutex>
+#include <random>
+
+#include "gemv.cuh"
+#include "tma.cuh"
+
+namespace impfp4 {
+
+namespace {
+
+constexpr int kNC = 8;          // components per row of X
+constexpr int kTileRows = 128;
+constexpr int kChunkK = 256;    // K per stage (four K64 MMAs)
+constexpr uint32_t kTmemCols = 512;
+constexpr int kXsplitThreads = 256;
+constexpr int kPrefetch = 12;   // stages of W prefetched into L2 at the start
+constexpr int kEpiWarp0 = 8;    // warps 8..11: epilogue (tensor-memory lane quarters 0..3)
+constexpr int kThreads = 384;
+// The split-tile partials are sized for at most kMaxGrid CTAs, so the
+// workspace size does not depend on the device.
+constexpr int kMaxGrid = 256;
+
+// ---- streamed-B kernel (M = 3..16)
+constexpr int kIssuersS = 4, kProducerS = 4, kNSS = 8;  // stage st and st - 8: same issuer
+template <int NMMA> struct StageS {
+  static constexpr uint32_t W = 0;                 // 128 x 128 B, swizzled
+  static constexpr uint32_t B = 16384;             // NMMA x 128 B, swizzled
+  static constexpr uint32_t RAW = B + 128 * NMMA;  // W scales, 128 x 16 B
+  static constexpr uint32_t SFA = RAW + 2048;      // 4 atoms
+  static constexpr uint32_t SFB = SFA + 2048;      // 4 atoms
+  static constexpr uint32_t BYTES = SFB + 2048;    // multiple of 1024
+  static constexpr uint32_t TX = 16384 + 128 * NMMA + 2048 + 2048;
+};
+
+// ---- resident-B kernel (M <= 2, N_MMA = 16)
+constexpr int kIssuersR = 3, kProducerR = 3, kNSR = 6;  // stage st and st - 6: same issuer
+constexpr int kMaxSlotsR = 24;                           // K chunks of X held per CTA
+constexpr int kHelperWarp0R = 4;                         // warps 4..11 split X
+constexpr int kHelperThreadsR = kThreads - 32 * kHelperWarp0R;
+struct StageR {
+  static constexpr uint32_t W = 0, RAW = 16384, SFA = RAW + 2048, BYTES = SFA + 2048;
+  static constexpr uint32_t TX = 16384 + 2048;
+};
+// B slot q: codes at BCODES + 2048 q (16 rows x 128 B, swizzled); the scale
+// atoms of its four K64 steps at BSF + 2048 q + 512 t.
+
+struct F4Args {
+  const uint16_t *x;    // resident kernel: X rows
+  int64_t ldx;
+  uint16_t *y;
+  int64_t ldy;
+  int M;
+  int64_t N, K;
+  const float *tensor_scale;
+  const uint8_t *sfb;   // streamed kernel: X component scale atoms, [K/64][512]
+  const int32_t *sh;    // streamed kernel: per-row prescale exponents
+  float *part;          // split-tile partial sums, [CTA][first/last segment][4][128]
+  unsigned __int128 *cnt;   // per tile: epoch, its check word and segments finished
+  int32_t *status;
+  int n_tiles;
+  int n_chunks;         // K / 256
+  unsigned long long epoch;  // unique per launch
+  int n_slots;          // resident kernel: B slots in shared memory
+};
+
+struct F4Bars {
+  uint64_t full[8], empty[8];
+  uint64_t d_full[4][2], d_empty[2];
+  uint64_t drain[4];
+  uint64_t part_done, flag_ready;  // split-tile hand-off among the epilogue warps
+  uint64_t b_ready[32];            // resident kernel: B slot q split and visible
+  uint32_t tmem;
+  int last;
+  uint32_t xmax[2];
+};
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                          uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)(layout & 7u) << 61;
+  return d;
+}
+constexpr uint32_t kSw128 = 2, kNoSwizzle = 0;
+
+template <int NMMA>
+__host__ __device__ constexpr uint32_t idesc_f4() {
+  // kind::mxf4nvf4: A and B E2M1 (format 1), K-major, N >> 3 at bit 17, M >> 4 at bit 24
+  return (1u << 7) | (1u << 10) | ((uint32_t)(NMMA >> 3) << 17) |
+         ((uint32_t)(kTileRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc_) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc_)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%5], [%6], p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(kTmemCols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free(uint32_t tmem) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+               : "memory");
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) { return f16lo_to_f32(e4m3x2_to_f16x2(b)); }
+
+// ---- the split of X ----------------------------------------------------------
+
+// Power-of-two prescale putting max|x| (bf16 bits of the magnitude) in
+// [2^14, 2^15); 0 for an all-zero or non-finite row.
+__device__ __forceinline__ int prescale_exponent(uint32_t mx_bits16) {
+  const float xmax = __uint_as_float(mx_bits16 << 16);
+  if (!(xmax > 0.0f && xmax < __int_as_float(0x7F800000))) return 0;
+  int e;
+  frexpf(xmax, &e);
+  return 15 - e;
+}
+
+__device__ __forceinline__ uint32_t absmax_bf16x8(const uint4 v) {
+  return max(max(max(v.x & 0x7FFFu, v.x >> 16 & 0x7FFFu), max(v.y & 0x7FFFu, v.y >> 16 & 0x7FFFu)),
+             max(max(v.z & 0x7FFFu, v.z >> 16 & 0x7FFFu), max(v.w & 0x7FFFu, v.w >> 16 & 0x7FFFu)));
+}
+
+// One 16-element block of X (16 bf16 in v, element order) -> eight
+// components: code[c] = 16 E2M1 codes (element 2i in the low nibble of byte
+// i), sb[c] = the E4M3 block scale in units of 2^(4 - 2c).
+__device__ __forceinline__ float pow2f(int e) {  // 2^e, -126 <= e <= 127
+  return __int_as_float((127 + e) << 23);
+}
+
+__device__ __forceinline__ void split_block_regs(const uint4 (&v)[2], int sh, uint2 (&code)[kNC],
+                                                 uint32_t (&sb)[kNC]) {
+  // x * 2^sh as two exact power-of-two products (|sh| may exceed 127)
+  const float p1 = pow2f(sh / 2), p2 = pow2f(sh - sh / 2);
+  float r[16];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t w[4] = {v[h].x, v[h].y, v[h].z, v[h].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      r[8 * h + 2 * t] = bf16_bits_to_f32(w[t] & 0xFFFFu) * p1 * p2;
+      r[8 * h + 2 * t + 1] = bf16_bits_to_f32(w[t] >> 16) * p1 * p2;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < kNC; ++c) {
+    float m8[8];  // |r| max as a tree
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m8[k] = fmaxf(fabsf(r[k]), fabsf(r[k + 8]));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
+    const float amax = fmaxf(fmaxf(m8[0], m8[2]), fmaxf(m8[1], m8[3]));
+    // Any scale is valid -- the residual tracks what was taken -- so a
+    // reciprocal stands in for the divisions.
+    sb[c] = f32_to_e4m3_satfinite(amax * (1.0f / 6.0f) * pow2f(2 * c - 4));
+    const float d = e4m3_to_f32(sb[c]) * pow2f(4 - 2 * c);
+    uint32_t cw[2] = {0u, 0u};
+    if (d > 0.0f) {
+      const float inv = 1.0f / d;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float q[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = r[8 * h + k] * inv;
+        cw[h] = f32x8_to_e2m1_packed(q);
+        uint32_t e[4];
+        e2m1x8_to_f16x2x4(cw[h], e);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          // e2m1 * d is exact in fp32; one rounding in the subtraction
+          r[8 * h + 2 * t] = fmaf(-f16lo_to_f32(e[t]), d, r[8 * h + 2 * t]);
+          r[8 * h + 2 * t + 1] = fmaf(-f16hi_to_f32(e[t]), d, r[8 * h + 2 * t + 1]);
+        }
+      }
+    }
+    code[c] = make_uint2(cw[0], cw[1]);
+  }
+}
+
+// The same for a block read from p (bf16, 16-byte aligned).
+__device__ __forceinline__ void split_block(const uint16_t *p, int sh, uint2 (&code)[kNC],
+                                            uint32_t (&sb)[kNC]) {
+  const uint4 v[2] = {__ldg(reinterpret_cast<const uint4 *>(p)),
+                      __ldg(reinterpret_cast<const uint4 *>(p) + 1)};
+  split_block_regs(v, sh, code, sb);
+}
+
+// ---- stream-K bookkeeping -----------------------------------------------------
+
+struct StreamK {
+  int64_t total, g_begin, g_end;
+  int nch, n_st, n_seg, G;
+  __device__ StreamK(int n_tiles, int n_chunks) {
+    G = gridDim.x;
+    nch = n_chunks;
+    total = (int64_t)n_tiles * nch;
+    g_begin = total * blockIdx.x / G;
+    g_end = total * (blockIdx.x + 1) / G;
+    n_st = (int)(g_end - g_begin);
+    n_seg = n_st > 0 ? (int)((g_end - 1) / nch - g_begin / nch) + 1 : 0;
+  }
+  __device__ int seg_begin(int j) const {  // first stage of local segment j
+    const int64_t g0 = (g_begin / nch + j) * nch;
+    return (int)((g0 > g_begin ? g0 : g_begin) - g_begin);
+  }
+  __device__ int seg_end(int j) const { return j + 1 < n_seg ? seg_begin(j + 1) : n_st; }
+  // Processing order: the first segment, then the last, then the middle ones
+  // (whole tiles), so a CTA's split tiles finish early and their fix-ups
+  // overlap whole-tile work.  jj: processing position of a segment; i: of a
+  // stage.
+  __device__ int proc_seg(int jj) const { return jj == 0 ? 0 : jj == 1 ? n_seg - 1 : jj - 1; }
+  __device__ int pbegin(int jj) const {
+    if (jj == 0) return 0;
+    const int e0 = seg_end(0);
+    if (jj == 1) return e0;
+    return n_st - seg_begin(n_seg - 1) + seg_begin(jj - 1);
+  }
+  __device__ int pend(int jj) const {
+    const int j = proc_seg(jj);
+    return pbegin(jj) + seg_end(j) - seg_begin(j);
+  }
+  __device__ int stage_of(int i) const {
+    if (n_seg < 2) return i;
+    const int e0 = seg_end(0), sl = seg_begin(n_seg - 1), nl = n_st - sl;
+    return i < e0 ? i : i < e0 + nl ? sl + (i - e0) : i - nl;
+  }
+  // CTA owning global chunk g
+  __device__ int owner(int64_t g) const { return (int)(((g + 1) * G - 1) / total); }
+};
+
+// Counts one finished segment of a split tile; true for the tile's last.
+// A counter is 16 bytes: the launch's epoch (64 bits), a check word derived
+// from it (32 bits) and the count.  A value that does not carry this
+// launch's epoch and check -- an earlier launch's, or whatever the workspace
+// held before (a 2^-96 chance of a false match) -- counts as zero, so no
+// call has to clear the counters; the last CTA of a tile still leaves zero,
+// the first guess of the next launch.  Epochs start at a random value per
+// process and grow by one per launch.
+__device__ __forceinline__ bool count_segment(unsigned __int128 *c, unsigned long long epoch,
+                                              int nslot) {
+  const unsigned long long chk = (epoch * 0x9E3779B97F4A7C15ull) >> 32;
+  unsigned __int128 old = 0;  // the tile's last CTA of each launch leaves zero
+  while (true) {
+    const unsigned long long hi = (unsigned long long)(old >> 64), lo = (unsigned long long)old;
+    const unsigned long long cnt = (hi == epoch && (lo >> 32) == chk) ? (lo & 0xFFFFFFFFull) + 1 : 1;
+    const unsigned __int128 nv = ((unsigned __int128)epoch << 64) | ((chk << 32) | cnt);
+    const unsigned __int128 prev = atomicCAS(c, old, nv);
+    if (prev == old) {
+      if ((int)cnt != nslot) return false;
+      __stcg(reinterpret_cast<uint4 *>(c), make_uint4(0, 0, 0, 0));  // for the next launch
+      return true;
+    }
+    old = prev;  // not what was guessed: at most nslot + 1 rounds
+  }
+}
+
+// ---- issuer and epilogue loops, shared by both kernels ------------------------
+
+// Issuer `is` of NI: stages (in processing order) i = is, is + NI, ...  The
+// warp relays the W scales of each stage into atoms; lane 0 copies both
+// operands' atoms and issues the MMAs.  `b_desc(i, st, t)` /
+// `sfb_desc(i, st, t)`: the B operand and its scale atom for K64 step t of
+// processing position i (stage st); `b_wait(st)`: waits (bounded) until that
+// B is in shared memory.
+template <int NI, int NS, int NMMA, class Stage, class BDesc, class SFBDesc, class BWait>
+__device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const StreamK &sk,
+                            int is, int lane, int32_t *status, BDesc b_desc, SFBDesc sfb_desc,
+                            BWait b_wait) {
+  constexpr uint32_t kIdesc = idesc_f4<NMMA>();
+  constexpr uint32_t kSF0 = 2 * NI * NMMA;  // scale columns after the accumulators
+  const uint32_t sbase = smem_u32(smem);
+  const uint64_t dA0 = sdesc(sbase + Stage::W, 16, 1024, kSw128);
+  const uint64_t dSA0 = sdesc(sbase + Stage::SFA, 0, 128, kNoSwizzle);
+  bool ok = true;
+  for (int jj = 0; jj < sk.n_seg && ok; ++jj) {
+    const int p0 = sk.pbegin(jj), p1 = sk.pend(jj);
+    const int d = jj & 1;
+    const int first = p0 + ((is - p0) % NI + NI) % NI;  // this issuer's first stage
+    for (int i = first; i < p1; i += NI) {
+      const int s = i % NS, st = sk.stage_of(i);
+      if (i == first && jj >= 2 &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.d_empty[d], (uint32_t)((jj / 2 - 1) & 1), status))) {
+        ok = false;
+        break;
+      }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.full[s], (uint32_t)((i / NS) & 1), status) &&
+                                       b_wait(st))) {
+        ok = false;
+        break;
+      }
+      {  // W scales, row-major [128][16 B] -> four 512-byte atoms
+        uint8_t *stg = smem + (size_t)s * Stage::BYTES;
+        uint4 rq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          rq[q] = *reinterpret_cast<const uint4 *>(stg + Stage::RAW + 16 * (lane + 32 * q));
+        *reinterpret_cast<uint4 *>(stg + Stage::SFA + 0 * 512 + 16 * lane) = make_uint4(rq[0].x, rq[1].x, rq[2].x, rq[3].x);
+        *reinterpret_cast<uint4 *>(stg + Stage::SFA + 1 * 512 + 16 * lane) = make_uint4(rq[0].y, rq[1].y, rq[2].y, rq[3].y);
+        *reinterpret_cast<uint4 *>(stg + Stage::SFA + 2 * 512 + 16 * lane) = make_uint4(rq[0].z, rq[1].z, rq[2].z, rq[3].z);
+        *reinterpret_cast<uint4 *>(stg + Stage::SFA + 3 * 512 + 16 * lane) = make_uint4(rq[0].w, rq[1].w, rq[2].w, rq[3].w);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) {
+        tc_fence_after();
+        const uint64_t off = (uint64_t)(s * (Stage::BYTES >> 4));
+        // Scale bank (i / NI) & 1: its previous user, stage i - 2 NI, was
+        // this issuer's too, and NS == 2 NI: the producer refilled slot s
+        // only after that stage's commit.
+        const uint32_t sf = tmem + kSF0 + 32u * (uint32_t)(2 * is + ((i / NI) & 1));
+        const uint32_t dt = tmem + (uint32_t)((2 * is + d) * NMMA);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          tc_cp_sf(sf + 8u * t, dSA0 + off + 32u * t);
+          tc_cp_sf(sf + 8u * t + 4, sfb_desc(i, st, t));
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          tc_mma_f4(dt, dA0 + off + 2u * t, b_desc(i, st, t), kIdesc, sf + 8u * t, sf + 8u * t + 4,
+                    (i == first && t == 0) ? 0u : 1u);
+        tc_commit(&bars.empty[s]);
+      }
+      __syncwarp();
+    }
+    // one completion per segment, whether or not this issuer had a stage in it
+    if (ok && lane == 0) tc_commit(&bars.d_full[is][d]);
+    __syncwarp();
+  }
+  if (lane == 0) {
+    // every MMA of this thread completes before tensor memory is freed
+    tc_commit(&bars.drain[is]);
+    mbar_wait_bounded(&bars.drain[is], 0u, status);
+  }
+}
+
+// Epilogue warps (kEpiWarp0..+3): per segment, the NI accumulators of each
+// row -> y (whole tile) or a partial sum (split tile, last CTA adds them).
+template <int NI, int NMMA>
+__device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, const StreamK &sk,
+                              int warp, int lane, const int (&sh)[4]) {
+  constexpr int MR = NMMA / kNC;  // rows of X per pass
+  const int q = warp & 3;
+  const int row_in_tile = 32 * q + lane;
+  const float out_scale = *a.tensor_scale;
+  volatile int *last_flag = &bars.last;
+  int n_split = 0;
+  for (int jj = 0; jj < sk.n_seg; ++jj) {
+    const int d = jj & 1, j = sk.proc_seg(jj);
+    const int s0 = sk.seg_begin(j), s1 = sk.seg_end(j);
+    const int p0 = sk.pbegin(jj);
+    const int64_t T = (sk.g_begin + s0) / sk.nch;
+    const int c0 = (int)((sk.g_begin + s0) % sk.nch), c1 = c0 + (s1 - s0);
+    bool ok = true;
+    for (int i = 0; i < NI; ++i)
+      ok = ok && mbar_wait_bounded(&bars.d_full[i][d], (uint32_t)((jj >> 1) & 1), a.status);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    tc_fence_after();
+    float acc[MR];
+#pragma unroll
+    for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      if (s1 - s0 >= NI || ((i - p0) % NI + NI) % NI < s1 - s0) {  // issuer i had a stage
+#pragma unroll
+        for (int h = 0; h < NMMA / 16; ++h) {
+          uint32_t v[16];
+          tc_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((2 * i + d) * NMMA + 16 * h), v);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int col = 16 * h + jj;
+            acc[col / kNC] += __uint_as_float(v[jj]) * pow2f(4 - 2 * (col % kNC));
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.d_empty[d]);
+    const int64_t row = T * kTileRows + row_in_tile;
+    // to true units: (acc * s_w) * 2^-sh (the power of two last: exact
+    // unless the result itself under- or overflows)
+#pragma unroll
+    for (int m = 0; m < MR; ++m) acc[m] = ldexpf(acc[m] * out_scale, -sh[m]);
+    if (c0 == 0 && c1 == sk.nch) {  // whole tile in this CTA
+      if (row < a.N) {
+#pragma unroll
+        for (int m = 0; m < MR; ++m)
+          if (m < a.M) a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+      }
+      continue;
+    }
+    // Split tile.  CTAs c_first..c_last share it; each keeps the partial sums
+    // of its first and last segment (slots 0 and 1; a single segment uses 0).
+    const int c_first = sk.owner(T * sk.nch), c_last = sk.owner(T * sk.nch + sk.nch - 1);
+    const int nslot = c_last - c_first + 1;
+    auto part_at = [&](int c, int sl, int m) {
+      return a.part + ((size_t)(2 * c + sl) * 4 + m) * kTileRows + row_in_tile;
+    };
+#pragma unroll
+    for (int m = 0; m < MR; ++m)
+      if (m < a.M) *part_at(blockIdx.x, j == 0 ? 0 : 1, m) = acc[m];
+    // The warps report in (a CTA-scope release); one thread makes the CTA's
+    // stores visible device-wide (a cumulative fence) and counts the
+    // segment; the tile's last CTA adds the partials in K order.
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.part_done);
+    const uint32_t par = (uint32_t)(n_split & 1);
+    ++n_split;
+    if (warp == kEpiWarp0 && lane == 0) {
+      const bool got = mbar_wait_bounded(&bars.part_done, par, a.status);
+      __threadfence();
+      *last_flag = got && count_segment(a.cnt + T, a.epoch, nslot);
+      __threadfence();
+      mbar_arrive(&bars.flag_ready);
+    }
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.flag_ready, par, a.status))) break;
+    if (*last_flag) {
+      __threadfence();
+      if (row < a.N) {
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+          if (m < a.M) {
+            float t = 0.0f;
+            for (int c = c_first; c <= c_last; ++c) {
+              // the tile is the last segment of c_first (its first too if c_first
+              // has only one) and the first segment of every later CTA
+              int sl = 0;
+              if (c == c_first) {
+                const int64_t gb = sk.total * c / sk.G, ge = sk.total * (c + 1) / sk.G;
+                sl = ((ge - 1) / sk.nch != gb / sk.nch) ? 1 : 0;
+              }
+              t += (c == (int)blockIdx.x && sl == (j == 0 ? 0 : 1)) ? acc[m] : __ldcg(part_at(c, sl, m));
+            }
+            a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(t));
+          }
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void init_common(F4Bars &bars, int ns, int ni) {
+  for (int s = 0; s < ns; ++s) {
+    mbar_init(&bars.full[s], 1);
+    mbar_init(&bars.empty[s], 1);
+  }
+  for (int i = 0; i < ni; ++i) {
+    mbar_init(&bars.d_full[i][0], 1);
+    mbar_init(&bars.d_full[i][1], 1);
+    mbar_init(&bars.drain[i], 1);
+  }
+  mbar_init(&bars.d_empty[0], 4);
+  mbar_init(&bars.d_empty[1], 4);
+  mbar_init(&bars.part_done, 4);
+  mbar_init(&bars.flag_ready, 1);
+  bars.xmax[0] = bars.xmax[1] = 0u;
+  fence_mbar_init();
+}
+
+// ---- streamed-B path -----------------------------------------------------------
+
+// X -> NVFP4 components in the workspace.  Grid (blocks of K / 256 threads,
+// M); every CTA finds its row's max|x|, then each thread splits one block.
+__global__ void __launch_bounds__(kXsplitThreads)
+    xsplit_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, int nmma, uint8_t *bcodes,
+                  uint8_t *sfb, int32_t *sh_out) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // X may come from the previous kernel, and the previous GEMV may still
+  // read the workspace: wait for it before touching either.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ uint32_t red[kXsplitThreads / 32];
+  const int m = blockIdx.y;
+  const uint16_t *xr = x + m * ldx;
+  const int64_t nb = K / 16;
+  uint32_t mx = 0;
+  for (int64_t i = threadIdx.x; i < K / 8; i += kXsplitThreads)
+    mx = max(mx, absmax_bf16x8(__ldg(reinterpret_cast<const uint4 *>(xr) + i)));
+  for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = 0;
+  for (int w = 0; w < kXsplitThreads / 32; ++w) mx = max(mx, red[w]);
+  const int sh = prescale_exponent(mx);
+  if (blockIdx.x == 0 && threadIdx.x == 0) sh_out[m] = sh;
+
+  const int64_t b = (int64_t)blockIdx.x * kXsplitThreads + threadIdx.x;
+  const int64_t KH = K / 2;
+  if (b < nb) {
+    uint2 code[kNC];
+    uint32_t sb[kNC];
+    split_block(xr + 16 * b, sh, code, sb);
+    // atom position of this block: K64 step b / 4, block b % 4
+    uint8_t *atom = sfb + (b >> 2) * 512 + (b & 3);
+#pragma unroll
+    for (int c = 0; c < kNC; ++c) {
+      const int n = m * kNC + c;
+      *reinterpret_cast<uint2 *>(bcodes + n * KH + 8 * b) = code[c];
+      atom[16 * (n & 31) + 4 * ((n >> 5) & 3)] = (uint8_t)sb[c];
+    }
+  }
+  // operand rows past the last component: zero scales (their codes then
+  // contribute nothing)
+  if (m == M - 1 && blockIdx.x == 0)
+    for (int64_t i = threadIdx.x; i < (K / 64) * (nmma - M * kNC); i += kXsplitThreads) {
+      const int64_t t = i / (nmma - M * kNC);
+      const int n = M * kNC + (int)(i % (nmma - M * kNC));
+      *reinterpret_cast<uint32_t *>(sfb + t * 512 + 16 * (n & 31) + 4 * ((n >> 5) & 3)) = 0u;
+    }
+}
+
+template <int NMMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
+                   const __grid_constant__ CUtensorMap tm_b, const F4Args a) {
+  using L = StageS<NMMA>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled tiles
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  F4Bars &bars = *reinterpret_cast<F4Bars *>(smem + kNSS * L::BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const StreamK sk(a.n_tiles, a.n_chunks);
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) init_common(bars, kNSS, kIssuersS);
+  if (warp == 0) tmem_alloc(&bars.tmem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem;
+
+  if (warp == kProducerS) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_w);
+      prefetch_tmap(&tm_ws);
+      prefetch_tmap(&tm_b);
+      // processing position i -> ring slot i % NS, stage stage_of(i)
+      auto load_w = [&](int i) {
+        const int s = i % kNSS;
+        uint8_t *stg = smem + (size_t)s * L::BYTES;
+        const int64_t g = sk.g_begin + sk.stage_of(i);
+        const int row0 = (int)(g / sk.nch) * kTileRows, ch = (int)(g % sk.nch);
+        mbar_arrive_expect_tx(&bars.full[s], L::TX);
+        tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
+        tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
+      };
+      auto load_x = [&](int i) {
+        const int s = i % kNSS;
+        uint8_t *stg = smem + (size_t)s * L::BYTES;
+        const int ch = (int)((sk.g_begin + sk.stage_of(i)) % sk.nch);
+        tma_load_2d(stg + L::B, &tm_b, ch * (kChunkK / 2), 0, &bars.full[s]);
+        bulk_g2s(stg + L::SFB, a.sfb + (size_t)ch * 2048, 2048u, &bars.full[s]);
+      };
+      // W of the first stages before the previous kernel has finished, and
+      // more W into L2: HBM keeps streaming while X is being split.
+      const int pre = min(kNSS, sk.n_st);
+      for (int i = 0; i < pre; ++i) load_w(i);
+      for (int i = pre; i < min(pre + kPrefetch, sk.n_st); ++i) {
+        const int64_t g = sk.g_begin + sk.stage_of(i);
+        const int row0 = (int)(g / sk.nch) * kTileRows, ch = (int)(g % sk.nch);
+        tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), row0);
+        tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), row0);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      for (int i = 0; i < pre; ++i) load_x(i);
+      int i = pre;
+      for (; i < sk.n_st; ++i) {
+        const int s = i % kNSS;
+        if (!mbar_wait_bounded(&bars.empty[s], (uint32_t)((i / kNSS - 1) & 1), a.status)) break;
+        load_w(i);
+        load_x(i);
+      }
+      // never leave with copies in flight
+      for (int k = (i > kNSS ? i - kNSS : 0); k < i; ++k)
+        mbar_wait_bounded(&bars.full[k % kNSS], (uint32_t)((k / kNSS) & 1), a.status);
+    }
+  } else if (warp < kIssuersS) {
+    const uint32_t sbase = smem_u32(smem);
+    const uint64_t dB0 = sdesc(sbase + L::B, 16, 1024, kSw128);
+    const uint64_t dSB0 = sdesc(sbase + L::SFB, 0, 128, kNoSwizzle);
+    auto b_desc = [&](int i, int, int t) {
+      return dB0 + (uint64_t)((i % kNSS) * (L::BYTES >> 4)) + 2u * t;
+    };
+    auto sfb_desc = [&](int i, int, int t) {
+      return dSB0 + (uint64_t)((i % kNSS) * (L::BYTES >> 4)) + 32u * t;
+    };
+    issuer_loop<kIssuersS, kNSS, NMMA, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
+                                          sfb_desc, [](int) { return true; });
+  } else if (warp >= kEpiWarp0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int sh[4] = {0, 0, 0, 0};
+    for (int m = 0; m < a.M; ++m) sh[m] = a.sh[m];
+    epilogue_loop<kIssuersS, NMMA>(a, bars, tmem, sk, warp, lane, sh);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_free(tmem);
+  }
+}
+
+// ---- resident-B path (M <= 2) ---------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_f4r_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
+                    const F4Args a) {
+  using L = StageR;
+  constexpr int NMMA = 16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t *bcodes = smem + kNSR * L::BYTES;                   // [slot][16 rows][128 B], swizzled
+  uint8_t *bsf = bcodes + (size_t)a.n_slots * 2048;           // [slot][4 steps][512 B]
+  F4Bars &bars = *reinterpret_cast<F4Bars *>(bsf + (size_t)a.n_slots * 2048);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const StreamK sk(a.n_tiles, a.n_chunks);
+  // B slot of chunk ch: this CTA's chunks run consecutively from ch_begin
+  const int ch_begin = (int)(sk.g_begin % sk.nch);
+  auto slot_of = [&](int st) {
+    const int ch = (int)((sk.g_begin + st) % sk.nch);
+    return (ch - ch_begin + sk.nch) % sk.nch;
+  };
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < kMaxSlotsR; ++q) mbar_init(&bars.b_ready[q], 1);
+    init_common(bars, kNSR, kIssuersR);
+  }
+  if (warp == 0) tmem_alloc(&bars.tmem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem;
+
+  if (warp == kProducerR) {
+    // W only: it is never written on the stream, so no wait for the
+    // previous kernel.
+    if (lane == 0) {
+      prefetch_tmap(&tm_w);
+      prefetch_tmap(&tm_ws);
+      // processing position i -> ring slot i % NS, stage stage_of(i)
+      auto load_w = [&](int i) {
+        const int s = i % kNSR;
+        uint8_t *stg = smem + (size_t)s * L::BYTES;
+        const int64_t g = sk.g_begin + sk.stage_of(i);
+        const int row0 = (int)(g / sk.nch) * kTileRows, ch = (int)(g % sk.nch);
+        mbar_arrive_expect_tx(&bars.full[s], L::TX);
+        tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
+        tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
+      };
+      const int pre = min(kNSR, sk.n_st);
+      for (int i = 0; i < pre; ++i) load_w(i);
+      for (int i = pre; i < min(pre + kPrefetch, sk.n_st); ++i) {
+        const int64_t g = sk.g_begin + sk.stage_of(i);
+        const int row0 = (int)(g / sk.nch) * kTileRows, ch = (int)(g % sk.nch);
+        tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), row0);
+        tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), row0);
+      }
+      int i = pre;
+      for (; i < sk.n_st; ++i) {
+        const int s = i % kNSR;
+        if (!mbar_wait_bounded(&bars.empty[s], (uint32_t)((i / kNSR - 1) & 1), a.status)) break;
+        load_w(i);
+      }
+      for (int k = (i > kNSR ? i - kNSR : 0); k < i; ++k)
+        mbar_wait_bounded(&bars.full[k % kNSR], (uint32_t)((k / kNSR) & 1), a.status);
+    }
+  } else if (warp >= kHelperWarp0R) {
+    // ---- warps 4..11: split this CTA's chunks of X into shared memory.
+    // Helper warp h (8 of them) takes slots h, h + 8, h + 16; lane 2 bb + f
+    // holds elements 8 f .. 8 f + 7 of block bb of each slot's chunk, for
+    // each row of X; the three slots are split together (independent chains
+    // side by side).  The prescale comes from this CTA's own blocks: partial
+    // sums leave the CTA in true units, so CTAs need not agree on it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int hw = warp - kHelperWarp0R;  // helper warp 0..7
+    const int bb_l = lane >> 1, hf = lane & 1;
+    constexpr int kHelperWarps = kHelperThreadsR / 32;
+    constexpr int KS = (kMaxSlotsR + kHelperWarps - 1) / kHelperWarps;
+    uint4 xv[KS][2];
+    uint32_t mx[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const int qs = hw + kHelperWarps * k;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        xv[k][m] = make_uint4(0, 0, 0, 0);
+        if (qs < a.n_slots && m < a.M) {
+          const int ch = (ch_begin + qs) % sk.nch;
+          xv[k][m] = __ldg(reinterpret_cast<const uint4 *>(a.x + m * a.ldx + (int64_t)ch * kChunkK +
+                                                           16 * bb_l + 8 * hf));
+          mx[m] = max(mx[m], absmax_bf16x8(xv[k][m]));
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      for (int o = 16; o; o >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], o));
+      if (lane == 0 && m < a.M) atomicMax(&bars.xmax[m], mx[m]);
+    }
+    named_bar(1, kHelperThreadsR);
+    int sh[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int m = 0; m < 2; ++m) sh[m] = m < a.M ? prescale_exponent(bars.xmax[m]) : 0;
+    // clear the slots' scale atoms (rows without a component keep zero
+    // scales) and, for M = 1, the codes of operand rows 8..15
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const int qs = hw + kHelperWarps * k;
+      if (qs >= a.n_slots) break;  // warp-uniform
+      uint4 *z = reinterpret_cast<uint4 *>(bsf + qs * 2048);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) z[lane + 32 * i] = make_uint4(0, 0, 0, 0);
+      if (a.M == 1) {
+        uint4 *zc = reinterpret_cast<uint4 *>(bcodes + qs * 2048 + 1024);
+        zc[lane] = make_uint4(0, 0, 0, 0);
+        zc[lane + 32] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      if (m >= a.M) break;
+      const float p1 = pow2f(sh[m] / 2), p2 = pow2f(sh[m] - sh[m] / 2);
+      float r[KS][8];
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        const uint32_t w[4] = {xv[k][m].x, xv[k][m].y, xv[k][m].z, xv[k][m].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          r[k][2 * t] = bf16_bits_to_f32(w[t] & 0xFFFFu) * p1 * p2;
+          r[k][2 * t + 1] = bf16_bits_to_f32(w[t] >> 16) * p1 * p2;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kNC; ++c) {
+        const int n = m * kNC + c;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          const int qs = hw + kHelperWarps * k;
+          float m4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m4[e] = fmaxf(fabsf(r[k][e]), fabsf(r[k][e + 4]));
+          float amax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));  // the block's other half
+          // Any scale is valid -- the residual tracks what was taken -- so
+          // an approximate reciprocal stands in for the division.
+          const uint32_t sb = f32_to_e4m3_satfinite(amax * (1.0f / 6.0f) * pow2f(2 * c - 4));
+          const float d = e4m3_to_f32(sb) * pow2f(4 - 2 * c);
+          uint32_t cw = 0u;
+          if (d > 0.0f) {
+            float inv;
+            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(d));
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = r[k][e] * inv;
+            cw = f32x8_to_e2m1_packed(q);
+            uint32_t v[4];
+            e2m1x8_to_f16x2x4(cw, v);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {  // e2m1 * d is exact; one rounding per update
+              r[k][2 * t] = fmaf(-f16lo_to_f32(v[t]), d, r[k][2 * t]);
+              r[k][2 * t + 1] = fmaf(-f16hi_to_f32(v[t]), d, r[k][2 * t + 1]);
+            }
+          }
+          if (qs < a.n_slots) {
+            *reinterpret_cast<uint32_t *>(bcodes + qs * 2048 + n * 128 +
+                                          (((bb_l >> 1) ^ (n & 7)) << 4) + 8 * (bb_l & 1) + 4 * hf) = cw;
+            if (hf == 0) bsf[qs * 2048 + (bb_l >> 2) * 512 + 16 * n + (bb_l & 3)] = (uint8_t)sb;
+          }
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0)
+      for (int k = 0; k < KS; ++k)
+        if (hw + kHelperWarps * k < a.n_slots) mbar_arrive(&bars.b_ready[hw + kHelperWarps * k]);
+
+    if (warp >= kEpiWarp0) epilogue_loop<kIssuersR, NMMA>(a, bars, tmem, sk, warp, lane, sh);
+  } else if (warp < kIssuersR) {
+    // ---- MMA issuers: each stage waits for its B slot
+    const uint64_t dB0 = sdesc(smem_u32(bcodes), 16, 1024, kSw128);
+    const uint64_t dSB0 = sdesc(smem_u32(bsf), 0, 128, kNoSwizzle);
+    auto b_desc = [&](int, int st, int t) { return dB0 + (uint64_t)(slot_of(st) * (2048 >> 4)) + 2u * t; };
+    auto sfb_desc = [&](int, int st, int t) {
+      return dSB0 + (uint64_t)(slot_of(st) * (2048 >> 4)) + (uint64_t)(32u * t);
+    };
+    auto b_wait = [&](int st) { return mbar_wait_bounded(&bars.b_ready[slot_of(st)], 0u, a.status); };
+    issuer_loop<kIssuersR, kNSR, NMMA, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
+                                          sfb_desc, b_wait);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_free(tmem);
+  }
+}
+
+// ---- host --------------------------------------------------------------------
+
+int nmma_for(int64_t M) { return M <= 2 ? 16 : 32; }
+
+struct F4Ws {
+  size_t bcodes, sfb, sh, cnt, part, total;
+  int grid;
+};
+// Workspace of a pass of up to four rows: X's components and scale atoms
+// (streamed path), prescale exponents, per-tile counters, partial sums.
+F4Ws f4_ws(int64_t M, int64_t N, int64_t K) {
+  F4Ws w;
+  const int nmma = nmma_for(M);
+  const int64_t n_tiles = ceil_div(N, kTileRows);
+  const int64_t chunks = n_tiles * (K / kChunkK);
+  const int64_t cap = chunks < kMaxGrid ? chunks : kMaxGrid;
+  w.grid = (int)(cap < num_sms() ? cap : num_sms());
+  // Not many fewer tiles than SMs: one whole tile per CTA (no split tiles,
+  // no fix-up) beats an even split.
+  if (n_tiles <= w.grid && 4 * n_tiles >= 3 * w.grid) w.grid = (int)n_tiles;
+  w.bcodes = 0;
+  w.sfb = (size_t)ceil_div((int64_t)nmma * (K / 2), 1024) * 1024;
+  w.sh = w.sfb + (size_t)(K / 64) * 512;
+  w.cnt = w.sh + 256;
+  w.part = w.cnt + (size_t)ceil_div(n_tiles * 16, 256) * 256;
+  w.total = w.part + (size_t)cap * 2 * 4 * kTileRows * sizeof(float);
+  return w;
+}
+
+template <int NMMA> size_t smem_s() { return (size_t)kNSS * StageS<NMMA>::BYTES + sizeof(F4Bars) + 1024; }
+size_t smem_r(int n_slots) {
+  return (size_t)kNSR * StageR::BYTES + (size_t)n_slots * (2048 + 2048) + sizeof(F4Bars) + 1024;
+}
+
+// B slots the resident kernel needs: the most distinct K chunks any CTA sees.
+int slots_r(int64_t N, int64_t K, int grid) {
+  const int64_t nch = K / kChunkK, total = ceil_div(N, kTileRows) * nch;
+  const int64_t per = ceil_div(total, grid);
+  return (int)(per < nch ? per : nch);
+}
+
+// Tensor maps cached per (array, shape).
+struct MapEntry {
+  const void *base;
+  uint64_t rows, row_bytes;
+  uint32_t box_rows, box_bytes;
+  bool swz;
+  CUtensorMap map;
+};
+std::mutex g_mu;
+MapEntry g_cache[32];
+int g_next = 0, g_used = 0;
+std::atomic<unsigned long long> g_epoch{0};
+std::once_flag g_epoch_once;
+
+bool cached_map(CUtensorMap &out, const void *base, uint64_t rows, uint64_t row_bytes,
+                uint32_t box_rows, uint32_t box_bytes, bool swz) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < g_used; ++i) {
+    const MapEntry &e = g_cache[i];
+    if (e.base == base && e.rows == rows && e.row_bytes == row_bytes && e.box_rows == box_rows &&
+        e.box_bytes == box_bytes && e.swz == swz) {
+      out = e.map;
+      return true;
+    }
+  }
+  if (!make_tmap_u8_2d(&out, base, rows, row_bytes, row_bytes, box_rows, box_bytes, swz))
+    return false;
+  MapEntry &e = g_cache[g_next];
+  e = MapEntry{base, rows, row_bytes, box_rows, box_bytes, swz, out};
+  g_next = (g_next + 1) % 32;
+  if (g_used < 32) ++g_used;
+  return true;
+}
+
+// Launch epochs for the split-tile counters: consecutive from a random start.
+unsigned long long next_epoch() {
+  std::call_once(g_epoch_once, [] {
+    std::random_device rd;
+    g_epoch = ((unsigned long long)rd() << 32) ^ rd() ^
+              (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+  });
+  return ++g_epoch;
+}
+
+template <class Kern, class... Args>
+cudaError_t launch_pdl(Kern kern, int grid, int threads, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+F4Args base_args(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const float *tensor_scale,
+                 int64_t N, uint16_t *y, int64_t ldy, int32_t *status, uint8_t *ws,
+                 const F4Ws &L) {
+  F4Args a = {};
+  a.x = x;
+  a.ldx = ldx;
+  a.y = y;
+  a.ldy = ldy;
+  a.M = (int)M;
+  a.N = N;
+  a.K = K;
+  a.tensor_scale = tensor_scale;
+  a.sfb = ws + L.sfb;
+  a.sh = reinterpret_cast<const int32_t *>(ws + L.sh);
+  a.part = reinterpret_cast<float *>(ws + L.part);
+  a.cnt = reinterpret_cast<unsigned __int128 *>(ws + L.cnt);
+  a.status = status;
+  a.n_tiles = (int)ceil_div(N, kTileRows);
+  a.n_chunks = (int)(K / kChunkK);
+  a.epoch = next_epoch();
+  return a;
+}
+
+cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                                 const uint8_t *codes, const uint8_t *scales,
+                                 const float *tensor_scale, int64_t N, uint16_t *y, int64_t ldy,
+                                 int32_t *status, void *workspace, cudaStream_t stream) {
+  const int nmma = nmma_for(M);
+  const F4Ws L = f4_ws(M, N, K);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  CUtensorMap mw, ms, mb;
+  if (!cached_map(mw, codes, (uint64_t)N, (uint64_t)(K / 2), kTileRows, 128, true) ||
+      !cached_map(ms, scales, (uint64_t)N, (uint64_t)(K / 16), kTileRows, 16, false) ||
+      !cached_map(mb, ws + L.bcodes, (uint64_t)nmma, (uint64_t)(K / 2), (uint32_t)nmma, 128, true))
+    return cudaErrorInvalidValue;
+  // components of X (programmatic dependent launch: may start while the
+  // previous kernel drains; it waits before reading X or writing the workspace)
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(K / 16, kXsplitThreads), (unsigned)M);
+    cfg.blockDim = dim3(kXsplitThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, xsplit_kernel, x, ldx, (int)M, K, nmma,
+                                             ws + L.bcodes, ws + L.sfb,
+                                             reinterpret_cast<int32_t *>(ws + L.sh));
+    if (e != cudaSuccess) return e;
+  }
+  const F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status, ws, L);
+  return nmma == 16
+             ? launch_pdl(gemv_f4_kernel<16>, L.grid, kThreads, smem_s<16>(), stream, mw, ms, mb, a)
+             : launch_pdl(gemv_f4_kernel<32>, L.grid, kThreads, smem_s<32>(), stream, mw, ms, mb, a);
+}
+
+}  // namespace
+
+bool gemv_f4_shape_ok(int64_t M, int64_t N, int64_t K) {
+  return M >= 1 && M <= kDecodeMaxM && N >= kTileRows && N <= 0x7FFFFFFFll && K >= 4 * kChunkK &&
+         K % kChunkK == 0 && K <= (1 << 24);
+}
+
+size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return f4_ws(M < 4 ? M : 4, N, K).total;
+}
+
+bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const void *scales) {
+  return gemv_f4_shape_ok(M, N, K) && !(((uintptr_t)codes | (uintptr_t)scales) & 15u);
+}
+
+cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                           const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
+                           int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
+                           cudaStream_t stream) {
+  if (M <= 2) {
+    const F4Ws L = f4_ws(M, N, K);
+    const int n_slots = slots_r(N, K, L.grid);
+    if (n_slots <= kMaxSlotsR) {
+      CUtensorMap mw, ms;
+      if (!cached_map(mw, codes, (uint64_t)N, (uint64_t)(K / 2), kTileRows, 128, true) ||
+          !cached_map(ms, scales, (uint64_t)N, (uint64_t)(K / 16), kTileRows, 16, false))
+        return cudaErrorInvalidValue;
+      F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status,
+                           static_cast<uint8_t *>(workspace), L);
+      a.n_slots = n_slots;
+      return launch_pdl(gemv_f4r_kernel, L.grid, kThreads, smem_r(n_slots), stream, mw, ms, a);
+    }
+  }
+  // passes of up to four rows of X, each one stream of W (the workspace is
+  // reused: each pass's split kernel waits for the previous GEMV)
+  for (int64_t m0 = 0; m0 < M; m0 += 4) {
+    const int64_t mp = M - m0 < 4 ? M - m0 : 4;
+    const cudaError_t e = launch_pass_streamed(x + m0 * ldx, mp, K, ldx, codes, scales,
+                                               tensor_scale, N, y + m0 * ldy, ldy, status,
+                                               workspace, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace impfp4

@@ -32,7 +32,15 @@ def test_status_strings():
 def test_workspace_sizes():
     assert pkg.imp_nvfp4_quantize_workspace_size(0, 64) == 0
     assert 0 < pkg.imp_nvfp4_quantize_workspace_size(151936, 5120) <= 4096
-    assert pkg.imp_nvfp4_gemm_workspace_size(1, 17408, 5120) == 0
+    # decode shapes on the FP4 tensor-core path need room for X's components
+    ws1 = pkg.imp_nvfp4_gemm_workspace_size(1, 17408, 5120)
+    assert 16 * 2560 + 80 * 512 <= ws1 <= 16 * 2560 + 80 * 512 + (2 << 20)
+    assert pkg.imp_nvfp4_gemm_workspace_size(4, 17408, 5120) == \
+        pkg.imp_nvfp4_gemm_workspace_size(16, 17408, 5120) > ws1
+    # shapes that path does not take need none
+    assert pkg.imp_nvfp4_gemm_workspace_size(1, 100, 5120) == 0
+    assert pkg.imp_nvfp4_gemm_workspace_size(1, 17408, 320) == 0
+    assert pkg.imp_nvfp4_gemm_workspace_size(1, 17408, 768) == 0
 
 
 A16 = 0x7F0000000000  # fake, 16-byte aligned "device" addresses: never dereferenced
@@ -58,6 +66,14 @@ def test_gemm_rejects_bad_arguments():
     assert g(A16 + 2, 1, 64, 64, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_ERR_MISALIGNED
     assert g(A16, 2, 64, 68, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_ERR_MISALIGNED
     assert g(A16, 2, 64, 64, _t(8, 64), A16, 12, None, None, 0, None) == pkg.IMP_ERR_MISALIGNED
+    # the decode path's workspace: missing, short or misaligned
+    need = pkg.imp_nvfp4_gemm_workspace_size(1, 256, 1024)
+    assert g(A16, 1, 1024, 1024, _t(256, 1024), A16, 256, None, None, 0, None) == \
+        pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    assert g(A16, 1, 1024, 1024, _t(256, 1024), A16, 256, None, A16, need - 1, None) == \
+        pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    assert g(A16, 1, 1024, 1024, _t(256, 1024), A16, 256, None, A16 + 8, need, None) == \
+        pkg.IMP_ERR_MISALIGNED
     # empty problems are valid and enqueue nothing
     assert g(A16, 0, 64, 64, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_OK
     assert g(A16, 4, 64, 64, _t(0, 64), A16, 8, None, None, 0, None) == pkg.IMP_OK

@@ -75,7 +75,13 @@ def test_full_size_sampled(lin):
     # memory (K % 256 != 0), several passes with inactive rows
     (8, 5120, 333, 5120, 336), (6, 3072, 200, 3080, 200), (8, 192, 70, 192, 72),
     (4, 17408, 100, 17408, 104), (11, 2304, 97, 2304, 104), (13, 1088, 40, 1088, 40),
-    (2, 320, 19, 320, 24), (4, 576, 1500, 576, 1504)])
+    (2, 320, 19, 320, 24), (4, 576, 1500, 576, 1504),
+    # the tensor-memory path (M <= 2, K % 256 == 0): one pair per row, a
+    # half-filled last pair, a last stage with fewer pairs, ragged row
+    # blocks, fewer row blocks than SMs, padded X rows
+    (1, 512, 32, 512, 32), (1, 768, 1000, 768, 1000), (1, 1280, 4097, 1288, 4104),
+    (2, 1280, 333, 1280, 336), (2, 768, 64, 776, 64), (1, 2560, 9733, 2560, 9736),
+    (2, 17408, 200, 17408, 200)])
 def test_edge_shapes(M, K, N, ldx, ldy):
     lin = synth.Linear("edge", M, K, N, 123, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
                        zero_block_p=0.02, x_outlier_frac=0.02)
@@ -101,11 +107,12 @@ def test_extreme_activation_magnitudes():
             check_within_tolerance(y, y_ref, bound, f"x ~ 2^{exp}")
 
 
-@pytest.mark.parametrize("M", [2, 4, 8, 12])
-def test_extreme_activation_magnitudes_per_row(M):
+@pytest.mark.parametrize("N", [96, 160])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 12])
+def test_extreme_activation_magnitudes_per_row(M, N):
     # Rows of X of very different magnitude in one call: each row keeps its
-    # own power-of-two staging factor.
-    lin = synth.Linear("mag", M, 2048, 96, 6)
+    # own power-of-two staging factor (N = 160 takes the FP4 path, 96 not).
+    lin = synth.Linear("mag", M, 2048, N, 6)
     c, s, ts = oracle_w(lin)
     rng = np.random.default_rng(M)
     exps = [(-130, -60, -20, 0, 20, 60, 100)[i % 7] for i in range(M)]
