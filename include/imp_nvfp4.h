@@ -150,40 +150,63 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                           const imp_nvfp4_tensor *w, void *y_bf16, int64_t ldy,
                           int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream);
 
-/* ---- tensor-core operand layout (prefill path) -----------------------------
- * The block-scaled FP4 MMA reads block scales as 512-byte atoms: one atom
- * holds the scales of 128 rows x 4 blocks (64 elements of K); row r of the
- * atom sits at byte 16*(r % 32) + 4*((r / 32) % 4), block j of it at + j.
- * Atoms of a 128-row block follow each other along K; row blocks follow each
- * other; rows are padded to a multiple of 256.  Codes keep the row-major
- * [rows][K/2] layout.  This is a one-time transform for weights (like an
- * engine's cache of transformed weights).                                   */
+/* ---- tensor-core operand layout ("MMA layout") -----------------------------
+ * A one-time transform of a weight for the tensor-core kernels (like an
+ * engine's cache of transformed weights); values are unchanged.
+ *   Scales: 512-byte atoms, one per 128 rows x 4 blocks (64 elements of K);
+ *     row r of the atom at byte 16*(r % 32) + 4*((r / 32) % 4), block j of it
+ *     at + j.  Atoms of a 128-row block follow each other along K; row blocks
+ *     follow each other.
+ *   Codes: 16 KB tiles of 128 rows x 256 elements (128 bytes per row), each
+ *     stored as a 128-byte-swizzled operand tile (row rr at rr * 128, its
+ *     16-byte unit u at unit u ^ (rr % 8)); tiles run along K (K padded to a
+ *     multiple of 256), then down the rows.
+ *   Rows are padded to a multiple of 256; padding is zero.
+ * An imp_nvfp4_tensor "in MMA layout" has codes and scales in these layouts
+ * (rows and K are the logical sizes; the tensor scale is unchanged).       */
 
-/* Bytes of atom-layout scales for a rows x K tensor (K % 64 == 0). */
+/* Bytes of MMA-layout scales / codes for a rows x K tensor (K % 64 == 0). */
 size_t imp_nvfp4_mma_scales_size(int64_t rows, int64_t K);
+size_t imp_nvfp4_mma_codes_size(int64_t rows, int64_t K);
 
-/* Copy the row-major block scales of `t` into the atom layout.
- *   t           NVFP4 tensor (row-major scales), rows >= 1, K % 64 == 0.
- *   mma_scales  device buffer of >= imp_nvfp4_mma_scales_size(rows, K) bytes,
- *               16-byte aligned; padding rows are written as 0.           */
-imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_scales, size_t bytes,
-                                 void *stream);
+/* Copy tensor `t` (row-major) into the MMA layout.
+ *   t           NVFP4 tensor, rows >= 1, K % 64 == 0.
+ *   mma_codes   device buffer of >= imp_nvfp4_mma_codes_size(rows, K) bytes;
+ *   mma_scales  device buffer of >= imp_nvfp4_mma_scales_size(rows, K) bytes;
+ *               both 16-byte aligned, padding written as 0.  Either may be
+ *               NULL (with 0 bytes) to skip that part.                     */
+imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_codes, size_t codes_bytes,
+                                 void *mma_scales, size_t scales_bytes, void *stream);
 
 /* Quantize like imp_nvfp4_quantize (bit-identical codes, scale bytes and
- * tensor scale) but write the scales in the atom layout: out->scales must
- * hold imp_nvfp4_mma_scales_size(rows, K) bytes.  K % 64 == 0.            */
+ * tensor scale) but write the scales in the MMA (atom) layout, for the X
+ * operand of imp_nvfp4_gemm_fp4: out->scales must hold
+ * imp_nvfp4_mma_scales_size(rows, K) bytes; codes stay row-major [rows][K/2].
+ * K % 64 == 0.                                                             */
 imp_status imp_nvfp4_quantize_mma(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
                                   const imp_nvfp4_tensor *out, int32_t *dev_status,
                                   void *workspace, size_t ws_bytes, void *stream);
 
-/* Y = Xq * Wq^T with both operands NVFP4 and their scales in the atom
- * layout: the block-scaled FP4 tensor-core GEMM alone (tcgen05.mma
- * kind::mxf4nvf4, fp32 accumulation in tensor memory), times
- * s_x * s_w, rounded to bf16.
- *   xq  M rows (M >= 1), K % 64 == 0;  wq  N rows, wq->K == K.
+/* Y = Xq * Wq^T, both operands NVFP4: the block-scaled FP4 tensor-core GEMM
+ * alone (tcgen05.mma kind::mxf4nvf4, fp32 accumulation in tensor memory),
+ * times s_x * s_w, rounded to bf16.
+ *   xq  from imp_nvfp4_quantize_mma: M rows (M >= 1), row-major codes,
+ *       atom-layout scales, K % 64 == 0;
+ *   wq  N rows in MMA layout, wq->K == K;
  *   y   bf16[M][ldy], ldy >= N, ldy % 8 == 0.                             */
 imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor *wq,
                               void *y_bf16, int64_t ldy, int32_t *dev_status, void *stream);
+
+/* Y = X * W^T like imp_nvfp4_gemm, with W in MMA layout (the serving form:
+ * weights prepared once, read as contiguous 16 KB tiles).  M <= 16 takes the
+ * decode path (FP4 tensor cores, X split per call), which needs
+ * K % 256 == 0, K >= 1024, N >= 128 (else IMP_ERR_UNSUPPORTED_SHAPE);
+ * M > 16 the prefill path.  Workspace: imp_nvfp4_gemm_workspace_size(M, N,
+ * K) bytes, 16-byte aligned.  Other arguments and the accuracy are those of
+ * imp_nvfp4_gemm.                                                          */
+imp_status imp_nvfp4_gemm_mma(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                              const imp_nvfp4_tensor *w_mma, void *y_bf16, int64_t ldy,
+                              int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *imp_status_string(imp_status status);

@@ -26,8 +26,8 @@ __all__ = [
     "imp_nvfp4_gemm_workspace_size", "imp_status_string", "NVFP4Tensor", "quantize", "gemm",
     "library_path", "header_functions", "ImpError", "load", "imp_nvfp4_mma_scales_size",
     "imp_nvfp4_prepare_mma", "imp_nvfp4_quantize_mma", "imp_nvfp4_gemm_fp4", "prepare_mma",
-    "imp_nvfp4_quantize_noalloc",
-    "quantize_mma", "gemm_fp4",
+    "imp_nvfp4_quantize_noalloc", "imp_nvfp4_mma_codes_size", "imp_nvfp4_gemm_mma",
+    "quantize_mma", "gemm_fp4", "gemm_mma",
 ]
 
 IMP_OK = 0
@@ -74,8 +74,12 @@ def _L():
     T = ctypes.POINTER(ImpNvfp4Tensor)
     lib.imp_nvfp4_mma_scales_size.restype = SZ
     lib.imp_nvfp4_mma_scales_size.argtypes = [I64, I64]
+    lib.imp_nvfp4_mma_codes_size.restype = SZ
+    lib.imp_nvfp4_mma_codes_size.argtypes = [I64, I64]
     lib.imp_nvfp4_prepare_mma.restype = ctypes.c_int
-    lib.imp_nvfp4_prepare_mma.argtypes = [T, P, SZ, P]
+    lib.imp_nvfp4_prepare_mma.argtypes = [T, P, SZ, P, SZ, P]
+    lib.imp_nvfp4_gemm_mma.restype = ctypes.c_int
+    lib.imp_nvfp4_gemm_mma.argtypes = [P, I64, I64, I64, T, P, I64, P, P, SZ, P]
     lib.imp_nvfp4_quantize_mma.restype = ctypes.c_int
     lib.imp_nvfp4_quantize_mma.argtypes = [P, I64, I64, I64, T, P, P, SZ, P]
     lib.imp_nvfp4_quantize_noalloc.restype = ctypes.c_int
@@ -132,9 +136,21 @@ def imp_nvfp4_mma_scales_size(rows: int, K: int) -> int:
     return _L().imp_nvfp4_mma_scales_size(rows, K)
 
 
-def imp_nvfp4_prepare_mma(t: ImpNvfp4Tensor, mma_scales: int, nbytes: int,
-                          stream: int | None) -> int:
-    return _L().imp_nvfp4_prepare_mma(ctypes.byref(t), mma_scales, nbytes, stream)
+def imp_nvfp4_mma_codes_size(rows: int, K: int) -> int:
+    return _L().imp_nvfp4_mma_codes_size(rows, K)
+
+
+def imp_nvfp4_prepare_mma(t: ImpNvfp4Tensor, mma_codes: int | None, codes_bytes: int,
+                          mma_scales: int | None, scales_bytes: int, stream: int | None) -> int:
+    return _L().imp_nvfp4_prepare_mma(ctypes.byref(t), mma_codes, codes_bytes, mma_scales,
+                                      scales_bytes, stream)
+
+
+def imp_nvfp4_gemm_mma(x_bf16: int, M: int, K: int, ldx: int, w: ImpNvfp4Tensor, y_bf16: int,
+                       ldy: int, dev_status: int | None, workspace: int | None, ws_bytes: int,
+                       stream: int | None) -> int:
+    return _L().imp_nvfp4_gemm_mma(x_bf16, M, K, ldx, ctypes.byref(w), y_bf16, ldy, dev_status,
+                                   workspace, ws_bytes, stream)
 
 
 def imp_nvfp4_quantize_mma(x_bf16: int, rows: int, K: int, ldx: int, out: ImpNvfp4Tensor,
@@ -169,18 +185,21 @@ class ImpError(RuntimeError):
 @dataclass
 class NVFP4Tensor:
     """Device NVFP4 tensor: codes uint8[rows][K/2], scales uint8[rows][K/16],
-    tensor_scale float32[1]."""
+    tensor_scale float32[1] -- or, with layout "mma" (prepare_mma), codes and
+    scales as flat arrays in the tensor-core layout, shape=(rows, K)."""
     codes: "object"
     scales: "object"
     tensor_scale: "object"
+    shape: "tuple | None" = None
+    layout: str = "rows"
 
     @property
     def rows(self) -> int:
-        return self.codes.shape[0]
+        return self.shape[0] if self.shape else self.codes.shape[0]
 
     @property
     def K(self) -> int:
-        return self.codes.shape[1] * 2
+        return self.shape[1] if self.shape else self.codes.shape[1] * 2
 
     def c_struct(self) -> ImpNvfp4Tensor:
         return ImpNvfp4Tensor(self.codes.data_ptr(), self.scales.data_ptr(),
@@ -239,19 +258,24 @@ def gemm(x, w: NVFP4Tensor, y=None, dev_status=None, stream=None, workspace=None
 
 
 def prepare_mma(w: NVFP4Tensor, stream=None) -> NVFP4Tensor:
-    """The same tensor with its block scales laid out as tensor-core atoms."""
+    """The same weight in the tensor-core (MMA) layout: code tiles and scale
+    atoms (flat uint8 arrays); the tensor scale is shared with `w`."""
     import torch
-    nbytes = imp_nvfp4_mma_scales_size(w.rows, w.K)
-    sc = torch.empty(nbytes, dtype=torch.uint8, device=w.codes.device)
-    st = imp_nvfp4_prepare_mma(w.c_struct(), sc.data_ptr(), nbytes, _stream_handle(stream))
+    assert w.layout == "rows"
+    cb = imp_nvfp4_mma_codes_size(w.rows, w.K)
+    sb = imp_nvfp4_mma_scales_size(w.rows, w.K)
+    codes = torch.empty(cb, dtype=torch.uint8, device=w.codes.device)
+    sc = torch.empty(sb, dtype=torch.uint8, device=w.codes.device)
+    st = imp_nvfp4_prepare_mma(w.c_struct(), codes.data_ptr(), cb, sc.data_ptr(), sb,
+                               _stream_handle(stream))
     if st != IMP_OK:
         raise ImpError(st, "imp_nvfp4_prepare_mma")
-    return NVFP4Tensor(w.codes, sc, w.tensor_scale)
+    return NVFP4Tensor(codes, sc, w.tensor_scale, shape=(w.rows, w.K), layout="mma")
 
 
 def _struct(t: NVFP4Tensor) -> ImpNvfp4Tensor:
     return ImpNvfp4Tensor(t.codes.data_ptr(), t.scales.data_ptr(), t.tensor_scale.data_ptr(),
-                          t.codes.shape[0], t.codes.shape[1] * 2)
+                          t.rows, t.K)
 
 
 def quantize_mma(x, dev_status=None, stream=None) -> NVFP4Tensor:
@@ -276,7 +300,8 @@ def quantize_mma(x, dev_status=None, stream=None) -> NVFP4Tensor:
 def gemm_fp4(xq: NVFP4Tensor, wq: NVFP4Tensor, y=None, dev_status=None, stream=None):
     """Y = Xq Wq^T on the block-scaled FP4 tensor cores (atom-layout scales)."""
     import torch
-    M, N = xq.codes.shape[0], wq.codes.shape[0]
+    assert wq.layout == "mma"
+    M, N = xq.rows, wq.rows
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.codes.device)
     st = imp_nvfp4_gemm_fp4(_struct(xq), _struct(wq), y.data_ptr(), y.stride(0),
@@ -284,4 +309,26 @@ def gemm_fp4(xq: NVFP4Tensor, wq: NVFP4Tensor, y=None, dev_status=None, stream=N
                             _stream_handle(stream))
     if st != IMP_OK:
         raise ImpError(st, "imp_nvfp4_gemm_fp4")
+    return y
+
+
+def gemm_mma(x, w: NVFP4Tensor, y=None, dev_status=None, stream=None, workspace=None):
+    """Y = X W^T for a bf16 CUDA matrix X and a weight in MMA layout
+    (prepare_mma): the serving path."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert w.layout == "mma"
+    M, K = x.shape
+    N = w.rows
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ws_bytes = imp_nvfp4_gemm_workspace_size(M, N, K)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    st = imp_nvfp4_gemm_mma(x.data_ptr(), M, K, x.stride(0), w.c_struct(), y.data_ptr(),
+                            y.stride(0), None if dev_status is None else dev_status.data_ptr(),
+                            None if workspace is None else workspace.data_ptr(), ws_bytes,
+                            _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_gemm_mma")
     return y

@@ -122,17 +122,30 @@ size_t imp_nvfp4_mma_scales_size(int64_t rows, int64_t K) {
   return impfp4::mma_scale_bytes(rows, K);
 }
 
-imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_scales, size_t bytes,
-                                 void *stream) {
-  if (!t || !mma_scales || t->rows < 1) return IMP_ERR_INVALID_ARG;
+size_t imp_nvfp4_mma_codes_size(int64_t rows, int64_t K) {
+  if (rows <= 0 || K <= 0 || K % 64) return 0;
+  return impfp4::mma_code_bytes(rows, K);
+}
+
+imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_codes, size_t codes_bytes,
+                                 void *mma_scales, size_t scales_bytes, void *stream) {
+  if (!t || t->rows < 1 || (!mma_codes && !mma_scales)) return IMP_ERR_INVALID_ARG;
   if (t->K <= 0 || t->K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
   imp_status st = check_tensor(t, t->rows, t->K);
   if (st != IMP_OK) return st;
-  if (!aligned16(mma_scales)) return IMP_ERR_MISALIGNED;
-  if (bytes < impfp4::mma_scale_bytes(t->rows, t->K)) return IMP_ERR_WORKSPACE_TOO_SMALL;
-  return from_cuda(impfp4::launch_scale_relayout(t->scales, t->rows, t->K,
-                                                 static_cast<uint8_t *>(mma_scales),
-                                                 static_cast<cudaStream_t>(stream)));
+  if (!aligned16(mma_codes) || !aligned16(mma_scales)) return IMP_ERR_MISALIGNED;
+  if (mma_codes && codes_bytes < impfp4::mma_code_bytes(t->rows, t->K))
+    return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (mma_scales && scales_bytes < impfp4::mma_scale_bytes(t->rows, t->K))
+    return IMP_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (mma_codes)
+    e = impfp4::launch_code_relayout(t->codes, t->rows, t->K, static_cast<uint8_t *>(mma_codes), s);
+  if (e == cudaSuccess && mma_scales)
+    e = impfp4::launch_scale_relayout(t->scales, t->rows, t->K, static_cast<uint8_t *>(mma_scales),
+                                      s);
+  return from_cuda(e);
 }
 
 imp_status imp_nvfp4_quantize_mma(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
@@ -167,7 +180,7 @@ imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor
   if (ldy < N) return IMP_ERR_INVALID_ARG;
   if (!aligned16(y_bf16) || ldy % 8) return IMP_ERR_MISALIGNED;
   return from_cuda(impfp4::launch_gemm_mxf4(xq->codes, xq->scales, xq->tensor_scale, wq->codes,
-                                            wq->scales, wq->tensor_scale, M, N, K,
+                                            true, wq->scales, wq->tensor_scale, M, N, K,
                                             static_cast<uint16_t *>(y_bf16), ldy, dev_status,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -209,8 +222,49 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                                               ws + L.partial, s);
   if (e == cudaSuccess) e = impfp4::launch_scale_relayout(w->scales, N, K, wq.scales, s);
   if (e == cudaSuccess)
-    e = impfp4::launch_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, wq.codes, wq.scales,
-                                 wq.tensor_scale, M, N, K, static_cast<uint16_t *>(y_bf16), ldy,
+    e = impfp4::launch_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, wq.codes, false,
+                                 wq.scales, wq.tensor_scale, M, N, K,
+                                 static_cast<uint16_t *>(y_bf16), ldy, dev_status, s);
+  return from_cuda(e);
+}
+
+imp_status imp_nvfp4_gemm_mma(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                              const imp_nvfp4_tensor *w, void *y_bf16, int64_t ldy,
+                              int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream) {
+  if (M < 0 || !w) return IMP_ERR_INVALID_ARG;
+  if (K <= 0 || K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  const int64_t N = w->rows;
+  if (N < 0 || w->K != K) return IMP_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return IMP_OK;
+  imp_status st = check_tensor(w, N, K);
+  if (st != IMP_OK) return st;
+  if (!x_bf16 || !y_bf16) return IMP_ERR_INVALID_ARG;
+  if (ldx < K || ldy < N) return IMP_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(y_bf16) || ldx % 8 || ldy % 8) return IMP_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M <= kDecodeMaxM) {
+    if (!impfp4::gemv_f4_shape_ok(M, N, K)) return IMP_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = impfp4::gemv_f4_workspace_bytes(M, N, K);
+    if (!workspace || ws_bytes < need) return IMP_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+    return from_cuda(impfp4::launch_gemv_f4(static_cast<const uint16_t *>(x_bf16), M, K, ldx,
+                                            w->codes, w->scales, w->tensor_scale, N,
+                                            static_cast<uint16_t *>(y_bf16), ldy, dev_status,
+                                            workspace, s, true));
+  }
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return IMP_ERR_UNSUPPORTED_SHAPE;
+  const size_t need = imp_nvfp4_gemm_workspace_size(M, N, K);
+  if (!workspace || ws_bytes < need) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  const PrefillWs L = prefill_ws(M, N, K);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  imp_nvfp4_tensor xq = {ws + L.xcodes, ws + L.xsc, reinterpret_cast<float *>(ws + L.sx), M, K};
+  cudaError_t e = impfp4::launch_quantize_mma(static_cast<const uint16_t *>(x_bf16), M, K, ldx,
+                                              xq.codes, xq.scales, xq.tensor_scale, dev_status,
+                                              ws + L.partial, s);
+  if (e == cudaSuccess)
+    e = impfp4::launch_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, w->codes, true, w->scales,
+                                 w->tensor_scale, M, N, K, static_cast<uint16_t *>(y_bf16), ldy,
                                  dev_status, s);
   return from_cuda(e);
 }

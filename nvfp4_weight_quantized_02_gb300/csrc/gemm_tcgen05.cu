@@ -9,10 +9,12 @@
 //
 // Structure (one CTA per SM, persistent over 128 x 256 output tiles):
 //  * warp 0, one thread: TMA producer.  Per K-stage of 256 elements it loads
-//    the X tile (128 rows x 128 bytes) and the W tile (256 rows x 128 bytes)
-//    with 2-D tensor copies in the 128-byte swizzle, and the matching block
-//    scales (already in the 512-byte atom layout, see quantize.cuh) with
-//    bulk copies, into a 4-deep shared-memory ring.
+//    the X tile (128 rows x 128 bytes) with a 2-D tensor copy in the 128-byte
+//    swizzle, the W tile (256 rows x 128 bytes) the same way -- or, for a
+//    weight in the tile layout (quantize.cuh), as two contiguous 16 KB bulk
+//    copies of the same swizzled image -- and the matching block scales
+//    (already in the 512-byte atom layout) with bulk copies, into a 4-deep
+//    shared-memory ring.
 //  * warp 1: allocates 512 tensor-memory columns; one thread issues, per
 //    stage, twelve tcgen05.cp (per 64-element K step: the scales of the X rows
 //    and of the two 128-row halves of the W tile, into one of two column
@@ -26,6 +28,8 @@
 //    the accumulator back, then stores to Y while the next tile's MMAs run.
 // Every wait is bounded; on a timeout the kernel reports IMP_DEV_TIMEOUT,
 // drains its own copies and MMAs, frees tensor memory and returns.
+#include <cstring>
+
 #include "gemm_tcgen05.cuh"
 #include "quantize.cuh"
 #include "tma.cuh"
@@ -56,6 +60,7 @@ constexpr size_t kSmemBytes = 1024 + NSTAGE * (size_t)STAGE_BYTES + kBarBytes;
 struct GemmArgs {
   const uint8_t *sfa;  // X block scales, atom layout
   const uint8_t *sfb;  // W block scales, atom layout
+  const uint8_t *w_tiles;  // W codes in the 16 KB tile layout, or nullptr: TMA on row-major codes
   const float *s_x, *s_w;
   uint16_t *y;
   int64_t ldy;
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
+    if (!a.w_tiles) prefetch_tmap(&tmB);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -189,7 +194,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t *st = smem + (size_t)s * STAGE_BYTES;
           mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES + 3u * natoms * 512u);
           tma_load_2d(st, &tmA, ks * (BK / 2), mb * BM, &full[s]);
-          tma_load_2d(st + OFF_B, &tmB, ks * (BK / 2), nb * BN, &full[s]);
+          if (a.w_tiles) {
+            // two 128-row tiles, each stored as its swizzled shared-memory image
+            const int64_t nch = (a.K + BK - 1) / BK;
+            bulk_g2s(st + OFF_B, a.w_tiles + ((int64_t)(2 * nb) * nch + ks) * 16384, 16384u,
+                     &full[s]);
+            bulk_g2s(st + OFF_B + 16384, a.w_tiles + ((int64_t)(2 * nb + 1) * nch + ks) * 16384,
+                     16384u, &full[s]);
+          } else {
+            tma_load_2d(st + OFF_B, &tmB, ks * (BK / 2), nb * BN, &full[s]);
+          }
           const int64_t atom0 = (int64_t)ks * KSTEPS;
           bulk_g2s(st + OFF_SFA, a.sfa + ((int64_t)mb * KA + atom0) * 512, natoms * 512u,
                    &full[s]);
@@ -377,19 +391,21 @@ bool make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
 size_t gemm_mxf4_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales,
-                             const float *s_x, const uint8_t *w_codes,
+                             const float *s_x, const uint8_t *w_codes, bool w_tiled,
                              const uint8_t *w_mma_scales, const float *s_w, int64_t M,
                              int64_t N, int64_t K, uint16_t *y, int64_t ldy, int32_t *status,
                              cudaStream_t stream) {
   CUtensorMap tmA, tmB;
+  memset(&tmB, 0, sizeof(tmB));  // not read with tiled W codes
   if (!make_tmap_u8_2d(&tmA, x_codes, (uint64_t)M, (uint64_t)(K / 2), (uint64_t)(K / 2), BM, 128,
                        true) ||
-      !make_tmap_u8_2d(&tmB, w_codes, (uint64_t)N, (uint64_t)(K / 2), (uint64_t)(K / 2), BN, 128,
-                       true))
+      (!w_tiled && !make_tmap_u8_2d(&tmB, w_codes, (uint64_t)N, (uint64_t)(K / 2),
+                                    (uint64_t)(K / 2), BN, 128, true)))
     return cudaErrorInvalidValue;
   GemmArgs a;
   a.sfa = x_mma_scales;
   a.sfb = w_mma_scales;
+  a.w_tiles = w_tiled ? w_codes : nullptr;
   a.s_x = s_x;
   a.s_w = s_w;
   a.y = y;

@@ -34,9 +34,12 @@ cudaError_t launch_gemv_tc(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
 bool gemv_f4_shape_ok(int64_t M, int64_t N, int64_t K);
 size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K);
 bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const void *scales);
+// `prepared`: codes and scales in the tensor-core (MMA) layout of
+// quantize.cuh (contiguous 16 KB code tiles and 2 KB scale-atom runs per
+// stage) instead of row-major.
 cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool prepared = false);
 
 }  // namespace impfp4

@@ -30,14 +30,15 @@
 //
 // Two kernels share that scheme:
 //  * gemv_f4r_kernel (M <= 2, the usual decode case): everything in one
-//    launch.  Warp 3 streams W (codes: 128 rows x 128 B tiles, 128-byte
-//    swizzle; scales: 128 rows x 16 B) through a 6-deep ring with TMA and
+//    launch.  Warp 4 streams W (codes: 128 rows x 128 B tiles, 128-byte
+//    swizzle; scales: 128 rows x 16 B) through an 8-deep ring with TMA and
 //    never waits for the previous kernel (W is never written on the
-//    stream).  Meanwhile warps 4..11 wait for it and split the K chunks of
+//    stream).  Meanwhile warps 5..11 wait for it and split the K chunks of
 //    X this CTA needs into components directly in shared memory (B operand,
-//    swizzled, and its scale atoms), publishing each chunk as soon as it is
-//    split; warps 0..2 issue the MMAs (stage i -> issuer i % 3) as chunks
-//    become ready, and warps 8..11 go on to the epilogue.
+//    swizzled, and its scale atoms); warps 0..3 issue the MMAs (stage i ->
+//    issuer i % 4) as chunks become ready, and warps 8..11 go on to the
+//    epilogue.  A weight already in the tensor-core layout (quantize.cuh)
+//    is read with two contiguous bulk copies per stage instead.
 //  * gemv_f4_kernel (M = 3..16, passes of up to four rows of X): a separate
 //    split kernel (xsplit_kernel) writes the components and scale atoms to
 //    the workspace, and they travel with W in each stage of an 8-deep ring;
@@ -50,6 +51,7 @@
 // Every wait is bounded; on a timeout the kernel reports IMP_DEV_TIMEOUT,
 // drains its own copies and MMAs, frees tensor memory and returns.
 #include <atomic>
+#include <cstring>
 #include <chrono>
 #include <mutex>
 #include <random>
@@ -86,16 +88,20 @@ template <int NMMA> struct StageS {
 };
 
 // ---- resident-B kernel (M <= 2, N_MMA = 16)
-constexpr int kIssuersR = 3, kProducerR = 3, kNSR = 6;  // stage st and st - 6: same issuer
+constexpr int kIssuersR = 4, kProducerR = 4, kNSR = 8;  // stage st and st - 8: same issuer
 constexpr int kMaxSlotsR = 24;                           // K chunks of X held per CTA
-constexpr int kHelperWarp0R = 4;                         // warps 4..11 split X
+constexpr int kHelperWarp0R = 5;                         // warps 5..11 split X
 constexpr int kHelperThreadsR = kThreads - 32 * kHelperWarp0R;
+// W scales land where their atoms go: a row-major weight's 128 x 16-byte
+// scale rows are relaid in place (read, warp sync, write).
 struct StageR {
-  static constexpr uint32_t W = 0, RAW = 16384, SFA = RAW + 2048, BYTES = SFA + 2048;
+  static constexpr uint32_t W = 0, RAW = 16384, SFA = 16384, BYTES = 18432;
   static constexpr uint32_t TX = 16384 + 2048;
 };
-// B slot q: codes at BCODES + 2048 q (16 rows x 128 B, swizzled); the scale
-// atoms of its four K64 steps at BSF + 2048 q + 512 t.
+// B slot q: codes at BCODES + 2048 q (16 rows x 128 B, swizzled); the scales
+// of its four K64 steps at BSF + 1024 q + 256 t: operand rows 0..15 are lines
+// 0..15 of a 512-byte atom, whose copy reads 256 bytes past them (the next
+// step's lines, or a zeroed pad) into lanes no N = 16 MMA reads.
 
 struct F4Args {
   const uint16_t *x;    // resident kernel: X rows
@@ -114,6 +120,8 @@ struct F4Args {
   int n_chunks;         // K / 256
   unsigned long long epoch;  // unique per launch
   int n_slots;          // resident kernel: B slots in shared memory
+  const uint8_t *wc;    // prepared weight: code tiles [128-row block][chunk][16 KB]
+  const uint8_t *wsa;   // prepared weight: scale atoms [128-row block][K/64][512 B]
 };
 
 struct F4Bars {
@@ -356,7 +364,7 @@ __device__ __forceinline__ bool count_segment(unsigned __int128 *c, unsigned lon
 // `sfb_desc(i, st, t)`: the B operand and its scale atom for K64 step t of
 // processing position i (stage st); `b_wait(st)`: waits (bounded) until that
 // B is in shared memory.
-template <int NI, int NS, int NMMA, class Stage, class BDesc, class SFBDesc, class BWait>
+template <int NI, int NS, int NMMA, bool PREP, class Stage, class BDesc, class SFBDesc, class BWait>
 __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const StreamK &sk,
                             int is, int lane, int32_t *status, BDesc b_desc, SFBDesc sfb_desc,
                             BWait b_wait) {
@@ -382,12 +390,13 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
         ok = false;
         break;
       }
-      {  // W scales, row-major [128][16 B] -> four 512-byte atoms
+      if (!PREP) {  // W scales, row-major [128][16 B] -> four 512-byte atoms
         uint8_t *stg = smem + (size_t)s * Stage::BYTES;
         uint4 rq[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           rq[q] = *reinterpret_cast<const uint4 *>(stg + Stage::RAW + 16 * (lane + 32 * q));
+        __syncwarp();  // the atoms may overwrite the rows just read
         *reinterpret_cast<uint4 *>(stg + Stage::SFA + 0 * 512 + 16 * lane) = make_uint4(rq[0].x, rq[1].x, rq[2].x, rq[3].x);
         *reinterpret_cast<uint4 *>(stg + Stage::SFA + 1 * 512 + 16 * lane) = make_uint4(rq[0].y, rq[1].y, rq[2].y, rq[3].y);
         *reinterpret_cast<uint4 *>(stg + Stage::SFA + 2 * 512 + 16 * lane) = make_uint4(rq[0].z, rq[1].z, rq[2].z, rq[3].z);
@@ -602,7 +611,7 @@ __global__ void __launch_bounds__(kXsplitThreads)
     }
 }
 
-template <int NMMA>
+template <int NMMA, bool PREP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
                    const __grid_constant__ CUtensorMap tm_b, const F4Args a) {
@@ -624,18 +633,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerS) {
     if (lane == 0) {
-      prefetch_tmap(&tm_w);
-      prefetch_tmap(&tm_ws);
+      if (!PREP) {
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_ws);
+      }
       prefetch_tmap(&tm_b);
       // processing position i -> ring slot i % NS, stage stage_of(i)
       auto load_w = [&](int i) {
         const int s = i % kNSS;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
         const int64_t g = sk.g_begin + sk.stage_of(i);
-        const int row0 = (int)(g / sk.nch) * kTileRows, ch = (int)(g % sk.nch);
+        const int64_t tile = g / sk.nch;
+        const int row0 = (int)tile * kTileRows, ch = (int)(g % sk.nch);
         mbar_arrive_expect_tx(&bars.full[s], L::TX);
-        tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
-        tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
+        if (PREP) {
+          bulk_g2s(stg + L::W, a.wc + (tile * sk.nch + ch) * 16384, 16384u, &bars.full[s]);
+          bulk_g2s(stg + L::SFA, a.wsa + (tile * (a.K / 64) + 4 * ch) * 512, 2048u, &bars.full[s]);
+        } else {
+          tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
+          tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
+        }
       };
       auto load_x = [&](int i) {
         const int s = i % kNSS;
@@ -644,16 +661,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(stg + L::B, &tm_b, ch * (kChunkK / 2), 0, &bars.full[s]);
         bulk_g2s(stg + L::SFB, a.sfb + (size_t)ch * 2048, 2048u, &bars.full[s]);
       };
+      auto prefetch_w = [&](int i) {
+        const int64_t g = sk.g_begin + sk.stage_of(i);
+        const int64_t tile = g / sk.nch;
+        const int ch = (int)(g % sk.nch);
+        if (PREP) {
+          bulk_prefetch_l2(a.wc + (tile * sk.nch + ch) * 16384, 16384u);
+          bulk_prefetch_l2(a.wsa + (tile * (a.K / 64) + 4 * ch) * 512, 2048u);
+        } else {
+          tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), (int)tile * kTileRows);
+          tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), (int)tile * kTileRows);
+        }
+      };
       // W of the first stages before the previous kernel has finished, and
       // more W into L2: HBM keeps streaming while X is being split.
       const int pre = min(kNSS, sk.n_st);
       for (int i = 0; i < pre; ++i) load_w(i);
-      for (int i = pre; i < min(pre + kPrefetch, sk.n_st); ++i) {
-        const int64_t g = sk.g_begin + sk.stage_of(i);
-        const int row0 = (int)(g / sk.nch) * kTileRows, ch = (int)(g % sk.nch);
-        tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), row0);
-        tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), row0);
-      }
+      for (int i = pre; i < min(pre + kPrefetch, sk.n_st); ++i) prefetch_w(i);
       asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int i = 0; i < pre; ++i) load_x(i);
       int i = pre;
@@ -677,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto sfb_desc = [&](int i, int, int t) {
       return dSB0 + (uint64_t)((i % kNSS) * (L::BYTES >> 4)) + 32u * t;
     };
-    issuer_loop<kIssuersS, kNSS, NMMA, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
+    issuer_loop<kIssuersS, kNSS, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
                                           sfb_desc, [](int) { return true; });
   } else if (warp >= kEpiWarp0) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -697,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- resident-B path (M <= 2) ---------------------------------------------------
 
+template <bool PREP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_f4r_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
                     const F4Args a) {
@@ -705,8 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *bcodes = smem + kNSR * L::BYTES;                   // [slot][16 rows][128 B], swizzled
-  uint8_t *bsf = bcodes + (size_t)a.n_slots * 2048;           // [slot][4 steps][512 B]
-  F4Bars &bars = *reinterpret_cast<F4Bars *>(bsf + (size_t)a.n_slots * 2048);
+  uint8_t *bsf = bcodes + (size_t)a.n_slots * 2048;           // [slot][4 steps][256 B] + pad
+  F4Bars &bars = *reinterpret_cast<F4Bars *>(bsf + (size_t)a.n_slots * 1024 + 256);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const StreamK sk(a.n_tiles, a.n_chunks);
   // B slot of chunk ch: this CTA's chunks run consecutively from ch_begin
@@ -731,25 +756,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     // W only: it is never written on the stream, so no wait for the
     // previous kernel.
     if (lane == 0) {
-      prefetch_tmap(&tm_w);
-      prefetch_tmap(&tm_ws);
+      if (!PREP) {
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_ws);
+      }
       // processing position i -> ring slot i % NS, stage stage_of(i)
       auto load_w = [&](int i) {
         const int s = i % kNSR;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
         const int64_t g = sk.g_begin + sk.stage_of(i);
-        const int row0 = (int)(g / sk.nch) * kTileRows, ch = (int)(g % sk.nch);
+        const int64_t tile = g / sk.nch;
+        const int row0 = (int)tile * kTileRows, ch = (int)(g % sk.nch);
         mbar_arrive_expect_tx(&bars.full[s], L::TX);
-        tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
-        tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
+        if (PREP) {
+          bulk_g2s(stg + L::W, a.wc + (tile * sk.nch + ch) * 16384, 16384u, &bars.full[s]);
+          bulk_g2s(stg + L::SFA, a.wsa + (tile * (a.K / 64) + 4 * ch) * 512, 2048u, &bars.full[s]);
+        } else {
+          tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
+          tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
+        }
       };
       const int pre = min(kNSR, sk.n_st);
       for (int i = 0; i < pre; ++i) load_w(i);
       for (int i = pre; i < min(pre + kPrefetch, sk.n_st); ++i) {
         const int64_t g = sk.g_begin + sk.stage_of(i);
-        const int row0 = (int)(g / sk.nch) * kTileRows, ch = (int)(g % sk.nch);
-        tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), row0);
-        tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), row0);
+        const int64_t tile = g / sk.nch;
+        const int ch = (int)(g % sk.nch);
+        if (PREP) {
+          bulk_prefetch_l2(a.wc + (tile * sk.nch + ch) * 16384, 16384u);
+          bulk_prefetch_l2(a.wsa + (tile * (a.K / 64) + 4 * ch) * 512, 2048u);
+        } else {
+          tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), (int)tile * kTileRows);
+          tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), (int)tile * kTileRows);
+        }
       }
       int i = pre;
       for (; i < sk.n_st; ++i) {
@@ -761,14 +800,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&bars.full[k % kNSR], (uint32_t)((k / kNSR) & 1), a.status);
     }
   } else if (warp >= kHelperWarp0R) {
-    // ---- warps 4..11: split this CTA's chunks of X into shared memory.
-    // Helper warp h (8 of them) takes slots h, h + 8, h + 16; lane 2 bb + f
+    // ---- warps 5..11: split this CTA's chunks of X into shared memory.
+    // Helper warp h (7 of them) takes slots h, h + 7, ...; lane 2 bb + f
     // holds elements 8 f .. 8 f + 7 of block bb of each slot's chunk, for
-    // each row of X; the three slots are split together (independent chains
+    // each row of X; a warp's slots are split together (independent chains
     // side by side).  The prescale comes from this CTA's own blocks: partial
     // sums leave the CTA in true units, so CTAs need not agree on it.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int hw = warp - kHelperWarp0R;  // helper warp 0..7
+    const int hw = warp - kHelperWarp0R;  // helper warp 0..6
     const int bb_l = lane >> 1, hf = lane & 1;
     constexpr int kHelperWarps = kHelperThreadsR / 32;
     constexpr int KS = (kMaxSlotsR + kHelperWarps - 1) / kHelperWarps;
@@ -803,9 +842,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < KS; ++k) {
       const int qs = hw + kHelperWarps * k;
       if (qs >= a.n_slots) break;  // warp-uniform
-      uint4 *z = reinterpret_cast<uint4 *>(bsf + qs * 2048);
+      uint4 *z = reinterpret_cast<uint4 *>(bsf + qs * 1024);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) z[lane + 32 * i] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < 2; ++i) z[lane + 32 * i] = make_uint4(0, 0, 0, 0);
+      if (qs == a.n_slots - 1 && lane < 16) z[64 + lane] = make_uint4(0, 0, 0, 0);  // the pad
       if (a.M == 1) {
         uint4 *zc = reinterpret_cast<uint4 *>(bcodes + qs * 2048 + 1024);
         zc[lane] = make_uint4(0, 0, 0, 0);
@@ -861,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (qs < a.n_slots) {
             *reinterpret_cast<uint32_t *>(bcodes + qs * 2048 + n * 128 +
                                           (((bb_l >> 1) ^ (n & 7)) << 4) + 8 * (bb_l & 1) + 4 * hf) = cw;
-            if (hf == 0) bsf[qs * 2048 + (bb_l >> 2) * 512 + 16 * n + (bb_l & 3)] = (uint8_t)sb;
+            if (hf == 0) bsf[qs * 1024 + (bb_l >> 2) * 256 + 16 * n + (bb_l & 3)] = (uint8_t)sb;
           }
         }
       }
@@ -879,10 +919,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dSB0 = sdesc(smem_u32(bsf), 0, 128, kNoSwizzle);
     auto b_desc = [&](int, int st, int t) { return dB0 + (uint64_t)(slot_of(st) * (2048 >> 4)) + 2u * t; };
     auto sfb_desc = [&](int, int st, int t) {
-      return dSB0 + (uint64_t)(slot_of(st) * (2048 >> 4)) + (uint64_t)(32u * t);
+      return dSB0 + (uint64_t)(slot_of(st) * (1024 >> 4)) + (uint64_t)(16u * t);
     };
     auto b_wait = [&](int st) { return mbar_wait_bounded(&bars.b_ready[slot_of(st)], 0u, a.status); };
-    issuer_loop<kIssuersR, kNSR, NMMA, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
+    issuer_loop<kIssuersR, kNSR, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
                                           sfb_desc, b_wait);
   }
 
@@ -926,7 +966,8 @@ F4Ws f4_ws(int64_t M, int64_t N, int64_t K) {
 
 template <int NMMA> size_t smem_s() { return (size_t)kNSS * StageS<NMMA>::BYTES + sizeof(F4Bars) + 1024; }
 size_t smem_r(int n_slots) {
-  return (size_t)kNSR * StageR::BYTES + (size_t)n_slots * (2048 + 2048) + sizeof(F4Bars) + 1024;
+  return (size_t)kNSR * StageR::BYTES + (size_t)n_slots * (2048 + 1024) + 256 + sizeof(F4Bars) +
+         1024;
 }
 
 // B slots the resident kernel needs: the most distinct K chunks any CTA sees.
@@ -1026,16 +1067,29 @@ F4Args base_args(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const flo
   return a;
 }
 
+// Tensor maps of a row-major weight (a prepared weight is read with bulk
+// copies: its maps stay zero and unread).
+bool weight_maps(bool prepared, const uint8_t *codes, const uint8_t *scales, int64_t N, int64_t K,
+                 CUtensorMap &mw, CUtensorMap &ms) {
+  if (prepared) {
+    memset(&mw, 0, sizeof(mw));
+    memset(&ms, 0, sizeof(ms));
+    return true;
+  }
+  return cached_map(mw, codes, (uint64_t)N, (uint64_t)(K / 2), kTileRows, 128, true) &&
+         cached_map(ms, scales, (uint64_t)N, (uint64_t)(K / 16), kTileRows, 16, false);
+}
+
 cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                                  const uint8_t *codes, const uint8_t *scales,
                                  const float *tensor_scale, int64_t N, uint16_t *y, int64_t ldy,
-                                 int32_t *status, void *workspace, cudaStream_t stream) {
+                                 int32_t *status, void *workspace, cudaStream_t stream,
+                                 bool prepared) {
   const int nmma = nmma_for(M);
   const F4Ws L = f4_ws(M, N, K);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   CUtensorMap mw, ms, mb;
-  if (!cached_map(mw, codes, (uint64_t)N, (uint64_t)(K / 2), kTileRows, 128, true) ||
-      !cached_map(ms, scales, (uint64_t)N, (uint64_t)(K / 16), kTileRows, 16, false) ||
+  if (!weight_maps(prepared, codes, scales, N, K, mw, ms) ||
       !cached_map(mb, ws + L.bcodes, (uint64_t)nmma, (uint64_t)(K / 2), (uint32_t)nmma, 128, true))
     return cudaErrorInvalidValue;
   // components of X (programmatic dependent launch: may start while the
@@ -1055,10 +1109,18 @@ cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_
                                              reinterpret_cast<int32_t *>(ws + L.sh));
     if (e != cudaSuccess) return e;
   }
-  const F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status, ws, L);
-  return nmma == 16
-             ? launch_pdl(gemv_f4_kernel<16>, L.grid, kThreads, smem_s<16>(), stream, mw, ms, mb, a)
-             : launch_pdl(gemv_f4_kernel<32>, L.grid, kThreads, smem_s<32>(), stream, mw, ms, mb, a);
+  F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status, ws, L);
+  a.wc = codes;
+  a.wsa = scales;
+  if (prepared)
+    return nmma == 16 ? launch_pdl(gemv_f4_kernel<16, true>, L.grid, kThreads, smem_s<16>(), stream,
+                                   mw, ms, mb, a)
+                      : launch_pdl(gemv_f4_kernel<32, true>, L.grid, kThreads, smem_s<32>(), stream,
+                                   mw, ms, mb, a);
+  return nmma == 16 ? launch_pdl(gemv_f4_kernel<16, false>, L.grid, kThreads, smem_s<16>(), stream,
+                                 mw, ms, mb, a)
+                    : launch_pdl(gemv_f4_kernel<32, false>, L.grid, kThreads, smem_s<32>(), stream,
+                                 mw, ms, mb, a);
 }
 
 }  // namespace
@@ -1079,19 +1141,22 @@ bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const
 cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool prepared) {
   if (M <= 2) {
     const F4Ws L = f4_ws(M, N, K);
     const int n_slots = slots_r(N, K, L.grid);
     if (n_slots <= kMaxSlotsR) {
       CUtensorMap mw, ms;
-      if (!cached_map(mw, codes, (uint64_t)N, (uint64_t)(K / 2), kTileRows, 128, true) ||
-          !cached_map(ms, scales, (uint64_t)N, (uint64_t)(K / 16), kTileRows, 16, false))
-        return cudaErrorInvalidValue;
+      if (!weight_maps(prepared, codes, scales, N, K, mw, ms)) return cudaErrorInvalidValue;
       F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status,
                            static_cast<uint8_t *>(workspace), L);
       a.n_slots = n_slots;
-      return launch_pdl(gemv_f4r_kernel, L.grid, kThreads, smem_r(n_slots), stream, mw, ms, a);
+      a.wc = codes;
+      a.wsa = scales;
+      return prepared ? launch_pdl(gemv_f4r_kernel<true>, L.grid, kThreads, smem_r(n_slots), stream,
+                                   mw, ms, a)
+                      : launch_pdl(gemv_f4r_kernel<false>, L.grid, kThreads, smem_r(n_slots), stream,
+                                   mw, ms, a);
     }
   }
   // passes of up to four rows of X, each one stream of W (the workspace is
@@ -1100,7 +1165,7 @@ cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
     const int64_t mp = M - m0 < 4 ? M - m0 : 4;
     const cudaError_t e = launch_pass_streamed(x + m0 * ldx, mp, K, ldx, codes, scales,
                                                tensor_scale, N, y + m0 * ldy, ldy, status,
-                                               workspace, stream);
+                                               workspace, stream, prepared);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -208,7 +208,35 @@ __global__ void scale_relayout_kernel(const uint8_t *__restrict__ scales, int64_
   }
 }
 
+// One thread per 16-byte unit of the tile layout.
+__global__ void code_relayout_kernel(const uint8_t *__restrict__ codes, int64_t rows, int64_t K,
+                                     uint8_t *__restrict__ mma_codes, int64_t total_units) {
+  const int64_t KH = K / 2, nch = mma_code_chunks(K);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_units;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = i / 1024, w = i % 1024;  // 1024 units of 16 B per tile
+    const int64_t rb = tile / nch, c = tile % nch;
+    const int rr = (int)(w / 8), up = (int)(w % 8);   // row in tile, stored unit
+    const int u = up ^ (rr & 7);                       // logical unit of that row
+    const int64_t r = rb * 128 + rr, kb = c * 128 + 16 * u;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < rows && kb < KH) v = *reinterpret_cast<const uint4 *>(codes + r * KH + kb);
+    reinterpret_cast<uint4 *>(mma_codes)[i] = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_code_relayout(const uint8_t *codes, int64_t rows, int64_t K, uint8_t *mma_codes,
+                                 cudaStream_t stream) {
+  const int64_t units = (int64_t)mma_code_bytes(rows, K) / 16;
+  int64_t grid = ceil_div(units, 256);
+  const int64_t cap = (int64_t)num_sms_cached() * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  code_relayout_kernel<<<(int)grid, 256, 0, stream>>>(codes, rows, K, mma_codes, units);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_scale_relayout(const uint8_t *scales, int64_t rows, int64_t K,
                                   uint8_t *mma_scales, cudaStream_t stream) {

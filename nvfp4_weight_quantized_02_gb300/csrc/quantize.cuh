@@ -48,6 +48,27 @@ __host__ __device__ inline int64_t mma_scale_offset(int64_t r, int64_t kb, int64
          (kb % 4);
 }
 
+// ---- code layout used by the tensor-core paths --------------------------------
+//
+// The E2M1 codes of a weight in "tiles": 128 rows x 256 elements (128 bytes
+// per row, 16 KB per tile), each tile stored exactly as a 128-byte-swizzled
+// shared-memory operand tile (row rr at rr * 128, its 16-byte unit u at unit
+// u ^ (rr % 8)), so one contiguous copy of 16 KB loads it.  Tiles run along K
+// (K padded to a multiple of 256), then down the rows (rows padded to a
+// multiple of 256, like the scales).  Padding is zero.
+__host__ __device__ inline int64_t mma_code_chunks(int64_t K) { return (K + 255) / 256; }
+__host__ __device__ inline size_t mma_code_bytes(int64_t rows, int64_t K) {
+  return (size_t)mma_scale_rows(rows) * (size_t)mma_code_chunks(K) * 128;
+}
+// Byte offset of the tile (row block rb of 128 rows, K chunk c of 256).
+__host__ __device__ inline int64_t mma_code_tile(int64_t rb, int64_t c, int64_t K) {
+  return (rb * mma_code_chunks(K) + c) * 16384;
+}
+
+// Row-major codes [rows][K/2] -> the tile layout above.
+cudaError_t launch_code_relayout(const uint8_t *codes, int64_t rows, int64_t K, uint8_t *mma_codes,
+                                 cudaStream_t stream);
+
 // Row-major scales [rows][K/16] -> the atom layout above (padding rows = 0).
 cudaError_t launch_scale_relayout(const uint8_t *scales, int64_t rows, int64_t K,
                                   uint8_t *mma_scales, cudaStream_t stream);

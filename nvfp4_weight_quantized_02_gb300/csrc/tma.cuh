@@ -34,6 +34,11 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x
                : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16) at 16-byte aligned `src` into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

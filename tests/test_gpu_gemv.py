@@ -14,17 +14,25 @@ pkg = pytest.importorskip("nvfp4_weight_quantized_02_gb300")
 pytestmark = pytest.mark.gpu
 
 
-def run_gemm(x_bits, w_dev, ldx=None, ldy=None):
+def run_gemm(x_bits, w_dev, ldx=None, ldy=None, via="gemm"):
     x = dev_bf16(x_bits, ldx)
     M, N = x_bits.shape[0], w_dev.rows
     ldy = ldy or N
     ybig = torch.full((M, ldy), float("nan"), dtype=torch.bfloat16, device="cuda")
     y = ybig[:, :N]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pkg.gemm(x, w_dev, y=y, dev_status=status)
+    if via == "gemm":
+        pkg.gemm(x, w_dev, y=y, dev_status=status)
+    else:  # the weight in MMA layout (decode kernels read 16 KB tiles)
+        pkg.gemm_mma(x, pkg.prepare_mma(w_dev), y=y, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return y.float().cpu().numpy()
+
+
+def mma_ok(M, K, N):
+    """Shapes the decode path of gemm_mma takes."""
+    return K % 256 == 0 and K >= 1024 and N >= 128
 
 
 def oracle_w(lin):
@@ -36,11 +44,12 @@ def oracle_w(lin):
 SMALL = synth.workload("single_1k") + synth.workload("decode_0p6b")
 
 
+@pytest.mark.parametrize("via", ["gemm", "gemm_mma"])
 @pytest.mark.parametrize("lin", SMALL, ids=lambda l: f"{l.name}_{l.K}x{l.N}")
-def test_small_workloads_every_element(lin):
+def test_small_workloads_every_element(lin, via):
     c, s, ts = oracle_w(lin)
     x = lin.act_bf16()
-    y = run_gemm(x, dev_nvfp4(c, s, ts))
+    y = run_gemm(x, dev_nvfp4(c, s, ts), via=via)
     y_ref, bound = oracle.reference_gemm(x, lin.M, c, s, ts)
     check_within_tolerance(y, y_ref, bound, lin.name)
 
@@ -48,12 +57,13 @@ def test_small_workloads_every_element(lin):
 FULL = synth.workload("decode_27b") + synth.workload("skinny_27b")
 
 
+@pytest.mark.parametrize("via", ["gemm", "gemm_mma"])
 @pytest.mark.parametrize("lin", FULL, ids=lambda l: f"{l.name}_M{l.M}_{l.K}x{l.N}")
-def test_full_size_sampled(lin):
+def test_full_size_sampled(lin, via):
     w_bits = lin.weight_bf16()
     w = pkg.quantize(dev_bf16(w_bits))
     x = lin.act_bf16()
-    y = run_gemm(x, w)
+    y = run_gemm(x, w, via=via)
     _, ts, _ = oracle.tensor_scale(w_bits)
     rows = sample_rows(lin.N, seed=lin.N + lin.M)
     c, s = oracle.quantize_rows(w_bits[rows], ts)
@@ -87,9 +97,18 @@ def test_edge_shapes(M, K, N, ldx, ldy):
                        zero_block_p=0.02, x_outlier_frac=0.02)
     c, s, ts = oracle_w(lin)
     x = lin.act_bf16()
-    y = run_gemm(x, dev_nvfp4(c, s, ts), ldx, ldy)
     y_ref, bound = oracle.reference_gemm(x, M, c, s, ts)
-    check_within_tolerance(y, y_ref, bound, f"M{M} K{K} N{N}")
+    vias = ["gemm", "gemm_mma"] if mma_ok(M, K, N) else ["gemm"]
+    for via in vias:
+        y = run_gemm(x, dev_nvfp4(c, s, ts), ldx, ldy, via=via)
+        check_within_tolerance(y, y_ref, bound, f"M{M} K{K} N{N} {via}")
+
+
+def test_gemm_mma_rejects_shapes_outside_the_decode_path():
+    lin = synth.Linear("rej", 1, 320, 200, 3)
+    c, s, ts = oracle_w(lin)
+    with pytest.raises(pkg.ImpError, match="UNSUPPORTED_SHAPE"):
+        run_gemm(lin.act_bf16(), dev_nvfp4(c, s, ts), via="gemm_mma")
 
 
 def test_extreme_activation_magnitudes():
@@ -123,10 +142,21 @@ def test_extreme_activation_magnitudes_per_row(M, N):
     check_within_tolerance(y, y_ref, bound, f"M{M} rows ~ 2^{exps}")
 
 
-def test_bitwise_repeatable():
+@pytest.mark.parametrize("via", ["gemm", "gemm_mma"])
+def test_bitwise_repeatable(via):
     lin = synth.workload("decode_27b")[2]
     w = pkg.quantize(dev_bf16(lin.weight_bf16()))
     x = lin.act_bf16()
-    a = run_gemm(x, w)
-    b = run_gemm(x, w)
+    a = run_gemm(x, w, via=via)
+    b = run_gemm(x, w, via=via)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_prepared_and_row_major_weights_give_identical_results():
+    # same kernels and schedule, only the copies differ
+    lin = synth.workload("decode_27b")[0]
+    w = pkg.quantize(dev_bf16(lin.weight_bf16()))
+    x = lin.act_bf16()
+    a = run_gemm(x, w, via="gemm")
+    b = run_gemm(x, w, via="gemm_mma")
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

@@ -27,13 +27,34 @@ def atom_layout(scales: np.ndarray, K: int) -> np.ndarray:
     return out
 
 
+def tile_layout(codes: np.ndarray, K: int) -> np.ndarray:
+    """Row-major [rows][K/2] code bytes -> the documented 16 KB tile layout
+    (128 rows x 128 bytes per tile, 16-byte unit u of row rr stored at unit
+    u ^ (rr % 8); tiles along K (padded to 256), then down the rows (padded
+    to 256))."""
+    rows = codes.shape[0]
+    rpad = (rows + 255) // 256 * 256
+    nch = (K + 255) // 256
+    src = np.zeros((rpad, nch * 128), np.uint8)
+    src[:rows, : K // 2] = codes
+    t = src.reshape(rpad // 128, 128, nch, 8, 16)       # [rb][rr][c][u][16]
+    t = t.transpose(0, 2, 1, 3, 4).copy()                # [rb][c][rr][u][16]
+    out = np.empty_like(t)
+    rr = np.arange(128)
+    for u in range(8):                                   # unit u goes to u ^ (rr % 8)
+        out[:, :, rr, u ^ (rr % 8), :] = t[:, :, rr, u, :]
+    return out.reshape(-1)
+
+
 def test_prepare_mma_matches_layout_definition():
     rng = np.random.default_rng(0)
-    for rows, K in [(1, 64), (130, 320), (300, 1024)]:
+    for rows, K in [(1, 64), (130, 320), (300, 1024), (260, 768)]:
         sc = rng.integers(0, 0x7F, size=(rows, K // 16), dtype=np.uint8)
-        t = dev_nvfp4(np.zeros((rows, K // 2), np.uint8), sc, 1.0)
-        got = pkg.prepare_mma(t).scales.cpu().numpy()
-        np.testing.assert_array_equal(got, atom_layout(sc, K))
+        cd = rng.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+        t = dev_nvfp4(cd, sc, 1.0)
+        p = pkg.prepare_mma(t)
+        np.testing.assert_array_equal(p.scales.cpu().numpy(), atom_layout(sc, K))
+        np.testing.assert_array_equal(p.codes.cpu().numpy(), tile_layout(cd, K))
 
 
 def test_quantize_mma_equals_quantize_plus_layout():
@@ -58,6 +79,8 @@ def run_prefill(lin, rows_check=None, cols_check=None, via="gemm"):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     if via == "gemm":
         y = pkg.gemm(dev_bf16(xb), w, dev_status=status)
+    elif via == "gemm_mma":
+        y = pkg.gemm_mma(dev_bf16(xb), pkg.prepare_mma(w), dev_status=status)
     else:
         xq = pkg.quantize_mma(dev_bf16(xb), dev_status=status)
         y = pkg.gemm_fp4(xq, pkg.prepare_mma(w), dev_status=status)
@@ -83,6 +106,7 @@ def test_small_shapes_every_element(M, K, N):
                        zero_block_p=0.01, x_outlier_frac=0.01)
     run_prefill(lin, via="gemm_fp4")
     run_prefill(lin, via="gemm")
+    run_prefill(lin, via="gemm_mma")
 
 
 @pytest.mark.parametrize("lin", synth.workload("prefill_27b"), ids=lambda l: f"{l.K}x{l.N}")
@@ -90,6 +114,7 @@ def test_full_size_sampled(lin):
     rows = np.arange(0, lin.M, 32)  # the 64-row sample m = 32 i
     cols = sample_rows(lin.N, seed=lin.K)
     run_prefill(lin, rows_check=rows, cols_check=cols)
+    run_prefill(lin, rows_check=rows, cols_check=cols, via="gemm_mma")
 
 
 def test_repeatable():
