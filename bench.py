@@ -197,11 +197,16 @@ def run_native(args):
         ys.append(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev))
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # one workspace per problem, allocated once (the FP4 decode path's split X,
+    # partial sums and counters)
+    wss = [torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), 16),
+                       dtype=torch.uint8, device=dev) for l in lins]
+    plans = [pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K) for l in lins]
     torch.cuda.synchronize()
 
     def step():
-        for x, w, y in zip(xs, weights, ys):
-            pkg.gemm(x, w, y=y, dev_status=status, stream=stream)
+        for x, w, y, ws in zip(xs, weights, ys, wss):
+            pkg.gemm(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
 
     # per-kernel timing events (on the launching stream)
     def timed_steps(k, per_kernel):
@@ -212,11 +217,11 @@ def run_native(args):
         for _ in range(k):
             if per_kernel:
                 row = []
-                for x, w, y in zip(xs, weights, ys):
+                for x, w, y, ws in zip(xs, weights, ys, wss):
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
-                    pkg.gemm(x, w, y=y, dev_status=status, stream=stream)
+                    pkg.gemm(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
                     e1.record(stream)
                     row.append((e0, e1))
                 evs.append(row)
@@ -261,9 +266,9 @@ def run_native(args):
     d2h = sum(p.numel() * 2 for p in pin_y)
 
     def e2e_step():
-        for px, x, w, y, py in zip(pin_x, xs, weights, ys, pin_y):
+        for px, x, w, y, py, ws in zip(pin_x, xs, weights, ys, pin_y, wss):
             x.copy_(px, non_blocking=True)
-            pkg.gemm(x, w, y=y, dev_status=status, stream=stream)
+            pkg.gemm(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
             py.copy_(y, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -283,11 +288,39 @@ def run_native(args):
     top = int(np.argmax(per_kernel_ms))
     top_bytes = lins[top].weight_bytes + 2 * lins[top].K + 2 * lins[top].N
     achieved = top_bytes / (per_kernel_ms[top] * 1e-3) / 1e9
-    traffic = load_traffic("gemv_tc_kernel", lins[top])
+    top_kernel = plans[top][1]
+    traffic = load_traffic(top_kernel, lins[top])
 
     extra = {}
     if rank == 0 and not args.no_extra:
         extra = bench_extras(args, pkg, dev, stream, hbm_peak)
+        # the same step on weights prepared once in the MMA layout (contiguous
+        # 16 KB code tiles, scale atoms) through imp_nvfp4_gemm_mma
+        prepared = [pkg.prepare_mma(w, stream=stream) for w in weights]
+        pws = [torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), 16),
+                           dtype=torch.uint8, device=dev) for l in lins]
+
+        def prepared_step():
+            for x, w, y, ws in zip(xs, prepared, ys, pws):
+                pkg.gemm_mma(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
+
+        for _ in range(args.warmup):
+            prepared_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            prepared_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        pms = e0.elapsed_time(e1) / args.steps
+        extra["decode_prepared_mma_layout"] = {
+            "ms_per_step": pms, "GB/s": bytes_step / (pms * 1e-3) / 1e9,
+            "frac_of_hbm_peak": bytes_step / (pms * 1e-3) / 1e9 / hbm_peak}
+        del prepared, pws
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} in the prepared step")
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -301,11 +334,12 @@ def run_native(args):
         "per_kernel_us": {l.name: 1e3 * t for l, t in zip(lins, per_kernel_ms)},
         "per_kernel_gbs": {l.name: (l.weight_bytes + 2 * l.K + 2 * l.N) / (t * 1e-3) / 1e9
                            for l, t in zip(lins, per_kernel_ms)},
-        "roofline": {"bound": "hbm", "kernel": f"gemv_tc_kernel ({lins[top].name} "
+        "roofline": {"bound": "hbm", "kernel": f"{top_kernel} ({lins[top].name} "
                      f"{lins[top].K}x{lins[top].N})", "achieved": achieved, "peak": hbm_peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic},
-        "gpu_launches": args.steps * len(lins),
+        "gpu_launches": args.steps * sum(n for n, _ in plans),
+        "kernels": {l.name: {"kernel": k, "launches_per_call": n} for l, (n, k) in zip(lins, plans)},
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -390,34 +424,47 @@ def bench_extras(args, pkg, dev, stream, hbm_peak):
     import torch
 
     out = {"prefill": bench_prefill(args, pkg, dev, stream)}
+    # Skinny M: back-to-back calls cycling through copies of W whose total
+    # exceeds L2 twice over, so each call reads its weight from HBM (no flush
+    # kernel between calls, which would idle the GPU and hide start-up cost).
     lins = synth.workload("skinny_27b")
     skinny = {}
     cache = {}
+    l2 = 129 * 1024 * 1024
     for l in lins:
         key = (l.K, l.N)
         if key not in cache:
             wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
-            cache[key] = pkg.quantize(wb)
+            w0 = pkg.quantize(wb)
             del wb
-        w = cache[key]
+            copies = max(2, -(-2 * l2 // l.weight_bytes))
+            cache[key] = [w0] + [pkg.NVFP4Tensor(w0.codes.clone(), w0.scales.clone(),
+                                                 w0.tensor_scale.clone())
+                                 for _ in range(copies - 1)]
+        ws_list = cache[key]
         x = torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
         y = torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev)
-        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-        times = []
-        for i in range(args.warmup + 10):
-            flush.zero_()  # evict W from L2 between launches
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            pkg.gemm(x, w, y=y, stream=stream)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            if i >= args.warmup:
-                times.append(e0.elapsed_time(e1))
-        t = statistics.median(times)
+        ws = torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), 16),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup):
+            for w in ws_list:
+                pkg.gemm(x, w, y=y, stream=stream, workspace=ws)
+        rounds = 10
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(rounds):
+            for w in ws_list:
+                pkg.gemm(x, w, y=y, stream=stream, workspace=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / (rounds * len(ws_list))
         b = l.weight_bytes + 2 * l.M * l.K + 2 * l.M * l.N
+        n, k = pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K)
         skinny[f"M{l.M}_{l.K}x{l.N}"] = {"us": 1e3 * t, "GB/s": b / (t * 1e-3) / 1e9,
-                                         "TFLOP/s": 2 * l.M * l.N * l.K / (t * 1e-3) / 1e12}
+                                         "TFLOP/s": 2 * l.M * l.N * l.K / (t * 1e-3) / 1e12,
+                                         "kernel": k, "launches": n}
     out["skinny_decode"] = skinny
     del cache
     # quantizer: the LM-head-sized weight

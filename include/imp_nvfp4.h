@@ -125,9 +125,22 @@ imp_status imp_nvfp4_quantize_noalloc(const void *x_bf16, int64_t rows, int64_t 
                                       const imp_nvfp4_tensor *out, int32_t *dev_status,
                                       void *stream);
 
-/* Bytes of workspace imp_nvfp4_gemm needs for Y[M][N] = X[M][K] W^T (0 for
- * M <= 16; for M > 16 the quantized X, X's and W's atom-layout scales). */
+/* Bytes of workspace imp_nvfp4_gemm (and imp_nvfp4_gemm_mma) needs for
+ * Y[M][N] = X[M][K] W^T.  M <= 16: the FP4 decode path's split X, its
+ * partial sums and counters when the shape takes that path
+ * (K % 256 == 0, K >= 1024, N >= 128), else 0.  M > 16: the quantized X and
+ * X's and W's atom-layout scales.  0 also for shapes no path accepts. */
 size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* The plan imp_nvfp4_gemm follows for Y[M][N] = X[M][K] W^T on the current
+ * device, given a workspace of imp_nvfp4_gemm_workspace_size bytes and
+ * 16-byte aligned arrays: returns the number of kernels one call launches
+ * (0 if the call rejects the shape) and stores in *kernel (when kernel is not
+ * NULL) the static name of the kernel that streams W: "gemv_f4r_kernel" /
+ * "gemv_f4_kernel" (FP4 tensor cores, X split per call), "gemv_tc_kernel"
+ * (f16 tensor cores), "gemv_kernel" (CUDA cores) or "gemm_mxf4_kernel"
+ * (prefill).  Host only; launches nothing. */
+int32_t imp_nvfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const char **kernel);
 
 /* Y = X * W^T.
  *   x_bf16   device bf16[M][ldx], ldx >= K, ldx % 8 == 0.

@@ -23,7 +23,8 @@ from .build import INCLUDE, LIB
 __all__ = [
     "IMP_OK", "IMP_DEV_OK", "IMP_DEV_NONFINITE_INPUT", "IMP_DEV_TIMEOUT", "ImpNvfp4Tensor",
     "imp_nvfp4_quantize", "imp_nvfp4_gemm", "imp_nvfp4_quantize_workspace_size",
-    "imp_nvfp4_gemm_workspace_size", "imp_status_string", "NVFP4Tensor", "quantize", "gemm",
+    "imp_nvfp4_gemm_workspace_size", "imp_nvfp4_gemm_plan", "imp_status_string", "NVFP4Tensor",
+    "quantize", "gemm",
     "library_path", "header_functions", "ImpError", "load", "imp_nvfp4_mma_scales_size",
     "imp_nvfp4_prepare_mma", "imp_nvfp4_quantize_mma", "imp_nvfp4_gemm_fp4", "prepare_mma",
     "imp_nvfp4_quantize_noalloc", "imp_nvfp4_mma_codes_size", "imp_nvfp4_gemm_mma",
@@ -66,6 +67,8 @@ def _L():
     lib.imp_nvfp4_quantize.argtypes = [P, I64, I64, I64, ctypes.POINTER(ImpNvfp4Tensor), P, P, SZ, P]
     lib.imp_nvfp4_gemm_workspace_size.restype = SZ
     lib.imp_nvfp4_gemm_workspace_size.argtypes = [I64, I64, I64]
+    lib.imp_nvfp4_gemm_plan.restype = ctypes.c_int32
+    lib.imp_nvfp4_gemm_plan.argtypes = [I64, I64, I64, ctypes.POINTER(ctypes.c_char_p)]
     lib.imp_nvfp4_gemm.restype = ctypes.c_int
     lib.imp_nvfp4_gemm.argtypes = [P, I64, I64, I64, ctypes.POINTER(ImpNvfp4Tensor), P, I64, P, P,
                                    SZ, P]
@@ -116,6 +119,14 @@ def imp_nvfp4_quantize_workspace_size(rows: int, K: int) -> int:
 
 def imp_nvfp4_gemm_workspace_size(M: int, N: int, K: int) -> int:
     return _L().imp_nvfp4_gemm_workspace_size(M, N, K)
+
+
+def imp_nvfp4_gemm_plan(M: int, N: int, K: int) -> tuple[int, str | None]:
+    """(kernel launches of one imp_nvfp4_gemm call, name of the kernel that
+    streams W) on the current device; (0, None) for rejected shapes."""
+    name = ctypes.c_char_p()
+    n = _L().imp_nvfp4_gemm_plan(M, N, K, ctypes.byref(name))
+    return n, (name.value.decode() if name.value else None)
 
 
 def imp_nvfp4_quantize(x_bf16: int, rows: int, K: int, ldx: int, out: ImpNvfp4Tensor,

@@ -117,6 +117,21 @@ size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   return prefill_ws(M, N, K).total;
 }
 
+int32_t imp_nvfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const char **kernel) {
+  const char *name = nullptr;
+  int n = 0;
+  if (M >= 1 && N >= 1 && K >= 64 && K % 64 == 0) {
+    if (M <= kDecodeMaxM) {
+      n = impfp4::gemv_launches(M, N, K, &name);
+    } else if (M <= INT32_MAX && N <= INT32_MAX && K <= INT32_MAX) {
+      name = "gemm_mxf4_kernel";
+      n = 4;  // X amax, X encode, W scale atoms, GEMM
+    }
+  }
+  if (kernel) *kernel = n ? name : nullptr;
+  return n;
+}
+
 size_t imp_nvfp4_mma_scales_size(int64_t rows, int64_t K) {
   if (rows <= 0 || K <= 0 || K % 64) return 0;
   return impfp4::mma_scale_bytes(rows, K);

@@ -352,26 +352,71 @@ int pass_tile(int64_t M_left, int64_t N, int64_t K, Plan &p) {
 
 }  // namespace
 
-bool gemv_supported(int64_t M, int64_t N, int64_t K) {
-  if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return false;
-  if (gemv_tc_supported(M, N, K)) return true;
-  for (int64_t m0 = 0; m0 < M;) {
+namespace {
+
+// CUDA-core passes needed for M rows of X (0: no plan fits).
+int cuda_core_passes(int64_t M, int64_t N, int64_t K) {
+  int passes = 0;
+  for (int64_t m0 = 0; m0 < M; ++passes) {
     Plan p;
     const int MT = pass_tile(M - m0, N, K, p);
-    if (MT == 0) return false;
+    if (MT == 0) return 0;
     m0 += MT;
   }
-  return true;
+  return passes;
+}
+
+enum class DecodePath { kNone, kFp4, kF16, kCudaCore };
+
+// The FP4 path for one row of X over many 128-row tiles of W; the f16
+// tensor-core path otherwise (it needs no cross-CTA sums, and for several
+// rows of X it shares each decoded weight between them) -- measured per
+// shape class on GB300.  The CUDA-core kernel takes what neither accepts.
+DecodePath choose_path(int64_t M, int64_t N, int64_t K, bool workspace, const void *codes,
+                       const void *scales) {
+  if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return DecodePath::kNone;
+  const bool f4 = workspace && gemv_f4_supported(M, N, K, codes, scales);
+  if (f4 && M == 1 && 4 * ((N + 127) / 128) >= 3 * (int64_t)num_sms()) return DecodePath::kFp4;
+  if (gemv_tc_supported(M, N, K)) return DecodePath::kF16;
+  if (f4) return DecodePath::kFp4;
+  return cuda_core_passes(M, N, K) ? DecodePath::kCudaCore : DecodePath::kNone;
+}
+
+}  // namespace
+
+bool gemv_supported(int64_t M, int64_t N, int64_t K) {
+  return choose_path(M, N, K, false, nullptr, nullptr) != DecodePath::kNone;
+}
+
+int gemv_launches(int64_t M, int64_t N, int64_t K, const char **kernel) {
+  switch (choose_path(M, N, K, true, nullptr, nullptr)) {
+    case DecodePath::kFp4:
+      return gemv_f4_launches(M, N, K, kernel);
+    case DecodePath::kF16:
+      *kernel = "gemv_tc_kernel";
+      return gemv_tc_launches(M, N, K);
+    case DecodePath::kCudaCore:
+      *kernel = "gemv_kernel";
+      return cuda_core_passes(M, N, K);
+    default:
+      return 0;
+  }
 }
 
 cudaError_t launch_gemv(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const uint8_t *codes,
                         const uint8_t *scales, const float *tensor_scale, int64_t N, uint16_t *y,
                         int64_t ldy, int32_t *status, void *workspace, cudaStream_t stream) {
-  if (workspace && gemv_f4_supported(M, N, K, codes, scales))
-    return launch_gemv_f4(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status, workspace,
-                          stream);
-  if (gemv_tc_supported(M, N, K))
-    return launch_gemv_tc(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status, stream);
+  switch (choose_path(M, N, K, workspace != nullptr, codes, scales)) {
+    case DecodePath::kFp4:
+      return launch_gemv_f4(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status,
+                            workspace, stream);
+    case DecodePath::kF16:
+      return launch_gemv_tc(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status, stream);
+    case DecodePath::kCudaCore:
+      break;
+    default:
+      return cudaErrorInvalidConfiguration;
+  }
   for (int64_t m0 = 0; m0 < M;) {
     Plan p;
     const int MT = pass_tile(M - m0, N, K, p);

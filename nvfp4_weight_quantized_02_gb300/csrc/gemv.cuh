@@ -11,6 +11,11 @@ int num_sms();
 // True if launch_gemv has a launch plan for this shape.
 bool gemv_supported(int64_t M, int64_t N, int64_t K);
 
+// Kernel launches of one launch_gemv call given a workspace and 16-byte
+// aligned W arrays, with the name of the kernel that streams W in *kernel
+// (0: no plan).
+int gemv_launches(int64_t M, int64_t N, int64_t K, const char **kernel);
+
 // Enqueue Y[M][N] = X[M][K] * W^T (bf16 X and Y, NVFP4 W) on `stream`.
 // Arguments are validated by the caller.  1 <= M <= 16, N >= 1, K % 64 == 0.
 // `workspace` (gemv_f4_workspace_bytes, 16-byte aligned) enables the FP4
@@ -23,6 +28,7 @@ cudaError_t launch_gemv(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, co
 // The tensor-core GEMV (gemv_tc.cu): passes of 1, 2, 4 or 8 rows of X,
 // each one stream of W.
 bool gemv_tc_supported(int64_t M, int64_t N, int64_t K);
+int gemv_tc_launches(int64_t M, int64_t N, int64_t K);  // passes; 0: no plan
 cudaError_t launch_gemv_tc(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status,
@@ -34,6 +40,7 @@ cudaError_t launch_gemv_tc(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
 bool gemv_f4_shape_ok(int64_t M, int64_t N, int64_t K);
 size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K);
 bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const void *scales);
+int gemv_f4_launches(int64_t M, int64_t N, int64_t K, const char **kernel);
 // `prepared`: codes and scales in the tensor-core (MMA) layout of
 // quantize.cuh (contiguous 16 KB code tiles and 2 KB scale-atom runs per
 // stage) instead of row-major.

@@ -1134,6 +1134,16 @@ size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return f4_ws(M < 4 ? M : 4, N, K).total;
 }
 
+int gemv_f4_launches(int64_t M, int64_t N, int64_t K, const char **kernel) {
+  if (!gemv_f4_shape_ok(M, N, K)) return 0;
+  if (M <= 2 && slots_r(N, K, f4_ws(M, N, K).grid) <= kMaxSlotsR) {
+    *kernel = "gemv_f4r_kernel";  // splits X itself
+    return 1;
+  }
+  *kernel = "gemv_f4_kernel";  // per pass of four rows: split kernel + GEMV
+  return 2 * (int)ceil_div(M, 4);
+}
+
 bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const void *scales) {
   return gemv_f4_shape_ok(M, N, K) && !(((uintptr_t)codes | (uintptr_t)scales) & 15u);
 }

@@ -507,16 +507,19 @@ int tc_pass_tile(int64_t M_left, int64_t N, int64_t K, M1Plan &p) {
 
 }  // namespace
 
-bool gemv_tc_supported(int64_t M, int64_t N, int64_t K) {
-  if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return false;
-  for (int64_t m0 = 0; m0 < M;) {
+int gemv_tc_launches(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return 0;
+  int passes = 0;
+  for (int64_t m0 = 0; m0 < M; ++passes) {
     M1Plan p;
     const int mt = tc_pass_tile(M - m0, N, K, p);
-    if (mt == 0) return false;
+    if (mt == 0) return 0;
     m0 += mt;
   }
-  return true;
+  return passes;
 }
+
+bool gemv_tc_supported(int64_t M, int64_t N, int64_t K) { return gemv_tc_launches(M, N, K) > 0; }
 
 cudaError_t launch_gemv_tc(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,

@@ -43,6 +43,20 @@ def test_workspace_sizes():
     assert pkg.imp_nvfp4_gemm_workspace_size(1, 17408, 768) == 0
 
 
+def test_gemm_plan():
+    # decode: one row of X over many 128-row tiles -> FP4 tensor cores, the
+    # GEMV kernel splitting X itself; few tiles or several rows -> f16 tensor
+    # cores, one launch per pass of 1/2/4/8 rows
+    assert pkg.imp_nvfp4_gemm_plan(1, 151936, 5120) == (1, "gemv_f4r_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(1, 17408, 5120) == (1, "gemv_f4r_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(1, 5120, 17408) == (1, "gemv_tc_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(4, 17408, 5120) == (1, "gemv_tc_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(16, 17408, 5120) == (2, "gemv_tc_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(2048, 17408, 5120) == (4, "gemm_mxf4_kernel")
+    for bad in [(0, 128, 1024), (1, 0, 1024), (1, 128, 100), (1, 128, 0)]:
+        assert pkg.imp_nvfp4_gemm_plan(*bad) == (0, None)
+
+
 A16 = 0x7F0000000000  # fake, 16-byte aligned "device" addresses: never dereferenced
 
 
