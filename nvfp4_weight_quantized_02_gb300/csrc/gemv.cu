@@ -368,17 +368,24 @@ int cuda_core_passes(int64_t M, int64_t N, int64_t K) {
 
 enum class DecodePath { kNone, kFp4, kF16, kCudaCore };
 
-// The FP4 path for one row of X over many 128-row tiles of W; the f16
-// tensor-core path otherwise (it needs no cross-CTA sums, and for several
-// rows of X it shares each decoded weight between them) -- measured per
-// shape class on GB300.  The CUDA-core kernel takes what neither accepts.
+// Measured per shape class on GB300 (back-to-back calls, weights from HBM):
+//  * one row of X over many 128-row tiles of W: the FP4 path (no per-weight
+//    work on the CUDA cores);
+//  * otherwise the f16 tensor-core path while one pass over W holds every
+//    row of X (it needs no cross-CTA sums, and it shares each decoded weight
+//    among the rows);
+//  * otherwise the FP4 path (one pass over W for any M <= 16, where the f16
+//    path would stream W once per 1, 2, 4 or 8 rows).
+// The CUDA-core kernel takes what neither tensor-core path accepts.
 DecodePath choose_path(int64_t M, int64_t N, int64_t K, bool workspace, const void *codes,
                        const void *scales) {
   if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return DecodePath::kNone;
   const bool f4 = workspace && gemv_f4_supported(M, N, K, codes, scales);
   if (f4 && M == 1 && 4 * ((N + 127) / 128) >= 3 * (int64_t)num_sms()) return DecodePath::kFp4;
-  if (gemv_tc_supported(M, N, K)) return DecodePath::kF16;
+  const int tc_passes = gemv_tc_launches(M, N, K);
+  if (tc_passes == 1) return DecodePath::kF16;
   if (f4) return DecodePath::kFp4;
+  if (tc_passes > 0) return DecodePath::kF16;
   return cuda_core_passes(M, N, K) ? DecodePath::kCudaCore : DecodePath::kNone;
 }
 

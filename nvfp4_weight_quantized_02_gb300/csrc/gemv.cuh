@@ -36,7 +36,7 @@ cudaError_t launch_gemv_tc(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
 
 // The block-scaled FP4 tensor-core GEMV (gemv_f4.cu): X split into NVFP4
 // components per call (needs a workspace), W streamed straight into
-// tcgen05.mma.kind::mxf4nvf4.  Passes of up to 4 rows of X.
+// tcgen05.mma.kind::mxf4nvf4.  One pass over W for every M <= 16.
 bool gemv_f4_shape_ok(int64_t M, int64_t N, int64_t K);
 size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K);
 bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const void *scales);

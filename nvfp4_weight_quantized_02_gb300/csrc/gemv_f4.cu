@@ -39,10 +39,13 @@
 //    issuer i % 4) as chunks become ready, and warps 8..11 go on to the
 //    epilogue.  A weight already in the tensor-core layout (quantize.cuh)
 //    is read with two contiguous bulk copies per stage instead.
-//  * gemv_f4_kernel (M = 3..16, passes of up to four rows of X): a separate
-//    split kernel (xsplit_kernel) writes the components and scale atoms to
-//    the workspace, and they travel with W in each stage of an 8-deep ring;
-//    four MMA issuers (warps 0..3), producer warp 4, epilogue warps 8..11.
+//  * gemv_f4_kernel (any M <= 16, one pass over W): a separate split
+//    kernel (xsplit_kernel) writes the components and scale atoms to the
+//    workspace, and they travel with W in each stage of the ring; producer
+//    warp 4, epilogue warps 8..11, and MMA issuers from warp 0 -- four for
+//    B operands of 16 or 32 rows (8-deep ring), two for 64 (6-deep), one for
+//    128 (5-deep): a wider MMA takes longer, so fewer issuers keep ahead of
+//    HBM, and the wider B stages fill the shared memory sooner.
 // Issuer: its warp relays the stage's W scales into 512-byte atoms; one
 // thread copies both operands' atoms to tensor memory (tcgen05.cp) and issues
 // four M=128 x N=N_MMA x K=64 MMAs into its own accumulator.  One issuing
@@ -75,8 +78,19 @@ constexpr int kThreads = 384;
 // workspace size does not depend on the device.
 constexpr int kMaxGrid = 256;
 
-// ---- streamed-B kernel (M = 3..16)
-constexpr int kIssuersS = 4, kProducerS = 4, kNSS = 8;  // stage st and st - 8: same issuer
+constexpr int kMaxRowsX = 16;  // rows of X per launch (operand rows: 8 per row)
+
+// ---- streamed-B kernel
+constexpr int kProducerS = 4;
+// Issuers and ring depth per operand width: the accumulators (two per
+// issuer, N_MMA columns each) and the scale banks (32 columns per ring slot)
+// share the 512 tensor-memory columns, and the ring fills the shared memory.
+// A wider B makes each MMA slower, so fewer issuers keep up with HBM.
+template <int NMMA> struct CfgS;
+template <> struct CfgS<16> { static constexpr int NI = 4, NS = 8; };
+template <> struct CfgS<32> { static constexpr int NI = 4, NS = 8; };
+template <> struct CfgS<64> { static constexpr int NI = 2, NS = 6; };
+template <> struct CfgS<128> { static constexpr int NI = 1, NS = 5; };
 template <int NMMA> struct StageS {
   static constexpr uint32_t W = 0;                 // 128 x 128 B, swizzled
   static constexpr uint32_t B = 16384;             // NMMA x 128 B, swizzled
@@ -113,7 +127,7 @@ struct F4Args {
   const float *tensor_scale;
   const uint8_t *sfb;   // streamed kernel: X component scale atoms, [K/64][512]
   const int32_t *sh;    // streamed kernel: per-row prescale exponents
-  float *part;          // split-tile partial sums, [CTA][first/last segment][4][128]
+  float *part;          // split-tile partial sums, [CTA][first/last segment][128][N_MMA / 8]
   unsigned __int128 *cnt;   // per tile: epoch, its check word and segments finished
   int32_t *status;
   int n_tiles;
@@ -370,6 +384,8 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
                             BWait b_wait) {
   constexpr uint32_t kIdesc = idesc_f4<NMMA>();
   constexpr uint32_t kSF0 = 2 * NI * NMMA;  // scale columns after the accumulators
+  constexpr int NB = NS / NI;               // scale banks per issuer
+  static_assert(NS % NI == 0 && kSF0 + 32 * NS <= kTmemCols, "tensor memory plan");
   const uint32_t sbase = smem_u32(smem);
   const uint64_t dA0 = sdesc(sbase + Stage::W, 16, 1024, kSw128);
   const uint64_t dSA0 = sdesc(sbase + Stage::SFA, 0, 128, kNoSwizzle);
@@ -407,10 +423,10 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
       if (lane == 0) {
         tc_fence_after();
         const uint64_t off = (uint64_t)(s * (Stage::BYTES >> 4));
-        // Scale bank (i / NI) & 1: its previous user, stage i - 2 NI, was
-        // this issuer's too, and NS == 2 NI: the producer refilled slot s
+        // Scale bank (i / NI) % NB: its previous user, stage i - NS, was
+        // this issuer's too (NS == NB NI), and the producer refilled slot s
         // only after that stage's commit.
-        const uint32_t sf = tmem + kSF0 + 32u * (uint32_t)(2 * is + ((i / NI) & 1));
+        const uint32_t sf = tmem + kSF0 + 32u * (uint32_t)(NB * is + (i / NI) % NB);
         const uint32_t dt = tmem + (uint32_t)((2 * is + d) * NMMA);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -440,7 +456,7 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
 // row -> y (whole tile) or a partial sum (split tile, last CTA adds them).
 template <int NI, int NMMA>
 __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, const StreamK &sk,
-                              int warp, int lane, const int (&sh)[4]) {
+                              int warp, int lane, const int (&sh)[kMaxRowsX]) {
   constexpr int MR = NMMA / kNC;  // rows of X per pass
   const int q = warp & 3;
   const int row_in_tile = 32 * q + lane;
@@ -496,12 +512,20 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     // of its first and last segment (slots 0 and 1; a single segment uses 0).
     const int c_first = sk.owner(T * sk.nch), c_last = sk.owner(T * sk.nch + sk.nch - 1);
     const int nslot = c_last - c_first + 1;
-    auto part_at = [&](int c, int sl, int m) {
-      return a.part + ((size_t)(2 * c + sl) * 4 + m) * kTileRows + row_in_tile;
+    // a row's MR partial sums are contiguous: one or a few vector accesses
+    auto part_at = [&](int c, int sl) {
+      return a.part + ((size_t)(2 * c + sl) * kTileRows + row_in_tile) * MR;
     };
+    {
+      float *p = part_at(blockIdx.x, j == 0 ? 0 : 1);
+      if constexpr (MR == 2) {
+        *reinterpret_cast<float2 *>(p) = make_float2(acc[0], acc[1]);
+      } else {
 #pragma unroll
-    for (int m = 0; m < MR; ++m)
-      if (m < a.M) *part_at(blockIdx.x, j == 0 ? 0 : 1, m) = acc[m];
+        for (int m = 0; m < MR; m += 4)
+          *reinterpret_cast<float4 *>(p + m) = make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+      }
+    }
     // The warps report in (a CTA-scope release); one thread makes the CTA's
     // stores visible device-wide (a cumulative fence) and counts the
     // segment; the tile's last CTA adds the partials in K order.
@@ -520,23 +544,54 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     if (*last_flag) {
       __threadfence();
       if (row < a.N) {
-#pragma unroll
-        for (int m = 0; m < MR; ++m) {
-          if (m < a.M) {
-            float t = 0.0f;
-            for (int c = c_first; c <= c_last; ++c) {
-              // the tile is the last segment of c_first (its first too if c_first
-              // has only one) and the first segment of every later CTA
-              int sl = 0;
-              if (c == c_first) {
-                const int64_t gb = sk.total * c / sk.G, ge = sk.total * (c + 1) / sk.G;
-                sl = ((ge - 1) / sk.nch != gb / sk.nch) ? 1 : 0;
-              }
-              t += (c == (int)blockIdx.x && sl == (j == 0 ? 0 : 1)) ? acc[m] : __ldcg(part_at(c, sl, m));
-            }
-            a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(t));
+        // Sums in K order, per row of X.  The partials sit in other SMs' L2
+        // lines (often across the die boundary), so the loads of several
+        // CTAs are put in flight together before any is added.
+        auto load_part = [&](int c, float (&v)[MR]) {
+          // the tile is the last segment of c_first (its first too if c_first
+          // has only one) and the first segment of every later CTA
+          int sl = 0;
+          if (c == c_first) {
+            const int64_t gb = sk.total * c / sk.G, ge = sk.total * (c + 1) / sk.G;
+            sl = ((ge - 1) / sk.nch != gb / sk.nch) ? 1 : 0;
           }
+          if (c == (int)blockIdx.x && sl == (j == 0 ? 0 : 1)) {
+#pragma unroll
+            for (int m = 0; m < MR; ++m) v[m] = acc[m];
+          } else if constexpr (MR == 2) {
+            const float2 q = __ldcg(reinterpret_cast<const float2 *>(part_at(c, sl)));
+            v[0] = q.x;
+            v[1] = q.y;
+          } else {
+#pragma unroll
+            for (int m = 0; m < MR; m += 4) {
+              const float4 q = __ldcg(reinterpret_cast<const float4 *>(part_at(c, sl) + m));
+              v[m] = q.x;
+              v[m + 1] = q.y;
+              v[m + 2] = q.z;
+              v[m + 3] = q.w;
+            }
+          }
+        };
+        constexpr int GP = MR >= 16 ? 2 : MR >= 8 ? 4 : 8;  // CTAs loaded together
+        float t[MR];
+#pragma unroll
+        for (int m = 0; m < MR; ++m) t[m] = 0.0f;
+        for (int c0 = c_first; c0 <= c_last; c0 += GP) {
+          float v[GP][MR];
+#pragma unroll
+          for (int g = 0; g < GP; ++g)
+            if (c0 + g <= c_last) load_part(c0 + g, v[g]);
+#pragma unroll
+          for (int g = 0; g < GP; ++g)
+            if (c0 + g <= c_last) {
+#pragma unroll
+              for (int m = 0; m < MR; ++m) t[m] += v[g][m];
+            }
         }
+#pragma unroll
+        for (int m = 0; m < MR; ++m)
+          if (m < a.M) a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(t[m]));
       }
     }
   }
@@ -616,15 +671,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemv_f4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
                    const __grid_constant__ CUtensorMap tm_b, const F4Args a) {
   using L = StageS<NMMA>;
+  constexpr int NI = CfgS<NMMA>::NI, NS = CfgS<NMMA>::NS;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  F4Bars &bars = *reinterpret_cast<F4Bars *>(smem + kNSS * L::BYTES);
+  F4Bars &bars = *reinterpret_cast<F4Bars *>(smem + NS * L::BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const StreamK sk(a.n_tiles, a.n_chunks);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) init_common(bars, kNSS, kIssuersS);
+  if (threadIdx.x == 0) init_common(bars, NS, NI);
   if (warp == 0) tmem_alloc(&bars.tmem);
   tc_fence_before();
   __syncthreads();
@@ -640,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_b);
       // processing position i -> ring slot i % NS, stage stage_of(i)
       auto load_w = [&](int i) {
-        const int s = i % kNSS;
+        const int s = i % NS;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
         const int64_t g = sk.g_begin + sk.stage_of(i);
         const int64_t tile = g / sk.nch;
@@ -655,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto load_x = [&](int i) {
-        const int s = i % kNSS;
+        const int s = i % NS;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
         const int ch = (int)((sk.g_begin + sk.stage_of(i)) % sk.nch);
         tma_load_2d(stg + L::B, &tm_b, ch * (kChunkK / 2), 0, &bars.full[s]);
@@ -675,39 +731,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // W of the first stages before the previous kernel has finished, and
       // more W into L2: HBM keeps streaming while X is being split.
-      const int pre = min(kNSS, sk.n_st);
+      const int pre = min(NS, sk.n_st);
       for (int i = 0; i < pre; ++i) load_w(i);
       for (int i = pre; i < min(pre + kPrefetch, sk.n_st); ++i) prefetch_w(i);
       asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int i = 0; i < pre; ++i) load_x(i);
       int i = pre;
       for (; i < sk.n_st; ++i) {
-        const int s = i % kNSS;
-        if (!mbar_wait_bounded(&bars.empty[s], (uint32_t)((i / kNSS - 1) & 1), a.status)) break;
+        const int s = i % NS;
+        if (!mbar_wait_bounded(&bars.empty[s], (uint32_t)((i / NS - 1) & 1), a.status)) break;
         load_w(i);
         load_x(i);
       }
       // never leave with copies in flight
-      for (int k = (i > kNSS ? i - kNSS : 0); k < i; ++k)
-        mbar_wait_bounded(&bars.full[k % kNSS], (uint32_t)((k / kNSS) & 1), a.status);
+      for (int k = (i > NS ? i - NS : 0); k < i; ++k)
+        mbar_wait_bounded(&bars.full[k % NS], (uint32_t)((k / NS) & 1), a.status);
     }
-  } else if (warp < kIssuersS) {
+  } else if (warp < NI) {
     const uint32_t sbase = smem_u32(smem);
     const uint64_t dB0 = sdesc(sbase + L::B, 16, 1024, kSw128);
     const uint64_t dSB0 = sdesc(sbase + L::SFB, 0, 128, kNoSwizzle);
     auto b_desc = [&](int i, int, int t) {
-      return dB0 + (uint64_t)((i % kNSS) * (L::BYTES >> 4)) + 2u * t;
+      return dB0 + (uint64_t)((i % NS) * (L::BYTES >> 4)) + 2u * t;
     };
     auto sfb_desc = [&](int i, int, int t) {
-      return dSB0 + (uint64_t)((i % kNSS) * (L::BYTES >> 4)) + 32u * t;
+      return dSB0 + (uint64_t)((i % NS) * (L::BYTES >> 4)) + 32u * t;
     };
-    issuer_loop<kIssuersS, kNSS, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
+    issuer_loop<NI, NS, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
                                           sfb_desc, [](int) { return true; });
   } else if (warp >= kEpiWarp0) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    int sh[4] = {0, 0, 0, 0};
-    for (int m = 0; m < a.M; ++m) sh[m] = a.sh[m];
-    epilogue_loop<kIssuersS, NMMA>(a, bars, tmem, sk, warp, lane, sh);
+    int sh[kMaxRowsX] = {};
+#pragma unroll
+    for (int m = 0; m < NMMA / kNC; ++m)
+      if (m < a.M) sh[m] = a.sh[m];
+    epilogue_loop<NI, NMMA>(a, bars, tmem, sk, warp, lane, sh);
   }
 
   tc_fence_before();
@@ -833,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && m < a.M) atomicMax(&bars.xmax[m], mx[m]);
     }
     named_bar(1, kHelperThreadsR);
-    int sh[4] = {0, 0, 0, 0};
+    int sh[kMaxRowsX] = {};
 #pragma unroll
     for (int m = 0; m < 2; ++m) sh[m] = m < a.M ? prescale_exponent(bars.xmax[m]) : 0;
     // clear the slots' scale atoms (rows without a component keep zero
@@ -937,13 +995,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host --------------------------------------------------------------------
 
-int nmma_for(int64_t M) { return M <= 2 ? 16 : 32; }
+// Operand rows: eight components per row of X, rounded up to an MMA width.
+int nmma_for(int64_t M) { return M <= 2 ? 16 : M <= 4 ? 32 : M <= 8 ? 64 : 128; }
 
 struct F4Ws {
   size_t bcodes, sfb, sh, cnt, part, total;
   int grid;
 };
-// Workspace of a pass of up to four rows: X's components and scale atoms
+// Workspace of one call: X's components and scale atoms
 // (streamed path), prescale exponents, per-tile counters, partial sums.
 F4Ws f4_ws(int64_t M, int64_t N, int64_t K) {
   F4Ws w;
@@ -960,11 +1019,13 @@ F4Ws f4_ws(int64_t M, int64_t N, int64_t K) {
   w.sh = w.sfb + (size_t)(K / 64) * 512;
   w.cnt = w.sh + 256;
   w.part = w.cnt + (size_t)ceil_div(n_tiles * 16, 256) * 256;
-  w.total = w.part + (size_t)cap * 2 * 4 * kTileRows * sizeof(float);
+  w.total = w.part + (size_t)cap * 2 * (nmma / kNC) * kTileRows * sizeof(float);
   return w;
 }
 
-template <int NMMA> size_t smem_s() { return (size_t)kNSS * StageS<NMMA>::BYTES + sizeof(F4Bars) + 1024; }
+template <int NMMA> size_t smem_s() {
+  return (size_t)CfgS<NMMA>::NS * StageS<NMMA>::BYTES + sizeof(F4Bars) + 1024;
+}
 size_t smem_r(int n_slots) {
   return (size_t)kNSR * StageR::BYTES + (size_t)n_slots * (2048 + 1024) + 256 + sizeof(F4Bars) +
          1024;
@@ -1080,6 +1141,15 @@ bool weight_maps(bool prepared, const uint8_t *codes, const uint8_t *scales, int
          cached_map(ms, scales, (uint64_t)N, (uint64_t)(K / 16), kTileRows, 16, false);
 }
 
+template <int NMMA>
+cudaError_t launch_streamed(bool prepared, int grid, cudaStream_t stream, const CUtensorMap &mw,
+                            const CUtensorMap &ms, const CUtensorMap &mb, const F4Args &a) {
+  return prepared ? launch_pdl(gemv_f4_kernel<NMMA, true>, grid, kThreads, smem_s<NMMA>(), stream,
+                               mw, ms, mb, a)
+                  : launch_pdl(gemv_f4_kernel<NMMA, false>, grid, kThreads, smem_s<NMMA>(),
+                               stream, mw, ms, mb, a);
+}
+
 cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                                  const uint8_t *codes, const uint8_t *scales,
                                  const float *tensor_scale, int64_t N, uint16_t *y, int64_t ldy,
@@ -1112,15 +1182,12 @@ cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_
   F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status, ws, L);
   a.wc = codes;
   a.wsa = scales;
-  if (prepared)
-    return nmma == 16 ? launch_pdl(gemv_f4_kernel<16, true>, L.grid, kThreads, smem_s<16>(), stream,
-                                   mw, ms, mb, a)
-                      : launch_pdl(gemv_f4_kernel<32, true>, L.grid, kThreads, smem_s<32>(), stream,
-                                   mw, ms, mb, a);
-  return nmma == 16 ? launch_pdl(gemv_f4_kernel<16, false>, L.grid, kThreads, smem_s<16>(), stream,
-                                 mw, ms, mb, a)
-                    : launch_pdl(gemv_f4_kernel<32, false>, L.grid, kThreads, smem_s<32>(), stream,
-                                 mw, ms, mb, a);
+  switch (nmma) {
+    case 16: return launch_streamed<16>(prepared, L.grid, stream, mw, ms, mb, a);
+    case 32: return launch_streamed<32>(prepared, L.grid, stream, mw, ms, mb, a);
+    case 64: return launch_streamed<64>(prepared, L.grid, stream, mw, ms, mb, a);
+    default: return launch_streamed<128>(prepared, L.grid, stream, mw, ms, mb, a);
+  }
 }
 
 }  // namespace
@@ -1131,7 +1198,7 @@ bool gemv_f4_shape_ok(int64_t M, int64_t N, int64_t K) {
 }
 
 size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  return f4_ws(M < 4 ? M : 4, N, K).total;
+  return f4_ws(M, N, K).total;
 }
 
 int gemv_f4_launches(int64_t M, int64_t N, int64_t K, const char **kernel) {
@@ -1140,8 +1207,8 @@ int gemv_f4_launches(int64_t M, int64_t N, int64_t K, const char **kernel) {
     *kernel = "gemv_f4r_kernel";  // splits X itself
     return 1;
   }
-  *kernel = "gemv_f4_kernel";  // per pass of four rows: split kernel + GEMV
-  return 2 * (int)ceil_div(M, 4);
+  *kernel = "gemv_f4_kernel";  // split kernel + GEMV
+  return 2;
 }
 
 bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const void *scales) {
@@ -1169,16 +1236,9 @@ cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                                    mw, ms, a);
     }
   }
-  // passes of up to four rows of X, each one stream of W (the workspace is
-  // reused: each pass's split kernel waits for the previous GEMV)
-  for (int64_t m0 = 0; m0 < M; m0 += 4) {
-    const int64_t mp = M - m0 < 4 ? M - m0 : 4;
-    const cudaError_t e = launch_pass_streamed(x + m0 * ldx, mp, K, ldx, codes, scales,
-                                               tensor_scale, N, y + m0 * ldy, ldy, status,
-                                               workspace, stream, prepared);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  // every row of X in one stream of W
+  return launch_pass_streamed(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status,
+                              workspace, stream, prepared);
 }
 
 }  // namespace impfp4

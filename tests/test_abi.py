@@ -35,8 +35,11 @@ def test_workspace_sizes():
     # decode shapes on the FP4 tensor-core path need room for X's components
     ws1 = pkg.imp_nvfp4_gemm_workspace_size(1, 17408, 5120)
     assert 16 * 2560 + 80 * 512 <= ws1 <= 16 * 2560 + 80 * 512 + (2 << 20)
-    assert pkg.imp_nvfp4_gemm_workspace_size(4, 17408, 5120) == \
-        pkg.imp_nvfp4_gemm_workspace_size(16, 17408, 5120) > ws1
+    # one pass over W for every M: X's components (8 operand rows per row of
+    # X, rounded up to 16/32/64/128) and the partial sums grow with M
+    ws = [pkg.imp_nvfp4_gemm_workspace_size(m, 17408, 5120) for m in (1, 2, 3, 4, 5, 8, 9, 16)]
+    assert ws[0] == ws[1] == ws1 < ws[2] == ws[3] < ws[4] == ws[5] < ws[6] == ws[7]
+    assert ws[7] >= 128 * 2560 + 80 * 512
     # shapes that path does not take need none
     assert pkg.imp_nvfp4_gemm_workspace_size(1, 100, 5120) == 0
     assert pkg.imp_nvfp4_gemm_workspace_size(1, 17408, 320) == 0
@@ -51,7 +54,12 @@ def test_gemm_plan():
     assert pkg.imp_nvfp4_gemm_plan(1, 17408, 5120) == (1, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(1, 5120, 17408) == (1, "gemv_tc_kernel")
     assert pkg.imp_nvfp4_gemm_plan(4, 17408, 5120) == (1, "gemv_tc_kernel")
-    assert pkg.imp_nvfp4_gemm_plan(16, 17408, 5120) == (2, "gemv_tc_kernel")
+    # several rows of X that one f16 pass cannot hold: FP4, split kernel + GEMV
+    assert pkg.imp_nvfp4_gemm_plan(16, 17408, 5120) == (2, "gemv_f4_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(3, 5120, 17408) == (2, "gemv_f4_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(2, 5120, 17408) == (1, "gemv_tc_kernel")
+    # FP4 shape rules not met (K % 256): f16 passes
+    assert pkg.imp_nvfp4_gemm_plan(16, 5120, 17344) == (8, "gemv_tc_kernel")
     assert pkg.imp_nvfp4_gemm_plan(2048, 17408, 5120) == (4, "gemm_mxf4_kernel")
     for bad in [(0, 128, 1024), (1, 0, 1024), (1, 128, 100), (1, 128, 0)]:
         assert pkg.imp_nvfp4_gemm_plan(*bad) == (0, None)
