@@ -224,6 +224,14 @@ imp_status imp_nvfp4_gemm_mma(const void *x_bf16, int64_t M, int64_t K, int64_t 
 /* Human-readable name of a status code (static storage). */
 const char *imp_status_string(imp_status status);
 
+/* Self-test of the in-kernel failure detection: launches one kernel whose
+ * single bounded wait (on an mbarrier that nothing arrives at) gives up after
+ * the library's wait limit (1 s), ORs IMP_DEV_TIMEOUT into *dev_status and
+ * returns -- the same wait every kernel of this library uses on its
+ * pipelines.  No fault, trap or hang: the context stays usable.
+ *   dev_status  device int32, 4-byte aligned (else IMP_ERR_INVALID_ARG). */
+imp_status imp_selftest_bounded_wait(int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ __all__ = [
     "library_path", "header_functions", "ImpError", "load", "imp_nvfp4_mma_scales_size",
     "imp_nvfp4_prepare_mma", "imp_nvfp4_quantize_mma", "imp_nvfp4_gemm_fp4", "prepare_mma",
     "imp_nvfp4_quantize_noalloc", "imp_nvfp4_mma_codes_size", "imp_nvfp4_gemm_mma",
-    "quantize_mma", "gemm_fp4", "gemm_mma",
+    "quantize_mma", "gemm_fp4", "gemm_mma", "imp_selftest_bounded_wait",
 ]
 
 IMP_OK = 0
@@ -73,6 +73,8 @@ def _L():
     lib.imp_nvfp4_gemm.argtypes = [P, I64, I64, I64, ctypes.POINTER(ImpNvfp4Tensor), P, I64, P, P,
                                    SZ, P]
     lib.imp_status_string.restype = ctypes.c_char_p
+    lib.imp_selftest_bounded_wait.restype = ctypes.c_int
+    lib.imp_selftest_bounded_wait.argtypes = [P, P]
     lib.imp_status_string.argtypes = [ctypes.c_int]
     T = ctypes.POINTER(ImpNvfp4Tensor)
     lib.imp_nvfp4_mma_scales_size.restype = SZ
@@ -119,6 +121,10 @@ def imp_nvfp4_quantize_workspace_size(rows: int, K: int) -> int:
 
 def imp_nvfp4_gemm_workspace_size(M: int, N: int, K: int) -> int:
     return _L().imp_nvfp4_gemm_workspace_size(M, N, K)
+
+
+def imp_selftest_bounded_wait(dev_status: int, stream: int | None) -> int:
+    return _L().imp_selftest_bounded_wait(dev_status, stream)
 
 
 def imp_nvfp4_gemm_plan(M: int, N: int, K: int) -> tuple[int, str | None]:

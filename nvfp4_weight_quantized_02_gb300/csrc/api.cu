@@ -39,9 +39,26 @@ PrefillWs prefill_ws(int64_t M, int64_t N, int64_t K) {
   return w;
 }
 
+// One thread waits, with the library's bounded wait, on an mbarrier that
+// nothing ever arrives at: after the wait limit it reports IMP_DEV_TIMEOUT
+// and returns, leaving the context usable.
+__global__ void bounded_wait_selftest_kernel(int32_t *status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  impfp4::mbar_init(&bar, 1);
+  impfp4::fence_mbar_init();
+  impfp4::mbar_wait_bounded(&bar, 0u, status);
+}
+
 }  // namespace
 
 extern "C" {
+
+imp_status imp_selftest_bounded_wait(int32_t *dev_status, void *stream) {
+  if (!dev_status || !aligned4(dev_status)) return IMP_ERR_INVALID_ARG;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_status);
+  return from_cuda(cudaGetLastError());
+}
 
 const char *imp_status_string(imp_status status) {
   switch (status) {

@@ -15,13 +15,16 @@
 //    copies of the same swizzled image -- and the matching block scales
 //    (already in the 512-byte atom layout) with bulk copies, into a 4-deep
 //    shared-memory ring.
+//  * warp 10, one thread: per stage, twelve tcgen05.cp (per 64-element K
+//    step: the scales of the X rows and of the two 128-row halves of the W
+//    tile) into the stage's own bank of tensor-memory columns, then a
+//    tcgen05.commit that tells the MMA warp the bank is ready.  A copy costs
+//    the issuing thread about as much as an MMA, so issuing both from one
+//    thread left the tensor pipe idle half of the time.
 //  * warp 1: allocates 512 tensor-memory columns; one thread issues, per
-//    stage, twelve tcgen05.cp (per 64-element K step: the scales of the X rows
-//    and of the two 128-row halves of the W tile, into one of two column
-//    banks) and then four tcgen05.mma (M = 128, N = 256, K = 64) accumulating
-//    into columns 0..255;
-//    tcgen05.commit releases each ring stage and, at the end of a tile,
-//    signals the epilogue.
+//    stage, four tcgen05.mma (M = 128, N = 256, K = 64) accumulating into
+//    columns 0..255; tcgen05.commit releases each ring stage and, at the end
+//    of a tile, signals the epilogue.
 //  * warps 2..9: epilogue.  Each thread owns half of one accumulator row
 //    (its warp's 32-lane quarter of tensor memory, 128 of the 256 columns),
 //    reads it with tcgen05.ld, multiplies by s_x * s_w, rounds to bf16, hands
@@ -48,12 +51,15 @@ constexpr uint32_t SFA_BYTES = (BM / 128) * KSTEPS * 512;    // 2 KB
 constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;    // 4 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t OFF_B = A_BYTES, OFF_SFA = A_BYTES + B_BYTES, OFF_SFB = OFF_SFA + SFA_BYTES;
-constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+// warp 0 TMA, warp 1 MMA, warps 2..9 epilogue, warps 10..12 scale copies
+constexpr int kScaleWarp0 = 10, kScaleWarps = 3;
+constexpr int kThreads = 32 * (kScaleWarp0 + kScaleWarps);
 constexpr int kEpiThreads = 256;
 constexpr int kEpiCols = 128;  // accumulator columns per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_D = 0;     // accumulator: columns 0..255
-constexpr uint32_t TMEM_SF = 256;  // scales: 12 columns per K step (X 4, W 8), 2 banks of 48
+constexpr uint32_t TMEM_SF = 256;  // scales: 12 columns per K step (X 4, W 8), a bank of 48 per ring stage
+static_assert(TMEM_SF + 48 * NSTAGE <= TMEM_COLS, "tensor memory plan");
 constexpr size_t kBarBytes = 256;
 constexpr size_t kSmemBytes = 1024 + NSTAGE * (size_t)STAGE_BYTES + kBarBytes;
 
@@ -143,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *empty = full + NSTAGE;
   uint64_t *accf = empty + NSTAGE;  // accumulator ready for the epilogue
   uint64_t *acce = accf + 1;        // accumulator drained by the epilogue
-  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(acce + 1);
+  uint64_t *sff = acce + 1;         // [NSTAGE] a stage's scales copied to tensor memory
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(sff + NSTAGE);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -156,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sff[s], kScaleWarps);
     }
     mbar_init(accf, 1);
     mbar_init(acce, kEpiThreads);
@@ -229,8 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t dA0 = smem_desc(smem_u32(smem), 16, 1024, kLayoutSw128);
       const uint64_t dB0 = smem_desc(smem_u32(smem + OFF_B), 16, 1024, kLayoutSw128);
-      const uint64_t dSA0 = smem_desc(smem_u32(smem + OFF_SFA), 0, 128, kLayoutNone);
-      const uint64_t dSB0 = smem_desc(smem_u32(smem + OFF_SFB), 0, 128, kLayoutNone);
       uint32_t s = 0, phase = 0;  // ring position of the next stage
       int64_t issued = 0;         // stages consumed (for the drain on abort)
       int tile_iter = 0;
@@ -247,35 +253,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           // issued behind in-flight tcgen05.mma stalls the issuing thread
           // (measured: ~2.5x slower MMA issue).  A stalled peer shows up as
           // a timed-out barrier wait instead.
-          if (!mbar_wait_bounded(&full[s], phase, a.status)) {
+          // the stage's operands have landed and its scales are in bank s
+          if (!mbar_wait_bounded(&full[s], phase, a.status) ||
+              !mbar_wait_bounded(&sff[s], phase, a.status)) {
             ok = false;
             break;
           }
+          tc_fence_after();
           const uint64_t off = (uint64_t)(s * (STAGE_BYTES >> 4));
-          const uint64_t dA = dA0 + off, dB = dB0 + off, dSA = dSA0 + off, dSB = dSB0 + off;
-          // scale columns alternate between two banks of 48 by stage parity
-          const uint32_t sf0 = tmem + TMEM_SF + 48u * (s & 1u);
+          const uint64_t dA = dA0 + off, dB = dB0 + off;
+          const uint32_t sf0 = tmem + TMEM_SF + 48u * s;
           const uint32_t acc0 = ks != 0 ? 1u : 0u;
-          if (ks + 1 < n_ks || a.K % BK == 0) {
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-              // descriptor start address is in 16-byte units: +512 B = +32
-              tc_cp_sf(sf0 + 12u * kk, dSA + 32u * kk);
-              tc_cp_sf(sf0 + 12u * kk + 4, dSB + 32u * kk);
-              tc_cp_sf(sf0 + 12u * kk + 8, dSB + 128u + 32u * kk);
-            }
+          const int nk = (ks + 1 < n_ks || a.K % BK == 0) ? KSTEPS : (a.K - ks * BK) / MMA_K;
+          if (nk == KSTEPS) {
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk)
               // K step kk: +32 bytes inside the 128-byte swizzle atom (+2 units)
               tc_mma(tmem + TMEM_D, dA + 2u * kk, dB + 2u * kk, kIdesc, sf0 + 12u * kk,
                      sf0 + 12u * kk + 4, kk ? 1u : acc0);
           } else {
-            const int nk = (a.K - ks * BK) / MMA_K;  // last, partial stage
-            for (int kk = 0; kk < nk; ++kk) {
-              tc_cp_sf(sf0 + 12u * kk, dSA + 32u * kk);
-              tc_cp_sf(sf0 + 12u * kk + 4, dSB + 32u * kk);
-              tc_cp_sf(sf0 + 12u * kk + 8, dSB + 128u + 32u * kk);
-            }
             for (int kk = 0; kk < nk; ++kk)
               tc_mma(tmem + TMEM_D, dA + 2u * kk, dB + 2u * kk, kIdesc, sf0 + 12u * kk,
                      sf0 + 12u * kk + 4, kk ? 1u : acc0);
@@ -301,6 +297,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if (warp >= kScaleWarp0) {
+    // ------------------------------ scale copies
+    // tcgen05.cp costs the issuing thread about as much as an MMA, so the
+    // twelve copies of a stage come from three warps, ahead of the MMA warp:
+    // per 64-element K step, warp 10 copies the X-row scales, warps 11 and
+    // 12 the two 128-row halves of the W tile, into the stage's own bank of
+    // 48 columns; the stage's barrier completes once all three committed.
+    // The bank is free again once the stage's MMAs completed, which the
+    // producer waited for before refilling the stage.
+    if (lane == 0) {
+      const int part = warp - kScaleWarp0;  // 0: X scales, 1, 2: W halves
+      const uint64_t d0 = part == 0 ? smem_desc(smem_u32(smem + OFF_SFA), 0, 128, kLayoutNone)
+                                    : smem_desc(smem_u32(smem + OFF_SFB + 2048 * (part - 1)), 0,
+                                                128, kLayoutNone);
+      const uint32_t col = 4u * (uint32_t)part;
+      uint32_t s = 0, phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        for (int ks = 0; ks < n_ks; ++ks) {
+          // no shared-memory flag is read here either (see the MMA loop)
+          if (!mbar_wait_bounded(&full[s], phase, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t d = d0 + (uint64_t)(s * (STAGE_BYTES >> 4));
+          const uint32_t sf0 = tmem + TMEM_SF + 48u * s + col;
+          const int nk = (ks + 1 < n_ks || a.K % BK == 0) ? KSTEPS : (a.K - ks * BK) / MMA_K;
+          if (nk == KSTEPS) {
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk)
+              // descriptor start address is in 16-byte units: +512 B = +32
+              tc_cp_sf(sf0 + 12u * kk, d + 32u * kk);
+          } else {
+            for (int kk = 0; kk < nk; ++kk) tc_cp_sf(sf0 + 12u * kk, d + 32u * kk);
+          }
+          tc_commit(&sff[s]);
+          ++issued;
+          if (++s == NSTAGE) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy completes before tensor memory is freed: the last commit
+      // went to the stage before the current ring position
+      if (issued > 0) {
+        const uint32_t ls = s == 0 ? NSTAGE - 1 : s - 1;
+        const uint32_t lp = s == 0 ? (phase ^ 1u) : phase;
+        mbar_wait_bounded(&sff[ls], lp, a.status);
+      }
+    }
   } else {
     // ------------------------------ epilogue: warps 2..9
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
@@ -319,36 +368,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mb = t % MB, nb = t / MB;
       const int64_t m = (int64_t)mb * BM + row_in_tile;
       const int n0 = nb * BN + col0;
-      // Drain this warp's 128 accumulator columns into registers (as bf16
-      // pairs), hand the accumulator back to the MMA warp, then store: the
-      // stores overlap the next tile's MMAs.
-      uint32_t p[kEpiCols / 2];
+      // Drain this warp's 128 accumulator columns 32 at a time, storing each
+      // chunk as bf16 straight away (stores do not wait), then hand the
+      // accumulator back to the MMA warp: the stores drain while the next
+      // tile's MMAs run.
+      uint16_t *dst = a.y + m * a.ldy + n0;
+      const bool full_row = m < a.M && n0 + kEpiCols <= a.N;
 #pragma unroll
       for (int c = 0; c < kEpiCols; c += 32) {
         uint32_t r[32];
         tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D + col0 + c, r);
+        uint32_t p[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          p[c / 2 + i] = pack_bf16(__uint_as_float(r[2 * i]) * scale,
-                                   __uint_as_float(r[2 * i + 1]) * scale);
-      }
-      tc_fence_before();
-      mbar_arrive(acce);  // accumulator may be overwritten now
-      if (m < a.M) {
-        uint16_t *dst = a.y + m * a.ldy + n0;
-        if (n0 + kEpiCols <= a.N) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+          p[i] = pack_bf16(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
+        if (full_row) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
-          for (int i = 0; i < kEpiCols / 8; ++i)
+          for (int i = 0; i < 4; ++i)
             d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
-        } else {
+        } else if (m < a.M) {
 #pragma unroll
-          for (int i = 0; i < kEpiCols / 2; ++i) {
-            if (n0 + 2 * i < a.N) dst[2 * i] = (uint16_t)(p[i] & 0xFFFFu);
-            if (n0 + 2 * i + 1 < a.N) dst[2 * i + 1] = (uint16_t)(p[i] >> 16);
+          for (int i = 0; i < 16; ++i) {
+            if (n0 + c + 2 * i < a.N) dst[c + 2 * i] = (uint16_t)(p[i] & 0xFFFFu);
+            if (n0 + c + 2 * i + 1 < a.N) dst[c + 2 * i + 1] = (uint16_t)(p[i] >> 16);
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(acce);  // accumulator may be overwritten now
     }
   }
 
