@@ -311,6 +311,36 @@ def run_native(args):
     extra = {}
     if rank == 0 and not args.no_extra:
         extra = bench_extras(args, pkg, dev, stream, hbm_peak)
+        # the same step replayed as one CUDA graph (the decode launches of a
+        # step captured once; programmatic dependent launch edges kept)
+        try:
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                for x, w, y, ws in zip(xs, weights, ys, wss):
+                    pkg.gemm(x, w, y=y, dev_status=status, stream=cap, workspace=ws)
+            torch.cuda.synchronize()
+            for _ in range(args.warmup):
+                graph.replay()
+            torch.cuda.synchronize()
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            gstream = torch.cuda.current_stream(dev)
+            g0.record(gstream)
+            for _ in range(args.steps):
+                graph.replay()
+            g1.record(gstream)
+            torch.cuda.synchronize()
+            gms = g0.elapsed_time(g1) / args.steps
+            if int(status.item()) != 0:
+                raise RuntimeError(f"device status {int(status.item())} in the graph replay")
+            extra["decode_graph_replay"] = {
+                "ms_per_step": gms, "GB/s": bytes_step / (gms * 1e-3) / 1e9,
+                "frac_of_hbm_peak": bytes_step / (gms * 1e-3) / 1e9 / hbm_peak}
+            del graph
+        except Exception as e:  # report, do not fail the benchmark line
+            extra["decode_graph_replay"] = {"error": str(e)[:200]}
         # the same step on weights prepared once in the MMA layout (contiguous
         # 16 KB code tiles, scale atoms) through imp_nvfp4_gemm_mma
         prepared = [pkg.prepare_mma(w, stream=stream) for w in weights]
