@@ -150,6 +150,14 @@ int32_t imp_nvfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const char **kernel
  *   K        K > 0, K % 64 == 0, and w->K == K.
  *   w        NVFP4 weight with w->rows = N >= 0 rows (0 = nothing to do).
  *   y_bf16   device bf16[M][ldy], ldy >= N, ldy % 8 == 0; fully overwritten.
+ *   workspace  imp_nvfp4_gemm_workspace_size(M, N, K) bytes, 16-byte aligned
+ *            (else IMP_ERR_WORKSPACE_TOO_SMALL / IMP_ERR_MISALIGNED); owned by
+ *            the caller, needs no clearing; calls that may run at the same
+ *            time on the GPU need separate workspaces.
+ *   Decode shapes: every K up to 61440; beyond that the FP4 path takes
+ *   K % 256 == 0 with N >= 128 (other long-K shapes return
+ *   IMP_ERR_UNSUPPORTED_SHAPE).  imp_nvfp4_gemm_plan tells which kernel a
+ *   shape takes.
  *   Decode (M <= 16) kernels are launched with programmatic dependent launch:
  *   when the previous kernel on the stream allows it (this library's decode
  *   kernels do), the call may start streaming W before that kernel finishes;

@@ -96,6 +96,11 @@ def test_gemm_rejects_bad_arguments():
         pkg.IMP_ERR_WORKSPACE_TOO_SMALL
     assert g(A16, 1, 1024, 1024, _t(256, 1024), A16, 256, None, A16 + 8, need, None) == \
         pkg.IMP_ERR_MISALIGNED
+    # a long K that no decode kernel takes (X beyond the register-resident
+    # plans, K % 256 != 0 or N < 128 for the FP4 path): rejected, nothing enqueued
+    assert pkg.imp_nvfp4_gemm_plan(2, 100, 65472) == (0, None)
+    assert g(A16, 2, 65472, 65472, _t(100, 65472), A16, 104, None, None, 0, None) == \
+        pkg.IMP_ERR_UNSUPPORTED_SHAPE
     # empty problems are valid and enqueue nothing
     assert g(A16, 0, 64, 64, _t(8, 64), A16, 8, None, None, 0, None) == pkg.IMP_OK
     assert g(A16, 4, 64, 64, _t(0, 64), A16, 8, None, None, 0, None) == pkg.IMP_OK

@@ -104,6 +104,20 @@ def test_edge_shapes(M, K, N, ldx, ldy):
         check_within_tolerance(y, y_ref, bound, f"M{M} K{K} N{N} {via}")
 
 
+@pytest.mark.parametrize("M,K,N", [(1, 41536, 100), (3, 41536, 40)])
+def test_cuda_core_kernel_shapes(M, K, N):
+    # K too long for the f16 path's register-resident X and K % 256 != 0
+    # (no FP4 path): the CUDA-core kernel takes these
+    assert pkg.imp_nvfp4_gemm_plan(M, N, K)[1] == "gemv_kernel"
+    lin = synth.Linear("cc", M, K, N, 77, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
+                       zero_block_p=0.02, x_outlier_frac=0.02)
+    c, s, ts = oracle_w(lin)
+    x = lin.act_bf16()
+    y_ref, bound = oracle.reference_gemm(x, M, c, s, ts)
+    y = run_gemm(x, dev_nvfp4(c, s, ts))
+    check_within_tolerance(y, y_ref, bound, f"M{M} K{K} N{N} cuda cores")
+
+
 def test_gemm_mma_rejects_shapes_outside_the_decode_path():
     lin = synth.Linear("rej", 1, 320, 200, 3)
     c, s, ts = oracle_w(lin)
