@@ -1,9 +1,16 @@
 // Decode-path NVFP4 GEMV / skinny GEMM: Y[M][N] = X[M][K] * W^T for M <= 16.
 //
+// This file holds the dispatch between the decode kernels (launch_gemv,
+// choose_path: the FP4 tensor-core kernel of gemv_f4.cu, the f16
+// tensor-core kernel of gemv_tc.cu) and the CUDA-core kernel below, which
+// takes the shapes neither tensor-core kernel accepts (K beyond the f16
+// kernel's register-resident X, up to 61440, when the FP4 kernel's shape
+// rules are not met).
+//
 // Decode is bandwidth-bound: every weight byte is read once per step and the
 // arithmetic is trivial next to it (imp README, "How it works"; "1. The big
-// picture", section "The most important number in this book").  The kernel
-// is therefore built around streaming W at HBM speed:
+// picture", section "The most important number in this book").  The
+// CUDA-core kernel is therefore built around streaming W at HBM speed:
 //
 //  * Persistent grid, one CTA per SM; CTA c owns the contiguous row range
 //    [N*c/G, N*(c+1)/G) of W, so the load is balanced to within one row.
