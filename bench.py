@@ -455,9 +455,14 @@ def bench_prefill(args, pkg, dev, stream):
         y = torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), dtype=torch.uint8,
                          device=dev)
+        wsf = torch.empty(pkg.imp_nvfp4_gemm_fp4_workspace_size(l.M, l.N, l.K),
+                          dtype=torch.uint8, device=dev)
         flops = 2.0 * l.M * l.N * l.K
         out = {}
         for name, fn in (("gemm_fp4", lambda: pkg.gemm_fp4(xq, wm, y=y, stream=stream)),
+                         ("gemm_fp4_stream_k", lambda: pkg.gemm_fp4(xq, wm, y=y, stream=stream,
+                                                                    workspace=wsf,
+                                                                    stream_k=True)),
                          ("imp_nvfp4_gemm", lambda: pkg.gemm(x, w, y=y, stream=stream,
                                                              workspace=ws))):
             for _ in range(args.warmup):
@@ -574,7 +579,8 @@ def run_prefill_workload(args):
         items.append(dict(l=l, w=w, wm=pkg.prepare_mma(w), x=x, xq=pkg.quantize_mma(x),
                           y=torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev),
                           ws=torch.empty(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K),
-                                         dtype=torch.uint8, device=dev)))
+                                         dtype=torch.uint8, device=dev),
+                          ))
     flops = sum(2.0 * it["l"].M * it["l"].N * it["l"].K for it in items)
 
     def step():

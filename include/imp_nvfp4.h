@@ -208,15 +208,29 @@ imp_status imp_nvfp4_quantize_mma(const void *x_bf16, int64_t rows, int64_t K, i
                                   const imp_nvfp4_tensor *out, int32_t *dev_status,
                                   void *workspace, size_t ws_bytes, void *stream);
 
+/* Bytes of the optional workspace of imp_nvfp4_gemm_fp4 (on the current
+ * device): per-tile counters and one partial 128 x 256 fp32 tile per CTA
+ * and split segment (~39 MB on a 152-SM GPU).  0 for invalid sizes.       */
+size_t imp_nvfp4_gemm_fp4_workspace_size(int64_t M, int64_t N, int64_t K);
+
 /* Y = Xq * Wq^T, both operands NVFP4: the block-scaled FP4 tensor-core GEMM
  * alone (tcgen05.mma kind::mxf4nvf4, fp32 accumulation in tensor memory),
  * times s_x * s_w, rounded to bf16.
  *   xq  from imp_nvfp4_quantize_mma: M rows (M >= 1), row-major codes,
  *       atom-layout scales, K % 64 == 0;
  *   wq  N rows in MMA layout, wq->K == K;
- *   y   bf16[M][ldy], ldy >= N, ldy % 8 == 0.                             */
+ *   y   bf16[M][ldy], ldy >= N, ldy % 8 == 0.
+ *   workspace  NULL, or imp_nvfp4_gemm_fp4_workspace_size(M, N, K) bytes,
+ *       16-byte aligned (else IMP_ERR_WORKSPACE_TOO_SMALL / MISALIGNED),
+ *       needing no clearing.  With it the (tile, K step) work is spread
+ *       evenly over the SMs (stream-K: tiles split between CTAs are summed
+ *       from fp32 partials in K order, so results stay bitwise repeatable);
+ *       without it each CTA computes whole 128 x 256 tiles.  The two
+ *       schedules round differently (both within the accuracy of
+ *       imp_nvfp4_gemm).                                                   */
 imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor *wq,
-                              void *y_bf16, int64_t ldy, int32_t *dev_status, void *stream);
+                              void *y_bf16, int64_t ldy, int32_t *dev_status, void *workspace,
+                              size_t ws_bytes, void *stream);
 
 /* Y = X * W^T like imp_nvfp4_gemm, with W in MMA layout (the serving form:
  * weights prepared once, read as contiguous 16 KB tiles).  M <= 16 takes the

@@ -27,6 +27,7 @@ __all__ = [
     "quantize", "gemm",
     "library_path", "header_functions", "ImpError", "load", "imp_nvfp4_mma_scales_size",
     "imp_nvfp4_prepare_mma", "imp_nvfp4_quantize_mma", "imp_nvfp4_gemm_fp4", "prepare_mma",
+    "imp_nvfp4_gemm_fp4_workspace_size",
     "imp_nvfp4_quantize_noalloc", "imp_nvfp4_mma_codes_size", "imp_nvfp4_gemm_mma",
     "quantize_mma", "gemm_fp4", "gemm_mma", "imp_selftest_bounded_wait",
 ]
@@ -90,7 +91,9 @@ def _L():
     lib.imp_nvfp4_quantize_noalloc.restype = ctypes.c_int
     lib.imp_nvfp4_quantize_noalloc.argtypes = [P, I64, I64, I64, T, P, P]
     lib.imp_nvfp4_gemm_fp4.restype = ctypes.c_int
-    lib.imp_nvfp4_gemm_fp4.argtypes = [T, T, P, I64, P, P]
+    lib.imp_nvfp4_gemm_fp4.argtypes = [T, T, P, I64, P, P, SZ, P]
+    lib.imp_nvfp4_gemm_fp4_workspace_size.restype = SZ
+    lib.imp_nvfp4_gemm_fp4_workspace_size.argtypes = [I64, I64, I64]
     _lib = lib
     return lib
 
@@ -185,10 +188,15 @@ def imp_nvfp4_quantize_noalloc(x_bf16: int, rows: int, K: int, ldx: int, out: Im
                                            stream)
 
 
+def imp_nvfp4_gemm_fp4_workspace_size(M: int, N: int, K: int) -> int:
+    return _L().imp_nvfp4_gemm_fp4_workspace_size(M, N, K)
+
+
 def imp_nvfp4_gemm_fp4(xq: ImpNvfp4Tensor, wq: ImpNvfp4Tensor, y_bf16: int, ldy: int,
-                       dev_status: int | None, stream: int | None) -> int:
+                       dev_status: int | None, workspace: int | None, ws_bytes: int,
+                       stream: int | None) -> int:
     return _L().imp_nvfp4_gemm_fp4(ctypes.byref(xq), ctypes.byref(wq), y_bf16, ldy, dev_status,
-                                   stream)
+                                   workspace, ws_bytes, stream)
 
 
 class ImpError(RuntimeError):
@@ -314,15 +322,23 @@ def quantize_mma(x, dev_status=None, stream=None) -> NVFP4Tensor:
     return out
 
 
-def gemm_fp4(xq: NVFP4Tensor, wq: NVFP4Tensor, y=None, dev_status=None, stream=None):
-    """Y = Xq Wq^T on the block-scaled FP4 tensor cores (atom-layout scales)."""
+def gemm_fp4(xq: NVFP4Tensor, wq: NVFP4Tensor, y=None, dev_status=None, stream=None,
+             workspace=None, stream_k=False):
+    """Y = Xq Wq^T on the block-scaled FP4 tensor cores (atom-layout scales).
+    Whole 128 x 256 tiles per CTA; stream_k=True splits the (tile, K step)
+    work evenly over the SMs instead (allocates the workspace if none is
+    passed)."""
     import torch
     assert wq.layout == "mma"
     M, N = xq.rows, wq.rows
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.codes.device)
+    ws_bytes = imp_nvfp4_gemm_fp4_workspace_size(M, N, xq.K) if stream_k else 0
+    if stream_k and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=xq.codes.device)
     st = imp_nvfp4_gemm_fp4(_struct(xq), _struct(wq), y.data_ptr(), y.stride(0),
                             None if dev_status is None else dev_status.data_ptr(),
+                            workspace.data_ptr() if stream_k else None, ws_bytes,
                             _stream_handle(stream))
     if st != IMP_OK:
         raise ImpError(st, "imp_nvfp4_gemm_fp4")

@@ -23,11 +23,13 @@ imp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? IMP_OK : IMP_ERR
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Workspace of the prefill path: amax partials | X codes | X atom scales |
-// W atom scales | s_x.
 struct PrefillWs {
   size_t partial, xcodes, xsc, wsc, sx, total;
 };
+// Workspace of the prefill path: amax partials | X codes | X atom scales |
+// W atom scales | s_x.  The GEMM runs whole tiles per CTA (its stream-K
+// schedule, measured slower on the prefill shapes, is opt-in through
+// imp_nvfp4_gemm_fp4).
 PrefillWs prefill_ws(int64_t M, int64_t N, int64_t K) {
   PrefillWs w;
   w.partial = 0;
@@ -198,8 +200,14 @@ imp_status imp_nvfp4_quantize_mma(const void *x_bf16, int64_t rows, int64_t K, i
                                                static_cast<cudaStream_t>(stream)));
 }
 
+size_t imp_nvfp4_gemm_fp4_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 1 || K <= 0 || K % 64) return 0;
+  return impfp4::gemm_mxf4_workspace_bytes(M, N, K);
+}
+
 imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor *wq,
-                              void *y_bf16, int64_t ldy, int32_t *dev_status, void *stream) {
+                              void *y_bf16, int64_t ldy, int32_t *dev_status, void *workspace,
+                              size_t ws_bytes, void *stream) {
   if (!xq || !wq || !y_bf16) return IMP_ERR_INVALID_ARG;
   const int64_t M = xq->rows, N = wq->rows, K = xq->K;
   if (M < 1 || N < 1 || wq->K != K) return IMP_ERR_INVALID_ARG;
@@ -211,10 +219,14 @@ imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor
   if (st != IMP_OK) return st;
   if (ldy < N) return IMP_ERR_INVALID_ARG;
   if (!aligned16(y_bf16) || ldy % 8) return IMP_ERR_MISALIGNED;
+  if (workspace) {
+    if (ws_bytes < impfp4::gemm_mxf4_workspace_bytes(M, N, K)) return IMP_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  }
   return from_cuda(impfp4::launch_gemm_mxf4(xq->codes, xq->scales, xq->tensor_scale, wq->codes,
                                             true, wq->scales, wq->tensor_scale, M, N, K,
                                             static_cast<uint16_t *>(y_bf16), ldy, dev_status,
-                                            static_cast<cudaStream_t>(stream)));
+                                            workspace, static_cast<cudaStream_t>(stream)));
 }
 
 imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
@@ -256,7 +268,7 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
   if (e == cudaSuccess)
     e = impfp4::launch_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, wq.codes, false,
                                  wq.scales, wq.tensor_scale, M, N, K,
-                                 static_cast<uint16_t *>(y_bf16), ldy, dev_status, s);
+                                 static_cast<uint16_t *>(y_bf16), ldy, dev_status, nullptr, s);
   return from_cuda(e);
 }
 
@@ -297,7 +309,7 @@ imp_status imp_nvfp4_gemm_mma(const void *x_bf16, int64_t M, int64_t K, int64_t 
   if (e == cudaSuccess)
     e = impfp4::launch_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, w->codes, true, w->scales,
                                  w->tensor_scale, M, N, K, static_cast<uint16_t *>(y_bf16), ldy,
-                                 dev_status, s);
+                                 dev_status, nullptr, s);
   return from_cuda(e);
 }
 

@@ -165,4 +165,37 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// ---- split-tile hand-off (stream-K schedules) --------------------------------
+
+// Launch epochs for the split-tile counters: consecutive from a random start
+// per process (host).
+unsigned long long next_launch_epoch();
+
+// Counts one finished segment of a split tile; true for the tile's last.
+// A counter is 16 bytes: the launch's epoch (64 bits), a check word derived
+// from it (32 bits) and the count.  A value that does not carry this
+// launch's epoch and check -- an earlier launch's, or whatever the workspace
+// held before (a 2^-96 chance of a false match) -- counts as zero, so no
+// call has to clear the counters; the last CTA of a tile still leaves zero,
+// the first guess of the next launch.  Epochs start at a random value per
+// process and grow by one per launch.
+__device__ __forceinline__ bool count_split_segment(unsigned __int128 *c, unsigned long long epoch,
+                                              int nslot) {
+  const unsigned long long chk = (epoch * 0x9E3779B97F4A7C15ull) >> 32;
+  unsigned __int128 old = 0;  // the tile's last CTA of each launch leaves zero
+  while (true) {
+    const unsigned long long hi = (unsigned long long)(old >> 64), lo = (unsigned long long)old;
+    const unsigned long long cnt = (hi == epoch && (lo >> 32) == chk) ? (lo & 0xFFFFFFFFull) + 1 : 1;
+    const unsigned __int128 nv = ((unsigned __int128)epoch << 64) | ((chk << 32) | cnt);
+    const unsigned __int128 prev = atomicCAS(c, old, nv);
+    if (prev == old) {
+      if ((int)cnt != nslot) return false;
+      __stcg(reinterpret_cast<uint4 *>(c), make_uint4(0, 0, 0, 0));  // for the next launch
+      return true;
+    }
+    old = prev;  // not what was guessed: at most nslot + 1 rounds
+  }
+}
+
+
 }  // namespace impfp4

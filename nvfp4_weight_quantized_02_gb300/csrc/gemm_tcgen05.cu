@@ -72,6 +72,60 @@ struct GemmArgs {
   int64_t ldy;
   int M, N, K;
   int32_t *status;
+  // stream-K (with a workspace): per-tile counters and per-CTA partial tiles
+  unsigned __int128 *cnt;  // [tiles]
+  float *part;             // [CTA][first/last segment][128 rows][256 columns]
+  unsigned long long epoch;
+  int stream_k;
+};
+
+// The work of one CTA as segments (tile, K-stage range), in processing order.
+//  * Without a workspace: whole tiles blockIdx.x, + gridDim.x, ...
+//  * Stream-K: the (tile, K stage) sequence, tile-major, cut into gridDim.x
+//    equal contiguous ranges; a CTA's range covers whole tiles and at most two
+//    partial ones, which it processes first (its first segment, then its
+//    last) so that the split tiles' fix-ups overlap its whole tiles.
+struct Sched {
+  int sk, n_tiles, n_ks, G, c;
+  int64_t total, g0, g1;
+  int n_seg;
+  __device__ Sched(int sk_, int n_tiles_, int n_ks_)
+      : sk(sk_), n_tiles(n_tiles_), n_ks(n_ks_), G((int)gridDim.x), c((int)blockIdx.x) {
+    total = (int64_t)n_tiles * n_ks;
+    if (sk) {
+      g0 = total * c / G;
+      g1 = total * (c + 1) / G;
+      n_seg = g1 > g0 ? (int)((g1 - 1) / n_ks - g0 / n_ks) + 1 : 0;
+    } else {
+      g0 = g1 = 0;
+      n_seg = c < n_tiles ? (n_tiles - 1 - c) / G + 1 : 0;
+    }
+  }
+  // natural (K-ordered) index of the segment processed at position jj
+  __device__ int natural(int jj) const {
+    if (!sk || n_seg < 2) return jj;
+    return jj == 0 ? 0 : jj == 1 ? n_seg - 1 : jj - 1;
+  }
+  __device__ void seg(int jj, int &tile, int &k0, int &k1) const {
+    const int j = natural(jj);
+    if (!sk) {
+      tile = c + j * G;
+      k0 = 0;
+      k1 = n_ks;
+      return;
+    }
+    tile = (int)(g0 / n_ks) + j;
+    const int64_t b = (int64_t)tile * n_ks;
+    k0 = (int)((g0 > b ? g0 : b) - b);
+    k1 = (int)((g1 < b + n_ks ? g1 : b + n_ks) - b);
+  }
+  // CTA owning unit g (stream-K)
+  __device__ int owner(int64_t g) const { return (int)(((g + 1) * G - 1) / total); }
+  // partial slot CTA cc uses for tile t: its first segment 0, its last 1
+  __device__ int slot_of(int cc, int t) const {
+    const int64_t b0 = total * cc / G;
+    return (b0 / n_ks == t) ? 0 : 1;
+  }
 };
 
 // ---- tcgen05 helpers (inline PTX) --------------------------------------------
@@ -150,14 +204,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *accf = empty + NSTAGE;  // accumulator ready for the epilogue
   uint64_t *acce = accf + 1;        // accumulator drained by the epilogue
   uint64_t *sff = acce + 1;         // [NSTAGE] a stage's scales copied to tensor memory
-  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(sff + NSTAGE);
+  uint64_t *part_done = sff + NSTAGE;  // epilogue warps stored a split tile's partials
+  uint64_t *flag_ready = part_done + 1;  // the tile's count is known
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(flag_ready + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MB = (a.M + BM - 1) / BM, NB = (a.N + BN - 1) / BN;
   const int n_tiles = MB * NB;
   const int n_ks = (a.K + BK - 1) / BK;
   const int KA = a.K / 64;  // scale atoms per 128-row block
+  const Sched sch(a.stream_k, n_tiles, n_ks);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
@@ -167,6 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(accf, 1);
     mbar_init(acce, kEpiThreads);
+    mbar_init(part_done, kEpiThreads / 32);
+    mbar_init(flag_ready, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -189,9 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int64_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      for (int jj = 0; ok && jj < sch.n_seg; ++jj) {
+        int t, k0, k1;
+        sch.seg(jj, t, k0, k1);
         const int mb = t % MB, nb = t / MB;
-        for (int ks = 0; ks < n_ks; ++ks, ++it) {
+        for (int ks = k0; ks < k1; ++ks, ++it) {
           const int s = (int)(it % NSTAGE);
           if (it >= NSTAGE &&
               !mbar_wait_bounded(&empty[s], (uint32_t)(((it / NSTAGE) - 1) & 1), a.status)) {
@@ -241,14 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t issued = 0;         // stages consumed (for the drain on abort)
       int tile_iter = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tile_iter) {
+      for (int jj = 0; ok && jj < sch.n_seg; ++jj, ++tile_iter) {
+        int t, k0, k1;
+        sch.seg(jj, t, k0, k1);
         if (tile_iter > 0 &&
             !mbar_wait_bounded(acce, (uint32_t)((tile_iter - 1) & 1), a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < n_ks; ++ks) {
+        for (int ks = k0; ks < k1; ++ks) {
           // No shared-memory flag is read in this loop: a generic shared load
           // issued behind in-flight tcgen05.mma stalls the issuing thread
           // (measured: ~2.5x slower MMA issue).  A stalled peer shows up as
@@ -263,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t off = (uint64_t)(s * (STAGE_BYTES >> 4));
           const uint64_t dA = dA0 + off, dB = dB0 + off;
           const uint32_t sf0 = tmem + TMEM_SF + 48u * s;
-          const uint32_t acc0 = ks != 0 ? 1u : 0u;
+          const uint32_t acc0 = ks != k0 ? 1u : 0u;
           const int nk = (ks + 1 < n_ks || a.K % BK == 0) ? KSTEPS : (a.K - ks * BK) / MMA_K;
           if (nk == KSTEPS) {
 #pragma unroll
@@ -315,8 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t s = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        for (int ks = 0; ks < n_ks; ++ks) {
+      for (int jj = 0; ok && jj < sch.n_seg; ++jj) {
+        int t, k0, k1;
+        sch.seg(jj, t, k0, k1);
+        for (int ks = k0; ks < k1; ++ks) {
           // no shared-memory flag is read here either (see the MMA loop)
           if (!mbar_wait_bounded(&full[s], phase, a.status)) {
             ok = false;
@@ -356,47 +422,121 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_in_tile = quarter * 32 + lane;
     const int col0 = (warp - 2) / 4 * kEpiCols;  // warps 2..5: columns 0..127, 6..9: 128..255
     const float scale = (*a.s_x) * (*a.s_w);
-    int tile_iter = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_iter) {
+    // bf16 of 32 fp32 values (times s_x s_w) to columns c .. c + 31 of this
+    // thread's part of row m
+    auto store_bf16 = [&](int64_t m, int n0, int c, const float (&v)[32]) {
+      if (m >= a.M) return;
+      uint32_t p[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) p[i] = pack_bf16(v[2 * i] * scale, v[2 * i + 1] * scale);
+      uint16_t *dst = a.y + m * a.ldy + n0 + c;
+      if (n0 + c + 32 <= a.N) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (n0 + c + 2 * i < a.N) dst[2 * i] = (uint16_t)(p[i] & 0xFFFFu);
+          if (n0 + c + 2 * i + 1 < a.N) dst[2 * i + 1] = (uint16_t)(p[i] >> 16);
+        }
+      }
+    };
+    int n_split = 0;
+    for (int jj = 0; jj < sch.n_seg; ++jj) {
       const bool ready =
-          __all_sync(0xFFFFFFFFu, mbar_wait_bounded(accf, (uint32_t)(tile_iter & 1), a.status));
+          __all_sync(0xFFFFFFFFu, mbar_wait_bounded(accf, (uint32_t)(jj & 1), a.status));
       if (!ready || *abort_flag) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
+      int t, k0, k1;
+      sch.seg(jj, t, k0, k1);
       const int mb = t % MB, nb = t / MB;
       const int64_t m = (int64_t)mb * BM + row_in_tile;
       const int n0 = nb * BN + col0;
-      // Drain this warp's 128 accumulator columns 32 at a time, storing each
-      // chunk as bf16 straight away (stores do not wait), then hand the
-      // accumulator back to the MMA warp: the stores drain while the next
-      // tile's MMAs run.
-      uint16_t *dst = a.y + m * a.ldy + n0;
-      const bool full_row = m < a.M && n0 + kEpiCols <= a.N;
+      const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D + col0;
+      if (k0 == 0 && k1 == n_ks) {
+        // Whole tile: drain this warp's 128 accumulator columns 32 at a time,
+        // storing each chunk as bf16 straight away (stores do not wait), then
+        // hand the accumulator back: the stores drain under the next MMAs.
 #pragma unroll
-      for (int c = 0; c < kEpiCols; c += 32) {
-        uint32_t r[32];
-        tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D + col0 + c, r);
-        uint32_t p[16];
+        for (int c = 0; c < kEpiCols; c += 32) {
+          uint32_t r[32];
+          tc_ld32(tacc + c, r);
+          float v[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          p[i] = pack_bf16(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
-        if (full_row) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          store_bf16(m, n0, c, v);
+        }
+        tc_fence_before();
+        mbar_arrive(acce);  // accumulator may be overwritten now
+        continue;
+      }
+      // Split tile (stream-K): this CTA's fp32 partial of the tile goes to its
+      // slot in the workspace; the last of the tile's CTAs to finish adds all
+      // partials in K order (CTA order) and writes Y.
+      const int sl = sch.natural(jj) == 0 ? 0 : 1;
+      auto part_row = [&](int cc, int slot) {
+        return a.part + ((size_t)(2 * cc + slot) * BM + row_in_tile) * BN + col0;
+      };
+      {
+        float *pr = part_row((int)blockIdx.x, sl);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
-        } else if (m < a.M) {
+        for (int c = 0; c < kEpiCols; c += 32) {
+          uint32_t r[32];
+          tc_ld32(tacc + c, r);
+          float4 *p4 = reinterpret_cast<float4 *>(pr + c);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if (n0 + c + 2 * i < a.N) dst[c + 2 * i] = (uint16_t)(p[i] & 0xFFFFu);
-            if (n0 + c + 2 * i + 1 < a.N) dst[c + 2 * i + 1] = (uint16_t)(p[i] >> 16);
-          }
+          for (int i = 0; i < 8; ++i)
+            p4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
         }
       }
       tc_fence_before();
-      mbar_arrive(acce);  // accumulator may be overwritten now
+      mbar_arrive(acce);
+      // The warps report in (CTA scope); one thread makes the CTA's stores
+      // visible device-wide (a cumulative fence) and counts the segment.
+      const int64_t u0 = (int64_t)t * n_ks;
+      const int c_first = sch.owner(u0), c_last = sch.owner(u0 + n_ks - 1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(part_done);
+      const uint32_t par = (uint32_t)(n_split & 1);
+      ++n_split;
+      if (warp == 2 && lane == 0) {
+        const bool got = mbar_wait_bounded(part_done, par, a.status);
+        __threadfence();
+        *last_flag = got && count_split_segment(a.cnt + t, a.epoch, c_last - c_first + 1);
+        __threadfence();
+        mbar_arrive(flag_ready);
+      }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(flag_ready, par, a.status))) {
+        *abort_flag = 1;
+        break;
+      }
+      if (!*last_flag) continue;
+      __threadfence();
+#pragma unroll 1
+      for (int c = 0; c < kEpiCols; c += 32) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        for (int cc = c_first; cc <= c_last; ++cc) {
+          const float4 *q4 = reinterpret_cast<const float4 *>(part_row(cc, sch.slot_of(cc, t)) + c);
+          float4 q[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) q[i] = __ldcg(q4 + i);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            v[4 * i] += q[i].x;
+            v[4 * i + 1] += q[i].y;
+            v[4 * i + 2] += q[i].z;
+            v[4 * i + 3] += q[i].w;
+          }
+        }
+        store_bf16(m, n0, c, v);
+      }
     }
   }
 
@@ -438,11 +578,39 @@ bool make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
 
 size_t gemm_mxf4_smem_bytes() { return kSmemBytes; }
 
+namespace {
+// CTAs of a launch: one per SM, at most 256 (the partial-tile slots of the
+// workspace are sized for that many), at most one per unit of work.
+int64_t gemm_grid(int64_t M, int64_t N, int64_t K, bool stream_k) {
+  const int64_t tiles = ceil_div(M, BM) * ceil_div(N, BN);
+  const int64_t units = stream_k ? tiles * ceil_div(K, BK) : tiles;
+  int64_t grid = num_sms();
+  if (grid > 256) grid = 256;
+  return grid < units ? grid : units;
+}
+struct GemmWs {
+  size_t cnt, part, total;
+};
+GemmWs gemm_ws(int64_t M, int64_t N, int64_t K) {
+  GemmWs w;
+  const int64_t tiles = ceil_div(M, BM) * ceil_div(N, BN);
+  w.cnt = 0;
+  w.part = (size_t)ceil_div(tiles * 16, 256) * 256;
+  w.total = w.part + (size_t)gemm_grid(M, N, K, true) * 2 * BM * BN * sizeof(float);
+  return w;
+}
+}  // namespace
+
+size_t gemm_mxf4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 1 || K < 64) return 0;
+  return gemm_ws(M, N, K).total;
+}
+
 cudaError_t launch_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales,
                              const float *s_x, const uint8_t *w_codes, bool w_tiled,
                              const uint8_t *w_mma_scales, const float *s_w, int64_t M,
                              int64_t N, int64_t K, uint16_t *y, int64_t ldy, int32_t *status,
-                             cudaStream_t stream) {
+                             void *workspace, cudaStream_t stream) {
   CUtensorMap tmA, tmB;
   memset(&tmB, 0, sizeof(tmB));  // not read with tiled W codes
   if (!make_tmap_u8_2d(&tmA, x_codes, (uint64_t)M, (uint64_t)(K / 2), (uint64_t)(K / 2), BM, 128,
@@ -462,9 +630,18 @@ cudaError_t launch_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales
   a.N = (int)N;
   a.K = (int)K;
   a.status = status;
-  const int64_t tiles = ceil_div(M, BM) * ceil_div(N, BN);
-  int64_t grid = num_sms();
-  if (grid > tiles) grid = tiles;
+  a.stream_k = workspace != nullptr;
+  a.cnt = nullptr;
+  a.part = nullptr;
+  a.epoch = 0;
+  if (workspace) {
+    const GemmWs L = gemm_ws(M, N, K);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.cnt = reinterpret_cast<unsigned __int128 *>(ws + L.cnt);
+    a.part = reinterpret_cast<float *>(ws + L.part);
+    a.epoch = next_launch_epoch();
+  }
+  const int64_t grid = gemm_grid(M, N, K, workspace != nullptr);
   cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);

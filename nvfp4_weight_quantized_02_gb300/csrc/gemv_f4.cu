@@ -344,32 +344,6 @@ struct StreamK {
   __device__ int owner(int64_t g) const { return (int)(((g + 1) * G - 1) / total); }
 };
 
-// Counts one finished segment of a split tile; true for the tile's last.
-// A counter is 16 bytes: the launch's epoch (64 bits), a check word derived
-// from it (32 bits) and the count.  A value that does not carry this
-// launch's epoch and check -- an earlier launch's, or whatever the workspace
-// held before (a 2^-96 chance of a false match) -- counts as zero, so no
-// call has to clear the counters; the last CTA of a tile still leaves zero,
-// the first guess of the next launch.  Epochs start at a random value per
-// process and grow by one per launch.
-__device__ __forceinline__ bool count_segment(unsigned __int128 *c, unsigned long long epoch,
-                                              int nslot) {
-  const unsigned long long chk = (epoch * 0x9E3779B97F4A7C15ull) >> 32;
-  unsigned __int128 old = 0;  // the tile's last CTA of each launch leaves zero
-  while (true) {
-    const unsigned long long hi = (unsigned long long)(old >> 64), lo = (unsigned long long)old;
-    const unsigned long long cnt = (hi == epoch && (lo >> 32) == chk) ? (lo & 0xFFFFFFFFull) + 1 : 1;
-    const unsigned __int128 nv = ((unsigned __int128)epoch << 64) | ((chk << 32) | cnt);
-    const unsigned __int128 prev = atomicCAS(c, old, nv);
-    if (prev == old) {
-      if ((int)cnt != nslot) return false;
-      __stcg(reinterpret_cast<uint4 *>(c), make_uint4(0, 0, 0, 0));  // for the next launch
-      return true;
-    }
-    old = prev;  // not what was guessed: at most nslot + 1 rounds
-  }
-}
-
 // ---- issuer and epilogue loops, shared by both kernels ------------------------
 
 // Issuer `is` of NI: stages (in processing order) i = is, is + NI, ...  The
@@ -536,7 +510,7 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     if (warp == kEpiWarp0 && lane == 0) {
       const bool got = mbar_wait_bounded(&bars.part_done, par, a.status);
       __threadfence();
-      *last_flag = got && count_segment(a.cnt + T, a.epoch, nslot);
+      *last_flag = got && count_split_segment(a.cnt + T, a.epoch, nslot);
       __threadfence();
       mbar_arrive(&bars.flag_ready);
     }
@@ -1049,8 +1023,6 @@ struct MapEntry {
 std::mutex g_mu;
 MapEntry g_cache[32];
 int g_next = 0, g_used = 0;
-std::atomic<unsigned long long> g_epoch{0};
-std::once_flag g_epoch_once;
 
 bool cached_map(CUtensorMap &out, const void *base, uint64_t rows, uint64_t row_bytes,
                 uint32_t box_rows, uint32_t box_bytes, bool swz) {
@@ -1070,16 +1042,6 @@ bool cached_map(CUtensorMap &out, const void *base, uint64_t rows, uint64_t row_
   g_next = (g_next + 1) % 32;
   if (g_used < 32) ++g_used;
   return true;
-}
-
-// Launch epochs for the split-tile counters: consecutive from a random start.
-unsigned long long next_epoch() {
-  std::call_once(g_epoch_once, [] {
-    std::random_device rd;
-    g_epoch = ((unsigned long long)rd() << 32) ^ rd() ^
-              (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
-  });
-  return ++g_epoch;
 }
 
 template <class Kern, class... Args>
@@ -1124,7 +1086,7 @@ F4Args base_args(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const flo
   a.status = status;
   a.n_tiles = (int)ceil_div(N, kTileRows);
   a.n_chunks = (int)(K / kChunkK);
-  a.epoch = next_epoch();
+  a.epoch = next_launch_epoch();
   return a;
 }
 
@@ -1191,6 +1153,17 @@ cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_
 }
 
 }  // namespace
+
+unsigned long long next_launch_epoch() {
+  static std::atomic<unsigned long long> epoch{0};
+  static std::once_flag once;
+  std::call_once(once, [] {
+    std::random_device rd;
+    epoch = ((unsigned long long)rd() << 32) ^ rd() ^
+            (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+  });
+  return ++epoch;
+}
 
 bool gemv_f4_shape_ok(int64_t M, int64_t N, int64_t K) {
   return M >= 1 && M <= kDecodeMaxM && N >= kTileRows && N <= 0x7FFFFFFFll && K >= 4 * kChunkK &&

@@ -81,9 +81,10 @@ def run_prefill(lin, rows_check=None, cols_check=None, via="gemm"):
         y = pkg.gemm(dev_bf16(xb), w, dev_status=status)
     elif via == "gemm_mma":
         y = pkg.gemm_mma(dev_bf16(xb), pkg.prepare_mma(w), dev_status=status)
-    else:
+    else:  # "gemm_fp4" (whole tiles per CTA) or "gemm_fp4_sk" (stream-K)
         xq = pkg.quantize_mma(dev_bf16(xb), dev_status=status)
-        y = pkg.gemm_fp4(xq, pkg.prepare_mma(w), dev_status=status)
+        y = pkg.gemm_fp4(xq, pkg.prepare_mma(w), dev_status=status,
+                         stream_k=(via == "gemm_fp4_sk"))
     torch.cuda.synchronize()
     assert int(status.item()) == 0, int(status.item())
     y = y.float().cpu().numpy()
@@ -104,9 +105,8 @@ def run_prefill(lin, rows_check=None, cols_check=None, via="gemm"):
 def test_small_shapes_every_element(M, K, N):
     lin = synth.Linear("pf", M, K, N, 77, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
                        zero_block_p=0.01, x_outlier_frac=0.01)
-    run_prefill(lin, via="gemm_fp4")
-    run_prefill(lin, via="gemm")
-    run_prefill(lin, via="gemm_mma")
+    for via in ("gemm_fp4", "gemm_fp4_sk", "gemm", "gemm_mma"):
+        run_prefill(lin, via=via)
 
 
 @pytest.mark.parametrize("lin", synth.workload("prefill_27b"), ids=lambda l: f"{l.K}x{l.N}")
@@ -117,10 +117,18 @@ def test_full_size_sampled(lin):
     run_prefill(lin, rows_check=rows, cols_check=cols, via="gemm_mma")
 
 
-def test_repeatable():
-    lin = synth.Linear("rep", 256, 1024, 512, 5, w_dist=synth.DIST_STUDENT_T4)
+@pytest.mark.parametrize("M,K,N", [(256, 1024, 512), (640, 5120, 768)])
+def test_repeatable(M, K, N):
+    # (640, 5120, 768): 15 tiles of 20 K stages over all SMs, so every tile
+    # is summed from the partials of several CTAs
+    lin = synth.Linear("rep", M, K, N, 5, w_dist=synth.DIST_STUDENT_T4)
     xb, wb = lin.act_bf16(), lin.weight_bf16()
     w = pkg.quantize(dev_bf16(wb))
-    a = pkg.gemm(dev_bf16(xb), w).cpu()
-    b = pkg.gemm(dev_bf16(xb), w).cpu()
-    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    outs = [pkg.gemm(dev_bf16(xb), w).cpu() for _ in range(3)]
+    xq, wm = pkg.quantize_mma(dev_bf16(xb)), pkg.prepare_mma(w)
+    ws = torch.empty(pkg.imp_nvfp4_gemm_fp4_workspace_size(M, N, K), dtype=torch.uint8,
+                     device="cuda")
+    sk = [pkg.gemm_fp4(xq, wm, workspace=ws, stream_k=True).cpu() for _ in range(3)]
+    for runs in (outs, sk):
+        for o in runs[1:]:
+            assert torch.equal(runs[0].view(torch.int16), o.view(torch.int16))
