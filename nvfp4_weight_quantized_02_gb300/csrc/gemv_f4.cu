@@ -431,7 +431,7 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
 template <int NI, int NMMA>
 __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, const StreamK &sk,
                               int warp, int lane, const int (&sh)[kMaxRowsX]) {
-  constexpr int MR = NMMA / kNC;  // rows of X per pass
+  constexpr int MR = NMMA / kNC;  // rows of X the operand holds (>= M)
   const int q = warp & 3;
   const int row_in_tile = 32 * q + lane;
   const float out_scale = *a.tensor_scale;
