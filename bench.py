@@ -141,6 +141,17 @@ def cpu_oracle_sample(lins, budget_s: float, max_rows: int | None = None):
     return done_bytes / dt / 1e9, dt, desc
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time; every rank gets it (no-op on one process)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -257,10 +268,8 @@ def run_native(args):
         # second pass with per-kernel events (for the roofline of the top kernel)
         _, _, evs = timed_steps(args.steps, per_kernel=True)
         torch.cuda.synchronize()
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
         dist.barrier()
     st = int(status.item())
     if st != 0:
@@ -294,7 +303,7 @@ def run_native(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
 
     hbm_peak, _, peak_kind = load_peaks()
@@ -565,6 +574,8 @@ def run_prefill_workload(args):
 
     import nvfp4_weight_quantized_02_gb300 as pkg
 
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0  # one GPU: the prefill workload is measured by rank 0 alone
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     pkg.load()
