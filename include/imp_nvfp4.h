@@ -35,8 +35,11 @@
  *
  * Conventions for every entry point:
  *   - All buffers are DEVICE memory allocated and owned by the caller.  The
- *     library never allocates, frees or synchronizes, and keeps no state
- *     between calls (it is thread-compatible).
+ *     library never allocates, frees or synchronizes.  Between calls it
+ *     keeps only host-side caches, guarded for use from several threads:
+ *     TMA descriptors keyed by array address and shape, the SM count, and a
+ *     launch counter (plus the fixed scratch of
+ *     imp_nvfp4_quantize_noalloc).  Results never depend on them.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); all work
  *     is enqueued on it asynchronously.
  *   - The return value reports argument and launch errors only.  A call that

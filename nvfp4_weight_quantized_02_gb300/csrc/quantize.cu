@@ -12,6 +12,8 @@
 //      bit copied from x.  Every fp32 step is an explicitly rounded IEEE op
 //      (__fdiv_rn, __fmul_rn), so no contraction or approximation can change
 //      a byte.
+#include <atomic>
+
 #include "quantize.cuh"
 
 namespace impfp4 {
@@ -142,17 +144,19 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(
   }
 }
 
+// SM count of the current device, cached per device (threads may race to
+// fill an entry: they store the same value).
 int num_sms_cached() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 // One warp per row at a time; at most kMaxPartials CTAs, so the workspace
