@@ -16,7 +16,7 @@
 // [2^14, 2^15) and component c quantizing the residual left by components
 // 0..c-1 (block amax / 6 -> E4M3 scale; value / scale -> E2M1, nearest).
 // Each component shrinks a block's residual by a factor of at least ~5.6,
-// so eight of them leave less than ~1e-9 of the block's largest |x| (fp32
+// so eight of them leave a few 1e-9 of the block's largest |x| at most (fp32
 // rounding of the residual updates dominates).  Every MMA product
 // (E2M1 x E4M3 x E2M1 x E4M3) is exact; accumulation is fp32 in tensor
 // memory.  y sums the component columns with their power-of-two weights, in
