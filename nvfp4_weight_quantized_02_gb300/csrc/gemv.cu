@@ -388,7 +388,7 @@ DecodePath choose_path(int64_t M, int64_t N, int64_t K, bool workspace, const vo
                        const void *scales) {
   if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return DecodePath::kNone;
   const bool f4 = workspace && gemv_f4_supported(M, N, K, codes, scales);
-  if (f4 && M == 1 && 4 * ((N + 127) / 128) >= 3 * (int64_t)num_sms()) return DecodePath::kFp4;
+  if (f4 && M <= 2) return DecodePath::kFp4;
   const int tc_passes = gemv_tc_launches(M, N, K);
   if (tc_passes == 1) return DecodePath::kF16;
   if (f4) return DecodePath::kFp4;

@@ -73,6 +73,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kXsplitThreads = 256;
 constexpr int kPrefetch = 12;   // stages of W prefetched into L2 at the start
 constexpr int kEpiWarp0 = 8;    // warps 8..11: epilogue (tensor-memory lane quarters 0..3)
+constexpr int kRelayWarp = 6;   // row-major W: relays the scale rows into atoms
 constexpr int kThreads = 384;
 // The split-tile partials are sized for at most kMaxGrid CTAs, so the
 // workspace size does not depend on the device.
@@ -104,18 +105,23 @@ template <int NMMA> struct StageS {
 // ---- resident-B kernel (M <= 2, N_MMA = 16)
 constexpr int kIssuersR = 4, kProducerR = 4, kNSR = 8;  // stage st and st - 8: same issuer
 constexpr int kMaxSlotsR = 24;                           // K chunks of X held per CTA
-constexpr int kHelperWarp0R = 5;                         // warps 5..11 split X
-constexpr int kHelperThreadsR = kThreads - 32 * kHelperWarp0R;
+constexpr int kLoaderWarpR = 5;                          // warp 5: copies the B slots in
+constexpr int kSplitWarps = 8;                           // chunks per CTA of the split kernel
 // W scales land where their atoms go: a row-major weight's 128 x 16-byte
 // scale rows are relaid in place (read, warp sync, write).
 struct StageR {
   static constexpr uint32_t W = 0, RAW = 16384, SFA = 16384, BYTES = 18432;
   static constexpr uint32_t TX = 16384 + 2048;
 };
-// B slot q: codes at BCODES + 2048 q (16 rows x 128 B, swizzled); the scales
-// of its four K64 steps at BSF + 1024 q + 256 t: operand rows 0..15 are lines
-// 0..15 of a 512-byte atom, whose copy reads 256 bytes past them (the next
-// step's lines, or a zeroed pad) into lanes no N = 16 MMA reads.
+// B slot image of one K chunk (written once per call by xsplit_slots_kernel
+// into the workspace, copied as is into shared memory): codes, 2 KB = 16
+// operand rows x 128 B, row n at 128 n with its 16-byte unit u at unit
+// u ^ (n % 8) (the 128-byte swizzle); scales, 1 KB = four K64 steps of 256 B,
+// operand row n of step t at 256 t + 16 n (the row's 4 block scales; 12 zero
+// bytes): lines 0..15 of a 512-byte atom, whose copy reads 256 bytes past
+// them (the next step's lines, or a zeroed pad) into lanes no N = 16 MMA
+// reads.  Operand row 8 m + c holds component c of row m of X; rows past the
+// last component are zero.
 
 struct F4Args {
   const uint16_t *x;    // resident kernel: X rows
@@ -125,7 +131,8 @@ struct F4Args {
   int M;
   int64_t N, K;
   const float *tensor_scale;
-  const uint8_t *sfb;   // streamed kernel: X component scale atoms, [K/64][512]
+  const uint8_t *sfb;   // X component scales: streamed kernel atoms [K/64][512]; resident kernel slot images [K/256][1 KB]
+  const uint8_t *slot_codes;  // resident kernel: X component codes, slot images [K/256][2 KB]
   const int32_t *sh;    // streamed kernel: per-row prescale exponents
   float *part;          // split-tile partial sums, [CTA][first/last segment][128][N_MMA / 8]
   unsigned __int128 *cnt;   // per tile: epoch, its check word and segments finished
@@ -134,19 +141,21 @@ struct F4Args {
   int n_chunks;         // K / 256
   unsigned long long epoch;  // unique per launch
   int n_slots;          // resident kernel: B slots in shared memory
+  int sched;            // kSchedStreamK / kSchedWhole / kSchedCluster
+  int ksplit;           // kSchedCluster: CTAs per tile (the cluster size)
   const uint8_t *wc;    // prepared weight: code tiles [128-row block][chunk][16 KB]
   const uint8_t *wsa;   // prepared weight: scale atoms [128-row block][K/64][512 B]
 };
 
 struct F4Bars {
-  uint64_t full[8], empty[8];
+  uint64_t full[8], empty[8], sf_ready[8];
   uint64_t d_full[4][2], d_empty[2];
   uint64_t drain[4];
   uint64_t part_done, flag_ready;  // split-tile hand-off among the epilogue warps
-  uint64_t b_ready[32];            // resident kernel: B slot q split and visible
+  uint64_t cl_full;                // kSchedCluster, rank 0: the other ranks' partials arrived
+  uint64_t b_ready;                // resident kernel: every B slot has landed
   uint32_t tmem;
   int last;
-  uint32_t xmax[2];
 };
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
@@ -168,9 +177,6 @@ __host__ __device__ constexpr uint32_t idesc_f4() {
          ((uint32_t)(kTileRows >> 4) << 24);
 }
 
-__device__ __forceinline__ void named_bar(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
@@ -219,6 +225,52 @@ __device__ __forceinline__ void tmem_free(uint32_t tmem) {
 }
 
 __device__ __forceinline__ float e4m3_to_f32(uint32_t b) { return f16lo_to_f32(e4m3x2_to_f16x2(b)); }
+
+// ---- thread-block cluster helpers (kSchedCluster) -----------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+// Bounded wait on a local mbarrier whose arrivals come from other CTAs of the
+// cluster (acquire at cluster scope: their stores before the arrive are seen).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity,
+                                                          int32_t *status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i) {
+      uint32_t ok;
+      asm volatile(
+          "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+          "selp.u32 %0, 1, 0, p;\n}"
+          : "=r"(ok)
+          : "r"(smem_u32(bar)), "r"(parity)
+          : "memory");
+      if (ok) return true;
+    }
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      report(status, IMP_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+// Every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
+}
 
 // ---- the split of X ----------------------------------------------------------
 
@@ -303,21 +355,47 @@ __device__ __forceinline__ void split_block(const uint16_t *p, int sh, uint2 (&c
 
 // ---- stream-K bookkeeping -----------------------------------------------------
 
+// Work schedules over the (128-row tile, 256-element chunk) sequence,
+// tile-major; every CTA gets one contiguous range of it:
+//  * kSchedStreamK: equal ranges (tiles split between CTAs are summed from
+//    fp32 partials in the workspace by the tile's last CTA);
+//  * kSchedWhole: whole tiles, as evenly as they divide (no split tiles);
+//  * kSchedCluster: each tile's chunks split evenly over the S CTAs of one
+//    thread-block cluster (CTA rank r takes part r); the ranks' partial sums
+//    meet in rank 0's shared memory (distributed shared memory, no global
+//    round trips) and rank 0 adds them in K order.
+enum { kSchedStreamK = 0, kSchedWhole = 1, kSchedCluster = 2 };
+
 struct StreamK {
   int64_t total, g_begin, g_end;
   int nch, n_st, n_seg, G;
-  __device__ StreamK(int n_tiles, int n_chunks) {
+  int tile0, ch0;  // tile and chunk of the CTA's first stage
+  int e0, sl, nl;  // end of the first segment; start and length of the last
+  __device__ StreamK(int n_tiles, int n_chunks, int sched, int S) {
     G = gridDim.x;
     nch = n_chunks;
     total = (int64_t)n_tiles * nch;
-    g_begin = total * blockIdx.x / G;
-    g_end = total * (blockIdx.x + 1) / G;
+    if (sched == kSchedWhole) {
+      g_begin = (int64_t)n_tiles * blockIdx.x / G * nch;
+      g_end = (int64_t)n_tiles * (blockIdx.x + 1) / G * nch;
+    } else if (sched == kSchedCluster) {
+      const int64_t t = blockIdx.x / S, r = blockIdx.x % S;
+      g_begin = t * nch + nch * r / S;
+      g_end = t * nch + nch * (r + 1) / S;
+    } else {
+      g_begin = total * blockIdx.x / G;
+      g_end = total * (blockIdx.x + 1) / G;
+    }
     n_st = (int)(g_end - g_begin);
     n_seg = n_st > 0 ? (int)((g_end - 1) / nch - g_begin / nch) + 1 : 0;
+    tile0 = (int)(g_begin / nch);
+    ch0 = (int)(g_begin % nch);
+    e0 = n_seg > 0 ? seg_end(0) : 0;
+    sl = n_seg > 0 ? seg_begin(n_seg - 1) : 0;
+    nl = n_st - sl;
   }
   __device__ int seg_begin(int j) const {  // first stage of local segment j
-    const int64_t g0 = (g_begin / nch + j) * nch;
-    return (int)((g0 > g_begin ? g0 : g_begin) - g_begin);
+    return j == 0 ? 0 : j * nch - ch0;
   }
   __device__ int seg_end(int j) const { return j + 1 < n_seg ? seg_begin(j + 1) : n_st; }
   // Processing order: the first segment, then the last, then the middle ones
@@ -327,9 +405,8 @@ struct StreamK {
   __device__ int proc_seg(int jj) const { return jj == 0 ? 0 : jj == 1 ? n_seg - 1 : jj - 1; }
   __device__ int pbegin(int jj) const {
     if (jj == 0) return 0;
-    const int e0 = seg_end(0);
     if (jj == 1) return e0;
-    return n_st - seg_begin(n_seg - 1) + seg_begin(jj - 1);
+    return nl + seg_begin(jj - 1);
   }
   __device__ int pend(int jj) const {
     const int j = proc_seg(jj);
@@ -337,8 +414,13 @@ struct StreamK {
   }
   __device__ int stage_of(int i) const {
     if (n_seg < 2) return i;
-    const int e0 = seg_end(0), sl = seg_begin(n_seg - 1), nl = n_st - sl;
     return i < e0 ? i : i < e0 + nl ? sl + (i - e0) : i - nl;
+  }
+  // tile and chunk of stage st (32-bit arithmetic)
+  __device__ void tile_ch(int st, int &tile, int &ch) const {
+    const int c = ch0 + st, q = c / nch;
+    tile = tile0 + q;
+    ch = c - q * nch;
   }
   // CTA owning global chunk g
   __device__ int owner(int64_t g) const { return (int)(((g + 1) * G - 1) / total); }
@@ -346,20 +428,48 @@ struct StreamK {
 
 // ---- issuer and epilogue loops, shared by both kernels ------------------------
 
-// Issuer `is` of NI: stages (in processing order) i = is, is + NI, ...  The
-// warp relays the W scales of each stage into atoms; lane 0 copies both
-// operands' atoms and issues the MMAs.  `b_desc(i, st, t)` /
+// W scale relay (one warp, weights in row-major layout): per stage, the
+// 128 x 16-byte scale rows that landed with the codes -> four 512-byte atoms
+// (the tcgen05.cp source layout), then sf_ready[s].  The issuers wait on
+// sf_ready instead of full, so the relay stays off their path.
+template <int NS, class Stage>
+__device__ void relay_loop(uint8_t *smem, F4Bars &bars, const StreamK &sk, int lane,
+                           int32_t *status) {
+  for (int i = 0; i < sk.n_st; ++i) {
+    const int s = i % NS;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.full[s], (uint32_t)((i / NS) & 1), status)))
+      return;
+    uint8_t *stg = smem + (size_t)s * Stage::BYTES;
+    uint4 rq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      rq[q] = *reinterpret_cast<const uint4 *>(stg + Stage::RAW + 16 * (lane + 32 * q));
+    __syncwarp();  // the atoms may overwrite the rows just read
+    *reinterpret_cast<uint4 *>(stg + Stage::SFA + 0 * 512 + 16 * lane) = make_uint4(rq[0].x, rq[1].x, rq[2].x, rq[3].x);
+    *reinterpret_cast<uint4 *>(stg + Stage::SFA + 1 * 512 + 16 * lane) = make_uint4(rq[0].y, rq[1].y, rq[2].y, rq[3].y);
+    *reinterpret_cast<uint4 *>(stg + Stage::SFA + 2 * 512 + 16 * lane) = make_uint4(rq[0].z, rq[1].z, rq[2].z, rq[3].z);
+    *reinterpret_cast<uint4 *>(stg + Stage::SFA + 3 * 512 + 16 * lane) = make_uint4(rq[0].w, rq[1].w, rq[2].w, rq[3].w);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.sf_ready[s]);
+  }
+}
+
+// Issuer `is` of NI: stages (in processing order) i = is, is + NI, ...  Lane
+// 0 copies both operands' scale atoms of the stage into its bank of tensor
+// memory (tcgen05.cp) and issues its four K64 MMAs into the issuer's own
+// accumulator; the epilogue adds the NI accumulators.  `b_desc(i, st, t)` /
 // `sfb_desc(i, st, t)`: the B operand and its scale atom for K64 step t of
 // processing position i (stage st); `b_wait(st)`: waits (bounded) until that
-// B is in shared memory.
+// B is in shared memory.  All per-stage bookkeeping is 32-bit integer work:
+// every instruction of this loop sits between MMA issues.
 template <int NI, int NS, int NMMA, bool PREP, class Stage, class BDesc, class SFBDesc, class BWait>
 __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const StreamK &sk,
                             int is, int lane, int32_t *status, BDesc b_desc, SFBDesc sfb_desc,
                             BWait b_wait) {
   constexpr uint32_t kIdesc = idesc_f4<NMMA>();
   constexpr uint32_t kSF0 = 2 * NI * NMMA;  // scale columns after the accumulators
-  constexpr int NB = NS / NI;               // scale banks per issuer
-  static_assert(NS % NI == 0 && kSF0 + 32 * NS <= kTmemCols, "tensor memory plan");
+  static_assert(kSF0 + 32 * NS <= kTmemCols, "tensor memory plan");
   const uint32_t sbase = smem_u32(smem);
   const uint64_t dA0 = sdesc(sbase + Stage::W, 16, 1024, kSw128);
   const uint64_t dSA0 = sdesc(sbase + Stage::SFA, 0, 128, kNoSwizzle);
@@ -375,32 +485,20 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
         ok = false;
         break;
       }
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.full[s], (uint32_t)((i / NS) & 1), status) &&
+      // the stage's W (and, row-major, its relaid scale atoms) and its B
+      uint64_t *ready = PREP ? &bars.full[s] : &bars.sf_ready[s];
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(ready, (uint32_t)((i / NS) & 1), status) &&
                                        b_wait(st))) {
         ok = false;
         break;
       }
-      if (!PREP) {  // W scales, row-major [128][16 B] -> four 512-byte atoms
-        uint8_t *stg = smem + (size_t)s * Stage::BYTES;
-        uint4 rq[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          rq[q] = *reinterpret_cast<const uint4 *>(stg + Stage::RAW + 16 * (lane + 32 * q));
-        __syncwarp();  // the atoms may overwrite the rows just read
-        *reinterpret_cast<uint4 *>(stg + Stage::SFA + 0 * 512 + 16 * lane) = make_uint4(rq[0].x, rq[1].x, rq[2].x, rq[3].x);
-        *reinterpret_cast<uint4 *>(stg + Stage::SFA + 1 * 512 + 16 * lane) = make_uint4(rq[0].y, rq[1].y, rq[2].y, rq[3].y);
-        *reinterpret_cast<uint4 *>(stg + Stage::SFA + 2 * 512 + 16 * lane) = make_uint4(rq[0].z, rq[1].z, rq[2].z, rq[3].z);
-        *reinterpret_cast<uint4 *>(stg + Stage::SFA + 3 * 512 + 16 * lane) = make_uint4(rq[0].w, rq[1].w, rq[2].w, rq[3].w);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      __syncwarp();
       if (lane == 0) {
         tc_fence_after();
         const uint64_t off = (uint64_t)(s * (Stage::BYTES >> 4));
-        // Scale bank (i / NI) % NB: its previous user, stage i - NS, was
-        // this issuer's too (NS == NB NI), and the producer refilled slot s
-        // only after that stage's commit.
-        const uint32_t sf = tmem + kSF0 + 32u * (uint32_t)(NB * is + (i / NI) % NB);
+        // Scale bank s (32 columns: step t's W atom at 8 t, B's at 8 t + 4):
+        // its previous user, stage i - NS, completed before the producer
+        // refilled slot s.
+        const uint32_t sf = tmem + kSF0 + 32u * (uint32_t)s;
         const uint32_t dt = tmem + (uint32_t)((2 * is + d) * NMMA);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -430,7 +528,7 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
 // row -> y (whole tile) or a partial sum (split tile, last CTA adds them).
 template <int NI, int NMMA>
 __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, const StreamK &sk,
-                              int warp, int lane, const int (&sh)[kMaxRowsX]) {
+                              int warp, int lane, const int (&sh)[kMaxRowsX], float *red) {
   constexpr int MR = NMMA / kNC;  // rows of X the operand holds (>= M)
   const int q = warp & 3;
   const int row_in_tile = 32 * q + lane;
@@ -440,9 +538,10 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
   for (int jj = 0; jj < sk.n_seg; ++jj) {
     const int d = jj & 1, j = sk.proc_seg(jj);
     const int s0 = sk.seg_begin(j), s1 = sk.seg_end(j);
-    const int p0 = sk.pbegin(jj);
-    const int64_t T = (sk.g_begin + s0) / sk.nch;
-    const int c0 = (int)((sk.g_begin + s0) % sk.nch), c1 = c0 + (s1 - s0);
+    int T32, c0;
+    sk.tile_ch(s0, T32, c0);
+    const int64_t T = T32;
+    const int c1 = c0 + (s1 - s0);
     bool ok = true;
     for (int i = 0; i < NI; ++i)
       ok = ok && mbar_wait_bounded(&bars.d_full[i][d], (uint32_t)((jj >> 1) & 1), a.status);
@@ -451,6 +550,7 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     float acc[MR];
 #pragma unroll
     for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
+    const int p0 = sk.pbegin(jj);
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
       if (s1 - s0 >= NI || ((i - p0) % NI + NI) % NI < s1 - s0) {  // issuer i had a stage
@@ -476,6 +576,30 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     for (int m = 0; m < MR; ++m) acc[m] = ldexpf(acc[m] * out_scale, -sh[m]);
     if (c0 == 0 && c1 == sk.nch) {  // whole tile in this CTA
       if (row < a.N) {
+#pragma unroll
+        for (int m = 0; m < MR; ++m)
+          if (m < a.M) a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+      }
+      continue;
+    }
+    if (a.sched == kSchedCluster) {
+      // Part r of the tile's chunks.  Ranks 1..S-1 store their row's partial
+      // sums into rank 0's buffer red[r - 1][row] and arrive (one per warp)
+      // on its barrier; rank 0 adds them to its own in rank (= K) order.
+      const uint32_t rank = cluster_ctarank();
+      if (rank != 0) {
+        const uint32_t dst =
+            cluster_map(smem_u32(red + ((size_t)(rank - 1) * kTileRows + row_in_tile) * MR), 0);
+#pragma unroll
+        for (int m = 0; m < MR; ++m) st_cluster_f32(dst + 4u * m, acc[m]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(cluster_map(smem_u32(&bars.cl_full), 0));
+      } else if (__all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(&bars.cl_full, 0u, a.status)) &&
+                 row < a.N) {
+        for (int r = 1; r < a.ksplit; ++r) {
+#pragma unroll
+          for (int m = 0; m < MR; ++m) acc[m] += red[((size_t)(r - 1) * kTileRows + row_in_tile) * MR + m];
+        }
 #pragma unroll
         for (int m = 0; m < MR; ++m)
           if (m < a.M) a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
@@ -575,6 +699,7 @@ __device__ __forceinline__ void init_common(F4Bars &bars, int ns, int ni) {
   for (int s = 0; s < ns; ++s) {
     mbar_init(&bars.full[s], 1);
     mbar_init(&bars.empty[s], 1);
+    mbar_init(&bars.sf_ready[s], 1);
   }
   for (int i = 0; i < ni; ++i) {
     mbar_init(&bars.d_full[i][0], 1);
@@ -585,7 +710,6 @@ __device__ __forceinline__ void init_common(F4Bars &bars, int ns, int ni) {
   mbar_init(&bars.d_empty[1], 4);
   mbar_init(&bars.part_done, 4);
   mbar_init(&bars.flag_ready, 1);
-  bars.xmax[0] = bars.xmax[1] = 0u;
   fence_mbar_init();
 }
 
@@ -651,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   F4Bars &bars = *reinterpret_cast<F4Bars *>(smem + NS * L::BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const StreamK sk(a.n_tiles, a.n_chunks);
+  const StreamK sk(a.n_tiles, a.n_chunks, a.sched, a.ksplit);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) init_common(bars, NS, NI);
@@ -672,13 +796,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_w = [&](int i) {
         const int s = i % NS;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
-        const int64_t g = sk.g_begin + sk.stage_of(i);
-        const int64_t tile = g / sk.nch;
-        const int row0 = (int)tile * kTileRows, ch = (int)(g % sk.nch);
+        int tile, ch;
+        sk.tile_ch(sk.stage_of(i), tile, ch);
+        const int row0 = tile * kTileRows;
         mbar_arrive_expect_tx(&bars.full[s], L::TX);
         if (PREP) {
-          bulk_g2s(stg + L::W, a.wc + (tile * sk.nch + ch) * 16384, 16384u, &bars.full[s]);
-          bulk_g2s(stg + L::SFA, a.wsa + (tile * (a.K / 64) + 4 * ch) * 512, 2048u, &bars.full[s]);
+          bulk_g2s(stg + L::W, a.wc + ((int64_t)tile * sk.nch + ch) * 16384, 16384u, &bars.full[s]);
+          bulk_g2s(stg + L::SFA, a.wsa + ((int64_t)tile * (a.K / 64) + 4 * ch) * 512, 2048u,
+                   &bars.full[s]);
         } else {
           tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
           tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
@@ -687,20 +812,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_x = [&](int i) {
         const int s = i % NS;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
-        const int ch = (int)((sk.g_begin + sk.stage_of(i)) % sk.nch);
+        int tile, ch;
+        sk.tile_ch(sk.stage_of(i), tile, ch);
         tma_load_2d(stg + L::B, &tm_b, ch * (kChunkK / 2), 0, &bars.full[s]);
         bulk_g2s(stg + L::SFB, a.sfb + (size_t)ch * 2048, 2048u, &bars.full[s]);
       };
       auto prefetch_w = [&](int i) {
-        const int64_t g = sk.g_begin + sk.stage_of(i);
-        const int64_t tile = g / sk.nch;
-        const int ch = (int)(g % sk.nch);
+        int tile, ch;
+        sk.tile_ch(sk.stage_of(i), tile, ch);
         if (PREP) {
-          bulk_prefetch_l2(a.wc + (tile * sk.nch + ch) * 16384, 16384u);
-          bulk_prefetch_l2(a.wsa + (tile * (a.K / 64) + 4 * ch) * 512, 2048u);
+          bulk_prefetch_l2(a.wc + ((int64_t)tile * sk.nch + ch) * 16384, 16384u);
+          bulk_prefetch_l2(a.wsa + ((int64_t)tile * (a.K / 64) + 4 * ch) * 512, 2048u);
         } else {
-          tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), (int)tile * kTileRows);
-          tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), (int)tile * kTileRows);
+          tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), tile * kTileRows);
+          tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), tile * kTileRows);
         }
       };
       // W of the first stages before the previous kernel has finished, and
@@ -733,13 +858,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     issuer_loop<NI, NS, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
                                           sfb_desc, [](int) { return true; });
+  } else if (warp == kRelayWarp) {
+    if (!PREP) relay_loop<NS, L>(smem, bars, sk, lane, a.status);
   } else if (warp >= kEpiWarp0) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int sh[kMaxRowsX] = {};
 #pragma unroll
     for (int m = 0; m < NMMA / kNC; ++m)
       if (m < a.M) sh[m] = a.sh[m];
-    epilogue_loop<NI, NMMA>(a, bars, tmem, sk, warp, lane, sh);
+    epilogue_loop<NI, NMMA>(a, bars, tmem, sk, warp, lane, sh, nullptr);
   }
 
   tc_fence_before();
@@ -753,6 +880,99 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- resident-B path (M <= 2) ---------------------------------------------------
 
+// X (M <= 2 rows) -> B slot images of every K chunk, once per call.  Grid
+// (chunks / kSplitWarps rounded up, M); CTA (j, m) finds row m's max|x| (the
+// prescale 2^sh puts it in [2^14, 2^15)), then warp w splits chunk
+// kSplitWarps j + w of row m into its eight components: lane 2 b + h holds
+// elements 8 h .. 8 h + 7 of the chunk's block b.  Writes the images' rows
+// 8 m .. 8 m + 7 (and, for the last row of X, zeros in the rows after it) and
+// sh[m].
+__global__ void __launch_bounds__(32 * kSplitWarps)
+    xsplit_slots_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, uint8_t *slot_codes,
+                        uint8_t *slot_sf, int32_t *sh_out) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // X may come from the previous kernel, and the previous GEMV may still
+  // read the workspace: wait for it before touching either.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ uint32_t red[kSplitWarps];
+  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint16_t *xr = x + m * ldx;
+  uint32_t mx = 0;
+  for (int64_t i = threadIdx.x; i < K / 8; i += 32 * kSplitWarps)
+    mx = max(mx, absmax_bf16x8(__ldg(reinterpret_cast<const uint4 *>(xr) + i)));
+  for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = 0;
+  for (int w = 0; w < kSplitWarps; ++w) mx = max(mx, red[w]);
+  const int sh = prescale_exponent(mx);
+  if (blockIdx.x == 0 && threadIdx.x == 0) sh_out[m] = sh;
+
+  const int ch = blockIdx.x * kSplitWarps + warp;
+  if (ch >= (int)(K / kChunkK)) return;
+  const int bb = lane >> 1, hf = lane & 1;
+  const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + (int64_t)ch * kChunkK + 16 * bb + 8 * hf));
+  uint8_t *codes = slot_codes + (size_t)ch * 2048;
+  uint8_t *sf = slot_sf + (size_t)ch * 1024;
+  const float p1 = pow2f(sh / 2), p2 = pow2f(sh - sh / 2);
+  float r[8];
+  {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      r[2 * t] = bf16_bits_to_f32(w[t] & 0xFFFFu) * p1 * p2;
+      r[2 * t + 1] = bf16_bits_to_f32(w[t] >> 16) * p1 * p2;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < kNC; ++c) {
+    const int n = m * kNC + c;
+    float m4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m4[e] = fmaxf(fabsf(r[e]), fabsf(r[e + 4]));
+    float amax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));  // the block's other half
+    // Any scale is valid -- the residual tracks what was taken -- so an
+    // approximate reciprocal stands in for the division.
+    const uint32_t sb = f32_to_e4m3_satfinite(amax * (1.0f / 6.0f) * pow2f(2 * c - 4));
+    const float d = e4m3_to_f32(sb) * pow2f(4 - 2 * c);
+    uint32_t cw = 0u;
+    if (d > 0.0f) {
+      float inv;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(d));
+      float q[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[e] = r[e] * inv;
+      cw = f32x8_to_e2m1_packed(q);
+      uint32_t e2[4];
+      e2m1x8_to_f16x2x4(cw, e2);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {  // e2m1 * d is exact; one rounding per update
+        r[2 * t] = fmaf(-f16lo_to_f32(e2[t]), d, r[2 * t]);
+        r[2 * t + 1] = fmaf(-f16hi_to_f32(e2[t]), d, r[2 * t + 1]);
+      }
+    }
+    *reinterpret_cast<uint32_t *>(codes + n * 128 + (((bb >> 1) ^ (n & 7)) << 4) + 8 * (bb & 1) +
+                                  4 * hf) = cw;
+    // the four scales of K64 step t sit in lanes 8 t, 8 t + 2, 8 t + 4, 8 t + 6
+    const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+    const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
+    const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
+    if ((lane & 7) == 0)
+      *reinterpret_cast<uint4 *>(sf + (lane >> 3) * 256 + 16 * n) =
+          make_uint4(sb | s1 << 8 | s2 << 16 | s3 << 24, 0u, 0u, 0u);
+  }
+  if (m == M - 1 && M * kNC < 16) {
+    // operand rows after the last component: zero codes and scale lines
+    const int n0 = M * kNC, nr = 16 - n0;
+    uint4 *zc = reinterpret_cast<uint4 *>(codes + n0 * 128);
+    for (int i = lane; i < nr * 8; i += 32) zc[i] = make_uint4(0, 0, 0, 0);
+    for (int i = lane; i < 4 * nr; i += 32)
+      *reinterpret_cast<uint4 *>(sf + (i / nr) * 256 + 16 * (n0 + i % nr)) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+
 template <bool PREP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_f4r_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
@@ -764,18 +984,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *bcodes = smem + kNSR * L::BYTES;                   // [slot][16 rows][128 B], swizzled
   uint8_t *bsf = bcodes + (size_t)a.n_slots * 2048;           // [slot][4 steps][256 B] + pad
   F4Bars &bars = *reinterpret_cast<F4Bars *>(bsf + (size_t)a.n_slots * 1024 + 256);
+  // kSchedCluster: the other ranks' partial sums, [rank - 1][128 rows][2]
+  float *red = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&bars) +
+                                         ((sizeof(F4Bars) + 15) & ~size_t(15)));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const StreamK sk(a.n_tiles, a.n_chunks);
+  const StreamK sk(a.n_tiles, a.n_chunks, a.sched, a.ksplit);
   // B slot of chunk ch: this CTA's chunks run consecutively from ch_begin
-  const int ch_begin = (int)(sk.g_begin % sk.nch);
-  auto slot_of = [&](int st) {
-    const int ch = (int)((sk.g_begin + st) % sk.nch);
-    return (ch - ch_begin + sk.nch) % sk.nch;
-  };
+  const int ch_begin = sk.ch0;
+  auto slot_of = [&](int st) { return st % sk.nch; };
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
-    for (int q = 0; q < kMaxSlotsR; ++q) mbar_init(&bars.b_ready[q], 1);
+    mbar_init(&bars.b_ready, 1);
+    mbar_init(&bars.cl_full, a.sched == kSchedCluster ? 4 * (a.ksplit - 1) : 1);
     init_common(bars, kNSR, kIssuersR);
   }
   if (warp == 0) tmem_alloc(&bars.tmem);
@@ -783,6 +1004,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem;
+  // the cluster's barriers are initialized before any rank arrives remotely
+  if (a.sched == kSchedCluster) cluster_sync_all();
 
   if (warp == kProducerR) {
     // W only: it is never written on the stream, so no wait for the
@@ -796,32 +1019,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_w = [&](int i) {
         const int s = i % kNSR;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
-        const int64_t g = sk.g_begin + sk.stage_of(i);
-        const int64_t tile = g / sk.nch;
-        const int row0 = (int)tile * kTileRows, ch = (int)(g % sk.nch);
+        int tile, ch;
+        sk.tile_ch(sk.stage_of(i), tile, ch);
+        const int row0 = tile * kTileRows;
         mbar_arrive_expect_tx(&bars.full[s], L::TX);
         if (PREP) {
-          bulk_g2s(stg + L::W, a.wc + (tile * sk.nch + ch) * 16384, 16384u, &bars.full[s]);
-          bulk_g2s(stg + L::SFA, a.wsa + (tile * (a.K / 64) + 4 * ch) * 512, 2048u, &bars.full[s]);
+          bulk_g2s(stg + L::W, a.wc + ((int64_t)tile * sk.nch + ch) * 16384, 16384u, &bars.full[s]);
+          bulk_g2s(stg + L::SFA, a.wsa + ((int64_t)tile * (a.K / 64) + 4 * ch) * 512, 2048u,
+                   &bars.full[s]);
         } else {
           tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
           tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
         }
       };
+      // The ring alone keeps W in flight: an extra L2 prefetch at the start
+      // only lengthened the queues every later access (X, B, the fix-ups)
+      // waits in.
       const int pre = min(kNSR, sk.n_st);
       for (int i = 0; i < pre; ++i) load_w(i);
-      for (int i = pre; i < min(pre + kPrefetch, sk.n_st); ++i) {
-        const int64_t g = sk.g_begin + sk.stage_of(i);
-        const int64_t tile = g / sk.nch;
-        const int ch = (int)(g % sk.nch);
-        if (PREP) {
-          bulk_prefetch_l2(a.wc + (tile * sk.nch + ch) * 16384, 16384u);
-          bulk_prefetch_l2(a.wsa + (tile * (a.K / 64) + 4 * ch) * 512, 2048u);
-        } else {
-          tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), (int)tile * kTileRows);
-          tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), (int)tile * kTileRows);
-        }
-      }
       int i = pre;
       for (; i < sk.n_st; ++i) {
         const int s = i % kNSR;
@@ -831,120 +1046,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = (i > kNSR ? i - kNSR : 0); k < i; ++k)
         mbar_wait_bounded(&bars.full[k % kNSR], (uint32_t)((k / kNSR) & 1), a.status);
     }
-  } else if (warp >= kHelperWarp0R) {
-    // ---- warps 5..11: split this CTA's chunks of X into shared memory.
-    // Helper warp h (7 of them) takes slots h, h + 7, ...; lane 2 bb + f
-    // holds elements 8 f .. 8 f + 7 of block bb of each slot's chunk, for
-    // each row of X; a warp's slots are split together (independent chains
-    // side by side).  The prescale comes from this CTA's own blocks: partial
-    // sums leave the CTA in true units, so CTAs need not agree on it.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int hw = warp - kHelperWarp0R;  // helper warp 0..6
-    const int bb_l = lane >> 1, hf = lane & 1;
-    constexpr int kHelperWarps = kHelperThreadsR / 32;
-    constexpr int KS = (kMaxSlotsR + kHelperWarps - 1) / kHelperWarps;
-    uint4 xv[KS][2];
-    uint32_t mx[2] = {0u, 0u};
-#pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      const int qs = hw + kHelperWarps * k;
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        xv[k][m] = make_uint4(0, 0, 0, 0);
-        if (qs < a.n_slots && m < a.M) {
-          const int ch = (ch_begin + qs) % sk.nch;
-          xv[k][m] = __ldg(reinterpret_cast<const uint4 *>(a.x + m * a.ldx + (int64_t)ch * kChunkK +
-                                                           16 * bb_l + 8 * hf));
-          mx[m] = max(mx[m], absmax_bf16x8(xv[k][m]));
-        }
+  } else if (warp == kLoaderWarpR) {
+    // ---- warp 5: the zero pad after the last slot's scales, then (once the
+    // split kernel has finished) this CTA's B slots: chunks ch_begin,
+    // ch_begin + 1, ... (mod K / 256), contiguous in the workspace up to the
+    // wrap-around, so at most two copies per array.
+    if (lane < 16)
+      reinterpret_cast<uint4 *>(bsf + (size_t)a.n_slots * 1024)[lane] = make_uint4(0, 0, 0, 0);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the pad is read by tcgen05.cp
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      const int n1 = min(a.n_slots, sk.nch - ch_begin), n2 = a.n_slots - n1;
+      mbar_arrive_expect_tx(&bars.b_ready, (uint32_t)a.n_slots * 3072u);
+      bulk_g2s(bcodes, a.slot_codes + (size_t)ch_begin * 2048, (uint32_t)n1 * 2048u, &bars.b_ready);
+      bulk_g2s(bsf, a.sfb + (size_t)ch_begin * 1024, (uint32_t)n1 * 1024u, &bars.b_ready);
+      if (n2 > 0) {
+        bulk_g2s(bcodes + (size_t)n1 * 2048, a.slot_codes, (uint32_t)n2 * 2048u, &bars.b_ready);
+        bulk_g2s(bsf + (size_t)n1 * 1024, a.sfb, (uint32_t)n2 * 1024u, &bars.b_ready);
       }
+      // never leave with copies in flight
+      mbar_wait_bounded(&bars.b_ready, 0u, a.status);
     }
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      for (int o = 16; o; o >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], o));
-      if (lane == 0 && m < a.M) atomicMax(&bars.xmax[m], mx[m]);
-    }
-    named_bar(1, kHelperThreadsR);
+  } else if (warp == kRelayWarp) {
+    if (!PREP) relay_loop<kNSR, L>(smem, bars, sk, lane, a.status);
+  } else if (warp >= kEpiWarp0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the split kernel wrote sh
     int sh[kMaxRowsX] = {};
 #pragma unroll
-    for (int m = 0; m < 2; ++m) sh[m] = m < a.M ? prescale_exponent(bars.xmax[m]) : 0;
-    // clear the slots' scale atoms (rows without a component keep zero
-    // scales) and, for M = 1, the codes of operand rows 8..15
-#pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      const int qs = hw + kHelperWarps * k;
-      if (qs >= a.n_slots) break;  // warp-uniform
-      uint4 *z = reinterpret_cast<uint4 *>(bsf + qs * 1024);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) z[lane + 32 * i] = make_uint4(0, 0, 0, 0);
-      if (qs == a.n_slots - 1 && lane < 16) z[64 + lane] = make_uint4(0, 0, 0, 0);  // the pad
-      if (a.M == 1) {
-        uint4 *zc = reinterpret_cast<uint4 *>(bcodes + qs * 2048 + 1024);
-        zc[lane] = make_uint4(0, 0, 0, 0);
-        zc[lane + 32] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    __syncwarp();
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      if (m >= a.M) break;
-      const float p1 = pow2f(sh[m] / 2), p2 = pow2f(sh[m] - sh[m] / 2);
-      float r[KS][8];
-#pragma unroll
-      for (int k = 0; k < KS; ++k) {
-        const uint32_t w[4] = {xv[k][m].x, xv[k][m].y, xv[k][m].z, xv[k][m].w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          r[k][2 * t] = bf16_bits_to_f32(w[t] & 0xFFFFu) * p1 * p2;
-          r[k][2 * t + 1] = bf16_bits_to_f32(w[t] >> 16) * p1 * p2;
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < kNC; ++c) {
-        const int n = m * kNC + c;
-#pragma unroll
-        for (int k = 0; k < KS; ++k) {
-          const int qs = hw + kHelperWarps * k;
-          float m4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m4[e] = fmaxf(fabsf(r[k][e]), fabsf(r[k][e + 4]));
-          float amax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));  // the block's other half
-          // Any scale is valid -- the residual tracks what was taken -- so
-          // an approximate reciprocal stands in for the division.
-          const uint32_t sb = f32_to_e4m3_satfinite(amax * (1.0f / 6.0f) * pow2f(2 * c - 4));
-          const float d = e4m3_to_f32(sb) * pow2f(4 - 2 * c);
-          uint32_t cw = 0u;
-          if (d > 0.0f) {
-            float inv;
-            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(d));
-            float q[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) q[e] = r[k][e] * inv;
-            cw = f32x8_to_e2m1_packed(q);
-            uint32_t v[4];
-            e2m1x8_to_f16x2x4(cw, v);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {  // e2m1 * d is exact; one rounding per update
-              r[k][2 * t] = fmaf(-f16lo_to_f32(v[t]), d, r[k][2 * t]);
-              r[k][2 * t + 1] = fmaf(-f16hi_to_f32(v[t]), d, r[k][2 * t + 1]);
-            }
-          }
-          if (qs < a.n_slots) {
-            *reinterpret_cast<uint32_t *>(bcodes + qs * 2048 + n * 128 +
-                                          (((bb_l >> 1) ^ (n & 7)) << 4) + 8 * (bb_l & 1) + 4 * hf) = cw;
-            if (hf == 0) bsf[qs * 1024 + (bb_l >> 2) * 256 + 16 * n + (bb_l & 3)] = (uint8_t)sb;
-          }
-        }
-      }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
-    if (lane == 0)
-      for (int k = 0; k < KS; ++k)
-        if (hw + kHelperWarps * k < a.n_slots) mbar_arrive(&bars.b_ready[hw + kHelperWarps * k]);
-
-    if (warp >= kEpiWarp0) epilogue_loop<kIssuersR, NMMA>(a, bars, tmem, sk, warp, lane, sh);
+    for (int m = 0; m < 2; ++m)
+      if (m < a.M) sh[m] = a.sh[m];
+    epilogue_loop<kIssuersR, NMMA>(a, bars, tmem, sk, warp, lane, sh, red);
   } else if (warp < kIssuersR) {
     // ---- MMA issuers: each stage waits for its B slot
     const uint64_t dB0 = sdesc(smem_u32(bcodes), 16, 1024, kSw128);
@@ -953,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto sfb_desc = [&](int, int st, int t) {
       return dSB0 + (uint64_t)(slot_of(st) * (1024 >> 4)) + (uint64_t)(16u * t);
     };
-    auto b_wait = [&](int st) { return mbar_wait_bounded(&bars.b_ready[slot_of(st)], 0u, a.status); };
+    auto b_wait = [&](int) { return mbar_wait_bounded(&bars.b_ready, 0u, a.status); };
     issuer_loop<kIssuersR, kNSR, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
                                           sfb_desc, b_wait);
   }
@@ -965,6 +1097,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_free(tmem);
   }
+  // no rank leaves while another may still write into its shared memory
+  if (a.sched == kSchedCluster) cluster_sync_all();
 }
 
 // ---- host --------------------------------------------------------------------
@@ -974,10 +1108,12 @@ int nmma_for(int64_t M) { return M <= 2 ? 16 : M <= 4 ? 32 : M <= 8 ? 64 : 128; 
 
 struct F4Ws {
   size_t bcodes, sfb, sh, cnt, part, total;
-  int grid;
+  int grid;  // streamed kernel: CTAs of its stream-K schedule
 };
-// Workspace of one call: X's components and scale atoms
-// (streamed path), prescale exponents, per-tile counters, partial sums.
+// Workspace of one call: X's components (the streamed kernel's codes
+// [N_MMA][K/2] and atoms [K/64][512], or the resident kernel's slot images,
+// codes [K/256][2 KB] -- the same size at N_MMA = 16 -- and scales
+// [K/256][1 KB]), prescale exponents, per-tile counters, split-tile partials.
 F4Ws f4_ws(int64_t M, int64_t N, int64_t K) {
   F4Ws w;
   const int nmma = nmma_for(M);
@@ -985,9 +1121,6 @@ F4Ws f4_ws(int64_t M, int64_t N, int64_t K) {
   const int64_t chunks = n_tiles * (K / kChunkK);
   const int64_t cap = chunks < kMaxGrid ? chunks : kMaxGrid;
   w.grid = (int)(cap < num_sms() ? cap : num_sms());
-  // Not many fewer tiles than SMs: one whole tile per CTA (no split tiles,
-  // no fix-up) beats an even split.
-  if (n_tiles <= w.grid && 4 * n_tiles >= 3 * w.grid) w.grid = (int)n_tiles;
   w.bcodes = 0;
   w.sfb = (size_t)ceil_div((int64_t)nmma * (K / 2), 1024) * 1024;
   w.sh = w.sfb + (size_t)(K / 64) * 512;
@@ -1000,16 +1133,53 @@ F4Ws f4_ws(int64_t M, int64_t N, int64_t K) {
 template <int NMMA> size_t smem_s() {
   return (size_t)CfgS<NMMA>::NS * StageS<NMMA>::BYTES + sizeof(F4Bars) + 1024;
 }
-size_t smem_r(int n_slots) {
-  return (size_t)kNSR * StageR::BYTES + (size_t)n_slots * (2048 + 1024) + 256 + sizeof(F4Bars) +
-         1024;
-}
 
-// B slots the resident kernel needs: the most distinct K chunks any CTA sees.
-int slots_r(int64_t N, int64_t K, int grid) {
-  const int64_t nch = K / kChunkK, total = ceil_div(N, kTileRows) * nch;
-  const int64_t per = ceil_div(total, grid);
-  return (int)(per < nch ? per : nch);
+// The resident kernel's schedule for a shape (M <= 2):
+//  * at least 3/4 as many tiles as SMs: whole tiles, as evenly as they
+//    divide over at most one CTA per SM (no split-tile fix-ups, whose
+//    global-memory round trips are slow while HBM is saturated; with fewer
+//    tiles than SMs the SMs left over start the next kernel's weight stream
+//    early);
+//  * fewer: each tile's K split over a cluster of S = SMs / tiles CTAs
+//    (at most 8, at most one chunk each), so that most SMs stream.
+// n_slots: the most distinct K chunks a CTA sees (its B slots).
+struct F4Plan {
+  int sched, ksplit, grid, n_slots;
+  size_t smem;
+  bool ok;  // the resident kernel takes the shape
+};
+F4Plan plan_r(int64_t M, int64_t N, int64_t K) {
+  F4Plan p = {};
+  const int64_t nch = K / kChunkK, n_tiles = ceil_div(N, kTileRows), sms = num_sms();
+  p.sched = kSchedStreamK;
+  p.ksplit = 1;
+  if (4 * n_tiles >= 3 * sms) {
+    p.sched = kSchedWhole;
+    p.grid = (int)(n_tiles < sms ? n_tiles : sms);
+    p.n_slots = (int)nch;
+  } else if (n_tiles < sms) {
+    int64_t S = sms / n_tiles;
+    if (S > 8) S = 8;
+    if (S > nch) S = nch;
+    if (S >= 2 && ceil_div(nch, S) <= kMaxSlotsR) {
+      p.sched = kSchedCluster;
+      p.ksplit = (int)S;
+      p.grid = (int)(n_tiles * S);
+      p.n_slots = (int)ceil_div(nch, S);
+    }
+  }
+  if (p.sched == kSchedStreamK || p.n_slots > kMaxSlotsR) {
+    p.sched = kSchedStreamK;
+    p.ksplit = 1;
+    p.grid = f4_ws(M, N, K).grid;
+    const int64_t per = ceil_div(n_tiles * nch, p.grid);
+    p.n_slots = (int)(per < nch ? per : nch);
+  }
+  const size_t red = p.sched == kSchedCluster ? (size_t)(p.ksplit - 1) * kTileRows * 2 * sizeof(float) : 0;
+  p.smem = (size_t)kNSR * StageR::BYTES + (size_t)p.n_slots * (2048 + 1024) + 256 +
+           ((sizeof(F4Bars) + 15) & ~size_t(15)) + red + 1024;
+  p.ok = M <= 2 && p.n_slots <= kMaxSlotsR;
+  return p;
 }
 
 // Tensor maps cached per (array, shape).
@@ -1044,9 +1214,11 @@ bool cached_map(CUtensorMap &out, const void *base, uint64_t rows, uint64_t row_
   return true;
 }
 
+// Launch with programmatic dependent launch allowed, in clusters of
+// `cluster` CTAs along x (1: no cluster).
 template <class Kern, class... Args>
 cudaError_t launch_pdl(Kern kern, int grid, int threads, size_t smem, cudaStream_t stream,
-                       Args... args) {
+                       int cluster, Args... args) {
   if (smem > 48 * 1024) {
     const cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1057,11 +1229,15 @@ cudaError_t launch_pdl(Kern kern, int grid, int threads, size_t smem, cudaStream
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1107,9 +1283,9 @@ template <int NMMA>
 cudaError_t launch_streamed(bool prepared, int grid, cudaStream_t stream, const CUtensorMap &mw,
                             const CUtensorMap &ms, const CUtensorMap &mb, const F4Args &a) {
   return prepared ? launch_pdl(gemv_f4_kernel<NMMA, true>, grid, kThreads, smem_s<NMMA>(), stream,
-                               mw, ms, mb, a)
+                               1, mw, ms, mb, a)
                   : launch_pdl(gemv_f4_kernel<NMMA, false>, grid, kThreads, smem_s<NMMA>(),
-                               stream, mw, ms, mb, a);
+                               stream, 1, mw, ms, mb, a);
 }
 
 cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
@@ -1176,9 +1352,9 @@ size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 int gemv_f4_launches(int64_t M, int64_t N, int64_t K, const char **kernel) {
   if (!gemv_f4_shape_ok(M, N, K)) return 0;
-  if (M <= 2 && slots_r(N, K, f4_ws(M, N, K).grid) <= kMaxSlotsR) {
-    *kernel = "gemv_f4r_kernel";  // splits X itself
-    return 1;
+  if (plan_r(M, N, K).ok) {
+    *kernel = "gemv_f4r_kernel";  // split kernel + GEMV holding its chunks of X
+    return 2;
   }
   *kernel = "gemv_f4_kernel";  // split kernel + GEMV
   return 2;
@@ -1192,22 +1368,42 @@ cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
                            cudaStream_t stream, bool prepared) {
-  if (M <= 2) {
+  const F4Plan P = plan_r(M, N, K);
+  if (P.ok) {
     const F4Ws L = f4_ws(M, N, K);
-    const int n_slots = slots_r(N, K, L.grid);
-    if (n_slots <= kMaxSlotsR) {
-      CUtensorMap mw, ms;
-      if (!weight_maps(prepared, codes, scales, N, K, mw, ms)) return cudaErrorInvalidValue;
-      F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status,
-                           static_cast<uint8_t *>(workspace), L);
-      a.n_slots = n_slots;
-      a.wc = codes;
-      a.wsa = scales;
-      return prepared ? launch_pdl(gemv_f4r_kernel<true>, L.grid, kThreads, smem_r(n_slots), stream,
-                                   mw, ms, a)
-                      : launch_pdl(gemv_f4r_kernel<false>, L.grid, kThreads, smem_r(n_slots), stream,
-                                   mw, ms, a);
+    CUtensorMap mw, ms;
+    if (!weight_maps(prepared, codes, scales, N, K, mw, ms)) return cudaErrorInvalidValue;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status, ws, L);
+    a.n_slots = P.n_slots;
+    a.sched = P.sched;
+    a.ksplit = P.ksplit;
+    a.wc = codes;
+    a.wsa = scales;
+    a.slot_codes = ws + L.bcodes;
+    // X -> B slot images (programmatic dependent launch: may start while the
+    // previous kernel drains; it waits before reading X or writing the
+    // workspace)
+    {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)ceil_div(K / kChunkK, kSplitWarps), (unsigned)M);
+      cfg.blockDim = dim3(32 * kSplitWarps);
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, xsplit_slots_kernel, x, ldx, (int)M, K,
+                                               ws + L.bcodes, ws + L.sfb,
+                                               reinterpret_cast<int32_t *>(ws + L.sh));
+      if (e != cudaSuccess) return e;
     }
+    const int cluster = P.sched == kSchedCluster ? P.ksplit : 1;
+    return prepared ? launch_pdl(gemv_f4r_kernel<true>, P.grid, kThreads, P.smem, stream, cluster,
+                                 mw, ms, a)
+                    : launch_pdl(gemv_f4r_kernel<false>, P.grid, kThreads, P.smem, stream, cluster,
+                                 mw, ms, a);
   }
   // every row of X in one stream of W
   return launch_pass_streamed(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status,

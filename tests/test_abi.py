@@ -47,17 +47,18 @@ def test_workspace_sizes():
 
 
 def test_gemm_plan():
-    # decode: one row of X over many 128-row tiles -> FP4 tensor cores, the
-    # GEMV kernel splitting X itself; few tiles or several rows -> f16 tensor
-    # cores, one launch per pass of 1/2/4/8 rows
-    assert pkg.imp_nvfp4_gemm_plan(1, 151936, 5120) == (1, "gemv_f4r_kernel")
-    assert pkg.imp_nvfp4_gemm_plan(1, 17408, 5120) == (1, "gemv_f4r_kernel")
-    assert pkg.imp_nvfp4_gemm_plan(1, 5120, 17408) == (1, "gemv_tc_kernel")
+    # decode, one or two rows of X on an FP4-eligible shape (K % 256 == 0,
+    # K >= 1024, N >= 128) -> FP4 tensor cores: a split kernel writing X's
+    # components once, then the GEMV holding its chunks of them; more rows
+    # that one f16 pass holds -> f16 tensor cores, one launch per pass
+    assert pkg.imp_nvfp4_gemm_plan(1, 151936, 5120) == (2, "gemv_f4r_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(1, 17408, 5120) == (2, "gemv_f4r_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(1, 5120, 17408) == (2, "gemv_f4r_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(2, 5120, 17408) == (2, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(4, 17408, 5120) == (1, "gemv_tc_kernel")
     # several rows of X that one f16 pass cannot hold: FP4, split kernel + GEMV
     assert pkg.imp_nvfp4_gemm_plan(16, 17408, 5120) == (2, "gemv_f4_kernel")
     assert pkg.imp_nvfp4_gemm_plan(3, 5120, 17408) == (2, "gemv_f4_kernel")
-    assert pkg.imp_nvfp4_gemm_plan(2, 5120, 17408) == (1, "gemv_tc_kernel")
     # FP4 shape rules not met (K % 256): f16 passes
     assert pkg.imp_nvfp4_gemm_plan(16, 5120, 17344) == (8, "gemv_tc_kernel")
     assert pkg.imp_nvfp4_gemm_plan(2048, 17408, 5120) == (4, "gemm_mxf4_kernel")

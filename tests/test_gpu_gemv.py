@@ -91,7 +91,14 @@ def test_full_size_sampled(lin, via):
     # blocks, fewer row blocks than SMs, padded X rows
     (1, 512, 32, 512, 32), (1, 768, 1000, 768, 1000), (1, 1280, 4097, 1288, 4104),
     (2, 1280, 333, 1280, 336), (2, 768, 64, 776, 64), (1, 2560, 9733, 2560, 9736),
-    (2, 17408, 200, 17408, 200)])
+    (2, 17408, 200, 17408, 200),
+    # the FP4 path's schedules for one or two rows of X: whole tiles (at
+    # least 3/4 as many tiles as SMs, a ragged last tile), K split over
+    # clusters of 3 and 8 CTAs (ragged last tile, uneven chunk parts),
+    # stream-K (tiles between half and 3/4 of the SMs)
+    (1, 1024, 15355, 1024, 15360), (2, 1024, 14600, 1032, 14600),
+    (1, 3072, 6000, 3072, 6000), (2, 5120, 2431, 5120, 2432), (1, 2304, 300, 2304, 304),
+    (1, 2048, 12000, 2048, 12000), (2, 6144, 1111, 6144, 1112)])
 def test_edge_shapes(M, K, N, ldx, ldy):
     lin = synth.Linear("edge", M, K, N, 123, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
                        zero_block_p=0.02, x_outlier_frac=0.02)
