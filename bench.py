@@ -1,20 +1,26 @@
 """Benchmark of the NVFP4 linear layer on GB300.
 
-One step is one decode pass of the 27B-class workload at M = 1: the up and
-gate projections (5120 -> 17408), the down projection (17408 -> 5120) and the
-LM head (5120 -> 151936), each Y = X W^T with an NVFP4 weight resident in
-HBM.  The metric is the rate at which the step streams its algorithmic bytes
-(NVFP4 weight bytes + bf16 X and Y), in GB/s, next to the HBM roofline.  The
-weights of one step (588 MB) exceed the 129 MB L2, so every step reads them
-from HBM.
+One step is one decode pass of the 27B-class workload at M = 1, with the
+dataflow of a decode layer: the up and gate projections (5120 -> 17408) read
+the step's activation x, the down projection (17408 -> 5120) reads the gate
+projection's output, the LM head (5120 -> 151936) reads the down
+projection's output.  Each is Y = X W^T with an NVFP4 weight resident in
+HBM, in the serving form (weights laid out once for the tensor cores by
+imp_nvfp4_prepare_mma, then imp_nvfp4_gemm_mma per call).  The metric is the
+rate at which the step streams its algorithmic bytes (NVFP4 weight bytes +
+bf16 X and Y), in GB/s, next to the HBM roofline.  The weights of one step
+(588 MB) exceed the 129 MB L2, so every step reads them from HBM.
 
-Also reported (same JSON line): the prefill GEMM on the block-scaled FP4
-tensor-core path when the library provides it, the per-M skinny decode
-rates, and the quantizer.
+Also reported (same JSON line): the same step on row-major weights through
+imp_nvfp4_gemm and with unrelated inputs per projection, replayed as a CUDA
+graph, the single 1024 x 1024 linear and the 0.6B-class layer (per call and
+as a layer, weight copies rotated past L2), the per-M skinny decode rates,
+the prefill GEMMs, the quantizer, and the spread (median, min, max) of every
+rate over its repetitions.
 
-The CPU baseline is the oracle (plain single-threaded C++, fp64 matmul) timed
-on a bounded row sample of the same workload.  ``--impl reference`` times only
-that oracle, as the reference arm.
+The CPU baseline is the oracle (plain single-threaded C++: quantizer, fp64
+matmul) timed on bounded samples of every workload.  ``--impl reference``
+times only that oracle, as the reference arm.
 """
 from __future__ import annotations
 
@@ -37,11 +43,21 @@ import synth  # noqa: E402
 
 WORKLOAD = "decode_27b"
 METRIC = "NVFP4 GEMV HBM GB/s (% of GB300 peak) at M=1; prefill FP4 TFLOPS (% peak)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def call_bytes(l) -> int:
+    """Algorithmic bytes of one call: NVFP4 weight + bf16 X and Y."""
+    return l.weight_bytes + 2 * l.M * l.K + 2 * l.M * l.N
 
 
 def step_bytes(lins) -> int:
-    """Algorithmic bytes of one decode step: NVFP4 weights + bf16 X + bf16 Y."""
-    return sum(l.weight_bytes + 2 * l.M * l.K + 2 * l.M * l.N for l in lins)
+    return sum(call_bytes(l) for l in lins)
+
+
+def spread(vals):
+    """median / min / max of a list of numbers."""
+    return {"median": statistics.median(vals), "min": min(vals), "max": max(vals), "n": len(vals)}
 
 
 def load_peaks():
@@ -114,69 +130,92 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_sample(lins, budget_s: float, max_rows: int | None = None):
-    """Time the oracle's decode GEMV (dequant + fp64 matmul) on leading rows of
-    each weight of the workload.  Returns (GB/s of NVFP4 weight, seconds,
-    description).  Quantization of the sampled rows happens before the clock."""
-    import oracle
+def _cpu_jobs(max_rows: int):
+    """(label, Linear, row sample) of every configuration of the workloads:
+    configs 1 and 2 whole, config 3 and 4 on their first `max_rows` weight
+    rows, config 5 on the 64-row sample of X (rows 32 i) against its first
+    `max_rows` weight rows."""
+    jobs = []
+    for name in ("single_1k", "decode_0p6b", "decode_27b", "skinny_27b", "prefill_27b"):
+        for l in synth.workload(name):
+            jobs.append((f"{name}:{l.name}_M{l.M}", l, min(l.N, max_rows)))
+    return jobs
 
-    prepared = []
-    for l in lins:
-        rows = max_rows or max(8, min(l.N, 512))
-        wb = l.weight_bf16(0, rows)
-        _, ts, _ = oracle.tensor_scale(wb)
-        c, s = oracle.quantize_rows(wb, ts)
-        prepared.append((l, c, s, ts, l.act_bf16(), rows))
-    done_bytes, t0, calls = 0, time.perf_counter(), 0
+
+def _prep_job(l, rows):
+    import oracle
+    wb = l.weight_bf16(0, rows)
+    if l.M > 16:
+        xs = l.act_bf16()[::32][:64]  # the 64-row sample
+        return (l, wb, xs)
+    return (l, wb, l.act_bf16())
+
+
+def _run_job(job):
+    """One pass of the oracle on a job: the quantizer on the sampled weight
+    rows (tensor scale of the sample), then the matmul (for prefill, the
+    activation quantized with the whole X's scale first).  Returns bytes of
+    NVFP4 weight processed."""
+    import oracle
+    l, wb, x = job
+    _, ts, _ = oracle.tensor_scale(wb)
+    c, s = oracle.quantize_rows(wb, ts)
+    oracle.reference_gemm(x, l.M, c, s, ts)
+    return wb.shape[0] * (l.K // 2 + l.K // 16)
+
+
+def cpu_oracle_sample(budget_s: float, max_rows: int = 128):
+    """Time the oracle (quantizer + fp64 matmul, 1 thread) over every
+    configuration's sample, repeated for about `budget_s` seconds.  Returns
+    (GB/s of NVFP4 weight, seconds, description, per-config seconds)."""
+    prepared = [(label, _prep_job(l, rows)) for label, l, rows in _cpu_jobs(max_rows)]
+    per = {label: 0.0 for label, _ in prepared}
+    done, passes, t0 = 0, 0, time.perf_counter()
     while True:
-        for l, c, s, ts, x, rows in prepared:
-            oracle.reference_gemm(x, l.M, c, s, ts)
-            done_bytes += rows * (l.K // 2 + l.K // 16)
-            calls += 1
+        for label, job in prepared:
+            t1 = time.perf_counter()
+            done += _run_job(job)
+            per[label] += time.perf_counter() - t1
+        passes += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    desc = (f"oracle decode GEMV (dequant + fp64 matmul, 1 thread) on the first "
-            f"{prepared[0][5]} rows of each of {len(lins)} weights, {calls} calls")
-    return done_bytes / dt / 1e9, dt, desc
+    desc = (f"oracle quantizer + fp64 matmul (1 thread) on every configuration: configs 1-2 "
+            f"whole, configs 3-4 on the first {max_rows} weight rows, config 5 on X rows 32 i "
+            f"(i < 64) x the first {max_rows} weight rows; {passes} passes")
+    return done / dt / 1e9, dt, desc, {k: v / passes for k, v in per.items()}
 
 
-def _oracle_slice_worker(job):
-    """One process of the all-core CPU baseline: the oracle's decode GEMV on
-    its own block of rows of each weight, repeated for `budget_s` seconds.
-    Returns (bytes of NVFP4 weight processed, seconds)."""
-    name, part, rows, budget_s = job
-    import oracle
-
+def _all_core_worker(args):
+    part, max_rows, budget_s = args
     prepared = []
-    for l in synth.workload(name):
+    for label, l, rows in _cpu_jobs(max_rows):
         r0 = min(part * rows, max(0, l.N - rows))
         wb = l.weight_bf16(r0, rows)
-        _, ts, _ = oracle.tensor_scale(wb)
-        c, s = oracle.quantize_rows(wb, ts)
-        prepared.append((l, c, s, ts, l.act_bf16()))
+        x = l.act_bf16()[::32][:64] if l.M > 16 else l.act_bf16()
+        prepared.append((l, wb, x))
     done, t0 = 0, time.perf_counter()
     while True:
-        for l, c, s, ts, x in prepared:
-            oracle.reference_gemm(x, l.M, c, s, ts)
-            done += rows * (l.K // 2 + l.K // 16)
+        for job in prepared:
+            done += _run_job(job)
         if time.perf_counter() - t0 >= budget_s:
             break
     return done, time.perf_counter() - t0
 
 
-def cpu_oracle_all_cores(workload: str, budget_s: float, rows: int = 256):
-    """The oracle as N independent copies, one process per core of this
-    process's affinity mask, each on its own row block (spawned processes:
-    nothing forked after the GPU was touched).  Returns (GB/s, cores, desc)."""
+def cpu_oracle_all_cores(budget_s: float, max_rows: int = 64):
+    """The same oracle work as independent copies, one spawned process per
+    core of this process's affinity mask, each on its own weight-row block
+    (nothing is forked after the GPU was touched).  Returns (GB/s, cores,
+    description)."""
     import multiprocessing as mp
 
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     with mp.get_context("spawn").Pool(cores) as pool:
-        res = pool.map(_oracle_slice_worker, [(workload, i, rows, budget_s) for i in range(cores)])
+        res = pool.map(_all_core_worker, [(i, max_rows, budget_s) for i in range(cores)])
     gbs = sum(b / t for b, t in res) / 1e9
-    desc = (f"oracle decode GEMV (dequant + fp64 matmul), {cores} processes, each on its own "
-            f"{rows}-row block of every weight of {workload} for ~{budget_s:.0f} s")
+    desc = (f"oracle quantizer + fp64 matmul on every configuration, {cores} processes, each on "
+            f"its own {max_rows}-row block of every weight, ~{budget_s:.0f} s")
     return gbs, cores, desc
 
 
@@ -192,16 +231,17 @@ def max_over_ranks(ms: float, world: int, device) -> float:
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle alone, on this host's cores."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    lins = synth.workload(args.workload)
-    per_step = []
+    budget = max(0.5, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        cpu_oracle_sample(lins, 0.0, max_rows=64)
-    gbs_all = []
+        cpu_oracle_sample(0.0, max_rows=16)
+    gbs_all, per_step = [], []
+    desc = ""
     for _ in range(args.steps):
-        gbs, dt, desc = cpu_oracle_sample(lins, 0.0, max_rows=256)
+        gbs, dt, desc, _ = cpu_oracle_sample(budget)
         per_step.append(dt)
         gbs_all.append(gbs)
     gbs = statistics.median(gbs_all)
@@ -209,10 +249,11 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.median(per_step), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "M": 1, "shapes_KxN": [[l.K, l.N] for l in lins],
+            "config": {"workload": args.workload, "M": 1,
+                       "shapes_KxN": [[l.K, l.N] for l in synth.workload(args.workload)],
                        "l2": "inputs larger than L2"},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "spread": spread(gbs_all)},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -220,6 +261,55 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- GPU arm
+
+def chain_inputs(lins, xs, ys):
+    """The X each problem of a decode pass reads, in a decode layer's
+    dataflow: gate reads up's x, down reads gate's output, the LM head reads
+    down's output (when those problems are in the list and the widths
+    match); every other problem reads its own synthetic X."""
+    by = {l.name: i for i, l in enumerate(lins)}
+    out = list(xs)
+    for dst, src, kind in (("gate", "up", "x"), ("down", "gate", "y"), ("lm_head", "down", "y")):
+        if dst in by and src in by:
+            i, j = by[dst], by[src]
+            width = lins[j].K if kind == "x" else lins[j].N
+            if width == lins[i].K and lins[i].M == lins[j].M:
+                out[i] = out[j] if kind == "x" else ys[j]
+    return out
+
+
+def layer_inputs_0p6b(lins, xs, ys):
+    """The 0.6B-class layer's dataflow: q, k, v, gate and up read x; o reads
+    q's output; down reads gate's output."""
+    by = {l.name: i for i, l in enumerate(lins)}
+    out = list(xs)
+    for name in ("k", "v", "gate", "up"):
+        out[by[name]] = xs[by["q"]]
+    out[by["o"]] = ys[by["q"]]
+    out[by["down"]] = ys[by["gate"]]
+    return out
+
+
+def event_pair():
+    import torch
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def time_blocks(fn, n_per_block, blocks, stream):
+    """Per-call µs of `blocks` blocks of `n_per_block` back-to-back calls."""
+    import torch
+    out = []
+    for _ in range(blocks):
+        e0, e1 = event_pair()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n_per_block):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(1e3 * e0.elapsed_time(e1) / n_per_block)
+    return out
+
 
 def run_native(args):
     import torch
@@ -235,63 +325,32 @@ def run_native(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkg.load()
+    hbm_peak, _, peak_kind = load_peaks()
 
-    # ---- inputs resident in HBM (weights quantized on device; not timed)
+    # ---- inputs resident in HBM (weights quantized and laid out on device; not timed)
     lins = synth.workload(args.workload)
-    weights, xs, ys = [], [], []
+    rows_w, weights, xs, ys = [], [], [], []
     for l in lins:
         wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
-        weights.append(pkg.quantize(wb))
+        w = pkg.quantize(wb)
         del wb
+        rows_w.append(w)
+        weights.append(pkg.prepare_mma(w))
         xs.append(torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev))
         ys.append(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev))
-    # X and Y of all problems as views into one buffer each, so a step's
-    # inputs arrive with one host-to-device copy and its results leave with
-    # one device-to-host copy (offsets stay 16-byte aligned: K, N % 8 == 0)
-    xcat = torch.empty(sum(x.numel() for x in xs), dtype=torch.bfloat16, device=dev)
-    ycat = torch.empty(sum(y.numel() for y in ys), dtype=torch.bfloat16, device=dev)
-    ox = oy = 0
-    for i, l in enumerate(lins):
-        v = xcat[ox:ox + l.M * l.K].view(l.M, l.K)
-        v.copy_(xs[i])
-        xs[i] = v
-        ys[i] = ycat[oy:oy + l.M * l.N].view(l.M, l.N)
-        ox += l.M * l.K
-        oy += l.M * l.N
+    chained = chain_inputs(lins, xs, ys)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    # one workspace per problem, allocated once (the FP4 decode path's split X,
-    # partial sums and counters)
+    # one workspace per problem, allocated once (the FP4 decode path's split
+    # X, partial sums and counters)
     wss = [torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), 16),
                        dtype=torch.uint8, device=dev) for l in lins]
     plans = [pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K) for l in lins]
     torch.cuda.synchronize()
 
     def step():
-        for x, w, y, ws in zip(xs, weights, ys, wss):
-            pkg.gemm(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
-
-    # per-kernel timing events (on the launching stream)
-    def timed_steps(k, per_kernel):
-        evs = []
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(k):
-            if per_kernel:
-                row = []
-                for x, w, y, ws in zip(xs, weights, ys, wss):
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    pkg.gemm(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
-                    e1.record(stream)
-                    row.append((e0, e1))
-                evs.append(row)
-            else:
-                step()
-        end.record(stream)
-        return start, end, evs
+        for x, w, y, ws in zip(chained, weights, ys, wss):
+            pkg.gemm_mma(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -299,136 +358,85 @@ def run_native(args):
     if world > 1:
         dist.barrier()
 
+    bytes_step = step_bytes(lins)
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
-        start, end, _ = timed_steps(args.steps, per_kernel=False)
+        e0, e1 = event_pair()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
         torch.cuda.synchronize()
-        elapsed_ms = start.elapsed_time(end)
-        # second pass with per-kernel events (for the roofline of the top kernel)
-        _, _, evs = timed_steps(args.steps, per_kernel=True)
-        torch.cuda.synchronize()
+        elapsed_ms = e0.elapsed_time(e1)
+        # spread: ten more blocks of max(steps, 50) steps
+        blocks = time_blocks(step, max(args.steps, 50), 10, stream)
+        # the dominant call timed on its own (events around each call) >= 50 times,
+        # on the stream it is launched on
+        top = int(np.argmax([l.weight_bytes for l in lins]))
+        per_call = {}
+        for i, l in enumerate(lins):
+            ts = []
+            for _ in range(max(50, args.steps // 4)):
+                a, b = event_pair()
+                a.record(stream)
+                pkg.gemm_mma(chained[i], weights[i], y=ys[i], dev_status=status, stream=stream,
+                             workspace=wss[i])
+                b.record(stream)
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            per_call[l.name] = [1e3 * a.elapsed_time(b) for a, b in ts]
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     if world > 1:
         dist.barrier()
     st = int(status.item())
     if st != 0:
         raise RuntimeError(f"device status {st} during the benchmark")
-
-    per_kernel_ms = [statistics.mean(row[i][0].elapsed_time(row[i][1]) for row in evs)
-                     for i in range(len(lins))]
-    bytes_step = step_bytes(lins)
     ms_per_step = elapsed_ms / args.steps
     value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
 
-    # ---- e2e through the public API with host buffers
-    pin_x = torch.empty(xcat.shape, dtype=torch.bfloat16, pin_memory=True).copy_(xcat)
-    pin_y = torch.empty(ycat.shape, dtype=torch.bfloat16, pin_memory=True)
-    h2d = pin_x.numel() * 2
-    d2h = pin_y.numel() * 2
+    # ---- e2e through the public API: x copied in from pinned host memory and
+    # the logits (the step's result) copied back, every step
+    x0 = chained[0]
+    pin_x = torch.empty(x0.shape, dtype=torch.bfloat16, pin_memory=True).copy_(x0)
+    y_last = ys[-1]
+    pin_y = torch.empty(y_last.shape, dtype=torch.bfloat16, pin_memory=True)
 
     def e2e_step():
-        xcat.copy_(pin_x, non_blocking=True)
-        for x, w, y, ws in zip(xs, weights, ys, wss):
-            pkg.gemm(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
-        pin_y.copy_(ycat, non_blocking=True)
+        x0.copy_(pin_x, non_blocking=True)
+        step()
+        pin_y.copy_(y_last, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    a, b = event_pair()
+    a.record(stream)
     for _ in range(args.steps):
         e2e_step()
-    e1.record(stream)
+    b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, dev)
     e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
 
-    hbm_peak, _, peak_kind = load_peaks()
-    top = int(np.argmax(per_kernel_ms))
-    top_bytes = lins[top].weight_bytes + 2 * lins[top].K + 2 * lins[top].N
-    achieved = top_bytes / (per_kernel_ms[top] * 1e-3) / 1e9
+    # ---- roofline of the dominant kernel: its call's bytes over the median
+    # duration of the call timed alone (the call is the X split kernel + the
+    # GEMV), and the same call launched back to back
+    lt = lins[top]
+    top_us = statistics.median(per_call[lt.name])
+    achieved = call_bytes(lt) / (top_us * 1e-6) / 1e9
     top_kernel = plans[top][1]
-    traffic = load_traffic(top_kernel, lins[top])
-    # The same kernel launched back to back (its weight alone exceeds L2, so
-    # every launch reads it from HBM): the launch interval once start-up
-    # overlaps the previous launch, next to the isolated duration above.
-    xt, wt, yt, wst = xs[top], weights[top], ys[top], wss[top]
-    for _ in range(3):
-        pkg.gemm(xt, wt, y=yt, dev_status=status, stream=stream, workspace=wst)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    reps = 20
-    e0.record(stream)
-    for _ in range(reps):
-        pkg.gemm(xt, wt, y=yt, dev_status=status, stream=stream, workspace=wst)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    b2b_ms = e0.elapsed_time(e1) / reps
-    b2b_gbs = top_bytes / (b2b_ms * 1e-3) / 1e9
+    traffic = load_traffic(top_kernel, lt)
+    b2b = time_blocks(lambda: pkg.gemm_mma(chained[top], weights[top], y=ys[top],
+                                           dev_status=status, stream=stream,
+                                           workspace=wss[top]), 20, 5, stream)
+    b2b_us = statistics.median(b2b)
 
     extra = {}
     if rank == 0 and not args.no_extra:
-        extra = bench_extras(args, pkg, dev, stream, hbm_peak)
-        # the same step replayed as one CUDA graph (the decode launches of a
-        # step captured once; programmatic dependent launch edges kept)
-        try:
-            cap = torch.cuda.Stream(dev)
-            cap.wait_stream(stream)
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=cap):
-                for x, w, y, ws in zip(xs, weights, ys, wss):
-                    pkg.gemm(x, w, y=y, dev_status=status, stream=cap, workspace=ws)
-            torch.cuda.synchronize()
-            for _ in range(args.warmup):
-                graph.replay()
-            torch.cuda.synchronize()
-            g0 = torch.cuda.Event(enable_timing=True)
-            g1 = torch.cuda.Event(enable_timing=True)
-            gstream = torch.cuda.current_stream(dev)
-            g0.record(gstream)
-            for _ in range(args.steps):
-                graph.replay()
-            g1.record(gstream)
-            torch.cuda.synchronize()
-            gms = g0.elapsed_time(g1) / args.steps
-            if int(status.item()) != 0:
-                raise RuntimeError(f"device status {int(status.item())} in the graph replay")
-            extra["decode_graph_replay"] = {
-                "ms_per_step": gms, "GB/s": bytes_step / (gms * 1e-3) / 1e9,
-                "frac_of_hbm_peak": bytes_step / (gms * 1e-3) / 1e9 / hbm_peak}
-            del graph
-        except Exception as e:  # report, do not fail the benchmark line
-            extra["decode_graph_replay"] = {"error": str(e)[:200]}
-        # the same step on weights prepared once in the MMA layout (contiguous
-        # 16 KB code tiles, scale atoms) through imp_nvfp4_gemm_mma
-        prepared = [pkg.prepare_mma(w, stream=stream) for w in weights]
-        pws = [torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), 16),
-                           dtype=torch.uint8, device=dev) for l in lins]
-
-        def prepared_step():
-            for x, w, y, ws in zip(xs, prepared, ys, pws):
-                pkg.gemm_mma(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
-
-        for _ in range(args.warmup):
-            prepared_step()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            prepared_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        pms = e0.elapsed_time(e1) / args.steps
-        extra["decode_prepared_mma_layout"] = {
-            "ms_per_step": pms, "GB/s": bytes_step / (pms * 1e-3) / 1e9,
-            "frac_of_hbm_peak": bytes_step / (pms * 1e-3) / 1e9 / hbm_peak}
-        del prepared, pws
-        if int(status.item()) != 0:
-            raise RuntimeError(f"device status {int(status.item())} in the prepared step")
+        extra = bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs,
+                             chained, ys, wss, status, step)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the extra measurements")
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -436,32 +444,40 @@ def run_native(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 weights, bf16 x/y, f32 accumulate",
         "data": "synthetic",
         "config": {"workload": args.workload, "M": 1, "shapes_KxN": [[l.K, l.N] for l in lins],
-                   "bytes_per_step": bytes_step, "l2": "inputs larger than L2 (588 MB per step)",
+                   "bytes_per_step": bytes_step,
+                   "dataflow": "decode layer: up and gate read x, down reads gate's output, "
+                               "the LM head reads down's output",
+                   "weights": "serving form (imp_nvfp4_prepare_mma once, imp_nvfp4_gemm_mma "
+                              "per call)",
+                   "l2": "inputs larger than L2 (588 MB of weights per step)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_hbm_peak": value / world / hbm_peak,
-        "per_kernel_us": {l.name: 1e3 * t for l, t in zip(lins, per_kernel_ms)},
-        "per_kernel_gbs": {l.name: (l.weight_bytes + 2 * l.K + 2 * l.N) / (t * 1e-3) / 1e9
-                           for l, t in zip(lins, per_kernel_ms)},
-        "roofline": {"bound": "hbm", "kernel": f"{top_kernel} ({lins[top].name} "
-                     f"{lins[top].K}x{lins[top].N})", "achieved": achieved, "peak": hbm_peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "traffic": traffic,
-                     "back_to_back": {"us_per_launch": 1e3 * b2b_ms, "achieved": b2b_gbs,
-                                      "frac": b2b_gbs / hbm_peak}},
+        "spread_us_per_step": spread(blocks),
+        "per_call_us": {l.name: spread(per_call[l.name]) for l in lins},
+        "per_call_gbs": {l.name: call_bytes(l) / (statistics.median(per_call[l.name]) * 1e-6) / 1e9
+                         for l in lins},
+        "roofline": {"bound": "hbm", "kernel": f"{top_kernel} ({lt.name} {lt.K}x{lt.N})",
+                     "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "bytes_per_launch": call_bytes(lt),
+                     "back_to_back": {"us_per_launch": b2b_us,
+                                      "achieved": call_bytes(lt) / (b2b_us * 1e-6) / 1e9,
+                                      "frac": call_bytes(lt) / (b2b_us * 1e-6) / 1e9 / hbm_peak}},
         "gpu_launches": args.steps * sum(n for n, _ in plans),
         "kernels": {l.name: {"kernel": k, "launches_per_call": n} for l, (n, k) in zip(lins, plans)},
         "clocks": clocks.summary(),
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": pin_x.numel() * 2,
+                "d2h_bytes_per_step": pin_y.numel() * 2},
     }
     line.update(extra)
     if rank == 0 and not args.no_cpu_baseline:
-        gbs, dt, desc = cpu_oracle_sample(lins, args.cpu_seconds)
+        gbs, dt, desc, per = cpu_oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+                                "sample": desc, "seconds": dt,
+                                "per_config_ms": {k: 1e3 * v for k, v in per.items()}}
         if world == 1:
             try:
-                gbs, cores, desc = cpu_oracle_all_cores(args.workload, args.cpu_seconds)
+                gbs, cores, desc = cpu_oracle_all_cores(args.cpu_seconds)
                 line["cpu_baseline_all_cores"] = {"value": gbs, "unit": "GB/s", "cores": cores,
                                                   "kind": "oracle", "sample": desc}
             except Exception as e:  # report, do not lose the benchmark line
@@ -492,10 +508,108 @@ def fp4_peak_tflops():
     return bf16 * (13.5 / 2.25), kind
 
 
+def rotated_copies(pkg, w, copies):
+    """`copies` device copies of a weight (the first is `w`)."""
+    return [w] + [pkg.NVFP4Tensor(w.codes.clone(), w.scales.clone(), w.tensor_scale.clone(),
+                                  layout=w.layout, shape=(w.rows, w.K)) for _ in range(copies - 1)]
+
+
+def bench_small_configs(pkg, dev, stream, hbm_peak, status):
+    """Configs 1 and 2 (launch-bound shapes): per call and, for the 0.6B-class
+    layer, as the seven calls of one layer in its dataflow -- eagerly and
+    replayed as a CUDA graph.  Weights rotate over enough copies to exceed
+    three times the L2, so every call reads its weight from HBM."""
+    import torch
+
+    out = {}
+    for name in ("single_1k", "decode_0p6b"):
+        lins = synth.workload(name)
+        base = []
+        for l in lins:
+            wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+            base.append(pkg.prepare_mma(pkg.quantize(wb)))
+            del wb
+        layer_bytes = step_bytes(lins)
+        ncopy = -(-3 * L2_BYTES // layer_bytes) + 1
+        copies = [rotated_copies(pkg, w, ncopy) for w in base]  # [problem][copy]
+        xs = [torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+              for l in lins]
+        ys = [torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev) for l in lins]
+        wss = [torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), 16),
+                           dtype=torch.uint8, device=dev) for l in lins]
+        ins = layer_inputs_0p6b(lins, xs, ys) if name == "decode_0p6b" else xs
+        res = {"weight_copies": ncopy, "calls": {}}
+        for i, l in enumerate(lins):
+            k = [0]
+
+            def one(i=i, k=k):
+                pkg.gemm_mma(ins[i], copies[i][k[0] % ncopy], y=ys[i], dev_status=status,
+                             stream=stream, workspace=wss[i])
+                k[0] += 1
+            for _ in range(ncopy):
+                one()
+            ts = time_blocks(one, ncopy, 10, stream)
+            med = statistics.median(ts)
+            res["calls"][f"{l.name}_{l.K}x{l.N}"] = {
+                "us": spread(ts), "GB/s": call_bytes(l) / (med * 1e-6) / 1e9,
+                "frac_of_hbm_peak": call_bytes(l) / (med * 1e-6) / 1e9 / hbm_peak,
+                "kernel": pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K)[1]}
+        if len(lins) > 1:
+            k = [0]
+
+            def layer(k=k):
+                c = k[0] % ncopy
+                for i in range(len(lins)):
+                    pkg.gemm_mma(ins[i], copies[i][c], y=ys[i], dev_status=status,
+                                 stream=stream, workspace=wss[i])
+                k[0] += 1
+            for _ in range(ncopy):
+                layer()
+            ts = time_blocks(layer, ncopy, 10, stream)
+            med = statistics.median(ts)
+            res["layer_eager"] = {"us": spread(ts), "GB/s": layer_bytes / (med * 1e-6) / 1e9,
+                                  "sum_of_calls_us": sum(v["us"]["median"]
+                                                         for v in res["calls"].values())}
+            # the layer captured once per weight copy and replayed
+            try:
+                cap = torch.cuda.Stream(dev)
+                cap.wait_stream(stream)
+                graphs = []
+                for c in range(ncopy):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=cap):
+                        for i in range(len(lins)):
+                            pkg.gemm_mma(ins[i], copies[i][c], y=ys[i], dev_status=status,
+                                         stream=cap, workspace=wss[i])
+                    graphs.append(g)
+                torch.cuda.synchronize()
+                gs = torch.cuda.current_stream(dev)
+                for g in graphs:
+                    g.replay()
+                ts = []
+                for _ in range(10):
+                    a, b = event_pair()
+                    torch.cuda.synchronize()
+                    a.record(gs)
+                    for g in graphs:
+                        g.replay()
+                    b.record(gs)
+                    torch.cuda.synchronize()
+                    ts.append(1e3 * a.elapsed_time(b) / ncopy)
+                med = statistics.median(ts)
+                res["layer_graph"] = {"us": spread(ts), "GB/s": layer_bytes / (med * 1e-6) / 1e9}
+                del graphs
+            except Exception as e:  # report, do not fail the line
+                res["layer_graph"] = {"error": str(e)[:200]}
+        out[name] = res
+        del copies, base
+    return out
+
+
 def bench_prefill(args, pkg, dev, stream):
     """Prefill GEMMs (M = 2048): the block-scaled FP4 tensor-core GEMM alone
-    (X already quantized, W scales in the atom layout) and the whole
-    imp_nvfp4_gemm call (X quantization + W scale layout + GEMM)."""
+    (X already quantized, W in the MMA layout) and the whole imp_nvfp4_gemm
+    call (X quantization + GEMM)."""
     import torch
 
     peak, kind = fp4_peak_tflops()
@@ -518,104 +632,128 @@ def bench_prefill(args, pkg, dev, stream):
                          ("gemm_fp4_stream_k", lambda: pkg.gemm_fp4(xq, wm, y=y, stream=stream,
                                                                     workspace=wsf,
                                                                     stream_k=True)),
-                         ("imp_nvfp4_gemm", lambda: pkg.gemm(x, w, y=y, stream=stream,
-                                                             workspace=ws))):
+                         ("imp_nvfp4_gemm_mma", lambda: pkg.gemm_mma(x, wm, y=y, stream=stream,
+                                                                     workspace=ws))):
             for _ in range(args.warmup):
                 fn()
-            torch.cuda.synchronize()
-            reps = 20
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                fn()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            t = e0.elapsed_time(e1) / reps
-            tf = flops / (t * 1e-3) / 1e12
-            out[name] = {"us": 1e3 * t, "TFLOP/s": tf, "frac_of_fp4_peak": tf / peak}
+            ts = time_blocks(fn, 10, 6, stream)
+            t = statistics.median(ts)
+            tf = flops / (t * 1e-6) / 1e12
+            out[name] = {"us": spread(ts), "TFLOP/s": tf, "frac_of_fp4_peak": tf / peak}
         res[f"M{l.M}_{l.K}x{l.N}"] = out
-        del w, wm, x, xq, y, ws
+        del w, wm, x, xq, y, ws, wsf
     res["fp4_peak_tflops"] = peak
     res["fp4_peak_kind"] = f"{kind} bf16 x 6 (nominal fp4:bf16 ratio)"
     return res
 
 
-def bench_extras(args, pkg, dev, stream, hbm_peak):
-    """Prefill GEMMs, skinny-M decode rates (M = 2..16) and the quantizer rate."""
+def bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs, chained, ys, wss,
+                 status, step):
+    """Variants of the step, configs 1 and 2, skinny M, prefill, quantizer."""
     import torch
 
-    out = {"prefill": bench_prefill(args, pkg, dev, stream)}
+    bytes_step = step_bytes(lins)
+
+    def rate(ts):
+        med = statistics.median(ts)
+        return {"us_per_step": spread(ts), "GB/s": bytes_step / (med * 1e-6) / 1e9,
+                "frac_of_hbm_peak": bytes_step / (med * 1e-6) / 1e9 / hbm_peak}
+
+    out = {}
+    n = max(args.steps, 50)
+
+    # the step on row-major weights (no layout transform) through imp_nvfp4_gemm
+    def rows_step():
+        for x, w, y, ws in zip(chained, rows_w, ys, wss):
+            pkg.gemm(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
+    for _ in range(args.warmup):
+        rows_step()
+    out["decode_row_major_weights"] = rate(time_blocks(rows_step, n, 10, stream))
+
+    # the step with an unrelated synthetic X per projection (no dataflow: every
+    # X is read from HBM, not from the previous call's output in L2)
+    def indep_step():
+        for x, w, y, ws in zip(xs, weights, ys, wss):
+            pkg.gemm_mma(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
+    for _ in range(args.warmup):
+        indep_step()
+    out["decode_independent_inputs"] = rate(time_blocks(indep_step, n, 10, stream))
+
+    # the step replayed as one CUDA graph (programmatic dependent launch kept)
+    try:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for x, w, y, ws in zip(chained, weights, ys, wss):
+                pkg.gemm_mma(x, w, y=y, dev_status=status, stream=cap, workspace=ws)
+        torch.cuda.synchronize()
+        gs = torch.cuda.current_stream(dev)
+        for _ in range(args.warmup):
+            graph.replay()
+        out["decode_graph_replay"] = rate(time_blocks(graph.replay, n, 10, gs))
+        del graph
+    except Exception as e:  # report, do not fail the benchmark line
+        out["decode_graph_replay"] = {"error": str(e)[:200]}
+
+    out["small_configs"] = bench_small_configs(pkg, dev, stream, hbm_peak, status)
+    out["prefill"] = bench_prefill(args, pkg, dev, stream)
+
     # Skinny M: back-to-back calls cycling through copies of W whose total
-    # exceeds L2 twice over, so each call reads its weight from HBM (no flush
-    # kernel between calls, which would idle the GPU and hide start-up cost).
-    lins = synth.workload("skinny_27b")
+    # exceeds L2 twice over, so each call reads its weight from HBM.
     skinny = {}
     cache = {}
-    l2 = 129 * 1024 * 1024
-    for l in lins:
+    for l in synth.workload("skinny_27b"):
         key = (l.K, l.N)
         if key not in cache:
             wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
             w0 = pkg.quantize(wb)
             del wb
-            copies = max(2, -(-2 * l2 // l.weight_bytes))
-            cache[key] = [w0] + [pkg.NVFP4Tensor(w0.codes.clone(), w0.scales.clone(),
-                                                 w0.tensor_scale.clone())
-                                 for _ in range(copies - 1)]
-        ws_list = cache[key]
+            cache[key] = rotated_copies(pkg, pkg.prepare_mma(w0), max(2, -(-2 * L2_BYTES // l.weight_bytes)))
+            del w0
+        wl = cache[key]
         x = torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
         y = torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), 16),
                          dtype=torch.uint8, device=dev)
-        for _ in range(args.warmup):
-            for w in ws_list:
-                pkg.gemm(x, w, y=y, stream=stream, workspace=ws)
-        rounds = 10
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(rounds):
-            for w in ws_list:
-                pkg.gemm(x, w, y=y, stream=stream, workspace=ws)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        t = e0.elapsed_time(e1) / (rounds * len(ws_list))
-        b = l.weight_bytes + 2 * l.M * l.K + 2 * l.M * l.N
-        n, k = pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K)
-        skinny[f"M{l.M}_{l.K}x{l.N}"] = {"us": 1e3 * t, "GB/s": b / (t * 1e-3) / 1e9,
-                                         "TFLOP/s": 2 * l.M * l.N * l.K / (t * 1e-3) / 1e12,
-                                         "kernel": k, "launches": n}
+        k = [0]
+
+        def one(k=k, wl=wl, x=x, y=y, ws=ws):
+            pkg.gemm_mma(x, wl[k[0] % len(wl)], y=y, dev_status=status, stream=stream,
+                         workspace=ws)
+            k[0] += 1
+        for _ in range(len(wl) * 2):
+            one()
+        ts = time_blocks(one, len(wl) * 5, 10, stream)
+        t = statistics.median(ts)
+        nk, kern = pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K)
+        skinny[f"M{l.M}_{l.K}x{l.N}"] = {"us": spread(ts), "GB/s": call_bytes(l) / (t * 1e-6) / 1e9,
+                                         "frac_of_hbm_peak": call_bytes(l) / (t * 1e-6) / 1e9 / hbm_peak,
+                                         "TFLOP/s": 2 * l.M * l.N * l.K / (t * 1e-6) / 1e12,
+                                         "kernel": kern, "launches": nk}
     out["skinny_decode"] = skinny
     del cache
-    # quantizer: the LM-head-sized weight
-    l = synth.workload("decode_27b")[3]
+
+    # quantizer: the LM-head-sized weight (two reads of X + codes and scales written)
+    l = lins[-1]
     wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
     q = pkg.quantize(wb)
-    times = []
-    for i in range(args.warmup + 5):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+    for _ in range(args.warmup):
         pkg.quantize(wb, out=q, stream=stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            times.append(e0.elapsed_time(e1))
-    t = statistics.median(times)
-    qb = 2 * 2 * l.N * l.K + l.N * l.K // 2 + l.N * l.K // 16  # two reads of X + writes
-    out["quantizer"] = {"shape": [l.N, l.K], "us": 1e3 * t, "GB/s": qb / (t * 1e-3) / 1e9,
-                        "frac_of_hbm_peak": qb / (t * 1e-3) / 1e9 / hbm_peak}
+    ts = time_blocks(lambda: pkg.quantize(wb, out=q, stream=stream), 1, 20, stream)
+    t = statistics.median(ts)
+    qb = 2 * 2 * l.N * l.K + l.N * l.K // 2 + l.N * l.K // 16
+    out["quantizer"] = {"shape": [l.N, l.K], "us": spread(ts), "GB/s": qb / (t * 1e-6) / 1e9,
+                        "frac_of_hbm_peak": qb / (t * 1e-6) / 1e9 / hbm_peak}
+    del wb, q
     return out
 
 
 def run_prefill_workload(args):
     """--workload prefill_27b: one step = the two prefill GEMMs (M = 2048) on
-    the block-scaled FP4 tensor cores, X already quantized and W's scales in
-    the atom layout; metric TFLOP/s.  e2e = imp_nvfp4_gemm from bf16 X copied
-    from pinned host memory (quantization + W scale layout + GEMM) with Y
-    copied back."""
+    the block-scaled FP4 tensor cores, X already quantized and W in the MMA
+    layout; metric TFLOP/s.  e2e = imp_nvfp4_gemm_mma from bf16 X copied from
+    pinned host memory (X quantization + GEMM) with Y copied back."""
     import torch
 
     import nvfp4_weight_quantized_02_gb300 as pkg
@@ -633,11 +771,11 @@ def run_prefill_workload(args):
         w = pkg.quantize(wb)
         del wb
         x = torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
-        items.append(dict(l=l, w=w, wm=pkg.prepare_mma(w), x=x, xq=pkg.quantize_mma(x),
+        items.append(dict(l=l, wm=pkg.prepare_mma(w), x=x, xq=pkg.quantize_mma(x),
                           y=torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev),
                           ws=torch.empty(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K),
-                                         dtype=torch.uint8, device=dev),
-                          ))
+                                         dtype=torch.uint8, device=dev)))
+        del w
     flops = sum(2.0 * it["l"].M * it["l"].N * it["l"].K for it in items)
 
     def step():
@@ -648,13 +786,13 @@ def run_prefill_workload(args):
         step()
     torch.cuda.synchronize()
     with ClockSampler(0) as clocks:
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+        e0, e1 = event_pair()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        blocks = time_blocks(step, max(args.steps, 10), 10, stream)
     ms = e0.elapsed_time(e1) / args.steps
     peak, kind = fp4_peak_tflops()
     value = flops / (ms * 1e-3) / 1e12
@@ -665,7 +803,7 @@ def run_prefill_workload(args):
     def e2e_step():
         for px, py, it in zip(pin_x, pin_y, items):
             it["x"].copy_(px, non_blocking=True)
-            pkg.gemm(it["x"], it["w"], y=it["y"], stream=stream, workspace=it["ws"])
+            pkg.gemm_mma(it["x"], it["wm"], y=it["y"], stream=stream, workspace=it["ws"])
             py.copy_(it["y"], non_blocking=True)
 
     for _ in range(args.warmup):
@@ -677,19 +815,22 @@ def run_prefill_workload(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    n_launch = sum(pkg.imp_nvfp4_gemm_plan(it["l"].M, it["l"].N, it["l"].K)[0] for it in items)
     line = {"metric": "prefill FP4 TFLOPS (block-scaled tcgen05 GEMM, M=2048)", "value": value,
             "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "nvfp4 x nvfp4, f32 accumulate, bf16 out", "data": "synthetic",
             "config": {"workload": args.workload,
                        "shapes_MxKxN": [[it["l"].M, it["l"].K, it["l"].N] for it in items]},
+            "spread_ms_per_step": spread([b / 1e3 for b in blocks]),
             "roofline": {"bound": "tensor", "kernel": "gemm_mxf4_kernel", "achieved": value,
                          "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
                          "frac": value / peak, "traffic": None},
             "gpu_launches": args.steps * len(items), "clocks": clocks.summary(),
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": sum(p.numel() * 2 for p in pin_x),
-                    "d2h_bytes_per_step": sum(p.numel() * 2 for p in pin_y)}}
+                    "d2h_bytes_per_step": sum(p.numel() * 2 for p in pin_y),
+                    "gpu_launches_per_step": n_launch}}
     print(json.dumps(line))
     return 0
 

@@ -52,7 +52,7 @@ constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;    // 4 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t OFF_B = A_BYTES, OFF_SFA = A_BYTES + B_BYTES, OFF_SFB = OFF_SFA + SFA_BYTES;
 // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue, warps 10..12 scale copies
-constexpr int kScaleWarp0 = 10, kScaleWarps = 3;
+constexpr int kScaleWarp0 = 10, kScaleWarps = 4;  // one per tensor-memory lane quarter
 constexpr int kThreads = 32 * (kScaleWarp0 + kScaleWarps);
 constexpr int kEpiThreads = 256;
 constexpr int kEpiCols = 128;  // accumulator columns per epilogue warp
@@ -186,6 +186,14 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Four consecutive tensor-memory columns of this warp's 32 lanes (one 32-bit
+// value per lane and column).
+__device__ __forceinline__ void tc_st4(uint32_t taddr, uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -362,58 +370,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= kScaleWarp0) {
-    // ------------------------------ scale copies
-    // tcgen05.cp costs the issuing thread about as much as an MMA, so the
-    // twelve copies of a stage come from three warps, ahead of the MMA warp:
-    // per 64-element K step, warp 10 copies the X-row scales, warps 11 and
-    // 12 the two 128-row halves of the W tile, into the stage's own bank of
-    // 48 columns; the stage's barrier completes once all three committed.
-    // The bank is free again once the stage's MMAs completed, which the
-    // producer waited for before refilling the stage.
-    if (lane == 0) {
-      const int part = warp - kScaleWarp0;  // 0: X scales, 1, 2: W halves
-      const uint64_t d0 = part == 0 ? smem_desc(smem_u32(smem + OFF_SFA), 0, 128, kLayoutNone)
-                                    : smem_desc(smem_u32(smem + OFF_SFB + 2048 * (part - 1)), 0,
-                                                128, kLayoutNone);
-      const uint32_t col = 4u * (uint32_t)part;
-      uint32_t s = 0, phase = 0;
-      int64_t issued = 0;
-      bool ok = true;
-      for (int jj = 0; ok && jj < sch.n_seg; ++jj) {
-        int t, k0, k1;
-        sch.seg(jj, t, k0, k1);
-        for (int ks = k0; ks < k1; ++ks) {
-          // no shared-memory flag is read here either (see the MMA loop)
-          if (!mbar_wait_bounded(&full[s], phase, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t d = d0 + (uint64_t)(s * (STAGE_BYTES >> 4));
-          const uint32_t sf0 = tmem + TMEM_SF + 48u * s + col;
-          const int nk = (ks + 1 < n_ks || a.K % BK == 0) ? KSTEPS : (a.K - ks * BK) / MMA_K;
-          if (nk == KSTEPS) {
+    // ------------------------------ block scales -> tensor memory
+    // Warp w fills the scale columns of its tensor-memory lane quarter
+    // q = w % 4 (lanes 32 q .. 32 q + 31) with tcgen05.st: for K step t and
+    // operand block g (0: the X rows; 1, 2: W rows 0..127, 128..255) the
+    // 4-column group the MMA reads gets, in lane 32 q + i, the 16-byte line i
+    // of that block's scale atom -- what a tcgen05.cp 32x128b.warpx4 of the
+    // atom writes, without occupying the tensor pipe, which then runs MMAs
+    // only.  The bank of stage s is free once the stage's previous MMAs
+    // completed, which the producer waited for before refilling the stage.
+    const int q = warp & 3;
+    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + TMEM_SF;
+    uint32_t s = 0, phase = 0;
+    bool ok = true;
+    for (int jj = 0; ok && jj < sch.n_seg; ++jj) {
+      int t, k0, k1;
+      sch.seg(jj, t, k0, k1);
+      for (int ks = k0; ks < k1; ++ks) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[s], phase, a.status))) {
+          ok = false;
+          break;
+        }
+        const uint8_t *st = smem + (size_t)s * STAGE_BYTES;
+        const uint32_t col = tq + 48u * s;
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk)
-              // descriptor start address is in 16-byte units: +512 B = +32
-              tc_cp_sf(sf0 + 12u * kk, d + 32u * kk);
-          } else {
-            for (int kk = 0; kk < nk; ++kk) tc_cp_sf(sf0 + 12u * kk, d + 32u * kk);
-          }
-          tc_commit(&sff[s]);
-          ++issued;
-          if (++s == NSTAGE) {
-            s = 0;
-            phase ^= 1u;
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+#pragma unroll
+          for (int g = 0; g < 3; ++g) {
+            const uint8_t *atom = (g == 0 ? st + OFF_SFA : st + OFF_SFB + 2048 * (g - 1)) + 512 * kk;
+            tc_st4(col + 12u * kk + 4u * g, *reinterpret_cast<const uint4 *>(atom + 16 * lane));
           }
         }
-      }
-      // every copy completes before tensor memory is freed: the last commit
-      // went to the stage before the current ring position
-      if (issued > 0) {
-        const uint32_t ls = s == 0 ? NSTAGE - 1 : s - 1;
-        const uint32_t lp = s == 0 ? (phase ^ 1u) : phase;
-        mbar_wait_bounded(&sff[ls], lp, a.status);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sff[s]);
+        if (++s == NSTAGE) {
+          s = 0;
+          phase ^= 1u;
+        }
       }
     }
   } else {
