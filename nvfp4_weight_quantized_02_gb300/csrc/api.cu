@@ -223,10 +223,13 @@ imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor
     if (ws_bytes < impfp4::gemm_mxf4_workspace_bytes(M, N, K)) return IMP_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
   }
-  return from_cuda(impfp4::launch_gemm_mxf4(xq->codes, xq->scales, xq->tensor_scale, wq->codes,
-                                            true, wq->scales, wq->tensor_scale, M, N, K,
-                                            static_cast<uint16_t *>(y_bf16), ldy, dev_status,
-                                            workspace, static_cast<cudaStream_t>(stream)));
+  impfp4::GemmMxf4Plan plan;
+  cudaError_t e = impfp4::plan_gemm_mxf4(xq->codes, xq->scales, xq->tensor_scale, wq->codes, true,
+                                         wq->scales, wq->tensor_scale, M, N, K,
+                                         static_cast<uint16_t *>(y_bf16), ldy, dev_status,
+                                         workspace, plan);
+  if (e == cudaSuccess) e = impfp4::enqueue_gemm_mxf4(plan, static_cast<cudaStream_t>(stream));
+  return from_cuda(e);
 }
 
 imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
@@ -254,21 +257,25 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                                          need ? workspace : nullptr, s));
   }
   // Prefill: quantize X (scales straight into the atom layout), lay W's
-  // scales out as atoms, then the block-scaled FP4 tensor-core GEMM.
+  // scales out as atoms, then the block-scaled FP4 tensor-core GEMM.  The GEMM
+  // is planned first, so a failure returns before anything is enqueued.
+  // (A weight in the MMA layout, imp_nvfp4_gemm_mma, skips the W layout.)
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return IMP_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
   const PrefillWs L = prefill_ws(M, N, K);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   imp_nvfp4_tensor xq = {ws + L.xcodes, ws + L.xsc, reinterpret_cast<float *>(ws + L.sx), M, K};
   imp_nvfp4_tensor wq = {w->codes, ws + L.wsc, w->tensor_scale, N, K};
-  cudaError_t e = impfp4::launch_quantize_mma(static_cast<const uint16_t *>(x_bf16), M, K, ldx,
-                                              xq.codes, xq.scales, xq.tensor_scale, dev_status,
-                                              ws + L.partial, s);
+  impfp4::GemmMxf4Plan plan;
+  cudaError_t e = impfp4::plan_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, wq.codes, false,
+                                         wq.scales, wq.tensor_scale, M, N, K,
+                                         static_cast<uint16_t *>(y_bf16), ldy, dev_status,
+                                         nullptr, plan);
+  if (e != cudaSuccess) return IMP_ERR_CUDA;
+  e = impfp4::launch_quantize_mma(static_cast<const uint16_t *>(x_bf16), M, K, ldx, xq.codes,
+                                  xq.scales, xq.tensor_scale, dev_status, ws + L.partial, s);
   if (e == cudaSuccess) e = impfp4::launch_scale_relayout(w->scales, N, K, wq.scales, s);
-  if (e == cudaSuccess)
-    e = impfp4::launch_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, wq.codes, false,
-                                 wq.scales, wq.tensor_scale, M, N, K,
-                                 static_cast<uint16_t *>(y_bf16), ldy, dev_status, nullptr, s);
+  if (e == cudaSuccess) e = impfp4::enqueue_gemm_mxf4(plan, s);
   return from_cuda(e);
 }
 
@@ -303,13 +310,15 @@ imp_status imp_nvfp4_gemm_mma(const void *x_bf16, int64_t M, int64_t K, int64_t 
   const PrefillWs L = prefill_ws(M, N, K);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   imp_nvfp4_tensor xq = {ws + L.xcodes, ws + L.xsc, reinterpret_cast<float *>(ws + L.sx), M, K};
-  cudaError_t e = impfp4::launch_quantize_mma(static_cast<const uint16_t *>(x_bf16), M, K, ldx,
-                                              xq.codes, xq.scales, xq.tensor_scale, dev_status,
-                                              ws + L.partial, s);
-  if (e == cudaSuccess)
-    e = impfp4::launch_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, w->codes, true, w->scales,
-                                 w->tensor_scale, M, N, K, static_cast<uint16_t *>(y_bf16), ldy,
-                                 dev_status, nullptr, s);
+  impfp4::GemmMxf4Plan plan;
+  cudaError_t e = impfp4::plan_gemm_mxf4(xq.codes, xq.scales, xq.tensor_scale, w->codes, true,
+                                         w->scales, w->tensor_scale, M, N, K,
+                                         static_cast<uint16_t *>(y_bf16), ldy, dev_status,
+                                         nullptr, plan);
+  if (e != cudaSuccess) return IMP_ERR_CUDA;
+  e = impfp4::launch_quantize_mma(static_cast<const uint16_t *>(x_bf16), M, K, ldx, xq.codes,
+                                  xq.scales, xq.tensor_scale, dev_status, ws + L.partial, s);
+  if (e == cudaSuccess) e = impfp4::enqueue_gemm_mxf4(plan, s);
   return from_cuda(e);
 }
 

@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *sff = acce + 1;         // [NSTAGE] a stage's scales copied to tensor memory
   uint64_t *part_done = sff + NSTAGE;  // epilogue warps stored a split tile's partials
   uint64_t *flag_ready = part_done + 1;  // the tile's count is known
-  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(flag_ready + 1);
+  uint64_t *drain = flag_ready + 1;      // the MMA thread's last MMAs completed
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *last_flag = abort_flag + 1;
 
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acce, kEpiThreads);
     mbar_init(part_done, kEpiThreads / 32);
     mbar_init(flag_ready, 1);
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -308,7 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dA0 = smem_desc(smem_u32(smem), 16, 1024, kLayoutSw128);
       const uint64_t dB0 = smem_desc(smem_u32(smem + OFF_B), 16, 1024, kLayoutSw128);
       uint32_t s = 0, phase = 0;  // ring position of the next stage
-      int64_t issued = 0;         // stages consumed (for the drain on abort)
       int tile_iter = 0;
       bool ok = true;
       for (int jj = 0; ok && jj < sch.n_seg; ++jj, ++tile_iter) {
@@ -349,7 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                      sf0 + 12u * kk + 4, kk ? 1u : acc0);
           }
           tc_commit(&empty[s]);  // stage free once these MMAs complete
-          ++issued;
           if (++s == NSTAGE) {
             s = 0;
             phase ^= 1u;
@@ -358,16 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_commit(accf);  // tile accumulated
       }
-      if (!ok) {
-        *abort_flag = 1;
-        // let every issued MMA finish before tensor memory is freed: the last
-        // commit went to the stage before the current ring position
-        if (issued > 0) {
-          const uint32_t ls = s == 0 ? NSTAGE - 1 : s - 1;
-          const uint32_t lp = s == 0 ? (phase ^ 1u) : phase;
-          mbar_wait_bounded(&empty[ls], lp, a.status);
-        }
-      }
+      if (!ok) *abort_flag = 1;
+      // Every issued MMA completes before tensor memory is freed, whether or
+      // not the epilogue waited for them (it stops early after an abort).
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0u, a.status);
     }
   } else if (warp >= kScaleWarp0) {
     // ------------------------------ block scales -> tensor memory
@@ -549,16 +544,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t row_bytes,
                      uint64_t pitch, uint32_t box_rows, uint32_t box_bytes, bool swizzle128) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
+  // looked up once (thread-safe static initialisation)
+  static const PFN_cuTensorMapEncodeTiled_v12000 encode = []() {
     cudaDriverEntryPointQueryResult q;
     void *fn = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return false;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!encode) return false;
   const cuuint64_t dims[2] = {row_bytes, rows};
   const cuuint64_t strides[1] = {pitch};
   const cuuint32_t box[2] = {box_bytes, box_rows};
@@ -601,19 +597,27 @@ size_t gemm_mxf4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return gemm_ws(M, N, K).total;
 }
 
-cudaError_t launch_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales,
-                             const float *s_x, const uint8_t *w_codes, bool w_tiled,
-                             const uint8_t *w_mma_scales, const float *s_w, int64_t M,
-                             int64_t N, int64_t K, uint16_t *y, int64_t ldy, int32_t *status,
-                             void *workspace, cudaStream_t stream) {
+struct GemmMxf4Plan::Impl {
   CUtensorMap tmA, tmB;
-  memset(&tmB, 0, sizeof(tmB));  // not read with tiled W codes
-  if (!make_tmap_u8_2d(&tmA, x_codes, (uint64_t)M, (uint64_t)(K / 2), (uint64_t)(K / 2), BM, 128,
-                       true) ||
-      (!w_tiled && !make_tmap_u8_2d(&tmB, w_codes, (uint64_t)N, (uint64_t)(K / 2),
+  GemmArgs a;
+  int grid;
+};
+GemmMxf4Plan::GemmMxf4Plan() : impl(new Impl()) {}
+GemmMxf4Plan::~GemmMxf4Plan() { delete impl; }
+
+cudaError_t plan_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales, const float *s_x,
+                           const uint8_t *w_codes, bool w_tiled, const uint8_t *w_mma_scales,
+                           const float *s_w, int64_t M, int64_t N, int64_t K, uint16_t *y,
+                           int64_t ldy, int32_t *status, void *workspace, GemmMxf4Plan &plan) {
+  GemmMxf4Plan::Impl &p = *plan.impl;
+  memset(&p.tmA, 0, sizeof(p.tmA));
+  memset(&p.tmB, 0, sizeof(p.tmB));  // not read with tiled W codes
+  if (!make_tmap_u8_2d(&p.tmA, x_codes, (uint64_t)M, (uint64_t)(K / 2), (uint64_t)(K / 2), BM,
+                       128, true) ||
+      (!w_tiled && !make_tmap_u8_2d(&p.tmB, w_codes, (uint64_t)N, (uint64_t)(K / 2),
                                     (uint64_t)(K / 2), BN, 128, true)))
     return cudaErrorInvalidValue;
-  GemmArgs a;
+  GemmArgs &a = p.a;
   a.sfa = x_mma_scales;
   a.sfb = w_mma_scales;
   a.w_tiles = w_tiled ? w_codes : nullptr;
@@ -636,12 +640,14 @@ cudaError_t launch_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales
     a.part = reinterpret_cast<float *>(ws + L.part);
     a.epoch = next_launch_epoch();
   }
-  const int64_t grid = gemm_grid(M, N, K, workspace != nullptr);
-  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
-  gemm_mxf4_kernel<<<(int)grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
+  p.grid = (int)gemm_grid(M, N, K, workspace != nullptr);
+  return cudaFuncSetAttribute(gemm_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSmemBytes);
+}
+
+cudaError_t enqueue_gemm_mxf4(const GemmMxf4Plan &plan, cudaStream_t stream) {
+  const GemmMxf4Plan::Impl &p = *plan.impl;
+  gemm_mxf4_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(p.tmA, p.tmB, p.a);
   return cudaGetLastError();
 }
 

@@ -94,14 +94,17 @@ def run_prefill(lin, rows_check=None, cols_check=None, via="gemm"):
     wc, wsc = oracle.quantize_rows(wb[cols], s_w)
     _, s_x, _ = oracle.tensor_scale(xb)
     y_ref, bound = oracle.reference_gemm(xb[rows], lin.M, wc, wsc, s_w, s_x=s_x)
-    ratio = check_within_tolerance(y[np.ix_(rows, cols)], y_ref, bound, lin.name, tight=False)
+    ratio = check_within_tolerance(y[np.ix_(rows, cols)], y_ref, bound, lin.name, tight=True)
     assert np.isfinite(y).all()
     return ratio
 
 
 @pytest.mark.parametrize("M,K,N", [(128, 64, 256), (128, 256, 256), (256, 1024, 512),
                                    (128, 320, 256), (200, 320, 312), (17, 128, 40),
-                                   (640, 5120, 768), (333, 2048, 1000)])
+                                   (640, 5120, 768), (333, 2048, 1000),
+                                   # a second N tile mostly past N; three N tiles of a
+                                   # 128-row-block-aligned prepared weight; ragged rows
+                                   (130, 512, 200), (256, 768, 576), (300, 4096, 1920)])
 def test_small_shapes_every_element(M, K, N):
     lin = synth.Linear("pf", M, K, N, 77, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
                        zero_block_p=0.01, x_outlier_frac=0.01)
@@ -129,6 +132,9 @@ def test_repeatable(M, K, N):
     ws = torch.empty(pkg.imp_nvfp4_gemm_fp4_workspace_size(M, N, K), dtype=torch.uint8,
                      device="cuda")
     sk = [pkg.gemm_fp4(xq, wm, workspace=ws, stream_k=True).cpu() for _ in range(3)]
-    for runs in (outs, sk):
+    fp4 = [pkg.gemm_fp4(xq, wm).cpu() for _ in range(3)]
+    for runs in (outs, sk, fp4):
         for o in runs[1:]:
             assert torch.equal(runs[0].view(torch.int16), o.view(torch.int16))
+    # whole tiles: the same GEMM whichever form the weight is in
+    assert torch.equal(outs[0].view(torch.int16), fp4[0].view(torch.int16))
