@@ -37,9 +37,10 @@
  *   - All buffers are DEVICE memory allocated and owned by the caller.  The
  *     library never allocates, frees or synchronizes.  Between calls it
  *     keeps only host-side caches, guarded for use from several threads:
- *     TMA descriptors keyed by array address and shape, the SM count, and a
- *     launch counter (plus the fixed scratch of
- *     imp_nvfp4_quantize_noalloc).  Results never depend on them.
+ *     TMA descriptors keyed by array address and shape, the SM count, a
+ *     launch counter, and the device address of the fixed scratch of
+ *     imp_nvfp4_quantize_noalloc (per device and context).  Results never
+ *     depend on them.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); all work
  *     is enqueued on it asynchronously.
  *   - The return value reports argument and launch errors only.  A call that
@@ -117,9 +118,10 @@ imp_status imp_nvfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64
  * keeps until the process exits.  Sizes whose scratch would exceed that
  * array return IMP_ERR_WORKSPACE_TOO_SMALL (with 4 KB no valid size does).
  *   - Allocates nothing and calls no allocating routine.
- *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture that is to contain later calls.
+ *   - The first call in a device's context looks up the array's device
+ *     address (with that device current) and caches it for that context (a
+ *     device reset or a new context looks it up again); make that first call
+ *     before any stream capture that is to contain later calls.
  *   - All calls share the one array: calls that can run at the same time on
  *     the GPU (different streams, concurrent graphs) race and corrupt each
  *     other's results.  The array needs no clearing: each call overwrites

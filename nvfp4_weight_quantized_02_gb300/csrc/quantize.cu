@@ -12,7 +12,10 @@
 //      bit copied from x.  Every fp32 step is an explicitly rounded IEEE op
 //      (__fdiv_rn, __fmul_rn), so no contraction or approximation can change
 //      a byte.
+#include <cuda.h>
+
 #include <atomic>
+#include <mutex>
 
 #include "quantize.cuh"
 
@@ -264,28 +267,81 @@ __device__ __align__(256) uint32_t g_noalloc_partials[kMaxPartials];
 
 size_t quantize_noalloc_capacity() { return sizeof(g_noalloc_partials); }
 
+namespace {
+
+// ID of the calling thread's current CUDA context (0 if none or unknown),
+// through the driver's cuCtxGetCurrent / cuCtxGetId, looked up once.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static const GetCurrent get_current = []() {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<GetCurrent>(fn);
+  }();
+  static const GetId get_id = []() {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<GetId>(fn);
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// The device address of g_noalloc_partials, per device, for the context it
+// was looked up in: a device reset or a new primary context loads the module
+// again (a new address), so a cached address is used only while the current
+// context is the one it came from.  One mutex per device guards the entry.
+struct NoallocAddr {
+  std::mutex mu;
+  unsigned long long ctx = 0;
+  void *addr = nullptr;
+};
+NoallocAddr g_noalloc_addr[64];
+
+}  // namespace
+
 cudaError_t launch_quantize_noalloc(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
                                     uint8_t *codes, uint8_t *scales, float *tensor_scale,
                                     int32_t *status, cudaStream_t stream) {
   if (quantize_workspace_bytes(rows, K) > sizeof(g_noalloc_partials))
     return cudaErrorInvalidValue;  // caller checks sizes first; kept as a guard
   // In host code g_noalloc_partials names a host-side shadow, not device
-  // memory: the device address is looked up once per device (with that
-  // device current) and cached.
-  static void *addr[64] = {nullptr};
+  // memory: the device address is looked up with the device current.
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!addr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_partials);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
+  NoallocAddr &slot = g_noalloc_addr[dev];
+  void *addr = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(slot.mu);
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && ctx == slot.ctx && slot.addr) {
+      addr = slot.addr;
+    } else {
+      e = cudaGetSymbolAddress(&addr, g_noalloc_partials);
+      if (e != cudaSuccess) return e;
+      // the lookup makes the device's context current if it was not yet
+      slot.ctx = ctx != 0 ? ctx : current_context_id();
+      slot.addr = addr;
+    }
   }
   // Pass 1 writes every partial that pass 2 reads, so the array needs no
   // clearing between calls.
-  return launch_quantize(x, rows, K, ldx, codes, scales, tensor_scale, status, addr[dev], stream);
+  return launch_quantize(x, rows, K, ldx, codes, scales, tensor_scale, status, addr, stream);
 }
 
 cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
