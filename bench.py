@@ -601,9 +601,78 @@ def bench_small_configs(pkg, dev, stream, hbm_peak, status):
                 del graphs
             except Exception as e:  # report, do not fail the line
                 res["layer_graph"] = {"error": str(e)[:200]}
+        if name == "decode_0p6b":
+            res.update(bench_grouped_layer(pkg, dev, stream, status, lins, copies, ncopy, ins,
+                                           ys, layer_bytes))
         out[name] = res
         del copies, base
     return out
+
+
+def bench_grouped_layer(pkg, dev, stream, status, lins, copies, ncopy, ins, ys, layer_bytes):
+    """The 0.6B-class layer as four calls: q/k/v grouped, o, gate/up grouped,
+    down (8 kernels instead of 14), eagerly and replayed as CUDA graphs."""
+    import torch
+
+    by = {l.name: i for i, l in enumerate(lins)}
+    x = ins[by["q"]]
+    groups = [("q", "k", "v"), ("o",), ("gate", "up"), ("down",)]
+    wsz = 16
+    for g in groups:
+        wsz = max(wsz, pkg.imp_nvfp4_gemm_grouped_workspace_size(1, lins[by[g[0]]].K,
+                                                                 [lins[by[n]].N for n in g]))
+    ws = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    launches = sum(pkg.imp_nvfp4_gemm_grouped_plan(1, lins[by[g[0]]].K,
+                                                   [lins[by[n]].N for n in g])[0] for g in groups)
+
+    def calls(c, st):
+        for g in groups:
+            i0 = by[g[0]]
+            pkg.gemm_grouped(x if len(g) > 1 else ins[i0], [copies[by[n]][c] for n in g],
+                             ys=[ys[by[n]] for n in g], dev_status=status, stream=st,
+                             workspace=ws)
+    k = [0]
+
+    def layer():
+        calls(k[0] % ncopy, stream)
+        k[0] += 1
+    for _ in range(ncopy):
+        layer()
+    res = {}
+    ts = time_blocks(layer, ncopy, 10, stream)
+    med = statistics.median(ts)
+    res["layer_grouped_eager"] = {"us": spread(ts), "GB/s": layer_bytes / (med * 1e-6) / 1e9,
+                                  "launches": launches}
+    try:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graphs = []
+        for c in range(ncopy):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                calls(c, cap)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        gs = torch.cuda.current_stream(dev)
+        for g in graphs:
+            g.replay()
+        ts = []
+        for _ in range(10):
+            a, b = event_pair()
+            torch.cuda.synchronize()
+            a.record(gs)
+            for g in graphs:
+                g.replay()
+            b.record(gs)
+            torch.cuda.synchronize()
+            ts.append(1e3 * a.elapsed_time(b) / ncopy)
+        med = statistics.median(ts)
+        res["layer_grouped_graph"] = {"us": spread(ts), "GB/s": layer_bytes / (med * 1e-6) / 1e9,
+                                      "launches": launches}
+        del graphs
+    except Exception as e:  # report, do not fail the line
+        res["layer_grouped_graph"] = {"error": str(e)[:200]}
+    return res
 
 
 def bench_prefill(args, pkg, dev, stream):
@@ -678,6 +747,25 @@ def bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs, ch
     for _ in range(args.warmup):
         indep_step()
     out["decode_independent_inputs"] = rate(time_blocks(indep_step, n, 10, stream))
+
+    # the step with up and gate as one grouped call (one split of x, one
+    # weight stream over both weights' tiles)
+    by = {l.name: i for i, l in enumerate(lins)}
+    if "up" in by and "gate" in by:
+        iu, ig = by["up"], by["gate"]
+        gws = torch.empty(pkg.imp_nvfp4_gemm_grouped_workspace_size(
+            1, lins[iu].K, [lins[iu].N, lins[ig].N]), dtype=torch.uint8, device=dev)
+
+        def grouped_step():
+            pkg.gemm_grouped(chained[iu], [weights[iu], weights[ig]], ys=[ys[iu], ys[ig]],
+                             dev_status=status, stream=stream, workspace=gws)
+            for i, (x, w, y, ws) in enumerate(zip(chained, weights, ys, wss)):
+                if i not in (iu, ig):
+                    pkg.gemm_mma(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
+        for _ in range(args.warmup):
+            grouped_step()
+        out["decode_grouped_up_gate"] = rate(time_blocks(grouped_step, n, 10, stream))
+        del gws
 
     # the step replayed as one CUDA graph (programmatic dependent launch kept)
     try:

@@ -137,7 +137,9 @@ imp_status imp_nvfp4_quantize_noalloc(const void *x_bf16, int64_t rows, int64_t 
  * X's and W's atom-layout scales.  0 also for shapes no path accepts. */
 size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
-/* The plan imp_nvfp4_gemm follows for Y[M][N] = X[M][K] W^T on the current
+/* An addition of this library (host-side query; the pages have no
+ * counterpart), used to count launches and name the weight-streaming kernel.
+ * The plan imp_nvfp4_gemm follows for Y[M][N] = X[M][K] W^T on the current
  * device, given a workspace of imp_nvfp4_gemm_workspace_size bytes and
  * 16-byte aligned arrays: returns the number of kernels one call launches
  * (0 if the call rejects the shape) and stores in *kernel (when kernel is not
@@ -157,7 +159,10 @@ int32_t imp_nvfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const char **kernel
  *   y_bf16   device bf16[M][ldy], ldy >= N, ldy % 8 == 0; fully overwritten.
  *   workspace  imp_nvfp4_gemm_workspace_size(M, N, K) bytes, 16-byte aligned
  *            (else IMP_ERR_WORKSPACE_TOO_SMALL / IMP_ERR_MISALIGNED); owned by
- *            the caller, needs no clearing; calls that may run at the same
+ *            the caller, needs no clearing (each launch leaves its per-tile
+ *            counters at zero, so a captured call replays correctly; only
+ *            after a call that reported IMP_DEV_TIMEOUT should it be zeroed
+ *            before that call is replayed); calls that may run at the same
  *            time on the GPU need separate workspaces.
  *   Decode shapes: every K up to 61440; beyond that the FP4 path takes
  *   K % 256 == 0 with N >= 128 (other long-K shapes return
@@ -177,8 +182,12 @@ imp_status imp_nvfp4_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                           int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream);
 
 /* ---- tensor-core operand layout ("MMA layout") -----------------------------
- * A one-time transform of a weight for the tensor-core kernels (like an
- * engine's cache of transformed weights); values are unchanged.
+ * A one-time transform of a weight for the tensor-core kernels; values are
+ * unchanged.  It follows "How imp turns a model file into words", part one
+ * ("loading the model (happens once)"): the engine converts every weight
+ * once at load so that the per-token steps read it in the form its kernels
+ * want.  The layout itself is this library's (what the sm_103a tensor-core
+ * copies read); the pages do not give one.
  *   Scales: 512-byte atoms, one per 128 rows x 4 blocks (64 elements of K);
  *     row r of the atom at byte 16*(r % 32) + 4*((r / 32) % 4), block j of it
  *     at + j.  Atoms of a 128-row block follow each other along K; row blocks
@@ -204,7 +213,10 @@ size_t imp_nvfp4_mma_codes_size(int64_t rows, int64_t K);
 imp_status imp_nvfp4_prepare_mma(const imp_nvfp4_tensor *t, void *mma_codes, size_t codes_bytes,
                                  void *mma_scales, size_t scales_bytes, void *stream);
 
-/* Quantize like imp_nvfp4_quantize (bit-identical codes, scale bytes and
+/* An addition of this library: the prefill path's on-device activation
+ * quantizer (the imp README, "How it works": prefill is compute-bound and
+ * runs on the 4-bit tensor cores) exposed on its own.
+ * Quantize like imp_nvfp4_quantize (bit-identical codes, scale bytes and
  * tensor scale) but write the scales in the MMA (atom) layout, for the X
  * operand of imp_nvfp4_gemm_fp4: out->scales must hold
  * imp_nvfp4_mma_scales_size(rows, K) bytes; codes stay row-major [rows][K/2].
@@ -213,12 +225,16 @@ imp_status imp_nvfp4_quantize_mma(const void *x_bf16, int64_t rows, int64_t K, i
                                   const imp_nvfp4_tensor *out, int32_t *dev_status,
                                   void *workspace, size_t ws_bytes, void *stream);
 
-/* Bytes of the optional workspace of imp_nvfp4_gemm_fp4 (on the current
+/* An addition of this library, with imp_nvfp4_gemm_fp4 below.
+ * Bytes of the optional workspace of imp_nvfp4_gemm_fp4 (on the current
  * device): per-tile counters and one partial 128 x 256 fp32 tile per CTA
  * and split segment (~39 MB on a 152-SM GPU).  0 for invalid sizes.       */
 size_t imp_nvfp4_gemm_fp4_workspace_size(int64_t M, int64_t N, int64_t K);
 
-/* Y = Xq * Wq^T, both operands NVFP4: the block-scaled FP4 tensor-core GEMM
+/* An addition of this library: the prefill GEMM step (the imp README
+ * feature matrix, "NVFP4 block-scaled ... GEMM/GEMV"; "How it works":
+ * prefill is compute-bound) callable without the activation quantizer.
+ * Y = Xq * Wq^T, both operands NVFP4: the block-scaled FP4 tensor-core GEMM
  * alone (tcgen05.mma kind::mxf4nvf4, fp32 accumulation in tensor memory),
  * times s_x * s_w, rounded to bf16.
  *   xq  from imp_nvfp4_quantize_mma: M rows (M >= 1), row-major codes,
@@ -238,7 +254,10 @@ imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor
                               size_t ws_bytes, void *stream);
 
 /* Y = X * W^T like imp_nvfp4_gemm, with W in MMA layout (the serving form:
- * weights prepared once, read as contiguous 16 KB tiles).  M <= 16 takes the
+ * weights prepared once at load -- "How imp turns a model file into words",
+ * part one -- and read as contiguous 16 KB tiles).  An addition of this
+ * library in place of an imp_nvfp4_gemm that would look for prepared scales
+ * beside the row-major tensor: the caller chooses the form explicitly.  M <= 16 takes the
  * decode path (FP4 tensor cores, X split per call), which needs
  * K % 256 == 0, K >= 1024, N >= 128 (else IMP_ERR_UNSUPPORTED_SHAPE);
  * M > 16 the prefill path.  Workspace: imp_nvfp4_gemm_workspace_size(M, N,
@@ -247,6 +266,50 @@ imp_status imp_nvfp4_gemm_fp4(const imp_nvfp4_tensor *xq, const imp_nvfp4_tensor
 imp_status imp_nvfp4_gemm_mma(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                               const imp_nvfp4_tensor *w_mma, void *y_bf16, int64_t ldy,
                               int32_t *dev_status, void *workspace, size_t ws_bytes, void *stream);
+
+/* ---- grouped decode GEMV ---------------------------------------------------
+ * One X times several weights of the same K in one call -- a layer's q, k
+ * and v projections, or its gate and up projections -- the same products as
+ * concatenating the weights along N, except that each weight keeps its own
+ * tensor scale and output.  It serves the engine's per-token launch sequence,
+ * which is recorded once and replayed ("How imp turns a model file into
+ * words", part one; the imp README, "How it works": CUDA graphs replay the
+ * decode launches): fewer, larger launches make that sequence shorter.  The
+ * grouping is an addition of this library.                                */
+#define IMP_NVFP4_MAX_GROUPS 4
+typedef struct {
+  imp_nvfp4_tensor w;  /* weight g in MMA layout: w.rows = N_g >= 1, w.K == K */
+  void *y_bf16;        /* device bf16[M][ldy]: Y_g = X * W_g^T, fully overwritten */
+  int64_t ldy;         /* >= N_g, multiple of 8 */
+} imp_nvfp4_group;
+
+/* Bytes of workspace imp_nvfp4_gemm_grouped needs (N: the n_groups row
+ * counts; 0 for invalid arguments). */
+size_t imp_nvfp4_gemm_grouped_workspace_size(int64_t M, int64_t K, const int64_t *N,
+                                             int32_t n_groups);
+
+/* Like imp_nvfp4_gemm_plan for a grouped call: kernels launched in total
+ * (0: rejected) and, in *kernel, the name of the first weight-streaming
+ * kernel.  Host only.                                                      */
+int32_t imp_nvfp4_gemm_grouped_plan(int64_t M, int64_t K, const int64_t *N, int32_t n_groups,
+                                    const char **kernel);
+
+/* Y_g = X * W_g^T for g < n_groups (1 <= n_groups <= IMP_NVFP4_MAX_GROUPS).
+ *   x_bf16, M, K, ldx   as for imp_nvfp4_gemm_mma (M = 0: nothing to do).
+ *   1 <= M <= 2, K % 256 == 0 and K >= 1024 (the decode case): one split of
+ *   X and one weight-streaming launch for all groups (2 kernels), scheduled
+ *   over the groups' 128-row tiles together.  Other shapes (and a tile or K
+ *   count that plan cannot hold) run imp_nvfp4_gemm_mma once per group, in
+ *   order, on `stream`; a shape it rejects returns
+ *   IMP_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
+ *   workspace  imp_nvfp4_gemm_grouped_workspace_size bytes, 16-byte aligned.
+ *   Accuracy as for imp_nvfp4_gemm; results are bitwise reproducible from
+ *   run to run, though the one-pass schedule may sum a tile's K chunks in
+ *   another grouping than a call on that weight alone.                     */
+imp_status imp_nvfp4_gemm_grouped(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                  const imp_nvfp4_group *groups, int32_t n_groups,
+                                  int32_t *dev_status, void *workspace, size_t ws_bytes,
+                                  void *stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *imp_status_string(imp_status status);

@@ -30,6 +30,8 @@ __all__ = [
     "imp_nvfp4_gemm_fp4_workspace_size",
     "imp_nvfp4_quantize_noalloc", "imp_nvfp4_mma_codes_size", "imp_nvfp4_gemm_mma",
     "quantize_mma", "gemm_fp4", "gemm_mma", "imp_selftest_bounded_wait",
+    "ImpNvfp4Group", "IMP_NVFP4_MAX_GROUPS", "imp_nvfp4_gemm_grouped",
+    "imp_nvfp4_gemm_grouped_workspace_size", "imp_nvfp4_gemm_grouped_plan", "gemm_grouped",
 ]
 
 IMP_OK = 0
@@ -42,11 +44,17 @@ IMP_DEV_OK = 0
 IMP_DEV_NONFINITE_INPUT = 1
 IMP_DEV_TIMEOUT = 2
 DECODE_M_MAX = 16
+IMP_NVFP4_MAX_GROUPS = 4
 
 class ImpNvfp4Tensor(ctypes.Structure):
     """ctypes mirror of imp_nvfp4_tensor."""
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("tensor_scale", ctypes.c_void_p), ("rows", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class ImpNvfp4Group(ctypes.Structure):
+    """ctypes mirror of imp_nvfp4_group."""
+    _fields_ = [("w", ImpNvfp4Tensor), ("y_bf16", ctypes.c_void_p), ("ldy", ctypes.c_int64)]
 
 
 _lib = None
@@ -94,6 +102,15 @@ def _L():
     lib.imp_nvfp4_gemm_fp4.argtypes = [T, T, P, I64, P, P, SZ, P]
     lib.imp_nvfp4_gemm_fp4_workspace_size.restype = SZ
     lib.imp_nvfp4_gemm_fp4_workspace_size.argtypes = [I64, I64, I64]
+    PI64 = ctypes.POINTER(I64)
+    lib.imp_nvfp4_gemm_grouped_workspace_size.restype = SZ
+    lib.imp_nvfp4_gemm_grouped_workspace_size.argtypes = [I64, I64, PI64, ctypes.c_int32]
+    lib.imp_nvfp4_gemm_grouped_plan.restype = ctypes.c_int32
+    lib.imp_nvfp4_gemm_grouped_plan.argtypes = [I64, I64, PI64, ctypes.c_int32,
+                                                ctypes.POINTER(ctypes.c_char_p)]
+    lib.imp_nvfp4_gemm_grouped.restype = ctypes.c_int
+    lib.imp_nvfp4_gemm_grouped.argtypes = [P, I64, I64, I64, ctypes.POINTER(ImpNvfp4Group),
+                                           ctypes.c_int32, P, P, SZ, P]
     _lib = lib
     return lib
 
@@ -197,6 +214,30 @@ def imp_nvfp4_gemm_fp4(xq: ImpNvfp4Tensor, wq: ImpNvfp4Tensor, y_bf16: int, ldy:
                        stream: int | None) -> int:
     return _L().imp_nvfp4_gemm_fp4(ctypes.byref(xq), ctypes.byref(wq), y_bf16, ldy, dev_status,
                                    workspace, ws_bytes, stream)
+
+
+def _i64s(N) -> "ctypes.Array":
+    return (ctypes.c_int64 * len(N))(*N)
+
+
+def imp_nvfp4_gemm_grouped_workspace_size(M: int, K: int, N: list[int]) -> int:
+    return _L().imp_nvfp4_gemm_grouped_workspace_size(M, K, _i64s(N), len(N))
+
+
+def imp_nvfp4_gemm_grouped_plan(M: int, K: int, N: list[int]) -> tuple[int, str | None]:
+    """(kernel launches of one imp_nvfp4_gemm_grouped call, name of the first
+    weight-streaming kernel); (0, None) if rejected."""
+    name = ctypes.c_char_p()
+    n = _L().imp_nvfp4_gemm_grouped_plan(M, K, _i64s(N), len(N), ctypes.byref(name))
+    return n, (name.value.decode() if name.value else None)
+
+
+def imp_nvfp4_gemm_grouped(x_bf16: int, M: int, K: int, ldx: int, groups: list[ImpNvfp4Group],
+                           dev_status: int | None, workspace: int | None, ws_bytes: int,
+                           stream: int | None) -> int:
+    arr = (ImpNvfp4Group * len(groups))(*groups)
+    return _L().imp_nvfp4_gemm_grouped(x_bf16, M, K, ldx, arr, len(groups), dev_status,
+                                       workspace, ws_bytes, stream)
 
 
 class ImpError(RuntimeError):
@@ -365,3 +406,27 @@ def gemm_mma(x, w: NVFP4Tensor, y=None, dev_status=None, stream=None, workspace=
     if st != IMP_OK:
         raise ImpError(st, "imp_nvfp4_gemm_mma")
     return y
+
+
+def gemm_grouped(x, ws: list, ys=None, dev_status=None, stream=None, workspace=None):
+    """[X W_g^T for W_g in ws] in one call for weights in MMA layout
+    (prepare_mma) sharing K: one X split and one weight stream for all of
+    them at M <= 2."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert all(w.layout == "mma" for w in ws)
+    M, K = x.shape
+    N = [w.rows for w in ws]
+    if ys is None:  # row strides rounded up to a multiple of 8 elements
+        ys = [torch.empty((M, (n + 7) // 8 * 8), dtype=torch.bfloat16, device=x.device)[:, :n]
+              for n in N]
+    ws_bytes = imp_nvfp4_gemm_grouped_workspace_size(M, K, N)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    groups = [ImpNvfp4Group(w.c_struct(), y.data_ptr(), y.stride(0)) for w, y in zip(ws, ys)]
+    st = imp_nvfp4_gemm_grouped(x.data_ptr(), M, K, x.stride(0), groups,
+                                None if dev_status is None else dev_status.data_ptr(),
+                                workspace.data_ptr(), ws_bytes, _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_gemm_grouped")
+    return ys

@@ -323,3 +323,118 @@ imp_status imp_nvfp4_gemm_mma(const void *x_bf16, int64_t M, int64_t K, int64_t 
 }
 
 }  // extern "C"
+
+namespace {
+
+// Kernels one imp_nvfp4_gemm_mma call launches (0: shape rejected).
+int32_t mma_plan(int64_t M, int64_t N, int64_t K, const char **kernel) {
+  const char *k = nullptr;
+  int32_t n = 0;
+  if (M >= 1 && N >= 1 && K > 0 && K % 64 == 0) {
+    if (M <= kDecodeMaxM) {
+      if (impfp4::gemv_f4_shape_ok(M, N, K)) n = impfp4::gemv_f4_launches(M, N, K, &k);
+    } else if (M <= INT32_MAX && N <= INT32_MAX && K <= INT32_MAX) {
+      n = 3;  // the activation quantizer's two passes and the GEMM
+      k = "gemm_mxf4_kernel";
+    }
+  }
+  if (kernel) *kernel = n ? k : nullptr;
+  return n;
+}
+
+bool grouped_one_pass(int64_t M, int64_t K, const imp_nvfp4_group *g, int32_t n) {
+  impfp4::GemvGroup d[IMP_NVFP4_MAX_GROUPS];
+  for (int i = 0; i < n; ++i)
+    d[i] = {g[i].w.codes, g[i].w.scales, g[i].w.tensor_scale,
+            static_cast<uint16_t *>(g[i].y_bf16), g[i].w.rows, g[i].ldy};
+  return impfp4::gemv_f4_grouped_ok(M, K, d, n);
+}
+
+bool grouped_one_pass_sizes(int64_t M, int64_t K, const int64_t *N, int32_t n) {
+  imp_nvfp4_group g[IMP_NVFP4_MAX_GROUPS] = {};
+  for (int i = 0; i < n; ++i) g[i].w.rows = N[i];
+  return grouped_one_pass(M, K, g, n);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t imp_nvfp4_gemm_grouped_workspace_size(int64_t M, int64_t K, const int64_t *N,
+                                             int32_t n_groups) {
+  if (!N || n_groups < 1 || n_groups > IMP_NVFP4_MAX_GROUPS || M < 0 || K <= 0) return 0;
+  size_t need = 0;
+  for (int i = 0; i < n_groups; ++i) {
+    if (N[i] < 0) return 0;
+    const size_t w = imp_nvfp4_gemm_workspace_size(M, N[i], K);
+    need = w > need ? w : need;
+  }
+  if (grouped_one_pass_sizes(M, K, N, n_groups)) {
+    const size_t w = impfp4::gemv_f4_grouped_workspace_bytes(M, K, N, n_groups);
+    need = w > need ? w : need;
+  }
+  return need;
+}
+
+int32_t imp_nvfp4_gemm_grouped_plan(int64_t M, int64_t K, const int64_t *N, int32_t n_groups,
+                                    const char **kernel) {
+  if (kernel) *kernel = nullptr;
+  if (!N || n_groups < 1 || n_groups > IMP_NVFP4_MAX_GROUPS) return 0;
+  if (grouped_one_pass_sizes(M, K, N, n_groups)) {
+    if (kernel) *kernel = "gemv_f4r_kernel";
+    return 2;
+  }
+  int32_t total = 0;
+  for (int i = 0; i < n_groups; ++i) {
+    const char *k = nullptr;
+    const int32_t n = mma_plan(M, N[i], K, &k);
+    if (n == 0) return 0;
+    total += n;
+    if (kernel && !*kernel) *kernel = k;
+  }
+  return total;
+}
+
+imp_status imp_nvfp4_gemm_grouped(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                  const imp_nvfp4_group *groups, int32_t n_groups,
+                                  int32_t *dev_status, void *workspace, size_t ws_bytes,
+                                  void *stream) {
+  if (M < 0 || !groups || n_groups < 1 || n_groups > IMP_NVFP4_MAX_GROUPS) return IMP_ERR_INVALID_ARG;
+  if (K <= 0 || K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  int64_t N[IMP_NVFP4_MAX_GROUPS];
+  for (int i = 0; i < n_groups; ++i) {
+    const imp_nvfp4_group &g = groups[i];
+    N[i] = g.w.rows;
+    if (N[i] < 1 || g.w.K != K) return IMP_ERR_INVALID_ARG;
+    imp_status st = check_tensor(&g.w, N[i], K);
+    if (st != IMP_OK) return st;
+    if (!g.y_bf16 || g.ldy < N[i]) return IMP_ERR_INVALID_ARG;
+    if (!aligned16(g.y_bf16) || g.ldy % 8) return IMP_ERR_MISALIGNED;
+  }
+  if (M == 0) return IMP_OK;
+  if (!x_bf16) return IMP_ERR_INVALID_ARG;
+  if (ldx < K) return IMP_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || ldx % 8) return IMP_ERR_MISALIGNED;
+  if (imp_nvfp4_gemm_grouped_plan(M, K, N, n_groups, nullptr) == 0) return IMP_ERR_UNSUPPORTED_SHAPE;
+  const size_t need = imp_nvfp4_gemm_grouped_workspace_size(M, K, N, n_groups);
+  if (!workspace || ws_bytes < need) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  if (grouped_one_pass(M, K, groups, n_groups)) {
+    impfp4::GemvGroup d[IMP_NVFP4_MAX_GROUPS];
+    for (int i = 0; i < n_groups; ++i)
+      d[i] = {groups[i].w.codes, groups[i].w.scales, groups[i].w.tensor_scale,
+              static_cast<uint16_t *>(groups[i].y_bf16), N[i], groups[i].ldy};
+    return from_cuda(impfp4::launch_gemv_f4_grouped(static_cast<const uint16_t *>(x_bf16), M, K,
+                                                    ldx, d, n_groups, dev_status, workspace,
+                                                    static_cast<cudaStream_t>(stream)));
+  }
+  // one call per weight, in order, sharing the workspace
+  for (int i = 0; i < n_groups; ++i) {
+    const imp_status st = imp_nvfp4_gemm_mma(x_bf16, M, K, ldx, &groups[i].w, groups[i].y_bf16,
+                                             groups[i].ldy, dev_status, workspace, ws_bytes, stream);
+    if (st != IMP_OK) return st;
+  }
+  return IMP_OK;
+}
+
+}  // extern "C"

@@ -49,4 +49,21 @@ cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
                            cudaStream_t stream, bool prepared = false);
 
+// Grouped decode GEMV: one X times up to four weights of the same K in one
+// launch pair (the weights' tiles follow each other in one schedule; each
+// keeps its tensor scale and output), weights in the MMA layout.
+struct GemvGroup {
+  const uint8_t *codes, *scales;  // MMA layout
+  const float *tensor_scale;
+  uint16_t *y;                    // bf16[M][ldy]
+  int64_t N, ldy;
+};
+// True if launch_gemv_f4_grouped takes these groups (1 <= M <= 2,
+// K % 256 == 0, K >= 1024, 1..4 groups, 16-byte aligned arrays).
+bool gemv_f4_grouped_ok(int64_t M, int64_t K, const GemvGroup *g, int n);
+size_t gemv_f4_grouped_workspace_bytes(int64_t M, int64_t K, const int64_t *N, int n);
+cudaError_t launch_gemv_f4_grouped(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                                   const GemvGroup *g, int n, int32_t *status, void *workspace,
+                                   cudaStream_t stream);
+
 }  // namespace impfp4

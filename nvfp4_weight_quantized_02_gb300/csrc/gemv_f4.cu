@@ -123,14 +123,25 @@ struct StageR {
 // reads.  Operand row 8 m + c holds component c of row m of X; rows past the
 // last component are zero.
 
+// A call multiplies one X by up to kMaxGroups weights of the same K (for
+// example a layer's q, k and v projections): their 128-row tiles follow each
+// other in the call's tile sequence, group g from tile tile0 on, and each
+// keeps its own tensor scale and output.  An ordinary call has one group.
+constexpr int kMaxGroups = 4;
+struct F4Group {
+  const uint8_t *wc;    // prepared weight: code tiles [128-row block][chunk][16 KB]
+  const uint8_t *wsa;   // prepared weight: scale atoms [128-row block][K/64][512 B]
+  const float *ts;      // tensor scale s_w
+  uint16_t *y;          // bf16[M][ldy]
+  int64_t N, ldy;
+  int tile0;            // the group's first tile in the call
+};
+
 struct F4Args {
   const uint16_t *x;    // resident kernel: X rows
   int64_t ldx;
-  uint16_t *y;
-  int64_t ldy;
   int M;
-  int64_t N, K;
-  const float *tensor_scale;
+  int64_t K;
   const uint8_t *sfb;   // X component scales: streamed kernel atoms [K/64][512]; resident kernel slot images [K/256][1 KB]
   const uint8_t *slot_codes;  // resident kernel: X component codes, slot images [K/256][2 KB]
   const int32_t *sh;    // streamed kernel: per-row prescale exponents
@@ -143,8 +154,39 @@ struct F4Args {
   int n_slots;          // resident kernel: B slots in shared memory
   int sched;            // kSchedStreamK / kSchedWhole / kSchedCluster
   int ksplit;           // kSchedCluster: CTAs per tile (the cluster size)
-  const uint8_t *wc;    // prepared weight: code tiles [128-row block][chunk][16 KB]
-  const uint8_t *wsa;   // prepared weight: scale atoms [128-row block][K/64][512 B]
+  int n_groups;         // weights of the call (row-major weight: 1)
+  F4Group grp[kMaxGroups];
+};
+
+// Group of call tile `tile` (groups in tile order).
+__device__ __forceinline__ int group_of(const F4Args &a, int tile) {
+  int g = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxGroups; ++i) g += (i < a.n_groups && tile >= a.grp[i].tile0) ? 1 : 0;
+  return g;
+}
+// a.grp[g] without a dynamically indexed parameter access
+__device__ __forceinline__ F4Group group_at(const F4Args &a, int g) {
+  F4Group r = a.grp[0];
+#pragma unroll
+  for (int i = 1; i < kMaxGroups; ++i)
+    if (g == i) r = a.grp[i];
+  return r;
+}
+// Code tiles and scale atoms of one call tile of a prepared weight (chunk ch
+// at wc + 16 KB ch and wsa + 2 KB ch), looked up again only when the tile
+// changes: the producer's per-stage work stays a few adds.
+struct PreparedTile {
+  int tile = -1;
+  const uint8_t *wc = nullptr, *wsa = nullptr;
+  __device__ __forceinline__ void at(const F4Args &a, int t, int nch) {
+    if (t == tile) return;
+    const F4Group g = group_at(a, group_of(a, t));
+    const int64_t lt = t - g.tile0;
+    wc = g.wc + lt * nch * 16384;
+    wsa = g.wsa + lt * (a.K / 64) * 512;
+    tile = t;
+  }
 };
 
 struct F4Bars {
@@ -532,7 +574,9 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
   constexpr int MR = NMMA / kNC;  // rows of X the operand holds (>= M)
   const int q = warp & 3;
   const int row_in_tile = 32 * q + lane;
-  const float out_scale = *a.tensor_scale;
+  float osc[kMaxGroups];  // the groups' tensor scales, loaded together
+#pragma unroll
+  for (int g = 0; g < kMaxGroups; ++g) osc[g] = g < a.n_groups ? *a.grp[g].ts : 0.0f;
   volatile int *last_flag = &bars.last;
   int n_split = 0;
   for (int jj = 0; jj < sk.n_seg; ++jj) {
@@ -569,16 +613,22 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars.d_empty[d]);
-    const int64_t row = T * kTileRows + row_in_tile;
+    const int gi = group_of(a, T32);
+    const F4Group gp = group_at(a, gi);
+    float out_scale = osc[0];
+#pragma unroll
+    for (int g = 1; g < kMaxGroups; ++g)
+      if (gi == g) out_scale = osc[g];
+    const int64_t row = (T - gp.tile0) * kTileRows + row_in_tile;  // row of the group's W and y
     // to true units: (acc * s_w) * 2^-sh (the power of two last: exact
     // unless the result itself under- or overflows)
 #pragma unroll
     for (int m = 0; m < MR; ++m) acc[m] = ldexpf(acc[m] * out_scale, -sh[m]);
     if (c0 == 0 && c1 == sk.nch) {  // whole tile in this CTA
-      if (row < a.N) {
+      if (row < gp.N) {
 #pragma unroll
         for (int m = 0; m < MR; ++m)
-          if (m < a.M) a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+          if (m < a.M) gp.y[m * gp.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
       }
       continue;
     }
@@ -595,14 +645,14 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(cluster_map(smem_u32(&bars.cl_full), 0));
       } else if (__all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(&bars.cl_full, 0u, a.status)) &&
-                 row < a.N) {
+                 row < gp.N) {
         for (int r = 1; r < a.ksplit; ++r) {
 #pragma unroll
           for (int m = 0; m < MR; ++m) acc[m] += red[((size_t)(r - 1) * kTileRows + row_in_tile) * MR + m];
         }
 #pragma unroll
         for (int m = 0; m < MR; ++m)
-          if (m < a.M) a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+          if (m < a.M) gp.y[m * gp.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
       }
       continue;
     }
@@ -641,7 +691,7 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.flag_ready, par, a.status))) break;
     if (*last_flag) {
       __threadfence();
-      if (row < a.N) {
+      if (row < gp.N) {
         // Sums in K order, per row of X.  The partials sit in other SMs' L2
         // lines (often across the die boundary), so the loads of several
         // CTAs are put in flight together before any is added.
@@ -689,7 +739,7 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
         }
 #pragma unroll
         for (int m = 0; m < MR; ++m)
-          if (m < a.M) a.y[m * a.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(t[m]));
+          if (m < a.M) gp.y[m * gp.ldy + row] = __bfloat16_as_ushort(__float2bfloat16_rn(t[m]));
       }
     }
   }
@@ -793,6 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       prefetch_tmap(&tm_b);
       // processing position i -> ring slot i % NS, stage stage_of(i)
+      PreparedTile src, psrc;
       auto load_w = [&](int i) {
         const int s = i % NS;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
@@ -801,9 +852,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row0 = tile * kTileRows;
         mbar_arrive_expect_tx(&bars.full[s], L::TX);
         if (PREP) {
-          bulk_g2s(stg + L::W, a.wc + ((int64_t)tile * sk.nch + ch) * 16384, 16384u, &bars.full[s]);
-          bulk_g2s(stg + L::SFA, a.wsa + ((int64_t)tile * (a.K / 64) + 4 * ch) * 512, 2048u,
-                   &bars.full[s]);
+          src.at(a, tile, sk.nch);
+          bulk_g2s(stg + L::W, src.wc + (size_t)ch * 16384, 16384u, &bars.full[s]);
+          bulk_g2s(stg + L::SFA, src.wsa + (size_t)ch * 2048, 2048u, &bars.full[s]);
         } else {
           tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
           tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
@@ -821,8 +872,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tile, ch;
         sk.tile_ch(sk.stage_of(i), tile, ch);
         if (PREP) {
-          bulk_prefetch_l2(a.wc + ((int64_t)tile * sk.nch + ch) * 16384, 16384u);
-          bulk_prefetch_l2(a.wsa + ((int64_t)tile * (a.K / 64) + 4 * ch) * 512, 2048u);
+          psrc.at(a, tile, sk.nch);
+          bulk_prefetch_l2(psrc.wc + (size_t)ch * 16384, 16384u);
+          bulk_prefetch_l2(psrc.wsa + (size_t)ch * 2048, 2048u);
         } else {
           tma_prefetch_l2_2d(&tm_w, ch * (kChunkK / 2), tile * kTileRows);
           tma_prefetch_l2_2d(&tm_ws, ch * (kChunkK / 16), tile * kTileRows);
@@ -1016,6 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_ws);
       }
       // processing position i -> ring slot i % NS, stage stage_of(i)
+      PreparedTile src, psrc;
       auto load_w = [&](int i) {
         const int s = i % kNSR;
         uint8_t *stg = smem + (size_t)s * L::BYTES;
@@ -1024,9 +1077,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row0 = tile * kTileRows;
         mbar_arrive_expect_tx(&bars.full[s], L::TX);
         if (PREP) {
-          bulk_g2s(stg + L::W, a.wc + ((int64_t)tile * sk.nch + ch) * 16384, 16384u, &bars.full[s]);
-          bulk_g2s(stg + L::SFA, a.wsa + ((int64_t)tile * (a.K / 64) + 4 * ch) * 512, 2048u,
-                   &bars.full[s]);
+          src.at(a, tile, sk.nch);
+          bulk_g2s(stg + L::W, src.wc + (size_t)ch * 16384, 16384u, &bars.full[s]);
+          bulk_g2s(stg + L::SFA, src.wsa + (size_t)ch * 2048, 2048u, &bars.full[s]);
         } else {
           tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
           tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
@@ -1243,24 +1296,32 @@ cudaError_t launch_pdl(Kern kern, int grid, int threads, size_t smem, cudaStream
   return cudaGetLastError();
 }
 
-F4Args base_args(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const float *tensor_scale,
-                 int64_t N, uint16_t *y, int64_t ldy, int32_t *status, uint8_t *ws,
-                 const F4Ws &L) {
+// 128-row tiles of all groups of a call
+int64_t group_tiles(const GemvGroup *g, int n) {
+  int64_t t = 0;
+  for (int i = 0; i < n; ++i) t += ceil_div(g[i].N, kTileRows);
+  return t;
+}
+
+F4Args base_args(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const GemvGroup *g, int n,
+                 int32_t *status, uint8_t *ws, const F4Ws &L) {
   F4Args a = {};
   a.x = x;
   a.ldx = ldx;
-  a.y = y;
-  a.ldy = ldy;
   a.M = (int)M;
-  a.N = N;
   a.K = K;
-  a.tensor_scale = tensor_scale;
   a.sfb = ws + L.sfb;
   a.sh = reinterpret_cast<const int32_t *>(ws + L.sh);
   a.part = reinterpret_cast<float *>(ws + L.part);
   a.cnt = reinterpret_cast<unsigned __int128 *>(ws + L.cnt);
   a.status = status;
-  a.n_tiles = (int)ceil_div(N, kTileRows);
+  a.n_groups = n;
+  int64_t t = 0;
+  for (int i = 0; i < n; ++i) {
+    a.grp[i] = F4Group{g[i].codes, g[i].scales, g[i].tensor_scale, g[i].y, g[i].N, g[i].ldy, (int)t};
+    t += ceil_div(g[i].N, kTileRows);
+  }
+  a.n_tiles = (int)t;
   a.n_chunks = (int)(K / kChunkK);
   a.epoch = next_launch_epoch();
   return a;
@@ -1317,9 +1378,8 @@ cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_
                                              reinterpret_cast<int32_t *>(ws + L.sh));
     if (e != cudaSuccess) return e;
   }
-  F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status, ws, L);
-  a.wc = codes;
-  a.wsa = scales;
+  const GemvGroup g = {codes, scales, tensor_scale, y, N, ldy};
+  F4Args a = base_args(x, M, K, ldx, &g, 1, status, ws, L);
   switch (nmma) {
     case 16: return launch_streamed<16>(prepared, L.grid, stream, mw, ms, mb, a);
     case 32: return launch_streamed<32>(prepared, L.grid, stream, mw, ms, mb, a);
@@ -1364,50 +1424,80 @@ bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const
   return gemv_f4_shape_ok(M, N, K) && !(((uintptr_t)codes | (uintptr_t)scales) & 15u);
 }
 
+// One launch pair for every group: the split kernel, then the resident
+// kernel over the groups' tiles (plan checked by the caller).
+static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                            const GemvGroup *g, int n, int32_t *status, void *workspace,
+                            cudaStream_t stream, bool prepared) {
+  const int64_t rows = group_tiles(g, n) * kTileRows;
+  const F4Plan P = plan_r(M, rows, K);
+  const F4Ws L = f4_ws(M, rows, K);
+  CUtensorMap mw, ms;
+  if (!weight_maps(prepared, g[0].codes, g[0].scales, g[0].N, K, mw, ms)) return cudaErrorInvalidValue;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  F4Args a = base_args(x, M, K, ldx, g, n, status, ws, L);
+  a.n_slots = P.n_slots;
+  a.sched = P.sched;
+  a.ksplit = P.ksplit;
+  a.slot_codes = ws + L.bcodes;
+  // X -> B slot images (programmatic dependent launch: may start while the
+  // previous kernel drains; it waits before reading X or writing the
+  // workspace)
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(K / kChunkK, kSplitWarps), (unsigned)M);
+    cfg.blockDim = dim3(32 * kSplitWarps);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, xsplit_slots_kernel, x, ldx, (int)M, K,
+                                             ws + L.bcodes, ws + L.sfb,
+                                             reinterpret_cast<int32_t *>(ws + L.sh));
+    if (e != cudaSuccess) return e;
+  }
+  const int cluster = P.sched == kSchedCluster ? P.ksplit : 1;
+  return prepared ? launch_pdl(gemv_f4r_kernel<true>, P.grid, kThreads, P.smem, stream, cluster,
+                               mw, ms, a)
+                  : launch_pdl(gemv_f4r_kernel<false>, P.grid, kThreads, P.smem, stream, cluster,
+                               mw, ms, a);
+}
+
 cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
                            cudaStream_t stream, bool prepared) {
-  const F4Plan P = plan_r(M, N, K);
-  if (P.ok) {
-    const F4Ws L = f4_ws(M, N, K);
-    CUtensorMap mw, ms;
-    if (!weight_maps(prepared, codes, scales, N, K, mw, ms)) return cudaErrorInvalidValue;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    F4Args a = base_args(x, M, K, ldx, tensor_scale, N, y, ldy, status, ws, L);
-    a.n_slots = P.n_slots;
-    a.sched = P.sched;
-    a.ksplit = P.ksplit;
-    a.wc = codes;
-    a.wsa = scales;
-    a.slot_codes = ws + L.bcodes;
-    // X -> B slot images (programmatic dependent launch: may start while the
-    // previous kernel drains; it waits before reading X or writing the
-    // workspace)
-    {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3((unsigned)ceil_div(K / kChunkK, kSplitWarps), (unsigned)M);
-      cfg.blockDim = dim3(32 * kSplitWarps);
-      cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      const cudaError_t e = cudaLaunchKernelEx(&cfg, xsplit_slots_kernel, x, ldx, (int)M, K,
-                                               ws + L.bcodes, ws + L.sfb,
-                                               reinterpret_cast<int32_t *>(ws + L.sh));
-      if (e != cudaSuccess) return e;
-    }
-    const int cluster = P.sched == kSchedCluster ? P.ksplit : 1;
-    return prepared ? launch_pdl(gemv_f4r_kernel<true>, P.grid, kThreads, P.smem, stream, cluster,
-                                 mw, ms, a)
-                    : launch_pdl(gemv_f4r_kernel<false>, P.grid, kThreads, P.smem, stream, cluster,
-                                 mw, ms, a);
+  if (plan_r(M, N, K).ok) {
+    const GemvGroup g = {codes, scales, tensor_scale, y, N, ldy};
+    return launch_resident(x, M, K, ldx, &g, 1, status, workspace, stream, prepared);
   }
   // every row of X in one stream of W
   return launch_pass_streamed(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status,
                               workspace, stream, prepared);
+}
+
+bool gemv_f4_grouped_ok(int64_t M, int64_t K, const GemvGroup *g, int n) {
+  if (n < 1 || n > kMaxGroups || M < 1 || M > 2 || K < 4 * kChunkK || K % kChunkK || K > (1 << 24))
+    return false;
+  for (int i = 0; i < n; ++i)
+    if (g[i].N < 1 || g[i].N > 0x7FFFFFFFll || (((uintptr_t)g[i].codes | (uintptr_t)g[i].scales) & 15u))
+      return false;
+  const int64_t tiles = group_tiles(g, n);
+  return tiles <= 0x7FFFFFFFll / kTileRows && plan_r(M, tiles * kTileRows, K).ok;
+}
+
+size_t gemv_f4_grouped_workspace_bytes(int64_t M, int64_t K, const int64_t *N, int n) {
+  int64_t tiles = 0;
+  for (int i = 0; i < n; ++i) tiles += ceil_div(N[i], kTileRows);
+  return f4_ws(M, tiles * kTileRows, K).total;
+}
+
+cudaError_t launch_gemv_f4_grouped(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                                   const GemvGroup *g, int n, int32_t *status, void *workspace,
+                                   cudaStream_t stream) {
+  return launch_resident(x, M, K, ldx, g, n, status, workspace, stream, true);
 }
 
 }  // namespace impfp4

@@ -66,6 +66,23 @@ def test_gemm_plan():
         assert pkg.imp_nvfp4_gemm_plan(*bad) == (0, None)
 
 
+def test_grouped_plan():
+    # one split + one weight stream for all groups at M <= 2 (a 0.6B-class
+    # layer's q/k/v and gate/up, a 27B-class layer's gate/up)
+    gp = pkg.imp_nvfp4_gemm_grouped_plan
+    assert gp(1, 1024, [2048, 1024, 1024]) == (2, "gemv_f4r_kernel")
+    assert gp(1, 1024, [3072, 3072]) == (2, "gemv_f4r_kernel")
+    assert gp(2, 5120, [17408, 17408]) == (2, "gemv_f4r_kernel")
+    assert gp(1, 1024, [100, 28, 1]) == (2, "gemv_f4r_kernel")  # ragged groups
+    # otherwise one imp_nvfp4_gemm_mma call per group
+    assert gp(4, 5120, [17408, 17408]) == (4, "gemv_f4_kernel")
+    assert gp(2048, 5120, [17408, 17408]) == (6, "gemm_mxf4_kernel")
+    for bad in [(1, 1024, []), (1, 1024, [128] * 5), (1, 1000, [128]), (1, 1024, [0])]:
+        assert gp(*bad) == (0, None)
+    assert pkg.imp_nvfp4_gemm_grouped_workspace_size(1, 1024, [2048, 1024, 1024]) >= \
+        pkg.imp_nvfp4_gemm_workspace_size(1, 2048, 1024)
+
+
 A16 = 0x7F0000000000  # fake, 16-byte aligned "device" addresses: never dereferenced
 
 
@@ -117,3 +134,24 @@ def test_quantize_rejects_bad_arguments():
     assert q(A16, 4, 64, 68, _t(4, 64), None, A16, 4096, None) == pkg.IMP_ERR_MISALIGNED
     assert q(A16, 4, 64, 64, _t(4, 64), None, None, 0, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL
     assert q(A16, 4, 64, 64, _t(4, 64), None, A16, 2, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_grouped_rejects_bad_arguments():
+    g = pkg.imp_nvfp4_gemm_grouped
+    G = pkg.ImpNvfp4Group
+    ok = [G(_t(2048, 1024), A16, 2048), G(_t(1024, 1024), A16, 1024)]
+    ws = pkg.imp_nvfp4_gemm_grouped_workspace_size(1, 1024, [2048, 1024])
+    assert g(A16, 1, 1024, 1024, [], None, A16, ws, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16, 1, 1024, 1024, ok * 3, None, A16, ws, None) == pkg.IMP_ERR_INVALID_ARG
+    assert g(A16, 1, 1000, 1000, ok, None, A16, ws, None) == pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    bad_k = [G(_t(2048, 1024), A16, 2048), G(_t(1024, 2048), A16, 1024)]
+    assert g(A16, 1, 1024, 1024, bad_k, None, A16, ws, None) == pkg.IMP_ERR_INVALID_ARG
+    short_ldy = [G(_t(2048, 1024), A16, 1024)]
+    assert g(A16, 1, 1024, 1024, short_ldy, None, A16, ws, None) == pkg.IMP_ERR_INVALID_ARG
+    odd_y = [G(_t(2048, 1024), A16 + 8, 2048)]
+    assert g(A16, 1, 1024, 1024, odd_y, None, A16, ws, None) == pkg.IMP_ERR_MISALIGNED
+    assert g(A16, 1, 1024, 1024, ok, None, A16, ws - 16, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    assert g(A16, 1, 1024, 1024, ok, None, None, 0, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    assert g(A16 + 8, 1, 1024, 1024, ok, None, A16, ws, None) == pkg.IMP_ERR_MISALIGNED
+    # M = 0: nothing to do
+    assert g(A16, 0, 1024, 1024, ok, None, None, 0, None) == pkg.IMP_OK
