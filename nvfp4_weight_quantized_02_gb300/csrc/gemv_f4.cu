@@ -941,17 +941,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 // sh[m].
 __global__ void __launch_bounds__(32 * kSplitWarps)
     xsplit_slots_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, uint8_t *slot_codes,
-                        uint8_t *slot_sf, int32_t *sh_out) {
+                        uint8_t *slot_sf, int32_t *sh_out, int32_t *status) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ uint4 xrow[];  // row m of X (K bf16), staged once
+  __shared__ uint64_t bar;
+  __shared__ uint32_t red[kSplitWarps];
+  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   // X may come from the previous kernel, and the previous GEMV may still
   // read the workspace: wait for it before touching either.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ uint32_t red[kSplitWarps];
-  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint16_t *xr = x + m * ldx;
+  // The row in one bulk copy: a single memory round trip, which matters
+  // because the next GEMV's weight stream is already filling the memory
+  // queues when this kernel runs.
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)(K * 2));
+    bulk_g2s(xrow, x + m * ldx, (uint32_t)(K * 2), &bar);
+  }
+  if (!mbar_wait_bounded(&bar, 0u, status)) return;
   uint32_t mx = 0;
-  for (int64_t i = threadIdx.x; i < K / 8; i += 32 * kSplitWarps)
-    mx = max(mx, absmax_bf16x8(__ldg(reinterpret_cast<const uint4 *>(xr) + i)));
+  for (int i = threadIdx.x; i < (int)(K / 8); i += 32 * kSplitWarps) mx = max(mx, absmax_bf16x8(xrow[i]));
   for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   if (lane == 0) red[warp] = mx;
   __syncthreads();
@@ -963,7 +976,7 @@ __global__ void __launch_bounds__(32 * kSplitWarps)
   const int ch = blockIdx.x * kSplitWarps + warp;
   if (ch >= (int)(K / kChunkK)) return;
   const int bb = lane >> 1, hf = lane & 1;
-  const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + (int64_t)ch * kChunkK + 16 * bb + 8 * hf));
+  const uint4 v = xrow[(ch * kChunkK + 16 * bb + 8 * hf) / 8];
   uint8_t *codes = slot_codes + (size_t)ch * 2048;
   uint8_t *sf = slot_sf + (size_t)ch * 1024;
   const float p1 = pow2f(sh / 2), p2 = pow2f(sh - sh / 2);
@@ -1067,34 +1080,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_ws);
       }
-      // processing position i -> ring slot i % NS, stage stage_of(i)
-      PreparedTile src, psrc;
-      auto load_w = [&](int i) {
-        const int s = i % kNSR;
-        uint8_t *stg = smem + (size_t)s * L::BYTES;
-        int tile, ch;
-        sk.tile_ch(sk.stage_of(i), tile, ch);
-        const int row0 = tile * kTileRows;
-        mbar_arrive_expect_tx(&bars.full[s], L::TX);
+      // processing position i -> ring slot i % NS, stage stage_of(i).  The
+      // source of a stage is worked out before its slot frees (where), so
+      // the copies go out the moment it does (issue): the slot's turnaround
+      // bounds the bytes in flight.
+      PreparedTile src;
+      struct Src {
+        const uint8_t *w, *sf;  // prepared weight
+        int ch, row0;           // row-major weight (tensor-map coordinates)
+      };
+      auto where = [&](int i) {
+        Src r;
+        int tile;
+        sk.tile_ch(sk.stage_of(i), tile, r.ch);
+        r.row0 = tile * kTileRows;
         if (PREP) {
           src.at(a, tile, sk.nch);
-          bulk_g2s(stg + L::W, src.wc + (size_t)ch * 16384, 16384u, &bars.full[s]);
-          bulk_g2s(stg + L::SFA, src.wsa + (size_t)ch * 2048, 2048u, &bars.full[s]);
+          r.w = src.wc + (size_t)r.ch * 16384;
+          r.sf = src.wsa + (size_t)r.ch * 2048;
+        }
+        return r;
+      };
+      auto issue = [&](int i, const Src &r) {
+        const int s = i % kNSR;
+        uint8_t *stg = smem + (size_t)s * L::BYTES;
+        mbar_arrive_expect_tx(&bars.full[s], L::TX);
+        if (PREP) {
+          bulk_g2s(stg + L::W, r.w, 16384u, &bars.full[s]);
+          bulk_g2s(stg + L::SFA, r.sf, 2048u, &bars.full[s]);
         } else {
-          tma_load_2d(stg + L::W, &tm_w, ch * (kChunkK / 2), row0, &bars.full[s]);
-          tma_load_2d(stg + L::RAW, &tm_ws, ch * (kChunkK / 16), row0, &bars.full[s]);
+          tma_load_2d(stg + L::W, &tm_w, r.ch * (kChunkK / 2), r.row0, &bars.full[s]);
+          tma_load_2d(stg + L::RAW, &tm_ws, r.ch * (kChunkK / 16), r.row0, &bars.full[s]);
         }
       };
       // The ring alone keeps W in flight: an extra L2 prefetch at the start
       // only lengthened the queues every later access (X, B, the fix-ups)
       // waits in.
       const int pre = min(kNSR, sk.n_st);
-      for (int i = 0; i < pre; ++i) load_w(i);
+      for (int i = 0; i < pre; ++i) issue(i, where(i));
       int i = pre;
       for (; i < sk.n_st; ++i) {
         const int s = i % kNSR;
+        const Src r = where(i);
         if (!mbar_wait_bounded(&bars.empty[s], (uint32_t)((i / kNSR - 1) & 1), a.status)) break;
-        load_w(i);
+        issue(i, r);
       }
       for (int k = (i > kNSR ? i - kNSR : 0); k < i; ++k)
         mbar_wait_bounded(&bars.full[k % kNSR], (uint32_t)((k / kNSR) & 1), a.status);
@@ -1231,7 +1260,8 @@ F4Plan plan_r(int64_t M, int64_t N, int64_t K) {
   const size_t red = p.sched == kSchedCluster ? (size_t)(p.ksplit - 1) * kTileRows * 2 * sizeof(float) : 0;
   p.smem = (size_t)kNSR * StageR::BYTES + (size_t)p.n_slots * (2048 + 1024) + 256 +
            ((sizeof(F4Bars) + 15) & ~size_t(15)) + red + 1024;
-  p.ok = M <= 2 && p.n_slots <= kMaxSlotsR;
+  // the split kernel stages a row of X (2 K bytes) in shared memory
+  p.ok = M <= 2 && p.n_slots <= kMaxSlotsR && K * 2 <= 200 * 1024;
   return p;
 }
 
@@ -1444,9 +1474,16 @@ static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int6
   // previous kernel drains; it waits before reading X or writing the
   // workspace)
   {
+    const size_t xs_bytes = (size_t)K * 2;  // the staged row
+    if (xs_bytes > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          xsplit_slots_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xs_bytes);
+      if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ceil_div(K / kChunkK, kSplitWarps), (unsigned)M);
     cfg.blockDim = dim3(32 * kSplitWarps);
+    cfg.dynamicSmemBytes = xs_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1455,7 +1492,7 @@ static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int6
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, xsplit_slots_kernel, x, ldx, (int)M, K,
                                              ws + L.bcodes, ws + L.sfb,
-                                             reinterpret_cast<int32_t *>(ws + L.sh));
+                                             reinterpret_cast<int32_t *>(ws + L.sh), status);
     if (e != cudaSuccess) return e;
   }
   const int cluster = P.sched == kSchedCluster ? P.ksplit : 1;
