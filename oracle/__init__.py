@@ -20,6 +20,17 @@ Functions and what pins them (tests/test_oracle.py):
   rational brute force on tiny shapes and closed forms.
 * ``reference_gemm`` -- Y = Xhat W^T with Xhat = X for M <= 16 and
   dequant(quantize(X)) for M > 16.
+* ``e8m0_value`` / ``mx_quantize`` / ``mx_dequant`` -- MXFP4 (OCP MX v1.0:
+  32-element blocks, E8M0 scale 2^(floor(log2 amax) - 2), E2M1 elements).
+  Pinned by hand-worked blocks (tests/golden/mx_*.txt), by all 255 finite
+  E8M0 bytes against torch.float8_e8m0fnu where torch has it and against
+  powers of two, and by the definition's invariants (the scale is the
+  largest power of two that keeps the block max below 8 times it; no code
+  but the clipped ones errs by more than half an E2M1 step).
+* ``fp8_tensor_scale`` / ``fp8_quantize_rows`` / ``fp8_quantize`` /
+  ``fp8_dequant`` -- FP8 E4M3 weights with one fp32 scale g/448.  Pinned by
+  hand-worked values (tests/golden/fp8_*.txt) and by torch's fp8 cast of
+  x / s8 (the same correctly rounded division).
 """
 from __future__ import annotations
 
@@ -75,6 +86,18 @@ def _load():
     lib.orc_bf16_to_f64.argtypes = [P, I64, P]
     lib.orc_matmul_abt.restype = None
     lib.orc_matmul_abt.argtypes = [P, I64, P, I64, I64, P, P]
+    lib.orc_e8m0_value.restype = ctypes.c_double
+    lib.orc_e8m0_value.argtypes = [ctypes.c_uint8]
+    lib.orc_mx_quantize.restype = ctypes.c_int
+    lib.orc_mx_quantize.argtypes = [P, I64, I64, I64, P, P]
+    lib.orc_mx_dequant.restype = None
+    lib.orc_mx_dequant.argtypes = [P, P, I64, I64, P]
+    lib.orc_fp8_tensor_scale.restype = ctypes.c_int
+    lib.orc_fp8_tensor_scale.argtypes = [P, I64, I64, I64, P]
+    lib.orc_fp8_quantize_rows.restype = None
+    lib.orc_fp8_quantize_rows.argtypes = [P, I64, I64, I64, F, P]
+    lib.orc_fp8_dequant.restype = None
+    lib.orc_fp8_dequant.argtypes = [P, F, I64, P]
     _lib = lib
     return lib
 
@@ -211,3 +234,78 @@ def tight_tolerance(bound: np.ndarray, y_ref: np.ndarray) -> np.ndarray:
     fp32: one bf16 ulp of y_ref plus 2^-14 * sum|x w| (room for ~1000 fp32
     roundings).  A dropped or doubled block moves y by far more than this."""
     return bf16_ulp(y_ref) + 2.0 ** -14 * bound + 1e-30
+
+
+# ---- MXFP4 -------------------------------------------------------------------
+
+def e8m0_value(byte: int) -> float:
+    return _load().orc_e8m0_value(byte)
+
+
+def mx_quantize(x_bf16: np.ndarray) -> tuple[np.ndarray, np.ndarray, bool]:
+    """[rows, K] uint16 -> (codes [rows, K/2], E8M0 scales [rows, K/32], nonfinite flag)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, K = x.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    codes = np.empty((rows, K // 2), np.uint8)
+    scales = np.empty((rows, K // 32), np.uint8)
+    bad = _load().orc_mx_quantize(_ptr(x), rows, K, K, _ptr(codes), _ptr(scales))
+    return codes, scales, bool(bad)
+
+
+def mx_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """fp64 [rows, K] values e2m1 * 2^(scale - 127)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, K = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((rows, K), np.float64)
+    _load().orc_mx_dequant(_ptr(codes), _ptr(scales), rows, K, _ptr(out))
+    return out
+
+
+def mx_reference_gemm(x_bf16: np.ndarray, M_total: int, w_codes: np.ndarray,
+                      w_scales: np.ndarray, s_x: float | None = None):
+    """(y_ref, bound) for rows of X against rows of an MXFP4 weight, in fp64
+    (X as in reference_gemm: bf16 for M <= 16, its NVFP4 quantization for
+    larger M)."""
+    return matmul_abt(activation_hat(x_bf16, M_total, s_x), mx_dequant(w_codes, w_scales))
+
+
+# ---- FP8 E4M3 weights ----------------------------------------------------------
+
+def fp8_tensor_scale(x_bf16: np.ndarray) -> tuple[float, bool]:
+    """(s8 = global amax / 448, nonfinite flag)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, K = x.shape
+    s = np.zeros(1, np.float32)
+    bad = _load().orc_fp8_tensor_scale(_ptr(x), rows, K, K, _ptr(s))
+    return float(s[0]), bool(bad)
+
+
+def fp8_quantize_rows(x_bf16: np.ndarray, s8: float) -> np.ndarray:
+    """E4M3 codes [rows, K] of x / s8."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, K = x.shape
+    codes = np.empty((rows, K), np.uint8)
+    _load().orc_fp8_quantize_rows(_ptr(x), rows, K, K, np.float32(s8), _ptr(codes))
+    return codes
+
+
+def fp8_quantize(x_bf16: np.ndarray) -> tuple[np.ndarray, float, bool]:
+    """Whole tensor -> (codes [rows, K], s8, nonfinite flag)."""
+    s8, bad = fp8_tensor_scale(x_bf16)
+    return fp8_quantize_rows(x_bf16, s8), s8, bad
+
+
+def fp8_dequant(codes: np.ndarray, s8: float) -> np.ndarray:
+    """fp64 values e4m3(code) * s8, same shape as codes."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().orc_fp8_dequant(_ptr(c), np.float32(s8), c.size, _ptr(out))
+    return out
+
+
+def fp8_reference_gemm(x_bf16: np.ndarray, w_codes: np.ndarray, s8: float):
+    """(y_ref, bound) for a decode-sized X against an FP8 weight, in fp64."""
+    return matmul_abt(bf16_to_f64(x_bf16), fp8_dequant(w_codes, s8))

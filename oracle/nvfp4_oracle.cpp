@@ -28,6 +28,22 @@
 //    code 0x8) except in blocks with d == 0, which are all 0x0.
 //  * g == 0 gives s = 0, every block scale 0x00 and every code 0x0.
 //  * Element 2i of a row is the low nibble of byte i, element 2i+1 the high one.
+//
+// Two more weight formats of the imp README's feature matrix (quantisation:
+// "NVFP4 (native, the primary path), MXFP4, ... FP8 E4M3 weights"):
+//  * MXFP4, as the OCP Microscaling Formats (MX) v1.0 define it: 32-element
+//    blocks along K, one E8M0 scale per block (the byte b stands for
+//    2^(b - 127); 0xFF is NaN and never produced), E2M1 elements, no tensor
+//    scale.  Conversion per the MX specification: shared exponent
+//    e = floor(log2(block amax)) - 2 (2 = the largest exponent of E2M1),
+//    clamped to [-127, 127]; element code = E2M1(x / 2^e), round to nearest
+//    even, saturating at 6.  Readings: an all-zero block takes e = -127
+//    (byte 0x00); the sign of a code is copied from x; x / 2^e is one IEEE
+//    fp32 division (exact but for underflow far below the E2M1 grid).
+//  * FP8 E4M3 weights: one fp32 scale per tensor, s8 = global amax / 448
+//    (the same recipe as the NVFP4 tensor scale, with 448 the largest E4M3
+//    value), code = E4M3(x / s8), round to nearest even, saturating at 448,
+//    sign copied from x; s8 == 0 gives all codes 0x00.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -124,6 +140,55 @@ void quantize_row(const uint16_t *x, int64_t K, float s, uint8_t *codes, uint8_t
   }
 }
 
+// ---- MXFP4 ------------------------------------------------------------------
+
+double e8m0_value(uint8_t b) {
+  if (b == 255) return std::nan("");
+  return std::ldexp(1.0, (int)b - 127);
+}
+
+// Shared exponent of a block with largest magnitude a (finite, >= 0).
+int mx_shared_exponent(float a) {
+  if (a == 0.0f) return -127;
+  int ex;
+  std::frexp((double)a, &ex);  // a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1
+  int e = (ex - 1) - 2;
+  return std::min(127, std::max(-127, e));
+}
+
+void mx_quantize_row(const uint16_t *x, int64_t K, uint8_t *codes, uint8_t *scales) {
+  for (int64_t b = 0; b < K / 32; ++b) {
+    float xs[32];
+    float a = 0.0f;
+    for (int j = 0; j < 32; ++j) {
+      xs[j] = bf16_to_f32(x[32 * b + j]);
+      a = std::max(a, std::fabs(xs[j]));
+    }
+    const int e = mx_shared_exponent(a);
+    scales[b] = (uint8_t)(e + 127);
+    const float X = std::ldexp(1.0f, e);  // 2^e, exact (2^-127 is a subnormal float)
+    uint8_t c[32];
+    for (int j = 0; j < 32; ++j) {
+      float q = div_rn(xs[j], X);
+      uint8_t sign = std::signbit(xs[j]) ? 8 : 0;
+      c[j] = (uint8_t)(sign | e2m1_encode_mag(std::fabs(q)));
+    }
+    for (int j = 0; j < 16; ++j) codes[16 * b + j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
+  }
+}
+
+// ---- FP8 E4M3 weights -------------------------------------------------------
+
+void fp8_quantize_row(const uint16_t *x, int64_t K, float s, uint8_t *codes) {
+  for (int64_t k = 0; k < K; ++k) {
+    if (s == 0.0f) { codes[k] = 0; continue; }
+    float v = bf16_to_f32(x[k]);
+    float q = div_rn(v, s);
+    uint8_t sign = std::signbit(v) ? 0x80 : 0;
+    codes[k] = (uint8_t)(sign | e4m3_encode_nonneg(std::fabs(q)));
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -179,6 +244,57 @@ void orc_dequant(const uint8_t *codes, const uint8_t *scales, float s, int64_t r
       uint8_t c = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
       out[r * K + k] = e2m1_value(c) * e4m3_value(scales[r * (K / 16) + k / 16]) * (double)s;
     }
+}
+
+double orc_e8m0_value(uint8_t b) { return e8m0_value(b); }
+
+// MXFP4 quantizer: codes [rows][K/2], E8M0 scales [rows][K/32].  Returns 1
+// if any element is NaN or Inf (outputs then unspecified), else 0.
+int orc_mx_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ld, uint8_t *codes,
+                    uint8_t *scales) {
+  int bad = 0;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t k = 0; k < K; ++k)
+      if (!std::isfinite(bf16_to_f32(x[r * ld + k]))) bad = 1;
+    mx_quantize_row(x + r * ld, K, codes + r * (K / 2), scales + r * (K / 32));
+  }
+  return bad;
+}
+
+// MXFP4 dequant: w[r][k] = e2m1(code) * 2^(scale - 127), fp64 (exact).
+void orc_mx_dequant(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t K,
+                    double *out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t k = 0; k < K; ++k) {
+      uint8_t byte = codes[r * (K / 2) + k / 2];
+      uint8_t c = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
+      out[r * K + k] = e2m1_value(c) * e8m0_value(scales[r * (K / 32) + k / 32]);
+    }
+}
+
+// FP8 tensor scale s8 = g / 448.  Returns 1 on NaN/Inf, else 0.
+int orc_fp8_tensor_scale(const uint16_t *x, int64_t rows, int64_t K, int64_t ld, float *s8) {
+  float g = 0.0f;
+  int bad = 0;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t k = 0; k < K; ++k) {
+      float v = bf16_to_f32(x[r * ld + k]);
+      if (!std::isfinite(v)) bad = 1;
+      else g = std::max(g, std::fabs(v));
+    }
+  *s8 = div_rn(g, 448.0f);
+  return bad;
+}
+
+// FP8 codes [rows][K] with a given tensor scale.
+void orc_fp8_quantize_rows(const uint16_t *x, int64_t rows, int64_t K, int64_t ld, float s,
+                           uint8_t *codes) {
+  for (int64_t r = 0; r < rows; ++r) fp8_quantize_row(x + r * ld, K, s, codes + r * K);
+}
+
+// FP8 dequant: w = e4m3(code) * s, fp64 (exact).
+void orc_fp8_dequant(const uint8_t *codes, float s, int64_t n, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]) * (double)s;
 }
 
 // bf16 bit patterns -> fp64.

@@ -44,3 +44,39 @@ def load(path):
 
 def all_cases():
     return [load(p) for p in sorted(glob.glob(os.path.join(GOLDEN_DIR, "*.txt")))]
+
+
+def _num(tok: str) -> float:
+    return float.fromhex(tok) if ("0x" in tok or "p" in tok) else float(tok)
+
+
+def load_format(path):
+    """A fixture of tests/golden/mxfp4/ or tests/golden/fp8/: rows x<r>,
+    optional tensor_scale, per-row scales<r> and codes<r> (hex bytes);
+    decimal or hex-float values."""
+    case = {"name": os.path.basename(path), "x": {}, "scales": {}, "codes": {}}
+    for raw in open(path):
+        line = raw.split("#", 1)[0].strip()
+        if not line:
+            continue
+        key, val = [p.strip() for p in line.split(":", 1)]
+        if key == "K":
+            case["K"] = int(val)
+        elif key == "tensor_scale":
+            case["tensor_scale"] = _num(val)
+        elif key.startswith("x"):
+            case["x"][int(key[1:])] = [_num(v) for v in val.split()]
+        elif key.startswith("scales"):
+            case["scales"][int(key[6:])] = bytes(int(v, 16) for v in val.split())
+        elif key.startswith("codes"):
+            case["codes"][int(key[5:])] = bytes(int(v, 16) for v in val.split())
+    rows = sorted(case["x"])
+    case["X"] = np.stack([bf16_bits(case["x"][r]) for r in rows])
+    case["codes_arr"] = np.stack([np.frombuffer(case["codes"][r], np.uint8) for r in rows])
+    if case["scales"]:
+        case["scales_arr"] = np.stack([np.frombuffer(case["scales"][r], np.uint8) for r in rows])
+    return case
+
+
+def format_cases(fmt):
+    return [load_format(p) for p in sorted(glob.glob(os.path.join(GOLDEN_DIR, fmt, "*.txt")))]
