@@ -675,6 +675,63 @@ def bench_grouped_layer(pkg, dev, stream, status, lins, copies, ncopy, ins, ys, 
     return res
 
 
+def bench_weight_formats(args, pkg, dev, stream, hbm_peak, lins, status):
+    """The decode step (same shapes and dataflow) on the README's other
+    weight formats: MXFP4 weights converted once to the NVFP4 form (so the
+    step streams the same 0.5625 B per weight as the NVFP4 step; the MXFP4
+    format itself is 0.53125 B), and FP8 E4M3 weights (1 B per weight)
+    through imp_fp8_gemm."""
+    import torch
+
+    out = {}
+    n = max(args.steps, 50)
+    mx_w, f8_w = [], []
+    for l in lins:
+        wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+        mx_w.append(pkg.prepare_mma(pkg.mxfp4_to_nvfp4(pkg.mxfp4_quantize(wb, dev_status=status),
+                                                       dev_status=status)))
+        f8_w.append(pkg.fp8_quantize(wb, dev_status=status))
+        del wb
+    xs = [torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev) for l in lins]
+    ys = [torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev) for l in lins]
+    chained = chain_inputs(lins, xs, ys)
+    wss = [torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K),
+                           pkg.imp_fp8_gemm_workspace_size(l.M, l.N, l.K), 16),
+                       dtype=torch.uint8, device=dev) for l in lins]
+    torch.cuda.synchronize()
+
+    def mx_step():
+        for x, w, y, ws in zip(chained, mx_w, ys, wss):
+            pkg.gemm_mma(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
+
+    def f8_step():
+        for x, w, y, ws in zip(chained, f8_w, ys, wss):
+            pkg.gemm_fp8(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
+
+    mx_bytes = sum(l.N * l.K // 2 + l.N * l.K // 32 + 2 * l.M * (l.K + l.N) for l in lins)
+    nv_bytes = step_bytes(lins)
+    f8_bytes = sum(l.N * l.K + 4 + 2 * l.M * (l.K + l.N) for l in lins)
+    for name, fn, nbytes, extra in (
+            ("decode_mxfp4_weights", mx_step, nv_bytes,
+             {"weights": "MXFP4 (OCP MX) quantized, converted once to NVFP4 form and prepared",
+              "mxfp4_format_bytes_per_step": mx_bytes}),
+            ("decode_fp8_weights", f8_step, f8_bytes,
+             {"weights": "FP8 E4M3, one fp32 tensor scale, row-major (imp_fp8_gemm)",
+              "kernels": [pkg.imp_fp8_gemm_plan(l.M, l.N, l.K) for l in lins]})):
+        for _ in range(args.warmup):
+            fn()
+        ts = time_blocks(fn, n, 10, stream)
+        med = statistics.median(ts)
+        out[name] = {"us_per_step": spread(ts), "bytes_per_step": nbytes,
+                     "GB/s": nbytes / (med * 1e-6) / 1e9,
+                     "frac_of_hbm_peak": nbytes / (med * 1e-6) / 1e9 / hbm_peak, **extra}
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the weight-format steps")
+    del mx_w, f8_w
+    return out
+
+
 def bench_prefill(args, pkg, dev, stream):
     """Prefill GEMMs (M = 2048): the block-scaled FP4 tensor-core GEMM alone
     (X already quantized, W in the MMA layout) and the whole imp_nvfp4_gemm
@@ -784,6 +841,7 @@ def bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs, ch
     except Exception as e:  # report, do not fail the benchmark line
         out["decode_graph_replay"] = {"error": str(e)[:200]}
 
+    out.update(bench_weight_formats(args, pkg, dev, stream, hbm_peak, lins, status))
     out["small_configs"] = bench_small_configs(pkg, dev, stream, hbm_peak, status)
     out["prefill"] = bench_prefill(args, pkg, dev, stream)
 

@@ -76,7 +76,9 @@ typedef enum {
 enum {
   IMP_DEV_OK = 0,
   IMP_DEV_NONFINITE_INPUT = 1, /* a NaN or Inf in a tensor being quantized; outputs unspecified */
-  IMP_DEV_TIMEOUT = 2          /* a bounded in-kernel wait gave up; outputs unspecified */
+  IMP_DEV_TIMEOUT = 2,         /* a bounded in-kernel wait gave up; outputs unspecified */
+  IMP_DEV_RANGE = 4            /* imp_mxfp4_to_nvfp4: a block's scale is too far below the
+                                  largest to be exact in NVFP4; outputs unspecified */
 };
 
 /* An NVFP4 tensor of `rows` x `K` elements (device pointers, caller-owned):
@@ -310,6 +312,85 @@ imp_status imp_nvfp4_gemm_grouped(const void *x_bf16, int64_t M, int64_t K, int6
                                   const imp_nvfp4_group *groups, int32_t n_groups,
                                   int32_t *dev_status, void *workspace, size_t ws_bytes,
                                   void *stream);
+
+/* ---- other weight formats ---------------------------------------------------
+ * The imp README's feature matrix lists, besides NVFP4 (the primary path),
+ * MXFP4 and FP8 E4M3 weights.                                              */
+
+/* MXFP4 tensor (OCP Microscaling Formats v1.0): rows x K elements, K % 32 == 0.
+ *   codes   uint8[rows][K/2]   packed E2M1 codes, low nibble = even element
+ *   scales  uint8[rows][K/32]  E8M0 block scales: byte b stands for 2^(b - 127) */
+typedef struct {
+  uint8_t *codes;
+  uint8_t *scales;
+  int64_t rows;
+  int64_t K;
+} imp_mxfp4_tensor;
+
+/* Quantize a bf16 matrix to MXFP4 as the MX specification converts: per
+ * 32-element block, shared exponent e = floor(log2(block amax)) - 2 clamped
+ * to [-127, 127] (an all-zero block takes -127), scale byte e + 127, codes
+ * E2M1(x / 2^e) rounded to nearest even and saturating at 6, sign copied
+ * from x.  Bit-exact.  rows >= 1, K % 32 == 0, ldx >= K, ldx % 8 == 0; no
+ * workspace.  NaN/Inf sets IMP_DEV_NONFINITE_INPUT.                        */
+imp_status imp_mxfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                              const imp_mxfp4_tensor *out, int32_t *dev_status, void *stream);
+
+/* Bytes of workspace imp_mxfp4_to_nvfp4 needs (one scratch word). */
+size_t imp_mxfp4_to_nvfp4_workspace_size(void);
+
+/* The same values in NVFP4 form, for the NVFP4 kernels (an addition of this
+ * library: MXFP4 weights are served by converting them once at load, like
+ * imp_nvfp4_prepare_mma).  Exact: each 16-element half of a block keeps the
+ * codes and gets the E4M3 scale 2^(e - t), with the fp32 tensor scale 2^t,
+ * t = (the largest e among halves with a nonzero code) - 8; halves whose
+ * codes are all zero get scale 0.  Exact whenever every such e is at least
+ * t - 9, i.e. no nonzero half sits more than 2^17 below the largest; one
+ * that does sets IMP_DEV_RANGE.
+ *   in    MXFP4 tensor, rows >= 1, K % 64 == 0.
+ *   out   NVFP4 tensor of the same rows and K (row-major layout); out->codes
+ *         may equal in->codes (then the codes are not copied).           */
+imp_status imp_mxfp4_to_nvfp4(const imp_mxfp4_tensor *in, const imp_nvfp4_tensor *out,
+                              int32_t *dev_status, void *workspace, size_t ws_bytes,
+                              void *stream);
+
+/* FP8 E4M3 weight tensor: codes uint8[rows][K] (OCP FP8 E4M3 "fn"), one fp32
+ * tensor scale s8; element value = e4m3(code) * s8.                        */
+typedef struct {
+  uint8_t *codes;
+  float *tensor_scale;
+  int64_t rows;
+  int64_t K;
+} imp_fp8_tensor;
+
+/* Workspace of imp_fp8_quantize (per-CTA partial maxima). */
+size_t imp_fp8_quantize_workspace_size(int64_t rows, int64_t K);
+
+/* Quantize a bf16 matrix to FP8 E4M3 with one tensor scale: s8 = global
+ * amax / 448 (fp32 division), code = E4M3(x / s8) rounded to nearest even,
+ * saturating at 448, sign copied from x; s8 = 0 gives all codes 0.
+ * Bit-exact.  rows >= 1, K % 16 == 0, ldx >= K, ldx % 8 == 0.             */
+imp_status imp_fp8_quantize(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                            const imp_fp8_tensor *out, int32_t *dev_status, void *workspace,
+                            size_t ws_bytes, void *stream);
+
+/* Workspace of imp_fp8_gemm (0 for shapes it rejects). */
+size_t imp_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* Kernels one imp_fp8_gemm call launches (0: rejected) and the name of the
+ * weight-streaming kernel.  Host only. */
+int32_t imp_fp8_gemm_plan(int64_t M, int64_t N, int64_t K, const char **kernel);
+
+/* Decode GEMV / skinny GEMM on FP8 weights: Y = X * W^T with
+ * w[n][k] = e4m3(code) * s8, X bf16, fp32 accumulation, bf16 Y.
+ *   1 <= M <= 16 (M = 0: nothing to do); K % 128 == 0, K >= 512; N >= 128.
+ *   The weight is fed to the FP8 tensor cores (tcgen05.mma kind::f8f6f4)
+ *   unchanged; X is split per call into eight E4M3 components (exact
+ *   products, fp32 sums), in passes of two rows of X.
+ *   Accuracy and the other conventions as for imp_nvfp4_gemm.             */
+imp_status imp_fp8_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                        const imp_fp8_tensor *w, void *y_bf16, int64_t ldy, int32_t *dev_status,
+                        void *workspace, size_t ws_bytes, void *stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *imp_status_string(imp_status status);

@@ -32,6 +32,11 @@ __all__ = [
     "quantize_mma", "gemm_fp4", "gemm_mma", "imp_selftest_bounded_wait",
     "ImpNvfp4Group", "IMP_NVFP4_MAX_GROUPS", "imp_nvfp4_gemm_grouped",
     "imp_nvfp4_gemm_grouped_workspace_size", "imp_nvfp4_gemm_grouped_plan", "gemm_grouped",
+    "IMP_DEV_RANGE", "ImpMxfp4Tensor", "ImpFp8Tensor", "imp_mxfp4_quantize",
+    "imp_mxfp4_to_nvfp4", "imp_mxfp4_to_nvfp4_workspace_size", "imp_fp8_quantize",
+    "imp_fp8_quantize_workspace_size", "imp_fp8_gemm", "imp_fp8_gemm_workspace_size",
+    "imp_fp8_gemm_plan", "MXFP4Tensor", "FP8Tensor", "mxfp4_quantize", "mxfp4_to_nvfp4",
+    "fp8_quantize", "gemm_fp8",
 ]
 
 IMP_OK = 0
@@ -43,6 +48,7 @@ IMP_ERR_CUDA = 5
 IMP_DEV_OK = 0
 IMP_DEV_NONFINITE_INPUT = 1
 IMP_DEV_TIMEOUT = 2
+IMP_DEV_RANGE = 4
 DECODE_M_MAX = 16
 IMP_NVFP4_MAX_GROUPS = 4
 
@@ -55,6 +61,18 @@ class ImpNvfp4Tensor(ctypes.Structure):
 class ImpNvfp4Group(ctypes.Structure):
     """ctypes mirror of imp_nvfp4_group."""
     _fields_ = [("w", ImpNvfp4Tensor), ("y_bf16", ctypes.c_void_p), ("ldy", ctypes.c_int64)]
+
+
+class ImpMxfp4Tensor(ctypes.Structure):
+    """ctypes mirror of imp_mxfp4_tensor."""
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("K", ctypes.c_int64)]
+
+
+class ImpFp8Tensor(ctypes.Structure):
+    """ctypes mirror of imp_fp8_tensor."""
+    _fields_ = [("codes", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 _lib = None
@@ -111,6 +129,23 @@ def _L():
     lib.imp_nvfp4_gemm_grouped.restype = ctypes.c_int
     lib.imp_nvfp4_gemm_grouped.argtypes = [P, I64, I64, I64, ctypes.POINTER(ImpNvfp4Group),
                                            ctypes.c_int32, P, P, SZ, P]
+    MX, F8 = ctypes.POINTER(ImpMxfp4Tensor), ctypes.POINTER(ImpFp8Tensor)
+    lib.imp_mxfp4_quantize.restype = ctypes.c_int
+    lib.imp_mxfp4_quantize.argtypes = [P, I64, I64, I64, MX, P, P]
+    lib.imp_mxfp4_to_nvfp4_workspace_size.restype = SZ
+    lib.imp_mxfp4_to_nvfp4_workspace_size.argtypes = []
+    lib.imp_mxfp4_to_nvfp4.restype = ctypes.c_int
+    lib.imp_mxfp4_to_nvfp4.argtypes = [MX, ctypes.POINTER(ImpNvfp4Tensor), P, P, SZ, P]
+    lib.imp_fp8_quantize_workspace_size.restype = SZ
+    lib.imp_fp8_quantize_workspace_size.argtypes = [I64, I64]
+    lib.imp_fp8_quantize.restype = ctypes.c_int
+    lib.imp_fp8_quantize.argtypes = [P, I64, I64, I64, F8, P, P, SZ, P]
+    lib.imp_fp8_gemm_workspace_size.restype = SZ
+    lib.imp_fp8_gemm_workspace_size.argtypes = [I64, I64, I64]
+    lib.imp_fp8_gemm_plan.restype = ctypes.c_int32
+    lib.imp_fp8_gemm_plan.argtypes = [I64, I64, I64, ctypes.POINTER(ctypes.c_char_p)]
+    lib.imp_fp8_gemm.restype = ctypes.c_int
+    lib.imp_fp8_gemm.argtypes = [P, I64, I64, I64, F8, P, I64, P, P, SZ, P]
     _lib = lib
     return lib
 
@@ -238,6 +273,49 @@ def imp_nvfp4_gemm_grouped(x_bf16: int, M: int, K: int, ldx: int, groups: list[I
     arr = (ImpNvfp4Group * len(groups))(*groups)
     return _L().imp_nvfp4_gemm_grouped(x_bf16, M, K, ldx, arr, len(groups), dev_status,
                                        workspace, ws_bytes, stream)
+
+
+def imp_mxfp4_quantize(x_bf16: int, rows: int, K: int, ldx: int, out: ImpMxfp4Tensor,
+                       dev_status: int | None, stream: int | None) -> int:
+    return _L().imp_mxfp4_quantize(x_bf16, rows, K, ldx, ctypes.byref(out), dev_status, stream)
+
+
+def imp_mxfp4_to_nvfp4_workspace_size() -> int:
+    return _L().imp_mxfp4_to_nvfp4_workspace_size()
+
+
+def imp_mxfp4_to_nvfp4(t: ImpMxfp4Tensor, out: ImpNvfp4Tensor, dev_status: int | None,
+                       workspace: int | None, ws_bytes: int, stream: int | None) -> int:
+    return _L().imp_mxfp4_to_nvfp4(ctypes.byref(t), ctypes.byref(out), dev_status, workspace,
+                                   ws_bytes, stream)
+
+
+def imp_fp8_quantize_workspace_size(rows: int, K: int) -> int:
+    return _L().imp_fp8_quantize_workspace_size(rows, K)
+
+
+def imp_fp8_quantize(x_bf16: int, rows: int, K: int, ldx: int, out: ImpFp8Tensor,
+                     dev_status: int | None, workspace: int | None, ws_bytes: int,
+                     stream: int | None) -> int:
+    return _L().imp_fp8_quantize(x_bf16, rows, K, ldx, ctypes.byref(out), dev_status, workspace,
+                                 ws_bytes, stream)
+
+
+def imp_fp8_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return _L().imp_fp8_gemm_workspace_size(M, N, K)
+
+
+def imp_fp8_gemm_plan(M: int, N: int, K: int) -> tuple[int, str | None]:
+    name = ctypes.c_char_p()
+    n = _L().imp_fp8_gemm_plan(M, N, K, ctypes.byref(name))
+    return n, (name.value.decode() if name.value else None)
+
+
+def imp_fp8_gemm(x_bf16: int, M: int, K: int, ldx: int, w: ImpFp8Tensor, y_bf16: int, ldy: int,
+                 dev_status: int | None, workspace: int | None, ws_bytes: int,
+                 stream: int | None) -> int:
+    return _L().imp_fp8_gemm(x_bf16, M, K, ldx, ctypes.byref(w), y_bf16, ldy, dev_status,
+                             workspace, ws_bytes, stream)
 
 
 class ImpError(RuntimeError):
@@ -430,3 +508,108 @@ def gemm_grouped(x, ws: list, ys=None, dev_status=None, stream=None, workspace=N
     if st != IMP_OK:
         raise ImpError(st, "imp_nvfp4_gemm_grouped")
     return ys
+
+
+# ---- MXFP4 and FP8 weights ----------------------------------------------------------
+
+@dataclass
+class MXFP4Tensor:
+    """Device MXFP4 tensor: codes uint8[rows][K/2], E8M0 scales uint8[rows][K/32]."""
+    codes: "object"
+    scales: "object"
+
+    @property
+    def rows(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.codes.shape[1] * 2
+
+    def c_struct(self) -> ImpMxfp4Tensor:
+        return ImpMxfp4Tensor(self.codes.data_ptr(), self.scales.data_ptr(), self.rows, self.K)
+
+
+@dataclass
+class FP8Tensor:
+    """Device FP8 E4M3 weight: codes uint8[rows][K], tensor_scale float32[1]."""
+    codes: "object"
+    tensor_scale: "object"
+
+    @property
+    def rows(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.codes.shape[1]
+
+    def c_struct(self) -> ImpFp8Tensor:
+        return ImpFp8Tensor(self.codes.data_ptr(), self.tensor_scale.data_ptr(), self.rows, self.K)
+
+
+def mxfp4_quantize(x, dev_status=None, stream=None) -> MXFP4Tensor:
+    """Quantize a 2-D bf16 CUDA tensor to MXFP4 (OCP MX v1.0)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, K = x.shape
+    out = MXFP4Tensor(torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device),
+                      torch.empty((rows, K // 32), dtype=torch.uint8, device=x.device))
+    st = imp_mxfp4_quantize(x.data_ptr(), rows, K, x.stride(0), out.c_struct(),
+                            None if dev_status is None else dev_status.data_ptr(),
+                            _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_mxfp4_quantize")
+    return out
+
+
+def mxfp4_to_nvfp4(t: MXFP4Tensor, dev_status=None, stream=None) -> NVFP4Tensor:
+    """The same values as an NVFP4 tensor (row-major) for the NVFP4 kernels."""
+    import torch
+    out = NVFP4Tensor(torch.empty_like(t.codes),
+                      torch.empty((t.rows, t.K // 16), dtype=torch.uint8, device=t.codes.device),
+                      torch.empty(1, dtype=torch.float32, device=t.codes.device))
+    wsb = imp_mxfp4_to_nvfp4_workspace_size()
+    ws = torch.empty(wsb, dtype=torch.uint8, device=t.codes.device)
+    st = imp_mxfp4_to_nvfp4(t.c_struct(), out.c_struct(),
+                            None if dev_status is None else dev_status.data_ptr(), ws.data_ptr(),
+                            wsb, _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_mxfp4_to_nvfp4")
+    return out
+
+
+def fp8_quantize(x, dev_status=None, stream=None) -> FP8Tensor:
+    """Quantize a 2-D bf16 CUDA tensor to FP8 E4M3 with one tensor scale."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, K = x.shape
+    out = FP8Tensor(torch.empty((rows, K), dtype=torch.uint8, device=x.device),
+                    torch.empty(1, dtype=torch.float32, device=x.device))
+    wsb = imp_fp8_quantize_workspace_size(rows, K)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=x.device)
+    st = imp_fp8_quantize(x.data_ptr(), rows, K, x.stride(0), out.c_struct(),
+                          None if dev_status is None else dev_status.data_ptr(), ws.data_ptr(),
+                          wsb, _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_fp8_quantize")
+    return out
+
+
+def gemm_fp8(x, w: FP8Tensor, y=None, dev_status=None, stream=None, workspace=None):
+    """Y = X W^T for a decode-sized bf16 X and an FP8 E4M3 weight."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    N = w.rows
+    if y is None:
+        y = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=x.device)[:, :N]
+    wsb = imp_fp8_gemm_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 16), dtype=torch.uint8, device=x.device)
+    st = imp_fp8_gemm(x.data_ptr(), M, K, x.stride(0), w.c_struct(), y.data_ptr(), y.stride(0),
+                      None if dev_status is None else dev_status.data_ptr(), workspace.data_ptr(),
+                      wsb, _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_fp8_gemm")
+    return y

@@ -437,4 +437,91 @@ imp_status imp_nvfp4_gemm_grouped(const void *x_bf16, int64_t M, int64_t K, int6
   return IMP_OK;
 }
 
+// ---- MXFP4 and FP8 weights ----------------------------------------------------
+
+imp_status imp_mxfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                              const imp_mxfp4_tensor *out, int32_t *dev_status, void *stream) {
+  if (rows < 1 || K <= 0 || !out || !x_bf16) return IMP_ERR_INVALID_ARG;
+  if (K % 32) return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K || out->rows != rows || out->K != K || !out->codes || !out->scales)
+    return IMP_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || ldx % 8 || !aligned16(out->codes)) return IMP_ERR_MISALIGNED;
+  return from_cuda(impfp4::launch_mx_quantize(static_cast<const uint16_t *>(x_bf16), rows, K, ldx,
+                                              out->codes, out->scales, dev_status,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+size_t imp_mxfp4_to_nvfp4_workspace_size(void) { return 16; }
+
+imp_status imp_mxfp4_to_nvfp4(const imp_mxfp4_tensor *in, const imp_nvfp4_tensor *out,
+                              int32_t *dev_status, void *workspace, size_t ws_bytes,
+                              void *stream) {
+  if (!in || !out || !in->codes || !in->scales) return IMP_ERR_INVALID_ARG;
+  if (in->rows < 1 || in->K <= 0) return IMP_ERR_INVALID_ARG;
+  if (in->K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  imp_status st = check_tensor(out, in->rows, in->K);
+  if (st != IMP_OK) return st;
+  if (!aligned16(in->codes)) return IMP_ERR_MISALIGNED;
+  if (!workspace || ws_bytes < imp_mxfp4_to_nvfp4_workspace_size()) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned4(workspace)) return IMP_ERR_MISALIGNED;
+  return from_cuda(impfp4::launch_mx_to_nvfp4(in->codes, in->scales, in->rows, in->K, out->codes,
+                                              out->scales, out->tensor_scale, dev_status,
+                                              workspace, static_cast<cudaStream_t>(stream)));
+}
+
+size_t imp_fp8_quantize_workspace_size(int64_t rows, int64_t K) {
+  if (rows <= 0 || K <= 0) return 0;
+  return impfp4::quantize_workspace_bytes(rows, K);
+}
+
+imp_status imp_fp8_quantize(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                            const imp_fp8_tensor *out, int32_t *dev_status, void *workspace,
+                            size_t ws_bytes, void *stream) {
+  if (rows < 1 || K <= 0 || !out || !x_bf16) return IMP_ERR_INVALID_ARG;
+  if (K % 16) return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K || out->rows != rows || out->K != K || !out->codes || !out->tensor_scale)
+    return IMP_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || ldx % 8 || !aligned16(out->codes) || !aligned4(out->tensor_scale))
+    return IMP_ERR_MISALIGNED;
+  if (!workspace || ws_bytes < impfp4::quantize_workspace_bytes(rows, K))
+    return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  return from_cuda(impfp4::launch_fp8_quantize(static_cast<const uint16_t *>(x_bf16), rows, K, ldx,
+                                               out->codes, out->tensor_scale, dev_status,
+                                               workspace, static_cast<cudaStream_t>(stream)));
+}
+
+size_t imp_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || M > kDecodeMaxM || !impfp4::gemv_fp8_shape_ok(M, N, K)) return 0;
+  return impfp4::gemv_fp8_workspace_bytes(N, K);
+}
+
+int32_t imp_fp8_gemm_plan(int64_t M, int64_t N, int64_t K, const char **kernel) {
+  const bool ok = M >= 1 && M <= kDecodeMaxM && impfp4::gemv_fp8_shape_ok(M, N, K);
+  if (kernel) *kernel = ok ? "gemv_f4r_kernel" : nullptr;
+  return ok ? impfp4::gemv_fp8_launches(M) : 0;
+}
+
+imp_status imp_fp8_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                        const imp_fp8_tensor *w, void *y_bf16, int64_t ldy, int32_t *dev_status,
+                        void *workspace, size_t ws_bytes, void *stream) {
+  if (M < 0 || !w) return IMP_ERR_INVALID_ARG;
+  const int64_t N = w->rows;
+  if (N < 0 || w->K != K || K <= 0) return IMP_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return IMP_OK;
+  if (!w->codes || !w->tensor_scale || !x_bf16 || !y_bf16) return IMP_ERR_INVALID_ARG;
+  if (ldx < K || ldy < N) return IMP_ERR_INVALID_ARG;
+  if (M > kDecodeMaxM || !impfp4::gemv_fp8_shape_ok(M, N, K)) return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x_bf16) || !aligned16(y_bf16) || !aligned16(w->codes) ||
+      !aligned4(w->tensor_scale) || ldx % 8 || ldy % 8)
+    return IMP_ERR_MISALIGNED;
+  const size_t need = impfp4::gemv_fp8_workspace_bytes(N, K);
+  if (!workspace || ws_bytes < need) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  return from_cuda(impfp4::launch_gemv_fp8(static_cast<const uint16_t *>(x_bf16), M, K, ldx,
+                                           w->codes, w->tensor_scale, N,
+                                           static_cast<uint16_t *>(y_bf16), ldy, dev_status,
+                                           workspace, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

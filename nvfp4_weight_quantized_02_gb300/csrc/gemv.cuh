@@ -66,4 +66,15 @@ cudaError_t launch_gemv_f4_grouped(const uint16_t *x, int64_t M, int64_t K, int6
                                    const GemvGroup *g, int n, int32_t *status, void *workspace,
                                    cudaStream_t stream);
 
+// FP8-E4M3 weights (codes [N][K], one fp32 tensor scale): X split into E4M3
+// components per call, W streamed into tcgen05.mma.kind::f8f6f4; passes of
+// two rows of X.  K % 128 == 0, K >= 512, N >= 128.
+bool gemv_fp8_shape_ok(int64_t M, int64_t N, int64_t K);
+size_t gemv_fp8_workspace_bytes(int64_t N, int64_t K);
+int gemv_fp8_launches(int64_t M);
+cudaError_t launch_gemv_fp8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                            const uint8_t *codes, const float *tensor_scale, int64_t N,
+                            uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
+                            cudaStream_t stream);
+
 }  // namespace impfp4

@@ -104,15 +104,34 @@ template <int NMMA> struct StageS {
 
 // ---- resident-B kernel (M <= 2, N_MMA = 16)
 constexpr int kIssuersR = 4, kProducerR = 4, kNSR = 8;  // stage st and st - 8: same issuer
-constexpr int kMaxSlotsR = 24;                           // K chunks of X held per CTA
 constexpr int kLoaderWarpR = 5;                          // warp 5: copies the B slots in
 constexpr int kSplitWarps = 8;                           // chunks per CTA of the split kernel
+// Weight formats of the resident kernel: NVFP4 (E2M1 codes, E4M3 block
+// scales; X split into NVFP4 components; tcgen05.mma kind::mxf4nvf4) and
+// FP8 E4M3 with one tensor scale (X split into E4M3 components; kind::f8f6f4,
+// no block scales).  A stage is 128 rows x 128 bytes of W either way: 256
+// elements of NVFP4 or 128 of FP8.
+enum { kFmtNv = 0, kFmtF8 = 1 };
+template <int FMT> struct FmtR;
+template <> struct FmtR<kFmtNv> {
+  static constexpr int kChunk = 256;          // K elements per stage
+  static constexpr uint32_t kStageBytes = 18432, kTX = 16384 + 2048;
+  static constexpr uint32_t kSlotSf = 1024;   // B scale bytes per slot
+  static constexpr int kMaxSlots = 24;
+};
+template <> struct FmtR<kFmtF8> {
+  static constexpr int kChunk = 128;
+  static constexpr uint32_t kStageBytes = 16384, kTX = 16384;
+  static constexpr uint32_t kSlotSf = 0;
+  static constexpr int kMaxSlots = 40;
+};
 // W scales land where their atoms go: a row-major weight's 128 x 16-byte
 // scale rows are relaid in place (read, warp sync, write).
-struct StageR {
-  static constexpr uint32_t W = 0, RAW = 16384, SFA = 16384, BYTES = 18432;
-  static constexpr uint32_t TX = 16384 + 2048;
+template <int FMT> struct StageRT {
+  static constexpr uint32_t W = 0, RAW = 16384, SFA = 16384, BYTES = FmtR<FMT>::kStageBytes;
+  static constexpr uint32_t TX = FmtR<FMT>::kTX;
 };
+using StageR = StageRT<kFmtNv>;
 // B slot image of one K chunk (written once per call by xsplit_slots_kernel
 // into the workspace, copied as is into shared memory): codes, 2 KB = 16
 // operand rows x 128 B, row n at 128 n with its 16-byte unit u at unit
@@ -219,6 +238,13 @@ __host__ __device__ constexpr uint32_t idesc_f4() {
          ((uint32_t)(kTileRows >> 4) << 24);
 }
 
+template <int NMMA>
+__host__ __device__ constexpr uint32_t idesc_f8() {
+  // kind::f8f6f4: D fp32 (1 at bit 4), A and B E4M3 (format 0), K-major,
+  // N >> 3 at bit 17, M >> 4 at bit 24
+  return (1u << 4) | ((uint32_t)(NMMA >> 3) << 17) | ((uint32_t)(kTileRows >> 4) << 24);
+}
+
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
@@ -242,6 +268,14 @@ __device__ __forceinline__ void tc_mma_f4(uint32_t d_tmem, uint64_t adesc, uint6
       "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
       "[%5], [%6], p;\n}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -566,9 +600,57 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
   }
 }
 
+// Issuer of the FP8 weight format: the same stage order and accumulators as
+// issuer_loop, four K32 MMAs (kind::f8f6f4, no block scales) per stage.
+template <int NI, int NS, int NMMA, class Stage, class BDesc, class BWait>
+__device__ void issuer_loop_f8(uint8_t *smem, F4Bars &bars, uint32_t tmem, const StreamK &sk,
+                               int is, int lane, int32_t *status, BDesc b_desc, BWait b_wait) {
+  constexpr uint32_t kIdesc = idesc_f8<NMMA>();
+  static_assert(2 * NI * NMMA <= kTmemCols, "tensor memory plan");
+  const uint64_t dA0 = sdesc(smem_u32(smem) + Stage::W, 16, 1024, kSw128);
+  bool ok = true;
+  for (int jj = 0; jj < sk.n_seg && ok; ++jj) {
+    const int p0 = sk.pbegin(jj), p1 = sk.pend(jj);
+    const int d = jj & 1;
+    const int first = p0 + ((is - p0) % NI + NI) % NI;
+    for (int i = first; i < p1; i += NI) {
+      const int s = i % NS, st = sk.stage_of(i);
+      if (i == first && jj >= 2 &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.d_empty[d], (uint32_t)((jj / 2 - 1) & 1), status))) {
+        ok = false;
+        break;
+      }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.full[s], (uint32_t)((i / NS) & 1), status) &&
+                                       b_wait(st))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint64_t off = (uint64_t)(s * (Stage::BYTES >> 4));
+        const uint32_t dt = tmem + (uint32_t)((2 * is + d) * NMMA);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          tc_mma_f8(dt, dA0 + off + 2u * t, b_desc(i, st, t), kIdesc,
+                    (i == first && t == 0) ? 0u : 1u);
+        tc_commit(&bars.empty[s]);
+      }
+      __syncwarp();
+    }
+    if (ok && lane == 0) tc_commit(&bars.d_full[is][d]);
+    __syncwarp();
+  }
+  if (lane == 0) {
+    tc_commit(&bars.drain[is]);
+    mbar_wait_bounded(&bars.drain[is], 0u, status);
+  }
+}
+
 // Epilogue warps (kEpiWarp0..+3): per segment, the NI accumulators of each
 // row -> y (whole tile) or a partial sum (split tile, last CTA adds them).
-template <int NI, int NMMA>
+// Column c of a row's operand rows carries component c mod 8 with weight
+// 2^(4 - 2c) (NVFP4 components) or 2^(-4c) (E4M3 components).
+template <int NI, int NMMA, int FMT = kFmtNv>
 __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, const StreamK &sk,
                               int warp, int lane, const int (&sh)[kMaxRowsX], float *red) {
   constexpr int MR = NMMA / kNC;  // rows of X the operand holds (>= M)
@@ -605,7 +687,8 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int col = 16 * h + jj;
-            acc[col / kNC] += __uint_as_float(v[jj]) * pow2f(4 - 2 * (col % kNC));
+            acc[col / kNC] += __uint_as_float(v[jj]) *
+                              pow2f(FMT == kFmtF8 ? -4 * (col % kNC) : 4 - 2 * (col % kNC));
           }
         }
       }
@@ -1037,18 +1120,98 @@ __global__ void __launch_bounds__(32 * kSplitWarps)
   }
 }
 
+// Two signed floats -> two E4M3 bytes (element 0 in the low byte), round to
+// nearest even, saturating.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2_rn(float lo, float hi) {
+  uint32_t out;
+  asm("{\n.reg .b16 r;\ncvt.rn.satfinite.e4m3x2.f32 r, %2, %1;\ncvt.u32.u16 %0, r;\n}"
+      : "=r"(out)
+      : "f"(lo), "f"(hi));
+  return out;
+}
 
-template <bool PREP>
+// X (M <= 2 rows) -> B slot images for an FP8 weight, once per call:
+//   x * 2^sh = sum_{c < 8} 2^(-4c) * e4m3(q_c),
+// component c the E4M3 rounding (nearest even) of 2^(4c) times what
+// components 0..c-1 left, the residual updated with the exact product; the
+// prescale 2^sh puts the row's max|x| in [2^7, 2^8), below the E4M3 maximum.
+// A slot holds one 128-element chunk: 16 operand rows x 128 B, row 8 m + c
+// = component c of row m, element e at byte e of its row with the 16-byte
+// unit u stored at u ^ (n % 8).  Grid (chunks / kSplitWarps rounded up, M);
+// warp w splits chunk kSplitWarps j + w, lane l elements 4 l .. 4 l + 3.
+__global__ void __launch_bounds__(32 * kSplitWarps)
+    xsplit_f8_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, uint8_t *slot_codes,
+                     int32_t *sh_out, int32_t *status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ uint4 xrow[];  // row m of X (K bf16), staged once
+  __shared__ uint64_t bar;
+  __shared__ uint32_t red[kSplitWarps];
+  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // X may come from the previous kernel, and the previous GEMV may still
+  // read the workspace: wait for it before touching either.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)(K * 2));
+    bulk_g2s(xrow, x + m * ldx, (uint32_t)(K * 2), &bar);
+  }
+  if (!mbar_wait_bounded(&bar, 0u, status)) return;
+  uint32_t mx = 0;
+  for (int i = threadIdx.x; i < (int)(K / 8); i += 32 * kSplitWarps) mx = max(mx, absmax_bf16x8(xrow[i]));
+  for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = 0;
+  for (int w = 0; w < kSplitWarps; ++w) mx = max(mx, red[w]);
+  const int sh = mx ? prescale_exponent(mx) - 7 : 0;  // max in [2^7, 2^8)
+  if (blockIdx.x == 0 && threadIdx.x == 0) sh_out[m] = sh;
+
+  const int ch = blockIdx.x * kSplitWarps + warp;
+  if (ch >= (int)(K / 128)) return;
+  const uint2 v = reinterpret_cast<const uint2 *>(xrow)[ch * 32 + lane];
+  const float p1 = pow2f(sh / 2), p2 = pow2f(sh - sh / 2);
+  float r[4] = {bf16_bits_to_f32(v.x & 0xFFFFu) * p1 * p2, bf16_bits_to_f32(v.x >> 16) * p1 * p2,
+                bf16_bits_to_f32(v.y & 0xFFFFu) * p1 * p2, bf16_bits_to_f32(v.y >> 16) * p1 * p2};
+  uint8_t *codes = slot_codes + (size_t)ch * 2048;
+#pragma unroll
+  for (int c = 0; c < kNC; ++c) {
+    const int n = m * kNC + c;
+    const float up = pow2f(4 * c), down = pow2f(-4 * c);
+    const uint32_t lo = f32x2_to_e4m3x2_rn(r[0] * up, r[1] * up);
+    const uint32_t hi = f32x2_to_e4m3x2_rn(r[2] * up, r[3] * up);
+    const uint32_t hl = e4m3x2_to_f16x2(lo), hh = e4m3x2_to_f16x2(hi);
+    r[0] = fmaf(-f16lo_to_f32(hl), down, r[0]);  // e4m3 * 2^-4c is exact; one rounding
+    r[1] = fmaf(-f16hi_to_f32(hl), down, r[1]);
+    r[2] = fmaf(-f16lo_to_f32(hh), down, r[2]);
+    r[3] = fmaf(-f16hi_to_f32(hh), down, r[3]);
+    *reinterpret_cast<uint32_t *>(codes + n * 128 + (((lane >> 2) ^ (n & 7)) << 4) + 4 * (lane & 3)) =
+        lo | hi << 16;
+  }
+  if (m == M - 1 && M * kNC < 16) {
+    // operand rows after the last component: zero
+    const int n0 = M * kNC, nr = 16 - n0;
+    uint4 *zc = reinterpret_cast<uint4 *>(codes + n0 * 128);
+    for (int i = lane; i < nr * 8; i += 32) zc[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <bool PREP, int FMT = kFmtNv>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_f4r_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
                     const F4Args a) {
-  using L = StageR;
+  using L = StageRT<FMT>;
+  constexpr uint32_t kSlotSf = FmtR<FMT>::kSlotSf;
+  static_assert(FMT == kFmtNv || !PREP, "FP8 weights are read row-major");
   constexpr int NMMA = 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *bcodes = smem + kNSR * L::BYTES;                   // [slot][16 rows][128 B], swizzled
-  uint8_t *bsf = bcodes + (size_t)a.n_slots * 2048;           // [slot][4 steps][256 B] + pad
-  F4Bars &bars = *reinterpret_cast<F4Bars *>(bsf + (size_t)a.n_slots * 1024 + 256);
+  uint8_t *bsf = bcodes + (size_t)a.n_slots * 2048;           // NVFP4: [slot][4 steps][256 B] + pad
+  F4Bars &bars = *reinterpret_cast<F4Bars *>(bsf + (size_t)a.n_slots * kSlotSf + 256);
   // kSchedCluster: the other ranks' partial sums, [rank - 1][128 rows][2]
   float *red = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&bars) +
                                          ((sizeof(F4Bars) + 15) & ~size_t(15)));
@@ -1078,7 +1241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       if (!PREP) {
         prefetch_tmap(&tm_w);
-        prefetch_tmap(&tm_ws);
+        if (FMT == kFmtNv) prefetch_tmap(&tm_ws);
       }
       // processing position i -> ring slot i % NS, stage stage_of(i).  The
       // source of a stage is worked out before its slot frees (where), so
@@ -1109,8 +1272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_g2s(stg + L::W, r.w, 16384u, &bars.full[s]);
           bulk_g2s(stg + L::SFA, r.sf, 2048u, &bars.full[s]);
         } else {
-          tma_load_2d(stg + L::W, &tm_w, r.ch * (kChunkK / 2), r.row0, &bars.full[s]);
-          tma_load_2d(stg + L::RAW, &tm_ws, r.ch * (kChunkK / 16), r.row0, &bars.full[s]);
+          // 128 bytes of each row per stage: 256 NVFP4 or 128 FP8 elements
+          tma_load_2d(stg + L::W, &tm_w, r.ch * 128, r.row0, &bars.full[s]);
+          if (FMT == kFmtNv)
+            tma_load_2d(stg + L::RAW, &tm_ws, r.ch * (kChunkK / 16), r.row0, &bars.full[s]);
         }
       };
       // The ring alone keeps W in flight: an extra L2 prefetch at the start
@@ -1133,32 +1298,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // split kernel has finished) this CTA's B slots: chunks ch_begin,
     // ch_begin + 1, ... (mod K / 256), contiguous in the workspace up to the
     // wrap-around, so at most two copies per array.
-    if (lane < 16)
-      reinterpret_cast<uint4 *>(bsf + (size_t)a.n_slots * 1024)[lane] = make_uint4(0, 0, 0, 0);
+    if (FMT == kFmtNv && lane < 16)
+      reinterpret_cast<uint4 *>(bsf + (size_t)a.n_slots * kSlotSf)[lane] = make_uint4(0, 0, 0, 0);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the pad is read by tcgen05.cp
     __syncwarp();
     if (lane == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       const int n1 = min(a.n_slots, sk.nch - ch_begin), n2 = a.n_slots - n1;
-      mbar_arrive_expect_tx(&bars.b_ready, (uint32_t)a.n_slots * 3072u);
+      mbar_arrive_expect_tx(&bars.b_ready, (uint32_t)a.n_slots * (2048u + kSlotSf));
       bulk_g2s(bcodes, a.slot_codes + (size_t)ch_begin * 2048, (uint32_t)n1 * 2048u, &bars.b_ready);
-      bulk_g2s(bsf, a.sfb + (size_t)ch_begin * 1024, (uint32_t)n1 * 1024u, &bars.b_ready);
+      if (FMT == kFmtNv)
+        bulk_g2s(bsf, a.sfb + (size_t)ch_begin * kSlotSf, (uint32_t)n1 * kSlotSf, &bars.b_ready);
       if (n2 > 0) {
         bulk_g2s(bcodes + (size_t)n1 * 2048, a.slot_codes, (uint32_t)n2 * 2048u, &bars.b_ready);
-        bulk_g2s(bsf + (size_t)n1 * 1024, a.sfb, (uint32_t)n2 * 1024u, &bars.b_ready);
+        if (FMT == kFmtNv)
+          bulk_g2s(bsf + (size_t)n1 * kSlotSf, a.sfb, (uint32_t)n2 * kSlotSf, &bars.b_ready);
       }
       // never leave with copies in flight
       mbar_wait_bounded(&bars.b_ready, 0u, a.status);
     }
   } else if (warp == kRelayWarp) {
-    if (!PREP) relay_loop<kNSR, L>(smem, bars, sk, lane, a.status);
+    if (!PREP && FMT == kFmtNv) relay_loop<kNSR, L>(smem, bars, sk, lane, a.status);
   } else if (warp >= kEpiWarp0) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the split kernel wrote sh
     int sh[kMaxRowsX] = {};
 #pragma unroll
     for (int m = 0; m < 2; ++m)
       if (m < a.M) sh[m] = a.sh[m];
-    epilogue_loop<kIssuersR, NMMA>(a, bars, tmem, sk, warp, lane, sh, red);
+    epilogue_loop<kIssuersR, NMMA, FMT>(a, bars, tmem, sk, warp, lane, sh, red);
   } else if (warp < kIssuersR) {
     // ---- MMA issuers: each stage waits for its B slot
     const uint64_t dB0 = sdesc(smem_u32(bcodes), 16, 1024, kSw128);
@@ -1168,8 +1335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       return dSB0 + (uint64_t)(slot_of(st) * (1024 >> 4)) + (uint64_t)(16u * t);
     };
     auto b_wait = [&](int) { return mbar_wait_bounded(&bars.b_ready, 0u, a.status); };
-    issuer_loop<kIssuersR, kNSR, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
-                                          sfb_desc, b_wait);
+    if constexpr (FMT == kFmtNv)
+      issuer_loop<kIssuersR, kNSR, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status,
+                                                  b_desc, sfb_desc, b_wait);
+    else
+      issuer_loop_f8<kIssuersR, kNSR, NMMA, L>(smem, bars, tmem, sk, warp, lane, a.status, b_desc,
+                                               b_wait);
   }
 
   tc_fence_before();
@@ -1230,9 +1401,13 @@ struct F4Plan {
   size_t smem;
   bool ok;  // the resident kernel takes the shape
 };
-F4Plan plan_r(int64_t M, int64_t N, int64_t K) {
+F4Plan plan_r(int64_t M, int64_t N, int64_t K, int fmt = kFmtNv) {
   F4Plan p = {};
-  const int64_t nch = K / kChunkK, n_tiles = ceil_div(N, kTileRows), sms = num_sms();
+  const int chunk = fmt == kFmtF8 ? FmtR<kFmtF8>::kChunk : FmtR<kFmtNv>::kChunk;
+  const int max_slots = fmt == kFmtF8 ? FmtR<kFmtF8>::kMaxSlots : FmtR<kFmtNv>::kMaxSlots;
+  const uint32_t stage = fmt == kFmtF8 ? FmtR<kFmtF8>::kStageBytes : FmtR<kFmtNv>::kStageBytes;
+  const uint32_t slot = 2048 + (fmt == kFmtF8 ? FmtR<kFmtF8>::kSlotSf : FmtR<kFmtNv>::kSlotSf);
+  const int64_t nch = K / chunk, n_tiles = ceil_div(N, kTileRows), sms = num_sms();
   p.sched = kSchedStreamK;
   p.ksplit = 1;
   if (4 * n_tiles >= 3 * sms) {
@@ -1243,25 +1418,28 @@ F4Plan plan_r(int64_t M, int64_t N, int64_t K) {
     int64_t S = sms / n_tiles;
     if (S > 8) S = 8;
     if (S > nch) S = nch;
-    if (S >= 2 && ceil_div(nch, S) <= kMaxSlotsR) {
+    if (S >= 2 && ceil_div(nch, S) <= max_slots) {
       p.sched = kSchedCluster;
       p.ksplit = (int)S;
       p.grid = (int)(n_tiles * S);
       p.n_slots = (int)ceil_div(nch, S);
     }
   }
-  if (p.sched == kSchedStreamK || p.n_slots > kMaxSlotsR) {
+  if (p.sched == kSchedStreamK || p.n_slots > max_slots) {
     p.sched = kSchedStreamK;
     p.ksplit = 1;
-    p.grid = f4_ws(M, N, K).grid;
+    int64_t g = n_tiles * nch;
+    if (g > kMaxGrid) g = kMaxGrid;
+    if (g > sms) g = sms;
+    p.grid = (int)g;
     const int64_t per = ceil_div(n_tiles * nch, p.grid);
     p.n_slots = (int)(per < nch ? per : nch);
   }
   const size_t red = p.sched == kSchedCluster ? (size_t)(p.ksplit - 1) * kTileRows * 2 * sizeof(float) : 0;
-  p.smem = (size_t)kNSR * StageR::BYTES + (size_t)p.n_slots * (2048 + 1024) + 256 +
+  p.smem = (size_t)kNSR * stage + (size_t)p.n_slots * slot + 256 +
            ((sizeof(F4Bars) + 15) & ~size_t(15)) + red + 1024;
   // the split kernel stages a row of X (2 K bytes) in shared memory
-  p.ok = M <= 2 && p.n_slots <= kMaxSlotsR && K * 2 <= 200 * 1024;
+  p.ok = M <= 2 && p.n_slots <= max_slots && K * 2 <= 200 * 1024 && p.smem <= 227 * 1024;
   return p;
 }
 
@@ -1513,6 +1691,95 @@ cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
   // every row of X in one stream of W
   return launch_pass_streamed(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status,
                               workspace, stream, prepared);
+}
+
+// ---- FP8-E4M3 weights ------------------------------------------------------------
+
+namespace {
+// Workspace of one FP8 call: slot images [K/128][2 KB] | prescale exponents |
+// per-tile counters | stream-K partials.
+struct F8Ws {
+  size_t sh, cnt, part, total;
+};
+F8Ws f8_ws(int64_t N, int64_t K) {
+  F8Ws w;
+  const int64_t n_tiles = ceil_div(N, kTileRows);
+  w.sh = (size_t)(K / 128) * 2048;
+  w.cnt = w.sh + 256;
+  w.part = w.cnt + (size_t)ceil_div(n_tiles * 16, 256) * 256;
+  w.total = w.part + (size_t)kMaxGrid * 2 * 2 * kTileRows * sizeof(float);
+  return w;
+}
+}  // namespace
+
+bool gemv_fp8_shape_ok(int64_t M, int64_t N, int64_t K) {
+  return M >= 1 && M <= kDecodeMaxM && N >= kTileRows && N <= 0x7FFFFFFFll && K >= 512 &&
+         K % 128 == 0 && plan_r(2, N, K, kFmtF8).ok;
+}
+
+size_t gemv_fp8_workspace_bytes(int64_t N, int64_t K) { return f8_ws(N, K).total; }
+
+int gemv_fp8_launches(int64_t M) { return 2 * (int)ceil_div(M, 2); }
+
+cudaError_t launch_gemv_fp8(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                            const uint8_t *codes, const float *tensor_scale, int64_t N,
+                            uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
+                            cudaStream_t stream) {
+  const F8Ws L = f8_ws(N, K);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  CUtensorMap mw, ms;
+  if (!cached_map(mw, codes, (uint64_t)N, (uint64_t)K, kTileRows, 128, true))
+    return cudaErrorInvalidValue;
+  memset(&ms, 0, sizeof(ms));
+  const size_t xs_bytes = (size_t)K * 2;
+  if (xs_bytes > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        xsplit_f8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xs_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  // passes of up to two rows of X (8 operand rows each), one stream of W each
+  for (int64_t m0 = 0; m0 < M; m0 += 2) {
+    const int mp = (int)(M - m0 < 2 ? M - m0 : 2);
+    const F4Plan P = plan_r(mp, N, K, kFmtF8);
+    F4Args a = {};
+    a.x = x + m0 * ldx;
+    a.ldx = ldx;
+    a.M = mp;
+    a.K = K;
+    a.sh = reinterpret_cast<const int32_t *>(ws + L.sh);
+    a.part = reinterpret_cast<float *>(ws + L.part);
+    a.cnt = reinterpret_cast<unsigned __int128 *>(ws + L.cnt);
+    a.status = status;
+    a.n_groups = 1;
+    a.grp[0] = F4Group{codes, nullptr, tensor_scale, y + m0 * ldy, N, ldy, 0};
+    a.n_tiles = (int)ceil_div(N, kTileRows);
+    a.n_chunks = (int)(K / 128);
+    a.epoch = next_launch_epoch();
+    a.n_slots = P.n_slots;
+    a.sched = P.sched;
+    a.ksplit = P.ksplit;
+    a.slot_codes = ws;
+    {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)ceil_div(K / 128, kSplitWarps), (unsigned)mp);
+      cfg.blockDim = dim3(32 * kSplitWarps);
+      cfg.dynamicSmemBytes = xs_bytes;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, xsplit_f8_kernel, a.x, ldx, mp, K, ws,
+                                               reinterpret_cast<int32_t *>(ws + L.sh), status);
+      if (e != cudaSuccess) return e;
+    }
+    const int cluster = P.sched == kSchedCluster ? P.ksplit : 1;
+    const cudaError_t e = launch_pdl(gemv_f4r_kernel<false, kFmtF8>, P.grid, kThreads, P.smem,
+                                     stream, cluster, mw, ms, a);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 bool gemv_f4_grouped_ok(int64_t M, int64_t K, const GemvGroup *g, int n) {

@@ -360,4 +360,212 @@ cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int6
   return cudaGetLastError();
 }
 
+// ---- MXFP4 (OCP MX v1.0) and FP8-E4M3 weights ---------------------------------
+//
+// MXFP4: 32-element blocks along K, one E8M0 scale byte (2^(b - 127)) per
+// block, E2M1 codes.  Shared exponent e = floor(log2(block amax)) - 2,
+// clamped to [-127, 127]; code = E2M1(|x| * 2^-e), nearest even, saturating
+// at 6 (cvt.rn.satfinite.e2m1x2), sign bit copied from x.  Multiplying by the
+// power of two 2^-e is exact (it is a normal float for every e a bf16 block
+// can give), so the codes equal those of the division x / 2^e.
+//
+// FP8 weights: one fp32 scale s8 = g / 448 per tensor (the global amax pass
+// of the NVFP4 quantizer), code = E4M3(|x| / s8) (cvt.rn.satfinite.e4m3x2),
+// sign bit copied from x; s8 == 0 gives all codes 0.
+namespace {
+
+constexpr int kMxThreads = 256;
+
+// floor(log2 v) of a nonzero finite bf16 magnitude (bits without the sign).
+__device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
+  const int E = (int)(mag >> 7);
+  if (E > 0) return E - 127;
+  return (31 - __clz((int)mag)) - 133;  // subnormal: mantissa * 2^-133
+}
+
+// One thread per 32-element block.
+__global__ void __launch_bounds__(kMxThreads) mx_quantize_kernel(
+    const uint16_t *__restrict__ x, int64_t rows, int64_t K, int64_t ldx,
+    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int32_t *status) {
+  const int64_t nb = K / 32, total = rows * nb;
+  for (int64_t i = (int64_t)blockIdx.x * kMxThreads + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * kMxThreads) {
+    const int64_t r = i / nb, b = i - r * nb;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + 32 * b);
+    uint32_t w[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 t = __ldg(src + v);
+      w[4 * v] = t.x;
+      w[4 * v + 1] = t.y;
+      w[4 * v + 2] = t.z;
+      w[4 * v + 3] = t.w;
+    }
+    uint32_t a2 = 0;
+#pragma unroll
+    for (int v = 0; v < 16; ++v) a2 = __vmaxu2(a2, w[v] & 0x7FFF7FFFu);
+    const uint32_t amag = max(a2 & 0xFFFFu, a2 >> 16);
+    if (amag >= 0x7F80u) report(status, IMP_DEV_NONFINITE_INPUT);
+    int e = amag ? bf16_floor_log2(amag) - 2 : -127;
+    e = min(127, max(-127, e));
+    scales[r * nb + b] = (uint8_t)(e + 127);
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, e <= 126 here
+    uint32_t packed[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      float q[8];
+      uint32_t sign = 0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint32_t wi = w[4 * h + v];
+        q[2 * v] = __fmul_rn(bf16_bits_to_f32(wi & 0x7FFFu), inv);
+        q[2 * v + 1] = __fmul_rn(bf16_bits_to_f32((wi >> 16) & 0x7FFFu), inv);
+        sign |= ((wi >> 15) & 1u) << (8 * v + 3);
+        sign |= (wi >> 31) << (8 * v + 7);
+      }
+      packed[h] = f32x8_to_e2m1_packed(q) | sign;
+    }
+    *reinterpret_cast<uint4 *>(codes + r * (K / 2) + 16 * b) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
+// Two E4M3 bytes (element 0 in the low byte) of two non-negative floats.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint32_t out;
+  asm("{\n.reg .b16 r;\ncvt.rn.satfinite.e4m3x2.f32 r, %2, %1;\ncvt.u32.u16 %0, r;\n}"
+      : "=r"(out)
+      : "f"(lo), "f"(hi));
+  return out;
+}
+
+// FP8 pass 2: s8 from the partial maxima, then one thread per 8 elements.
+__global__ void __launch_bounds__(kEncThreads) fp8_encode_kernel(
+    const uint16_t *__restrict__ x, int64_t rows, int64_t K, int64_t ldx,
+    const uint32_t *__restrict__ partial, int num_partial, uint8_t *__restrict__ codes,
+    float *__restrict__ tensor_scale) {
+  __shared__ uint32_t red[kEncThreads / 32];
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < num_partial; i += kEncThreads) m = max(m, partial[i]);
+  m = block_max_u32<kEncThreads>(m, red);
+  const float g = bf16_bits_to_f32(m < 0x7F80u ? m : 0u);
+  const float s8 = __fdiv_rn(g, 448.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s8;
+  const int64_t per_row = K / 8, total = rows * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * kEncThreads + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * kEncThreads) {
+    const int64_t r = i / per_row, j = i - r * per_row;
+    uint2 out = make_uint2(0u, 0u);
+    if (s8 != 0.0f) {
+      const uint4 t = __ldg(reinterpret_cast<const uint4 *>(x + r * ldx + 8 * j));
+      const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+      uint32_t b[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const float lo = __fdiv_rn(bf16_bits_to_f32(w[v] & 0x7FFFu), s8);
+        const float hi = __fdiv_rn(bf16_bits_to_f32((w[v] >> 16) & 0x7FFFu), s8);
+        b[v] = f32x2_to_e4m3x2(lo, hi) | ((w[v] >> 8) & 0x80u) | ((w[v] >> 16) & 0x8000u);
+      }
+      out = make_uint2(b[0] | b[1] << 16, b[2] | b[3] << 16);
+    }
+    *reinterpret_cast<uint2 *>(codes + r * K + 8 * j) = out;
+  }
+}
+
+// MXFP4 -> NVFP4, pass 1: the largest E8M0 byte among 16-element halves of a
+// block that hold a nonzero code (atomicMax into *bmax, zeroed beforehand).
+__global__ void __launch_bounds__(256) mx_scale_max_kernel(const uint8_t *__restrict__ codes,
+                                                           const uint8_t *__restrict__ scales,
+                                                           int64_t halves, uint32_t *bmax) {
+  __shared__ uint32_t red[8];
+  uint32_t m = 0;
+  for (int64_t h = (int64_t)blockIdx.x * 256 + threadIdx.x; h < halves;
+       h += (int64_t)gridDim.x * 256) {
+    const uint2 c = *reinterpret_cast<const uint2 *>(codes + 8 * h);
+    if ((c.x | c.y) & 0x77777777u) m = max(m, (uint32_t)scales[h / 2]);
+  }
+  m = block_max_u32<256>(m, red);
+  if (threadIdx.x == 0 && m) atomicMax(bmax, m);
+}
+
+// E4M3 byte of 2^k for k in [-9, 8] (normal from 2^-6, subnormal below).
+__device__ __forceinline__ uint32_t e4m3_pow2(int k) {
+  return k >= -6 ? (uint32_t)(k + 7) << 3 : 1u << (k + 9);
+}
+
+// Pass 2: each half gets the E4M3 scale 2^(b - bmax + 8), exact while that
+// is at least 2^-9; a half whose codes are all zero gets 0x00; a half with
+// nonzero codes more than 2^17 below the largest is reported
+// (IMP_DEV_RANGE).  Block 0 writes the tensor scale 2^(bmax - 135).
+__global__ void __launch_bounds__(256) mx_to_nvfp4_kernel(
+    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, int64_t halves,
+    const uint32_t *__restrict__ bmax_p, uint8_t *__restrict__ nv_scales, float *tensor_scale,
+    int32_t *status) {
+  const int bmax = (int)*bmax_p;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const int t = bmax - 135;  // exponent of the tensor scale, in [-135, 119]
+    *tensor_scale = t >= -126 ? __uint_as_float((uint32_t)(t + 127) << 23)
+                              : __uint_as_float(1u << (t + 149));
+  }
+  for (int64_t h = (int64_t)blockIdx.x * 256 + threadIdx.x; h < halves;
+       h += (int64_t)gridDim.x * 256) {
+    const uint2 c = *reinterpret_cast<const uint2 *>(codes + 8 * h);
+    uint32_t out = 0;
+    if ((c.x | c.y) & 0x77777777u) {
+      const int k = (int)scales[h / 2] - bmax + 8;
+      if (k < -9) report(status, IMP_DEV_RANGE);
+      else out = e4m3_pow2(k);
+    }
+    nv_scales[h] = (uint8_t)out;
+  }
+}
+
+int grid_for(int64_t items, int threads) {
+  int64_t g = ceil_div(items, threads);
+  const int64_t cap = (int64_t)num_sms_cached() * 8;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_mx_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                               uint8_t *codes, uint8_t *scales, int32_t *status,
+                               cudaStream_t stream) {
+  mx_quantize_kernel<<<grid_for(rows * (K / 32), kMxThreads), kMxThreads, 0, stream>>>(
+      x, rows, K, ldx, codes, scales, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                                uint8_t *codes, float *tensor_scale, int32_t *status,
+                                void *workspace, cudaStream_t stream) {
+  const int ga = amax_grid(rows);
+  uint32_t *partial = static_cast<uint32_t *>(workspace);
+  amax_partial_kernel<<<ga, kAmaxThreads, 0, stream>>>(x, rows, K, ldx, partial, status);
+  fp8_encode_kernel<<<grid_for(rows * (K / 8), kEncThreads), kEncThreads, 0, stream>>>(
+      x, rows, K, ldx, partial, ga, codes, tensor_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_to_nvfp4(const uint8_t *codes, const uint8_t *mx_scales, int64_t rows,
+                               int64_t K, uint8_t *out_codes, uint8_t *nv_scales,
+                               float *tensor_scale, int32_t *status, void *workspace,
+                               cudaStream_t stream) {
+  uint32_t *bmax = static_cast<uint32_t *>(workspace);
+  const int64_t halves = rows * (K / 16);
+  cudaError_t e = cudaMemsetAsync(bmax, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  if (out_codes != codes) {
+    e = cudaMemcpyAsync(out_codes, codes, (size_t)rows * (size_t)(K / 2), cudaMemcpyDeviceToDevice,
+                        stream);
+    if (e != cudaSuccess) return e;
+  }
+  mx_scale_max_kernel<<<grid_for(halves, 256), 256, 0, stream>>>(codes, mx_scales, halves, bmax);
+  mx_to_nvfp4_kernel<<<grid_for(halves, 256), 256, 0, stream>>>(codes, mx_scales, halves, bmax,
+                                                                nv_scales, tensor_scale, status);
+  return cudaGetLastError();
+}
+
 }  // namespace impfp4

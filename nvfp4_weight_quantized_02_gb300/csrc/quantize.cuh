@@ -20,6 +20,26 @@ cudaError_t launch_quantize_noalloc(const uint16_t *x, int64_t rows, int64_t K, 
                                     uint8_t *codes, uint8_t *scales, float *tensor_scale,
                                     int32_t *status, cudaStream_t stream);
 
+// MXFP4 quantizer (one pass, no workspace): codes [rows][K/2], E8M0 scales
+// [rows][K/32].  K % 32 == 0.
+cudaError_t launch_mx_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                               uint8_t *codes, uint8_t *scales, int32_t *status,
+                               cudaStream_t stream);
+
+// FP8-E4M3 weight quantizer: the global amax pass (workspace as for
+// launch_quantize), then codes [rows][K] and s8 = g / 448.  K % 16 == 0.
+cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                                uint8_t *codes, float *tensor_scale, int32_t *status,
+                                void *workspace, cudaStream_t stream);
+
+// MXFP4 -> the same values in NVFP4 form (codes copied unless out_codes ==
+// codes; E4M3 half-block scales; power-of-two tensor scale).  workspace: 4
+// bytes, 4-byte aligned.
+cudaError_t launch_mx_to_nvfp4(const uint8_t *codes, const uint8_t *mx_scales, int64_t rows,
+                               int64_t K, uint8_t *out_codes, uint8_t *nv_scales,
+                               float *tensor_scale, int32_t *status, void *workspace,
+                               cudaStream_t stream);
+
 // Enqueue the two quantizer passes on `stream`.  Arguments are validated by
 // the caller (api.cu).  rows > 0.
 cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,

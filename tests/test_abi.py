@@ -155,3 +155,34 @@ def test_grouped_rejects_bad_arguments():
     assert g(A16 + 8, 1, 1024, 1024, ok, None, A16, ws, None) == pkg.IMP_ERR_MISALIGNED
     # M = 0: nothing to do
     assert g(A16, 0, 1024, 1024, ok, None, None, 0, None) == pkg.IMP_OK
+
+
+def test_formats_reject_bad_arguments():
+    MX, F8 = pkg.ImpMxfp4Tensor, pkg.ImpFp8Tensor
+    q = pkg.imp_mxfp4_quantize
+    assert q(A16, 4, 48, 48, MX(A16, A16, 4, 48), None, None) == pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    assert q(A16, 4, 64, 64, MX(A16, A16, 5, 64), None, None) == pkg.IMP_ERR_INVALID_ARG
+    assert q(A16 + 8, 4, 64, 64, MX(A16, A16, 4, 64), None, None) == pkg.IMP_ERR_MISALIGNED
+    c = pkg.imp_mxfp4_to_nvfp4
+    ws = pkg.imp_mxfp4_to_nvfp4_workspace_size()
+    assert c(MX(A16, A16, 4, 32), _t(4, 32), None, A16, ws, None) == pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    assert c(MX(A16, A16, 4, 64), _t(5, 64), None, A16, ws, None) == pkg.IMP_ERR_INVALID_ARG
+    assert c(MX(A16, A16, 4, 64), _t(4, 64), None, None, 0, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    f = pkg.imp_fp8_quantize
+    fws = pkg.imp_fp8_quantize_workspace_size(4, 64)
+    assert f(A16, 4, 40, 40, F8(A16, A16, 4, 40), None, A16, fws, None) == pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    assert f(A16, 4, 64, 64, F8(A16, A16, 4, 64), None, None, 0, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    g = pkg.imp_fp8_gemm
+    gws = pkg.imp_fp8_gemm_workspace_size(1, 1024, 1024)
+    assert gws > 0
+    assert g(A16, 1, 1000, 1000, F8(A16, A16, 1024, 1000), A16, 1024, None, A16, gws, None) == \
+        pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    assert g(A16, 17, 1024, 1024, F8(A16, A16, 1024, 1024), A16, 1024, None, A16, gws, None) == \
+        pkg.IMP_ERR_UNSUPPORTED_SHAPE
+    assert g(A16, 1, 1024, 1024, F8(A16, A16, 1024, 1024), A16, 1024, None, A16, gws - 16, None) == \
+        pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    assert g(A16, 1, 1024, 1024, F8(A16, A16, 1024, 1024), A16 + 8, 1024, None, A16, gws, None) == \
+        pkg.IMP_ERR_MISALIGNED
+    assert g(A16, 0, 1024, 1024, F8(A16, A16, 1024, 1024), A16, 1024, None, None, 0, None) == pkg.IMP_OK
+    assert pkg.imp_fp8_gemm_plan(1, 17408, 5120) == (2, "gemv_f4r_kernel")
+    assert pkg.imp_fp8_gemm_plan(1, 5120, 17408) == (2, "gemv_f4r_kernel")

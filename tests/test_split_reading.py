@@ -100,3 +100,44 @@ def test_exact_when_the_block_is_representable():
     # component takes it exactly
     x = _bf16(np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0.5, -1, -1.5, -2, -3, -4, -6, 6.0]) * 0.75)
     assert np.abs(split_row(x)).max() == 0.0
+
+
+# ---- the FP8 weight path's reading of X: eight E4M3 components ----------------
+
+def split_row_e4m3(row):
+    """x * 2^sh = sum_c 2^(-4c) e4m3(q_c), q_c the E4M3 rounding of 2^(4c)
+    times what components 0..c-1 left; sh puts max|x| in [2^7, 2^8).
+    Returns the residual in true units (fp32 arithmetic as on the device)."""
+    mx = np.abs(row).max()
+    sh = 0 if mx == 0 else 8 - math.frexp(mx)[1]
+    r = (row * 2.0 ** sh).astype(np.float32)
+    for c in range(8):
+        for k in range(len(r)):
+            u = float(r[k]) * 2.0 ** (4 * c)
+            mag = oracle.e4m3_value(oracle.e4m3_encode(abs(u)))
+            v = math.copysign(mag, u)
+            r[k] = np.float32(r[k] - np.float32(v * 2.0 ** (-4 * c)))
+    return r.astype(np.float64) * 2.0 ** -sh
+
+
+def test_e4m3_split_residual_negligible():
+    rng = np.random.default_rng(7)
+    worst = 0.0
+    for i in range(20):
+        row = _bf16(rng.standard_normal(128) * 2.0 ** rng.integers(-20, 20))
+        row[rng.integers(0, 128, 3)] *= 20.0 * (i + 1)
+        if i % 5 == 0:
+            row[rng.integers(0, 128, 8)] *= 2.0 ** -30  # far below the row max
+        res = split_row_e4m3(row)
+        worst = max(worst, np.abs(res).max() / np.abs(row).max())
+        # its share of a dot product's band with any weights
+        w = rng.standard_normal(128)
+        assert abs(np.dot(res, w)) <= 1e-4 * 2e-3 * np.sum(np.abs(row * w)) + 1e-300
+    assert worst < 1e-9
+
+
+def test_e4m3_split_exact_for_two_component_values():
+    # a bf16 value has 8 significant bits: two E4M3 components (4 bits each)
+    # hold it exactly when it is within the E4M3 normal range after the prescale
+    row = _bf16(np.array([1.0, -1.5, 3.0 + 2 ** -6, 100.0, -255.0, 2 ** -3 + 2 ** -7] * 2))
+    assert np.all(split_row_e4m3(row) == 0.0)
