@@ -981,6 +981,56 @@ def run_prefill_workload(args):
     return 0
 
 
+def run_quantizer_workload(args):
+    """--workload quantizer: one step = the NVFP4 quantizer (global amax pass,
+    block encode pass) on the 27B-class LM-head weight (151936 x 5120 bf16);
+    metric GB/s of its algorithmic bytes (X read twice, codes and scales
+    written)."""
+    import torch
+
+    import nvfp4_weight_quantized_02_gb300 as pkg
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pkg.load()
+    stream = torch.cuda.current_stream(dev)
+    l = [w for w in synth.workload("decode_27b") if w.name == "lm_head"][0]
+    wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+    q = pkg.NVFP4Tensor.empty(l.N, l.K, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    step = lambda: pkg.quantize(wb, out=q, dev_status=status, stream=stream)  # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clocks:
+        e0, e1 = event_pair()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        blocks = time_blocks(step, max(args.steps, 5), 10, stream)
+    assert int(status.item()) == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = 2 * 2 * l.N * l.K + l.N * l.K // 2 + l.N * l.K // 16
+    hbm_peak, _, peak_kind = load_peaks()
+    value = nbytes / (ms * 1e-3) / 1e9
+    line = {"metric": "NVFP4 quantizer GB/s (two passes, bit-exact)", "value": value,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 in, nvfp4 out", "data": "synthetic",
+            "config": {"workload": "quantizer", "shape": [l.N, l.K]},
+            "spread_ms_per_step": spread([b / 1e3 for b in blocks]),
+            "roofline": {"bound": "hbm", "kernel": "amax_partial_kernel + encode_kernel",
+                         "achieved": value, "peak": hbm_peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": value / hbm_peak, "traffic": None},
+            "gpu_launches": 2 * args.steps, "clocks": clocks.summary()}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -999,6 +1049,8 @@ def main():
         return run_reference(args)
     if args.workload.startswith("prefill"):
         return run_prefill_workload(args)
+    if args.workload == "quantizer":
+        return run_quantizer_workload(args)
     return run_native(args)
 
 

@@ -137,8 +137,8 @@ __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float u) {
   return out & 0xFFu;
 }
 
-// Eight non-negative fp32 magnitudes -> eight E2M1 magnitude codes (round to
-// nearest even, saturating at 6), packed element 0 in the low nibble.
+// Eight fp32 values -> eight E2M1 codes (round to nearest even, saturating
+// at 6, sign bit from the value), packed element 0 in the low nibble.
 __device__ __forceinline__ uint32_t f32x8_to_e2m1_packed(const float (&q)[8]) {
   uint32_t out;
   asm("{\n.reg .b8 b0, b1, b2, b3;\n"

@@ -83,6 +83,40 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partial_kernel(const uint16
   }
 }
 
+// The codes of q_i = RN(x_i / d) for eight elements (signed; the E2M1
+// conversion keeps the sign, also of a zero) without eight IEEE divisions.
+// x_i * RN(1/d) is within 2^-22.4 (relative) of RN(x_i / d); the products
+// with RN(1/d) (1 -/+ 2^-20) therefore bracket RN(x_i / d) in magnitude, and
+// rounding to E2M1 is monotone in the magnitude: if both brackets give the
+// same codes, those are the codes of the quotients.  Only when an element
+// sits that close to a rounding boundary (or 1/d is not finite) are the
+// eight quotients divided exactly.
+__device__ __forceinline__ uint32_t e2m1x8_of_quotients(const float (&x)[8], float d, float inv_lo,
+                                                        float inv_hi) {
+  float lo[8], hi[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    lo[i] = __fmul_rn(x[i], inv_lo);
+    hi[i] = __fmul_rn(x[i], inv_hi);
+  }
+  const uint32_t c = f32x8_to_e2m1_packed(lo);
+  if (c == f32x8_to_e2m1_packed(hi) && inv_hi < INFINITY) return c;
+  float q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], d);
+  return f32x8_to_e2m1_packed(q);
+}
+
+// The E4M3 block scale of u = RN(RN(a / 6) / s) the same way: a times
+// RN(RN(1/6) RN(1/s)) is within 2^-21.7 of u; bracketed by (1 -/+ 2^-20),
+// the exact two divisions run only next to a rounding boundary.
+__device__ __forceinline__ uint32_t e4m3_block_scale(float a, float s, float c_lo, float c_hi) {
+  if (s == 0.0f) return 0u;
+  const uint32_t lo = f32_to_e4m3_satfinite(__fmul_rn(a, c_lo));
+  if (lo == f32_to_e4m3_satfinite(__fmul_rn(a, c_hi)) && c_hi < INFINITY) return lo;
+  return f32_to_e4m3_satfinite(__fdiv_rn(__fdiv_rn(a, 6.0f), s));
+}
+
 // Pass 2: fold the partial maxima, then encode one 16-element block per thread.
 // MMA_LAYOUT: write the scale bytes in the tensor-core atom layout
 // (mma_scale_offset) instead of row-major.
@@ -98,45 +132,43 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(
   const float g = bf16_bits_to_f32(m < 0x7F80u ? m : 0u);
   const float s = __fdiv_rn(g, 2688.0f);
   if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s;
+  constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+  const float c6s = __fmul_rn(__frcp_rn(6.0f), __frcp_rn(s));  // ~ 1 / (6 s)
+  const float c_lo = __fmul_rn(c6s, kDown), c_hi = __fmul_rn(c6s, kUp);
 
-  // Warps stride over segments of 32 consecutive blocks of a row; each lane
-  // encodes one block of its warp's segment.
+  // Warps stride over segments of 64 consecutive blocks of a row; each lane
+  // encodes blocks lane and lane + 32 of its warp's segment, both loaded
+  // before either is encoded (four 16-byte loads in flight per thread).
   const int64_t blocks_per_row = K / 16;
-  const int64_t segs_per_row = ceil_div(blocks_per_row, 32);
+  const int64_t segs_per_row = ceil_div(blocks_per_row, 64);
   const int64_t total_segs = rows * segs_per_row;
   const int lane = threadIdx.x & 31;
-  for (int64_t seg = (int64_t)blockIdx.x * (kEncThreads / 32) + (threadIdx.x >> 5); seg < total_segs;
-       seg += (int64_t)gridDim.x * (kEncThreads / 32)) {
-    const int64_t r = seg / segs_per_row;
-    const int64_t b = (seg - r * segs_per_row) * 32 + lane;
-    if (b >= blocks_per_row) continue;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + b * 16);
-    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+  // (32-bit index arithmetic while the segment count allows: a 64-bit
+  // division per segment costs more than the block's encoding)
+  const bool narrow = total_segs < (int64_t)0x7FFFFFFF;
+  const uint32_t spr32 = (uint32_t)segs_per_row;
+  auto encode = [&](const uint4 v0, const uint4 v1, int64_t r, int64_t b) {
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     uint32_t a2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) a2 = __vmaxu2(a2, w[i] & 0x7FFF7FFFu);
     const float a = bf16_bits_to_f32(max(a2 & 0xFFFFu, a2 >> 16));
-    float u = 0.0f;
-    if (s != 0.0f) u = __fdiv_rn(__fdiv_rn(a, 6.0f), s);
-    const uint32_t sb = f32_to_e4m3_satfinite(u);
+    const uint32_t sb = e4m3_block_scale(a, s, c_lo, c_hi);
     const float d = __fmul_rn(f16lo_to_f32(e4m3x2_to_f16x2(sb)), s);
     uint32_t packed[2] = {0u, 0u};
     if (d != 0.0f) {
+      const float inv = __frcp_rn(d);
+      const float inv_lo = __fmul_rn(inv, kDown), inv_hi = __fmul_rn(inv, kUp);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float q[8];
-        uint32_t sign = 0;
+        float xv[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t wi = w[4 * h + i];
-          q[2 * i] = __fdiv_rn(bf16_bits_to_f32(wi & 0x7FFFu), d);
-          q[2 * i + 1] = __fdiv_rn(bf16_bits_to_f32((wi >> 16) & 0x7FFFu), d);
-          // sign of element 2i -> bit 3 of nibble 2i; element 2i+1 -> bit 3 of nibble 2i+1
-          sign |= ((wi >> 15) & 1u) << (8 * i + 3);
-          sign |= (wi >> 31) << (8 * i + 7);
+          xv[2 * i] = bf16_bits_to_f32(wi & 0xFFFFu);
+          xv[2 * i + 1] = bf16_bits_to_f32(wi >> 16);
         }
-        packed[h] = f32x8_to_e2m1_packed(q) | sign;
+        packed[h] = e2m1x8_of_quotients(xv, d, inv_lo, inv_hi);
       }
     }
     *reinterpret_cast<uint2 *>(codes + r * (K / 2) + b * 8) = make_uint2(packed[0], packed[1]);
@@ -144,6 +176,29 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(
       scales[mma_scale_offset(r, b, K)] = static_cast<uint8_t>(sb);
     else
       scales[r * blocks_per_row + b] = static_cast<uint8_t>(sb);
+  };
+  for (int64_t seg = (int64_t)blockIdx.x * (kEncThreads / 32) + (threadIdx.x >> 5); seg < total_segs;
+       seg += (int64_t)gridDim.x * (kEncThreads / 32)) {
+    int64_t r, b;
+    if (narrow) {
+      const uint32_t r32 = (uint32_t)seg / spr32;
+      r = r32;
+      b = (int64_t)(((uint32_t)seg - r32 * spr32) * 64u + (uint32_t)lane);
+    } else {
+      r = seg / segs_per_row;
+      b = (seg - r * segs_per_row) * 64 + lane;
+    }
+    if (b >= blocks_per_row) continue;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + b * 16);
+    const bool two = b + 32 < blocks_per_row;
+    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    uint4 v2 = make_uint4(0, 0, 0, 0), v3 = v2;
+    if (two) {
+      v2 = __ldg(src + 64);  // block b + 32: 32 blocks x 32 bytes further
+      v3 = __ldg(src + 65);
+    }
+    encode(v0, v1, r, b);
+    if (two) encode(v2, v3, r, b + 32);
   }
 }
 
@@ -187,7 +242,7 @@ cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t 
   const int ga = amax_grid(rows);
   uint32_t *partial = static_cast<uint32_t *>(workspace);
   amax_partial_kernel<<<ga, kAmaxThreads, 0, stream>>>(x, rows, K, ldx, partial, status);
-  const int64_t segs = rows * ceil_div(K / 16, 32);
+  const int64_t segs = rows * ceil_div(K / 16, 64);
   int64_t ge = ceil_div(segs, kEncThreads / 32);
   const int64_t cap = (int64_t)num_sms_cached() * 8;
   if (ge > cap) ge = cap;
@@ -350,7 +405,7 @@ cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int6
   const int ga = amax_grid(rows);
   uint32_t *partial = static_cast<uint32_t *>(workspace);
   amax_partial_kernel<<<ga, kAmaxThreads, 0, stream>>>(x, rows, K, ldx, partial, status);
-  const int64_t segs = rows * ceil_div(K / 16, 32);
+  const int64_t segs = rows * ceil_div(K / 16, 64);
   int64_t ge = ceil_div(segs, kEncThreads / 32);
   const int64_t cap = (int64_t)num_sms_cached() * 8;
   if (ge > cap) ge = cap;
@@ -450,6 +505,7 @@ __global__ void __launch_bounds__(kEncThreads) fp8_encode_kernel(
   m = block_max_u32<kEncThreads>(m, red);
   const float g = bf16_bits_to_f32(m < 0x7F80u ? m : 0u);
   const float s8 = __fdiv_rn(g, 448.0f);
+  const float inv8 = __frcp_rn(s8);
   if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s8;
   const int64_t per_row = K / 8, total = rows * per_row;
   for (int64_t i = (int64_t)blockIdx.x * kEncThreads + threadIdx.x; i < total;
@@ -459,13 +515,31 @@ __global__ void __launch_bounds__(kEncThreads) fp8_encode_kernel(
     if (s8 != 0.0f) {
       const uint4 t = __ldg(reinterpret_cast<const uint4 *>(x + r * ldx + 8 * j));
       const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-      uint32_t b[4];
+      float m[8];
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const float lo = __fdiv_rn(bf16_bits_to_f32(w[v] & 0x7FFFu), s8);
-        const float hi = __fdiv_rn(bf16_bits_to_f32((w[v] >> 16) & 0x7FFFu), s8);
-        b[v] = f32x2_to_e4m3x2(lo, hi) | ((w[v] >> 8) & 0x80u) | ((w[v] >> 16) & 0x8000u);
+        m[2 * v] = bf16_bits_to_f32(w[v] & 0x7FFFu);
+        m[2 * v + 1] = bf16_bits_to_f32((w[v] >> 16) & 0x7FFFu);
       }
+      // as e2m1x8_of_quotients: m * RN(1/s8), with the exact division only
+      // next to a rounding boundary of E4M3
+      constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+      uint32_t b[4];
+      bool exact = true;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const float q0 = __fmul_rn(m[2 * v], inv8), q1 = __fmul_rn(m[2 * v + 1], inv8);
+        b[v] = f32x2_to_e4m3x2(q0, q1);
+        exact = exact && b[v] == f32x2_to_e4m3x2(__fmul_rn(q0, kDown), __fmul_rn(q1, kDown)) &&
+                b[v] == f32x2_to_e4m3x2(__fmul_rn(q0, kUp), __fmul_rn(q1, kUp));
+      }
+      if (!exact || !(inv8 < INFINITY)) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          b[v] = f32x2_to_e4m3x2(__fdiv_rn(m[2 * v], s8), __fdiv_rn(m[2 * v + 1], s8));
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v) b[v] |= ((w[v] >> 8) & 0x80u) | ((w[v] >> 16) & 0x8000u);
       out = make_uint2(b[0] | b[1] << 16, b[2] | b[3] << 16);
     }
     *reinterpret_cast<uint2 *>(codes + r * K + 8 * j) = out;

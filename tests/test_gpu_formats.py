@@ -207,3 +207,41 @@ def test_fp8_gemv_repeatable_and_plan():
     assert pkg.imp_fp8_gemm_plan(1, 5120, 5120) == (2, "gemv_f4r_kernel")
     assert pkg.imp_fp8_gemm_plan(5, 5120, 5120) == (6, "gemv_f4r_kernel")
     assert pkg.imp_fp8_gemm_plan(17, 5120, 5120) == (0, None)
+
+
+def test_fp8_quotients_next_to_rounding_boundaries():
+    """Elements whose x / s8 lies within 2^-20 (relative) of the midpoint of
+    two E4M3 values, where a quotient computed as x * (1/s8) could round
+    differently from the division.  Each tensor's amax g (exact in bf16, not
+    a multiple of 7) gives s8 = g / 448 a full 24-bit mantissa; the search
+    runs over many g."""
+    e4 = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    mids = (e4[:-1] + e4[1:]) / 2
+    mids = mids[mids > 2.0 ** -6]
+    found = 0
+    rng = np.random.default_rng(0)
+    for gi in range(256, 448):
+        g = np.float32(gi)
+        if gi % 7 == 0:
+            continue
+        s8 = float(np.float32(g / np.float32(448.0)))
+        cand = torch.tensor(mids * s8).bfloat16().float()
+        near = []
+        for c in (cand, torch.nextafter(cand, torch.zeros_like(cand)).bfloat16().float(),
+                  torch.nextafter(cand, torch.full_like(cand, 1e30)).bfloat16().float()):
+            v = c.double().numpy()
+            ok = (v > 0) & (v < gi) & (np.abs(v / s8 - mids) / mids < 2.0 ** -20)
+            near += v[ok].tolist()
+        if not near:
+            continue
+        row = np.zeros(128, np.float32)
+        row[0] = g
+        row[1:1 + min(len(near), 127)] = near[:127]
+        row *= np.where(rng.random(128) < 0.5, -1.0, 1.0).astype(np.float32)
+        bits = torch.from_numpy(row.reshape(1, 128)).bfloat16().view(torch.int16).numpy().view(np.uint16)
+        t = pkg.fp8_quantize(dev_bf16(bits))
+        c, s, _ = oracle.fp8_quantize(bits)
+        assert np.float32(t.tensor_scale.item()) == np.float32(s)
+        np.testing.assert_array_equal(t.codes.cpu().numpy(), c)
+        found += len(near)
+    assert found >= 10

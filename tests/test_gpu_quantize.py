@@ -126,3 +126,45 @@ def test_repeatable():
     bits = synth.workload("decode_0p6b")[6].weight_bf16()
     a, b = gpu_quantize(bits), gpu_quantize(bits)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2] == b[2]
+
+
+def _near_boundary_tensor(seed, n_blocks=512):
+    """Rows of 16-element blocks whose elements x make x / d land within
+    2^-20 (relative) of an E2M1 rounding boundary without being on it, plus
+    exact ties -- the cases a quotient computed as x * (1/d) could round
+    differently from the division.  Found by search on the CPU: the tensor
+    scale is fixed by one element g; each block's amax a sets d."""
+    rng = np.random.default_rng(seed)
+    g = np.float32(1992.0)  # exact in bf16; s = g / 2688 has a full 24-bit mantissa
+    s = np.float32(g / np.float32(2688.0))
+    bounds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    blocks = []
+    while len(blocks) < n_blocks:
+        a = np.float32(torch.tensor(float(rng.uniform(0.05, 1.9) * float(g) / 6)).bfloat16().float().item())
+        u = np.float32(np.float32(a / np.float32(6.0)) / s)
+        sb = torch.tensor([float(u)]).to(torch.float8_e4m3fn).float().item()
+        d = np.float32(np.float32(sb) * s)
+        xs = []
+        for t in bounds:
+            target = t * float(d)
+            b = torch.tensor([target]).bfloat16()
+            for cand in (b.float().item(), torch.nextafter(b.float(), torch.tensor([0.0])).bfloat16().float().item(),
+                         torch.nextafter(b.float(), torch.tensor([1e30])).bfloat16().float().item()):
+                rel = abs(cand / float(d) - t) / t
+                if rel < 2.0 ** -20 and cand <= float(a):
+                    xs.append(cand)
+        if xs:
+            row = [float(a)] + xs[:15]
+            row += [0.0] * (16 - len(row))
+            blocks.append(row)
+    x = np.array(blocks, np.float32).reshape(-1, 32 * 16)[: n_blocks // 32]
+    x[0, 1] = g
+    x *= np.where(rng.random(x.shape) < 0.5, -1.0, 1.0).astype(np.float32)
+    return torch.from_numpy(x).bfloat16().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quotients_next_to_rounding_boundaries():
+    bits = _near_boundary_tensor(0)
+    got = gpu_quantize(bits)
+    assert got[3] == 0
+    assert_same(got, oracle.quantize(bits), "near-boundary quotients")
