@@ -770,7 +770,60 @@ def bench_prefill(args, pkg, dev, stream):
         del w, wm, x, xq, y, ws, wsf
     res["fp4_peak_tflops"] = peak
     res["fp4_peak_kind"] = f"{kind} bf16 x 6 (nominal fp4:bf16 ratio)"
+    res["mlp_27b"] = bench_prefill_mlp(args, pkg, dev, stream, peak)
     return res
+
+
+def bench_prefill_mlp(args, pkg, dev, stream, peak):
+    """The 27B-class MLP at M = 2048 (X 2048 x 5120 -> gate/up 17408 ->
+    SwiGLU -> down 5120): fused = imp_nvfp4_gemm_swiglu (X quantization +
+    gate/up GEMM with the activation and the amax of h in its epilogue) +
+    imp_nvfp4_quantize_mma_amax (one read of h) + the down GEMM; unfused =
+    imp_nvfp4_gemm_mma for gate and for up + the two-pass quantizer of h +
+    the down GEMM (the activation itself, which the library has no separate
+    kernel for, left out: the unfused figure is a lower bound)."""
+    import torch
+
+    lg = [l for l in synth.workload("prefill_27b") if l.K == 5120][0]
+    ld = [l for l in synth.workload("prefill_27b") if l.K == 17408][0]
+    lu = synth.Linear("up_27b", lg.M, lg.K, lg.N, 41, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
+                      zero_block_p=0.001)
+    mk = lambda l: pkg.prepare_mma(pkg.quantize(  # noqa: E731
+        torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)))
+    wg, wu, wd = mk(lg), mk(lu), mk(ld)
+    x = torch.from_numpy(lg.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
+    h = torch.empty((lg.M, lg.N), dtype=torch.bfloat16, device=dev)
+    hu = torch.empty_like(h)
+    amax = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = torch.empty((ld.M, ld.N), dtype=torch.bfloat16, device=dev)
+    wss = torch.empty(pkg.imp_nvfp4_gemm_swiglu_workspace_size(lg.M, lg.N, lg.K), dtype=torch.uint8,
+                      device=dev)
+    wsg = torch.empty(pkg.imp_nvfp4_gemm_workspace_size(lg.M, lg.N, lg.K), dtype=torch.uint8,
+                      device=dev)
+    hq = pkg.quantize_mma(h)
+
+    def fused():
+        pkg.gemm_swiglu(x, wg, wu, h=h, h_amax=amax, stream=stream, workspace=wss)
+        q = pkg.quantize_mma_amax(h, amax, stream=stream)
+        pkg.gemm_fp4(q, wd, y=y, stream=stream)
+
+    def unfused():
+        pkg.gemm_mma(x, wg, y=h, stream=stream, workspace=wsg)
+        pkg.gemm_mma(x, wu, y=hu, stream=stream, workspace=wsg)
+        q = pkg.quantize_mma(h, stream=stream)
+        pkg.gemm_fp4(q, wd, y=y, stream=stream)
+
+    flops = 2.0 * lg.M * lg.K * lg.N * 2 + 2.0 * ld.M * ld.K * ld.N
+    out = {"shapes": {"x": [lg.M, lg.K], "gate_up_N": lg.N, "down_N": ld.N}, "flop": flops}
+    for name, fn in (("fused", fused), ("unfused_without_activation", unfused)):
+        for _ in range(args.warmup):
+            fn()
+        ts = time_blocks(fn, 5, 6, stream)
+        t = statistics.median(ts)
+        out[name] = {"us": spread(ts), "TFLOP/s": flops / (t * 1e-6) / 1e12,
+                     "frac_of_fp4_peak": flops / (t * 1e-6) / 1e12 / peak}
+    del wg, wu, wd, x, h, hu, y, wss, wsg, hq
+    return out
 
 
 def bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs, chained, ys, wss,

@@ -313,6 +313,43 @@ imp_status imp_nvfp4_gemm_grouped(const void *x_bf16, int64_t M, int64_t K, int6
                                   int32_t *dev_status, void *workspace, size_t ws_bytes,
                                   void *stream);
 
+/* ---- fused prefill MLP pieces -------------------------------------------------
+ * A layer's MLP ("1. The big picture": the MLP transforms each token's vector
+ * on its own) in the Qwen-class models the pages run is gate and up
+ * projections, h = silu(gate) * up, then the down projection.  These two
+ * calls fuse the activation into the gate/up GEMM's epilogue and fold the
+ * global amax of h into it, so the down projection's activation quantizer
+ * reads h once instead of twice.  Additions of this library.            */
+
+/* Workspace of imp_nvfp4_gemm_swiglu (X's quantization), 0 if rejected. */
+size_t imp_nvfp4_gemm_swiglu_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* h = silu(X Wg^T) * (X Wu^T) for prefill (M > 16): X quantized on device as
+ * in imp_nvfp4_gemm, both products on the block-scaled FP4 tensor cores in
+ * one kernel (each 256-row W tile = 128 rows of Wg + the same 128 rows of
+ * Wu), silu(v) = v / (1 + e^-v) and the product in fp32, h rounded to bf16.
+ *   w_gate, w_up  MMA layout (imp_nvfp4_prepare_mma), same N and K.
+ *   h_bf16        device bf16[M][ldh], ldh >= N, ldh % 8 == 0.
+ *   h_amax        device uint32, 4-byte aligned: receives the largest |h| as
+ *                 bf16 magnitude bits (zeroed by this call), for
+ *                 imp_nvfp4_quantize_mma_amax.  A non-finite h sets
+ *                 IMP_DEV_NONFINITE_INPUT.
+ *   M <= 16 returns IMP_ERR_UNSUPPORTED_SHAPE.  Accuracy: g and u within
+ *   the fp32 accumulation of exact products, then the two roundings above. */
+imp_status imp_nvfp4_gemm_swiglu(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                 const imp_nvfp4_tensor *w_gate, const imp_nvfp4_tensor *w_up,
+                                 void *h_bf16, int64_t ldh, uint32_t *h_amax,
+                                 int32_t *dev_status, void *workspace, size_t ws_bytes,
+                                 void *stream);
+
+/* imp_nvfp4_quantize_mma with the global amax already known (bf16 magnitude
+ * bits of max|x| in device memory, as imp_nvfp4_gemm_swiglu writes it): the
+ * encode pass alone, one read of X.  Bit-identical to imp_nvfp4_quantize_mma
+ * when *amax is the true max|x|.  rows >= 1, K % 64 == 0.                 */
+imp_status imp_nvfp4_quantize_mma_amax(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                                       const uint32_t *amax, const imp_nvfp4_tensor *out,
+                                       int32_t *dev_status, void *stream);
+
 /* ---- other weight formats ---------------------------------------------------
  * The imp README's feature matrix lists, besides NVFP4 (the primary path),
  * MXFP4 and FP8 E4M3 weights.                                              */

@@ -36,7 +36,8 @@ __all__ = [
     "imp_mxfp4_to_nvfp4", "imp_mxfp4_to_nvfp4_workspace_size", "imp_fp8_quantize",
     "imp_fp8_quantize_workspace_size", "imp_fp8_gemm", "imp_fp8_gemm_workspace_size",
     "imp_fp8_gemm_plan", "MXFP4Tensor", "FP8Tensor", "mxfp4_quantize", "mxfp4_to_nvfp4",
-    "fp8_quantize", "gemm_fp8",
+    "fp8_quantize", "gemm_fp8", "imp_nvfp4_gemm_swiglu", "imp_nvfp4_gemm_swiglu_workspace_size",
+    "imp_nvfp4_quantize_mma_amax", "gemm_swiglu", "quantize_mma_amax",
 ]
 
 IMP_OK = 0
@@ -146,6 +147,12 @@ def _L():
     lib.imp_fp8_gemm_plan.argtypes = [I64, I64, I64, ctypes.POINTER(ctypes.c_char_p)]
     lib.imp_fp8_gemm.restype = ctypes.c_int
     lib.imp_fp8_gemm.argtypes = [P, I64, I64, I64, F8, P, I64, P, P, SZ, P]
+    lib.imp_nvfp4_gemm_swiglu_workspace_size.restype = SZ
+    lib.imp_nvfp4_gemm_swiglu_workspace_size.argtypes = [I64, I64, I64]
+    lib.imp_nvfp4_gemm_swiglu.restype = ctypes.c_int
+    lib.imp_nvfp4_gemm_swiglu.argtypes = [P, I64, I64, I64, T, T, P, I64, P, P, P, SZ, P]
+    lib.imp_nvfp4_quantize_mma_amax.restype = ctypes.c_int
+    lib.imp_nvfp4_quantize_mma_amax.argtypes = [P, I64, I64, I64, P, T, P, P]
     _lib = lib
     return lib
 
@@ -316,6 +323,25 @@ def imp_fp8_gemm(x_bf16: int, M: int, K: int, ldx: int, w: ImpFp8Tensor, y_bf16:
                  stream: int | None) -> int:
     return _L().imp_fp8_gemm(x_bf16, M, K, ldx, ctypes.byref(w), y_bf16, ldy, dev_status,
                              workspace, ws_bytes, stream)
+
+
+def imp_nvfp4_gemm_swiglu_workspace_size(M: int, N: int, K: int) -> int:
+    return _L().imp_nvfp4_gemm_swiglu_workspace_size(M, N, K)
+
+
+def imp_nvfp4_gemm_swiglu(x_bf16: int, M: int, K: int, ldx: int, w_gate: ImpNvfp4Tensor,
+                          w_up: ImpNvfp4Tensor, h_bf16: int, ldh: int, h_amax: int,
+                          dev_status: int | None, workspace: int | None, ws_bytes: int,
+                          stream: int | None) -> int:
+    return _L().imp_nvfp4_gemm_swiglu(x_bf16, M, K, ldx, ctypes.byref(w_gate), ctypes.byref(w_up),
+                                      h_bf16, ldh, h_amax, dev_status, workspace, ws_bytes, stream)
+
+
+def imp_nvfp4_quantize_mma_amax(x_bf16: int, rows: int, K: int, ldx: int, amax: int,
+                                out: ImpNvfp4Tensor, dev_status: int | None,
+                                stream: int | None) -> int:
+    return _L().imp_nvfp4_quantize_mma_amax(x_bf16, rows, K, ldx, amax, ctypes.byref(out),
+                                            dev_status, stream)
 
 
 class ImpError(RuntimeError):
@@ -613,3 +639,47 @@ def gemm_fp8(x, w: FP8Tensor, y=None, dev_status=None, stream=None, workspace=No
     if st != IMP_OK:
         raise ImpError(st, "imp_fp8_gemm")
     return y
+
+
+def gemm_swiglu(x, w_gate: NVFP4Tensor, w_up: NVFP4Tensor, h=None, h_amax=None, dev_status=None,
+                stream=None, workspace=None):
+    """(h, h_amax): h = silu(X Wg^T) * (X Wu^T) for a prefill-sized bf16 X and
+    gate/up weights in MMA layout; h_amax = max|h| as bf16 magnitude bits
+    (device int32[1])."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert w_gate.layout == "mma" and w_up.layout == "mma"
+    M, K = x.shape
+    N = w_gate.rows
+    if h is None:
+        h = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=x.device)[:, :N]
+    if h_amax is None:
+        h_amax = torch.zeros(1, dtype=torch.int32, device=x.device)
+    wsb = imp_nvfp4_gemm_swiglu_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 16), dtype=torch.uint8, device=x.device)
+    st = imp_nvfp4_gemm_swiglu(x.data_ptr(), M, K, x.stride(0), w_gate.c_struct(), w_up.c_struct(),
+                               h.data_ptr(), h.stride(0), h_amax.data_ptr(),
+                               None if dev_status is None else dev_status.data_ptr(),
+                               workspace.data_ptr(), wsb, _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_gemm_swiglu")
+    return h, h_amax
+
+
+def quantize_mma_amax(x, amax, dev_status=None, stream=None) -> NVFP4Tensor:
+    """quantize_mma with the global amax given (device int32[1], bf16 bits)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, K = x.shape
+    out = NVFP4Tensor(torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device),
+                      torch.empty(imp_nvfp4_mma_scales_size(rows, K), dtype=torch.uint8,
+                                  device=x.device),
+                      torch.empty(1, dtype=torch.float32, device=x.device))
+    st = imp_nvfp4_quantize_mma_amax(x.data_ptr(), rows, K, x.stride(0), amax.data_ptr(),
+                                     _struct(out),
+                                     None if dev_status is None else dev_status.data_ptr(),
+                                     _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_quantize_mma_amax")
+    return out

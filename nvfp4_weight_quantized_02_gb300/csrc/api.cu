@@ -524,4 +524,69 @@ imp_status imp_fp8_gemm(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
                                            workspace, static_cast<cudaStream_t>(stream)));
 }
 
+// ---- fused prefill MLP pieces ---------------------------------------------------
+
+size_t imp_nvfp4_gemm_swiglu_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= kDecodeMaxM || N < 1 || K <= 0 || K % 64) return 0;
+  return prefill_ws(M, N, K).total;
+}
+
+imp_status imp_nvfp4_gemm_swiglu(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                 const imp_nvfp4_tensor *w_gate, const imp_nvfp4_tensor *w_up,
+                                 void *h_bf16, int64_t ldh, uint32_t *h_amax,
+                                 int32_t *dev_status, void *workspace, size_t ws_bytes,
+                                 void *stream) {
+  if (M < 0 || !w_gate || !w_up) return IMP_ERR_INVALID_ARG;
+  if (K <= 0 || K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  const int64_t N = w_gate->rows;
+  if (N < 1 || w_up->rows != N || w_gate->K != K || w_up->K != K) return IMP_ERR_INVALID_ARG;
+  imp_status st = check_tensor(w_gate, N, K);
+  if (st == IMP_OK) st = check_tensor(w_up, N, K);
+  if (st != IMP_OK) return st;
+  if (M == 0) return IMP_OK;
+  if (!x_bf16 || !h_bf16 || !h_amax || ldx < K || ldh < N) return IMP_ERR_INVALID_ARG;
+  if (M <= kDecodeMaxM || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+    return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x_bf16) || !aligned16(h_bf16) || !aligned4(h_amax) || ldx % 8 || ldh % 8)
+    return IMP_ERR_MISALIGNED;
+  const size_t need = imp_nvfp4_gemm_swiglu_workspace_size(M, N, K);
+  if (!workspace || ws_bytes < need) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  const PrefillWs L = prefill_ws(M, N, K);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  imp_nvfp4_tensor xq = {ws + L.xcodes, ws + L.xsc, reinterpret_cast<float *>(ws + L.sx), M, K};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  impfp4::GemmMxf4Plan plan;
+  cudaError_t e = impfp4::plan_gemm_mxf4_swiglu(
+      xq.codes, xq.scales, xq.tensor_scale, w_gate->codes, w_gate->scales, w_gate->tensor_scale,
+      w_up->codes, w_up->scales, w_up->tensor_scale, M, N, K, static_cast<uint16_t *>(h_bf16), ldh,
+      h_amax, dev_status, plan);
+  if (e != cudaSuccess) return IMP_ERR_CUDA;
+  e = cudaMemsetAsync(h_amax, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)
+    e = impfp4::launch_quantize_mma(static_cast<const uint16_t *>(x_bf16), M, K, ldx, xq.codes,
+                                    xq.scales, xq.tensor_scale, dev_status, ws + L.partial, s);
+  if (e == cudaSuccess) e = impfp4::enqueue_gemm_mxf4(plan, s);
+  return from_cuda(e);
+}
+
+imp_status imp_nvfp4_quantize_mma_amax(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
+                                       const uint32_t *amax, const imp_nvfp4_tensor *out,
+                                       int32_t *dev_status, void *stream) {
+  (void)dev_status;
+  if (rows < 1 || K <= 0 || !x_bf16 || !amax) return IMP_ERR_INVALID_ARG;
+  if (K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K) return IMP_ERR_INVALID_ARG;
+  if (!out || out->rows != rows || out->K != K || !out->codes || !out->scales ||
+      !out->tensor_scale)
+    return IMP_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || ldx % 8 || !aligned16(out->codes) || !aligned4(amax) ||
+      !aligned4(out->tensor_scale))
+    return IMP_ERR_MISALIGNED;
+  return from_cuda(impfp4::launch_encode_with_amax(static_cast<const uint16_t *>(x_bf16), rows, K,
+                                                   ldx, amax, out->codes, out->scales,
+                                                   out->tensor_scale, true,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

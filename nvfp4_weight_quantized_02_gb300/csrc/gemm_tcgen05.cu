@@ -77,6 +77,14 @@ struct GemmArgs {
   float *part;             // [CTA][first/last segment][128 rows][256 columns]
   unsigned long long epoch;
   int stream_k;
+  // SwiGLU (w2_tiles set; whole tiles, tiled weights): a tile's 256 W rows
+  // are 128 rows of the gate weight (w_tiles, sfb, s_w) and the same 128
+  // rows of the up weight (w2_tiles, sfb2, s_w2); the epilogue writes
+  // h = silu(g) * u for 128 columns and folds max|h| (bf16 magnitude bits)
+  // into *h_amax.
+  const uint8_t *w2_tiles, *sfb2;
+  const float *s_w2;
+  uint32_t *h_amax;
 };
 
 // The work of one CTA as segments (tile, K-stage range), in processing order.
@@ -220,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int MB = (a.M + BM - 1) / BM, NB = (a.N + BN - 1) / BN;
+  const bool swiglu = a.w2_tiles != nullptr;
+  const int bn_out = swiglu ? BN / 2 : BN;  // output columns per tile
+  const int MB = (a.M + BM - 1) / BM, NB = (a.N + bn_out - 1) / bn_out;
   const int n_tiles = MB * NB;
   const int n_ks = (a.K + BK - 1) / BK;
   const int KA = a.K / 64;  // scale atoms per 128-row block
@@ -274,23 +284,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t *st = smem + (size_t)s * STAGE_BYTES;
           mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES + 3u * natoms * 512u);
           tma_load_2d(st, &tmA, ks * (BK / 2), mb * BM, &full[s]);
+          // the two 128-row halves of the W tile: 128-row blocks 2 nb and
+          // 2 nb + 1 of W, or (SwiGLU) block nb of the gate and of the up weight
+          const int64_t blk0 = swiglu ? nb : 2 * nb, blk1 = swiglu ? nb : 2 * nb + 1;
+          const uint8_t *w1 = swiglu ? a.w2_tiles : a.w_tiles;
+          const uint8_t *sf1 = swiglu ? a.sfb2 : a.sfb;
           if (a.w_tiles) {
             // two 128-row tiles, each stored as its swizzled shared-memory image
             const int64_t nch = (a.K + BK - 1) / BK;
-            bulk_g2s(st + OFF_B, a.w_tiles + ((int64_t)(2 * nb) * nch + ks) * 16384, 16384u,
-                     &full[s]);
-            bulk_g2s(st + OFF_B + 16384, a.w_tiles + ((int64_t)(2 * nb + 1) * nch + ks) * 16384,
-                     16384u, &full[s]);
+            bulk_g2s(st + OFF_B, a.w_tiles + (blk0 * nch + ks) * 16384, 16384u, &full[s]);
+            bulk_g2s(st + OFF_B + 16384, w1 + (blk1 * nch + ks) * 16384, 16384u, &full[s]);
           } else {
             tma_load_2d(st + OFF_B, &tmB, ks * (BK / 2), nb * BN, &full[s]);
           }
           const int64_t atom0 = (int64_t)ks * KSTEPS;
           bulk_g2s(st + OFF_SFA, a.sfa + ((int64_t)mb * KA + atom0) * 512, natoms * 512u,
                    &full[s]);
-          bulk_g2s(st + OFF_SFB, a.sfb + ((int64_t)(2 * nb) * KA + atom0) * 512, natoms * 512u,
+          bulk_g2s(st + OFF_SFB, a.sfb + (blk0 * KA + atom0) * 512, natoms * 512u, &full[s]);
+          bulk_g2s(st + OFF_SFB + 2048, sf1 + (blk1 * KA + atom0) * 512, natoms * 512u,
                    &full[s]);
-          bulk_g2s(st + OFF_SFB + 2048, a.sfb + ((int64_t)(2 * nb + 1) * KA + atom0) * 512,
-                   natoms * 512u, &full[s]);
         }
       }
       if (!ok) {
@@ -414,11 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = (*a.s_x) * (*a.s_w);
     // bf16 of 32 fp32 values (times s_x s_w) to columns c .. c + 31 of this
     // thread's part of row m
-    auto store_bf16 = [&](int64_t m, int n0, int c, const float (&v)[32]) {
+    auto store_bf16 = [&](int64_t m, int n0, int c, const float (&v)[32], float sc) {
       if (m >= a.M) return;
       uint32_t p[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) p[i] = pack_bf16(v[2 * i] * scale, v[2 * i + 1] * scale);
+      for (int i = 0; i < 16; ++i) p[i] = pack_bf16(v[2 * i] * sc, v[2 * i + 1] * sc);
       uint16_t *dst = a.y + m * a.ldy + n0 + c;
       if (n0 + c + 32 <= a.N) {
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);
@@ -445,6 +457,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       sch.seg(jj, t, k0, k1);
       const int mb = t % MB, nb = t / MB;
       const int64_t m = (int64_t)mb * BM + row_in_tile;
+      if (swiglu) {
+        // This warp's 64 of the tile's 128 output columns: gate accumulators
+        // in columns c, up in 128 + c of its lane quarter.
+        const int h0 = (warp - 2) / 4 * 64;
+        const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D;
+        const float sg = (*a.s_x) * (*a.s_w), su = (*a.s_x) * (*a.s_w2);
+        const int n0 = nb * (BN / 2) + h0;
+        uint32_t hmax = 0;
+        bool finite = true;
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t rg[32], ru[32];
+          tc_ld32(tq + h0 + c, rg);
+          tc_ld32(tq + BN / 2 + h0 + c, ru);
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float g = __uint_as_float(rg[i]) * sg, u = __uint_as_float(ru[i]) * su;
+            v[i] = g / (1.0f + expf(-g)) * u;  // silu(g) * u
+            const uint32_t hb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[i])) & 0x7FFFu;
+            const bool in = m < a.M && n0 + c + i < a.N;
+            if (in) {
+              hmax = max(hmax, hb < 0x7F80u ? hb : 0u);
+              finite = finite && hb < 0x7F80u;
+            }
+          }
+          store_bf16(m, n0, c, v, 1.0f);
+        }
+        tc_fence_before();
+        mbar_arrive(acce);
+        for (int o = 16; o; o >>= 1) hmax = max(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, o));
+        if (!__all_sync(0xFFFFFFFFu, finite) && lane == 0) report(a.status, IMP_DEV_NONFINITE_INPUT);
+        if (lane == 0 && hmax) atomicMax(a.h_amax, hmax);
+        continue;
+      }
       const int n0 = nb * BN + col0;
       const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D + col0;
       if (k0 == 0 && k1 == n_ks) {
@@ -458,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          store_bf16(m, n0, c, v);
+          store_bf16(m, n0, c, v, scale);
         }
         tc_fence_before();
         mbar_arrive(acce);  // accumulator may be overwritten now
@@ -525,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * i + 3] += q[i].w;
           }
         }
-        store_bf16(m, n0, c, v);
+        store_bf16(m, n0, c, v, scale);
       }
     }
   }
@@ -618,6 +665,7 @@ cudaError_t plan_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales, 
                                     (uint64_t)(K / 2), BN, 128, true)))
     return cudaErrorInvalidValue;
   GemmArgs &a = p.a;
+  a = GemmArgs{};
   a.sfa = x_mma_scales;
   a.sfb = w_mma_scales;
   a.w_tiles = w_tiled ? w_codes : nullptr;
@@ -643,6 +691,25 @@ cudaError_t plan_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales, 
   p.grid = (int)gemm_grid(M, N, K, workspace != nullptr);
   return cudaFuncSetAttribute(gemm_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)kSmemBytes);
+}
+
+cudaError_t plan_gemm_mxf4_swiglu(const uint8_t *x_codes, const uint8_t *x_mma_scales,
+                                  const float *s_x, const uint8_t *gate_tiles,
+                                  const uint8_t *gate_scales, const float *s_gate,
+                                  const uint8_t *up_tiles, const uint8_t *up_scales,
+                                  const float *s_up, int64_t M, int64_t N, int64_t K, uint16_t *h,
+                                  int64_t ldh, uint32_t *h_amax, int32_t *status,
+                                  GemmMxf4Plan &plan) {
+  const cudaError_t e = plan_gemm_mxf4(x_codes, x_mma_scales, s_x, gate_tiles, true, gate_scales,
+                                       s_gate, M, N, K, h, ldh, status, nullptr, plan);
+  if (e != cudaSuccess) return e;
+  GemmArgs &a = plan.impl->a;
+  a.w2_tiles = up_tiles;
+  a.sfb2 = up_scales;
+  a.s_w2 = s_up;
+  a.h_amax = h_amax;
+  plan.impl->grid = (int)gemm_grid(M, 2 * N, K, false);  // 128 output columns per tile
+  return cudaSuccess;
 }
 
 cudaError_t enqueue_gemm_mxf4(const GemmMxf4Plan &plan, cudaStream_t stream) {

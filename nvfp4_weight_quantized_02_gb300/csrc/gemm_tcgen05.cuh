@@ -36,6 +36,18 @@ cudaError_t plan_gemm_mxf4(const uint8_t *x_codes, const uint8_t *x_mma_scales, 
                            const float *s_w, int64_t M, int64_t N, int64_t K, uint16_t *y,
                            int64_t ldy, int32_t *status, void *workspace, GemmMxf4Plan &plan);
 
+// Plan the SwiGLU form: h[M][N] = silu(s_x s_g (Xq . Wg^T)) * s_x s_u (Xq . Wu^T),
+// gate and up weights in the tile layout (same N and K), whole tiles of 128
+// output columns; the kernel folds max|h| (bf16 magnitude bits) into
+// *h_amax with atomicMax (the caller zeroes it).  Enqueues nothing.
+cudaError_t plan_gemm_mxf4_swiglu(const uint8_t *x_codes, const uint8_t *x_mma_scales,
+                                  const float *s_x, const uint8_t *gate_tiles,
+                                  const uint8_t *gate_scales, const float *s_gate,
+                                  const uint8_t *up_tiles, const uint8_t *up_scales,
+                                  const float *s_up, int64_t M, int64_t N, int64_t K, uint16_t *h,
+                                  int64_t ldh, uint32_t *h_amax, int32_t *status,
+                                  GemmMxf4Plan &plan);
+
 // Enqueue a planned GEMM on `stream`.
 cudaError_t enqueue_gemm_mxf4(const GemmMxf4Plan &plan, cudaStream_t stream);
 

@@ -399,6 +399,23 @@ cudaError_t launch_quantize_noalloc(const uint16_t *x, int64_t rows, int64_t K, 
   return launch_quantize(x, rows, K, ldx, codes, scales, tensor_scale, status, addr, stream);
 }
 
+cudaError_t launch_encode_with_amax(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                                   const uint32_t *amax_bits, uint8_t *codes, uint8_t *scales,
+                                   float *tensor_scale, bool mma_layout, cudaStream_t stream) {
+  const int64_t segs = rows * ceil_div(K / 16, 64);
+  int64_t ge = ceil_div(segs, kEncThreads / 32);
+  const int64_t cap = (int64_t)num_sms_cached() * 8;
+  if (ge > cap) ge = cap;
+  if (ge < 1) ge = 1;
+  if (mma_layout)
+    encode_kernel<true><<<static_cast<int>(ge), kEncThreads, 0, stream>>>(
+        x, rows, K, ldx, amax_bits, 1, codes, scales, tensor_scale);
+  else
+    encode_kernel<false><<<static_cast<int>(ge), kEncThreads, 0, stream>>>(
+        x, rows, K, ldx, amax_bits, 1, codes, scales, tensor_scale);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
                                 uint8_t *codes, uint8_t *mma_scales, float *tensor_scale,
                                 int32_t *status, void *workspace, cudaStream_t stream) {

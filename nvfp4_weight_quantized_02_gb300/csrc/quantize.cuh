@@ -93,6 +93,13 @@ cudaError_t launch_code_relayout(const uint8_t *codes, int64_t rows, int64_t K, 
 cudaError_t launch_scale_relayout(const uint8_t *scales, int64_t rows, int64_t K,
                                   uint8_t *mma_scales, cudaStream_t stream);
 
+// The encode pass alone, the global amax given (bf16 magnitude bits of
+// max|x| in device memory, e.g. folded by the SwiGLU GEMM epilogue);
+// scales row-major or (mma_layout) in the atom layout.
+cudaError_t launch_encode_with_amax(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
+                                   const uint32_t *amax_bits, uint8_t *codes, uint8_t *scales,
+                                   float *tensor_scale, bool mma_layout, cudaStream_t stream);
+
 // The quantizer writing its block scales in the atom layout (codes stay
 // row-major [rows][K/2]).  K % 64 == 0.
 cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,

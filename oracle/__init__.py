@@ -27,6 +27,12 @@ Functions and what pins them (tests/test_oracle.py):
   powers of two, and by the definition's invariants (the scale is the
   largest power of two that keeps the block max below 8 times it; no code
   but the clipped ones errs by more than half an E2M1 step).
+* ``silu`` / ``reference_swiglu`` -- the gate/up MLP activation
+  h = silu(g) * u (silu(v) = v / (1 + e^-v)) on reference_gemm's g and u, in
+  fp64, with the band derived in reference_swiglu.  silu pinned by
+  scipy.special.expit; the band by its own properties (it admits the
+  correctly rounded result under the worst g/u errors it allows and rejects
+  a dropped block of g).
 * ``fp8_tensor_scale`` / ``fp8_quantize_rows`` / ``fp8_quantize`` /
   ``fp8_dequant`` -- FP8 E4M3 weights with one fp32 scale g/448.  Pinned by
   hand-worked values (tests/golden/fp8_*.txt) and by torch's fp8 cast of
@@ -309,3 +315,38 @@ def fp8_dequant(codes: np.ndarray, s8: float) -> np.ndarray:
 def fp8_reference_gemm(x_bf16: np.ndarray, w_codes: np.ndarray, s8: float):
     """(y_ref, bound) for a decode-sized X against an FP8 weight, in fp64."""
     return matmul_abt(bf16_to_f64(x_bf16), fp8_dequant(w_codes, s8))
+
+
+# ---- gate/up MLP activation (SwiGLU) ------------------------------------------------
+
+SILU_SLOPE_MAX = 1.1  # max |d silu / dv| = 1.0998 (at v = 2.3994)
+
+
+def silu(v: np.ndarray) -> np.ndarray:
+    """silu(v) = v / (1 + e^-v), fp64 (exp overflow for v < -709 gives -0)."""
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def reference_swiglu(x_bf16: np.ndarray, M_total: int, gate, up, s_x: float | None = None):
+    """(h_ref, tol) for h = silu(g) * u with g = X Wg^T and u = X Wu^T as
+    reference_gemm forms them (gate and up: (codes, scales, tensor scale)).
+
+    The band: g and u reach the epilogue in fp32 from exact products summed
+    in fp32, so |dg| <= t_g = 2^-14 sum|x w_g| + 2^-22 |g| (the tight band of
+    the GEMM without its bf16 term, plus the rounding of the scale factor);
+    likewise t_u.  Then |silu(g') u' - silu(g) u| <= 1.1 t_g (|u| + t_u) +
+    |silu(g)| t_u, the fp32 evaluation of silu and the product adds at most
+    2^-20 of |silu(g')| |u'|, and the result is rounded to bf16 (2^-8 of
+    itself)."""
+    g, bg = reference_gemm(x_bf16, M_total, *gate, s_x=s_x)
+    u, bu = reference_gemm(x_bf16, M_total, *up, s_x=s_x)
+    tg = 2.0 ** -14 * bg + 2.0 ** -22 * np.abs(g)
+    tu = 2.0 ** -14 * bu + 2.0 ** -22 * np.abs(u)
+    sg = np.abs(silu(g))
+    a = SILU_SLOPE_MAX * tg * (np.abs(u) + tu) + sg * tu
+    a = a + 2.0 ** -20 * (sg + SILU_SLOPE_MAX * tg) * (np.abs(u) + tu)
+    h = silu(g) * u
+    tol = a + BF16_UNIT_ROUNDOFF * (np.abs(h) + a) + 1e-30
+    return h, tol

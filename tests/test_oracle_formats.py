@@ -182,3 +182,42 @@ def test_fp8_dequant_exact_and_zero_tensor():
     assert zs == 0.0 and not zc.any()
     x = oracle.fp8_reference_gemm(lin.act_bf16(), codes, s8)[0]
     assert x.shape == (1, 4)
+
+
+# ---- SwiGLU reference -------------------------------------------------------------
+
+def test_silu_vs_scipy_expit():
+    scipy_special = pytest.importorskip("scipy.special")
+    v = np.concatenate([np.linspace(-30, 30, 2001), [-800.0, -1e-300, 0.0, 1e-300, 800.0]])
+    ref = v * scipy_special.expit(v)
+    got = oracle.silu(v)
+    assert np.all(np.abs(got - ref) <= 4e-16 * np.abs(ref) + 1e-300)
+    # the slope bound the band uses
+    h = 1e-6
+    slope = np.abs((oracle.silu(v + h) - oracle.silu(v - h)) / (2 * h))
+    assert slope.max() <= oracle.SILU_SLOPE_MAX and slope.max() > 1.09
+
+
+def test_swiglu_band_admits_worst_case_and_rejects_a_dropped_block():
+    lin_g = synth.Linear("sg", 40, 256, 24, 1, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
+                         x_outlier_frac=0.01)
+    lin_u = synth.Linear("su", 40, 256, 24, 2, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02)
+    x = lin_g.act_bf16()
+    gate = oracle.quantize(lin_g.weight_bf16())[:3]
+    up = oracle.quantize(lin_u.weight_bf16())[:3]
+    h, tol = oracle.reference_swiglu(x, 40, gate, up)
+    g, bg = oracle.reference_gemm(x, 40, *gate)
+    u, bu = oracle.reference_gemm(x, 40, *up)
+    # worst-case g and u errors inside the GEMM band, then bf16 rounding
+    tg = 2.0 ** -14 * bg + 2.0 ** -22 * np.abs(g)
+    tu = 2.0 ** -14 * bu + 2.0 ** -22 * np.abs(u)
+    for sg_, su_ in ((1, 1), (1, -1), (-1, 1), (-1, -1)):
+        hp = oracle.silu(g + sg_ * tg) * (u + su_ * tu)
+        hb = torch.from_numpy(hp.astype(np.float32)).bfloat16().double().numpy()
+        assert np.all(np.abs(hb - h) <= tol)
+    # a dropped 16-element block of the gate product leaves the band
+    xh = oracle.activation_hat(x, 40)
+    wg = oracle.dequant(gate[0], gate[1], gate[2])
+    drop = (xh[:, 16:32] @ wg[:, 16:32].T)
+    hd = oracle.silu(g - drop) * u
+    assert np.mean(np.abs(hd - h) > tol) > 0.5
