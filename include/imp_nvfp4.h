@@ -146,7 +146,8 @@ size_t imp_nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  * 16-byte aligned arrays: returns the number of kernels one call launches
  * (0 if the call rejects the shape) and stores in *kernel (when kernel is not
  * NULL) the static name of the kernel that streams W: "gemv_f4r_kernel" /
- * "gemv_f4_kernel" (FP4 tensor cores, X split per call), "gemv_tc_kernel"
+ * "gemv_f4_kernel" (FP4 tensor cores, X split per call, inside the kernel
+ * or by a split kernel before it), "gemv_tc_kernel"
  * (f16 tensor cores), "gemv_kernel" (CUDA cores) or "gemm_mxf4_kernel"
  * (prefill).  Host only; launches nothing. */
 int32_t imp_nvfp4_gemm_plan(int64_t M, int64_t N, int64_t K, const char **kernel);
@@ -298,9 +299,10 @@ int32_t imp_nvfp4_gemm_grouped_plan(int64_t M, int64_t K, const int64_t *N, int3
 
 /* Y_g = X * W_g^T for g < n_groups (1 <= n_groups <= IMP_NVFP4_MAX_GROUPS).
  *   x_bf16, M, K, ldx   as for imp_nvfp4_gemm_mma (M = 0: nothing to do).
- *   1 <= M <= 2, K % 256 == 0 and K >= 1024 (the decode case): one split of
- *   X and one weight-streaming launch for all groups (2 kernels), scheduled
- *   over the groups' 128-row tiles together.  Other shapes (and a tile or K
+ *   1 <= M <= 2, K % 256 == 0 and K >= 1024 (the decode case): one
+ *   weight-streaming kernel for all groups, scheduled over the groups'
+ *   128-row tiles together (after one split of X, or splitting X itself
+ *   when a CTA holds at most six K chunks).  Other shapes (and a tile or K
  *   count that plan cannot hold) run imp_nvfp4_gemm_mma once per group, in
  *   order, on `stream`; a shape it rejects returns
  *   IMP_ERR_UNSUPPORTED_SHAPE before anything is enqueued.

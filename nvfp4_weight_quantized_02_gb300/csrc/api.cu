@@ -381,8 +381,12 @@ int32_t imp_nvfp4_gemm_grouped_plan(int64_t M, int64_t K, const int64_t *N, int3
   if (kernel) *kernel = nullptr;
   if (!N || n_groups < 1 || n_groups > IMP_NVFP4_MAX_GROUPS) return 0;
   if (grouped_one_pass_sizes(M, K, N, n_groups)) {
-    if (kernel) *kernel = "gemv_f4r_kernel";
-    return 2;
+    int64_t rows = 0;  // the groups' tiles, scheduled together
+    for (int i = 0; i < n_groups; ++i) rows += (N[i] + 127) / 128 * 128;
+    const char *k = nullptr;
+    const int32_t n = impfp4::gemv_f4_launches(M, rows, K, &k);
+    if (kernel) *kernel = k;
+    return n;
   }
   int32_t total = 0;
   for (int i = 0; i < n_groups; ++i) {

@@ -104,7 +104,9 @@ template <int NMMA> struct StageS {
 
 // ---- resident-B kernel (M <= 2, N_MMA = 16)
 constexpr int kIssuersR = 4, kProducerR = 4, kNSR = 8;  // stage st and st - 8: same issuer
-constexpr int kLoaderWarpR = 5;                          // warp 5: copies the B slots in
+constexpr int kLoaderWarpR = 5;                          // warp 5: copies the B slots in (FP8)
+constexpr int kSplitWarpX = 7;                           // warps 5, 7, 8..11 split X (NVFP4)
+constexpr int kSplitW = 6;                               // split warps, one slot each
 constexpr int kSplitWarps = 8;                           // chunks per CTA of the split kernel
 // Weight formats of the resident kernel: NVFP4 (E2M1 codes, E4M3 block
 // scales; X split into NVFP4 components; tcgen05.mma kind::mxf4nvf4) and
@@ -132,8 +134,8 @@ template <int FMT> struct StageRT {
   static constexpr uint32_t TX = FmtR<FMT>::kTX;
 };
 using StageR = StageRT<kFmtNv>;
-// B slot image of one K chunk (written once per call by xsplit_slots_kernel
-// into the workspace, copied as is into shared memory): codes, 2 KB = 16
+// B slot image of one K chunk (written into shared memory by the resident
+// kernel's split warps, split_chunk_slot): codes, 2 KB = 16
 // operand rows x 128 B, row n at 128 n with its 16-byte unit u at unit
 // u ^ (n % 8) (the 128-byte swizzle); scales, 1 KB = four K64 steps of 256 B,
 // operand row n of step t at 256 t + 16 n (the row's 4 block scales; 12 zero
@@ -214,9 +216,15 @@ struct F4Bars {
   uint64_t drain[4];
   uint64_t part_done, flag_ready;  // split-tile hand-off among the epilogue warps
   uint64_t cl_full;                // kSchedCluster, rank 0: the other ranks' partials arrived
-  uint64_t b_ready;                // resident kernel: every B slot has landed
+  uint64_t b_ready;                // resident kernel: every B slot has landed (copied in)
   uint32_t tmem;
   int last;
+};
+// Resident kernel splitting X itself: a barrier per B slot and the split
+// warps' per-row maxima (after the cluster reduction buffer).
+struct F4SplitBars {
+  uint64_t slot_ready[6];
+  uint32_t xmax[6][2];
 };
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
@@ -1015,53 +1023,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- resident-B path (M <= 2) ---------------------------------------------------
 
-// X (M <= 2 rows) -> B slot images of every K chunk, once per call.  Grid
-// (chunks / kSplitWarps rounded up, M); CTA (j, m) finds row m's max|x| (the
-// prescale 2^sh puts it in [2^14, 2^15)), then warp w splits chunk
-// kSplitWarps j + w of row m into its eight components: lane 2 b + h holds
-// elements 8 h .. 8 h + 7 of the chunk's block b.  Writes the images' rows
-// 8 m .. 8 m + 7 (and, for the last row of X, zeros in the rows after it) and
-// sh[m].
-__global__ void __launch_bounds__(32 * kSplitWarps)
-    xsplit_slots_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, uint8_t *slot_codes,
-                        uint8_t *slot_sf, int32_t *sh_out, int32_t *status) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  extern __shared__ uint4 xrow[];  // row m of X (K bf16), staged once
-  __shared__ uint64_t bar;
-  __shared__ uint32_t red[kSplitWarps];
-  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  // X may come from the previous kernel, and the previous GEMV may still
-  // read the workspace: wait for it before touching either.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // The row in one bulk copy: a single memory round trip, which matters
-  // because the next GEMV's weight stream is already filling the memory
-  // queues when this kernel runs.
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&bar, (uint32_t)(K * 2));
-    bulk_g2s(xrow, x + m * ldx, (uint32_t)(K * 2), &bar);
-  }
-  if (!mbar_wait_bounded(&bar, 0u, status)) return;
-  uint32_t mx = 0;
-  for (int i = threadIdx.x; i < (int)(K / 8); i += 32 * kSplitWarps) mx = max(mx, absmax_bf16x8(xrow[i]));
-  for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  mx = 0;
-  for (int w = 0; w < kSplitWarps; ++w) mx = max(mx, red[w]);
-  const int sh = prescale_exponent(mx);
-  if (blockIdx.x == 0 && threadIdx.x == 0) sh_out[m] = sh;
-
-  const int ch = blockIdx.x * kSplitWarps + warp;
-  if (ch >= (int)(K / kChunkK)) return;
+// One 256-element chunk of row m of X -> its eight NVFP4 components in a B
+// slot image (codes: 16 operand rows x 128 B, row n at 128 n with its
+// 16-byte unit u at u ^ (n % 8); scales: four K64 steps of 16 lines of 16 B),
+// in shared or global memory.  One warp: lane 2 b + h holds elements
+// 8 h .. 8 h + 7 of the chunk's block b (v).  The last row of X also zeroes
+// the operand rows after its components.
+__device__ __forceinline__ void split_chunk_slot(const uint4 v, int sh, int m, int M, uint8_t *codes,
+                                                 uint8_t *sf, int lane) {
   const int bb = lane >> 1, hf = lane & 1;
-  const uint4 v = xrow[(ch * kChunkK + 16 * bb + 8 * hf) / 8];
-  uint8_t *codes = slot_codes + (size_t)ch * 2048;
-  uint8_t *sf = slot_sf + (size_t)ch * 1024;
   const float p1 = pow2f(sh / 2), p2 = pow2f(sh - sh / 2);
   float r[8];
   {
@@ -1118,6 +1088,55 @@ __global__ void __launch_bounds__(32 * kSplitWarps)
     for (int i = lane; i < 4 * nr; i += 32)
       *reinterpret_cast<uint4 *>(sf + (i / nr) * 256 + 16 * (n0 + i % nr)) = make_uint4(0, 0, 0, 0);
   }
+}
+
+
+// X (M <= 2 rows) -> B slot images of every K chunk, once per call.  Grid
+// (chunks / kSplitWarps rounded up, M); CTA (j, m) finds row m's max|x| (the
+// prescale 2^sh puts it in [2^14, 2^15)), then warp w splits chunk
+// kSplitWarps j + w of row m into its eight components: lane 2 b + h holds
+// elements 8 h .. 8 h + 7 of the chunk's block b.  Writes the images' rows
+// 8 m .. 8 m + 7 (and, for the last row of X, zeros in the rows after it) and
+// sh[m].
+__global__ void __launch_bounds__(32 * kSplitWarps)
+    xsplit_slots_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, uint8_t *slot_codes,
+                        uint8_t *slot_sf, int32_t *sh_out, int32_t *status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ uint4 xrow[];  // row m of X (K bf16), staged once
+  __shared__ uint64_t bar;
+  __shared__ uint32_t red[kSplitWarps];
+  const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // X may come from the previous kernel, and the previous GEMV may still
+  // read the workspace: wait for it before touching either.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The row in one bulk copy: a single memory round trip, which matters
+  // because the next GEMV's weight stream is already filling the memory
+  // queues when this kernel runs.
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)(K * 2));
+    bulk_g2s(xrow, x + m * ldx, (uint32_t)(K * 2), &bar);
+  }
+  if (!mbar_wait_bounded(&bar, 0u, status)) return;
+  uint32_t mx = 0;
+  for (int i = threadIdx.x; i < (int)(K / 8); i += 32 * kSplitWarps) mx = max(mx, absmax_bf16x8(xrow[i]));
+  for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = 0;
+  for (int w = 0; w < kSplitWarps; ++w) mx = max(mx, red[w]);
+  const int sh = prescale_exponent(mx);
+  if (blockIdx.x == 0 && threadIdx.x == 0) sh_out[m] = sh;
+
+  const int ch = blockIdx.x * kSplitWarps + warp;
+  if (ch >= (int)(K / kChunkK)) return;
+  const int bb = lane >> 1, hf = lane & 1;
+  split_chunk_slot(xrow[(ch * kChunkK + 16 * bb + 8 * hf) / 8], sh, m, M,
+                   slot_codes + (size_t)ch * 2048, slot_sf + (size_t)ch * 1024, lane);
 }
 
 // Two signed floats -> two E4M3 bytes (element 0 in the low byte), round to
@@ -1199,7 +1218,7 @@ __global__ void __launch_bounds__(32 * kSplitWarps)
   }
 }
 
-template <bool PREP, int FMT = kFmtNv>
+template <bool PREP, int FMT = kFmtNv, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_f4r_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
                     const F4Args a) {
@@ -1215,6 +1234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kSchedCluster: the other ranks' partial sums, [rank - 1][128 rows][2]
   float *red = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&bars) +
                                          ((sizeof(F4Bars) + 15) & ~size_t(15)));
+  F4SplitBars &sbars = *reinterpret_cast<F4SplitBars *>(
+      red + (a.sched == kSchedCluster ? (size_t)(a.ksplit - 1) * kTileRows * 2 : 0));
+  static_assert(!SPLIT || FMT == kFmtNv, "the kernel splits NVFP4 components only");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const StreamK sk(a.n_tiles, a.n_chunks, a.sched, a.ksplit);
   // B slot of chunk ch: this CTA's chunks run consecutively from ch_begin
@@ -1225,6 +1247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars.b_ready, 1);
     mbar_init(&bars.cl_full, a.sched == kSchedCluster ? 4 * (a.ksplit - 1) : 1);
+    if (SPLIT)
+      for (int j = 0; j < a.n_slots; ++j) mbar_init(&sbars.slot_ready[j], 1);
     init_common(bars, kNSR, kIssuersR);
   }
   if (warp == 0) tmem_alloc(&bars.tmem);
@@ -1293,6 +1317,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = (i > kNSR ? i - kNSR : 0); k < i; ++k)
         mbar_wait_bounded(&bars.full[k % kNSR], (uint32_t)((k / kNSR) & 1), a.status);
     }
+  } else if (SPLIT && (warp == kLoaderWarpR || warp == kSplitWarpX || warp >= kEpiWarp0)) {
+    // ---- NVFP4 with at most six slots: X split into components here, one
+    // slot per warp, while the ring fills (no split launch, no slot copy).
+    // Six warps (5, 7 and the epilogue warps, which go on to the epilogue);
+    // the prescale comes from this CTA's chunks of each row of X (all ranks
+    // and CTAs leave their sums in true units).  With more slots the split
+    // kernel's many warps finish them sooner than six warps here would.
+    const int widx = warp == kLoaderWarpR ? 0 : warp - kSplitWarpX + 1;
+    const int bb = lane >> 1, hf = lane & 1;
+    if (widx == 0 && lane < 16)  // read (into lanes no N = 16 MMA uses) after the last slot
+      reinterpret_cast<uint4 *>(bsf + (size_t)a.n_slots * kSlotSf)[lane] = make_uint4(0, 0, 0, 0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // X may come from the previous kernel
+    // split warp w: slot w (a.n_slots <= kSplitW)
+    const int j = widx;
+    uint4 v[2];
+    uint32_t mx[2] = {0u, 0u};
+    if (j < a.n_slots) {
+      const int ch = (ch_begin + j) % sk.nch;
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+        if (m < a.M) {
+          v[m] = __ldcg(reinterpret_cast<const uint4 *>(a.x + m * a.ldx + (int64_t)ch * kChunkK +
+                                                       16 * bb + 8 * hf));
+          mx[m] = absmax_bf16x8(v[m]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      for (int o = 16; o; o >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], o));
+      if (lane == 0) sbars.xmax[widx][m] = mx[m];
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the pad
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kSplitW) : "memory");
+    int sh[kMaxRowsX] = {};
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      uint32_t r = 0;
+#pragma unroll
+      for (int w = 0; w < kSplitW; ++w) r = max(r, sbars.xmax[w][m]);
+      sh[m] = prescale_exponent(r);
+    }
+    if (j < a.n_slots) {
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+        if (m < a.M)
+          split_chunk_slot(v[m], sh[m], m, a.M, bcodes + (size_t)j * 2048, bsf + (size_t)j * 1024,
+                           lane);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by tcgen05.mma / .cp
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sbars.slot_ready[j]);
+    }
+    if (warp >= kEpiWarp0) epilogue_loop<kIssuersR, NMMA, FMT>(a, bars, tmem, sk, warp, lane, sh, red);
   } else if (warp == kLoaderWarpR) {
     // ---- warp 5: the zero pad after the last slot's scales, then (once the
     // split kernel has finished) this CTA's B slots: chunks ch_begin,
@@ -1334,7 +1410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto sfb_desc = [&](int, int st, int t) {
       return dSB0 + (uint64_t)(slot_of(st) * (1024 >> 4)) + (uint64_t)(16u * t);
     };
-    auto b_wait = [&](int) { return mbar_wait_bounded(&bars.b_ready, 0u, a.status); };
+    // one barrier for all slots (copied in), or one per slot (split here)
+    auto b_wait = [&](int st) {
+      return SPLIT ? mbar_wait_bounded(&sbars.slot_ready[slot_of(st)], 0u, a.status)
+                   : mbar_wait_bounded(&bars.b_ready, 0u, a.status);
+    };
     if constexpr (FMT == kFmtNv)
       issuer_loop<kIssuersR, kNSR, NMMA, PREP, L>(smem, bars, tmem, sk, warp, lane, a.status,
                                                   b_desc, sfb_desc, b_wait);
@@ -1398,6 +1478,7 @@ template <int NMMA> size_t smem_s() {
 // n_slots: the most distinct K chunks a CTA sees (its B slots).
 struct F4Plan {
   int sched, ksplit, grid, n_slots;
+  bool split_inside;  // NVFP4: the kernel splits X itself (at most kSplitW slots)
   size_t smem;
   bool ok;  // the resident kernel takes the shape
 };
@@ -1440,6 +1521,8 @@ F4Plan plan_r(int64_t M, int64_t N, int64_t K, int fmt = kFmtNv) {
            ((sizeof(F4Bars) + 15) & ~size_t(15)) + red + 1024;
   // the split kernel stages a row of X (2 K bytes) in shared memory
   p.ok = M <= 2 && p.n_slots <= max_slots && K * 2 <= 200 * 1024 && p.smem <= 227 * 1024;
+  p.split_inside = fmt == kFmtNv && p.n_slots <= kSplitW;
+  if (p.split_inside) p.smem += sizeof(F4SplitBars);
   return p;
 }
 
@@ -1620,9 +1703,10 @@ size_t gemv_f4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 int gemv_f4_launches(int64_t M, int64_t N, int64_t K, const char **kernel) {
   if (!gemv_f4_shape_ok(M, N, K)) return 0;
-  if (plan_r(M, N, K).ok) {
-    *kernel = "gemv_f4r_kernel";  // split kernel + GEMV holding its chunks of X
-    return 2;
+  const F4Plan P = plan_r(M, N, K);
+  if (P.ok) {
+    *kernel = "gemv_f4r_kernel";  // the GEMV, after a split kernel unless it splits X itself
+    return P.split_inside ? 1 : 2;
   }
   *kernel = "gemv_f4_kernel";  // split kernel + GEMV
   return 2;
@@ -1648,10 +1732,10 @@ static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int6
   a.sched = P.sched;
   a.ksplit = P.ksplit;
   a.slot_codes = ws + L.bcodes;
-  // X -> B slot images (programmatic dependent launch: may start while the
-  // previous kernel drains; it waits before reading X or writing the
-  // workspace)
-  {
+  if (!P.split_inside) {
+    // X -> B slot images by the split kernel (programmatic dependent launch:
+    // it may start while the previous kernel drains and waits before reading
+    // X or writing the workspace); each CTA then copies its slots in
     const size_t xs_bytes = (size_t)K * 2;  // the staged row
     if (xs_bytes > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(
@@ -1674,6 +1758,11 @@ static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int6
     if (e != cudaSuccess) return e;
   }
   const int cluster = P.sched == kSchedCluster ? P.ksplit : 1;
+  if (P.split_inside)
+    return prepared ? launch_pdl(gemv_f4r_kernel<true, kFmtNv, true>, P.grid, kThreads, P.smem,
+                                 stream, cluster, mw, ms, a)
+                    : launch_pdl(gemv_f4r_kernel<false, kFmtNv, true>, P.grid, kThreads, P.smem,
+                                 stream, cluster, mw, ms, a);
   return prepared ? launch_pdl(gemv_f4r_kernel<true>, P.grid, kThreads, P.smem, stream, cluster,
                                mw, ms, a)
                   : launch_pdl(gemv_f4r_kernel<false>, P.grid, kThreads, P.smem, stream, cluster,

@@ -49,13 +49,16 @@ def test_workspace_sizes():
 def test_gemm_plan():
     # decode, one or two rows of X on an FP4-eligible shape (K % 256 == 0,
     # K >= 1024, N >= 128) -> FP4 tensor cores: a split kernel writing X's
-    # components once, then the GEMV holding its chunks of them; more rows
-    # that one f16 pass holds -> f16 tensor cores, one launch per pass
+    # components once, then the GEMV holding its chunks of them -- or, with
+    # at most six K chunks per CTA, the GEMV alone, splitting them itself;
+    # more rows that one f16 pass holds -> f16 tensor cores, one launch per pass
     assert pkg.imp_nvfp4_gemm_plan(1, 151936, 5120) == (2, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(1, 17408, 5120) == (2, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(1, 5120, 17408) == (2, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(2, 5120, 17408) == (2, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(4, 17408, 5120) == (1, "gemv_tc_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(1, 1024, 1024) == (1, "gemv_f4r_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(2, 3072, 1024) == (1, "gemv_f4r_kernel")
     # several rows of X that one f16 pass cannot hold: FP4, split kernel + GEMV
     assert pkg.imp_nvfp4_gemm_plan(16, 17408, 5120) == (2, "gemv_f4_kernel")
     assert pkg.imp_nvfp4_gemm_plan(3, 5120, 17408) == (2, "gemv_f4_kernel")
@@ -67,13 +70,14 @@ def test_gemm_plan():
 
 
 def test_grouped_plan():
-    # one split + one weight stream for all groups at M <= 2 (a 0.6B-class
+    # one weight stream for all groups at M <= 2 (plus the split kernel when
+    # a CTA holds more than six K chunks) (a 0.6B-class
     # layer's q/k/v and gate/up, a 27B-class layer's gate/up)
     gp = pkg.imp_nvfp4_gemm_grouped_plan
-    assert gp(1, 1024, [2048, 1024, 1024]) == (2, "gemv_f4r_kernel")
-    assert gp(1, 1024, [3072, 3072]) == (2, "gemv_f4r_kernel")
+    assert gp(1, 1024, [2048, 1024, 1024]) == (1, "gemv_f4r_kernel")
+    assert gp(1, 1024, [3072, 3072]) == (1, "gemv_f4r_kernel")
     assert gp(2, 5120, [17408, 17408]) == (2, "gemv_f4r_kernel")
-    assert gp(1, 1024, [100, 28, 1]) == (2, "gemv_f4r_kernel")  # ragged groups
+    assert gp(1, 1024, [100, 28, 1]) == (1, "gemv_f4r_kernel")  # ragged groups
     # otherwise one imp_nvfp4_gemm_mma call per group
     assert gp(4, 5120, [17408, 17408]) == (4, "gemv_f4_kernel")
     assert gp(2048, 5120, [17408, 17408]) == (6, "gemm_mxf4_kernel")

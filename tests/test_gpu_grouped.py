@@ -37,7 +37,7 @@ def test_0p6b_groups_every_element(names):
     L = layer("decode_0p6b")
     lins = [L[n] for n in names]
     K = lins[0].K
-    assert pkg.imp_nvfp4_gemm_grouped_plan(1, K, [l.N for l in lins]) == (2, "gemv_f4r_kernel")
+    assert pkg.imp_nvfp4_gemm_grouped_plan(1, K, [l.N for l in lins]) == (1, "gemv_f4r_kernel")
     ref, dev = zip(*(prepared(l) for l in lins))
     x = lins[0].act_bf16()
     for y, (c, s, ts), l in zip(run_grouped(x, list(dev)), ref, lins):
@@ -93,7 +93,7 @@ def test_grouped_repeatable():
 
 
 def test_layer_graph_replay_matches_eager():
-    """A 0.6B-class decode layer (q/k/v grouped, o, gate/up grouped, down: 8
+    """A 0.6B-class decode layer (q/k/v grouped, o, gate/up grouped, down: 4
     kernels) captured once and replayed on new inputs."""
     L = layer("decode_0p6b")
     dev = {n: prepared(L[n])[1] for n in L}
