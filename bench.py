@@ -332,10 +332,15 @@ def run_native(args):
     rows_w, weights, xs, ys = [], [], [], []
     for l in lins:
         wb = torch.from_numpy(l.weight_bf16().view(np.int16)).view(torch.bfloat16).to(dev)
-        w = pkg.quantize(wb)
+        if args.weights == "fp8":
+            w = pkg.fp8_quantize(wb)
+        elif args.weights == "mxfp4":
+            w = pkg.mxfp4_to_nvfp4(pkg.mxfp4_quantize(wb))
+        else:
+            w = pkg.quantize(wb)
         del wb
         rows_w.append(w)
-        weights.append(pkg.prepare_mma(w))
+        weights.append(w if args.weights == "fp8" else pkg.prepare_mma(w))
         xs.append(torch.from_numpy(l.act_bf16().view(np.int16)).view(torch.bfloat16).to(dev))
         ys.append(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev))
     chained = chain_inputs(lins, xs, ys)
@@ -343,14 +348,18 @@ def run_native(args):
     stream = torch.cuda.current_stream(dev)
     # one workspace per problem, allocated once (the FP4 decode path's split
     # X, partial sums and counters)
-    wss = [torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K), 16),
+    wss = [torch.empty(max(pkg.imp_nvfp4_gemm_workspace_size(l.M, l.N, l.K),
+                           pkg.imp_fp8_gemm_workspace_size(l.M, l.N, l.K), 16),
                        dtype=torch.uint8, device=dev) for l in lins]
-    plans = [pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K) for l in lins]
+    fp8 = args.weights == "fp8"
+    plans = [pkg.imp_fp8_gemm_plan(l.M, l.N, l.K) if fp8 else pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K)
+             for l in lins]
+    call = pkg.gemm_fp8 if fp8 else pkg.gemm_mma
     torch.cuda.synchronize()
 
     def step():
         for x, w, y, ws in zip(chained, weights, ys, wss):
-            pkg.gemm_mma(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
+            call(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -359,6 +368,8 @@ def run_native(args):
         dist.barrier()
 
     bytes_step = step_bytes(lins)
+    if fp8:  # one byte per weight, one tensor scale
+        bytes_step = sum(l.N * l.K + 4 + 2 * l.M * (l.K + l.N) for l in lins)
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
         e0, e1 = event_pair()
@@ -379,8 +390,8 @@ def run_native(args):
             for _ in range(max(50, args.steps // 4)):
                 a, b = event_pair()
                 a.record(stream)
-                pkg.gemm_mma(chained[i], weights[i], y=ys[i], dev_status=status, stream=stream,
-                             workspace=wss[i])
+                call(chained[i], weights[i], y=ys[i], dev_status=status, stream=stream,
+                     workspace=wss[i])
                 b.record(stream)
                 ts.append((a, b))
             torch.cuda.synchronize()
@@ -422,17 +433,18 @@ def run_native(args):
     # duration of the call timed alone (the call is the X split kernel + the
     # GEMV), and the same call launched back to back
     lt = lins[top]
+    cbytes = (lambda l: l.N * l.K + 4 + 2 * l.M * (l.K + l.N)) if fp8 else call_bytes
     top_us = statistics.median(per_call[lt.name])
-    achieved = call_bytes(lt) / (top_us * 1e-6) / 1e9
+    achieved = cbytes(lt) / (top_us * 1e-6) / 1e9
     top_kernel = plans[top][1]
-    traffic = load_traffic(top_kernel, lt)
-    b2b = time_blocks(lambda: pkg.gemm_mma(chained[top], weights[top], y=ys[top],
-                                           dev_status=status, stream=stream,
-                                           workspace=wss[top]), 20, 5, stream)
+    traffic = None if args.weights != "nvfp4" else load_traffic(top_kernel, lt)
+    b2b = time_blocks(lambda: call(chained[top], weights[top], y=ys[top],
+                                   dev_status=status, stream=stream,
+                                   workspace=wss[top]), 20, 5, stream)
     b2b_us = statistics.median(b2b)
 
     extra = {}
-    if rank == 0 and not args.no_extra:
+    if rank == 0 and not args.no_extra and args.weights == "nvfp4":
         extra = bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs,
                              chained, ys, wss, status, step)
     if int(status.item()) != 0:
@@ -441,28 +453,33 @@ def run_native(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 weights, bf16 x/y, f32 accumulate",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"nvfp4": "nvfp4 weights, bf16 x/y, f32 accumulate",
+                  "mxfp4": "mxfp4 weights (served in nvfp4 form), bf16 x/y, f32 accumulate",
+                  "fp8": "fp8 e4m3 weights, bf16 x/y, f32 accumulate"}[args.weights],
         "data": "synthetic",
         "config": {"workload": args.workload, "M": 1, "shapes_KxN": [[l.K, l.N] for l in lins],
                    "bytes_per_step": bytes_step,
                    "dataflow": "decode layer: up and gate read x, down reads gate's output, "
                                "the LM head reads down's output",
-                   "weights": "serving form (imp_nvfp4_prepare_mma once, imp_nvfp4_gemm_mma "
-                              "per call)",
+                   "weights": {"nvfp4": "serving form (imp_nvfp4_prepare_mma once, "
+                                        "imp_nvfp4_gemm_mma per call)",
+                               "mxfp4": "MXFP4, converted once to NVFP4 form and prepared",
+                               "fp8": "FP8 E4M3 row-major (imp_fp8_gemm per call)"}[args.weights],
                    "l2": "inputs larger than L2 (588 MB of weights per step)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_hbm_peak": value / world / hbm_peak,
         "spread_us_per_step": spread(blocks),
         "per_call_us": {l.name: spread(per_call[l.name]) for l in lins},
-        "per_call_gbs": {l.name: call_bytes(l) / (statistics.median(per_call[l.name]) * 1e-6) / 1e9
+        "per_call_gbs": {l.name: cbytes(l) / (statistics.median(per_call[l.name]) * 1e-6) / 1e9
                          for l in lins},
         "roofline": {"bound": "hbm", "kernel": f"{top_kernel} ({lt.name} {lt.K}x{lt.N})",
                      "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
-                     "bytes_per_launch": call_bytes(lt),
+                     "bytes_per_launch": cbytes(lt),
                      "back_to_back": {"us_per_launch": b2b_us,
-                                      "achieved": call_bytes(lt) / (b2b_us * 1e-6) / 1e9,
-                                      "frac": call_bytes(lt) / (b2b_us * 1e-6) / 1e9 / hbm_peak}},
+                                      "achieved": cbytes(lt) / (b2b_us * 1e-6) / 1e9,
+                                      "frac": cbytes(lt) / (b2b_us * 1e-6) / 1e9 / hbm_peak}},
         "gpu_launches": args.steps * sum(n for n, _ in plans),
         "kernels": {l.name: {"kernel": k, "launches_per_call": n} for l, (n, k) in zip(lins, plans)},
         "clocks": clocks.summary(),
@@ -470,7 +487,7 @@ def run_native(args):
                 "d2h_bytes_per_step": pin_y.numel() * 2},
     }
     line.update(extra)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.weights == "nvfp4":
         gbs, dt, desc, per = cpu_oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": desc, "seconds": dt,
@@ -1095,6 +1112,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--weights", choices=["nvfp4", "mxfp4", "fp8"], default="nvfp4",
+                    help="weight format of the decode step (mxfp4: converted once to the NVFP4 "
+                         "form; fp8: E4M3 with one tensor scale)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
