@@ -104,7 +104,9 @@ def run_prefill(lin, rows_check=None, cols_check=None, via="gemm"):
                                    (640, 5120, 768), (333, 2048, 1000),
                                    # a second N tile mostly past N; three N tiles of a
                                    # 128-row-block-aligned prepared weight; ragged rows
-                                   (130, 512, 200), (256, 768, 576), (300, 4096, 1920)])
+                                   (130, 512, 200), (256, 768, 576), (300, 4096, 1920),
+                                   # more tiles than SMs, a partial last wave
+                                   (1280, 256, 4096), (2048, 320, 2600)])
 def test_small_shapes_every_element(M, K, N):
     lin = synth.Linear("pf", M, K, N, 77, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
                        zero_block_p=0.01, x_outlier_frac=0.01)
