@@ -347,7 +347,10 @@ imp_status imp_nvfp4_gemm_swiglu(const void *x_bf16, int64_t M, int64_t K, int64
 /* imp_nvfp4_quantize_mma with the global amax already known (bf16 magnitude
  * bits of max|x| in device memory, as imp_nvfp4_gemm_swiglu writes it): the
  * encode pass alone, one read of X.  Bit-identical to imp_nvfp4_quantize_mma
- * when *amax is the true max|x|.  rows >= 1, K % 64 == 0.                 */
+ * when *amax is the true max|x|.  rows >= 1, K % 64 == 0.  dev_status is not
+ * written: non-finite values are reported by whoever folded the amax
+ * (imp_nvfp4_gemm_swiglu does); a non-finite *amax gives a zero tensor
+ * scale and all-zero codes.                                                */
 imp_status imp_nvfp4_quantize_mma_amax(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,
                                        const uint32_t *amax, const imp_nvfp4_tensor *out,
                                        int32_t *dev_status, void *stream);
