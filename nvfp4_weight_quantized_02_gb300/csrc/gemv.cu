@@ -375,23 +375,21 @@ int cuda_core_passes(int64_t M, int64_t N, int64_t K) {
 
 enum class DecodePath { kNone, kFp4, kF16, kCudaCore };
 
-// Measured per shape class on GB300 (back-to-back calls, weights from HBM):
-//  * one row of X over many 128-row tiles of W: the FP4 path (no per-weight
-//    work on the CUDA cores);
-//  * otherwise the f16 tensor-core path while one pass over W holds every
-//    row of X (it needs no cross-CTA sums, and it shares each decoded weight
-//    among the rows);
-//  * otherwise the FP4 path (one pass over W for any M <= 16, where the f16
-//    path would stream W once per 1, 2, 4 or 8 rows).
-// The CUDA-core kernel takes what neither tensor-core path accepts.
+// Measured on GB300 (back-to-back calls, weights from HBM): wherever the
+// FP4 path takes the shape it is the faster one for every M <= 16 (one pass
+// over W, no per-weight work on the CUDA cores; whole-tile or cluster K-split
+// schedules without global-memory round trips): on the 27B-class
+// projections 16.0 / 16.7 / 21.6 us at M = 4 / 8 / 16 against 22.4 / 26.3 /
+// ~35 us for the f16 tensor-core path.  The f16 path takes the shapes the
+// FP4 path rejects (K % 256 != 0, K < 1024, N < 128, no workspace), the
+// CUDA-core kernel what neither tensor-core path accepts.
 DecodePath choose_path(int64_t M, int64_t N, int64_t K, bool workspace, const void *codes,
                        const void *scales) {
   if (M < 1 || M > kDecodeMaxM || N < 1 || K < 64 || K % 64) return DecodePath::kNone;
   const bool f4 = workspace && gemv_f4_supported(M, N, K, codes, scales);
-  if (f4 && M <= 2) return DecodePath::kFp4;
+  if (f4) return DecodePath::kFp4;
   const int tc_passes = gemv_tc_launches(M, N, K);
   if (tc_passes == 1) return DecodePath::kF16;
-  if (f4) return DecodePath::kFp4;
   if (tc_passes > 0) return DecodePath::kF16;
   return cuda_core_passes(M, N, K) ? DecodePath::kCudaCore : DecodePath::kNone;
 }

@@ -915,16 +915,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 1024-byte alignment for the swizzled tiles
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   F4Bars &bars = *reinterpret_cast<F4Bars *>(smem + NS * L::BYTES);
+  // kSchedCluster: the other ranks' partial sums, [rank - 1][128 rows][N_MMA / 8]
+  float *red = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&bars) +
+                                         ((sizeof(F4Bars) + 15) & ~size_t(15)));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const StreamK sk(a.n_tiles, a.n_chunks, a.sched, a.ksplit);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) init_common(bars, NS, NI);
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.cl_full, a.sched == kSchedCluster ? 4 * (a.ksplit - 1) : 1);
+    init_common(bars, NS, NI);
+  }
   if (warp == 0) tmem_alloc(&bars.tmem);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem;
+  // the cluster's barriers are initialized before any rank arrives remotely
+  if (a.sched == kSchedCluster) cluster_sync_all();
 
   if (warp == kProducerS) {
     if (lane == 0) {
@@ -1009,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < NMMA / kNC; ++m)
       if (m < a.M) sh[m] = a.sh[m];
-    epilogue_loop<NI, NMMA>(a, bars, tmem, sk, warp, lane, sh, nullptr);
+    epilogue_loop<NI, NMMA>(a, bars, tmem, sk, warp, lane, sh, red);
   }
 
   tc_fence_before();
@@ -1019,6 +1027,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_free(tmem);
   }
+  // no rank leaves while another may still write into its shared memory
+  if (a.sched == kSchedCluster) cluster_sync_all();
 }
 
 // ---- resident-B path (M <= 2) ---------------------------------------------------
@@ -1631,13 +1641,49 @@ bool weight_maps(bool prepared, const uint8_t *codes, const uint8_t *scales, int
          cached_map(ms, scales, (uint64_t)N, (uint64_t)(K / 16), kTileRows, 16, false);
 }
 
+// The streamed kernel's schedule, chosen as for the resident kernel: whole
+// tiles with at least 3/4 as many tiles as SMs; fewer tiles: each tile's K
+// split over a cluster of S CTAs whose partials meet in rank 0's shared
+// memory (S limited by that buffer's room); otherwise stream-K.
+struct SPlan {
+  int sched, ksplit, grid;
+  size_t smem;
+};
 template <int NMMA>
-cudaError_t launch_streamed(bool prepared, int grid, cudaStream_t stream, const CUtensorMap &mw,
-                            const CUtensorMap &ms, const CUtensorMap &mb, const F4Args &a) {
-  return prepared ? launch_pdl(gemv_f4_kernel<NMMA, true>, grid, kThreads, smem_s<NMMA>(), stream,
-                               1, mw, ms, mb, a)
-                  : launch_pdl(gemv_f4_kernel<NMMA, false>, grid, kThreads, smem_s<NMMA>(),
-                               stream, 1, mw, ms, mb, a);
+SPlan plan_s(int64_t N, int64_t K, int sk_grid) {
+  SPlan p = {kSchedStreamK, 1, sk_grid, smem_s<NMMA>()};
+  const int64_t nch = K / kChunkK, n_tiles = ceil_div(N, kTileRows), sms = num_sms();
+  const size_t per_rank = (size_t)kTileRows * (NMMA / kNC) * sizeof(float);
+  if (4 * n_tiles >= 3 * sms) {
+    p.sched = kSchedWhole;
+    p.grid = (int)(n_tiles < sms ? n_tiles : sms);
+  } else if (n_tiles < sms) {
+    int64_t S = sms / n_tiles;
+    if (S > 8) S = 8;
+    if (S > nch) S = nch;
+    while (S >= 2 && smem_s<NMMA>() + (size_t)(S - 1) * per_rank > 227 * 1024) --S;
+    if (S >= 2) {
+      p.sched = kSchedCluster;
+      p.ksplit = (int)S;
+      p.grid = (int)(n_tiles * S);
+      p.smem = smem_s<NMMA>() + (size_t)(S - 1) * per_rank;
+    }
+  }
+  return p;
+}
+
+template <int NMMA>
+cudaError_t launch_streamed(bool prepared, int sk_grid, cudaStream_t stream,
+                            const CUtensorMap &mw, const CUtensorMap &ms, const CUtensorMap &mb,
+                            F4Args a) {
+  const SPlan P = plan_s<NMMA>(a.grp[0].N, a.K, sk_grid);
+  a.sched = P.sched;
+  a.ksplit = P.ksplit;
+  const int cluster = P.sched == kSchedCluster ? P.ksplit : 1;
+  return prepared ? launch_pdl(gemv_f4_kernel<NMMA, true>, P.grid, kThreads, P.smem, stream,
+                               cluster, mw, ms, mb, a)
+                  : launch_pdl(gemv_f4_kernel<NMMA, false>, P.grid, kThreads, P.smem, stream,
+                               cluster, mw, ms, mb, a);
 }
 
 cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,

@@ -51,15 +51,15 @@ def test_gemm_plan():
     # K >= 1024, N >= 128) -> FP4 tensor cores: a split kernel writing X's
     # components once, then the GEMV holding its chunks of them -- or, with
     # at most six K chunks per CTA, the GEMV alone, splitting them itself;
-    # more rows that one f16 pass holds -> f16 tensor cores, one launch per pass
+    # more rows -> the FP4 path with X's components streamed with W
     assert pkg.imp_nvfp4_gemm_plan(1, 151936, 5120) == (2, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(1, 17408, 5120) == (2, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(1, 5120, 17408) == (2, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(2, 5120, 17408) == (2, "gemv_f4r_kernel")
-    assert pkg.imp_nvfp4_gemm_plan(4, 17408, 5120) == (1, "gemv_tc_kernel")
+    assert pkg.imp_nvfp4_gemm_plan(4, 17408, 5120) == (2, "gemv_f4_kernel")
     assert pkg.imp_nvfp4_gemm_plan(1, 1024, 1024) == (1, "gemv_f4r_kernel")
     assert pkg.imp_nvfp4_gemm_plan(2, 3072, 1024) == (1, "gemv_f4r_kernel")
-    # several rows of X that one f16 pass cannot hold: FP4, split kernel + GEMV
+    # several rows of X: FP4, split kernel + GEMV
     assert pkg.imp_nvfp4_gemm_plan(16, 17408, 5120) == (2, "gemv_f4_kernel")
     assert pkg.imp_nvfp4_gemm_plan(3, 5120, 17408) == (2, "gemv_f4_kernel")
     # FP4 shape rules not met (K % 256): f16 passes
