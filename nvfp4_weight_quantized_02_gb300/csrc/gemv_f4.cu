@@ -103,7 +103,7 @@ template <int NMMA> struct StageS {
 };
 
 // ---- resident-B kernel (M <= 2, N_MMA = 16)
-constexpr int kIssuersR = 4, kProducerR = 4, kNSR = 8;  // stage st and st - 8: same issuer
+constexpr int kIssuersR = 4, kProducerR = 4, kNSR = 8;  // a multiple of the issuers: stage st and st - 8, same issuer
 constexpr int kLoaderWarpR = 5;                          // warp 5: copies the B slots in (FP8)
 constexpr int kSplitWarpX = 7;                           // warps 5, 7, 8..11 split X (NVFP4)
 constexpr int kSplitW = 6;                               // split warps, one slot each
@@ -554,6 +554,10 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
   constexpr uint32_t kIdesc = idesc_f4<NMMA>();
   constexpr uint32_t kSF0 = 2 * NI * NMMA;  // scale columns after the accumulators
   static_assert(kSF0 + 32 * NS <= kTmemCols, "tensor memory plan");
+  // Stages i and i + NS share a ring slot; with NS a multiple of NI the same
+  // issuer takes both, in order, so it never waits on a slot's full barrier
+  // more than one phase ahead (a parity wait cannot tell phase p from p + 2).
+  static_assert(NS % NI == 0, "ring depth must be a multiple of the issuer count");
   const uint32_t sbase = smem_u32(smem);
   const uint64_t dA0 = sdesc(sbase + Stage::W, 16, 1024, kSw128);
   const uint64_t dSA0 = sdesc(sbase + Stage::SFA, 0, 128, kNoSwizzle);
@@ -615,6 +619,7 @@ __device__ void issuer_loop_f8(uint8_t *smem, F4Bars &bars, uint32_t tmem, const
                                int is, int lane, int32_t *status, BDesc b_desc, BWait b_wait) {
   constexpr uint32_t kIdesc = idesc_f8<NMMA>();
   static_assert(2 * NI * NMMA <= kTmemCols, "tensor memory plan");
+  static_assert(NS % NI == 0, "ring depth must be a multiple of the issuer count");
   const uint64_t dA0 = sdesc(smem_u32(smem) + Stage::W, 16, 1024, kSw128);
   bool ok = true;
   for (int jj = 0; jj < sk.n_seg && ok; ++jj) {
