@@ -22,23 +22,31 @@
 // memory.  y sums the component columns with their power-of-two weights, in
 // a fixed order.
 //
-// Work split ("stream-K"): the (128-row tile, 256-element K chunk) sequence,
-// tile-major, is cut into gridDim.x equal contiguous ranges, one per CTA (one
-// CTA per SM).  A CTA's range covers whole tiles and at most two partial ones
-// ("segments"); a partial tile's CTAs leave fp32 partial sums in the
-// workspace and the last of them to finish adds them in K order.
+// Work split over the (128-row tile, 256-element K chunk) grid, one CTA per
+// SM at most:
+//  * whole tiles, as evenly as they divide (at least 3/4 as many tiles as
+//    SMs);
+//  * fewer tiles: each tile's K chunks split over a thread-block cluster of
+//    S CTAs, whose fp32 partial sums meet in rank 0's shared memory
+//    (distributed shared memory) and are added in rank (= K) order;
+//  * otherwise stream-K: the tile-major chunk sequence cut into equal
+//    contiguous ranges; a partial tile's CTAs leave fp32 partial sums in the
+//    workspace and the last of them to finish adds them in K order.
 //
-// Two kernels share that scheme:
-//  * gemv_f4r_kernel (M <= 2, the usual decode case): everything in one
-//    launch.  Warp 4 streams W (codes: 128 rows x 128 B tiles, 128-byte
-//    swizzle; scales: 128 rows x 16 B) through an 8-deep ring with TMA and
-//    never waits for the previous kernel (W is never written on the
-//    stream).  Meanwhile warps 5..11 wait for it and split the K chunks of
-//    X this CTA needs into components directly in shared memory (B operand,
-//    swizzled, and its scale atoms); warps 0..3 issue the MMAs (stage i ->
-//    issuer i % 4) as chunks become ready, and warps 8..11 go on to the
-//    epilogue.  A weight already in the tensor-core layout (quantize.cuh)
-//    is read with two contiguous bulk copies per stage instead.
+// Two kernels share those schedules:
+//  * gemv_f4r_kernel (M <= 2, the usual decode case): X's components are
+//    held in shared memory for the whole call (B "slots", one per K chunk
+//    the CTA sees).  Warp 4 streams W through an 8-deep ring (a weight in the
+//    tensor-core layout of quantize.cuh: two contiguous bulk copies per
+//    stage; row-major: 2-D TMA of 128 x 128-byte code tiles, 128-byte
+//    swizzle, and 128 x 16-byte scale rows, which warp 6 relays into atoms)
+//    and never waits for the previous kernel (W is never written on the
+//    stream).  The slots come from a split kernel (xsplit_slots_kernel, once
+//    per call; warp 5 copies them in) or, with at most six chunks per CTA,
+//    from the kernel's own warps 5, 7 and 8..11, one slot each.  Warps 0..3
+//    issue the MMAs (stage i -> issuer i % 4), warps 8..11 run the epilogue.
+//    The same kernel serves FP8-E4M3 weights (kind::f8f6f4, X split into
+//    E4M3 components by xsplit_f8_kernel, no block scales).
 //  * gemv_f4_kernel (any M <= 16, one pass over W): a separate split
 //    kernel (xsplit_kernel) writes the components and scale atoms to the
 //    workspace, and they travel with W in each stage of the ring; producer
@@ -46,11 +54,11 @@
 //    B operands of 16 or 32 rows (8-deep ring), two for 64 (6-deep), one for
 //    128 (5-deep): a wider MMA takes longer, so fewer issuers keep ahead of
 //    HBM, and the wider B stages fill the shared memory sooner.
-// Issuer: its warp relays the stage's W scales into 512-byte atoms; one
-// thread copies both operands' atoms to tensor memory (tcgen05.cp) and issues
-// four M=128 x N=N_MMA x K=64 MMAs into its own accumulator.  One issuing
-// thread sustains one MMA per ~130 cycles; three or four keep the tensor core
-// ahead of HBM.  Epilogue: thread = tile row (its tensor-memory lane).
+// Issuer: one thread copies both operands' scale atoms of a stage to tensor
+// memory (tcgen05.cp) and issues four M=128 x N=N_MMA x K=64 MMAs into its
+// own accumulator.  One issuing thread sustains one MMA per ~130 cycles;
+// three or four keep the tensor core ahead of HBM.  Epilogue: thread = tile
+// row (its tensor-memory lane).
 // Every wait is bounded; on a timeout the kernel reports IMP_DEV_TIMEOUT,
 // drains its own copies and MMAs, frees tensor memory and returns.
 #include <atomic>
