@@ -24,6 +24,7 @@ namespace impfp4 {
 namespace {
 
 constexpr int kAmaxThreads = 256;
+constexpr int64_t kAmaxSeg = 512;  // 16-byte vectors per amax segment (4096 elements)
 constexpr int kEncThreads = 256;
 
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
@@ -52,8 +53,10 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
   return r;
 }
 
-// Pass 1: per-CTA max of |x| as bf16 magnitude bits.  Warps stride over rows;
-// lanes read 16-byte vectors (8 elements) of a row.
+// Pass 1: per-CTA max of |x| as bf16 magnitude bits.  Warps stride over
+// segments of kAmaxSeg 16-byte vectors (4096 elements) of a row, so that a
+// tensor of few long rows (an activation) still spreads over every SM;
+// lanes read four vectors at a time.
 __global__ void __launch_bounds__(kAmaxThreads) amax_partial_kernel(const uint16_t *__restrict__ x,
                                                                     int64_t rows, int64_t K,
                                                                     int64_t ldx,
@@ -63,17 +66,20 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partial_kernel(const uint16
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (kAmaxThreads / 32);
   const int64_t vec_per_row = K / 8;
+  const int64_t nseg = ceil_div(vec_per_row, kAmaxSeg);
   uint32_t m2 = 0;  // two 16-bit maxima side by side
-  for (int64_t r = (int64_t)blockIdx.x * (kAmaxThreads / 32) + (threadIdx.x >> 5); r < rows;
-       r += warps_total) {
+  for (int64_t g = (int64_t)blockIdx.x * (kAmaxThreads / 32) + (threadIdx.x >> 5); g < rows * nseg;
+       g += warps_total) {
+    const int64_t r = g / nseg, v0 = (g - r * nseg) * kAmaxSeg;
+    const int64_t v1 = v0 + kAmaxSeg < vec_per_row ? v0 + kAmaxSeg : vec_per_row;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + r * ldx);
-    int64_t v = lane;
-    for (; v + 96 < vec_per_row; v += 128) {
+    int64_t v = v0 + lane;
+    for (; v + 96 < v1; v += 128) {
       const uint4 a = __ldg(row + v), b = __ldg(row + v + 32), c = __ldg(row + v + 64),
                   d = __ldg(row + v + 96);
       m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(absmax8(a), absmax8(b)), __vmaxu2(absmax8(c), absmax8(d))));
     }
-    for (; v < vec_per_row; v += 32) m2 = __vmaxu2(m2, absmax8(__ldg(row + v)));
+    for (; v < v1; v += 32) m2 = __vmaxu2(m2, absmax8(__ldg(row + v)));
   }
   uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
   m = block_max_u32<kAmaxThreads>(m, red);
@@ -221,8 +227,8 @@ int num_sms_cached() {
 // size does not depend on the device.
 constexpr int kMaxPartials = 1024;
 
-int amax_grid(int64_t rows) {
-  int64_t g = ceil_div(rows, kAmaxThreads / 32);
+int amax_grid(int64_t rows, int64_t K) {
+  int64_t g = ceil_div(rows * ceil_div(K / 8, kAmaxSeg), kAmaxThreads / 32);
   if (g > kMaxPartials) g = kMaxPartials;
   if (g < 1) g = 1;
   return static_cast<int>(g);
@@ -232,14 +238,14 @@ int amax_grid(int64_t rows) {
 
 int num_sms() { return num_sms_cached(); }
 
-size_t quantize_workspace_bytes(int64_t rows, int64_t /*K*/) {
-  return static_cast<size_t>(amax_grid(rows)) * sizeof(uint32_t);
+size_t quantize_workspace_bytes(int64_t rows, int64_t K) {
+  return static_cast<size_t>(amax_grid(rows, K)) * sizeof(uint32_t);
 }
 
 cudaError_t launch_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
                             uint8_t *codes, uint8_t *scales, float *tensor_scale,
                             int32_t *status, void *workspace, cudaStream_t stream) {
-  const int ga = amax_grid(rows);
+  const int ga = amax_grid(rows, K);
   uint32_t *partial = static_cast<uint32_t *>(workspace);
   amax_partial_kernel<<<ga, kAmaxThreads, 0, stream>>>(x, rows, K, ldx, partial, status);
   const int64_t segs = rows * ceil_div(K / 16, 64);
@@ -419,7 +425,7 @@ cudaError_t launch_encode_with_amax(const uint16_t *x, int64_t rows, int64_t K, 
 cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
                                 uint8_t *codes, uint8_t *mma_scales, float *tensor_scale,
                                 int32_t *status, void *workspace, cudaStream_t stream) {
-  const int ga = amax_grid(rows);
+  const int ga = amax_grid(rows, K);
   uint32_t *partial = static_cast<uint32_t *>(workspace);
   amax_partial_kernel<<<ga, kAmaxThreads, 0, stream>>>(x, rows, K, ldx, partial, status);
   const int64_t segs = rows * ceil_div(K / 16, 64);
@@ -632,7 +638,7 @@ cudaError_t launch_mx_quantize(const uint16_t *x, int64_t rows, int64_t K, int64
 cudaError_t launch_fp8_quantize(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx,
                                 uint8_t *codes, float *tensor_scale, int32_t *status,
                                 void *workspace, cudaStream_t stream) {
-  const int ga = amax_grid(rows);
+  const int ga = amax_grid(rows, K);
   uint32_t *partial = static_cast<uint32_t *>(workspace);
   amax_partial_kernel<<<ga, kAmaxThreads, 0, stream>>>(x, rows, K, ldx, partial, status);
   fp8_encode_kernel<<<grid_for(rows * (K / 8), kEncThreads), kEncThreads, 0, stream>>>(
