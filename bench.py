@@ -723,6 +723,40 @@ def bench_grouped_layer(pkg, dev, stream, status, lins, copies, ncopy, ins, ys, 
         del graphs
     except Exception as e:  # report, do not fail the line
         res["layer_grouped_graph"] = {"error": str(e)[:200]}
+    # the same four calls as one decode chain (imp_nvfp4_gemm_chain: one
+    # launch; o and down read their predecessors' outputs)
+    try:
+        def links_for(c):
+            spec = []
+            for g in groups:
+                i0 = by[g[0]]
+                gl = [pkg.ImpNvfp4Group(copies[by[n]][c].c_struct(), ys[by[n]].data_ptr(),
+                                        ys[by[n]].stride(0)) for n in g]
+                dep = len(g) == 1 and ins[i0] is ys[by[groups[groups.index(g) - 1][0]]]
+                xx = x if len(g) > 1 else ins[i0]
+                spec.append((gl, None if dep else xx.data_ptr(), 0 if dep else xx.stride(0)))
+            return pkg.ChainLinks(spec)
+        cls = [links_for(c) for c in range(ncopy)]
+        cws = torch.empty(max(pkg.imp_nvfp4_gemm_chain_workspace_size(1, cl) for cl in cls),
+                          dtype=torch.uint8, device=dev)
+        sh = pkg._stream_handle(stream)
+        kc = [0]
+
+        def chain_layer():
+            st = pkg.imp_nvfp4_gemm_chain(1, cls[kc[0] % ncopy], status.data_ptr(),
+                                          cws.data_ptr(), cws.numel(), sh)
+            if st != pkg.IMP_OK:
+                raise pkg.ImpError(st, "imp_nvfp4_gemm_chain")
+            kc[0] += 1
+        for _ in range(ncopy):
+            chain_layer()
+        ts = time_blocks(chain_layer, ncopy, 10, stream)
+        med = statistics.median(ts)
+        res["layer_chain"] = {"us": spread(ts), "GB/s": layer_bytes / (med * 1e-6) / 1e9,
+                              "launches": 1,
+                              "persistent_launch": pkg.imp_nvfp4_gemm_chain_plan(1, cls[0]) == 1}
+    except Exception as e:  # report, do not fail the line
+        res["layer_chain"] = {"error": str(e)[:200]}
     return res
 
 
@@ -927,6 +961,33 @@ def bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs, ch
             grouped_step()
         out["decode_grouped_up_gate"] = rate(time_blocks(grouped_step, n, 10, stream))
         del gws
+
+    # the step as one decode chain (imp_nvfp4_gemm_chain: one persistent
+    # launch; down and the LM head wait for their X, gate keeps up's split X)
+    try:
+        spec = []
+        for i, (x, w, y) in enumerate(zip(chained, weights, ys)):
+            g = [pkg.ImpNvfp4Group(w.c_struct(), y.data_ptr(), y.stride(0))]
+            dep = i > 0 and x is ys[i - 1]
+            spec.append((g, None if dep else x.data_ptr(), 0 if dep else x.stride(0)))
+        cl = pkg.ChainLinks(spec)
+        cws = torch.empty(pkg.imp_nvfp4_gemm_chain_workspace_size(1, cl), dtype=torch.uint8,
+                          device=dev)
+        sh = pkg._stream_handle(stream)
+
+        def chain_step():
+            st = pkg.imp_nvfp4_gemm_chain(1, cl, status.data_ptr(), cws.data_ptr(), cws.numel(),
+                                          sh)
+            if st != pkg.IMP_OK:
+                raise pkg.ImpError(st, "imp_nvfp4_gemm_chain")
+        for _ in range(args.warmup):
+            chain_step()
+        out["decode_chain"] = dict(rate(time_blocks(chain_step, n, 10, stream)),
+                                   persistent_launch=pkg.imp_nvfp4_gemm_chain_plan(1, cl) == 1,
+                                   launches_per_step=1)
+        del cws
+    except Exception as e:  # report, do not fail the benchmark line
+        out["decode_chain"] = {"error": str(e)[:200]}
 
     # the step replayed as one CUDA graph (programmatic dependent launch kept)
     try:

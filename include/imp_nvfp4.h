@@ -315,6 +315,69 @@ imp_status imp_nvfp4_gemm_grouped(const void *x_bf16, int64_t M, int64_t K, int6
                                   int32_t *dev_status, void *workspace, size_t ws_bytes,
                                   void *stream);
 
+/* ---- decode chain ----------------------------------------------------------------
+ * A decode step is a chain of GEMVs in which a call's X is often the
+ * previous call's output (a layer's projections one after another, the last
+ * layer feeding the LM head).  The engine records that per-token sequence
+ * once and replays it ("How imp turns a model file into words", part one;
+ * the imp README, "How it works": CUDA graphs replay the decode launches).
+ * This call runs up to four such calls ("links") in ONE persistent launch:
+ * one CTA per SM streams every link's weight through one pipeline, and only
+ * a link whose X is the previous link's output waits for it (a per-link
+ * count of finished CTAs in the workspace), so the weight stream does not
+ * stop between calls.  One launch instead of a few per call: on launch-
+ * bound layers (a 0.6B-class layer's 7 projections as 4 links: 38 us,
+ * against 49 us as grouped calls and 35 us as those calls replayed from a
+ * CUDA graph) it beats separate calls without a graph; on a 27B-class step
+ * it runs within ~1 % of the separate calls (109.5 vs 108.5 us).
+ * An addition of this library.                                            */
+#define IMP_NVFP4_MAX_CHAIN 4
+typedef struct {
+  const imp_nvfp4_group *groups; /* 1..IMP_NVFP4_MAX_GROUPS weights of one K (MMA layout),
+                                    each with its output, as for imp_nvfp4_gemm_grouped */
+  int32_t n_groups;
+  const void *x_bf16;            /* device bf16[M][ldx]; NULL: X is the previous link's
+                                    groups[0] output (its K must equal that weight's rows) */
+  int64_t ldx;                   /* ignored when x_bf16 is NULL */
+} imp_nvfp4_chain_link;
+
+/* Bytes of workspace imp_nvfp4_gemm_chain needs (on the current device;
+ * 0 for invalid arguments). */
+size_t imp_nvfp4_gemm_chain_workspace_size(int64_t M, const imp_nvfp4_chain_link *links,
+                                           int32_t n_links);
+
+/* 1 if imp_nvfp4_gemm_chain runs these links as one persistent launch, 0 if
+ * it runs them one grouped call after another (or rejects them).  Host only. */
+int32_t imp_nvfp4_gemm_chain_plan(int64_t M, const imp_nvfp4_chain_link *links, int32_t n_links);
+
+/* For each link c in order (1 <= n_links <= IMP_NVFP4_MAX_CHAIN):
+ * Y_cg = X_c * W_cg^T for its groups g, with X_c = links[c].x_bf16 or, if
+ * that is NULL (c >= 1), the output of links[c-1].groups[0].
+ *   M             M >= 0 (M = 0: nothing to do).
+ *   links         host array; weights, outputs and strides as for
+ *                 imp_nvfp4_gemm_grouped.  No output may overlap another
+ *                 link's output or any link's X (except the NULL form),
+ *                 else IMP_ERR_INVALID_ARG: links run concurrently on
+ *                 different SMs.
+ *   workspace     imp_nvfp4_gemm_chain_workspace_size bytes, 16-byte
+ *                 aligned, needing no clearing (the launch's first CTA
+ *                 clears its counters and publishes the launch; graph
+ *                 replay is fine).  Launches that can run at the same time
+ *                 must not share it.
+ * 1 <= M <= 2, every K % 256 == 0 and K >= 1024, and a schedule that fits
+ * (at most 24 K chunks of 256 per CTA and link): one launch of one CTA per
+ * SM, all of which must be resident at once (its CTAs wait for each other):
+ * it needs the GPU to itself while it runs -- with another kernel holding
+ * SMs for more than a second a wait gives up and sets IMP_DEV_TIMEOUT.
+ * Otherwise each link runs as imp_nvfp4_gemm_grouped, in order, on
+ * `stream`.  Accuracy as for imp_nvfp4_gemm; results are
+ * bitwise reproducible from run to run (each CTA splits its own chunks of X
+ * with its own power-of-two prescale, so the roundings can differ from a
+ * grouped call's).                                                          */
+imp_status imp_nvfp4_gemm_chain(int64_t M, const imp_nvfp4_chain_link *links, int32_t n_links,
+                                int32_t *dev_status, void *workspace, size_t ws_bytes,
+                                void *stream);
+
 /* ---- fused prefill MLP pieces -------------------------------------------------
  * A layer's MLP ("1. The big picture": the MLP transforms each token's vector
  * on its own) in the Qwen-class models the pages run is gate and up

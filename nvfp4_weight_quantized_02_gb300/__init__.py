@@ -64,6 +64,12 @@ class ImpNvfp4Group(ctypes.Structure):
     _fields_ = [("w", ImpNvfp4Tensor), ("y_bf16", ctypes.c_void_p), ("ldy", ctypes.c_int64)]
 
 
+class ImpNvfp4ChainLink(ctypes.Structure):
+    """ctypes mirror of imp_nvfp4_chain_link."""
+    _fields_ = [("groups", ctypes.POINTER(ImpNvfp4Group)), ("n_groups", ctypes.c_int32),
+                ("x_bf16", ctypes.c_void_p), ("ldx", ctypes.c_int64)]
+
+
 class ImpMxfp4Tensor(ctypes.Structure):
     """ctypes mirror of imp_mxfp4_tensor."""
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("rows", ctypes.c_int64),
@@ -130,6 +136,13 @@ def _L():
     lib.imp_nvfp4_gemm_grouped.restype = ctypes.c_int
     lib.imp_nvfp4_gemm_grouped.argtypes = [P, I64, I64, I64, ctypes.POINTER(ImpNvfp4Group),
                                            ctypes.c_int32, P, P, SZ, P]
+    CL = ctypes.POINTER(ImpNvfp4ChainLink)
+    lib.imp_nvfp4_gemm_chain_workspace_size.restype = SZ
+    lib.imp_nvfp4_gemm_chain_workspace_size.argtypes = [I64, CL, ctypes.c_int32]
+    lib.imp_nvfp4_gemm_chain_plan.restype = ctypes.c_int32
+    lib.imp_nvfp4_gemm_chain_plan.argtypes = [I64, CL, ctypes.c_int32]
+    lib.imp_nvfp4_gemm_chain.restype = ctypes.c_int
+    lib.imp_nvfp4_gemm_chain.argtypes = [I64, CL, ctypes.c_int32, P, P, SZ, P]
     MX, F8 = ctypes.POINTER(ImpMxfp4Tensor), ctypes.POINTER(ImpFp8Tensor)
     lib.imp_mxfp4_quantize.restype = ctypes.c_int
     lib.imp_mxfp4_quantize.argtypes = [P, I64, I64, I64, MX, P, P]
@@ -280,6 +293,34 @@ def imp_nvfp4_gemm_grouped(x_bf16: int, M: int, K: int, ldx: int, groups: list[I
     arr = (ImpNvfp4Group * len(groups))(*groups)
     return _L().imp_nvfp4_gemm_grouped(x_bf16, M, K, ldx, arr, len(groups), dev_status,
                                        workspace, ws_bytes, stream)
+
+
+class ChainLinks:
+    """A host array of imp_nvfp4_chain_link built from (groups, x_bf16, ldx)
+    triples (x_bf16 None: the previous link's first output); keeps the
+    groups' arrays alive for as long as it lives."""
+
+    def __init__(self, links: list):
+        self._groups = [(ImpNvfp4Group * len(g))(*g) for g, _, _ in links]
+        self.array = (ImpNvfp4ChainLink * len(links))(*[
+            ImpNvfp4ChainLink(ctypes.cast(ga, ctypes.POINTER(ImpNvfp4Group)), len(g), x, ldx)
+            for ga, (g, x, ldx) in zip(self._groups, links)])
+        self.n = len(links)
+
+
+def imp_nvfp4_gemm_chain_workspace_size(M: int, links: ChainLinks) -> int:
+    return _L().imp_nvfp4_gemm_chain_workspace_size(M, links.array, links.n)
+
+
+def imp_nvfp4_gemm_chain_plan(M: int, links: ChainLinks) -> int:
+    """1: one persistent launch; 0: one grouped call per link (or rejected)."""
+    return _L().imp_nvfp4_gemm_chain_plan(M, links.array, links.n)
+
+
+def imp_nvfp4_gemm_chain(M: int, links: ChainLinks, dev_status: int | None, workspace: int | None,
+                         ws_bytes: int, stream: int | None) -> int:
+    return _L().imp_nvfp4_gemm_chain(M, links.array, links.n, dev_status, workspace, ws_bytes,
+                                      stream)
 
 
 def imp_mxfp4_quantize(x_bf16: int, rows: int, K: int, ldx: int, out: ImpMxfp4Tensor,
@@ -533,6 +574,38 @@ def gemm_grouped(x, ws: list, ys=None, dev_status=None, stream=None, workspace=N
                                 workspace.data_ptr(), ws_bytes, _stream_handle(stream))
     if st != IMP_OK:
         raise ImpError(st, "imp_nvfp4_gemm_grouped")
+    return ys
+
+
+def gemm_chain(links: list, ys=None, dev_status=None, stream=None, workspace=None):
+    """A decode chain in one call: links = [(weights, x), ...] with weights a
+    list of MMA-layout tensors of one K and x a bf16 [M][K] tensor, or None
+    for the previous link's first output.  Returns the outputs, one list per
+    link (allocated with row strides rounded up to 8 unless given)."""
+    import torch
+    x0 = links[0][1]
+    assert x0 is not None and x0.dtype == torch.bfloat16 and x0.dim() == 2
+    M = x0.shape[0]
+    if ys is None:
+        ys = [[torch.empty((M, (w.rows + 7) // 8 * 8), dtype=torch.bfloat16,
+                           device=x0.device)[:, :w.rows] for w in ws] for ws, _ in links]
+    spec = []
+    for (ws, x), yl in zip(links, ys):
+        assert all(w.layout == "mma" for w in ws)
+        groups = [ImpNvfp4Group(w.c_struct(), y.data_ptr(), y.stride(0)) for w, y in zip(ws, yl)]
+        if x is None:
+            spec.append((groups, None, 0))
+        else:
+            assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+            spec.append((groups, x.data_ptr(), x.stride(0)))
+    cl = ChainLinks(spec)
+    ws_bytes = imp_nvfp4_gemm_chain_workspace_size(M, cl)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x0.device)
+    st = imp_nvfp4_gemm_chain(M, cl, None if dev_status is None else dev_status.data_ptr(),
+                              workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_gemm_chain")
     return ys
 
 

@@ -441,6 +441,136 @@ imp_status imp_nvfp4_gemm_grouped(const void *x_bf16, int64_t M, int64_t K, int6
   return IMP_OK;
 }
 
+}  // extern "C"
+
+// ---- decode chain ------------------------------------------------------------------
+
+namespace {
+struct ChainResolved {
+  impfp4::GemvGroup g[IMP_NVFP4_MAX_CHAIN][IMP_NVFP4_MAX_GROUPS];
+  int64_t N[IMP_NVFP4_MAX_CHAIN][IMP_NVFP4_MAX_GROUPS];
+  impfp4::ChainLink l[IMP_NVFP4_MAX_CHAIN];
+};
+
+// Bytes spanned by M rows of `cols` bf16 elements at stride ld.
+uintptr_t span_bytes(int64_t M, int64_t ld, int64_t cols) {
+  return (uintptr_t)(((M - 1) * ld + cols) * 2);
+}
+bool overlap(const void *a, uintptr_t na, const void *b, uintptr_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+// The links with each X resolved (the NULL form reads the previous link's
+// first output).  sizes_only: look at K and the weights' rows alone.
+imp_status resolve_chain(int64_t M, const imp_nvfp4_chain_link *links, int32_t n, bool sizes_only,
+                         ChainResolved &r) {
+  if (M < 0 || !links || n < 1 || n > IMP_NVFP4_MAX_CHAIN) return IMP_ERR_INVALID_ARG;
+  for (int c = 0; c < n; ++c) {
+    const imp_nvfp4_chain_link &L = links[c];
+    if (!L.groups || L.n_groups < 1 || L.n_groups > IMP_NVFP4_MAX_GROUPS) return IMP_ERR_INVALID_ARG;
+    const int64_t K = L.groups[0].w.K;
+    if (K <= 0 || K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+    for (int i = 0; i < L.n_groups; ++i) {
+      const imp_nvfp4_group &g = L.groups[i];
+      const int64_t N = g.w.rows;
+      if (N < 1 || g.w.K != K) return IMP_ERR_INVALID_ARG;
+      if (!sizes_only) {
+        const imp_status st = check_tensor(&g.w, N, K);
+        if (st != IMP_OK) return st;
+        if (!g.y_bf16 || g.ldy < N) return IMP_ERR_INVALID_ARG;
+        if (!aligned16(g.y_bf16) || g.ldy % 8) return IMP_ERR_MISALIGNED;
+      }
+      r.N[c][i] = N;
+      r.g[c][i] = {g.w.codes, g.w.scales, g.w.tensor_scale, static_cast<uint16_t *>(g.y_bf16), N,
+                   g.ldy};
+    }
+    const uint16_t *x = static_cast<const uint16_t *>(L.x_bf16);
+    int64_t ldx = L.ldx;
+    const bool dep = x == nullptr;
+    if (dep) {
+      if (c == 0 || K != links[c - 1].groups[0].w.rows) return IMP_ERR_INVALID_ARG;
+      x = static_cast<const uint16_t *>(links[c - 1].groups[0].y_bf16);
+      ldx = links[c - 1].groups[0].ldy;
+    } else if (!sizes_only && M > 0) {
+      if (ldx < K) return IMP_ERR_INVALID_ARG;
+      if (!aligned16(x) || ldx % 8) return IMP_ERR_MISALIGNED;
+    }
+    r.l[c] = impfp4::ChainLink{r.g[c], L.n_groups, x, ldx, K, dep};
+  }
+  if (sizes_only || M == 0) return IMP_OK;
+  // links run concurrently on different SMs: no output may overlap another
+  // link's output or any explicit X
+  for (int c = 0; c < n; ++c)
+    for (int i = 0; i < links[c].n_groups; ++i) {
+      const imp_nvfp4_group &g = links[c].groups[i];
+      const uintptr_t ny = span_bytes(M, g.ldy, g.w.rows);
+      for (int d = 0; d < n; ++d) {
+        if (links[d].x_bf16 &&
+            overlap(g.y_bf16, ny, links[d].x_bf16, span_bytes(M, links[d].ldx, r.l[d].K)))
+          return IMP_ERR_INVALID_ARG;
+        if (d == c) continue;
+        for (int j = 0; j < links[d].n_groups; ++j) {
+          const imp_nvfp4_group &h = links[d].groups[j];
+          if (overlap(g.y_bf16, ny, h.y_bf16, span_bytes(M, h.ldy, h.w.rows)))
+            return IMP_ERR_INVALID_ARG;
+        }
+      }
+    }
+  return IMP_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t imp_nvfp4_gemm_chain_workspace_size(int64_t M, const imp_nvfp4_chain_link *links,
+                                           int32_t n_links) {
+  ChainResolved r;
+  if (resolve_chain(M, links, n_links, true, r) != IMP_OK) return 0;
+  size_t need = 0;
+  for (int c = 0; c < n_links; ++c) {
+    const size_t w = imp_nvfp4_gemm_grouped_workspace_size(M, r.l[c].K, r.N[c], links[c].n_groups);
+    need = w > need ? w : need;
+  }
+  if (M >= 1 && impfp4::gemv_f4_chain_ok(M, r.l, n_links)) {
+    const size_t w = impfp4::gemv_f4_chain_workspace_bytes(M, r.l, n_links);
+    need = w > need ? w : need;
+  }
+  return need;
+}
+
+int32_t imp_nvfp4_gemm_chain_plan(int64_t M, const imp_nvfp4_chain_link *links, int32_t n_links) {
+  ChainResolved r;
+  if (resolve_chain(M, links, n_links, true, r) != IMP_OK) return 0;
+  return M >= 1 && impfp4::gemv_f4_chain_ok(M, r.l, n_links) ? 1 : 0;
+}
+
+imp_status imp_nvfp4_gemm_chain(int64_t M, const imp_nvfp4_chain_link *links, int32_t n_links,
+                                int32_t *dev_status, void *workspace, size_t ws_bytes,
+                                void *stream) {
+  ChainResolved r;
+  const imp_status st = resolve_chain(M, links, n_links, false, r);
+  if (st != IMP_OK) return st;
+  if (M == 0) return IMP_OK;
+  const size_t need = imp_nvfp4_gemm_chain_workspace_size(M, links, n_links);
+  if (!workspace || ws_bytes < need) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  if (impfp4::gemv_f4_chain_ok(M, r.l, n_links))
+    return from_cuda(impfp4::launch_gemv_f4_chain(M, r.l, n_links, dev_status, workspace,
+                                                  static_cast<cudaStream_t>(stream)));
+  // one grouped call per link, in order (every link checked before any runs)
+  for (int c = 0; c < n_links; ++c)
+    if (imp_nvfp4_gemm_grouped_plan(M, r.l[c].K, r.N[c], links[c].n_groups, nullptr) == 0)
+      return IMP_ERR_UNSUPPORTED_SHAPE;
+  for (int c = 0; c < n_links; ++c) {
+    const imp_status s = imp_nvfp4_gemm_grouped(r.l[c].x, M, r.l[c].K, r.l[c].ldx, links[c].groups,
+                                                links[c].n_groups, dev_status, workspace, ws_bytes,
+                                                stream);
+    if (s != IMP_OK) return s;
+  }
+  return IMP_OK;
+}
+
 // ---- MXFP4 and FP8 weights ----------------------------------------------------
 
 imp_status imp_mxfp4_quantize(const void *x_bf16, int64_t rows, int64_t K, int64_t ldx,

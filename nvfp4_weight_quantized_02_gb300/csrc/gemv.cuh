@@ -66,6 +66,22 @@ cudaError_t launch_gemv_f4_grouped(const uint16_t *x, int64_t M, int64_t K, int6
                                    const GemvGroup *g, int n, int32_t *status, void *workspace,
                                    cudaStream_t stream);
 
+// Chained decode calls in one persistent launch (one CTA per SM, launched
+// cooperatively): link c multiplies its X by its groups' weights (MMA
+// layout, K = K of the link); dep: X is link c - 1's first output, which the
+// kernel waits for.  1 <= M <= 2, at most four links.
+struct ChainLink {
+  const GemvGroup *g;
+  int n;
+  const uint16_t *x;
+  int64_t ldx, K;
+  bool dep;
+};
+bool gemv_f4_chain_ok(int64_t M, const ChainLink *l, int n);
+size_t gemv_f4_chain_workspace_bytes(int64_t M, const ChainLink *l, int n);
+cudaError_t launch_gemv_f4_chain(int64_t M, const ChainLink *l, int n, int32_t *status,
+                                 void *workspace, cudaStream_t stream);
+
 // FP8-E4M3 weights (codes [N][K], one fp32 tensor scale): X split into E4M3
 // components per call, W streamed into tcgen05.mma.kind::f8f6f4; passes of
 // two rows of X.  K % 128 == 0, K >= 512, N >= 128.

@@ -183,6 +183,9 @@ struct F4Args {
   int n_slots;          // resident kernel: B slots in shared memory
   int sched;            // kSchedStreamK / kSchedWhole / kSchedCluster
   int ksplit;           // kSchedCluster: CTAs per tile (the cluster size)
+  int grid;             // CTAs the call is spread over (0: the whole grid)
+  unsigned int *cnt32;  // per tile: segments finished, cleared before the launch counts
+                        // (a persistent launch's own protocol); nullptr: cnt
   int n_groups;         // weights of the call (row-major weight: 1)
   F4Group grp[kMaxGroups];
 };
@@ -463,11 +466,16 @@ struct StreamK {
   int nch, n_st, n_seg, G;
   int tile0, ch0;  // tile and chunk of the CTA's first stage
   int e0, sl, nl;  // end of the first segment; start and length of the last
-  __device__ StreamK(int n_tiles, int n_chunks, int sched, int S) {
-    G = gridDim.x;
+  // grid > 0: the call is spread over CTAs 0..grid-1 only (the others get
+  // nothing), so that a stream-K call with fewer chunks than CTAs leaves no
+  // empty CTA between the owners of a tile.
+  __device__ StreamK(int n_tiles, int n_chunks, int sched, int S, int grid = 0) {
+    G = grid > 0 ? grid : (int)gridDim.x;
     nch = n_chunks;
     total = (int64_t)n_tiles * nch;
-    if (sched == kSchedWhole) {
+    if ((int)blockIdx.x >= G) {
+      g_begin = g_end = total;
+    } else if (sched == kSchedWhole) {
       g_begin = (int64_t)n_tiles * blockIdx.x / G * nch;
       g_end = (int64_t)n_tiles * (blockIdx.x + 1) / G * nch;
     } else if (sched == kSchedCluster) {
@@ -547,6 +555,14 @@ __device__ void relay_loop(uint8_t *smem, F4Bars &bars, const StreamK &sk, int l
   }
 }
 
+// Every MMA of issuer `is` completes before tensor memory is freed.
+__device__ __forceinline__ void issuer_drain(F4Bars &bars, int is, int lane, int32_t *status) {
+  if (lane == 0) {
+    tc_commit(&bars.drain[is]);
+    mbar_wait_bounded(&bars.drain[is], 0u, status);
+  }
+}
+
 // Issuer `is` of NI: stages (in processing order) i = is, is + NI, ...  Lane
 // 0 copies both operands' scale atoms of the stage into its bank of tensor
 // memory (tcgen05.cp) and issues its four K64 MMAs into the issuer's own
@@ -555,10 +571,16 @@ __device__ void relay_loop(uint8_t *smem, F4Bars &bars, const StreamK &sk, int l
 // processing position i (stage st); `b_wait(st)`: waits (bounded) until that
 // B is in shared memory.  All per-stage bookkeeping is 32-bit integer work:
 // every instruction of this loop sits between MMA issues.
+// Chained calls (one launch running several calls in turn) continue the ring
+// and the accumulator hand-off: ib = ring positions and jb = segments that
+// the earlier calls used; there an issuer with no stage in a segment still
+// waits for the accumulator's previous segment to be read, since a run of
+// such segments could otherwise complete d_full two phases ahead of the
+// epilogue.  Returns false after a wait gave up.
 template <int NI, int NS, int NMMA, bool PREP, class Stage, class BDesc, class SFBDesc, class BWait>
-__device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const StreamK &sk,
+__device__ bool issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const StreamK &sk,
                             int is, int lane, int32_t *status, BDesc b_desc, SFBDesc sfb_desc,
-                            BWait b_wait) {
+                            BWait b_wait, int ib = 0, int jb = 0, bool chain = false) {
   constexpr uint32_t kIdesc = idesc_f4<NMMA>();
   constexpr uint32_t kSF0 = 2 * NI * NMMA;  // scale columns after the accumulators
   static_assert(kSF0 + 32 * NS <= kTmemCols, "tensor memory plan");
@@ -572,18 +594,23 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
   bool ok = true;
   for (int jj = 0; jj < sk.n_seg && ok; ++jj) {
     const int p0 = sk.pbegin(jj), p1 = sk.pend(jj);
-    const int d = jj & 1;
-    const int first = p0 + ((is - p0) % NI + NI) % NI;  // this issuer's first stage
+    const int J = jb + jj, d = J & 1;
+    const int first = p0 + ((is - ib - p0) % NI + NI) % NI;  // this issuer's first stage
+    if (chain && first >= p1 && J >= 2 &&
+        !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.d_empty[d], (uint32_t)((J / 2 - 1) & 1), status))) {
+      ok = false;
+      break;
+    }
     for (int i = first; i < p1; i += NI) {
-      const int s = i % NS, st = sk.stage_of(i);
-      if (i == first && jj >= 2 &&
-          !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.d_empty[d], (uint32_t)((jj / 2 - 1) & 1), status))) {
+      const int s = (ib + i) % NS, st = sk.stage_of(i);
+      if (i == first && J >= 2 &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.d_empty[d], (uint32_t)((J / 2 - 1) & 1), status))) {
         ok = false;
         break;
       }
       // the stage's W (and, row-major, its relaid scale atoms) and its B
       uint64_t *ready = PREP ? &bars.full[s] : &bars.sf_ready[s];
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(ready, (uint32_t)((i / NS) & 1), status) &&
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(ready, (uint32_t)(((ib + i) / NS) & 1), status) &&
                                        b_wait(st))) {
         ok = false;
         break;
@@ -613,11 +640,8 @@ __device__ void issuer_loop(uint8_t *smem, F4Bars &bars, uint32_t tmem, const St
     if (ok && lane == 0) tc_commit(&bars.d_full[is][d]);
     __syncwarp();
   }
-  if (lane == 0) {
-    // every MMA of this thread completes before tensor memory is freed
-    tc_commit(&bars.drain[is]);
-    mbar_wait_bounded(&bars.drain[is], 0u, status);
-  }
+  if (!chain) issuer_drain(bars, is, lane, status);
+  return ok;
 }
 
 // Issuer of the FP8 weight format: the same stage order and accumulators as
@@ -671,9 +695,13 @@ __device__ void issuer_loop_f8(uint8_t *smem, F4Bars &bars, uint32_t tmem, const
 // row -> y (whole tile) or a partial sum (split tile, last CTA adds them).
 // Column c of a row's operand rows carries component c mod 8 with weight
 // 2^(4 - 2c) (NVFP4 components) or 2^(-4c) (E4M3 components).
+// Chained calls pass the ring positions (ib) and segments (jb) of the earlier
+// calls and carry the split-tile count (n_split) from call to call.
+// Returns false after a wait gave up.
 template <int NI, int NMMA, int FMT = kFmtNv>
-__device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, const StreamK &sk,
-                              int warp, int lane, const int (&sh)[kMaxRowsX], float *red) {
+__device__ bool epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, const StreamK &sk,
+                              int warp, int lane, const int (&sh)[kMaxRowsX], float *red,
+                              int ib, int jb, int &n_split) {
   constexpr int MR = NMMA / kNC;  // rows of X the operand holds (>= M)
   const int q = warp & 3;
   const int row_in_tile = 32 * q + lane;
@@ -681,9 +709,8 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
 #pragma unroll
   for (int g = 0; g < kMaxGroups; ++g) osc[g] = g < a.n_groups ? *a.grp[g].ts : 0.0f;
   volatile int *last_flag = &bars.last;
-  int n_split = 0;
   for (int jj = 0; jj < sk.n_seg; ++jj) {
-    const int d = jj & 1, j = sk.proc_seg(jj);
+    const int J = jb + jj, d = J & 1, j = sk.proc_seg(jj);
     const int s0 = sk.seg_begin(j), s1 = sk.seg_end(j);
     int T32, c0;
     sk.tile_ch(s0, T32, c0);
@@ -691,8 +718,8 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     const int c1 = c0 + (s1 - s0);
     bool ok = true;
     for (int i = 0; i < NI; ++i)
-      ok = ok && mbar_wait_bounded(&bars.d_full[i][d], (uint32_t)((jj >> 1) & 1), a.status);
-    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      ok = ok && mbar_wait_bounded(&bars.d_full[i][d], (uint32_t)((J >> 1) & 1), a.status);
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
     tc_fence_after();
     float acc[MR];
 #pragma unroll
@@ -700,7 +727,7 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     const int p0 = sk.pbegin(jj);
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      if (s1 - s0 >= NI || ((i - p0) % NI + NI) % NI < s1 - s0) {  // issuer i had a stage
+      if (s1 - s0 >= NI || ((i - ib - p0) % NI + NI) % NI < s1 - s0) {  // issuer i had a stage
 #pragma unroll
         for (int h = 0; h < NMMA / 16; ++h) {
           uint32_t v[16];
@@ -788,11 +815,12 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
     if (warp == kEpiWarp0 && lane == 0) {
       const bool got = mbar_wait_bounded(&bars.part_done, par, a.status);
       __threadfence();
-      *last_flag = got && count_split_segment(a.cnt + T, a.epoch, nslot);
+      *last_flag = got && (a.cnt32 ? atomicAdd(a.cnt32 + T, 1u) == (unsigned)(nslot - 1)
+                                    : count_split_segment(a.cnt + T, a.epoch, nslot));
       __threadfence();
       mbar_arrive(&bars.flag_ready);
     }
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.flag_ready, par, a.status))) break;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bars.flag_ready, par, a.status))) return false;
     if (*last_flag) {
       __threadfence();
       if (row < gp.N) {
@@ -847,6 +875,7 @@ __device__ void epilogue_loop(const F4Args &a, F4Bars &bars, uint32_t tmem, cons
       }
     }
   }
+  return true;
 }
 
 __device__ __forceinline__ void init_common(F4Bars &bars, int ns, int ni) {
@@ -1030,7 +1059,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < NMMA / kNC; ++m)
       if (m < a.M) sh[m] = a.sh[m];
-    epilogue_loop<NI, NMMA>(a, bars, tmem, sk, warp, lane, sh, red);
+    int n_split = 0;
+    epilogue_loop<NI, NMMA>(a, bars, tmem, sk, warp, lane, sh, red, 0, 0, n_split);
   }
 
   tc_fence_before();
@@ -1391,7 +1421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sbars.slot_ready[j]);
     }
-    if (warp >= kEpiWarp0) epilogue_loop<kIssuersR, NMMA, FMT>(a, bars, tmem, sk, warp, lane, sh, red);
+    int n_split = 0;
+    if (warp >= kEpiWarp0)
+      epilogue_loop<kIssuersR, NMMA, FMT>(a, bars, tmem, sk, warp, lane, sh, red, 0, 0, n_split);
   } else if (warp == kLoaderWarpR) {
     // ---- warp 5: the zero pad after the last slot's scales, then (once the
     // split kernel has finished) this CTA's B slots: chunks ch_begin,
@@ -1424,7 +1456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < 2; ++m)
       if (m < a.M) sh[m] = a.sh[m];
-    epilogue_loop<kIssuersR, NMMA, FMT>(a, bars, tmem, sk, warp, lane, sh, red);
+    int n_split = 0;
+    epilogue_loop<kIssuersR, NMMA, FMT>(a, bars, tmem, sk, warp, lane, sh, red, 0, 0, n_split);
   } else if (warp < kIssuersR) {
     // ---- MMA issuers: each stage waits for its B slot
     const uint64_t dB0 = sdesc(smem_u32(bcodes), 16, 1024, kSw128);
@@ -1455,6 +1488,324 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // no rank leaves while another may still write into its shared memory
   if (a.sched == kSchedCluster) cluster_sync_all();
+}
+
+// ---- chained decode calls (one persistent launch) --------------------------------
+//
+// A decode step is a chain of GEMVs in which a call's X may be the previous
+// call's output (a layer's gate projection feeding its down projection, the
+// last layer feeding the LM head).  Launched one by one, every call pays a
+// kernel boundary: its CTAs start only when the previous call's leave the
+// SMs and the first weight bytes land microseconds later.  Here one launch
+// of one CTA per SM runs the calls in turn: the producer streams the next
+// call's weight into the ring as slots free (a weight is never written on
+// the stream, so it needs no wait), and only the MMAs of a call whose X is
+// the previous call's output wait, for a per-call count of finished CTAs in
+// the workspace.  Every CTA splits the K chunks of X it needs itself (seven
+// warps, in rounds; the issuers take each slot as soon as its round wrote
+// it), with its own prescale, so its partial sums leave in true units; a
+// call with the same X and chunks as the previous one keeps its slots.  The
+// B slots fill the shared memory the 8-stage ring leaves, so a call's split
+// waits until this CTA's MMAs of the previous call completed: the split and
+// its load of X sit between the calls (~3 us), as the separate split kernel
+// does between separate calls.  Split tiles of stream-K calls are counted
+// with plain atomic adds on counters the launch's first CTA clears (a
+// compare-and-swap counter under four contenders cost microseconds).
+// The CTAs wait for each other, so all of them must be resident at once:
+// one per SM (shared memory allows no second) and grid = SM count.  A
+// cooperative launch would guarantee it but measured ~3.5 us slower per
+// launch (it gives up the overlap with the previous kernel); the waits are
+// bounded instead.
+constexpr int kMaxChain = 4;
+constexpr int kChainSplitW = 7;  // warps 5, 6, 7 and 8..11 split X
+constexpr int kChainSlots = FmtR<kFmtNv>::kMaxSlots;
+// The chain's counters (workspace).  CTA 0 clears them at the start of a
+// launch and then publishes the launch's epoch in `ready`; every CTA waits
+// for that before it counts or reads a count, so a count left by another
+// launch, or whatever the workspace held, is never taken for this one's.
+// The last CTA to finish sets `ready` back to 0 (a graph replay reuses the
+// epoch).  Plain atomic adds: no compare-and-swap retries under contention.
+struct ChainCounters {
+  unsigned long long ready;
+  unsigned int done[kMaxChain];  // CTAs done with call c
+  unsigned int finished;         // CTAs past their last wait
+};
+struct F4Chain {
+  F4Args call[kMaxChain];
+  int n_calls;
+  int dep[kMaxChain];          // 1: call c reads call c - 1's output (wait for it)
+  int reuse[kMaxChain];        // 1: call c reads the same X and K chunks as call c - 1
+  int n_slots;                 // B slot images in shared memory (the most any call needs)
+  ChainCounters *cnt;          // in the workspace
+  unsigned long long epoch;    // unique per launch
+};
+struct F4ChainBars {
+  uint64_t slot_ready[kChainSlots];  // one phase per split (none for a call that keeps the slots)
+  uint32_t xmax[kChainSplitW][2];
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait until *p >= want (acquire); v: the value of an 8-byte word
+// (ready) or of a 4-byte count.
+__device__ __forceinline__ bool chain_wait_ready(const ChainCounters *k, unsigned long long epoch,
+                                                 int32_t *status) {
+  if (ld_acquire_u64(&k->ready) == epoch) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_u64(&k->ready) != epoch) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      report(status, IMP_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+__device__ __forceinline__ bool chain_wait_count(const unsigned int *c, unsigned int want,
+                                                 int32_t *status) {
+  if (ld_acquire_u32(c) >= want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_u32(c) < want) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      report(status, IMP_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// The split warps' share of one call: this CTA's B slots j < a.n_slots
+// (slot j = K chunk (ch0 + j) mod nch, as the issuers read them), warp w
+// taking slots w, w + 7, ...; the prescale of row m from this CTA's chunks.
+// Every slot barrier j < n_all gets one arrival per call.
+__device__ __forceinline__ void chain_split(const F4Args &a, int ch0, int nch, int n_all, int w,
+                                            int lane, F4ChainBars &cb, uint8_t *bcodes,
+                                            uint8_t *bsf, int (&sh)[kMaxRowsX]) {
+  constexpr int R = (kChainSlots + kChainSplitW - 1) / kChainSplitW;
+  const int bb = lane >> 1, hf = lane & 1;
+  uint4 v[R][2];
+  uint32_t mx[2] = {0u, 0u};
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int j = w + kChainSplitW * r;
+    if (j < a.n_slots) {
+      const int chn = (ch0 + j) % nch;
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+        if (m < a.M) {
+          // L2 only: X may have been written by other SMs in this launch
+          v[r][m] = __ldcg(reinterpret_cast<const uint4 *>(a.x + m * a.ldx +
+                                                          (int64_t)chn * kChunkK + 16 * bb + 8 * hf));
+          mx[m] = max(mx[m], absmax_bf16x8(v[r][m]));
+        }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    for (int o = 16; o; o >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], o));
+    if (lane == 0) cb.xmax[w][m] = mx[m];
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kChainSplitW) : "memory");
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < kChainSplitW; ++i) r = max(r, cb.xmax[i][m]);
+    sh[m] = prescale_exponent(r);
+  }
+  // round r makes slots 7 r .. 7 r + 6 ready: the issuers, which take the
+  // slots in order, start after the first round
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int j = w + kChainSplitW * r;
+    if (j < a.n_slots) {
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+        if (m < a.M)
+          split_chunk_slot(v[r][m], sh[m], m, a.M, bcodes + (size_t)j * 2048, bsf + (size_t)j * 1024,
+                           lane);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by tcgen05.mma / .cp
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cb.slot_ready[j]);
+    }
+  }
+  // slots this call does not use: one arrival per call all the same
+  if (lane == 0)
+    for (int j = w; j < n_all; j += kChainSplitW)
+      if (j >= a.n_slots) mbar_arrive(&cb.slot_ready[j]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemv_f4c_kernel(const __grid_constant__ F4Chain ch) {
+  using L = StageR;
+  constexpr int NMMA = 16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t *bcodes = smem + kNSR * L::BYTES;              // [slot][16 rows][128 B], swizzled
+  uint8_t *bsf = bcodes + (size_t)ch.n_slots * 2048;     // [slot][4 steps][256 B] + pad
+  F4Bars &bars = *reinterpret_cast<F4Bars *>(bsf + (size_t)ch.n_slots * 1024 + 256);
+  F4ChainBars &cb = *reinterpret_cast<F4ChainBars *>(reinterpret_cast<uint8_t *>(&bars) +
+                                                     ((sizeof(F4Bars) + 15) & ~size_t(15)));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t *status = ch.call[0].status;
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < ch.n_slots; ++j) mbar_init(&cb.slot_ready[j], 1);
+    init_common(bars, kNSR, kIssuersR);
+  }
+  if (warp == 0) tmem_alloc(&bars.tmem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem;
+
+  if (warp == kProducerR) {
+    // Every call's weight in turn through one ring (position g -> slot
+    // g % 8); the source of a stage is found before its slot frees.
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int c = 0; c < ch.n_calls && ok; ++c) {
+        const F4Args &a = ch.call[c];
+        const StreamK sk(a.n_tiles, a.n_chunks, a.sched, a.ksplit, a.grid);
+        PreparedTile src;
+        for (int i = 0; i < sk.n_st; ++i) {
+          int tile, chn;
+          sk.tile_ch(sk.stage_of(i), tile, chn);
+          src.at(a, tile, sk.nch);
+          const uint8_t *w = src.wc + (size_t)chn * 16384, *sf = src.wsa + (size_t)chn * 2048;
+          const int s = issued % kNSR;
+          if (issued >= kNSR &&
+              !mbar_wait_bounded(&bars.empty[s], (uint32_t)((issued / kNSR - 1) & 1), status)) {
+            ok = false;
+            break;
+          }
+          uint8_t *stg = smem + (size_t)s * L::BYTES;
+          mbar_arrive_expect_tx(&bars.full[s], L::TX);
+          bulk_g2s(stg + L::W, w, 16384u, &bars.full[s]);
+          bulk_g2s(stg + L::SFA, sf, 2048u, &bars.full[s]);
+          ++issued;
+        }
+      }
+      // never leave with copies in flight
+      for (int k = (issued > kNSR ? issued - kNSR : 0); k < issued; ++k)
+        mbar_wait_bounded(&bars.full[k % kNSR], (uint32_t)((k / kNSR) & 1), status);
+    }
+  } else if (warp < kIssuersR) {
+    const uint64_t dB0 = sdesc(smem_u32(bcodes), 16, 1024, kSw128);
+    const uint64_t dSB0 = sdesc(smem_u32(bsf), 0, 128, kNoSwizzle);
+    int ib = 0, jb = 0, n_splits = 0;
+    bool ok = true;
+    for (int c = 0; c < ch.n_calls && ok; ++c) {
+      const F4Args &a = ch.call[c];
+      const StreamK sk(a.n_tiles, a.n_chunks, a.sched, a.ksplit, a.grid);
+      // a call that keeps the previous call's slots waits on the same phase
+      if (!ch.reuse[c]) ++n_splits;
+      const uint32_t par = (uint32_t)((n_splits - 1) & 1);
+      // Wait for this call's split even with no stage in it: a parity wait
+      // is only right one phase ahead, and an issuer that skipped calls
+      // would otherwise take an older phase for this call's.  Every split
+      // arrives on slot 0 after all warps finished the previous split, so
+      // every slot barrier is at this call's phase or the one before.
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&cb.slot_ready[0], par, status))) {
+        ok = false;
+        break;
+      }
+      auto b_desc = [&](int, int st, int t) {
+        return dB0 + (uint64_t)((st % sk.nch) * (2048 >> 4)) + 2u * t;
+      };
+      auto sfb_desc = [&](int, int st, int t) {
+        return dSB0 + (uint64_t)((st % sk.nch) * (1024 >> 4)) + (uint64_t)(16u * t);
+      };
+      auto b_wait = [&](int st) { return mbar_wait_bounded(&cb.slot_ready[st % sk.nch], par, status); };
+      ok = issuer_loop<kIssuersR, kNSR, NMMA, true, L>(smem, bars, tmem, sk, warp, lane, status, b_desc,
+                                                       sfb_desc, b_wait, ib, jb, true);
+      ib += sk.n_st;
+      jb += sk.n_seg;
+    }
+    issuer_drain(bars, warp, lane, status);
+  } else if (warp == kLoaderWarpR || warp == kRelayWarp || warp == kSplitWarpX || warp >= kEpiWarp0) {
+    // Split warps (5, 6, 7, 8..11); 8..11 also run the epilogue.  Per call:
+    // wait for X if it is the previous call's output (one thread), meet
+    // (every split warp, the epilogue warps after the previous call's
+    // epilogue: its MMAs are complete, so the slots are free), split, then
+    // the epilogue and this CTA's count for the call.
+    const int w = warp < kEpiWarp0 ? warp - kLoaderWarpR : warp - kEpiWarp0 + 3;
+    if (w == 0 && lane < 16)  // read (into lanes no N = 16 MMA uses) after the last slot
+      reinterpret_cast<uint4 *>(bsf + (size_t)ch.n_slots * 1024)[lane] = make_uint4(0, 0, 0, 0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // X may come from the previous kernel
+    if (blockIdx.x == 0 && w == 0) {
+      // clear the counters (and the split-tile counts of stream-K calls),
+      // then publish this launch (the previous launch on the stream has
+      // finished: the wait above)
+      for (int c = 0; c < ch.n_calls; ++c)
+        if (ch.call[c].cnt32)
+          for (int t = lane; t < ch.call[c].n_tiles; t += 32) ch.call[c].cnt32[t] = 0u;
+      if (lane < kMaxChain) ch.cnt->done[lane] = 0u;
+      if (lane == 0) ch.cnt->finished = 0u;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(&ch.cnt->ready), "l"(ch.epoch) : "memory");
+    }
+    // A thread checks that the counters are this launch's right before it
+    // first counts or reads a count (by then CTA 0 has long published).
+    bool ready_seen = false;
+    int ib = 0, jb = 0, n_split = 0;
+    bool ok = true;
+    int sh[kMaxRowsX] = {};
+    for (int c = 0; c < ch.n_calls; ++c) {
+      const F4Args &a = ch.call[c];
+      const StreamK sk(a.n_tiles, a.n_chunks, a.sched, a.ksplit, a.grid);
+      if (!ch.reuse[c]) {
+        if (c > 0 && ch.dep[c] && w == 0 && lane == 0) {
+          if (!ready_seen) ready_seen = chain_wait_ready(ch.cnt, ch.epoch, status) || true;
+          chain_wait_count(&ch.cnt->done[c - 1], gridDim.x, status);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kChainSplitW) : "memory");
+        chain_split(a, sk.ch0, sk.nch, ch.n_slots, w, lane, cb, bcodes, bsf, sh);
+      }
+      if (warp >= kEpiWarp0) {
+        // the thread that counts split tiles and calls checks the counters
+        // once (CTA 0 published them long before)
+        if (c == 0 && warp == kEpiWarp0 && lane == 0) chain_wait_ready(ch.cnt, ch.epoch, status);
+        if (ok) ok = epilogue_loop<kIssuersR, NMMA>(a, bars, tmem, sk, warp, lane, sh, nullptr, ib, jb, n_split);
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (warp == kEpiWarp0 && lane == 0) {
+          __threadfence();  // this CTA's outputs of call c, then its count
+          atomicAdd(&ch.cnt->done[c], 1u);
+        }
+      }
+      ib += sk.n_st;
+      jb += sk.n_seg;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_free(tmem);
+  }
+  // the last CTA to finish withdraws the launch (all others are past their
+  // waits); the next launch's CTA 0 clears the counts
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&ch.cnt->finished, 1u) == gridDim.x - 1) {
+      __threadfence();
+      ch.cnt->ready = 0ull;
+    }
+  }
 }
 
 // ---- host --------------------------------------------------------------------
@@ -1950,6 +2301,134 @@ cudaError_t launch_gemv_f4_grouped(const uint16_t *x, int64_t M, int64_t K, int6
                                    const GemvGroup *g, int n, int32_t *status, void *workspace,
                                    cudaStream_t stream) {
   return launch_resident(x, M, K, ldx, g, n, status, workspace, stream, true);
+}
+
+
+// ---- chained calls ------------------------------------------------------------------
+
+namespace {
+// The chain's schedule: per link whole tiles (at least 3/4 as many tiles as
+// SMs) or stream-K over all SMs, and its B slots; the workspace: the
+// counters (256 bytes), then per stream-K link its tile counters and
+// partial sums.
+struct ChainPlan {
+  int sched[kMaxChain], grid[kMaxChain], n_slots[kMaxChain], max_slots;
+  size_t cnt[kMaxChain], part[kMaxChain], total, smem;
+  bool ok;
+};
+ChainPlan plan_chain(int64_t M, const ChainLink *l, int n) {
+  ChainPlan p = {};
+  const int64_t G = num_sms();
+  if (n < 1 || n > kMaxChain || M < 1 || M > 2 || G > kMaxGrid) return p;
+  size_t off = 256;
+  for (int c = 0; c < n; ++c) {
+    const int64_t K = l[c].K;
+    if (l[c].n < 1 || l[c].n > kMaxGroups || K < 4 * kChunkK || K % kChunkK || K > (1 << 24))
+      return p;
+    for (int i = 0; i < l[c].n; ++i) {
+      const GemvGroup &g = l[c].g[i];
+      if (g.N < 1 || g.N > 0x7FFFFFFFll || (((uintptr_t)g.codes | (uintptr_t)g.scales) & 15u))
+        return p;
+    }
+    const int64_t tiles = group_tiles(l[c].g, l[c].n), nch = K / kChunkK;
+    if (tiles * nch > 0x7FFFFFFFll) return p;
+    if (4 * tiles >= 3 * G) {
+      p.sched[c] = kSchedWhole;
+      p.n_slots[c] = (int)nch;
+    } else {
+      p.sched[c] = kSchedStreamK;
+      p.grid[c] = (int)(tiles * nch < G ? tiles * nch : G);
+      const int64_t per = ceil_div(tiles * nch, p.grid[c]);
+      p.n_slots[c] = (int)(per < nch ? per : nch);
+      p.cnt[c] = off;
+      off += (size_t)ceil_div(tiles * 16, 256) * 256;
+      p.part[c] = off;
+      off += (size_t)kMaxGrid * 2 * 2 * kTileRows * sizeof(float);
+    }
+    if (p.n_slots[c] > kChainSlots) return p;
+    if (p.n_slots[c] > p.max_slots) p.max_slots = p.n_slots[c];
+  }
+  p.total = off;
+  p.smem = (size_t)kNSR * StageR::BYTES + (size_t)p.max_slots * (2048 + 1024) + 256 +
+           ((sizeof(F4Bars) + 15) & ~size_t(15)) + sizeof(F4ChainBars) + 1024;
+  p.ok = p.smem <= 227 * 1024;
+  return p;
+}
+}  // namespace
+
+bool gemv_f4_chain_ok(int64_t M, const ChainLink *l, int n) { return plan_chain(M, l, n).ok; }
+
+size_t gemv_f4_chain_workspace_bytes(int64_t M, const ChainLink *l, int n) {
+  const ChainPlan P = plan_chain(M, l, n);
+  return P.ok ? P.total : 0;
+}
+
+cudaError_t launch_gemv_f4_chain(int64_t M, const ChainLink *l, int n, int32_t *status,
+                                 void *workspace, cudaStream_t stream) {
+  const ChainPlan P = plan_chain(M, l, n);
+  if (!P.ok) return cudaErrorInvalidValue;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  F4Chain ch = {};
+  ch.n_calls = n;
+  ch.n_slots = P.max_slots;
+  ch.cnt = reinterpret_cast<ChainCounters *>(ws);
+  ch.epoch = next_launch_epoch();
+  for (int c = 0; c < n; ++c) {
+    F4Args &a = ch.call[c];
+    a.x = l[c].x;
+    a.ldx = l[c].ldx;
+    a.M = (int)M;
+    a.K = l[c].K;
+    a.status = status;
+    if (P.sched[c] == kSchedStreamK) {
+      a.cnt32 = reinterpret_cast<unsigned int *>(ws + P.cnt[c]);
+      a.part = reinterpret_cast<float *>(ws + P.part[c]);
+    }
+    a.n_groups = l[c].n;
+    int64_t t = 0;
+    for (int i = 0; i < l[c].n; ++i) {
+      const GemvGroup &g = l[c].g[i];
+      a.grp[i] = F4Group{g.codes, g.scales, g.tensor_scale, g.y, g.N, g.ldy, (int)t};
+      t += ceil_div(g.N, kTileRows);
+    }
+    a.n_tiles = (int)t;
+    a.n_chunks = (int)(l[c].K / kChunkK);
+    a.epoch = next_launch_epoch();
+    a.n_slots = P.n_slots[c];
+    a.sched = P.sched[c];
+    a.grid = P.grid[c];
+    a.ksplit = 1;
+    ch.dep[c] = l[c].dep ? 1 : 0;
+    // the previous call's B slots serve again: same X, same chunks in every
+    // CTA (whole tiles: all of them), and not two such calls in a row (the
+    // slot barriers' phases may run at most one call ahead of the issuers)
+    ch.reuse[c] = c > 0 && !l[c].dep && !ch.reuse[c - 1] && l[c].x == l[c - 1].x &&
+                  l[c].ldx == l[c - 1].ldx && l[c].K == l[c - 1].K &&
+                  P.sched[c] == kSchedWhole && P.sched[c - 1] == kSchedWhole;
+  }
+  cudaError_t e = cudaFuncSetAttribute(gemv_f4c_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)P.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = P.smem;
+  cfg.stream = stream;
+  // The CTAs wait for each other, so all of them must be resident at once:
+  // one per SM (its shared memory allows no second) and as many as SMs,
+  // which holds whenever no other kernel occupies SMs for long (a wait gives
+  // up after kWaitLimitNs and reports IMP_DEV_TIMEOUT).  A cooperative
+  // launch would guarantee it but measured ~3.5 us slower per launch (it
+  // gives up the overlap with the previous kernel).  Programmatic dependent
+  // launch lets the weight stream start while the previous kernel drains.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemv_f4c_kernel, ch);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace impfp4

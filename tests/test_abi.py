@@ -90,6 +90,59 @@ def test_grouped_plan():
 A16 = 0x7F0000000000  # fake, 16-byte aligned "device" addresses: never dereferenced
 
 
+def _chain(spec):
+    """ChainLinks from [(K, [N...], chained?)] with fake aligned addresses
+    (outputs 16 MB apart, explicit X beyond them)."""
+    links, k = [], 0
+    for c, (K, Ns, chained) in enumerate(spec):
+        gs = []
+        for N in Ns:
+            gs.append(pkg.ImpNvfp4Group(_t(N, K), A16 + (1 + k) * (1 << 24), (N + 7) // 8 * 8))
+            k += 1
+        links.append((gs, None if chained else A16 + (100 + c) * (1 << 24), K))
+    return pkg.ChainLinks(links)
+
+
+def test_chain_plan():
+    # the 27B-class decode step as one persistent launch: up, gate (x), down
+    # (gate's output), LM head (down's output); a 0.6B-class layer
+    step = [(5120, [17408], False), (5120, [17408], False), (17408, [5120], True),
+            (5120, [151936], True)]
+    assert pkg.imp_nvfp4_gemm_chain_plan(1, _chain(step)) == 1
+    assert pkg.imp_nvfp4_gemm_chain_plan(2, _chain(step)) == 1
+    small = [(1024, [2048, 1024, 1024], False), (2048, [1024], True), (1024, [3072, 3072], False),
+             (3072, [1024], False)]
+    assert pkg.imp_nvfp4_gemm_chain_plan(1, _chain(small)) == 1
+    # grouped calls one after another: more rows of X, a K below 1024, a
+    # CTA needing more than 24 K chunks (17408 x 17408: ~60 per CTA)
+    assert pkg.imp_nvfp4_gemm_chain_plan(4, _chain(step)) == 0
+    assert pkg.imp_nvfp4_gemm_chain_plan(1, _chain([(512, [1024], False)])) == 0
+    assert pkg.imp_nvfp4_gemm_chain_plan(1, _chain([(17408, [17408], False)])) == 0
+    ws = pkg.imp_nvfp4_gemm_chain_workspace_size(1, _chain(step))
+    assert ws >= pkg.imp_nvfp4_gemm_workspace_size(1, 151936, 5120)
+    # invalid: chained link 0, chained K != the previous output's length, 5 links
+    assert pkg.imp_nvfp4_gemm_chain_plan(1, _chain([(1024, [128], True)])) == 0
+    assert pkg.imp_nvfp4_gemm_chain_workspace_size(1, _chain([(1024, [512], False),
+                                                              (1024, [128], True)])) == 0
+    assert pkg.imp_nvfp4_gemm_chain_workspace_size(1, _chain([(1024, [1024], False)] * 5)) == 0
+
+
+def test_chain_rejects_overlaps():
+    g = pkg.imp_nvfp4_gemm_chain
+    ok = _chain([(1024, [1024], False), (1024, [512], True)])
+    assert g(1, ok, None, None, 0, None) == pkg.IMP_ERR_WORKSPACE_TOO_SMALL
+    # two links writing the same output
+    y = A16 + (1 << 30)
+    dup = pkg.ChainLinks([([pkg.ImpNvfp4Group(_t(1024, 1024), y, 1024)], A16, 1024),
+                          ([pkg.ImpNvfp4Group(_t(512, 1024), y + 512, 512)], None, 0)])
+    assert g(1, dup, None, A16, 1 << 30, None) == pkg.IMP_ERR_INVALID_ARG
+    # an output over an explicit X
+    over = pkg.ChainLinks([([pkg.ImpNvfp4Group(_t(1024, 1024), y, 1024)], y + 1024, 1024)])
+    assert g(1, over, None, A16, 1 << 30, None) == pkg.IMP_ERR_INVALID_ARG
+    # M = 0: nothing to do
+    assert g(0, ok, None, None, 0, None) == pkg.IMP_OK
+
+
 def _t(rows, K, codes=A16, scales=A16 + 0x100000, ts=A16 + 0x200000):
     return ImpNvfp4Tensor(codes, scales, ts, rows, K)
 
