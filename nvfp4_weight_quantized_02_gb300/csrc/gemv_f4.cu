@@ -54,6 +54,10 @@
 //    B operands of 16 or 32 rows (8-deep ring), two for 64 (6-deep), one for
 //    128 (5-deep): a wider MMA takes longer, so fewer issuers keep ahead of
 //    HBM, and the wider B stages fill the shared memory sooner.
+//  * gemv_f4c_kernel (M <= 2, several calls in one launch): the resident
+//    kernel's roles run call after call through one ring; each CTA splits
+//    its chunks of a call's X itself (warps 5..11), after a per-call count
+//    of finished CTAs when X is the previous call's output.
 // Issuer: one thread copies both operands' scale atoms of a stage to tensor
 // memory (tcgen05.cp) and issues four M=128 x N=N_MMA x K=64 MMAs into its
 // own accumulator.  One issuing thread sustains one MMA per ~130 cycles;
