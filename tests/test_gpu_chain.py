@@ -174,3 +174,33 @@ def test_chain_rejects():
         pkg.gemm_chain([([d0], x), ([d0], x)], ys=[[y], [y]])
     with pytest.raises(pkg.ImpError):  # an output over an explicit X
         pkg.gemm_chain([([d0], x)], ys=[[x]])
+
+
+@pytest.mark.parametrize("case", [0, 4])
+def test_chain_back_to_back_launches(case):
+    """Ten launches queued back to back on one workspace (each may start
+    while the previous one drains): no wait gives up and every launch writes
+    the same bits.  Case 4 keeps the split X between calls, whose barrier
+    phases must stay in step from launch to launch."""
+    M, spec = chains()[case]
+    links, xs = [], []
+    for c, (K, Ns, src) in enumerate(spec):
+        d = [prepared(lin(f"b{case}{c}g{i}", M, K, N, 31 * c + i))[1] for i, N in enumerate(Ns)]
+        x = None if src == "prev" else xs[-1] if src == "same" else \
+            dev_bf16(lin(f"bx{c}", M, K, 1, 5 + c).act_bf16())
+        xs.append(x)
+        links.append((d, x))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = [[y.clone() for y in yl] for yl in run_chain(links)]
+    ys = [[torch.empty_like(y) for y in yl] for yl in ref]
+    ws_bytes = pkg.imp_nvfp4_gemm_chain_workspace_size(M, pkg.ChainLinks(
+        [([pkg.ImpNvfp4Group(w.c_struct(), 0, 0) for w in d], None if x is None else 16, 0)
+         for d, x in links]))
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    for _ in range(10):
+        pkg.gemm_chain(links, ys=ys, dev_status=status, workspace=work)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for ya, yb in zip(ref, ys):
+        for u, v in zip(ya, yb):
+            assert torch.equal(u.view(torch.int16), v.view(torch.int16))
