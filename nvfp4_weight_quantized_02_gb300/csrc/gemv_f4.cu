@@ -1772,7 +1772,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_f4c_kernel(const __grid_cons
       const StreamK sk(a.n_tiles, a.n_chunks, a.sched, a.ksplit, a.grid);
       if (!ch.reuse[c]) {
         if (c > 0 && ch.dep[c] && w == 0 && lane == 0) {
-          if (!ready_seen) ready_seen = chain_wait_ready(ch.cnt, ch.epoch, status) || true;
+          if (!ready_seen) {
+            chain_wait_ready(ch.cnt, ch.epoch, status);  // gives up (and reports) after 1 s
+            ready_seen = true;
+          }
           chain_wait_count(&ch.cnt->done[c - 1], gridDim.x, status);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kChainSplitW) : "memory");
