@@ -355,9 +355,35 @@ def run_native(args):
     plans = [pkg.imp_fp8_gemm_plan(l.M, l.N, l.K) if fp8 else pkg.imp_nvfp4_gemm_plan(l.M, l.N, l.K)
              for l in lins]
     call = pkg.gemm_fp8 if fp8 else pkg.gemm_mma
+    use_chain = args.chain and not fp8
+
+    def chain_of(ins, outs):
+        """The step's calls as one decode chain (a call reading the previous
+        call's output takes it from there)."""
+        spec = []
+        for i, (x, w, y) in enumerate(zip(ins, weights, outs)):
+            g = [pkg.ImpNvfp4Group(w.c_struct(), y.data_ptr(), y.stride(0))]
+            dep = i > 0 and x is outs[i - 1]
+            spec.append((g, None if dep else x.data_ptr(), 0 if dep else x.stride(0)))
+        return pkg.ChainLinks(spec)
+
+    def run_chain(cl, ws, st):
+        r = pkg.imp_nvfp4_gemm_chain(1, cl, status.data_ptr(), ws.data_ptr(), ws.numel(), st)
+        if r != pkg.IMP_OK:
+            raise pkg.ImpError(r, "imp_nvfp4_gemm_chain")
+
+    if use_chain:
+        step_chain = chain_of(chained, ys)
+        chain_ws = torch.empty(pkg.imp_nvfp4_gemm_chain_workspace_size(1, step_chain),
+                               dtype=torch.uint8, device=dev)
+        if pkg.imp_nvfp4_gemm_chain_plan(1, step_chain) != 1:
+            raise RuntimeError("the decode chain has no persistent plan for this workload")
     torch.cuda.synchronize()
 
     def step():
+        if use_chain:
+            run_chain(step_chain, chain_ws, pkg._stream_handle(stream))
+            return
         for x, w, y, ws in zip(chained, weights, ys, wss):
             call(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
 
@@ -423,7 +449,12 @@ def run_native(args):
         feeds.append((ins, outs))
     copy_stream = torch.cuda.Stream(dev)
 
+    feed_chains = [chain_of(ins, outs) for ins, outs in feeds] if use_chain else None
+
     def step_on(k):
+        if use_chain:
+            run_chain(feed_chains[k], chain_ws, pkg._stream_handle(stream))
+            return
         ins, outs = feeds[k]
         for x, w, y, ws in zip(ins, weights, outs, wss):
             call(x, w, y=y, dev_status=status, stream=stream, workspace=ws)
@@ -498,6 +529,8 @@ def run_native(args):
                                         "imp_nvfp4_gemm_mma per call)",
                                "mxfp4": "MXFP4, converted once to NVFP4 form and prepared",
                                "fp8": "FP8 E4M3 row-major (imp_fp8_gemm per call)"}[args.weights],
+                   "step_api": ("imp_nvfp4_gemm_chain, one launch per step" if use_chain else
+                                "one imp_nvfp4_gemm_mma (fp8: imp_fp8_gemm) per call"),
                    "l2": "inputs larger than L2 (588 MB of weights per step)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_hbm_peak": value / world / hbm_peak,
@@ -512,8 +545,9 @@ def run_native(args):
                      "back_to_back": {"us_per_launch": b2b_us,
                                       "achieved": cbytes(lt) / (b2b_us * 1e-6) / 1e9,
                                       "frac": cbytes(lt) / (b2b_us * 1e-6) / 1e9 / hbm_peak}},
-        "gpu_launches": args.steps * sum(n for n, _ in plans),
-        "kernels": {l.name: {"kernel": k, "launches_per_call": n} for l, (n, k) in zip(lins, plans)},
+        "gpu_launches": args.steps * (1 if use_chain else sum(n for n, _ in plans)),
+        "kernels": ({"step": {"kernel": "gemv_f4c_kernel", "launches_per_step": 1}} if use_chain else
+                    {l.name: {"kernel": k, "launches_per_call": n} for l, (n, k) in zip(lins, plans)}),
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": pin_x.numel() * 2,
                 "d2h_bytes_per_step": pin_y[0].numel() * 2,
@@ -1207,6 +1241,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--chain", action="store_true",
+                    help="run the decode step as one decode-chain launch (imp_nvfp4_gemm_chain)")
     ap.add_argument("--weights", choices=["nvfp4", "mxfp4", "fp8"], default="nvfp4",
                     help="weight format of the decode step (mxfp4: converted once to the NVFP4 "
                          "form; fp8: E4M3 with one tensor scale)")
