@@ -994,6 +994,27 @@ def bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs, ch
         for _ in range(args.warmup):
             grouped_step()
         out["decode_grouped_up_gate"] = rate(time_blocks(grouped_step, n, 10, stream))
+
+        # the layer's true MLP dataflow: gate and up grouped, the down
+        # projection on silu(gate) * up (formed in its X split), the LM head
+        # on down's output
+        if "down" in by and lins[by["down"]].K == lins[ig].N:
+            idn = by["down"]
+            rest = [i for i in range(len(lins)) if i not in (iu, ig, idn)]
+
+            def swiglu_step():
+                pkg.gemm_grouped(chained[iu], [weights[ig], weights[iu]], ys=[ys[ig], ys[iu]],
+                                 dev_status=status, stream=stream, workspace=gws)
+                pkg.gemm_mma_swiglu(ys[ig], ys[iu], weights[idn], y=ys[idn], dev_status=status,
+                                    stream=stream, workspace=wss[idn])
+                for i in rest:
+                    pkg.gemm_mma(chained[i], weights[i], y=ys[i], dev_status=status,
+                                 stream=stream, workspace=wss[i])
+            for _ in range(args.warmup):
+                swiglu_step()
+            out["decode_swiglu_mlp"] = dict(
+                rate(time_blocks(swiglu_step, n, 10, stream)),
+                dataflow="gate and up grouped on x; down on silu(gate) * up; LM head on down")
         del gws
 
     # the step as one decode chain (imp_nvfp4_gemm_chain: one persistent
@@ -1077,6 +1098,32 @@ def bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs, ch
                                          "TFLOP/s": 2 * l.M * l.N * l.K / (t * 1e-6) / 1e12,
                                          "kernel": kern, "launches": nk}
     out["skinny_decode"] = skinny
+
+    # The step's 50 MB projections (M = 1) one call after another, each call
+    # on another copy of its weight (the copies exceed L2 twice over, so every
+    # call streams its weight from HBM): a call's cost inside a stream of
+    # calls, without event records between them.
+    b2b, seen = {}, set()
+    for i, l in enumerate(lins):
+        if l.weight_bytes > L2_BYTES // 2 or (l.K, l.N) in seen:
+            continue
+        seen.add((l.K, l.N))
+        wl = rotated_copies(pkg, weights[i], max(2, -(-2 * L2_BYTES // l.weight_bytes)))
+        k = [0]
+
+        def one(i=i, k=k, wl=wl):
+            pkg.gemm_mma(chained[i], wl[k[0] % len(wl)], y=ys[i], dev_status=status,
+                         stream=stream, workspace=wss[i])
+            k[0] += 1
+        for _ in range(len(wl) * 2):
+            one()
+        ts = time_blocks(one, len(wl) * 5, 10, stream)
+        t = statistics.median(ts)
+        b2b[f"{l.name}_{l.K}x{l.N}"] = {"us": spread(ts), "GB/s": call_bytes(l) / (t * 1e-6) / 1e9,
+                                        "frac_of_hbm_peak": call_bytes(l) / (t * 1e-6) / 1e9 / hbm_peak,
+                                        "weight_copies": len(wl)}
+        del wl
+    out["per_call_back_to_back"] = b2b
     del cache
 
     # quantizer: the LM-head-sized weight (two reads of X + codes and scales written)

@@ -407,6 +407,26 @@ imp_status imp_nvfp4_gemm_swiglu(const void *x_bf16, int64_t M, int64_t K, int64
                                  int32_t *dev_status, void *workspace, size_t ws_bytes,
                                  void *stream);
 
+/* The decode counterpart (M <= 16): the down projection of an MLP whose
+ * input is the activation of its gate and up outputs,
+ *   Y = h * W^T,   h = bf16(silu(gate) * up)   (silu(v) = v / (1 + e^-v),
+ * evaluated in fp32 as imp_nvfp4_gemm_swiglu does), with h formed where the
+ * decode path's split of X reads it (no separate activation kernel, h is
+ * not written).  gate_bf16 and up_bf16: device bf16[M][ld], ld >= K,
+ * ld % 8 == 0, 16-byte aligned (the outputs of the layer's gate and up
+ * projections, e.g. one imp_nvfp4_gemm_grouped call).  w in MMA layout.
+ * The shape must take the FP4 decode path (K % 256 == 0, K >= 1024,
+ * N >= 128, M <= 16), else IMP_ERR_UNSUPPORTED_SHAPE.  Workspace as for
+ * imp_nvfp4_gemm_mma.  Accuracy: that of imp_nvfp4_gemm on h.  An addition
+ * of this library.                                                          */
+imp_status imp_nvfp4_gemm_mma_swiglu(const void *gate_bf16, const void *up_bf16, int64_t M,
+                                     int64_t K, int64_t ld, const imp_nvfp4_tensor *w_mma,
+                                     void *y_bf16, int64_t ldy, int32_t *dev_status,
+                                     void *workspace, size_t ws_bytes, void *stream);
+/* Kernel launches of imp_nvfp4_gemm_mma_swiglu (0: rejected) and, in
+ * *kernel, the weight-streaming kernel.  Host only. */
+int32_t imp_nvfp4_gemm_mma_swiglu_plan(int64_t M, int64_t N, int64_t K, const char **kernel);
+
 /* imp_nvfp4_quantize_mma with the global amax already known (bf16 magnitude
  * bits of max|x| in device memory, as imp_nvfp4_gemm_swiglu writes it): the
  * encode pass alone, one read of X.  Bit-identical to imp_nvfp4_quantize_mma

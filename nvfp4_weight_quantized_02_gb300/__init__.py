@@ -119,6 +119,10 @@ def _L():
     lib.imp_nvfp4_prepare_mma.argtypes = [T, P, SZ, P, SZ, P]
     lib.imp_nvfp4_gemm_mma.restype = ctypes.c_int
     lib.imp_nvfp4_gemm_mma.argtypes = [P, I64, I64, I64, T, P, I64, P, P, SZ, P]
+    lib.imp_nvfp4_gemm_mma_swiglu.restype = ctypes.c_int
+    lib.imp_nvfp4_gemm_mma_swiglu.argtypes = [P, P, I64, I64, I64, T, P, I64, P, P, SZ, P]
+    lib.imp_nvfp4_gemm_mma_swiglu_plan.restype = ctypes.c_int32
+    lib.imp_nvfp4_gemm_mma_swiglu_plan.argtypes = [I64, I64, I64, ctypes.POINTER(ctypes.c_char_p)]
     lib.imp_nvfp4_quantize_mma.restype = ctypes.c_int
     lib.imp_nvfp4_quantize_mma.argtypes = [P, I64, I64, I64, T, P, P, SZ, P]
     lib.imp_nvfp4_quantize_noalloc.restype = ctypes.c_int
@@ -243,6 +247,19 @@ def imp_nvfp4_gemm_mma(x_bf16: int, M: int, K: int, ldx: int, w: ImpNvfp4Tensor,
                        stream: int | None) -> int:
     return _L().imp_nvfp4_gemm_mma(x_bf16, M, K, ldx, ctypes.byref(w), y_bf16, ldy, dev_status,
                                    workspace, ws_bytes, stream)
+
+
+def imp_nvfp4_gemm_mma_swiglu(gate_bf16: int, up_bf16: int, M: int, K: int, ld: int,
+                              w: ImpNvfp4Tensor, y_bf16: int, ldy: int, dev_status: int | None,
+                              workspace: int | None, ws_bytes: int, stream: int | None) -> int:
+    return _L().imp_nvfp4_gemm_mma_swiglu(gate_bf16, up_bf16, M, K, ld, ctypes.byref(w), y_bf16,
+                                          ldy, dev_status, workspace, ws_bytes, stream)
+
+
+def imp_nvfp4_gemm_mma_swiglu_plan(M: int, N: int, K: int) -> tuple[int, str | None]:
+    name = ctypes.c_char_p()
+    n = _L().imp_nvfp4_gemm_mma_swiglu_plan(M, N, K, ctypes.byref(name))
+    return n, (name.value.decode() if name.value else None)
 
 
 def imp_nvfp4_quantize_mma(x_bf16: int, rows: int, K: int, ldx: int, out: ImpNvfp4Tensor,
@@ -550,6 +567,31 @@ def gemm_mma(x, w: NVFP4Tensor, y=None, dev_status=None, stream=None, workspace=
                             _stream_handle(stream))
     if st != IMP_OK:
         raise ImpError(st, "imp_nvfp4_gemm_mma")
+    return y
+
+
+def gemm_mma_swiglu(gate, up, w: NVFP4Tensor, y=None, dev_status=None, stream=None,
+                    workspace=None):
+    """Y = bf16(silu(gate) * up) W^T at decode sizes (M <= 16), the
+    activation formed inside the call (imp_nvfp4_gemm_mma_swiglu)."""
+    import torch
+    for t in (gate, up):
+        assert t.dtype == torch.bfloat16 and t.dim() == 2 and t.stride(1) == 1
+    assert gate.shape == up.shape and gate.stride(0) == up.stride(0) and w.layout == "mma"
+    M, K = gate.shape
+    N = w.rows
+    if y is None:  # row stride rounded up to a multiple of 8 elements
+        y = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=gate.device)[:, :N]
+    ws_bytes = imp_nvfp4_gemm_workspace_size(M, N, K)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=gate.device)
+    st = imp_nvfp4_gemm_mma_swiglu(gate.data_ptr(), up.data_ptr(), M, K, gate.stride(0),
+                                   w.c_struct(), y.data_ptr(), y.stride(0),
+                                   None if dev_status is None else dev_status.data_ptr(),
+                                   None if workspace is None else workspace.data_ptr(), ws_bytes,
+                                   _stream_handle(stream))
+    if st != IMP_OK:
+        raise ImpError(st, "imp_nvfp4_gemm_mma_swiglu")
     return y
 
 

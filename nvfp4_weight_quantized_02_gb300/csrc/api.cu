@@ -322,6 +322,38 @@ imp_status imp_nvfp4_gemm_mma(const void *x_bf16, int64_t M, int64_t K, int64_t 
   return from_cuda(e);
 }
 
+int32_t imp_nvfp4_gemm_mma_swiglu_plan(int64_t M, int64_t N, int64_t K, const char **kernel) {
+  const char *k = nullptr;
+  const int32_t n = M >= 1 && M <= kDecodeMaxM ? impfp4::gemv_f4_swiglu_launches(M, N, K, &k) : 0;
+  if (kernel) *kernel = n ? k : nullptr;
+  return n;
+}
+
+imp_status imp_nvfp4_gemm_mma_swiglu(const void *gate_bf16, const void *up_bf16, int64_t M,
+                                     int64_t K, int64_t ld, const imp_nvfp4_tensor *w,
+                                     void *y_bf16, int64_t ldy, int32_t *dev_status,
+                                     void *workspace, size_t ws_bytes, void *stream) {
+  if (M < 0 || !w) return IMP_ERR_INVALID_ARG;
+  if (K <= 0 || K % 64) return IMP_ERR_UNSUPPORTED_SHAPE;
+  const int64_t N = w->rows;
+  if (N < 0 || w->K != K) return IMP_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return IMP_OK;
+  imp_status st = check_tensor(w, N, K);
+  if (st != IMP_OK) return st;
+  if (!gate_bf16 || !up_bf16 || !y_bf16) return IMP_ERR_INVALID_ARG;
+  if (ld < K || ldy < N) return IMP_ERR_INVALID_ARG;
+  if (!aligned16(gate_bf16) || !aligned16(up_bf16) || !aligned16(y_bf16) || ld % 8 || ldy % 8)
+    return IMP_ERR_MISALIGNED;
+  if (M > kDecodeMaxM || !impfp4::gemv_f4_shape_ok(M, N, K)) return IMP_ERR_UNSUPPORTED_SHAPE;
+  const size_t need = impfp4::gemv_f4_workspace_bytes(M, N, K);
+  if (!workspace || ws_bytes < need) return IMP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return IMP_ERR_MISALIGNED;
+  return from_cuda(impfp4::launch_gemv_f4(
+      static_cast<const uint16_t *>(gate_bf16), M, K, ld, w->codes, w->scales, w->tensor_scale, N,
+      static_cast<uint16_t *>(y_bf16), ldy, dev_status, workspace,
+      static_cast<cudaStream_t>(stream), true, static_cast<const uint16_t *>(up_bf16), ld));
+}
+
 }  // extern "C"
 
 namespace {

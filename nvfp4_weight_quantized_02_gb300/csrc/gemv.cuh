@@ -43,11 +43,16 @@ bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const
 int gemv_f4_launches(int64_t M, int64_t N, int64_t K, const char **kernel);
 // `prepared`: codes and scales in the tensor-core (MMA) layout of
 // quantize.cuh (contiguous 16 KB code tiles and 2 KB scale-atom runs per
-// stage) instead of row-major.
+// stage) instead of row-major.  `x2` (optional, bf16[M][ldx2]): X is then
+// bf16(silu(x) * x2), formed where the split kernel reads it.
 cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
-                           cudaStream_t stream, bool prepared = false);
+                           cudaStream_t stream, bool prepared = false,
+                           const uint16_t *x2 = nullptr, int64_t ldx2 = 0);
+// Kernel launches of a call with the SwiGLU X (x2 given): always through a
+// split kernel; 0 if the FP4 decode path does not take the shape.
+int gemv_f4_swiglu_launches(int64_t M, int64_t N, int64_t K, const char **kernel);
 
 // Grouped decode GEMV: one X times up to four weights of the same K in one
 // launch pair (the weights' tiles follow each other in one schedule; each

@@ -383,6 +383,21 @@ __device__ __forceinline__ int prescale_exponent(uint32_t mx_bits16) {
   return 15 - e;
 }
 
+// h = silu(g) * u for eight bf16 pairs, in fp32 (silu(v) = v / (1 + e^-v),
+// as the prefill SwiGLU epilogue evaluates it), rounded to bf16: the X of a
+// down projection whose input is the activation of its gate and up outputs.
+__device__ __forceinline__ uint32_t swiglu_bf16x2(uint32_t g2, uint32_t u2) {
+  const float g0 = __uint_as_float(g2 << 16), g1 = __uint_as_float(g2 & 0xFFFF0000u);
+  const float u0 = __uint_as_float(u2 << 16), u1 = __uint_as_float(u2 & 0xFFFF0000u);
+  const float h0 = g0 / (1.0f + expf(-g0)) * u0, h1 = g1 / (1.0f + expf(-g1)) * u1;
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(h0)) |
+         (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(h1)) << 16;
+}
+__device__ __forceinline__ uint4 swiglu_bf16x8(const uint4 g, const uint4 u) {
+  return make_uint4(swiglu_bf16x2(g.x, u.x), swiglu_bf16x2(g.y, u.y), swiglu_bf16x2(g.z, u.z),
+                    swiglu_bf16x2(g.w, u.w));
+}
+
 __device__ __forceinline__ uint32_t absmax_bf16x8(const uint4 v) {
   return max(max(max(v.x & 0x7FFFu, v.x >> 16 & 0x7FFFu), max(v.y & 0x7FFFu, v.y >> 16 & 0x7FFFu)),
              max(max(v.z & 0x7FFFu, v.z >> 16 & 0x7FFFu), max(v.w & 0x7FFFu, v.w >> 16 & 0x7FFFu)));
@@ -906,7 +921,7 @@ __device__ __forceinline__ void init_common(F4Bars &bars, int ns, int ni) {
 // M); every CTA finds its row's max|x|, then each thread splits one block.
 __global__ void __launch_bounds__(kXsplitThreads)
     xsplit_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, int nmma, uint8_t *bcodes,
-                  uint8_t *sfb, int32_t *sh_out) {
+                  uint8_t *sfb, int32_t *sh_out, const uint16_t *x2, int64_t ldx2) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // X may come from the previous kernel, and the previous GEMV may still
   // read the workspace: wait for it before touching either.
@@ -914,10 +929,15 @@ __global__ void __launch_bounds__(kXsplitThreads)
   __shared__ uint32_t red[kXsplitThreads / 32];
   const int m = blockIdx.y;
   const uint16_t *xr = x + m * ldx;
+  // x2 (optional): X is silu(x) * x2, computed where it is read
+  const uint16_t *ur = x2 ? x2 + m * ldx2 : nullptr;
+  auto ld8 = [&](int64_t i) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr) + i);
+    return ur ? swiglu_bf16x8(v, __ldg(reinterpret_cast<const uint4 *>(ur) + i)) : v;
+  };
   const int64_t nb = K / 16;
   uint32_t mx = 0;
-  for (int64_t i = threadIdx.x; i < K / 8; i += kXsplitThreads)
-    mx = max(mx, absmax_bf16x8(__ldg(reinterpret_cast<const uint4 *>(xr) + i)));
+  for (int64_t i = threadIdx.x; i < K / 8; i += kXsplitThreads) mx = max(mx, absmax_bf16x8(ld8(i)));
   for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
   __syncthreads();
@@ -931,7 +951,8 @@ __global__ void __launch_bounds__(kXsplitThreads)
   if (b < nb) {
     uint2 code[kNC];
     uint32_t sb[kNC];
-    split_block(xr + 16 * b, sh, code, sb);
+    const uint4 v[2] = {ld8(2 * b), ld8(2 * b + 1)};
+    split_block_regs(v, sh, code, sb);
     // atom position of this block: K64 step b / 4, block b % 4
     uint8_t *atom = sfb + (b >> 2) * 512 + (b & 3);
 #pragma unroll
@@ -1157,7 +1178,8 @@ __device__ __forceinline__ void split_chunk_slot(const uint4 v, int sh, int m, i
 // sh[m].
 __global__ void __launch_bounds__(32 * kSplitWarps)
     xsplit_slots_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, uint8_t *slot_codes,
-                        uint8_t *slot_sf, int32_t *sh_out, int32_t *status) {
+                        uint8_t *slot_sf, int32_t *sh_out, int32_t *status, const uint16_t *x2,
+                        int64_t ldx2) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint4 xrow[];  // row m of X (K bf16), staged once
   __shared__ uint64_t bar;
@@ -1173,12 +1195,19 @@ __global__ void __launch_bounds__(32 * kSplitWarps)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // The row in one bulk copy: a single memory round trip, which matters
   // because the next GEMV's weight stream is already filling the memory
-  // queues when this kernel runs.
+  // queues when this kernel runs.  With x2, X = silu(x) * x2: both rows
+  // staged, then combined in place.
+  uint4 *urow = xrow + K / 8;
   if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&bar, (uint32_t)(K * 2));
+    mbar_arrive_expect_tx(&bar, (uint32_t)(K * 2) * (x2 ? 2u : 1u));
     bulk_g2s(xrow, x + m * ldx, (uint32_t)(K * 2), &bar);
+    if (x2) bulk_g2s(urow, x2 + m * ldx2, (uint32_t)(K * 2), &bar);
   }
   if (!mbar_wait_bounded(&bar, 0u, status)) return;
+  if (x2) {
+    for (int i = threadIdx.x; i < (int)(K / 8); i += 32 * kSplitWarps) xrow[i] = swiglu_bf16x8(xrow[i], urow[i]);
+    __syncthreads();
+  }
   uint32_t mx = 0;
   for (int i = threadIdx.x; i < (int)(K / 8); i += 32 * kSplitWarps) mx = max(mx, absmax_bf16x8(xrow[i]));
   for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
@@ -2061,7 +2090,7 @@ cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_
                                  const uint8_t *codes, const uint8_t *scales,
                                  const float *tensor_scale, int64_t N, uint16_t *y, int64_t ldy,
                                  int32_t *status, void *workspace, cudaStream_t stream,
-                                 bool prepared) {
+                                 bool prepared, const uint16_t *x2, int64_t ldx2) {
   const int nmma = nmma_for(M);
   const F4Ws L = f4_ws(M, N, K);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -2083,7 +2112,7 @@ cudaError_t launch_pass_streamed(const uint16_t *x, int64_t M, int64_t K, int64_
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, xsplit_kernel, x, ldx, (int)M, K, nmma,
                                              ws + L.bcodes, ws + L.sfb,
-                                             reinterpret_cast<int32_t *>(ws + L.sh));
+                                             reinterpret_cast<int32_t *>(ws + L.sh), x2, ldx2);
     if (e != cudaSuccess) return e;
   }
   const GemvGroup g = {codes, scales, tensor_scale, y, N, ldy};
@@ -2129,6 +2158,12 @@ int gemv_f4_launches(int64_t M, int64_t N, int64_t K, const char **kernel) {
   return 2;
 }
 
+int gemv_f4_swiglu_launches(int64_t M, int64_t N, int64_t K, const char **kernel) {
+  if (!gemv_f4_shape_ok(M, N, K)) return 0;
+  *kernel = plan_r(M, N, K).ok ? "gemv_f4r_kernel" : "gemv_f4_kernel";
+  return 2;  // the split kernel forms X from the two rows, then the weight stream
+}
+
 bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const void *scales) {
   return gemv_f4_shape_ok(M, N, K) && !(((uintptr_t)codes | (uintptr_t)scales) & 15u);
 }
@@ -2137,7 +2172,8 @@ bool gemv_f4_supported(int64_t M, int64_t N, int64_t K, const void *codes, const
 // kernel over the groups' tiles (plan checked by the caller).
 static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                             const GemvGroup *g, int n, int32_t *status, void *workspace,
-                            cudaStream_t stream, bool prepared) {
+                            cudaStream_t stream, bool prepared, const uint16_t *x2 = nullptr,
+                            int64_t ldx2 = 0) {
   const int64_t rows = group_tiles(g, n) * kTileRows;
   const F4Plan P = plan_r(M, rows, K);
   const F4Ws L = f4_ws(M, rows, K);
@@ -2149,11 +2185,13 @@ static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int6
   a.sched = P.sched;
   a.ksplit = P.ksplit;
   a.slot_codes = ws + L.bcodes;
-  if (!P.split_inside) {
+  // an X made from two rows (x2) is split by the split kernel only
+  const bool inside = P.split_inside && !x2;
+  if (!inside) {
     // X -> B slot images by the split kernel (programmatic dependent launch:
     // it may start while the previous kernel drains and waits before reading
     // X or writing the workspace); each CTA then copies its slots in
-    const size_t xs_bytes = (size_t)K * 2;  // the staged row
+    const size_t xs_bytes = (size_t)K * 2 * (x2 ? 2 : 1);  // the staged row(s)
     if (xs_bytes > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(
           xsplit_slots_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xs_bytes);
@@ -2171,11 +2209,12 @@ static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int6
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, xsplit_slots_kernel, x, ldx, (int)M, K,
                                              ws + L.bcodes, ws + L.sfb,
-                                             reinterpret_cast<int32_t *>(ws + L.sh), status);
+                                             reinterpret_cast<int32_t *>(ws + L.sh), status, x2,
+                                             ldx2);
     if (e != cudaSuccess) return e;
   }
   const int cluster = P.sched == kSchedCluster ? P.ksplit : 1;
-  if (P.split_inside)
+  if (inside)
     return prepared ? launch_pdl(gemv_f4r_kernel<true, kFmtNv, true>, P.grid, kThreads, P.smem,
                                  stream, cluster, mw, ms, a)
                     : launch_pdl(gemv_f4r_kernel<false, kFmtNv, true>, P.grid, kThreads, P.smem,
@@ -2189,14 +2228,15 @@ static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int6
 cudaError_t launch_gemv_f4(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
                            const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
                            int64_t N, uint16_t *y, int64_t ldy, int32_t *status, void *workspace,
-                           cudaStream_t stream, bool prepared) {
+                           cudaStream_t stream, bool prepared, const uint16_t *x2,
+                           int64_t ldx2) {
   if (plan_r(M, N, K).ok) {
     const GemvGroup g = {codes, scales, tensor_scale, y, N, ldy};
-    return launch_resident(x, M, K, ldx, &g, 1, status, workspace, stream, prepared);
+    return launch_resident(x, M, K, ldx, &g, 1, status, workspace, stream, prepared, x2, ldx2);
   }
   // every row of X in one stream of W
   return launch_pass_streamed(x, M, K, ldx, codes, scales, tensor_scale, N, y, ldy, status,
-                              workspace, stream, prepared);
+                              workspace, stream, prepared, x2, ldx2);
 }
 
 // ---- FP8-E4M3 weights ------------------------------------------------------------

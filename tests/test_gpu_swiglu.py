@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from _gpu import check_within_tolerance, dev_bf16, sample_rows
+from _gpu import check_within_tolerance, dev_bf16, dev_nvfp4, sample_rows
 
 pkg = pytest.importorskip("nvfp4_weight_quantized_02_gb300")
 pytestmark = pytest.mark.gpu
@@ -94,3 +94,95 @@ def test_swiglu_repeatable_and_rejects_decode_sizes():
     w = pkg.prepare_mma(pkg.quantize(dev_bf16(lg.weight_bf16())))
     with pytest.raises(pkg.ImpError):
         pkg.gemm_swiglu(dev_bf16(synth.Linear("d", 16, 1024, 512, 1).act_bf16()), w, w)
+
+
+# ---- decode: the down projection with the activation formed in its X split --------
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def swiglu_decode_reference(gb, ub, codes, scales, ts, M):
+    """y = bf16(silu(g) * u) W^T from the oracle, and the extra tolerance for
+    elements of h whose fp64 value sits within the kernel's fp32 evaluation
+    error of a bf16 rounding boundary (there the kernel may round to the
+    neighbouring bf16: one ulp of h times |w|)."""
+    g, u = oracle.bf16_to_f64(gb), oracle.bf16_to_f64(ub)
+    h = oracle.silu(g) * u
+    hb = _bits(torch.from_numpy(h).to(torch.float32).to(torch.bfloat16))
+    hq = oracle.bf16_to_f64(hb)
+    e = np.floor(np.log2(np.maximum(np.abs(h), 1e-300)))
+    ulp = np.exp2(e - 7)
+    mid = np.abs(np.abs(h) - (np.abs(hq) + 0.5 * ulp * np.sign(np.abs(h) - np.abs(hq))))
+    near = (mid <= 2.0 ** -16 * np.abs(h)) | (np.abs(h) < 2.0 ** -120)
+    y_ref, bound = oracle.reference_gemm(hb, M, codes, scales, ts)
+    wd = np.abs(oracle.dequant(codes, scales, ts))
+    extra = (near * ulp) @ wd.T
+    return y_ref, bound, extra
+
+
+def check_decode_swiglu(y, y_ref, bound, extra, what):
+    err = np.abs(y.astype(np.float64) - y_ref)
+    tol = oracle.tight_tolerance(bound, y_ref) + extra
+    bad = np.argwhere(~(err <= tol))
+    assert bad.size == 0, (f"{what}: {len(bad)} outside, first {bad[:4].tolist()}, "
+                           f"err {err[tuple(bad[0])]:.3e} tol {tol[tuple(bad[0])]:.3e}")
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1024, 256), (2, 3072, 1000), (4, 1024, 384),
+                                   (16, 2048, 130), (1, 5120, 152 * 128 + 40)])
+def test_decode_swiglu_every_element(M, K, N):
+    lg = synth.Linear("dg", M, K, 1, 61, x_outlier_frac=0.01)
+    lu = synth.Linear("du", M, K, 1, 62)
+    ld = synth.Linear("dd", M, K, N, 63, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
+                      zero_block_p=0.01)
+    gb, ub = lg.act_bf16(), lu.act_bf16()
+    c, s, ts, _ = oracle.quantize(ld.weight_bf16())
+    w = pkg.prepare_mma(dev_nvfp4(c, s, ts))
+    assert pkg.imp_nvfp4_gemm_mma_swiglu_plan(M, N, K)[0] == 2
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = pkg.gemm_mma_swiglu(dev_bf16(gb), dev_bf16(ub), w, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    y_ref, bound, extra = swiglu_decode_reference(gb, ub, c, s, ts, M)
+    check_decode_swiglu(y.float().cpu().numpy(), y_ref, bound, extra, f"decode swiglu {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_decode_mlp_27b_sampled(M):
+    """A 27B-class decode MLP: gate and up in one grouped call, then the down
+    projection on silu(gate) * up; each output against the oracle on the
+    inputs it read."""
+    L = {l.name: l for l in synth.workload("decode_27b")}
+    ws = {}
+    for n in ("gate", "up", "down"):
+        wb = L[n].weight_bf16()
+        ws[n] = (wb, oracle.tensor_scale(wb)[1], pkg.prepare_mma(pkg.quantize(dev_bf16(wb))))
+    x = np.concatenate([L["up"].act_bf16()] + [synth.Linear(f"r{i}", 1, 5120, 1, 70 + i).act_bf16()
+                                               for i in range(M - 1)])
+    g, u = pkg.gemm_grouped(dev_bf16(x), [ws["gate"][2], ws["up"][2]])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = pkg.gemm_mma_swiglu(g, u, ws["down"][2], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for t, n in ((g, "gate"), (u, "up")):
+        rows = sample_rows(L[n].N, seed=M + len(n))
+        wb, s_w, _ = ws[n]
+        c, s = oracle.quantize_rows(wb[rows], s_w)
+        y_ref, bound = oracle.reference_gemm(x, M, c, s, s_w)
+        check_within_tolerance(t.float().cpu().numpy()[:, rows], y_ref, bound, f"27b {n}")
+    rows = sample_rows(L["down"].N, seed=M + 9)
+    wb, s_w, _ = ws["down"]
+    c, s = oracle.quantize_rows(wb[rows], s_w)
+    y_ref, bound, extra = swiglu_decode_reference(_bits(g), _bits(u), c, s, s_w, M)
+    check_decode_swiglu(y.float().cpu().numpy()[:, rows], y_ref, bound, extra, "27b down(swiglu)")
+
+
+def test_decode_swiglu_rejects():
+    ld = synth.Linear("rj", 1, 1024, 256, 1)
+    c, s, ts, _ = oracle.quantize(ld.weight_bf16())
+    w = pkg.prepare_mma(dev_nvfp4(c, s, ts))
+    g = dev_bf16(ld.act_bf16())
+    with pytest.raises(pkg.ImpError):  # more rows than the decode path holds
+        pkg.gemm_mma_swiglu(torch.cat([g] * 17), torch.cat([g] * 17), w)
+    assert pkg.imp_nvfp4_gemm_mma_swiglu_plan(1, 256, 512) == (0, None)  # K below 1024
