@@ -339,6 +339,9 @@ typedef struct {
   const void *x_bf16;            /* device bf16[M][ldx]; NULL: X is the previous link's
                                     groups[0] output (its K must equal that weight's rows) */
   int64_t ldx;                   /* ignored when x_bf16 is NULL */
+  int32_t x_swiglu;              /* with x_bf16 NULL: 1 takes X = bf16(silu(g) * u), g and u
+                                    the previous link's groups[0] and groups[1] outputs (the
+                                    activation of imp_nvfp4_gemm_mma_swiglu); 0 takes g */
 } imp_nvfp4_chain_link;
 
 /* Bytes of workspace imp_nvfp4_gemm_chain needs (on the current device;
@@ -352,7 +355,9 @@ int32_t imp_nvfp4_gemm_chain_plan(int64_t M, const imp_nvfp4_chain_link *links, 
 
 /* For each link c in order (1 <= n_links <= IMP_NVFP4_MAX_CHAIN):
  * Y_cg = X_c * W_cg^T for its groups g, with X_c = links[c].x_bf16 or, if
- * that is NULL (c >= 1), the output of links[c-1].groups[0].
+ * that is NULL (c >= 1), the output of links[c-1].groups[0] -- or, with
+ * x_swiglu, bf16(silu(that output) * the output of links[c-1].groups[1])
+ * (a layer's down projection after its grouped gate and up).
  *   M             M >= 0 (M = 0: nothing to do).
  *   links         host array; weights, outputs and strides as for
  *                 imp_nvfp4_gemm_grouped.  No output may overlap another

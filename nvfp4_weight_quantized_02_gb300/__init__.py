@@ -67,7 +67,7 @@ class ImpNvfp4Group(ctypes.Structure):
 class ImpNvfp4ChainLink(ctypes.Structure):
     """ctypes mirror of imp_nvfp4_chain_link."""
     _fields_ = [("groups", ctypes.POINTER(ImpNvfp4Group)), ("n_groups", ctypes.c_int32),
-                ("x_bf16", ctypes.c_void_p), ("ldx", ctypes.c_int64)]
+                ("x_bf16", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("x_swiglu", ctypes.c_int32)]
 
 
 class ImpMxfp4Tensor(ctypes.Structure):
@@ -313,15 +313,17 @@ def imp_nvfp4_gemm_grouped(x_bf16: int, M: int, K: int, ldx: int, groups: list[I
 
 
 class ChainLinks:
-    """A host array of imp_nvfp4_chain_link built from (groups, x_bf16, ldx)
-    triples (x_bf16 None: the previous link's first output); keeps the
-    groups' arrays alive for as long as it lives."""
+    """A host array of imp_nvfp4_chain_link built from (groups, x_bf16, ldx
+    [, x_swiglu]) tuples (x_bf16 None: the previous link's first output, or
+    with x_swiglu the activation of its first two); keeps the groups' arrays
+    alive for as long as it lives."""
 
     def __init__(self, links: list):
-        self._groups = [(ImpNvfp4Group * len(g))(*g) for g, _, _ in links]
+        links = [tuple(l) + (0,) * (4 - len(l)) for l in links]
+        self._groups = [(ImpNvfp4Group * len(l[0]))(*l[0]) for l in links]
         self.array = (ImpNvfp4ChainLink * len(links))(*[
-            ImpNvfp4ChainLink(ctypes.cast(ga, ctypes.POINTER(ImpNvfp4Group)), len(g), x, ldx)
-            for ga, (g, x, ldx) in zip(self._groups, links)])
+            ImpNvfp4ChainLink(ctypes.cast(ga, ctypes.POINTER(ImpNvfp4Group)), len(g), x, ldx, sw)
+            for ga, (g, x, ldx, sw) in zip(self._groups, links)])
         self.n = len(links)
 
 
@@ -621,8 +623,9 @@ def gemm_grouped(x, ws: list, ys=None, dev_status=None, stream=None, workspace=N
 
 def gemm_chain(links: list, ys=None, dev_status=None, stream=None, workspace=None):
     """A decode chain in one call: links = [(weights, x), ...] with weights a
-    list of MMA-layout tensors of one K and x a bf16 [M][K] tensor, or None
-    for the previous link's first output.  Returns the outputs, one list per
+    list of MMA-layout tensors of one K and x a bf16 [M][K] tensor, None for
+    the previous link's first output, or "swiglu" for silu(g) * u of the
+    previous link's first two outputs.  Returns the outputs, one list per
     link (allocated with row strides rounded up to 8 unless given)."""
     import torch
     x0 = links[0][1]
@@ -635,8 +638,9 @@ def gemm_chain(links: list, ys=None, dev_status=None, stream=None, workspace=Non
     for (ws, x), yl in zip(links, ys):
         assert all(w.layout == "mma" for w in ws)
         groups = [ImpNvfp4Group(w.c_struct(), y.data_ptr(), y.stride(0)) for w, y in zip(ws, yl)]
-        if x is None:
-            spec.append((groups, None, 0))
+        if x is None or isinstance(x, str):
+            assert x in (None, "swiglu")
+            spec.append((groups, None, 0, 1 if x == "swiglu" else 0))
         else:
             assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
             spec.append((groups, x.data_ptr(), x.stride(0)))

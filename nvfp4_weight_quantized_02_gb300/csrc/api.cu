@@ -519,16 +519,25 @@ imp_status resolve_chain(int64_t M, const imp_nvfp4_chain_link *links, int32_t n
     }
     const uint16_t *x = static_cast<const uint16_t *>(L.x_bf16);
     int64_t ldx = L.ldx;
+    const uint16_t *x2 = nullptr;
+    int64_t ldx2 = 0;
     const bool dep = x == nullptr;
+    if (L.x_swiglu && !dep) return IMP_ERR_INVALID_ARG;
     if (dep) {
       if (c == 0 || K != links[c - 1].groups[0].w.rows) return IMP_ERR_INVALID_ARG;
       x = static_cast<const uint16_t *>(links[c - 1].groups[0].y_bf16);
       ldx = links[c - 1].groups[0].ldy;
+      if (L.x_swiglu) {  // X = silu(previous groups[0] output) * previous groups[1] output
+        if (links[c - 1].n_groups < 2 || links[c - 1].groups[1].w.rows != K)
+          return IMP_ERR_INVALID_ARG;
+        x2 = static_cast<const uint16_t *>(links[c - 1].groups[1].y_bf16);
+        ldx2 = links[c - 1].groups[1].ldy;
+      }
     } else if (!sizes_only && M > 0) {
       if (ldx < K) return IMP_ERR_INVALID_ARG;
       if (!aligned16(x) || ldx % 8) return IMP_ERR_MISALIGNED;
     }
-    r.l[c] = impfp4::ChainLink{r.g[c], L.n_groups, x, ldx, K, dep};
+    r.l[c] = impfp4::ChainLink{r.g[c], L.n_groups, x, ldx, K, dep, x2, ldx2};
   }
   if (sizes_only || M == 0) return IMP_OK;
   // links run concurrently on different SMs: no output may overlap another
@@ -590,14 +599,30 @@ imp_status imp_nvfp4_gemm_chain(int64_t M, const imp_nvfp4_chain_link *links, in
   if (impfp4::gemv_f4_chain_ok(M, r.l, n_links))
     return from_cuda(impfp4::launch_gemv_f4_chain(M, r.l, n_links, dev_status, workspace,
                                                   static_cast<cudaStream_t>(stream)));
-  // one grouped call per link, in order (every link checked before any runs)
-  for (int c = 0; c < n_links; ++c)
-    if (imp_nvfp4_gemm_grouped_plan(M, r.l[c].K, r.N[c], links[c].n_groups, nullptr) == 0)
-      return IMP_ERR_UNSUPPORTED_SHAPE;
+  // one grouped call per link, in order (every link checked before any
+  // runs); a link on silu(g) * u runs its groups one by one
   for (int c = 0; c < n_links; ++c) {
-    const imp_status s = imp_nvfp4_gemm_grouped(r.l[c].x, M, r.l[c].K, r.l[c].ldx, links[c].groups,
-                                                links[c].n_groups, dev_status, workspace, ws_bytes,
-                                                stream);
+    if (r.l[c].x2) {
+      if (r.l[c].ldx2 != r.l[c].ldx) return IMP_ERR_UNSUPPORTED_SHAPE;
+      for (int i = 0; i < links[c].n_groups; ++i)
+        if (imp_nvfp4_gemm_mma_swiglu_plan(M, r.N[c][i], r.l[c].K, nullptr) == 0)
+          return IMP_ERR_UNSUPPORTED_SHAPE;
+    } else if (imp_nvfp4_gemm_grouped_plan(M, r.l[c].K, r.N[c], links[c].n_groups, nullptr) == 0) {
+      return IMP_ERR_UNSUPPORTED_SHAPE;
+    }
+  }
+  for (int c = 0; c < n_links; ++c) {
+    imp_status s = IMP_OK;
+    if (r.l[c].x2) {
+      for (int i = 0; i < links[c].n_groups && s == IMP_OK; ++i)
+        s = imp_nvfp4_gemm_mma_swiglu(r.l[c].x, r.l[c].x2, M, r.l[c].K, r.l[c].ldx,
+                                      &links[c].groups[i].w, links[c].groups[i].y_bf16,
+                                      links[c].groups[i].ldy, dev_status, workspace, ws_bytes,
+                                      stream);
+    } else {
+      s = imp_nvfp4_gemm_grouped(r.l[c].x, M, r.l[c].K, r.l[c].ldx, links[c].groups,
+                                 links[c].n_groups, dev_status, workspace, ws_bytes, stream);
+    }
     if (s != IMP_OK) return s;
   }
   return IMP_OK;

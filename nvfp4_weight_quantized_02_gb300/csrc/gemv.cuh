@@ -81,6 +81,8 @@ struct ChainLink {
   const uint16_t *x;
   int64_t ldx, K;
   bool dep;
+  const uint16_t *x2 = nullptr;  // X = bf16(silu(x) * x2) when set (dep links)
+  int64_t ldx2 = 0;
 };
 bool gemv_f4_chain_ok(int64_t M, const ChainLink *l, int n);
 size_t gemv_f4_chain_workspace_bytes(int64_t M, const ChainLink *l, int n);

@@ -190,6 +190,8 @@ struct F4Args {
   int grid;             // CTAs the call is spread over (0: the whole grid)
   unsigned int *cnt32;  // per tile: segments finished, cleared before the launch counts
                         // (a persistent launch's own protocol); nullptr: cnt
+  const uint16_t *x2;   // chained calls: X = bf16(silu(x) * x2) when set
+  int64_t ldx2;
   int n_groups;         // weights of the call (row-major weight: 1)
   F4Group grp[kMaxGroups];
 };
@@ -1636,8 +1638,11 @@ __device__ __forceinline__ void chain_split(const F4Args &a, int ch0, int nch, i
       for (int m = 0; m < 2; ++m)
         if (m < a.M) {
           // L2 only: X may have been written by other SMs in this launch
-          v[r][m] = __ldcg(reinterpret_cast<const uint4 *>(a.x + m * a.ldx +
-                                                          (int64_t)chn * kChunkK + 16 * bb + 8 * hf));
+          const int64_t e = (int64_t)chn * kChunkK + 16 * bb + 8 * hf;
+          v[r][m] = __ldcg(reinterpret_cast<const uint4 *>(a.x + m * a.ldx + e));
+          if (a.x2)  // X = silu(x) * x2 (a down projection after gate and up)
+            v[r][m] = swiglu_bf16x8(v[r][m],
+                                    __ldcg(reinterpret_cast<const uint4 *>(a.x2 + m * a.ldx2 + e)));
           mx[m] = max(mx[m], absmax_bf16x8(v[r][m]));
         }
     }
@@ -2424,6 +2429,8 @@ cudaError_t launch_gemv_f4_chain(int64_t M, const ChainLink *l, int n, int32_t *
     F4Args &a = ch.call[c];
     a.x = l[c].x;
     a.ldx = l[c].ldx;
+    a.x2 = l[c].x2;
+    a.ldx2 = l[c].ldx2;
     a.M = (int)M;
     a.K = l[c].K;
     a.status = status;
@@ -2450,7 +2457,7 @@ cudaError_t launch_gemv_f4_chain(int64_t M, const ChainLink *l, int n, int32_t *
     // CTA (whole tiles: all of them), and not two such calls in a row (the
     // slot barriers' phases may run at most one call ahead of the issuers)
     ch.reuse[c] = c > 0 && !l[c].dep && !ch.reuse[c - 1] && l[c].x == l[c - 1].x &&
-                  l[c].ldx == l[c - 1].ldx && l[c].K == l[c - 1].K &&
+                  l[c].ldx == l[c - 1].ldx && l[c].K == l[c - 1].K && !l[c].x2 && !l[c - 1].x2 &&
                   P.sched[c] == kSchedWhole && P.sched[c - 1] == kSchedWhole;
   }
   cudaError_t e = cudaFuncSetAttribute(gemv_f4c_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

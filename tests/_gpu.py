@@ -55,3 +55,34 @@ def check_within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarr
     assert bad.size == 0, (f"{what}: {len(bad)} elements outside tolerance, first {bad[:4].tolist()}, "
                            f"err {err[tuple(bad[0])]:.3e} tol {tol[tuple(bad[0])]:.3e}")
     return float((err / tol).max()) if err.size else 0.0
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def swiglu_decode_reference(gb, ub, codes, scales, ts, M):
+    """y = bf16(silu(g) * u) W^T from the oracle, and the extra tolerance for
+    elements of h whose fp64 value sits within the kernel's fp32 evaluation
+    error of a bf16 rounding boundary (there the kernel may round to the
+    neighbouring bf16: one ulp of h times |w|)."""
+    g, u = oracle.bf16_to_f64(gb), oracle.bf16_to_f64(ub)
+    h = oracle.silu(g) * u
+    hb = _bits(torch.from_numpy(h).to(torch.float32).to(torch.bfloat16))
+    hq = oracle.bf16_to_f64(hb)
+    e = np.floor(np.log2(np.maximum(np.abs(h), 1e-300)))
+    ulp = np.exp2(e - 7)
+    mid = np.abs(np.abs(h) - (np.abs(hq) + 0.5 * ulp * np.sign(np.abs(h) - np.abs(hq))))
+    near = (mid <= 2.0 ** -16 * np.abs(h)) | (np.abs(h) < 2.0 ** -120)
+    y_ref, bound = oracle.reference_gemm(hb, M, codes, scales, ts)
+    wd = np.abs(oracle.dequant(codes, scales, ts))
+    extra = (near * ulp) @ wd.T
+    return y_ref, bound, extra
+
+
+def check_decode_swiglu(y, y_ref, bound, extra, what):
+    err = np.abs(y.astype(np.float64) - y_ref)
+    tol = oracle.tight_tolerance(bound, y_ref) + extra
+    bad = np.argwhere(~(err <= tol))
+    assert bad.size == 0, (f"{what}: {len(bad)} outside, first {bad[:4].tolist()}, "
+                           f"err {err[tuple(bad[0])]:.3e} tol {tol[tuple(bad[0])]:.3e}")

@@ -12,7 +12,8 @@ import torch
 
 import oracle
 import synth
-from _gpu import check_within_tolerance, dev_bf16, dev_nvfp4, num_sms, sample_rows
+from _gpu import (_bits, check_decode_swiglu, check_within_tolerance, dev_bf16, dev_nvfp4,
+                  num_sms, sample_rows, swiglu_decode_reference)
 
 pkg = pytest.importorskip("nvfp4_weight_quantized_02_gb300")
 pytestmark = pytest.mark.gpu
@@ -204,3 +205,28 @@ def test_chain_back_to_back_launches(case):
     for ya, yb in zip(ref, ys):
         for u, v in zip(ya, yb):
             assert torch.equal(u.view(torch.int16), v.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_chain_decode_mlp_swiglu(M):
+    """A decode MLP as one chain: gate and up grouped on x, down on
+    silu(gate) * up (x_swiglu), then a projection of down's output.  M = 4
+    runs the links one call after another (the same results are required)."""
+    K, F = 1024, 2048
+    lg, lu = lin("mg", M, K, F, 81), lin("mu", M, K, F, 82)
+    ld, lo = lin("md", M, F, K, 83), lin("mo", M, K, 300, 84)
+    (rg, dg), (ru, du), (rd, dd), (ro, do) = (prepared(l) for l in (lg, lu, ld, lo))
+    x = lg.act_bf16()
+    links = [([dg, du], dev_bf16(x)), ([dd], "swiglu"), ([do], None)]
+    cl = pkg.ChainLinks([([pkg.ImpNvfp4Group(w.c_struct(), 0, 0) for w in ws],
+                          None if isinstance(xx, str) or xx is None else 16, 0,
+                          1 if xx == "swiglu" else 0) for ws, xx in links])
+    assert pkg.imp_nvfp4_gemm_chain_plan(M, cl) == (1 if M <= 2 else 0)
+    ys = run_chain(links)
+    for y, r in zip(ys[0], (rg, ru)):
+        y_ref, bound = oracle.reference_gemm(x, M, *r)
+        check_within_tolerance(y.float().cpu().numpy(), y_ref, bound, "gate/up")
+    y_ref, bound, extra = swiglu_decode_reference(_bits(ys[0][0]), _bits(ys[0][1]), *rd, M)
+    check_decode_swiglu(ys[1][0].float().cpu().numpy(), y_ref, bound, extra, "down on silu(g) u")
+    y_ref, bound = oracle.reference_gemm(_bits(ys[1][0]), M, *ro)
+    check_within_tolerance(ys[2][0].float().cpu().numpy(), y_ref, bound, "after down")

@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import synth
-from _gpu import check_within_tolerance, dev_bf16, dev_nvfp4, sample_rows
+from _gpu import (_bits, check_decode_swiglu, check_within_tolerance, dev_bf16, dev_nvfp4,
+                  sample_rows, swiglu_decode_reference)
 
 pkg = pytest.importorskip("nvfp4_weight_quantized_02_gb300")
 pytestmark = pytest.mark.gpu
@@ -97,37 +98,6 @@ def test_swiglu_repeatable_and_rejects_decode_sizes():
 
 
 # ---- decode: the down projection with the activation formed in its X split --------
-
-def _bits(t):
-    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-
-
-def swiglu_decode_reference(gb, ub, codes, scales, ts, M):
-    """y = bf16(silu(g) * u) W^T from the oracle, and the extra tolerance for
-    elements of h whose fp64 value sits within the kernel's fp32 evaluation
-    error of a bf16 rounding boundary (there the kernel may round to the
-    neighbouring bf16: one ulp of h times |w|)."""
-    g, u = oracle.bf16_to_f64(gb), oracle.bf16_to_f64(ub)
-    h = oracle.silu(g) * u
-    hb = _bits(torch.from_numpy(h).to(torch.float32).to(torch.bfloat16))
-    hq = oracle.bf16_to_f64(hb)
-    e = np.floor(np.log2(np.maximum(np.abs(h), 1e-300)))
-    ulp = np.exp2(e - 7)
-    mid = np.abs(np.abs(h) - (np.abs(hq) + 0.5 * ulp * np.sign(np.abs(h) - np.abs(hq))))
-    near = (mid <= 2.0 ** -16 * np.abs(h)) | (np.abs(h) < 2.0 ** -120)
-    y_ref, bound = oracle.reference_gemm(hb, M, codes, scales, ts)
-    wd = np.abs(oracle.dequant(codes, scales, ts))
-    extra = (near * ulp) @ wd.T
-    return y_ref, bound, extra
-
-
-def check_decode_swiglu(y, y_ref, bound, extra, what):
-    err = np.abs(y.astype(np.float64) - y_ref)
-    tol = oracle.tight_tolerance(bound, y_ref) + extra
-    bad = np.argwhere(~(err <= tol))
-    assert bad.size == 0, (f"{what}: {len(bad)} outside, first {bad[:4].tolist()}, "
-                           f"err {err[tuple(bad[0])]:.3e} tol {tol[tuple(bad[0])]:.3e}")
-
 
 @pytest.mark.parametrize("M,K,N", [(1, 1024, 256), (2, 3072, 1000), (4, 1024, 384),
                                    (16, 2048, 130), (1, 5120, 152 * 128 + 40)])
