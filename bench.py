@@ -1015,6 +1015,32 @@ def bench_extras(args, pkg, dev, stream, hbm_peak, lins, rows_w, weights, xs, ch
             out["decode_swiglu_mlp"] = dict(
                 rate(time_blocks(swiglu_step, n, 10, stream)),
                 dataflow="gate and up grouped on x; down on silu(gate) * up; LM head on down")
+            # the same as one decode-chain launch (x_swiglu link)
+            if "lm_head" in by and rest == [by["lm_head"]]:
+                il = by["lm_head"]
+                g2 = [pkg.ImpNvfp4Group(weights[j].c_struct(), ys[j].data_ptr(), ys[j].stride(0))
+                      for j in (ig, iu)]
+                cl = pkg.ChainLinks([
+                    (g2, chained[iu].data_ptr(), chained[iu].stride(0)),
+                    ([pkg.ImpNvfp4Group(weights[idn].c_struct(), ys[idn].data_ptr(),
+                                        ys[idn].stride(0))], None, 0, 1),
+                    ([pkg.ImpNvfp4Group(weights[il].c_struct(), ys[il].data_ptr(),
+                                        ys[il].stride(0))], None, 0)])
+                cws = torch.empty(pkg.imp_nvfp4_gemm_chain_workspace_size(1, cl),
+                                  dtype=torch.uint8, device=dev)
+                sh = pkg._stream_handle(stream)
+
+                def swiglu_chain():
+                    st = pkg.imp_nvfp4_gemm_chain(1, cl, status.data_ptr(), cws.data_ptr(),
+                                                  cws.numel(), sh)
+                    if st != pkg.IMP_OK:
+                        raise pkg.ImpError(st, "imp_nvfp4_gemm_chain")
+                for _ in range(args.warmup):
+                    swiglu_chain()
+                out["decode_swiglu_mlp_chain"] = dict(
+                    rate(time_blocks(swiglu_chain, n, 10, stream)), launches_per_step=1,
+                    persistent_launch=pkg.imp_nvfp4_gemm_chain_plan(1, cl) == 1)
+                del cws
         del gws
 
     # the step as one decode chain (imp_nvfp4_gemm_chain: one persistent
