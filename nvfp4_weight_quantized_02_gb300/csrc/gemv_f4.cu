@@ -1178,15 +1178,16 @@ __device__ __forceinline__ void split_chunk_slot(const uint4 v, int sh, int m, i
 // elements 8 h .. 8 h + 7 of the chunk's block b.  Writes the images' rows
 // 8 m .. 8 m + 7 (and, for the last row of X, zeros in the rows after it) and
 // sh[m].
-__global__ void __launch_bounds__(32 * kSplitWarps)
+__global__ void __launch_bounds__(128 * kSplitWarps)
     xsplit_slots_kernel(const uint16_t *x, int64_t ldx, int M, int64_t K, uint8_t *slot_codes,
                         uint8_t *slot_sf, int32_t *sh_out, int32_t *status, const uint16_t *x2,
                         int64_t ldx2) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint4 xrow[];  // row m of X (K bf16), staged once
   __shared__ uint64_t bar;
-  __shared__ uint32_t red[kSplitWarps];
+  __shared__ uint32_t red[32];
   const int m = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = blockDim.x;  // 32 kSplitWarps, or 4x that to form silu(x) * x2 sooner
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
@@ -1198,7 +1199,8 @@ __global__ void __launch_bounds__(32 * kSplitWarps)
   // The row in one bulk copy: a single memory round trip, which matters
   // because the next GEMV's weight stream is already filling the memory
   // queues when this kernel runs.  With x2, X = silu(x) * x2: both rows
-  // staged, then combined in place.
+  // staged, then combined in place by all the CTA's threads (every CTA
+  // forms the whole row: its max sets the prescale).
   uint4 *urow = xrow + K / 8;
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&bar, (uint32_t)(K * 2) * (x2 ? 2u : 1u));
@@ -1207,21 +1209,21 @@ __global__ void __launch_bounds__(32 * kSplitWarps)
   }
   if (!mbar_wait_bounded(&bar, 0u, status)) return;
   if (x2) {
-    for (int i = threadIdx.x; i < (int)(K / 8); i += 32 * kSplitWarps) xrow[i] = swiglu_bf16x8(xrow[i], urow[i]);
+    for (int i = threadIdx.x; i < (int)(K / 8); i += nt) xrow[i] = swiglu_bf16x8(xrow[i], urow[i]);
     __syncthreads();
   }
   uint32_t mx = 0;
-  for (int i = threadIdx.x; i < (int)(K / 8); i += 32 * kSplitWarps) mx = max(mx, absmax_bf16x8(xrow[i]));
+  for (int i = threadIdx.x; i < (int)(K / 8); i += nt) mx = max(mx, absmax_bf16x8(xrow[i]));
   for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   if (lane == 0) red[warp] = mx;
   __syncthreads();
   mx = 0;
-  for (int w = 0; w < kSplitWarps; ++w) mx = max(mx, red[w]);
+  for (int w = 0; w < nt / 32; ++w) mx = max(mx, red[w]);
   const int sh = prescale_exponent(mx);
   if (blockIdx.x == 0 && threadIdx.x == 0) sh_out[m] = sh;
 
   const int ch = blockIdx.x * kSplitWarps + warp;
-  if (ch >= (int)(K / kChunkK)) return;
+  if (warp >= kSplitWarps || ch >= (int)(K / kChunkK)) return;
   const int bb = lane >> 1, hf = lane & 1;
   split_chunk_slot(xrow[(ch * kChunkK + 16 * bb + 8 * hf) / 8], sh, m, M,
                    slot_codes + (size_t)ch * 2048, slot_sf + (size_t)ch * 1024, lane);
@@ -2204,7 +2206,7 @@ static cudaError_t launch_resident(const uint16_t *x, int64_t M, int64_t K, int6
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ceil_div(K / kChunkK, kSplitWarps), (unsigned)M);
-    cfg.blockDim = dim3(32 * kSplitWarps);
+    cfg.blockDim = dim3(32 * kSplitWarps * (x2 ? 4 : 1));
     cfg.dynamicSmemBytes = xs_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
