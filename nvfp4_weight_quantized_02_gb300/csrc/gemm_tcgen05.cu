@@ -209,6 +209,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// 32 bf16 (16 packed pairs, low half first) to Y[m][n .. n + 31] (columns
+// >= N and rows >= M are not written).
+__device__ __forceinline__ void store_packed_bf16(const GemmArgs &a, int64_t m, int n,
+                                                  const uint32_t (&p)[16]) {
+  if (m >= a.M) return;
+  uint16_t *dst = a.y + m * a.ldy + n;
+  if (n + 32 <= a.N) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (n + 2 * i < a.N) dst[2 * i] = (uint16_t)(p[i] & 0xFFFFu);
+      if (n + 2 * i + 1 < a.N) dst[2 * i + 1] = (uint16_t)(p[i] >> 16);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
@@ -466,27 +485,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n0 = nb * (BN / 2) + h0;
         uint32_t hmax = 0;
         bool finite = true;
-#pragma unroll 1
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t rg[32], ru[32];
-          tc_ld32(tq + h0 + c, rg);
-          tc_ld32(tq + BN / 2 + h0 + c, ru);
-          float v[32];
+        // h of both 32-column chunks as bf16 in registers; the accumulator
+        // is handed back once the second chunk is read, before the stores
+        uint32_t hp[2][16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float g = __uint_as_float(rg[i]) * sg, u = __uint_as_float(ru[i]) * su;
-            v[i] = g / (1.0f + expf(-g)) * u;  // silu(g) * u
-            const uint32_t hb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[i])) & 0x7FFFu;
-            const bool in = m < a.M && n0 + c + i < a.N;
-            if (in) {
-              hmax = max(hmax, hb < 0x7F80u ? hb : 0u);
-              finite = finite && hb < 0x7F80u;
+        for (int h = 0; h < 2; ++h) {
+          uint32_t rg[32], ru[32];
+          tc_ld32(tq + h0 + 32 * h, rg);
+          tc_ld32(tq + BN / 2 + h0 + 32 * h, ru);
+          if (h == 1) {
+            tc_fence_before();
+            mbar_arrive(acce);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float g0 = __uint_as_float(rg[i]) * sg, u0 = __uint_as_float(ru[i]) * su;
+            const float g1 = __uint_as_float(rg[i + 1]) * sg, u1 = __uint_as_float(ru[i + 1]) * su;
+            hp[h][i / 2] = pack_bf16(g0 / (1.0f + expf(-g0)) * u0,   // silu(g) * u
+                                     g1 / (1.0f + expf(-g1)) * u1);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint32_t hb = (e ? hp[h][i / 2] >> 16 : hp[h][i / 2]) & 0x7FFFu;
+              if (m < a.M && n0 + 32 * h + i + e < a.N) {
+                hmax = max(hmax, hb < 0x7F80u ? hb : 0u);
+                finite = finite && hb < 0x7F80u;
+              }
             }
           }
-          store_bf16(m, n0, c, v, 1.0f);
         }
-        tc_fence_before();
-        mbar_arrive(acce);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) store_packed_bf16(a, m, n0 + 32 * h, hp[h]);
         for (int o = 16; o; o >>= 1) hmax = max(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, o));
         if (!__all_sync(0xFFFFFFFFu, finite) && lane == 0) report(a.status, IMP_DEV_NONFINITE_INPUT);
         if (lane == 0 && hmax) atomicMax(a.h_amax, hmax);
@@ -495,20 +523,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = nb * BN + col0;
       const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_D + col0;
       if (k0 == 0 && k1 == n_ks) {
-        // Whole tile: drain this warp's 128 accumulator columns 32 at a time,
-        // storing each chunk as bf16 straight away (stores do not wait), then
-        // hand the accumulator back: the stores drain under the next MMAs.
+        // Whole tile: this warp's 128 accumulator columns as bf16 in
+        // registers, the accumulator handed back, then the stores (rows of
+        // 64 bytes, one per lane: they take longer than the reads and now
+        // run under the next tile's MMAs).
+        uint32_t pk[kEpiCols / 32][16];
 #pragma unroll
-        for (int c = 0; c < kEpiCols; c += 32) {
+        for (int c = 0; c < kEpiCols / 32; ++c) {
           uint32_t r[32];
-          tc_ld32(tacc + c, r);
-          float v[32];
+          tc_ld32(tacc + 32 * c, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          store_bf16(m, n0, c, v, scale);
+          for (int i = 0; i < 16; ++i)
+            pk[c][i] = pack_bf16(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
         }
         tc_fence_before();
         mbar_arrive(acce);  // accumulator may be overwritten now
+#pragma unroll
+        for (int c = 0; c < kEpiCols / 32; ++c) store_packed_bf16(a, m, n0 + 32 * c, pk[c]);
         continue;
       }
       // Split tile (stream-K): this CTA's fp32 partial of the tile goes to its
