@@ -271,6 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmA);
     if (!a.w_tiles) prefetch_tmap(&tmB);
   }
+  // Launched with programmatic dependent launch: the launch and the set-up
+  // above overlap the previous kernel (X's quantizer).  Nothing is read, Y
+  // is not written and tensor memory is not claimed (the previous kernel
+  // may still need to allocate it) before that kernel has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(const_cast<uint32_t *>(tmem_slot))),
@@ -745,8 +750,18 @@ cudaError_t plan_gemm_mxf4_swiglu(const uint8_t *x_codes, const uint8_t *x_mma_s
 
 cudaError_t enqueue_gemm_mxf4(const GemmMxf4Plan &plan, cudaStream_t stream) {
   const GemmMxf4Plan::Impl &p = *plan.impl;
-  gemm_mxf4_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(p.tmA, p.tmB, p.a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_mxf4_kernel, p.tmA, p.tmB, p.a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace impfp4

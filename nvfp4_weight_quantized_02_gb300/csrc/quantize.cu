@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partial_kernel(const uint16
                                                                     int64_t ldx,
                                                                     uint32_t *__restrict__ partial,
                                                                     int32_t *status) {
+  // the encode pass may be launched now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ uint32_t red[kAmaxThreads / 32];
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (kAmaxThreads / 32);
@@ -132,6 +134,11 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(
     const uint32_t *__restrict__ partial, int num_partial, uint8_t *__restrict__ codes,
     uint8_t *__restrict__ scales, float *__restrict__ tensor_scale) {
   __shared__ uint32_t red[kEncThreads / 32];
+  // Launched early after the amax pass (programmatic dependent launch): the
+  // GEMM that reads the codes may be launched in turn, and nothing is read
+  // before the amax pass has finished and its partial maxima are visible.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   uint32_t m = 0;
   for (int i = threadIdx.x; i < num_partial; i += kEncThreads) m = max(m, partial[i]);
   m = block_max_u32<kEncThreads>(m, red);
@@ -433,9 +440,20 @@ cudaError_t launch_quantize_mma(const uint16_t *x, int64_t rows, int64_t K, int6
   const int64_t cap = (int64_t)num_sms_cached() * 8;
   if (ge > cap) ge = cap;
   if (ge < 1) ge = 1;
-  encode_kernel<true><<<static_cast<int>(ge), kEncThreads, 0, stream>>>(
-      x, rows, K, ldx, partial, ga, codes, mma_scales, tensor_scale);
-  return cudaGetLastError();
+  // the encode pass with programmatic dependent launch (it waits in-kernel)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ge);
+  cfg.blockDim = dim3(kEncThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, encode_kernel<true>, x, rows, K, ldx,
+                                           static_cast<const uint32_t *>(partial), ga, codes,
+                                           mma_scales, tensor_scale);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ---- MXFP4 (OCP MX v1.0) and FP8-E4M3 weights ---------------------------------
