@@ -140,3 +140,40 @@ def test_repeatable(M, K, N):
             assert torch.equal(runs[0].view(torch.int16), o.view(torch.int16))
     # whole tiles: the same GEMM whichever form the weight is in
     assert torch.equal(outs[0].view(torch.int16), fp4[0].view(torch.int16))
+
+
+def test_back_to_back_calls_share_one_workspace():
+    """Calls of imp_nvfp4_gemm_mma in a row on one stream and one workspace,
+    each with its own X, nothing synchronised between them: X's quantizer,
+    its encode pass and the GEMM of a call are chained by programmatic
+    dependent launch, so each must wait for its predecessor before touching
+    the shared X codes and scales.  Every result equals the same call made
+    alone (the arithmetic is deterministic), and the first is checked
+    against the oracle."""
+    M, K, N = 640, 5120, 768
+    lins = [synth.Linear(f"b2b{i}", M, K, N, 90 + i, w_dist=synth.DIST_STUDENT_T4, w_scale=0.02,
+                         x_outlier_frac=0.01) for i in range(3)]
+    wb = lins[0].weight_bf16()
+    wm = pkg.prepare_mma(pkg.quantize(dev_bf16(wb)))
+    xs = [dev_bf16(l.act_bf16()) for l in lins]
+    ws = torch.empty(pkg.imp_nvfp4_gemm_workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in xs]
+    for _ in range(2):
+        for x, y in zip(xs, ys):
+            pkg.gemm_mma(x, wm, y=y, dev_status=status, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for x, y in zip(xs, ys):
+        alone = pkg.gemm_mma(x, wm, dev_status=status, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(alone.view(torch.int16), y.view(torch.int16))
+    xb = lins[0].act_bf16()
+    _, s_w, _ = oracle.tensor_scale(wb)
+    cols = np.arange(0, N, 7)
+    wc, wsc = oracle.quantize_rows(wb[cols], s_w)
+    _, s_x, _ = oracle.tensor_scale(xb)
+    rows = np.arange(0, M, 5)
+    y_ref, bound = oracle.reference_gemm(xb[rows], M, wc, wsc, s_w, s_x=s_x)
+    check_within_tolerance(ys[0].float().cpu().numpy()[np.ix_(rows, cols)], y_ref, bound,
+                           "b2b", tight=True)
